@@ -1,0 +1,226 @@
+"""fp64 CPU oracle for the SwiGLU FFN and the top-k MoE forward.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports this module:
+only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may call it.  It shares no code with the CUDA library.
+
+Every function is the plain definition written out in float64 numpy, in the
+order and notation of the pages it follows.  A matrix product (``@``) and a
+sort (``np.lexsort``) are the only library primitives used; nothing is
+blocked, fused or reordered.
+
+Sources (cited by tag below):
+  [L13]   MiniMind course, lesson 13 "FFN 与 MoE" (course/13_ffn_and_moe.md)
+  [CH4]   minimind3.com, chapter 4 "前馈网络 MLP & MoE"
+  [DEMO]  minimind3.com, example "前馈网络 MLP & MoE：示例代码" (04-mlp-moe-demo.py)
+
+Notation (as on the pages): T tokens (the pages' N = B*S), H hidden size,
+I intermediate size, E experts, k experts per token.  Weights follow the
+nn.Linear layout [out, in]: Wg, Wu: [I, H]; Wd: [H, I]; Wr: [E, H].
+
+Readings taken where the pages are silent or inconsistent (each one is
+listed with its reason in the design notes of the repository):
+  * top-k order: descending probability; equal probabilities -> the lower
+    expert index first ([L13] step 4 uses torch.topk(sorted=False), which
+    leaves both unspecified).
+  * aux loss for k > 1: load_e = count_e / T, i.e. the [k, E] "load" of
+    [L13] step 6 / [CH4] §4.4 summed over the k slots (the value the module
+    returns), not the per-slot mean of the demo's printed breakdown.
+  * aux loss is always computed; coef = 0 gives 0 (the eval branch).
+  * The "+1e-20" of the renormalisation is kept.
+Parity is pinned for every function here (tests/test_oracle.py); no
+function is "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+F64 = np.float64
+
+#: Added to the denominator of the top-k renormalisation ([L13] step 5;
+#: [CH4] §4.3 step 2).
+RENORM_EPS = 1e-20
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=F64)
+
+
+# --------------------------------------------------------------------------
+# Dense SwiGLU FFN
+# --------------------------------------------------------------------------
+def silu(z):
+    """SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z))  ([CH4] §4.2 "原理说明")."""
+    z = _f64(z)
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def swiglu_ffn(x, Wg, Wu, Wd):
+    """Dense SwiGLU feed-forward, [L13] §0 / §1.2 equations:
+
+        u = W_up x,  g = W_gate x,  h = SiLU(g) ⊙ u,  y = W_down h
+
+    x: [T, H]; Wg, Wu: [I, H]; Wd: [H, I]  ->  y: [T, H]  (all float64).
+    """
+    x, Wg, Wu, Wd = _f64(x), _f64(Wg), _f64(Wu), _f64(Wd)
+    u = x @ Wu.T            # [T, I]
+    g = x @ Wg.T            # [T, I]
+    h = silu(g) * u         # [T, I]
+    return h @ Wd.T         # [T, H]
+
+
+# --------------------------------------------------------------------------
+# Router: logits, softmax, top-k, renormalisation
+# --------------------------------------------------------------------------
+def router_logits(x, Wr, logit_bias=None):
+    """r = W_router x  ([L13] §1.5; [CH4] §4.3 "gate" = nn.Linear(H, E, bias=False)).
+
+    ``logit_bias`` ([E] or None) is added to every token's logits; None gives
+    the pages' bias-free router exactly.
+    """
+    r = _f64(x) @ _f64(Wr).T                      # [T, E]
+    if logit_bias is not None:
+        r = r + _f64(logit_bias)[None, :]
+    return r
+
+
+def softmax(r):
+    """p_e = exp(r_e) / sum_j exp(r_j) over the expert axis ([L13] §1.5).
+
+    The row maximum is subtracted first; the quotient is unchanged.
+    """
+    r = _f64(r)
+    z = np.exp(r - r.max(axis=-1, keepdims=True))
+    return z / z.sum(axis=-1, keepdims=True)
+
+
+def topk(p, k):
+    """S = TopK(p, k) per token ([L13] §1.5 and step 4).
+
+    Returns (idx [T, k] int64, val [T, k] float64) with each row ordered by
+    descending probability, equal probabilities broken towards the lower
+    expert index.
+    """
+    p = _f64(p)
+    T, E = p.shape
+    if not 1 <= k <= E:
+        raise ValueError(f"need 1 <= k <= E, got k={k}, E={E}")
+    ids = np.broadcast_to(np.arange(E), (T, E))
+    # np.lexsort sorts by the LAST key first: primary -p, secondary index.
+    order = np.lexsort((ids, -p), axis=-1)
+    idx = order[:, :k].astype(np.int64)
+    val = np.take_along_axis(p, idx, axis=-1)
+    return idx, val
+
+
+def renormalise(val):
+    """alpha_e = p_e / (sum_{j in S} p_j + 1e-20)  ([L13] step 5; [CH4] §4.3 step 2)."""
+    val = _f64(val)
+    return val / (val.sum(axis=-1, keepdims=True) + RENORM_EPS)
+
+
+# --------------------------------------------------------------------------
+# Load-balancing auxiliary loss
+# --------------------------------------------------------------------------
+def expert_load(topk_idx, E):
+    """load_e = (1/T) * #{(t, s): topk_idx[t, s] == e}  ([L13] §1.6; [CH4] §4.4 step 1).
+
+    For k = 1 this is the fraction of tokens routed to e; for k > 1 it is the
+    [k, E] one-hot mean of the pages summed over the k slots.
+    """
+    topk_idx = np.asarray(topk_idx)
+    T = topk_idx.shape[0]
+    counts = np.zeros(E, dtype=np.int64)
+    for e in topk_idx.reshape(-1):
+        counts[int(e)] += 1
+    return counts.astype(F64) / F64(T), counts
+
+
+def mean_prob(p):
+    """prob_e = (1/T) * sum_t p_{t,e}  ([L13] §1.6; [CH4] §4.4 step 2)."""
+    return _f64(p).mean(axis=0)
+
+
+def aux_loss_from_stats(load, prob, E, coef):
+    """L_aux = E * coef * sum_e load_e * prob_e  ([L13] §1.6 equation; [CH4] §4.4 step 3)."""
+    return F64(E) * F64(coef) * float(np.sum(_f64(load) * _f64(prob)))
+
+
+def aux_loss(topk_idx, p, coef):
+    p = _f64(p)
+    E = p.shape[1]
+    load, _ = expert_load(topk_idx, E)
+    return aux_loss_from_stats(load, mean_prob(p), E, coef)
+
+
+# --------------------------------------------------------------------------
+# MoE layer
+# --------------------------------------------------------------------------
+def combine(x, Wg, Wu, Wd, topk_idx, alpha):
+    """y_t = sum_s alpha_{t,s} * Expert_{idx[t,s]}(x_t)  ([L13] §0 MoE equation, step 5).
+
+    The pages' dispatch: for each expert e, gather the tokens that chose it,
+    run the expert on them, scale by their weight and add into y at those
+    tokens (index_add_).  Wg/Wu/Wd are sequences of E per-expert matrices.
+    """
+    x = _f64(x)
+    topk_idx = np.asarray(topk_idx)
+    alpha = _f64(alpha)
+    T, H = x.shape
+    y = np.zeros((T, H), dtype=F64)
+    for e in range(len(Wg)):
+        mask = topk_idx == e                         # [T, k]
+        if not mask.any():
+            continue
+        tok = np.nonzero(mask.any(axis=-1))[0]       # tokens that chose e
+        w = alpha[mask]                              # their weights, token order
+        out = swiglu_ffn(x[tok], Wg[e], Wu[e], Wd[e])
+        y[tok] += out * w[:, None]
+    return y
+
+
+def moe_forward(x, Wr, Wg, Wu, Wd, k, coef, logit_bias=None):
+    """The MoE layer forward ([L13] step 4-6; [CH4] §4.3-4.4).
+
+    Returns a dict with y [T, H], topk_idx [T, k], topk_w (alpha) [T, k],
+    aux_loss (float), probs p [T, E] and the per-expert counts [E].
+    """
+    x = _f64(x)
+    E = len(Wg)
+    p = softmax(router_logits(x, Wr, logit_bias))
+    idx, val = topk(p, k)
+    alpha = renormalise(val)
+    y = combine(x, Wg, Wu, Wd, idx, alpha)
+    load, counts = expert_load(idx, E)
+    aux = aux_loss_from_stats(load, mean_prob(p), E, coef)
+    return {"y": y, "topk_idx": idx, "topk_w": alpha, "aux_loss": aux,
+            "probs": p, "counts": counts}
+
+
+def moe_route(x, Wr, k, coef, logit_bias=None):
+    """Router half of :func:`moe_forward` (no experts): idx, alpha, aux, probs."""
+    x = _f64(x)
+    p = softmax(router_logits(x, Wr, logit_bias))
+    E = p.shape[1]
+    idx, val = topk(p, k)
+    alpha = renormalise(val)
+    load, counts = expert_load(idx, E)
+    aux = aux_loss_from_stats(load, mean_prob(p), E, coef)
+    return {"topk_idx": idx, "topk_w": alpha, "aux_loss": aux, "probs": p,
+            "counts": counts}
+
+
+def near_tie_tokens(p, k, gap=1e-6):
+    """Tokens whose top-k choice or slot order is decided by a probability gap
+    below ``gap``: sort the row descending, q_1 >= ... >= q_E; the token is a
+    near-tie if q_j - q_{j+1} < gap for some j <= k (j + 1 <= E).
+    Returns a boolean mask [T].
+    """
+    q = -np.sort(-_f64(p), axis=-1)
+    E = q.shape[1]
+    jmax = min(k, E - 1)
+    if jmax <= 0:
+        return np.zeros(q.shape[0], dtype=bool)
+    gaps = q[:, :jmax] - q[:, 1:jmax + 1]
+    return (gaps < gap).any(axis=-1)

@@ -1,0 +1,443 @@
+"""Pins for the fp64 oracle against values the pages print and against
+mathematics that fixes the result independently of the oracle's own code.
+
+Each test names the passage (page title + section) or the identity it uses.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+# --------------------------------------------------------------------------
+# SiLU
+# --------------------------------------------------------------------------
+def test_silu_printed_values():
+    """Demo example 2: SiLU(0) = 0; minimum near -1.278 with value -0.278."""
+    g = golden("silu_values.json")
+    assert O.silu(0.0) == g["silu_at_zero"]
+    # locate the minimum of the oracle's SiLU by golden-section search
+    a, b = -3.0, 0.0
+    phi = (math.sqrt(5) - 1) / 2
+    for _ in range(200):
+        c, d = b - phi * (b - a), a + phi * (b - a)
+        if O.silu(c) < O.silu(d):
+            b = d
+        else:
+            a = c
+    xmin = 0.5 * (a + b)
+    tol = 0.5 * 10 ** -g["printed_decimals"]
+    assert abs(xmin - g["argmin_approx"]) <= tol
+    assert abs(float(O.silu(xmin)) - g["min_approx"]) <= tol
+    # closed form at the minimum: d/dx x*s(x) = s(x)(1 + x(1 - s(x))) = 0
+    # -> x(1 - s(x)) = -1 -> SiLU(x*) = x* * s(x*) = x* + 1.  Solve the
+    # stationarity condition by bisection (s from its definition, not the oracle).
+    s = lambda v: 1.0 / (1.0 + math.exp(-v))
+    lo, hi = -2.0, -1.0                      # x(1-s(x)) + 1 changes sign here
+    for _ in range(200):
+        mid = 0.5 * (lo + hi)
+        if mid * (1 - s(mid)) + 1 > 0:     # f(-2) < 0 < f(-1)
+            hi = mid
+        else:
+            lo = mid
+    xstar = 0.5 * (lo + hi)
+    assert abs(xstar - xmin) < 1e-6
+    assert abs(float(O.silu(xstar)) - (xstar + 1.0)) < 1e-14
+    assert O.silu(xstar - 1e-4) > O.silu(xstar) < O.silu(xstar + 1e-4)
+
+
+def test_silu_asymptotes_and_sign():
+    z = np.array([30.0, 50.0, -30.0, -50.0, 1.0, -1.0])
+    s = O.silu(z)
+    assert abs(s[0] - 30.0) < 1e-9 and abs(s[1] - 50.0) < 1e-12
+    assert -1e-11 < s[2] < 0 and -1e-20 < s[3] < 0
+    # SiLU(1) = e/(1+e); SiLU(-1) = -1/(1+e)
+    assert abs(s[4] - math.e / (1 + math.e)) < 1e-15
+    assert abs(s[5] + 1.0 / (1 + math.e)) < 1e-15
+    # no overflow for very negative arguments
+    assert O.silu(-1000.0) == 0.0
+
+
+# --------------------------------------------------------------------------
+# Dense SwiGLU FFN
+# --------------------------------------------------------------------------
+def test_swiglu_hand_case():
+    """Lesson 13 §0/§1.2 equations, evaluated by hand (H=2, I=3)."""
+    g = golden("swiglu_hand_case.json")
+    y = O.swiglu_ffn(np.array([g["x"]]), np.array(g["Wg"]), np.array(g["Wu"]),
+                     np.array(g["Wd"]))
+    e = math.e
+    expect = [eval(s, {"e": e}) for s in g["y_closed_form"]]
+    assert y.shape == (1, 2)
+    np.testing.assert_allclose(y[0], expect, rtol=0, atol=1e-15)
+
+
+def test_swiglu_zero_gate_or_value_gives_zero():
+    r = rng(1)
+    x = r.normal(size=(5, 6))
+    Wg, Wu, Wd = r.normal(size=(7, 6)), r.normal(size=(7, 6)), r.normal(size=(6, 7))
+    assert np.all(O.swiglu_ffn(x, np.zeros_like(Wg), Wu, Wd) == 0)   # SiLU(0) = 0
+    assert np.all(O.swiglu_ffn(x, Wg, np.zeros_like(Wu), Wd) == 0)
+
+
+def test_swiglu_linear_in_down_and_up():
+    r = rng(2)
+    x = r.normal(size=(4, 6))
+    Wg, Wu = r.normal(size=(9, 6)), r.normal(size=(9, 6))
+    D1, D2 = r.normal(size=(6, 9)), r.normal(size=(6, 9))
+    y = O.swiglu_ffn(x, Wg, Wu, D1 + 3.0 * D2)
+    np.testing.assert_allclose(y, O.swiglu_ffn(x, Wg, Wu, D1) + 3.0 * O.swiglu_ffn(x, Wg, Wu, D2),
+                               atol=1e-11)
+    U2 = r.normal(size=(9, 6))
+    y = O.swiglu_ffn(x, Wg, Wu - 2.0 * U2, D1)
+    np.testing.assert_allclose(y, O.swiglu_ffn(x, Wg, Wu, D1) - 2.0 * O.swiglu_ffn(x, Wg, U2, D1),
+                               atol=1e-11)
+
+
+def test_swiglu_token_permutation_equivariance():
+    """The FFN acts on each position independently (lesson 13 §1.1)."""
+    r = rng(3)
+    x = r.normal(size=(11, 5))
+    W = (r.normal(size=(8, 5)), r.normal(size=(8, 5)), r.normal(size=(5, 8)))
+    perm = r.permutation(11)
+    np.testing.assert_allclose(O.swiglu_ffn(x[perm], *W), O.swiglu_ffn(x, *W)[perm], atol=1e-13)
+
+
+def test_swiglu_large_gate_is_bilinear():
+    """For g >> 0, SiLU(g) -> g, so y -> Wd((Wg x) * (Wu x)) (elementwise)."""
+    x = np.array([[1.0, 2.0]])
+    Wg = np.array([[40.0, 0.0], [0.0, 30.0], [20.0, 20.0]])   # g = [40, 60, 60]
+    Wu = np.array([[1.0, -1.0], [0.5, 0.0], [0.0, 2.0]])      # u = [-1, 0.5, 4]
+    Wd = np.array([[1.0, 2.0, 3.0], [-1.0, 0.0, 1.0]])
+    h = np.array([40.0 * -1.0, 60.0 * 0.5, 60.0 * 4.0])
+    np.testing.assert_allclose(O.swiglu_ffn(x, Wg, Wu, Wd)[0], Wd @ h, rtol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# Router, top-k, renormalisation
+# --------------------------------------------------------------------------
+def _logits_for_probs(p, H=6):
+    """x = e_0, Wr[:, 0] = log p  ->  r = log p  ->  softmax(r) = p exactly (up to rounding)."""
+    E = len(p)
+    x = np.zeros((1, H))
+    x[0, 0] = 1.0
+    Wr = np.zeros((E, H))
+    Wr[:, 0] = np.log(p)
+    return x, Wr
+
+
+@pytest.mark.parametrize("via", ["weights", "bias"])
+def test_routing_worked_example(via):
+    """Lesson 13 §1.5: p = [0.05, 0.10, 0.80, 0.05]."""
+    g = golden("routing_worked_example.json")
+    p = np.array(g["p"])
+    if via == "weights":
+        x, Wr = _logits_for_probs(p)
+        bias = None
+    else:
+        x, Wr, bias = np.ones((1, 3)), np.zeros((4, 3)), np.log(p)
+    probs = O.softmax(O.router_logits(x, Wr, bias))
+    np.testing.assert_allclose(probs[0], p, rtol=1e-14)
+    for key, k in (("top1", 1), ("top2", 2)):
+        r = O.moe_route(x, Wr, k, 0.0, bias)
+        assert r["topk_idx"][0].tolist() == g[key]["idx"]
+        np.testing.assert_allclose(r["topk_w"][0], g[key]["alpha"], rtol=1e-14)
+
+
+def test_softmax_properties():
+    r = rng(4)
+    logits = r.normal(size=(7, 5)) * 3
+    p = O.softmax(logits)
+    np.testing.assert_allclose(p.sum(-1), 1.0, atol=1e-15)
+    np.testing.assert_allclose(O.softmax(logits + 123.0), p, atol=1e-15)
+    # two experts: p_0 = sigmoid(r_0 - r_1)
+    two = O.softmax(np.array([[0.7, -0.4]]))
+    assert abs(two[0, 0] - 1.0 / (1.0 + math.exp(-1.1))) < 1e-15
+    assert np.all(O.softmax(np.zeros((2, 6))) == 1.0 / 6)
+    # large logits do not overflow
+    assert np.all(np.isfinite(O.softmax(np.array([[1000.0, 0.0, -1000.0]]))))
+
+
+def _bruteforce_topk(p_row, k):
+    """The unique k-subset whose members all precede every non-member in the
+    order (descending p, then ascending index); slots ordered the same way."""
+    E = len(p_row)
+    before = lambda a, b: (p_row[a] > p_row[b]) or (p_row[a] == p_row[b] and a < b)
+    hits = [S for S in itertools.combinations(range(E), k)
+            if all(before(a, b) for a in S for b in range(E) if b not in S)]
+    assert len(hits) == 1
+    S = list(hits[0])
+    # order the slots by insertion sort with the same comparison
+    out = []
+    for a in S:
+        i = 0
+        while i < len(out) and before(out[i], a):
+            i += 1
+        out.insert(i, a)
+    return out
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_topk_vs_bruteforce(seed):
+    r = rng(10 + seed)
+    E = int(r.integers(1, 7))
+    p = O.softmax(r.normal(size=(9, E)))
+    # plant exact ties in some rows
+    if E >= 3:
+        p[0, 1] = p[0, 2]
+        p[1, :] = p[1, 0]
+    for k in range(1, E + 1):
+        idx, val = O.topk(p, k)
+        for t in range(p.shape[0]):
+            assert idx[t].tolist() == _bruteforce_topk(p[t], k)
+            assert val[t].tolist() == [p[t, e] for e in idx[t]]
+        # the selected values are the k largest, in descending order
+        np.testing.assert_array_equal(val, -np.sort(-p, axis=-1)[:, :k])
+
+
+def test_topk_rejects_bad_k():
+    with pytest.raises(ValueError):
+        O.topk(np.ones((2, 3)), 0)
+    with pytest.raises(ValueError):
+        O.topk(np.ones((2, 3)), 4)
+
+
+@pytest.mark.parametrize("E,k", [(4, 1), (4, 2), (8, 2), (8, 3), (5, 5)])
+def test_tie_break_uniform_router(E, k):
+    """Wr = 0 -> every p = 1/E exactly -> experts 0..k-1, alpha = 1/k."""
+    x = rng(5).normal(size=(6, 7))
+    r = O.moe_route(x, np.zeros((E, 7)), k, 0.01)
+    assert np.all(r["probs"] == 1.0 / E)
+    assert np.all(r["topk_idx"] == np.arange(k)[None, :])
+    np.testing.assert_allclose(r["topk_w"], 1.0 / k, rtol=1e-15)
+
+
+def test_alpha_sums_to_one_and_k1_is_one():
+    """Demo example 6: renormalised top-k weights sum to 1 (atol 1e-5 there)."""
+    r = rng(6)
+    x, Wr = r.normal(size=(50, 8)), r.normal(size=(6, 8))
+    for k in (1, 2, 3, 6):
+        a = O.moe_route(x, Wr, k, 0.0)["topk_w"]
+        np.testing.assert_allclose(a.sum(-1), 1.0, atol=1e-15)
+        assert np.all(a > 0)
+        assert np.all(np.diff(a, axis=-1) <= 0)         # descending like p
+    assert np.all(O.moe_route(x, Wr, 1, 0.0)["topk_w"] == 1.0)
+
+
+# --------------------------------------------------------------------------
+# aux loss
+# --------------------------------------------------------------------------
+def test_aux_extremes_table():
+    """Chapter 4 §4.4 table: balanced -> 0.25 (x E = 1.0); collapsed -> 0.7 (x E = 2.8)."""
+    g = golden("aux_loss_tables.json")
+    for row in g["extremes"]:
+        E = len(row["load"])
+        s = O.aux_loss_from_stats(row["load"], row["prob"], 1, 1.0)
+        assert abs(s - row["sum_f_P"]) < 1e-15
+        assert abs(O.aux_loss_from_stats(row["load"], row["prob"], E, 1.0) - row["times_E"]) < 1e-14
+
+
+def test_load_example():
+    """Chapter 4 §4.4 step 1: 30 of 100 tokens on expert 0 -> load 0.3."""
+    g = golden("aux_loss_tables.json")["load_example"]
+    idx = np.array([0] * g["count_expert0"] + [1] * (g["T"] - g["count_expert0"]))[:, None]
+    load, counts = O.expert_load(idx, g["E"])
+    assert counts[0] == g["count_expert0"]
+    assert load[0] == g["load_expert0"]
+
+
+@pytest.mark.parametrize("E,k", [(4, 1), (8, 2), (6, 3)])
+def test_aux_uniform_router_is_k_coef(E, k):
+    """Wr = 0: load = 1 on experts 0..k-1, prob = 1/E  ->  aux = E*coef*k/E = k*coef."""
+    x = rng(7).normal(size=(12, 5))
+    coef = 0.01
+    r = O.moe_route(x, np.zeros((E, 5)), k, coef)
+    assert abs(r["aux_loss"] - k * coef) < 1e-17
+
+
+@pytest.mark.parametrize("E", [2, 4, 8])
+def test_aux_uniform_top1_load_is_coef(E):
+    """Exactly uniform top-1 counts (count_e = T/E) give aux = coef whatever
+    the probabilities: E*coef*sum_e (1/E) P_e = coef * sum_e P_e = coef."""
+    H = E + 3
+    T = 5 * E
+    r = rng(8)
+    Wr = np.zeros((E, H))
+    Wr[:, :E] = 4.0 * np.eye(E)
+    Wr[:, E:] = r.normal(size=(E, 3)) * 0.1          # perturb the probabilities
+    x = np.zeros((T, H))
+    for t in range(T):
+        x[t, t % E] = 1.0
+        x[t, E:] = r.normal(size=3)
+    coef = 0.01
+    out = O.moe_route(x, Wr, 1, coef)
+    assert np.bincount(out["topk_idx"][:, 0], minlength=E).tolist() == [T // E] * E
+    assert abs(out["aux_loss"] - coef) < 1e-15
+
+
+def test_aux_coef_zero_is_zero():
+    r = rng(9)
+    out = O.moe_route(r.normal(size=(10, 4)), r.normal(size=(3, 4)), 2, 0.0)
+    assert out["aux_loss"] == 0.0
+
+
+# --------------------------------------------------------------------------
+# MoE layer: special cases that reduce to known forms
+# --------------------------------------------------------------------------
+def _experts(r, E, H, I, scale=0.3):
+    return ([r.normal(size=(I, H)) * scale for _ in range(E)],
+            [r.normal(size=(I, H)) * scale for _ in range(E)],
+            [r.normal(size=(H, I)) * scale for _ in range(E)])
+
+
+def test_k_equals_E_is_dense_softmax_mixture():
+    """k = E: alpha = p, so y_t = sum_e p_{t,e} FFN_e(x_t); load_e = 1 -> aux = E*coef."""
+    r = rng(11)
+    T, H, I, E = 7, 5, 6, 4
+    x, Wr = r.normal(size=(T, H)), r.normal(size=(E, H))
+    Wg, Wu, Wd = _experts(r, E, H, I)
+    out = O.moe_forward(x, Wr, Wg, Wu, Wd, E, 0.02)
+    p = out["probs"]
+    mix = sum(p[:, e:e + 1] * O.swiglu_ffn(x, Wg[e], Wu[e], Wd[e]) for e in range(E))
+    np.testing.assert_allclose(out["y"], mix, atol=1e-13)
+    assert abs(out["aux_loss"] - E * 0.02) < 1e-15
+
+
+def test_single_expert_is_dense_ffn():
+    """E = 1: alpha = 1, y = FFN(x), aux = coef."""
+    r = rng(12)
+    x = r.normal(size=(6, 5))
+    Wg, Wu, Wd = _experts(r, 1, 5, 7)
+    out = O.moe_forward(x, r.normal(size=(1, 5)), Wg, Wu, Wd, 1, 0.05)
+    np.testing.assert_allclose(out["y"], O.swiglu_ffn(x, Wg[0], Wu[0], Wd[0]), rtol=1e-12, atol=1e-15)
+    assert abs(out["aux_loss"] - 0.05) < 1e-16
+
+
+@pytest.mark.parametrize("k", [1, 2, 3])
+def test_identical_experts_give_dense(k):
+    """All experts equal: y = sum_S alpha * FFN(x) = FFN(x) since sum alpha = 1."""
+    r = rng(13)
+    x = r.normal(size=(9, 5))
+    Wg, Wu, Wd = _experts(r, 1, 5, 6)
+    E = 4
+    out = O.moe_forward(x, r.normal(size=(E, 5)), Wg * E, Wu * E, Wd * E, k, 0.0)
+    np.testing.assert_allclose(out["y"], O.swiglu_ffn(x, Wg[0], Wu[0], Wd[0]), atol=1e-13)
+
+
+def test_expert_routing_selects_the_right_expert():
+    """A token routed (top-1) to expert e gets exactly FFN_e(x_t)."""
+    r = rng(14)
+    T, H, I, E = 8, 6, 5, 4
+    Wr = np.zeros((E, H))
+    Wr[:, :E] = 10.0 * np.eye(E)
+    x = r.normal(size=(T, H)) * 0.1
+    route = [3, 0, 2, 2, 1, 3, 0, 1]
+    for t, e in enumerate(route):
+        x[t, e] = 1.0
+    Wg, Wu, Wd = _experts(r, E, H, I)
+    out = O.moe_forward(x, Wr, Wg, Wu, Wd, 1, 0.0)
+    assert out["topk_idx"][:, 0].tolist() == route
+    for t, e in enumerate(route):
+        np.testing.assert_allclose(out["y"][t], O.swiglu_ffn(x[t:t + 1], Wg[e], Wu[e], Wd[e])[0],
+                                   rtol=1e-12, atol=1e-15)
+
+
+def _bruteforce_moe(x, Wr, Wg, Wu, Wd, k, coef, bias=None):
+    """Per-token scalar loops in Python floats (fp64)."""
+    T, H = len(x), len(x[0])
+    E, I = len(Wr), len(Wg[0])
+    y = [[0.0] * H for _ in range(T)]
+    idx_all, a_all = [], []
+    count = [0] * E
+    psum = [0.0] * E
+    for t in range(T):
+        logit = [sum(Wr[e][j] * x[t][j] for j in range(H)) + (bias[e] if bias is not None else 0.0)
+                 for e in range(E)]
+        m = max(logit)
+        ex = [math.exp(v - m) for v in logit]
+        z = sum(ex)
+        p = [v / z for v in ex]
+        S = _bruteforce_topk(p, k)
+        denom = sum(p[e] for e in S) + 1e-20
+        alpha = [p[e] / denom for e in S]
+        idx_all.append(S)
+        a_all.append(alpha)
+        for e in range(E):
+            psum[e] += p[e]
+        for e, a in zip(S, alpha):
+            count[e] += 1
+            hvec = []
+            for i in range(I):
+                g = sum(Wg[e][i][j] * x[t][j] for j in range(H))
+                u = sum(Wu[e][i][j] * x[t][j] for j in range(H))
+                hvec.append(g / (1.0 + math.exp(-g)) * u)
+            for o in range(H):
+                y[t][o] += a * sum(Wd[e][o][i] * hvec[i] for i in range(I))
+    aux = E * coef * sum((count[e] / T) * (psum[e] / T) for e in range(E))
+    return np.array(y), np.array(idx_all), np.array(a_all), aux
+
+
+@pytest.mark.parametrize("seed,E,k,with_bias", [(0, 3, 1, False), (1, 3, 2, False),
+                                                (2, 5, 2, True), (3, 4, 3, False)])
+def test_moe_bruteforce_tiny(seed, E, k, with_bias):
+    r = rng(20 + seed)
+    T, H, I = 6, 4, 5
+    x, Wr = r.normal(size=(T, H)), r.normal(size=(E, H))
+    Wg, Wu, Wd = _experts(r, E, H, I, scale=0.5)
+    bias = r.normal(size=E) if with_bias else None
+    out = O.moe_forward(x, Wr, Wg, Wu, Wd, k, 0.03, bias)
+    y, idx, a, aux = _bruteforce_moe(x.tolist(), Wr.tolist(), [w.tolist() for w in Wg],
+                                     [w.tolist() for w in Wu], [w.tolist() for w in Wd],
+                                     k, 0.03, None if bias is None else bias.tolist())
+    np.testing.assert_array_equal(out["topk_idx"], idx)
+    np.testing.assert_allclose(out["topk_w"], a, atol=1e-15)
+    np.testing.assert_allclose(out["y"], y, atol=1e-13)
+    assert abs(out["aux_loss"] - aux) < 1e-15
+
+
+def test_moe_token_permutation_equivariance():
+    r = rng(30)
+    T, H, I, E = 10, 4, 6, 5
+    x, Wr = r.normal(size=(T, H)), r.normal(size=(E, H))
+    Wg, Wu, Wd = _experts(r, E, H, I)
+    perm = r.permutation(T)
+    a = O.moe_forward(x, Wr, Wg, Wu, Wd, 2, 0.01)
+    b = O.moe_forward(x[perm], Wr, Wg, Wu, Wd, 2, 0.01)
+    np.testing.assert_allclose(b["y"], a["y"][perm], atol=1e-13)
+    np.testing.assert_array_equal(b["topk_idx"], a["topk_idx"][perm])
+    assert abs(a["aux_loss"] - b["aux_loss"]) < 1e-16
+
+
+def test_near_tie_detection():
+    p = np.array([[0.5, 0.3, 0.2],
+                  [0.4, 0.4 - 5e-7, 0.2 + 5e-7],      # slot-order tie at j = 1
+                  [0.6, 0.2, 0.2 - 1e-9 + 1e-9],       # exact tie at the k/k+1 boundary
+                  [0.6, 0.3, 0.1]])
+    m1 = O.near_tie_tokens(p, 1)
+    m2 = O.near_tie_tokens(p, 2)
+    assert m1.tolist() == [False, True, False, False]
+    assert m2.tolist() == [False, True, True, False]
+    assert O.near_tie_tokens(p, 3).tolist() == m2.tolist()
+
+
+def test_config_intermediate_size():
+    """Chapter 4 §4.1: I = ceil(768 * pi / 64) * 64 = 2432."""
+    from swiglu_mlp_top_gb300.inputs import intermediate_size
+    g = golden("minimind_config.json")
+    assert intermediate_size(g["hidden_size"]) == g["intermediate_size"]
