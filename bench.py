@@ -1,0 +1,389 @@
+"""Benchmark of the MoE / FFN forward on one GB300 (or N replicas under torchrun).
+
+One step = one forward pass of the whole hot path over one batch of synthetic
+tokens: router (logits, softmax, top-k, alpha, aux partials), dispatch (aux
+finalisation + token permute), grouped gate/up GEMM with the SwiGLU
+epilogue, grouped down GEMM with the alpha-scaled combine.  The default
+workload is the top-2 MoE with skewed load (E=8, k=2, T=16384, H=768,
+I=2432), the only configuration whose single pass runs every step of the
+path; --workload selects another named workload.
+
+Prints ONE JSON line (rank 0).  --impl reference times the fp64 CPU oracle
+instead, on a bounded token sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from swiglu_mlp_top_gb300.inputs import WORKLOADS, make_workload_inputs  # noqa: E402
+
+DEFAULT_WORKLOAD = "moe_e8k2_t16384_skew"
+METRIC = "MoE/FFN forward tokens/s and TFLOP/s on 1 GB300; % of bf16 tensor or HBM roofline"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def algorithmic_flops(w, T=None) -> float:
+    """T * (k * 6 * H * I + 2 * H * E): the three GEMMs per assignment plus
+    the router (dense FFN: no router term)."""
+    T = w.T if T is None else T
+    router = 0 if w.kind == "dense" else 2 * w.H * w.E
+    return float(T) * (w.k * 6.0 * w.H * w.I + router)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- our arm
+class Step:
+    """One forward of the workload through the public API, on device inputs."""
+
+    def __init__(self, w, dev, n_sets):
+        import swiglu_mlp_top_gb300 as mm
+        self.mm = mm
+        self.w = w
+        cpu = make_workload_inputs(w, seed=0)
+        self.cpu = cpu
+        self.sets = []
+        for _ in range(n_sets):   # distinct copies so that consecutive steps miss in L2
+            s = {}
+            for n, v in cpu.items():
+                if v is None:
+                    s[n] = None
+                elif isinstance(v, torch.Tensor):
+                    s[n] = v.to(dev)
+                else:
+                    s[n] = [t.to(dev) for t in v]
+            self.sets.append(s)
+        T, H, I = w.T, w.H, w.I
+        dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        self.y = torch.empty(T, H, dtype=dt, device=dev)
+        if w.kind == "moe":
+            self.idx = torch.empty(T, w.k, dtype=torch.int32, device=dev)
+            self.tw = torch.empty(T, w.k, dtype=torch.float32, device=dev)
+            self.aux = torch.empty((), dtype=torch.float32, device=dev)
+            nbytes = mm.moe_workspace_bytes(T, H, I, w.E, w.k, dt)
+        else:
+            nbytes = mm.ffn_workspace_bytes(T, H, I, dt)
+        self.ws = mm.new_workspace(nbytes, dev)
+
+    def input_bytes(self):
+        s = self.sets[0]
+        tot = 0
+        for v in s.values():
+            if isinstance(v, torch.Tensor):
+                tot += v.numel() * v.element_size()
+            elif isinstance(v, list):
+                tot += sum(t.numel() * t.element_size() for t in v)
+        return tot
+
+    def __call__(self, i, x=None):
+        s = self.sets[i % len(self.sets)]
+        x = s["x"] if x is None else x
+        if self.w.kind == "moe":
+            self.mm.moe_forward(x, s["Wr"], s["Wg"], s["Wu"], s["Wd"], self.w.k, self.w.coef,
+                                logit_bias=s.get("logit_bias"), out=self.y, topk_idx=self.idx,
+                                topk_w=self.tw, aux_loss=self.aux, workspace=self.ws)
+        else:
+            self.mm.swiglu_ffn(x, s["Wg"], s["Wu"], s["Wd"], out=self.y, workspace=self.ws)
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, ws: int, dev) -> float:
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(w, budget_s: float = 12.0):
+    """The fp64 oracle as it stands, on a bounded token sample of the workload."""
+    import oracle
+    from swiglu_mlp_top_gb300.inputs import to_f64
+    probe_T = max(1, min(w.T, 64))
+    cpu = make_workload_inputs(w, seed=0)
+    x = to_f64(cpu["x"])
+    args = {n: to_f64(cpu[n]) for n in ("Wg", "Wu", "Wd")}
+
+    def run(T):
+        t0 = time.perf_counter()
+        if w.kind == "moe":
+            oracle.moe_forward(x[:T], to_f64(cpu["Wr"]), args["Wg"], args["Wu"], args["Wd"], w.k,
+                               w.coef, to_f64(cpu.get("logit_bias")))
+        else:
+            oracle.swiglu_ffn(x[:T], args["Wg"], args["Wu"], args["Wd"])
+        return time.perf_counter() - t0
+
+    dt = run(probe_T)
+    T = probe_T
+    while T < w.T and dt < budget_s / 4:
+        T = min(w.T, T * 4)
+        dt = run(T)
+    return {"value": T / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{T} of {w.T} tokens of {w.name} (fp64 numpy, one pass, {dt:.2f} s)",
+            "tflops": algorithmic_flops(w, T) / dt / 1e12}
+
+
+def run_reference_arm(args, w):
+    ws, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    vals = []
+    samples = []
+    for _ in range(args.warmup):
+        cpu_baseline(w, budget_s=2.0)
+    for _ in range(args.steps):
+        r = cpu_baseline(w, budget_s=min(8.0, 60.0 / max(1, args.steps)))
+        vals.append(r["value"])
+        samples.append(r["sample"])
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * w.T / v, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "k": w.k,
+                       "note": "the fp64 CPU oracle timed on a token sample per step"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": samples[-1]},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_our_arm(args, w):
+    ws, rank, local = dist_setup()
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import swiglu_mlp_top_gb300 as mm
+    from swiglu_mlp_top_gb300 import _lib as L
+    lib = L.load()
+
+    probe = Step(w, dev, 1)
+    per_set = probe.input_bytes()
+    n_sets = max(1, min(8, int(np.ceil(2.0 * L2_BYTES / per_set)) + 0))
+    if n_sets > 1:
+        del probe
+        step = Step(w, dev, n_sets)
+    else:
+        step = probe
+    stream = torch.cuda.current_stream()
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert mm.check_status(step.ws) == 0
+
+    # ---- timed region: K steps, device events on the launching stream
+    dominant = L.MM_KERNEL_GATEUP
+    lib.mm_profile_start(dominant, args.steps)
+    launches0 = lib.mm_launch_count()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    launches = int(lib.mm_launch_count() - launches0)
+    import ctypes as C
+    tot = C.c_double(0)
+    nl = C.c_int(0)
+    lib.mm_profile_stop(C.byref(tot), C.byref(nl))
+    ms = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(ms, ws, dev)
+    status = mm.check_status(step.ws)
+    assert status == 0, f"device watchdog status {status}"
+    ms_per_step = ms / args.steps
+    value = ws * w.T * args.steps / (ms / 1e3)
+    flops = algorithmic_flops(w)
+    tflops = flops / (ms_per_step / 1e3) / 1e12
+
+    # ---- dominant kernel roofline: gate/up GEMM, 4*H*I flops per assignment
+    peaks, peak_src = measured_peaks()
+    k_ms = tot.value / max(1, nl.value)
+    gate_flops = float(w.T) * w.k * 4.0 * w.H * w.I
+    achieved = gate_flops / (k_ms / 1e3) / 1e12
+    roof = {"kernel": "gateup_tc_kernel (grouped gate/up GEMM + SwiGLU epilogue)",
+            "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+            "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)",
+            "kernel_ms": k_ms, "launches_timed": nl.value,
+            "flops_per_launch": gate_flops}
+
+    # ---- end to end through the public API: pinned host x in, y/idx/w/aux out
+    e2e = None
+    if args.e2e_steps > 0:
+        x_host = step.cpu["x"].pin_memory()
+        x_dev = torch.empty_like(step.sets[0]["x"])
+        y_host = torch.empty(step.y.shape, dtype=step.y.dtype).pin_memory()
+        outs = [y_host]
+        if w.kind == "moe":
+            outs += [torch.empty(step.idx.shape, dtype=torch.int32).pin_memory(),
+                     torch.empty(step.tw.shape, dtype=torch.float32).pin_memory(),
+                     torch.empty((), dtype=torch.float32).pin_memory()]
+        devs = [step.y] + ([step.idx, step.tw, step.aux] if w.kind == "moe" else [])
+        h2d = x_host.numel() * x_host.element_size()
+        d2h = sum(t.numel() * t.element_size() for t in outs)
+
+        def e2e_step(i):
+            x_dev.copy_(x_host, non_blocking=True)
+            step(i, x=x_dev)
+            for hst, d in zip(outs, devs):
+                hst.copy_(d, non_blocking=True)
+
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(e0.elapsed_time(e1), ws, dev)
+        e2e = {"value": ws * w.T * args.e2e_steps / (ems / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": ems / args.e2e_steps}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": w.dtype, "data": "synthetic",
+                "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E,
+                           "k": w.k, "coef": w.coef,
+                           "logit_bias": list(w.logit_bias) if w.logit_bias else None,
+                           "parallelism": f"replicas{ws}" if ws > 1 else "single",
+                           "l2": f"{len(step.sets)} rotating input sets of "
+                                 f"{per_set / 2**20:.0f} MiB (> L2 in total)"},
+                "tflops": tflops,
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches, "clocks": clk.summary()}
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference_arm(args, w)
+    else:
+        run_our_arm(args, w)
+
+
+if __name__ == "__main__":
+    main()

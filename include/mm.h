@@ -1,0 +1,191 @@
+/*
+ * mm.h — C ABI of the GB300 (sm_103a) SwiGLU FFN and top-k MoE forward.
+ *
+ * The operations follow the MiniMind pages on the FFN / MoE sub-layer:
+ *   [L13] MiniMind course, lesson 13 "FFN 与 MoE" (course/13_ffn_and_moe.md),
+ *         §0 / §1.2 (SwiGLU equations), §1.5 (router, softmax, top-k, alpha),
+ *         §1.6 (load-balancing aux loss), §3 steps 3-6 (module forward).
+ *   [CH4] minimind3.com, chapter 4 "前馈网络 MLP & MoE", §4.2 (SwiGLU),
+ *         §4.3 (MoE routing, renormalisation, dispatch), §4.4 (aux loss).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensors are dense, row-major, in DEVICE memory owned by the caller,
+ *     and 16-byte aligned.  Weights use the nn.Linear layout [out, in]:
+ *       Wg, Wu: [I, H]   Wd: [H, I]   Wr: [E, H]   x, y: [T, H].
+ *   - dtype selects the element type of x, the weights and y:
+ *       MM_DTYPE_BF16 — bf16 storage, fp32 accumulation (tcgen05 tensor
+ *                       cores for T > 64, weight streaming for T <= 64);
+ *       MM_DTYPE_F32  — fp32 storage and fp32 SIMT arithmetic (no TF32).
+ *     Router logits, probabilities, alpha and the aux loss are always fp32.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call only enqueues work on that stream and returns; none synchronises
+ *     the host except mm_check_status().  The library allocates no device
+ *     memory: scratch lives in the caller's `workspace`, whose size the
+ *     matching *_workspace_bytes() function returns.  Calls that share a
+ *     workspace must be ordered on one stream.
+ *   - Argument errors are reported synchronously as a non-zero mm_status
+ *     with nothing enqueued.  Device-side watchdog failures (a pipeline wait
+ *     that exceeded its time limit) are recorded in the workspace and
+ *     reported by mm_check_status().
+ *   - The library keeps only a host-side cache of TMA tensor maps keyed by
+ *     (device pointer, shape); it is safe to call from one host thread at a
+ *     time per process.
+ */
+#ifndef MM_H_
+#define MM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MM_OK = 0,
+  MM_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, k > E, ... */
+  MM_ERR_UNSUPPORTED = 2,   /* valid but outside this build's limits          */
+  MM_ERR_WORKSPACE = 3,     /* workspace null or smaller than required        */
+  MM_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed              */
+  MM_ERR_TIMEOUT = 5        /* a device pipeline wait hit its time limit      */
+} mm_status;
+
+typedef enum { MM_DTYPE_F32 = 0, MM_DTYPE_BF16 = 1 } mm_dtype;
+
+/* Which kernels carry the FFN part of a call (the *_ex entry points). */
+typedef enum {
+  MM_PATH_AUTO = 0,    /* bf16: tensor-core GEMMs if T > 64, else streaming; f32: SIMT */
+  MM_PATH_TENSOR = 1,  /* bf16 only: grouped tcgen05/TMEM GEMMs fed by TMA          */
+  MM_PATH_STREAM = 2,  /* bf16 only: decode-shaped weight-streaming kernels          */
+  MM_PATH_SIMT = 3     /* any dtype: plain fp32-FMA CUDA-core kernels                */
+} mm_path;
+
+/* Limits of this build. */
+#define MM_MAX_EXPERTS 64
+
+/* Human-readable name of an mm_status value (static string). */
+const char* mm_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int mm_version(void);
+
+/* Text of the last CUDA failure reported as MM_ERR_CUDA on this host thread
+ * (static thread-local storage; empty if none). */
+const char* mm_last_error(void);
+
+/* ------------------------------------------------------------------------
+ * Dense SwiGLU FFN   ([L13] §0 / §1.2; [CH4] §4.2)
+ *
+ *   u = Wu x,  g = Wg x,  h = SiLU(g) ⊙ u,  y = Wd h,  SiLU(z) = z·sigmoid(z)
+ *
+ * x [T,H], Wg/Wu [I,H], Wd [H,I] in; y [T,H] out (overwritten).  g and u
+ * never reach memory; h ([T,I], the dtype of x) lives in the workspace.
+ * Limits: T >= 0 (T = 0 enqueues nothing); H, I >= 1; bf16 tensor and
+ * streaming paths need H and I to be multiples of 64.
+ * ---------------------------------------------------------------------- */
+size_t mm_swiglu_ffn_workspace_bytes(int64_t T, int H, int I, int dtype);
+
+int mm_swiglu_ffn(const void* x, const void* Wg, const void* Wu, const void* Wd,
+                  void* y, int64_t T, int H, int I, int dtype,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* Wd,
+                     void* y, int64_t T, int H, int I, int dtype,
+                     void* workspace, size_t workspace_bytes, void* stream, int path);
+
+/* ------------------------------------------------------------------------
+ * Top-k MoE forward   ([L13] §1.5, §1.6, §3 steps 4-6; [CH4] §4.3, §4.4)
+ *
+ *   r = Wr x (+ logit_bias);  p = softmax(r)            (fp32)
+ *   S = TopK(p, k): descending p, equal p -> lower expert index first
+ *   alpha_e = p_e / (sum_{j in S} p_j + 1e-20)
+ *   y = sum_{e in S} alpha_e · SwiGLU_e(x)   — each term is rounded to y's
+ *       dtype and the terms are added in ascending expert order in y's dtype
+ *       (the pages' index_add_ into a zeroed y)
+ *   count_e = #{(t,s): S_t[s] = e},  P_e = sum_t p_{t,e}
+ *   aux_loss = E · coef · sum_e (count_e / T) · (P_e / T)
+ *
+ * Arguments:
+ *   x [T,H], Wr [E,H]                 device, dtype
+ *   Wg, Wu, Wd                        HOST arrays of E device pointers, one
+ *                                     [I,H] / [I,H] / [H,I] matrix per expert
+ *   logit_bias                        device fp32 [E], or NULL (no bias: the
+ *                                     pages' router exactly)
+ *   y [T,H]                           device, dtype, overwritten
+ *   topk_idx [T,k]                    device int32, slots in descending p
+ *   topk_w [T,k]                      device fp32, alpha of each slot
+ *   aux_loss                          device fp32 scalar (coef = 0 gives 0)
+ * Limits: T >= 1; 1 <= k <= E <= MM_MAX_EXPERTS; E*H*4 <= 200 KiB.
+ * ---------------------------------------------------------------------- */
+size_t mm_moe_workspace_bytes(int64_t T, int H, int I, int E, int k, int dtype);
+
+int mm_moe_forward(const void* x, const void* Wr,
+                   const void* const* Wg, const void* const* Wu, const void* const* Wd,
+                   int64_t T, int H, int I, int E, int k, float coef, int dtype,
+                   const float* logit_bias,
+                   void* y, int32_t* topk_idx, float* topk_w, float* aux_loss,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+int mm_moe_forward_ex(const void* x, const void* Wr,
+                      const void* const* Wg, const void* const* Wu, const void* const* Wd,
+                      int64_t T, int H, int I, int E, int k, float coef, int dtype,
+                      const float* logit_bias,
+                      void* y, int32_t* topk_idx, float* topk_w, float* aux_loss,
+                      void* workspace, size_t workspace_bytes, void* stream, int path);
+
+/* Router half of the MoE forward only (logits, softmax, top-k, alpha, aux):
+ * same arguments and meaning as mm_moe_forward without the experts and y.
+ * expert_counts (device int32 [E], nullable) receives count_e. */
+size_t mm_moe_route_workspace_bytes(int64_t T, int E);
+
+int mm_moe_route(const void* x, const void* Wr, int64_t T, int H, int E, int k,
+                 float coef, int dtype, const float* logit_bias,
+                 int32_t* topk_idx, float* topk_w, float* aux_loss,
+                 int32_t* expert_counts,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Status
+ * ---------------------------------------------------------------------- */
+/* Synchronises `stream`, reads and clears the device watchdog word kept at
+ * the start of `workspace` (any workspace used by the calls above), and
+ * returns MM_ERR_TIMEOUT if a kernel gave up on a pipeline wait since the
+ * last check, MM_ERR_CUDA if the stream reported an error, else MM_OK. */
+int mm_check_status(void* workspace, void* stream);
+
+/* Self-test of the watchdog: launches one block that waits on a barrier no
+ * one arrives on, with the given limit in microseconds (1 .. 10,000,000).
+ * The wait gives up, records MM_ERR_TIMEOUT in `workspace` (>= 256 bytes)
+ * and the kernel returns normally; mm_check_status() then reports it. */
+int mm_watchdog_selftest(void* workspace, size_t workspace_bytes,
+                         uint32_t limit_us, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Measurement hooks (host-side only; they add no work to the kernels)
+ * ---------------------------------------------------------------------- */
+typedef enum {
+  MM_KERNEL_ROUTER = 1,     /* logits/softmax/top-k/alpha/aux partials      */
+  MM_KERNEL_DISPATCH = 2,   /* aux finalisation + token permute             */
+  MM_KERNEL_GATEUP = 3,     /* gate/up GEMM with the SwiGLU epilogue        */
+  MM_KERNEL_DOWN = 4,       /* down GEMM with the alpha-scale/combine       */
+  MM_KERNEL_COMBINE = 5     /* ordered combine (k >= 3)                     */
+} mm_kernel_id;
+
+/* Number of kernels this library has enqueued since it was loaded. */
+uint64_t mm_launch_count(void);
+
+/* Start timing every launch of one kernel (mm_kernel_id) with a pair of CUDA
+ * events recorded on the launching stream around it, for at most
+ * max_launches launches (1 .. 100000).  The events are created by the
+ * library.  Returns MM_ERR_INVALID_ARG for a bad id or count. */
+int mm_profile_start(int kernel_id, int max_launches);
+
+/* Stop timing: waits for the last recorded event, returns the summed
+ * duration in milliseconds and the number of launches timed. */
+int mm_profile_stop(double* total_ms, int* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MM_H_ */

@@ -1,0 +1,147 @@
+"""Python face of the C ABI: argument marshalling only.
+
+torch supplies device memory and the current CUDA stream; every step of the
+computation runs in the CUDA kernels of libmm.so.  Nothing here computes.
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib as L
+
+_DTYPES = {torch.bfloat16: L.MM_DTYPE_BF16, torch.float32: L.MM_DTYPE_F32}
+_PATHS = {"auto": L.MM_PATH_AUTO, "tensor": L.MM_PATH_TENSOR, "stream": L.MM_PATH_STREAM,
+          "simt": L.MM_PATH_SIMT}
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dtype_code(x: torch.Tensor) -> int:
+    if x.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {x.dtype}")
+    return _DTYPES[x.dtype]
+
+
+def ffn_workspace_bytes(T: int, H: int, I: int, dtype: torch.dtype) -> int:
+    return int(L.load().mm_swiglu_ffn_workspace_bytes(T, H, I, _DTYPES[dtype]))
+
+
+def moe_workspace_bytes(T: int, H: int, I: int, E: int, k: int, dtype: torch.dtype) -> int:
+    return int(L.load().mm_moe_workspace_bytes(T, H, I, E, k, _DTYPES[dtype]))
+
+
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """Caller-owned scratch; the first 256 bytes hold the watchdog word and
+    must start at zero."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def swiglu_ffn(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Tensor, *,
+               out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+               path: str = "auto", stream=None) -> torch.Tensor:
+    """y = Wd (SiLU(Wg x) ⊙ Wu x) for x [T, H] (mm_swiglu_ffn)."""
+    lib = L.load()
+    T, H = x.shape
+    I = Wg.shape[0]
+    dt = _dtype_code(x)
+    if out is None:
+        out = torch.empty_like(x)
+    need = lib.mm_swiglu_ffn_workspace_bytes(T, H, I, dt)
+    if workspace is None:
+        workspace = new_workspace(need, x.device)
+    rc = lib.mm_swiglu_ffn_ex(
+        _dev(x, "x"), _dev(Wg, "Wg", x.dtype), _dev(Wu, "Wu", x.dtype), _dev(Wd, "Wd", x.dtype),
+        _dev(out, "out", x.dtype), T, H, I, dt, _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream), _PATHS[path])
+    L.check(rc, "mm_swiglu_ffn")
+    return out
+
+
+def moe_forward(x: torch.Tensor, Wr: torch.Tensor, Wg: Sequence[torch.Tensor],
+                Wu: Sequence[torch.Tensor], Wd: Sequence[torch.Tensor], k: int, coef: float, *,
+                logit_bias: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                topk_idx: Optional[torch.Tensor] = None, topk_w: Optional[torch.Tensor] = None,
+                aux_loss: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                path: str = "auto", stream=None):
+    """Top-k MoE forward (mm_moe_forward).
+
+    Returns (y [T,H], topk_idx [T,k] int32, topk_w [T,k] fp32, aux_loss [] fp32).
+    """
+    lib = L.load()
+    T, H = x.shape
+    E = len(Wg)
+    I = Wg[0].shape[0]
+    dt = _dtype_code(x)
+    dev = x.device
+    out = torch.empty_like(x) if out is None else out
+    topk_idx = torch.empty(T, k, dtype=torch.int32, device=dev) if topk_idx is None else topk_idx
+    topk_w = torch.empty(T, k, dtype=torch.float32, device=dev) if topk_w is None else topk_w
+    aux_loss = torch.empty((), dtype=torch.float32, device=dev) if aux_loss is None else aux_loss
+    need = lib.mm_moe_workspace_bytes(T, H, I, E, k, dt)
+    if workspace is None:
+        workspace = new_workspace(need, dev)
+    pg, ag = L.ptr_array([_dev(w, "Wg", x.dtype) for w in Wg])
+    pu, au = L.ptr_array([_dev(w, "Wu", x.dtype) for w in Wu])
+    pd, ad = L.ptr_array([_dev(w, "Wd", x.dtype) for w in Wd])
+    bias_ptr = None if logit_bias is None else _dev(logit_bias, "logit_bias", torch.float32)
+    rc = lib.mm_moe_forward_ex(
+        _dev(x, "x"), _dev(Wr, "Wr", x.dtype), pg, pu, pd, T, H, I, E, k, float(coef), dt,
+        bias_ptr, _dev(out, "out", x.dtype), _dev(topk_idx, "topk_idx", torch.int32),
+        _dev(topk_w, "topk_w", torch.float32), _dev(aux_loss, "aux_loss", torch.float32),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream), _PATHS[path])
+    del ag, au, ad
+    L.check(rc, "mm_moe_forward")
+    return out, topk_idx, topk_w, aux_loss
+
+
+def moe_route(x: torch.Tensor, Wr: torch.Tensor, k: int, coef: float, *,
+              logit_bias: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+              stream=None):
+    """Router only (mm_moe_route): (topk_idx, topk_w, aux_loss, expert_counts)."""
+    lib = L.load()
+    T, H = x.shape
+    E = Wr.shape[0]
+    dt = _dtype_code(x)
+    dev = x.device
+    idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    aux = torch.empty((), dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    need = lib.mm_moe_route_workspace_bytes(T, E)
+    if workspace is None:
+        workspace = new_workspace(need, dev)
+    bias_ptr = None if logit_bias is None else _dev(logit_bias, "logit_bias", torch.float32)
+    rc = lib.mm_moe_route(_dev(x, "x"), _dev(Wr, "Wr", x.dtype), T, H, E, k, float(coef), dt,
+                          bias_ptr, idx.data_ptr(), w.data_ptr(), aux.data_ptr(),
+                          counts.data_ptr(), _dev(workspace, "workspace"),
+                          workspace.numel() * workspace.element_size(), _stream(stream))
+    L.check(rc, "mm_moe_route")
+    return idx, w, aux, counts
+
+
+def check_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise and return the device watchdog status (0 = fine); clears it."""
+    return int(L.load().mm_check_status(_dev(workspace, "workspace"), _stream(stream)))
+
+
+def watchdog_selftest(workspace: torch.Tensor, limit_us: int, stream=None) -> None:
+    rc = L.load().mm_watchdog_selftest(_dev(workspace, "workspace"),
+                                       workspace.numel() * workspace.element_size(),
+                                       int(limit_us), _stream(stream))
+    L.check(rc, "mm_watchdog_selftest")

@@ -1,0 +1,404 @@
+// C ABI (include/mm.h): argument checks, workspace layout, kernel sequencing.
+// Every entry point only enqueues work on the caller's stream.
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "mm_kernels.cuh"
+
+namespace mm {
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t elem_bytes(int dtype) { return dtype == kDtypeBF16 ? 2 : 4; }
+inline int route_blocks(int64_t T) {
+  return static_cast<int>((T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock);
+}
+
+thread_local char g_last_error[256] = "";
+
+int cuda_fail(cudaError_t e, const char* what) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s", what, cudaGetErrorString(e));
+  return MM_ERR_CUDA;
+}
+
+// ----------------------------------------------------------------- layouts
+struct MoeLayout {
+  size_t offsets, counts, blk_cnt, blk_prob, perm, xp, h, slots, total;
+};
+
+MoeLayout moe_layout(int64_t T, int H, int I, int E, int k, int dtype) {
+  MoeLayout L;
+  const size_t es = elem_bytes(dtype);
+  const size_t nblk = static_cast<size_t>(route_blocks(T));
+  const size_t rows = static_cast<size_t>(T) * static_cast<size_t>(k);
+  size_t off = sizeof(WsHeader);
+  L.offsets = off;  off += align_up(4 * static_cast<size_t>(E + 1));
+  L.counts = off;   off += align_up(4 * static_cast<size_t>(E));
+  L.blk_cnt = off;  off += align_up(4 * nblk * E);
+  L.blk_prob = off; off += align_up(4 * nblk * E);
+  L.perm = off;     off += align_up(4 * rows);
+  L.xp = off;       off += align_up(es * rows * H);
+  L.h = off;        off += align_up(es * rows * I);
+  L.slots = off;    if (k >= 3) off += align_up(es * rows * H);
+  L.total = off;
+  return L;
+}
+
+struct RouteLayout {
+  size_t blk_cnt, blk_prob, total;
+};
+RouteLayout route_layout(int64_t T, int E) {
+  RouteLayout L;
+  const size_t nblk = static_cast<size_t>(route_blocks(T));
+  size_t off = sizeof(WsHeader);
+  L.blk_cnt = off;  off += align_up(4 * nblk * E);
+  L.blk_prob = off; off += align_up(4 * nblk * E);
+  L.total = off;
+  return L;
+}
+
+size_t dense_ws_bytes(int64_t T, int I, int dtype) {
+  return sizeof(WsHeader) + align_up(elem_bytes(dtype) * static_cast<size_t>(T) * I);
+}
+
+bool valid_dtype(int dtype) { return dtype == kDtypeF32 || dtype == kDtypeBF16; }
+
+// bf16 tensor-core / streaming kernels tile K and N by 64
+bool tensor_shape_ok(int H, int I) { return H % 64 == 0 && I % 64 == 0; }
+
+int resolve_path(int path, int dtype, int64_t T) {
+  if (path == MM_PATH_AUTO) {
+    if (dtype == kDtypeF32) return MM_PATH_SIMT;
+    (void)T;
+    return MM_PATH_TENSOR;
+  }
+  return path;
+}
+
+inline char* ws_at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
+
+// ----------------------------------------------------------- measurement hooks
+std::atomic<uint64_t> g_launches{0};
+
+struct Profiler {
+  std::mutex mu;
+  int kernel = 0;
+  int max = 0;
+  int used = 0;
+  std::vector<cudaEvent_t> start, stop;
+};
+Profiler g_prof;
+
+// Runs `launch` (which enqueues one kernel on `st`), bracketed by timing
+// events when that kernel is being profiled.
+template <class F>
+cudaError_t counted_launch(int kernel, cudaStream_t st, F&& launch) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    if (g_prof.kernel == kernel && g_prof.used < g_prof.max) {
+      const int i = g_prof.used;
+      if (i >= static_cast<int>(g_prof.start.size())) {
+        cudaEvent_t e0, e1;
+        if (cudaEventCreate(&e0) == cudaSuccess && cudaEventCreate(&e1) == cudaSuccess) {
+          g_prof.start.push_back(e0);
+          g_prof.stop.push_back(e1);
+        }
+      }
+      if (i < static_cast<int>(g_prof.start.size())) {
+        a = g_prof.start[i];
+        b = g_prof.stop[i];
+        ++g_prof.used;
+      }
+    }
+  }
+  if (a) cudaEventRecord(a, st);
+  cudaError_t e = launch();
+  if (b) cudaEventRecord(b, st);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
+
+}  // namespace
+}  // namespace mm
+
+using namespace mm;
+
+extern "C" {
+
+const char* mm_status_string(int status) {
+  switch (status) {
+    case MM_OK: return "MM_OK";
+    case MM_ERR_INVALID_ARG: return "MM_ERR_INVALID_ARG";
+    case MM_ERR_UNSUPPORTED: return "MM_ERR_UNSUPPORTED";
+    case MM_ERR_WORKSPACE: return "MM_ERR_WORKSPACE";
+    case MM_ERR_CUDA: return "MM_ERR_CUDA";
+    case MM_ERR_TIMEOUT: return "MM_ERR_TIMEOUT";
+    default: return "MM_ERR_UNKNOWN";
+  }
+}
+
+int mm_version(void) { return 100; }
+
+const char* mm_last_error(void) { return g_last_error; }
+
+size_t mm_swiglu_ffn_workspace_bytes(int64_t T, int H, int I, int dtype) {
+  if (T < 0 || H < 1 || I < 1 || !valid_dtype(dtype)) return 0;
+  return dense_ws_bytes(T, I, dtype);
+}
+
+int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* Wd, void* y,
+                     int64_t T, int H, int I, int dtype, void* workspace, size_t workspace_bytes,
+                     void* stream, int path) {
+  if (!valid_dtype(dtype) || T < 0 || H < 1 || I < 1) return MM_ERR_INVALID_ARG;
+  if (H % 8 != 0 || I % 8 != 0) return MM_ERR_UNSUPPORTED;
+  if (T > (int64_t{1} << 30)) return MM_ERR_UNSUPPORTED;
+  if (path < MM_PATH_AUTO || path > MM_PATH_SIMT) return MM_ERR_INVALID_ARG;
+  if (T == 0) return MM_OK;
+  if (!x || !Wg || !Wu || !Wd || !y) return MM_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) || !aligned16(y))
+    return MM_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return MM_ERR_WORKSPACE;
+  if (workspace_bytes < dense_ws_bytes(T, I, dtype)) return MM_ERR_WORKSPACE;
+  const int p = resolve_path(path, dtype, T);
+  if ((p == MM_PATH_TENSOR || p == MM_PATH_STREAM) &&
+      (dtype != kDtypeBF16 || !tensor_shape_ok(H, I)))
+    return MM_ERR_UNSUPPORTED;
+  if (p == MM_PATH_STREAM) return MM_ERR_UNSUPPORTED;   // decode kernels: not in this build yet
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
+  void* h = ws_at(workspace, sizeof(WsHeader));
+  GroupRows g{nullptr, 1, static_cast<int>(T)};
+  DownEpilogue ep{y, nullptr, nullptr, 1, kCombineStore};
+  const void* wg[1] = {Wg};
+  const void* wu[1] = {Wu};
+  const void* wd[1] = {Wd};
+  cudaError_t e;
+  if (p == MM_PATH_TENSOR) {
+    e = counted_launch(MM_KERNEL_GATEUP, st, [&] { return launch_gateup_tc(x, T, H, I, g, wg, wu, h, 0, hdr, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "gateup_tc");
+    e = counted_launch(MM_KERNEL_DOWN, st, [&] { return launch_down_tc(h, T, H, I, g, wd, ep, hdr, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "down_tc");
+  } else {
+    e = counted_launch(MM_KERNEL_GATEUP, st, [&] { return launch_gateup_simt(dtype, x, T, H, I, g, wg, wu, h, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "gateup_simt");
+    e = counted_launch(MM_KERNEL_DOWN, st, [&] { return launch_down_simt(dtype, h, T, H, I, g, wd, ep, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "down_simt");
+  }
+  return MM_OK;
+}
+
+int mm_swiglu_ffn(const void* x, const void* Wg, const void* Wu, const void* Wd, void* y,
+                  int64_t T, int H, int I, int dtype, void* workspace, size_t workspace_bytes,
+                  void* stream) {
+  return mm_swiglu_ffn_ex(x, Wg, Wu, Wd, y, T, H, I, dtype, workspace, workspace_bytes, stream,
+                          MM_PATH_AUTO);
+}
+
+size_t mm_moe_workspace_bytes(int64_t T, int H, int I, int E, int k, int dtype) {
+  if (T < 1 || H < 1 || I < 1 || E < 1 || E > MM_MAX_EXPERTS || k < 1 || k > E ||
+      !valid_dtype(dtype))
+    return 0;
+  return moe_layout(T, H, I, E, k, dtype).total;
+}
+
+static int check_route_args(const void* x, const void* Wr, int64_t T, int H, int E, int k,
+                            int dtype, const float* logit_bias, const int32_t* topk_idx,
+                            const float* topk_w, const float* aux_loss) {
+  if (!valid_dtype(dtype) || T < 1 || H < 1 || E < 1 || k < 1 || k > E) return MM_ERR_INVALID_ARG;
+  if (E > MM_MAX_EXPERTS) return MM_ERR_UNSUPPORTED;
+  if (H % 8 != 0) return MM_ERR_UNSUPPORTED;
+  if (static_cast<size_t>(E) * H * 4 > 200 * 1024) return MM_ERR_UNSUPPORTED;
+  if (T > (int64_t{1} << 30) / k) return MM_ERR_UNSUPPORTED;
+  if (!x || !Wr || !topk_idx || !topk_w || !aux_loss) return MM_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wr)) return MM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(topk_idx) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u) ||
+      (reinterpret_cast<uintptr_t>(aux_loss) & 3u))
+    return MM_ERR_INVALID_ARG;
+  if (logit_bias && (reinterpret_cast<uintptr_t>(logit_bias) & 3u)) return MM_ERR_INVALID_ARG;
+  return MM_OK;
+}
+
+int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
+                      const void* const* Wu, const void* const* Wd, int64_t T, int H, int I, int E,
+                      int k, float coef, int dtype, const float* logit_bias, void* y,
+                      int32_t* topk_idx, float* topk_w, float* aux_loss, void* workspace,
+                      size_t workspace_bytes, void* stream, int path) {
+  int rc = check_route_args(x, Wr, T, H, E, k, dtype, logit_bias, topk_idx, topk_w, aux_loss);
+  if (rc != MM_OK) return rc;
+  if (I < 1) return MM_ERR_INVALID_ARG;
+  if (I % 8 != 0) return MM_ERR_UNSUPPORTED;
+  if (path < MM_PATH_AUTO || path > MM_PATH_SIMT) return MM_ERR_INVALID_ARG;
+  if (!Wg || !Wu || !Wd || !y || !aligned16(y)) return MM_ERR_INVALID_ARG;
+  for (int e = 0; e < E; ++e) {
+    if (!Wg[e] || !Wu[e] || !Wd[e]) return MM_ERR_INVALID_ARG;
+    if (!aligned16(Wg[e]) || !aligned16(Wu[e]) || !aligned16(Wd[e])) return MM_ERR_INVALID_ARG;
+  }
+  if (!workspace || !aligned16(workspace)) return MM_ERR_WORKSPACE;
+  const MoeLayout L = moe_layout(T, H, I, E, k, dtype);
+  if (workspace_bytes < L.total) return MM_ERR_WORKSPACE;
+  const int p = resolve_path(path, dtype, T);
+  if ((p == MM_PATH_TENSOR || p == MM_PATH_STREAM) &&
+      (dtype != kDtypeBF16 || !tensor_shape_ok(H, I)))
+    return MM_ERR_UNSUPPORTED;
+  if (p == MM_PATH_STREAM) return MM_ERR_UNSUPPORTED;   // decode kernels: not in this build yet
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws_at(workspace, L.offsets));
+  int32_t* counts = reinterpret_cast<int32_t*>(ws_at(workspace, L.counts));
+  int32_t* blk_cnt = reinterpret_cast<int32_t*>(ws_at(workspace, L.blk_cnt));
+  float* blk_prob = reinterpret_cast<float*>(ws_at(workspace, L.blk_prob));
+  int32_t* perm = reinterpret_cast<int32_t*>(ws_at(workspace, L.perm));
+  void* xp = ws_at(workspace, L.xp);
+  void* h = ws_at(workspace, L.h);
+  void* slots = ws_at(workspace, L.slots);
+
+  cudaError_t e = counted_launch(MM_KERNEL_ROUTER, st, [&] {
+    return launch_router(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w, blk_cnt,
+                         blk_prob, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "router");
+  e = counted_launch(MM_KERNEL_DISPATCH, st, [&] {
+    return launch_dispatch(dtype, x, T, H, E, k, coef, topk_idx, blk_cnt, blk_prob, offsets,
+                           counts, aux_loss, perm, xp, (k == 2) ? y : nullptr, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "dispatch");
+
+  const int64_t rows = T * k;
+  GroupRows g{offsets, E, 0};
+  DownEpilogue ep;
+  ep.perm = perm;
+  ep.topk_w = topk_w;
+  ep.k = k;
+  if (k == 1) {
+    ep.y = y;
+    ep.mode = kCombineStore;
+  } else if (k == 2) {
+    ep.y = y;
+    ep.mode = kCombineAtomic;
+  } else {
+    ep.y = slots;
+    ep.mode = kCombineSlots;
+  }
+  if (p == MM_PATH_TENSOR) {
+    e = counted_launch(MM_KERNEL_GATEUP, st, [&] { return launch_gateup_tc(xp, rows, H, I, g, Wg, Wu, h, 0, hdr, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "gateup_tc");
+    e = counted_launch(MM_KERNEL_DOWN, st, [&] { return launch_down_tc(h, rows, H, I, g, Wd, ep, hdr, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "down_tc");
+  } else {
+    e = counted_launch(MM_KERNEL_GATEUP, st, [&] { return launch_gateup_simt(dtype, xp, rows, H, I, g, Wg, Wu, h, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "gateup_simt");
+    e = counted_launch(MM_KERNEL_DOWN, st, [&] { return launch_down_simt(dtype, h, rows, H, I, g, Wd, ep, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "down_simt");
+  }
+  if (k >= 3) {
+    e = counted_launch(MM_KERNEL_COMBINE, st, [&] { return launch_combine_ordered(dtype, slots, topk_idx, T, H, k, y, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "combine");
+  }
+  return MM_OK;
+}
+
+int mm_moe_forward(const void* x, const void* Wr, const void* const* Wg, const void* const* Wu,
+                   const void* const* Wd, int64_t T, int H, int I, int E, int k, float coef,
+                   int dtype, const float* logit_bias, void* y, int32_t* topk_idx, float* topk_w,
+                   float* aux_loss, void* workspace, size_t workspace_bytes, void* stream) {
+  return mm_moe_forward_ex(x, Wr, Wg, Wu, Wd, T, H, I, E, k, coef, dtype, logit_bias, y, topk_idx,
+                           topk_w, aux_loss, workspace, workspace_bytes, stream, MM_PATH_AUTO);
+}
+
+size_t mm_moe_route_workspace_bytes(int64_t T, int E) {
+  if (T < 1 || E < 1 || E > MM_MAX_EXPERTS) return 0;
+  return route_layout(T, E).total;
+}
+
+int mm_moe_route(const void* x, const void* Wr, int64_t T, int H, int E, int k, float coef,
+                 int dtype, const float* logit_bias, int32_t* topk_idx, float* topk_w,
+                 float* aux_loss, int32_t* expert_counts, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  int rc = check_route_args(x, Wr, T, H, E, k, dtype, logit_bias, topk_idx, topk_w, aux_loss);
+  if (rc != MM_OK) return rc;
+  if (expert_counts && (reinterpret_cast<uintptr_t>(expert_counts) & 3u)) return MM_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return MM_ERR_WORKSPACE;
+  const RouteLayout L = route_layout(T, E);
+  if (workspace_bytes < L.total) return MM_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* blk_cnt = reinterpret_cast<int32_t*>(ws_at(workspace, L.blk_cnt));
+  float* blk_prob = reinterpret_cast<float*>(ws_at(workspace, L.blk_prob));
+  cudaError_t e = counted_launch(MM_KERNEL_ROUTER, st, [&] {
+    return launch_router(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w, blk_cnt,
+                         blk_prob, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "router");
+  e = counted_launch(MM_KERNEL_DISPATCH, st, [&] {
+    return launch_route_finalize(E, route_blocks(T), T, coef, blk_cnt, blk_prob, nullptr, nullptr,
+                                 aux_loss, expert_counts, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "route_finalize");
+  return MM_OK;
+}
+
+uint64_t mm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int mm_profile_start(int kernel_id, int max_launches) {
+  if (kernel_id < MM_KERNEL_ROUTER || kernel_id > MM_KERNEL_COMBINE) return MM_ERR_INVALID_ARG;
+  if (max_launches < 1 || max_launches > 100000) return MM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  g_prof.kernel = kernel_id;
+  g_prof.max = max_launches;
+  g_prof.used = 0;
+  return MM_OK;
+}
+
+int mm_profile_stop(double* total_ms, int* launches) {
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  double sum = 0.0;
+  int n = g_prof.used;
+  for (int i = 0; i < n; ++i) {
+    cudaError_t e = cudaEventSynchronize(g_prof.stop[i]);
+    if (e != cudaSuccess) return cuda_fail(e, "profile sync");
+    float ms = 0.f;
+    e = cudaEventElapsedTime(&ms, g_prof.start[i], g_prof.stop[i]);
+    if (e != cudaSuccess) return cuda_fail(e, "profile elapsed");
+    sum += ms;
+  }
+  g_prof.kernel = 0;
+  g_prof.used = 0;
+  if (total_ms) *total_ms = sum;
+  if (launches) *launches = n;
+  return MM_OK;
+}
+
+int mm_check_status(void* workspace, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "stream");
+  if (workspace == nullptr) return MM_OK;
+  unsigned int word = 0;
+  e = cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (word != 0) {
+    e = cudaMemset(workspace, 0, sizeof(WsHeader));
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+    return static_cast<int>(word);
+  }
+  return MM_OK;
+}
+
+int mm_watchdog_selftest(void* workspace, size_t workspace_bytes, uint32_t limit_us, void* stream) {
+  if (!workspace || workspace_bytes < sizeof(WsHeader) || !aligned16(workspace))
+    return MM_ERR_WORKSPACE;
+  if (limit_us < 1 || limit_us > 10000000u) return MM_ERR_INVALID_ARG;
+  cudaError_t e = launch_watchdog_selftest(reinterpret_cast<WsHeader*>(workspace), limit_us,
+                                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "watchdog_selftest");
+  return MM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include "../../include/mm.h"
+#include "mm_device.cuh"
+
+namespace mm {
+
+constexpr int kDtypeF32 = MM_DTYPE_F32;
+constexpr int kDtypeBF16 = MM_DTYPE_BF16;
+
+// Router / dispatch geometry.
+constexpr int kRouteThreads = 256;          // 8 warps
+constexpr int kRouteTokensPerBlock = 64;    // 8 tokens per warp
+
+// Tensor-core GEMM geometry (tcgen05, cta_group::1).
+constexpr int kTcBM = 128;                  // rows per tile (TMEM lanes)
+constexpr int kTcBK = 64;                   // K per stage: one 128-byte swizzle row of bf16
+constexpr int kUpBN = 128;                  // h columns per gate/up tile (MMA N = 256: g | u)
+constexpr int kDownBN = 192;                // y columns per down tile
+constexpr int kTcThreads = 192;             // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer
+
+// How the down-projection epilogue writes its rows.
+enum CombineMode : int {
+  kCombineStore = 0,    // y[token] = alpha * acc            (dense, k = 1)
+  kCombineAtomic = 1,   // y[token] += alpha * acc  (y zeroed first; k = 2: two terms commute)
+  kCombineSlots = 2     // slots[t*k + s] = alpha * acc     (k >= 3: ordered combine afterwards)
+};
+
+// Description of the row groups (experts) of a grouped GEMM.
+struct GroupRows {
+  const int32_t* offsets;   // device [E+1] row offsets, or nullptr: one group of dense_rows rows
+  int E;
+  int dense_rows;
+};
+
+// Epilogue inputs of the down projection.
+struct DownEpilogue {
+  void* y;                  // [T, H] (store / atomic) or slots [T*k, H]
+  const int32_t* perm;      // row -> t*k + s, or nullptr (row == token, alpha = 1)
+  const float* topk_w;      // [T*k] alpha, or nullptr (alpha = 1)
+  int k;
+  int mode;                 // CombineMode
+};
+
+cudaError_t launch_router(int dtype, const void* x, const void* Wr, const float* bias, int64_t T,
+                          int H, int E, int k, int32_t* topk_idx, float* topk_w, int32_t* blk_cnt,
+                          float* blk_prob, cudaStream_t st);
+cudaError_t launch_route_finalize(int E, int nblk, int64_t T, float coef, const int32_t* blk_cnt,
+                                  const float* blk_prob, int32_t* offsets, int32_t* counts,
+                                  float* aux_loss, int32_t* counts_out, cudaStream_t st);
+cudaError_t launch_dispatch(int dtype, const void* x, int64_t T, int H, int E, int k, float coef,
+                            const int32_t* topk_idx, const int32_t* blk_cnt, const float* blk_prob,
+                            int32_t* offsets, int32_t* counts, float* aux_loss, int32_t* perm,
+                            void* Xp, void* y_zero, cudaStream_t st);
+cudaError_t launch_combine_ordered(int dtype, const void* slots, const int32_t* topk_idx, int64_t T,
+                                   int H, int k, void* y, cudaStream_t st);
+
+// Tensor-core grouped GEMMs (bf16).  A is [rows, K] row-major; each group e
+// multiplies its rows by its own weight matrices.
+cudaError_t launch_gateup_tc(const void* A, int64_t a_rows, int H, int I, const GroupRows& g,
+                             const void* const* Wg, const void* const* Wu, void* h_out,
+                             int max_groups_tiles_hint, WsHeader* hdr, cudaStream_t st);
+cudaError_t launch_down_tc(const void* h, int64_t a_rows, int H, int I, const GroupRows& g,
+                           const void* const* Wd, const DownEpilogue& ep, WsHeader* hdr,
+                           cudaStream_t st);
+
+// CUDA-core (fp32 FMA) grouped kernels, any dtype.
+cudaError_t launch_gateup_simt(int dtype, const void* A, int64_t a_rows, int H, int I,
+                               const GroupRows& g, const void* const* Wg, const void* const* Wu,
+                               void* h_out, cudaStream_t st);
+cudaError_t launch_down_simt(int dtype, const void* h, int64_t a_rows, int H, int I,
+                             const GroupRows& g, const void* const* Wd, const DownEpilogue& ep,
+                             cudaStream_t st);
+
+cudaError_t launch_watchdog_selftest(WsHeader* hdr, uint32_t limit_us, cudaStream_t st);
+
+int num_sms();
+
+}  // namespace mm

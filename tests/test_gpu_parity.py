@@ -1,0 +1,180 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle,
+element by element, on seeded inputs.  Small cases span several tiles and a
+ragged tail; the full-size workloads are checked on every routing output and
+on sampled rows of y (the oracle computes those rows one by one).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import swiglu_mlp_top_gb300 as mm
+from swiglu_mlp_top_gb300.inputs import WORKLOADS, make_inputs, make_workload_inputs, to_f64
+
+from parity import (Y_TOL, check_route, inputs64, moe_inputs, ref_y_rows, rel_err, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+def run_moe(inp, k, coef, path="auto"):
+    g = to_dev(inp)
+    y, idx, w, aux = mm.moe_forward(g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], k, coef,
+                                    logit_bias=g.get("logit_bias"), path=path)
+    torch.cuda.synchronize()
+    return (y.double().cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy(), float(aux))
+
+
+def full_moe_check(inp, k, coef, dtype, path="auto"):
+    y, idx, w, aux = run_moe(inp, k, coef, path)
+    i64 = inputs64(inp)
+    ref = oracle.moe_forward(i64["x"], i64["Wr"], i64["Wg"], i64["Wu"], i64["Wd"], k, coef,
+                             i64.get("logit_bias"))
+    tie, diff = check_route(idx, w, aux, ref, k)
+    yref = ref["y"].copy()
+    if diff.any():
+        rows = np.nonzero(diff)[0]
+        yref[rows] = ref_y_rows(i64, ref, idx, rows, k)
+    err = rel_err(y, yref)
+    assert err <= Y_TOL[dtype], f"y rel err {err}"
+    return err, int(tie.sum())
+
+
+# ------------------------------------------------------------------ fp32 (SIMT)
+def test_tiny_moe_f32_config():
+    """B=2, S=16, H=64, I=256, E=4, k=1, coef 0.01, fp32."""
+    w = WORKLOADS["tiny_moe_f32"]
+    inp = make_workload_inputs(w)
+    full_moe_check(inp, w.k, w.coef, "f32")
+
+
+@pytest.mark.parametrize("T,H,I,E,k", [(77, 64, 96, 5, 2), (45, 32, 64, 6, 3), (33, 64, 128, 4, 4)])
+def test_moe_f32_ragged(T, H, I, E, k):
+    full_moe_check(moe_inputs(T, H, I, E, "f32", seed=3), k, 0.01, "f32")
+
+
+def test_dense_f32():
+    inp = make_inputs(70, 64, 256, "f32", seed=4)
+    g = to_dev(inp)
+    y = mm.swiglu_ffn(g["x"], g["Wg"], g["Wu"], g["Wd"])
+    ref = oracle.swiglu_ffn(*[to_f64(inp[n]) for n in ("x", "Wg", "Wu", "Wd")])
+    assert rel_err(y.double().cpu().numpy(), ref) <= Y_TOL["f32"]
+
+
+# ------------------------------------------------------------------ bf16 tensor cores
+@pytest.mark.parametrize("T", [1, 100, 300, 1000])
+def test_dense_bf16_tensor(T):
+    inp = make_inputs(T, 256, 384, "bf16", seed=T)
+    g = to_dev(inp)
+    y = mm.swiglu_ffn(g["x"], g["Wg"], g["Wu"], g["Wd"], path="tensor")
+    ref = oracle.swiglu_ffn(*[to_f64(inp[n]) for n in ("x", "Wg", "Wu", "Wd")])
+    assert rel_err(y.double().cpu().numpy(), ref) <= Y_TOL["bf16"]
+
+
+@pytest.mark.parametrize("T,H,I,E,k,bias", [
+    (1000, 256, 384, 4, 1, None),
+    (777, 256, 320, 8, 2, (1.5, 0.5, 0, 0, 0, 0, 0, 0)),
+    (513, 128, 192, 6, 3, None),
+    (260, 192, 256, 4, 4, None),
+    (130, 64, 128, 1, 1, None),
+    (1, 256, 384, 8, 2, None),
+])
+def test_moe_bf16_tensor(T, H, I, E, k, bias):
+    full_moe_check(moe_inputs(T, H, I, E, "bf16", seed=7, bias=bias), k, 0.01, "bf16", path="tensor")
+
+
+@pytest.mark.parametrize("T,E,k", [(300, 4, 1), (257, 8, 2)])
+def test_moe_bf16_simt_second_path(T, E, k):
+    full_moe_check(moe_inputs(T, 128, 192, E, "bf16", seed=9), k, 0.01, "bf16", path="simt")
+
+
+def test_tensor_and_simt_paths_agree_on_routing():
+    inp = moe_inputs(400, 256, 256, 8, "bf16", seed=11)
+    a = run_moe(inp, 2, 0.01, "tensor")
+    b = run_moe(inp, 2, 0.01, "simt")
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2]) and a[3] == b[3]
+    assert rel_err(a[0], b[0]) < 2e-2
+
+
+def test_uniform_router_tie_break_on_gpu():
+    """Wr = 0 -> p = 1/E for every token -> experts 0..k-1, alpha = 1/k, aux = k*coef."""
+    inp = moe_inputs(200, 128, 128, 8, "bf16", seed=12)
+    inp["Wr"] = torch.zeros_like(inp["Wr"])
+    y, idx, w, aux = run_moe(inp, 3, 0.01, "tensor")
+    assert np.all(idx == np.arange(3)[None, :])
+    assert np.allclose(w, 1.0 / 3, atol=1e-7)
+    assert abs(aux - 0.03) < 1e-6
+
+
+def test_moe_deterministic():
+    inp = moe_inputs(900, 256, 256, 8, "bf16", seed=13)
+    a = run_moe(inp, 2, 0.01)
+    b = run_moe(inp, 2, 0.01)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]) and a[3] == b[3]
+
+
+def test_route_only_entry_point():
+    inp = moe_inputs(5000, 768, 64, 8, "bf16", seed=14, bias=(1.5, 0.5, 0, 0, 0, 0, 0, 0))
+    g = to_dev(inp)
+    idx, w, aux, counts = mm.moe_route(g["x"], g["Wr"], 2, 0.01, logit_bias=g["logit_bias"])
+    torch.cuda.synchronize()
+    i64 = inputs64(inp)
+    ref = oracle.moe_route(i64["x"], i64["Wr"], 2, 0.01, i64["logit_bias"])
+    tie, diff = check_route(idx.cpu().numpy(), w.cpu().numpy(), float(aux), ref, 2)
+    if not diff.any():
+        assert counts.cpu().numpy().tolist() == ref["counts"].tolist()
+
+
+def test_dense_empty_input():
+    x = torch.empty(0, 256, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(384, 256, dtype=torch.bfloat16, device="cuda")
+    Wd = torch.zeros(256, 384, dtype=torch.bfloat16, device="cuda")
+    y = mm.swiglu_ffn(x, W, W, Wd)
+    assert y.shape == (0, 256)
+
+
+# ------------------------------------------------------------------ full-size workloads
+def _sample_rows(T, n=256, seed=0):
+    r = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([[0, T - 1], r.choice(T, size=min(n, T), replace=False)]))
+    return rows
+
+
+@pytest.mark.parametrize("name", ["dense_t4096", "dense_t100"])
+def test_dense_full_size(name):
+    w = WORKLOADS[name]
+    inp = make_workload_inputs(w)
+    g = to_dev(inp)
+    y = mm.swiglu_ffn(g["x"], g["Wg"], g["Wu"], g["Wd"])
+    torch.cuda.synchronize()
+    ref = oracle.swiglu_ffn(*[to_f64(inp[n]) for n in ("x", "Wg", "Wu", "Wd")])
+    assert rel_err(y.double().cpu().numpy(), ref) <= Y_TOL["bf16"]
+
+
+@pytest.mark.parametrize("name", ["moe_e4k1_t8192", "moe_e8k2_t16384_skew"])
+def test_moe_full_size(name):
+    w = WORKLOADS[name]
+    inp = make_workload_inputs(w)
+    y, idx, wt, aux = run_moe(inp, w.k, w.coef)
+    i64 = inputs64(inp)
+    ref = oracle.moe_route(i64["x"], i64["Wr"], w.k, w.coef, i64.get("logit_bias"))
+    tie, diff = check_route(idx, wt, aux, ref, w.k)
+    rows = _sample_rows(w.T)
+    yref = ref_y_rows(i64, ref, idx, rows, w.k)
+    err = rel_err(y[rows], yref)
+    assert err <= Y_TOL["bf16"], f"sampled y rel err {err}"
+    # every output row is finite and the layout is dense
+    assert np.isfinite(y).all()
+
+
+# ------------------------------------------------------------------ watchdog
+def test_watchdog_reports_timeout_and_recovers():
+    ws = mm.new_workspace(256)
+    assert mm.check_status(ws) == 0
+    mm.watchdog_selftest(ws, 2000)          # 2 ms wait that nothing ends
+    assert mm.check_status(ws) == 5          # MM_ERR_TIMEOUT
+    assert mm.check_status(ws) == 0          # cleared
+    # the context is still usable
+    inp = make_inputs(64, 128, 128, "bf16", seed=2)
+    g = to_dev(inp)
+    mm.swiglu_ffn(g["x"], g["Wg"], g["Wu"], g["Wd"], workspace=None)
+    torch.cuda.synchronize()
