@@ -62,6 +62,7 @@ typedef enum {
 
 /* Limits of this build. */
 #define MM_MAX_EXPERTS 64
+#define MM_MAX_TOPK 8
 
 /* Human-readable name of an mm_status value (static string). */
 const char* mm_status_string(int status);
@@ -99,9 +100,9 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
  *   r = Wr x (+ logit_bias);  p = softmax(r)            (fp32)
  *   S = TopK(p, k): descending p, equal p -> lower expert index first
  *   alpha_e = p_e / (sum_{j in S} p_j + 1e-20)
- *   y = sum_{e in S} alpha_e · SwiGLU_e(x)   — each term is rounded to y's
- *       dtype and the terms are added in ascending expert order in y's dtype
- *       (the pages' index_add_ into a zeroed y)
+ *   y = sum_{e in S} alpha_e · SwiGLU_e(x)   — the k terms are added in fp32
+ *       in slot order and rounded once to y's dtype (deterministic; the
+ *       pages' index_add_ into y rounds every term, which costs accuracy)
  *   count_e = #{(t,s): S_t[s] = e},  P_e = sum_t p_{t,e}
  *   aux_loss = E · coef · sum_e (count_e / T) · (P_e / T)
  *
@@ -115,7 +116,8 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
  *   topk_idx [T,k]                    device int32, slots in descending p
  *   topk_w [T,k]                      device fp32, alpha of each slot
  *   aux_loss                          device fp32 scalar (coef = 0 gives 0)
- * Limits: T >= 1; 1 <= k <= E <= MM_MAX_EXPERTS; E*H*4 <= 200 KiB.
+ * Limits: T >= 1; 1 <= E <= MM_MAX_EXPERTS; 1 <= k <= min(E, MM_MAX_TOPK);
+ * H a multiple of 8 and (E*H + k*E)*4 <= 200 KiB.
  * ---------------------------------------------------------------------- */
 size_t mm_moe_workspace_bytes(int64_t T, int H, int I, int E, int k, int dtype);
 
@@ -136,7 +138,7 @@ int mm_moe_forward_ex(const void* x, const void* Wr,
 /* Router half of the MoE forward only (logits, softmax, top-k, alpha, aux):
  * same arguments and meaning as mm_moe_forward without the experts and y.
  * expert_counts (device int32 [E], nullable) receives count_e. */
-size_t mm_moe_route_workspace_bytes(int64_t T, int E);
+size_t mm_moe_route_workspace_bytes(int64_t T, int E, int k);
 
 int mm_moe_route(const void* x, const void* Wr, int64_t T, int H, int E, int k,
                  float coef, int dtype, const float* logit_bias,
@@ -165,10 +167,10 @@ int mm_watchdog_selftest(void* workspace, size_t workspace_bytes,
  * ---------------------------------------------------------------------- */
 typedef enum {
   MM_KERNEL_ROUTER = 1,     /* logits/softmax/top-k/alpha/aux partials      */
-  MM_KERNEL_DISPATCH = 2,   /* aux finalisation + token permute             */
-  MM_KERNEL_GATEUP = 3,     /* gate/up GEMM with the SwiGLU epilogue        */
-  MM_KERNEL_DOWN = 4,       /* down GEMM with the alpha-scale/combine       */
-  MM_KERNEL_COMBINE = 5     /* ordered combine (k >= 3)                     */
+  MM_KERNEL_SCAN = 2,       /* group offsets + aux loss finalisation        */
+  MM_KERNEL_DISPATCH = 3,   /* token permute into expert-contiguous rows    */
+  MM_KERNEL_GATEUP = 4,     /* gate/up GEMM with the SwiGLU epilogue        */
+  MM_KERNEL_DOWN = 5        /* down GEMM with the alpha-scaled combine      */
 } mm_kernel_id;
 
 /* Number of kernels this library has enqueued since it was loaded. */

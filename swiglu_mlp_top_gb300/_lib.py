@@ -14,6 +14,7 @@ MM_OK, MM_ERR_INVALID_ARG, MM_ERR_UNSUPPORTED, MM_ERR_WORKSPACE, MM_ERR_CUDA, MM
 MM_DTYPE_F32, MM_DTYPE_BF16 = 0, 1
 MM_PATH_AUTO, MM_PATH_TENSOR, MM_PATH_STREAM, MM_PATH_SIMT = 0, 1, 2, 3
 MM_MAX_EXPERTS = 64
+MM_MAX_TOPK = 8
 
 _vp, _i32, _i64, _f32, _sz = C.c_void_p, C.c_int, C.c_int64, C.c_float, C.c_size_t
 _pp = C.POINTER(C.c_void_p)
@@ -32,7 +33,7 @@ SIGNATURES = {
                               _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "mm_moe_forward_ex": (_i32, [_vp, _vp, _pp, _pp, _pp, _i64, _i32, _i32, _i32, _i32, _f32,
                                  _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _i32]),
-    "mm_moe_route_workspace_bytes": (_sz, [_i64, _i32]),
+    "mm_moe_route_workspace_bytes": (_sz, [_i64, _i32, _i32]),
     "mm_moe_route": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _f32, _i32, _vp, _vp, _vp, _vp,
                             _vp, _vp, _sz, _vp]),
     "mm_check_status": (_i32, [_vp, _vp]),
@@ -41,7 +42,7 @@ SIGNATURES = {
     "mm_profile_start": (_i32, [_i32, _i32]),
     "mm_profile_stop": (_i32, [C.POINTER(C.c_double), C.POINTER(C.c_int)]),
 }
-MM_KERNEL_ROUTER, MM_KERNEL_DISPATCH, MM_KERNEL_GATEUP, MM_KERNEL_DOWN, MM_KERNEL_COMBINE = 1, 2, 3, 4, 5
+MM_KERNEL_ROUTER, MM_KERNEL_SCAN, MM_KERNEL_DISPATCH, MM_KERNEL_GATEUP, MM_KERNEL_DOWN = 1, 2, 3, 4, 5
 
 _lib = None
 

@@ -123,7 +123,7 @@ def moe_route(x: torch.Tensor, Wr: torch.Tensor, k: int, coef: float, *,
     w = torch.empty(T, k, dtype=torch.float32, device=dev)
     aux = torch.empty((), dtype=torch.float32, device=dev)
     counts = torch.empty(E, dtype=torch.int32, device=dev)
-    need = lib.mm_moe_route_workspace_bytes(T, E)
+    need = lib.mm_moe_route_workspace_bytes(T, E, k)
     if workspace is None:
         workspace = new_workspace(need, dev)
     bias_ptr = None if logit_bias is None else _dev(logit_bias, "logit_bias", torch.float32)

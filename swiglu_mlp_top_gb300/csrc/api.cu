@@ -28,23 +28,28 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 // ----------------------------------------------------------------- layouts
 struct MoeLayout {
-  size_t offsets, counts, blk_cnt, blk_prob, perm, xp, h, slots, total;
+  size_t offsets, counts, blk_cnt, blk_base, blk_prob, perm, xp, h, acc32, total;
 };
 
+// Workspace of the MoE forward: routing tables, the dispatched rows Xp
+// ([T*k, H], grouped by slot, then expert, then token), h ([T*k, I]) and,
+// for bf16 with k >= 2, the fp32 running sum of y ([T, H]).
 MoeLayout moe_layout(int64_t T, int H, int I, int E, int k, int dtype) {
   MoeLayout L;
   const size_t es = elem_bytes(dtype);
   const size_t nblk = static_cast<size_t>(route_blocks(T));
   const size_t rows = static_cast<size_t>(T) * static_cast<size_t>(k);
+  const size_t G = static_cast<size_t>(k) * E;
   size_t off = sizeof(WsHeader);
-  L.offsets = off;  off += align_up(4 * static_cast<size_t>(E + 1));
+  L.offsets = off;  off += align_up(4 * (G + 1));
   L.counts = off;   off += align_up(4 * static_cast<size_t>(E));
-  L.blk_cnt = off;  off += align_up(4 * nblk * E);
+  L.blk_cnt = off;  off += align_up(4 * nblk * G);
+  L.blk_base = off; off += align_up(4 * nblk * G);
   L.blk_prob = off; off += align_up(4 * nblk * E);
   L.perm = off;     off += align_up(4 * rows);
   L.xp = off;       off += align_up(es * rows * H);
   L.h = off;        off += align_up(es * rows * I);
-  L.slots = off;    if (k >= 3) off += align_up(es * rows * H);
+  L.acc32 = off;    if (k >= 2 && dtype == kDtypeBF16) off += align_up(4 * static_cast<size_t>(T) * H);
   L.total = off;
   return L;
 }
@@ -52,11 +57,11 @@ MoeLayout moe_layout(int64_t T, int H, int I, int E, int k, int dtype) {
 struct RouteLayout {
   size_t blk_cnt, blk_prob, total;
 };
-RouteLayout route_layout(int64_t T, int E) {
+RouteLayout route_layout(int64_t T, int E, int k) {
   RouteLayout L;
   const size_t nblk = static_cast<size_t>(route_blocks(T));
   size_t off = sizeof(WsHeader);
-  L.blk_cnt = off;  off += align_up(4 * nblk * E);
+  L.blk_cnt = off;  off += align_up(4 * nblk * static_cast<size_t>(k) * E);
   L.blk_prob = off; off += align_up(4 * nblk * E);
   L.total = off;
   return L;
@@ -174,14 +179,14 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
   void* h = ws_at(workspace, sizeof(WsHeader));
-  GroupRows g{nullptr, 1, static_cast<int>(T)};
-  DownEpilogue ep{y, nullptr, nullptr, 1, kCombineStore};
+  GroupRows g{nullptr, 1, static_cast<int>(T), 1};
+  DownEpilogue ep{y, nullptr, nullptr, nullptr, 1, kCombineStore};
   const void* wg[1] = {Wg};
   const void* wu[1] = {Wu};
   const void* wd[1] = {Wd};
   cudaError_t e;
   if (p == MM_PATH_TENSOR) {
-    e = counted_launch(MM_KERNEL_GATEUP, st, [&] { return launch_gateup_tc(x, T, H, I, g, wg, wu, h, 0, hdr, st); });
+    e = counted_launch(MM_KERNEL_GATEUP, st, [&] { return launch_gateup_tc(x, T, H, I, g, wg, wu, h, hdr, st); });
     if (e != cudaSuccess) return cuda_fail(e, "gateup_tc");
     e = counted_launch(MM_KERNEL_DOWN, st, [&] { return launch_down_tc(h, T, H, I, g, wd, ep, hdr, st); });
     if (e != cudaSuccess) return cuda_fail(e, "down_tc");
@@ -205,6 +210,7 @@ size_t mm_moe_workspace_bytes(int64_t T, int H, int I, int E, int k, int dtype) 
   if (T < 1 || H < 1 || I < 1 || E < 1 || E > MM_MAX_EXPERTS || k < 1 || k > E ||
       !valid_dtype(dtype))
     return 0;
+  if (k > MM_MAX_TOPK) return 0;
   return moe_layout(T, H, I, E, k, dtype).total;
 }
 
@@ -212,9 +218,9 @@ static int check_route_args(const void* x, const void* Wr, int64_t T, int H, int
                             int dtype, const float* logit_bias, const int32_t* topk_idx,
                             const float* topk_w, const float* aux_loss) {
   if (!valid_dtype(dtype) || T < 1 || H < 1 || E < 1 || k < 1 || k > E) return MM_ERR_INVALID_ARG;
-  if (E > MM_MAX_EXPERTS) return MM_ERR_UNSUPPORTED;
+  if (E > MM_MAX_EXPERTS || k > MM_MAX_TOPK) return MM_ERR_UNSUPPORTED;
   if (H % 8 != 0) return MM_ERR_UNSUPPORTED;
-  if (static_cast<size_t>(E) * H * 4 > 200 * 1024) return MM_ERR_UNSUPPORTED;
+  if (router_smem_bytes(H, E, k) > 200 * 1024) return MM_ERR_UNSUPPORTED;
   if (T > (int64_t{1} << 30) / k) return MM_ERR_UNSUPPORTED;
   if (!x || !Wr || !topk_idx || !topk_w || !aux_loss) return MM_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(Wr)) return MM_ERR_INVALID_ARG;
@@ -254,53 +260,57 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
   int32_t* offsets = reinterpret_cast<int32_t*>(ws_at(workspace, L.offsets));
   int32_t* counts = reinterpret_cast<int32_t*>(ws_at(workspace, L.counts));
   int32_t* blk_cnt = reinterpret_cast<int32_t*>(ws_at(workspace, L.blk_cnt));
+  int32_t* blk_base = reinterpret_cast<int32_t*>(ws_at(workspace, L.blk_base));
   float* blk_prob = reinterpret_cast<float*>(ws_at(workspace, L.blk_prob));
   int32_t* perm = reinterpret_cast<int32_t*>(ws_at(workspace, L.perm));
   void* xp = ws_at(workspace, L.xp);
   void* h = ws_at(workspace, L.h);
-  void* slots = ws_at(workspace, L.slots);
+  float* acc32 = (dtype == kDtypeF32) ? static_cast<float*>(y)
+                                      : reinterpret_cast<float*>(ws_at(workspace, L.acc32));
 
   cudaError_t e = counted_launch(MM_KERNEL_ROUTER, st, [&] {
     return launch_router(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w, blk_cnt,
                          blk_prob, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "router");
+  e = counted_launch(MM_KERNEL_SCAN, st, [&] {
+    return launch_route_scan(E, k, T, coef, blk_cnt, blk_prob, blk_base, offsets, counts,
+                             aux_loss, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "route_scan");
   e = counted_launch(MM_KERNEL_DISPATCH, st, [&] {
-    return launch_dispatch(dtype, x, T, H, E, k, coef, topk_idx, blk_cnt, blk_prob, offsets,
-                           counts, aux_loss, perm, xp, (k == 2) ? y : nullptr, st);
+    return launch_dispatch(dtype, x, T, H, E, k, topk_idx, blk_base, offsets, perm, xp, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "dispatch");
 
   const int64_t rows = T * k;
-  GroupRows g{offsets, E, 0};
-  DownEpilogue ep;
-  ep.perm = perm;
-  ep.topk_w = topk_w;
-  ep.k = k;
-  if (k == 1) {
-    ep.y = y;
-    ep.mode = kCombineStore;
-  } else if (k == 2) {
-    ep.y = y;
-    ep.mode = kCombineAtomic;
-  } else {
-    ep.y = slots;
-    ep.mode = kCombineSlots;
-  }
-  if (p == MM_PATH_TENSOR) {
-    e = counted_launch(MM_KERNEL_GATEUP, st, [&] { return launch_gateup_tc(xp, rows, H, I, g, Wg, Wu, h, 0, hdr, st); });
-    if (e != cudaSuccess) return cuda_fail(e, "gateup_tc");
-    e = counted_launch(MM_KERNEL_DOWN, st, [&] { return launch_down_tc(h, rows, H, I, g, Wd, ep, hdr, st); });
-    if (e != cudaSuccess) return cuda_fail(e, "down_tc");
-  } else {
-    e = counted_launch(MM_KERNEL_GATEUP, st, [&] { return launch_gateup_simt(dtype, xp, rows, H, I, g, Wg, Wu, h, st); });
-    if (e != cudaSuccess) return cuda_fail(e, "gateup_simt");
-    e = counted_launch(MM_KERNEL_DOWN, st, [&] { return launch_down_simt(dtype, h, rows, H, I, g, Wd, ep, st); });
-    if (e != cudaSuccess) return cuda_fail(e, "down_simt");
-  }
-  if (k >= 3) {
-    e = counted_launch(MM_KERNEL_COMBINE, st, [&] { return launch_combine_ordered(dtype, slots, topk_idx, T, H, k, y, st); });
-    if (e != cudaSuccess) return cuda_fail(e, "combine");
+  // gate/up over all k*E (slot, expert) groups at once
+  GroupRows gu{offsets, k * E, 0, E};
+  if (p == MM_PATH_TENSOR)
+    e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
+      return launch_gateup_tc(xp, rows, H, I, gu, Wg, Wu, h, hdr, st);
+    });
+  else
+    e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
+      return launch_gateup_simt(dtype, xp, rows, H, I, gu, Wg, Wu, h, st);
+    });
+  if (e != cudaSuccess) return cuda_fail(e, "gateup");
+  // down: one phase per slot; the k contributions of a token are summed in
+  // fp32 in slot order and rounded once
+  for (int s = 0; s < k; ++s) {
+    GroupRows gd{offsets + static_cast<size_t>(s) * E, E, 0, E};
+    DownEpilogue ep{y, acc32, perm, topk_w, k,
+                    k == 1 ? kCombineStore
+                           : (s == 0 ? kCombineFirst : (s == k - 1 ? kCombineLast : kCombineAccum))};
+    if (p == MM_PATH_TENSOR)
+      e = counted_launch(MM_KERNEL_DOWN, st, [&] {
+        return launch_down_tc(h, rows, H, I, gd, Wd, ep, hdr, st);
+      });
+    else
+      e = counted_launch(MM_KERNEL_DOWN, st, [&] {
+        return launch_down_simt(dtype, h, rows, H, I, gd, Wd, ep, st);
+      });
+    if (e != cudaSuccess) return cuda_fail(e, "down");
   }
   return MM_OK;
 }
@@ -313,9 +323,9 @@ int mm_moe_forward(const void* x, const void* Wr, const void* const* Wg, const v
                            topk_w, aux_loss, workspace, workspace_bytes, stream, MM_PATH_AUTO);
 }
 
-size_t mm_moe_route_workspace_bytes(int64_t T, int E) {
-  if (T < 1 || E < 1 || E > MM_MAX_EXPERTS) return 0;
-  return route_layout(T, E).total;
+size_t mm_moe_route_workspace_bytes(int64_t T, int E, int k) {
+  if (T < 1 || E < 1 || E > MM_MAX_EXPERTS || k < 1 || k > E || k > MM_MAX_TOPK) return 0;
+  return route_layout(T, E, k).total;
 }
 
 int mm_moe_route(const void* x, const void* Wr, int64_t T, int H, int E, int k, float coef,
@@ -326,7 +336,7 @@ int mm_moe_route(const void* x, const void* Wr, int64_t T, int H, int E, int k, 
   if (rc != MM_OK) return rc;
   if (expert_counts && (reinterpret_cast<uintptr_t>(expert_counts) & 3u)) return MM_ERR_INVALID_ARG;
   if (!workspace || !aligned16(workspace)) return MM_ERR_WORKSPACE;
-  const RouteLayout L = route_layout(T, E);
+  const RouteLayout L = route_layout(T, E, k);
   if (workspace_bytes < L.total) return MM_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int32_t* blk_cnt = reinterpret_cast<int32_t*>(ws_at(workspace, L.blk_cnt));
@@ -336,18 +346,18 @@ int mm_moe_route(const void* x, const void* Wr, int64_t T, int H, int E, int k, 
                          blk_prob, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "router");
-  e = counted_launch(MM_KERNEL_DISPATCH, st, [&] {
-    return launch_route_finalize(E, route_blocks(T), T, coef, blk_cnt, blk_prob, nullptr, nullptr,
-                                 aux_loss, expert_counts, st);
+  e = counted_launch(MM_KERNEL_SCAN, st, [&] {
+    return launch_route_scan(E, k, T, coef, blk_cnt, blk_prob, nullptr, nullptr, expert_counts,
+                             aux_loss, st);
   });
-  if (e != cudaSuccess) return cuda_fail(e, "route_finalize");
+  if (e != cudaSuccess) return cuda_fail(e, "route_scan");
   return MM_OK;
 }
 
 uint64_t mm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int mm_profile_start(int kernel_id, int max_launches) {
-  if (kernel_id < MM_KERNEL_ROUTER || kernel_id > MM_KERNEL_COMBINE) return MM_ERR_INVALID_ARG;
+  if (kernel_id < MM_KERNEL_ROUTER || kernel_id > MM_KERNEL_DOWN) return MM_ERR_INVALID_ARG;
   if (max_launches < 1 || max_launches > 100000) return MM_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_prof.mu);
   g_prof.kernel = kernel_id;

@@ -50,39 +50,42 @@ struct DownParams {
 };
 
 struct TileInfo {
-  int e, row0, rows, n0;
+  int g, w, row0, rows, n0;   // group, weight index, first row, valid rows, first column
 };
 
 // Tile t of the grouped problem: groups in order, within a group m-blocks of
-// 128 rows, n-blocks fastest.
-template <int MAXE>
-__device__ __forceinline__ TileInfo decode_tile(int t, const int* s_off, const int* s_tstart, int E,
-                                                int n_tiles, int BN) {
-  int e = 0;
-  while (e + 1 < E && t >= s_tstart[e + 1]) ++e;
-  const int local = t - s_tstart[e];
+// 128 rows, n-blocks fastest.  Binary search over the groups' first tiles.
+__device__ __forceinline__ TileInfo decode_tile(int t, const int* s_off, const int* s_tstart, int G,
+                                                int n_weights, int n_tiles, int BN) {
+  int lo = 0, hi = G - 1;            // last group with s_tstart[g] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_tstart[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int g = lo;
+  const int local = t - s_tstart[g];
   const int mb = local / n_tiles, nb = local - mb * n_tiles;
   TileInfo ti;
-  ti.e = e;
-  ti.row0 = s_off[e] + mb * kTcBM;
-  ti.rows = min(kTcBM, s_off[e + 1] - ti.row0);
+  ti.g = g;
+  ti.w = g % n_weights;
+  ti.row0 = s_off[g] + mb * kTcBM;
+  ti.rows = min(kTcBM, s_off[g + 1] - ti.row0);
   ti.n0 = nb * BN;
   return ti;
 }
 
-template <int MAXE>
-__device__ __forceinline__ void build_schedule(const GroupRows& g, int n_tiles, int* s_off,
+__device__ __forceinline__ void build_schedule(const GroupRows& gr, int n_tiles, int* s_off,
                                                int* s_tstart) {
   int run = 0;
-  for (int e = 0; e < g.E; ++e) {
-    const int o0 = g.offsets ? g.offsets[e] : 0;
-    const int o1 = g.offsets ? g.offsets[e + 1] : g.dense_rows;
-    s_off[e] = o0;
-    s_tstart[e] = run;
+  for (int g = 0; g < gr.G; ++g) {
+    const int o0 = gr.offsets ? gr.offsets[g] : 0;
+    const int o1 = gr.offsets ? gr.offsets[g + 1] : gr.dense_rows;
+    s_off[g] = o0;
+    s_tstart[g] = run;
     run += ((o1 - o0 + kTcBM - 1) / kTcBM) * n_tiles;
   }
-  s_off[g.E] = g.offsets ? g.offsets[g.E] : g.dense_rows;
-  s_tstart[g.E] = run;
+  s_off[gr.G] = gr.offsets ? gr.offsets[gr.G] : gr.dense_rows;
+  s_tstart[gr.G] = run;
 }
 
 __device__ __forceinline__ uint8_t* align1024(unsigned char* p) {
@@ -113,7 +116,7 @@ gateup_tc_kernel(const __grid_constant__ UpParams<MAXE> P, const GroupRows g, co
   uint64_t* drained = tempty + 2;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int s_off[MAXE + 1], s_tstart[MAXE + 1];
+  __shared__ int s_off[kMaxGroups + 1], s_tstart[kMaxGroups + 1];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = (I + kUpBN - 1) / kUpBN;
@@ -131,7 +134,7 @@ gateup_tc_kernel(const __grid_constant__ UpParams<MAXE> P, const GroupRows g, co
     mbar_init(drained, 1);
     fence_mbar_init();
     s_abort = 0;
-    build_schedule<MAXE>(g, n_tiles, s_off, s_tstart);
+    build_schedule(g, n_tiles, s_off, s_tstart);
   }
   if (warp == 4 && lane == 0) tma_prefetch_desc(&P.a);
   if (warp == 5) {
@@ -142,7 +145,7 @@ gateup_tc_kernel(const __grid_constant__ UpParams<MAXE> P, const GroupRows g, co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const int total = s_tstart[g.E];
+  const int total = s_tstart[g.G];
   volatile int* abort = &s_abort;
 
   if (warp == 4) {
@@ -151,15 +154,15 @@ gateup_tc_kernel(const __grid_constant__ UpParams<MAXE> P, const GroupRows g, co
       int it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileInfo ti = decode_tile<MAXE>(tile, s_off, s_tstart, g.E, n_tiles, kUpBN);
+        const TileInfo ti = decode_tile(tile, s_off, s_tstart, g.G, g.n_weights, n_tiles, kUpBN);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kUpStages;
           const uint32_t ph = (it / kUpStages) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, abort, hdr, 1)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[s], kUpAStage + kUpBStage);
           tma_load_2d(sA + s * kUpAStage, &P.a, &full[s], kb * kTcBK, ti.row0);
-          tma_load_2d(sB + s * kUpBStage, &P.wg[ti.e], &full[s], kb * kTcBK, ti.n0);
-          tma_load_2d(sB + s * kUpBStage + kUpBStage / 2, &P.wu[ti.e], &full[s], kb * kTcBK,
+          tma_load_2d(sB + s * kUpBStage, &P.wg[ti.w], &full[s], kb * kTcBK, ti.n0);
+          tma_load_2d(sB + s * kUpBStage + kUpBStage / 2, &P.wu[ti.w], &full[s], kb * kTcBK,
                       ti.n0);
         }
       }
@@ -211,7 +214,7 @@ gateup_tc_kernel(const __grid_constant__ UpParams<MAXE> P, const GroupRows g, co
     const int row = warp * 32 + lane;
     int local = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
-      const TileInfo ti = decode_tile<MAXE>(tile, s_off, s_tstart, g.E, n_tiles, kUpBN);
+      const TileInfo ti = decode_tile(tile, s_off, s_tstart, g.G, g.n_weights, n_tiles, kUpBN);
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       if (!warp_wait(&tfull[acc], aph, abort, hdr, 6)) break;
@@ -269,7 +272,7 @@ down_tc_kernel(const __grid_constant__ DownParams<MAXE> P, const GroupRows g, co
   uint64_t* drained = tempty + 2;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int s_off[MAXE + 1], s_tstart[MAXE + 1];
+  __shared__ int s_off[kMaxGroups + 1], s_tstart[kMaxGroups + 1];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = (H + kDownBN - 1) / kDownBN;
@@ -287,7 +290,7 @@ down_tc_kernel(const __grid_constant__ DownParams<MAXE> P, const GroupRows g, co
     mbar_init(drained, 1);
     fence_mbar_init();
     s_abort = 0;
-    build_schedule<MAXE>(g, n_tiles, s_off, s_tstart);
+    build_schedule(g, n_tiles, s_off, s_tstart);
   }
   if (warp == 4 && lane == 0) tma_prefetch_desc(&P.a);
   if (warp == 5) {
@@ -298,7 +301,7 @@ down_tc_kernel(const __grid_constant__ DownParams<MAXE> P, const GroupRows g, co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const int total = s_tstart[g.E];
+  const int total = s_tstart[g.G];
   volatile int* abort = &s_abort;
 
   if (warp == 4) {
@@ -306,14 +309,14 @@ down_tc_kernel(const __grid_constant__ DownParams<MAXE> P, const GroupRows g, co
       int it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const TileInfo ti = decode_tile<MAXE>(tile, s_off, s_tstart, g.E, n_tiles, kDownBN);
+        const TileInfo ti = decode_tile(tile, s_off, s_tstart, g.G, g.n_weights, n_tiles, kDownBN);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kDnStages;
           const uint32_t ph = (it / kDnStages) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, abort, hdr, 11)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[s], kDnAStage + kDnBStage);
           tma_load_2d(sA + s * kDnAStage, &P.a, &full[s], kb * kTcBK, ti.row0);
-          tma_load_2d(sB + s * kDnBStage, &P.wd[ti.e], &full[s], kb * kTcBK, ti.n0);
+          tma_load_2d(sB + s * kDnBStage, &P.wd[ti.w], &full[s], kb * kTcBK, ti.n0);
         }
       }
       if (!ok) {
@@ -360,24 +363,25 @@ down_tc_kernel(const __grid_constant__ DownParams<MAXE> P, const GroupRows g, co
     const int row = warp * 32 + lane;
     int local = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
-      const TileInfo ti = decode_tile<MAXE>(tile, s_off, s_tstart, g.E, n_tiles, kDownBN);
+      const TileInfo ti = decode_tile(tile, s_off, s_tstart, g.G, g.n_weights, n_tiles, kDownBN);
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       // per-row routing info is read before the accumulator is ready
       const bool valid = row < ti.rows;
-      int64_t out_row = 0;
+      int64_t tok = 0;
       float alpha = 1.0f;
       if (valid) {
         const int pos = ti.row0 + row;
         if (ep.perm != nullptr) {
           const int a = ep.perm[pos];
           alpha = ep.topk_w != nullptr ? ep.topk_w[a] : 1.0f;
-          out_row = (ep.mode == kCombineSlots) ? a : a / ep.k;
+          tok = a / ep.k;
         } else {
-          out_row = pos;
+          tok = pos;
         }
       }
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(ep.y) + out_row * H + ti.n0;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(ep.y) + tok * H + ti.n0;
+      float* acc32 = ep.acc32 + tok * H + ti.n0;
       if (!warp_wait(&tfull[acc], aph, abort, hdr, 16)) break;
       tc_fence_after();
       const uint32_t tb = tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * kDnAccStride;
@@ -387,21 +391,35 @@ down_tc_kernel(const __grid_constant__ DownParams<MAXE> P, const GroupRows g, co
         tmem_ld_32x32b_x32(tb + c * 32, r);
         tmem_ld_wait();
         if (valid && ti.n0 + c * 32 < H) {
-          uint32_t pk[16];
+          float v[32];
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            pk[j] = pack_bf16x2(alpha * __uint_as_float(r[2 * j]),
-                                alpha * __uint_as_float(r[2 * j + 1]));
-          if (ep.mode == kCombineAtomic) {
+          for (int j = 0; j < 32; ++j) v[j] = alpha * __uint_as_float(r[j]);
+          float4* a4 = reinterpret_cast<float4*>(acc32 + c * 32);
+          if (ep.mode == kCombineFirst) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              red_add_bf16x8(dst + c * 32 + q * 8, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
-                             pk[4 * q + 3]);
+            for (int q = 0; q < 8; ++q)
+              a4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
           } else {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+            if (ep.mode != kCombineStore) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+              for (int q = 0; q < 8; ++q) {
+                const float4 o = a4[q];
+                v[4 * q] += o.x; v[4 * q + 1] += o.y; v[4 * q + 2] += o.z; v[4 * q + 3] += o.w;
+              }
+            }
+            if (ep.mode == kCombineAccum) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                a4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            } else {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                d4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]),
+                                   pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                   pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                                   pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+            }
           }
         }
       }
@@ -478,7 +496,7 @@ static int grid_for(int64_t a_rows, const GroupRows& g, int n_tiles) {
   if (g.offsets == nullptr)
     tiles = ((g.dense_rows + kTcBM - 1) / kTcBM) * static_cast<int64_t>(n_tiles);
   else
-    tiles = ((a_rows + kTcBM - 1) / kTcBM + g.E) * static_cast<int64_t>(n_tiles);
+    tiles = ((a_rows + kTcBM - 1) / kTcBM + g.G) * static_cast<int64_t>(n_tiles);
   const int sms = num_sms();
   return static_cast<int>(tiles < sms ? (tiles > 0 ? tiles : 1) : sms);
 }
@@ -490,7 +508,7 @@ static cudaError_t gateup_impl(const void* A, int64_t a_rows, int H, int I, cons
   UpParams<MAXE> p;
   memset(&p, 0, sizeof(p));
   if (!make_map_bf16(&p.a, A, H, a_rows, kTcBM)) return cudaErrorInvalidValue;
-  for (int e = 0; e < g.E; ++e) {
+  for (int e = 0; e < g.n_weights; ++e) {
     if (!make_map_bf16(&p.wg[e], Wg[e], H, I, kUpBN)) return cudaErrorInvalidValue;
     if (!make_map_bf16(&p.wu[e], Wu[e], H, I, kUpBN)) return cudaErrorInvalidValue;
   }
@@ -510,7 +528,7 @@ static cudaError_t down_impl(const void* h, int64_t a_rows, int H, int I, const 
   DownParams<MAXE> p;
   memset(&p, 0, sizeof(p));
   if (!make_map_bf16(&p.a, h, I, a_rows, kTcBM)) return cudaErrorInvalidValue;
-  for (int e = 0; e < g.E; ++e)
+  for (int e = 0; e < g.n_weights; ++e)
     if (!make_map_bf16(&p.wd[e], Wd[e], I, H, kDownBN)) return cudaErrorInvalidValue;
   auto fn = down_tc_kernel<MAXE>;
   cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDnSmem);
@@ -522,15 +540,15 @@ static cudaError_t down_impl(const void* h, int64_t a_rows, int H, int I, const 
 
 cudaError_t launch_gateup_tc(const void* A, int64_t a_rows, int H, int I, const GroupRows& g,
                              const void* const* Wg, const void* const* Wu, void* h_out,
-                             int /*hint*/, WsHeader* hdr, cudaStream_t st) {
-  if (g.E <= 8) return gateup_impl<8>(A, a_rows, H, I, g, Wg, Wu, h_out, hdr, st);
+                             WsHeader* hdr, cudaStream_t st) {
+  if (g.n_weights <= 8) return gateup_impl<8>(A, a_rows, H, I, g, Wg, Wu, h_out, hdr, st);
   return gateup_impl<MM_MAX_EXPERTS>(A, a_rows, H, I, g, Wg, Wu, h_out, hdr, st);
 }
 
 cudaError_t launch_down_tc(const void* h, int64_t a_rows, int H, int I, const GroupRows& g,
                            const void* const* Wd, const DownEpilogue& ep, WsHeader* hdr,
                            cudaStream_t st) {
-  if (g.E <= 8) return down_impl<8>(h, a_rows, H, I, g, Wd, ep, hdr, st);
+  if (g.n_weights <= 8) return down_impl<8>(h, a_rows, H, I, g, Wd, ep, hdr, st);
   return down_impl<MM_MAX_EXPERTS>(h, a_rows, H, I, g, Wd, ep, hdr, st);
 }
 

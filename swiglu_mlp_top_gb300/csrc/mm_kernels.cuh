@@ -12,6 +12,8 @@ constexpr int kDtypeBF16 = MM_DTYPE_BF16;
 // Router / dispatch geometry.
 constexpr int kRouteThreads = 256;          // 8 warps
 constexpr int kRouteTokensPerBlock = 64;    // 8 tokens per warp
+constexpr int kScanThreads = 512;
+constexpr int kMaxGroups = MM_MAX_EXPERTS * MM_MAX_TOPK;     // (slot, expert) groups
 
 // Tensor-core GEMM geometry (tcgen05, cta_group::1).
 constexpr int kTcBM = 128;                  // rows per tile (TMEM lanes)
@@ -20,23 +22,30 @@ constexpr int kUpBN = 128;                  // h columns per gate/up tile (MMA N
 constexpr int kDownBN = 192;                // y columns per down tile
 constexpr int kTcThreads = 192;             // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer
 
-// How the down-projection epilogue writes its rows.
+// How the down-projection epilogue writes its rows.  With k >= 2 the
+// contributions of a token are summed in fp32 in slot order, one slot per
+// launch (phase): the first phase stores, middle phases add, the last phase
+// adds and rounds once to y's dtype.  No atomics; the result is deterministic.
 enum CombineMode : int {
-  kCombineStore = 0,    // y[token] = alpha * acc            (dense, k = 1)
-  kCombineAtomic = 1,   // y[token] += alpha * acc  (y zeroed first; k = 2: two terms commute)
-  kCombineSlots = 2     // slots[t*k + s] = alpha * acc     (k >= 3: ordered combine afterwards)
+  kCombineStore = 0,    // y[token] = alpha * acc                   (dense, k = 1)
+  kCombineFirst = 1,    // acc32[token] = alpha * acc                (slot 0 of k >= 2)
+  kCombineAccum = 2,    // acc32[token] += alpha * acc               (slots 1 .. k-2)
+  kCombineLast = 3      // y[token] = round(acc32[token] + alpha * acc)   (slot k-1)
 };
 
-// Description of the row groups (experts) of a grouped GEMM.
+// Description of the row groups of a grouped GEMM: group g owns rows
+// [offsets[g], offsets[g+1]) of A and uses weight matrix g % n_weights.
 struct GroupRows {
-  const int32_t* offsets;   // device [E+1] row offsets, or nullptr: one group of dense_rows rows
-  int E;
+  const int32_t* offsets;   // device [G+1], or nullptr: one group of dense_rows rows
+  int G;
   int dense_rows;
+  int n_weights;
 };
 
 // Epilogue inputs of the down projection.
 struct DownEpilogue {
-  void* y;                  // [T, H] (store / atomic) or slots [T*k, H]
+  void* y;                  // [T, H], x's dtype
+  float* acc32;             // [T, H] fp32 running sum (k >= 2), may alias y for fp32
   const int32_t* perm;      // row -> t*k + s, or nullptr (row == token, alpha = 1)
   const float* topk_w;      // [T*k] alpha, or nullptr (alpha = 1)
   int k;
@@ -46,21 +55,19 @@ struct DownEpilogue {
 cudaError_t launch_router(int dtype, const void* x, const void* Wr, const float* bias, int64_t T,
                           int H, int E, int k, int32_t* topk_idx, float* topk_w, int32_t* blk_cnt,
                           float* blk_prob, cudaStream_t st);
-cudaError_t launch_route_finalize(int E, int nblk, int64_t T, float coef, const int32_t* blk_cnt,
-                                  const float* blk_prob, int32_t* offsets, int32_t* counts,
-                                  float* aux_loss, int32_t* counts_out, cudaStream_t st);
-cudaError_t launch_dispatch(int dtype, const void* x, int64_t T, int H, int E, int k, float coef,
-                            const int32_t* topk_idx, const int32_t* blk_cnt, const float* blk_prob,
-                            int32_t* offsets, int32_t* counts, float* aux_loss, int32_t* perm,
-                            void* Xp, void* y_zero, cudaStream_t st);
-cudaError_t launch_combine_ordered(int dtype, const void* slots, const int32_t* topk_idx, int64_t T,
-                                   int H, int k, void* y, cudaStream_t st);
+size_t router_smem_bytes(int H, int E, int k);
+cudaError_t launch_route_scan(int E, int k, int64_t T, float coef, const int32_t* blk_cnt,
+                              const float* blk_prob, int32_t* blk_base, int32_t* offsets,
+                              int32_t* counts, float* aux_loss, cudaStream_t st);
+cudaError_t launch_dispatch(int dtype, const void* x, int64_t T, int H, int E, int k,
+                            const int32_t* topk_idx, const int32_t* blk_base,
+                            const int32_t* offsets, int32_t* perm, void* Xp, cudaStream_t st);
 
 // Tensor-core grouped GEMMs (bf16).  A is [rows, K] row-major; each group e
 // multiplies its rows by its own weight matrices.
 cudaError_t launch_gateup_tc(const void* A, int64_t a_rows, int H, int I, const GroupRows& g,
                              const void* const* Wg, const void* const* Wu, void* h_out,
-                             int max_groups_tiles_hint, WsHeader* hdr, cudaStream_t st);
+                             WsHeader* hdr, cudaStream_t st);
 cudaError_t launch_down_tc(const void* h, int64_t a_rows, int H, int I, const GroupRows& g,
                            const void* const* Wd, const DownEpilogue& ep, WsHeader* hdr,
                            cudaStream_t st);

@@ -33,42 +33,42 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
   return __float2bfloat16_rn(v);
 }
 
-__device__ __forceinline__ void atomic_add_out(float* p, float v) { atomicAdd(p, v); }
-__device__ __forceinline__ void atomic_add_out(__nv_bfloat16* p, float v) {
-  atomicAdd(p, __float2bfloat16_rn(v));
-}
-
 struct SimtTile {
-  int e, row0, rows, n0;
+  int g, w, row0, rows, n0;
 };
 
 __device__ __forceinline__ void simt_schedule(const GroupRows& g, int n_tiles, int* s_off,
                                               int* s_tstart) {
   if (threadIdx.x == 0) {
     int run = 0;
-    for (int e = 0; e < g.E; ++e) {
-      const int o0 = g.offsets ? g.offsets[e] : 0;
-      const int o1 = g.offsets ? g.offsets[e + 1] : g.dense_rows;
-      s_off[e] = o0;
-      s_tstart[e] = run;
+    for (int q = 0; q < g.G; ++q) {
+      const int o0 = g.offsets ? g.offsets[q] : 0;
+      const int o1 = g.offsets ? g.offsets[q + 1] : g.dense_rows;
+      s_off[q] = o0;
+      s_tstart[q] = run;
       run += ((o1 - o0 + kSimtBM - 1) / kSimtBM) * n_tiles;
     }
-    s_off[g.E] = g.offsets ? g.offsets[g.E] : g.dense_rows;
-    s_tstart[g.E] = run;
+    s_off[g.G] = g.offsets ? g.offsets[g.G] : g.dense_rows;
+    s_tstart[g.G] = run;
   }
   __syncthreads();
 }
 
-__device__ __forceinline__ SimtTile simt_tile(int t, const int* s_off, const int* s_tstart, int E,
-                                              int n_tiles) {
-  int e = 0;
-  while (e + 1 < E && t >= s_tstart[e + 1]) ++e;
-  const int local = t - s_tstart[e];
+__device__ __forceinline__ SimtTile simt_tile(int t, const int* s_off, const int* s_tstart, int G,
+                                              int n_weights, int n_tiles) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_tstart[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int q = lo;
+  const int local = t - s_tstart[q];
   const int mb = local / n_tiles;
   SimtTile st;
-  st.e = e;
-  st.row0 = s_off[e] + mb * kSimtBM;
-  st.rows = min(kSimtBM, s_off[e + 1] - st.row0);
+  st.g = q;
+  st.w = q % n_weights;
+  st.row0 = s_off[q] + mb * kSimtBM;
+  st.rows = min(kSimtBM, s_off[q + 1] - st.row0);
   st.n0 = (local - mb * n_tiles) * kSimtBN;
   return st;
 }
@@ -77,19 +77,19 @@ template <typename T>
 __global__ void __launch_bounds__(kSimtThreads)
 gateup_simt_kernel(const T* __restrict__ A, const GroupRows g, const PtrArray wg, const PtrArray wu,
                    int H, int I, T* __restrict__ hout) {
-  __shared__ int s_off[MM_MAX_EXPERTS + 1], s_tstart[MM_MAX_EXPERTS + 1];
+  __shared__ int s_off[kMaxGroups + 1], s_tstart[kMaxGroups + 1];
   __shared__ float As[kSimtBM][kSimtBK + 1];
   __shared__ float Gs[kSimtBN][kSimtBK + 1];
   __shared__ float Us[kSimtBN][kSimtBK + 1];
   const int n_tiles = (I + kSimtBN - 1) / kSimtBN;
   simt_schedule(g, n_tiles, s_off, s_tstart);
-  const int total = s_tstart[g.E];
+  const int total = s_tstart[g.G];
   const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
 
   for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-    const SimtTile ti = simt_tile(tile, s_off, s_tstart, g.E, n_tiles);
-    const T* Wg = static_cast<const T*>(wg.p[ti.e]);
-    const T* Wu = static_cast<const T*>(wu.p[ti.e]);
+    const SimtTile ti = simt_tile(tile, s_off, s_tstart, g.G, g.n_weights, n_tiles);
+    const T* Wg = static_cast<const T*>(wg.p[ti.w]);
+    const T* Wu = static_cast<const T*>(wu.p[ti.w]);
     float ag[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, au[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
     for (int k0 = 0; k0 < H; k0 += kSimtBK) {
       for (int i = tid; i < kSimtBM * kSimtBK; i += kSimtThreads) {
@@ -131,18 +131,18 @@ template <typename T>
 __global__ void __launch_bounds__(kSimtThreads)
 down_simt_kernel(const T* __restrict__ Hm, const GroupRows g, const PtrArray wd, int H, int I,
                  const DownEpilogue ep) {
-  __shared__ int s_off[MM_MAX_EXPERTS + 1], s_tstart[MM_MAX_EXPERTS + 1];
+  __shared__ int s_off[kMaxGroups + 1], s_tstart[kMaxGroups + 1];
   __shared__ float As[kSimtBM][kSimtBK + 1];
   __shared__ float Ds[kSimtBN][kSimtBK + 1];
   const int n_tiles = (H + kSimtBN - 1) / kSimtBN;
   simt_schedule(g, n_tiles, s_off, s_tstart);
-  const int total = s_tstart[g.E];
+  const int total = s_tstart[g.G];
   const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
   T* y = static_cast<T*>(ep.y);
 
   for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-    const SimtTile ti = simt_tile(tile, s_off, s_tstart, g.E, n_tiles);
-    const T* Wd = static_cast<const T*>(wd.p[ti.e]);
+    const SimtTile ti = simt_tile(tile, s_off, s_tstart, g.G, g.n_weights, n_tiles);
+    const T* Wd = static_cast<const T*>(wd.p[ti.w]);
     float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
     for (int k0 = 0; k0 < I; k0 += kSimtBK) {
       for (int i = tid; i < kSimtBM * kSimtBK; i += kSimtThreads) {
@@ -166,23 +166,28 @@ down_simt_kernel(const T* __restrict__ Hm, const GroupRows g, const PtrArray wd,
       const int r = 2 * ty + i;
       if (r >= ti.rows) continue;
       const int pos = ti.row0 + r;
-      int64_t out_row = pos;
+      int64_t tok = pos;
       float alpha = 1.0f;
       if (ep.perm != nullptr) {
         const int a = ep.perm[pos];
         alpha = ep.topk_w != nullptr ? ep.topk_w[a] : 1.0f;
-        out_row = (ep.mode == kCombineSlots) ? a : a / ep.k;
+        tok = a / ep.k;
       }
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int c = ti.n0 + 2 * tx + j;
         if (c >= H) continue;
-        const float v = alpha * acc[i][j];
-        T* dst = y + out_row * H + c;
-        if (ep.mode == kCombineAtomic)
-          atomic_add_out(dst, v);
+        float v = alpha * acc[i][j];
+        const int64_t o = tok * H + c;
+        if (ep.mode == kCombineFirst) {
+          ep.acc32[o] = v;
+          continue;
+        }
+        if (ep.mode != kCombineStore) v += ep.acc32[o];
+        if (ep.mode == kCombineAccum)
+          ep.acc32[o] = v;
         else
-          *dst = from_f32<T>(v);
+          y[o] = from_f32<T>(v);
       }
     }
   }
@@ -191,7 +196,7 @@ down_simt_kernel(const T* __restrict__ Hm, const GroupRows g, const PtrArray wd,
 static int simt_grid(int64_t a_rows, const GroupRows& g, int n_tiles) {
   int64_t tiles = (g.offsets == nullptr)
                       ? ((g.dense_rows + kSimtBM - 1) / kSimtBM) * static_cast<int64_t>(n_tiles)
-                      : ((a_rows + kSimtBM - 1) / kSimtBM + g.E) * static_cast<int64_t>(n_tiles);
+                      : ((a_rows + kSimtBM - 1) / kSimtBM + g.G) * static_cast<int64_t>(n_tiles);
   const int64_t cap = 8LL * num_sms();
   if (tiles > cap) tiles = cap;
   return static_cast<int>(tiles > 0 ? tiles : 1);
@@ -201,7 +206,7 @@ cudaError_t launch_gateup_simt(int dtype, const void* A, int64_t a_rows, int H, 
                                const GroupRows& g, const void* const* Wg, const void* const* Wu,
                                void* h_out, cudaStream_t st) {
   PtrArray pg, pu;
-  for (int e = 0; e < g.E; ++e) {
+  for (int e = 0; e < g.n_weights; ++e) {
     pg.p[e] = Wg[e];
     pu.p[e] = Wu[e];
   }
@@ -219,7 +224,7 @@ cudaError_t launch_down_simt(int dtype, const void* h, int64_t a_rows, int H, in
                              const GroupRows& g, const void* const* Wd, const DownEpilogue& ep,
                              cudaStream_t st) {
   PtrArray pd;
-  for (int e = 0; e < g.E; ++e) pd.p[e] = Wd[e];
+  for (int e = 0; e < g.n_weights; ++e) pd.p[e] = Wd[e];
   const int grid = simt_grid(a_rows, g, (H + kSimtBN - 1) / kSimtBN);
   if (dtype == kDtypeBF16)
     down_simt_kernel<__nv_bfloat16><<<grid, kSimtThreads, 0, st>>>(
