@@ -80,7 +80,8 @@ const char* mm_last_error(void);
  *   u = Wu x,  g = Wg x,  h = SiLU(g) ⊙ u,  y = Wd h,  SiLU(z) = z·sigmoid(z)
  *
  * x [T,H], Wg/Wu [I,H], Wd [H,I] in; y [T,H] out (overwritten).  g and u
- * never reach memory; h ([T,I], the dtype of x) lives in the workspace.
+ * never reach memory; h ([T,I]) lives in the workspace, in fp16 for bf16
+ * inputs (|h| must stay below 65504) and fp32 for fp32 inputs.
  * Limits: T >= 0 (T = 0 enqueues nothing); H, I >= 1; bf16 tensor and
  * streaming paths need H and I to be multiples of 64.
  * ---------------------------------------------------------------------- */
@@ -170,7 +171,8 @@ typedef enum {
   MM_KERNEL_SCAN = 2,       /* group offsets + aux loss finalisation        */
   MM_KERNEL_DISPATCH = 3,   /* token permute into expert-contiguous rows    */
   MM_KERNEL_GATEUP = 4,     /* gate/up GEMM with the SwiGLU epilogue        */
-  MM_KERNEL_DOWN = 5        /* down GEMM with the alpha-scaled combine      */
+  MM_KERNEL_DOWN = 5,       /* down GEMM with the alpha-scaled combine      */
+  MM_KERNEL_WCONVERT = 6    /* bf16 -> fp16 copy of the down weights        */
 } mm_kernel_id;
 
 /* Number of kernels this library has enqueued since it was loaded. */

@@ -28,12 +28,16 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 // ----------------------------------------------------------------- layouts
 struct MoeLayout {
-  size_t offsets, counts, blk_cnt, blk_base, blk_prob, perm, xp, h, acc32, total;
+  size_t offsets, counts, blk_cnt, blk_base, blk_prob, perm, xp, h, acc32, wd16, total;
 };
+
+// h is stored in fp16 for bf16 inputs (see gemm_tc.cu) and in fp32 for fp32.
+inline size_t h_bytes(int dtype) { return dtype == kDtypeBF16 ? 2 : 4; }
 
 // Workspace of the MoE forward: routing tables, the dispatched rows Xp
 // ([T*k, H], grouped by slot, then expert, then token), h ([T*k, I]) and,
-// for bf16 with k >= 2, the fp32 running sum of y ([T, H]).
+// for bf16, the fp32 running sum of y ([T, H], k >= 2) and fp16 copies of the
+// E down-projection matrices.
 MoeLayout moe_layout(int64_t T, int H, int I, int E, int k, int dtype) {
   MoeLayout L;
   const size_t es = elem_bytes(dtype);
@@ -48,8 +52,9 @@ MoeLayout moe_layout(int64_t T, int H, int I, int E, int k, int dtype) {
   L.blk_prob = off; off += align_up(4 * nblk * E);
   L.perm = off;     off += align_up(4 * rows);
   L.xp = off;       off += align_up(es * rows * H);
-  L.h = off;        off += align_up(es * rows * I);
+  L.h = off;        off += align_up(h_bytes(dtype) * rows * I);
   L.acc32 = off;    if (k >= 2 && dtype == kDtypeBF16) off += align_up(4 * static_cast<size_t>(T) * H);
+  L.wd16 = off;     if (dtype == kDtypeBF16) off += align_up(2 * static_cast<size_t>(E) * H * I);
   L.total = off;
   return L;
 }
@@ -67,8 +72,13 @@ RouteLayout route_layout(int64_t T, int E, int k) {
   return L;
 }
 
-size_t dense_ws_bytes(int64_t T, int I, int dtype) {
-  return sizeof(WsHeader) + align_up(elem_bytes(dtype) * static_cast<size_t>(T) * I);
+// Dense workspace: h [T, I], then (bf16) the fp16 copy of Wd.
+size_t dense_h_bytes(int64_t T, int I, int dtype) {
+  return align_up(h_bytes(dtype) * static_cast<size_t>(T) * I);
+}
+size_t dense_ws_bytes(int64_t T, int H, int I, int dtype) {
+  return sizeof(WsHeader) + dense_h_bytes(T, I, dtype) +
+         (dtype == kDtypeBF16 ? align_up(2 * static_cast<size_t>(H) * I) : 0);
 }
 
 bool valid_dtype(int dtype) { return dtype == kDtypeF32 || dtype == kDtypeBF16; }
@@ -154,7 +164,7 @@ const char* mm_last_error(void) { return g_last_error; }
 
 size_t mm_swiglu_ffn_workspace_bytes(int64_t T, int H, int I, int dtype) {
   if (T < 0 || H < 1 || I < 1 || !valid_dtype(dtype)) return 0;
-  return dense_ws_bytes(T, I, dtype);
+  return dense_ws_bytes(T, H, I, dtype);
 }
 
 int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* Wd, void* y,
@@ -169,7 +179,7 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
   if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) || !aligned16(y))
     return MM_ERR_INVALID_ARG;
   if (!workspace || !aligned16(workspace)) return MM_ERR_WORKSPACE;
-  if (workspace_bytes < dense_ws_bytes(T, I, dtype)) return MM_ERR_WORKSPACE;
+  if (workspace_bytes < dense_ws_bytes(T, H, I, dtype)) return MM_ERR_WORKSPACE;
   const int p = resolve_path(path, dtype, T);
   if ((p == MM_PATH_TENSOR || p == MM_PATH_STREAM) &&
       (dtype != kDtypeBF16 || !tensor_shape_ok(H, I)))
@@ -186,9 +196,15 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
   const void* wd[1] = {Wd};
   cudaError_t e;
   if (p == MM_PATH_TENSOR) {
+    void* wd16 = ws_at(workspace, sizeof(WsHeader) + dense_h_bytes(T, I, dtype));
+    const void* wd16p[1] = {wd16};
+    e = counted_launch(MM_KERNEL_WCONVERT, st, [&] {
+      return launch_convert_bf16_to_f16(wd, 1, static_cast<int64_t>(H) * I, wd16, st);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "wd convert");
     e = counted_launch(MM_KERNEL_GATEUP, st, [&] { return launch_gateup_tc(x, T, H, I, g, wg, wu, h, hdr, st); });
     if (e != cudaSuccess) return cuda_fail(e, "gateup_tc");
-    e = counted_launch(MM_KERNEL_DOWN, st, [&] { return launch_down_tc(h, T, H, I, g, wd, ep, hdr, st); });
+    e = counted_launch(MM_KERNEL_DOWN, st, [&] { return launch_down_tc(h, T, H, I, g, wd16p, ep, hdr, st); });
     if (e != cudaSuccess) return cuda_fail(e, "down_tc");
   } else {
     e = counted_launch(MM_KERNEL_GATEUP, st, [&] { return launch_gateup_simt(dtype, x, T, H, I, g, wg, wu, h, st); });
@@ -284,6 +300,15 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
   if (e != cudaSuccess) return cuda_fail(e, "dispatch");
 
   const int64_t rows = T * k;
+  const void* wd16p[MM_MAX_EXPERTS];
+  if (p == MM_PATH_TENSOR) {
+    char* wd16 = ws_at(workspace, L.wd16);
+    for (int q = 0; q < E; ++q) wd16p[q] = wd16 + static_cast<size_t>(q) * H * I * 2;
+    e = counted_launch(MM_KERNEL_WCONVERT, st, [&] {
+      return launch_convert_bf16_to_f16(Wd, E, static_cast<int64_t>(H) * I, wd16, st);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "wd convert");
+  }
   // gate/up over all k*E (slot, expert) groups at once
   GroupRows gu{offsets, k * E, 0, E};
   if (p == MM_PATH_TENSOR)
@@ -304,7 +329,7 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
                            : (s == 0 ? kCombineFirst : (s == k - 1 ? kCombineLast : kCombineAccum))};
     if (p == MM_PATH_TENSOR)
       e = counted_launch(MM_KERNEL_DOWN, st, [&] {
-        return launch_down_tc(h, rows, H, I, gd, Wd, ep, hdr, st);
+        return launch_down_tc(h, rows, H, I, gd, wd16p, ep, hdr, st);
       });
     else
       e = counted_launch(MM_KERNEL_DOWN, st, [&] {
@@ -357,7 +382,7 @@ int mm_moe_route(const void* x, const void* Wr, int64_t T, int H, int E, int k, 
 uint64_t mm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int mm_profile_start(int kernel_id, int max_launches) {
-  if (kernel_id < MM_KERNEL_ROUTER || kernel_id > MM_KERNEL_DOWN) return MM_ERR_INVALID_ARG;
+  if (kernel_id < MM_KERNEL_ROUTER || kernel_id > MM_KERNEL_WCONVERT) return MM_ERR_INVALID_ARG;
   if (max_launches < 1 || max_launches > 100000) return MM_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_prof.mu);
   g_prof.kernel = kernel_id;

@@ -5,14 +5,17 @@
 //   warp 5     MMA issuer (one elected lane); owns the TMEM allocation
 // Two TMEM accumulators let the epilogue of tile i overlap the MMAs of i+1.
 //
-// gate/up:  for the rows of group e:  G = A Wg_e^T, U = A Wu_e^T  (one UMMA
-//           with N = 256: Wg rows n0..n0+127 stacked over Wu rows n0..n0+127),
-//           epilogue h = SiLU(G) ⊙ U -> bf16.  G and U stay in TMEM.
+// gate/up:  for the rows of group e:  G = A Wg_e^T, U = A Wu_e^T  (bf16; one
+//           UMMA with N = 256: Wg rows n0..n0+127 stacked over Wu rows
+//           n0..n0+127), epilogue h = SiLU(G) ⊙ U -> fp16.  G and U stay in TMEM.
 //           (MiniMind lesson 13 "FFN 与 MoE" §0/§1.2 equations; minimind3.com
-//           chapter 4 §4.2.)
-// down:     Y = h Wd_e^T; the epilogue scales each row by its routing weight
-//           alpha and writes / accumulates it into y at the row's token
-//           (lesson 13 step 5: expert output times weight, index_add_ into y).
+//           chapter 4 §4.2.)  h is stored in fp16 (11-bit significand): bf16
+//           storage of h alone added ~0.005 RMS-relative max error on top of
+//           the unavoidable bf16 rounding of y.
+// down:     Y = h Wd_e^T (fp16 x fp16, Wd converted from bf16 exactly); the
+//           epilogue scales each row by its routing weight alpha and writes /
+//           accumulates it into y at the row's token (lesson 13 step 5:
+//           expert output times weight, index_add_ into y).
 #include <mutex>
 #include <map>
 #include <tuple>
@@ -103,7 +106,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 template <int MAXE>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gateup_tc_kernel(const __grid_constant__ UpParams<MAXE> P, const GroupRows g, const int H,
-                 const int I, __nv_bfloat16* __restrict__ hout, WsHeader* hdr) {
+                 const int I, __half* __restrict__ hout, WsHeader* hdr) {
   extern __shared__ unsigned char smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
@@ -221,7 +224,7 @@ gateup_tc_kernel(const __grid_constant__ UpParams<MAXE> P, const GroupRows g, co
       tc_fence_after();
       const uint32_t tb = tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * kUpAccStride;
       const bool valid = row < ti.rows;
-      __nv_bfloat16* dst = hout + static_cast<int64_t>(ti.row0 + (valid ? row : 0)) * I + ti.n0;
+      __half* dst = hout + static_cast<int64_t>(ti.row0 + (valid ? row : 0)) * I + ti.n0;
 #pragma unroll 1
       for (int c = 0; c < kUpBN / 32; ++c) {
         uint32_t gr[32], ur[32];
@@ -236,7 +239,7 @@ gateup_tc_kernel(const __grid_constant__ UpParams<MAXE> P, const GroupRows g, co
             const float u0 = __uint_as_float(ur[2 * j]), u1 = __uint_as_float(ur[2 * j + 1]);
             const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
             const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
-            pk[j] = pack_bf16x2(h0, h1);
+            pk[j] = pack_f16x2(h0, h1);
           }
           uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
@@ -330,7 +333,7 @@ down_tc_kernel(const __grid_constant__ DownParams<MAXE> P, const GroupRows g, co
     __syncwarp();
   } else if (warp == 5) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kTcBM, kDownBN);
+      constexpr uint32_t idesc = idesc_f16_f32(kTcBM, kDownBN);
       int it = 0, local = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++local) {
@@ -454,14 +457,15 @@ static EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// bf16 row-major [outer, inner] matrix, box = 64 (inner) x box_rows (outer),
-// 128-byte swizzle, zero fill outside the matrix.  Cached by (ptr, shape, box).
-static bool make_map_bf16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
-                          uint32_t box_rows) {
-  using Key = std::tuple<uintptr_t, uint64_t, uint64_t, uint32_t>;
+// 16-bit row-major [outer, inner] matrix (bf16 or fp16), box = 64 (inner) x
+// box_rows (outer), 128-byte swizzle, zero fill outside the matrix.  Cached by
+// (ptr, shape, box, type).
+static bool make_map_16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
+                        uint32_t box_rows, bool is_f16) {
+  using Key = std::tuple<uintptr_t, uint64_t, uint64_t, uint32_t, bool>;
   static std::mutex mu;
   static std::map<Key, CUtensorMap> cache;
-  const Key key{reinterpret_cast<uintptr_t>(ptr), inner, outer, box_rows};
+  const Key key{reinterpret_cast<uintptr_t>(ptr), inner, outer, box_rows, is_f16};
   std::lock_guard<std::mutex> lock(mu);
   auto itc = cache.find(key);
   if (itc != cache.end()) {
@@ -474,10 +478,10 @@ static bool make_map_bf16(CUtensorMap* out, const void* ptr, uint64_t inner, uin
   cuuint64_t strides[1] = {inner * 2};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBK), box_rows};
   cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
-                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = enc(out, is_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         2, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   if (cache.size() > 4096) cache.clear();
   cache.emplace(key, *out);
@@ -507,17 +511,17 @@ static cudaError_t gateup_impl(const void* A, int64_t a_rows, int H, int I, cons
                                WsHeader* hdr, cudaStream_t st) {
   UpParams<MAXE> p;
   memset(&p, 0, sizeof(p));
-  if (!make_map_bf16(&p.a, A, H, a_rows, kTcBM)) return cudaErrorInvalidValue;
+  if (!make_map_16(&p.a, A, H, a_rows, kTcBM, false)) return cudaErrorInvalidValue;
   for (int e = 0; e < g.n_weights; ++e) {
-    if (!make_map_bf16(&p.wg[e], Wg[e], H, I, kUpBN)) return cudaErrorInvalidValue;
-    if (!make_map_bf16(&p.wu[e], Wu[e], H, I, kUpBN)) return cudaErrorInvalidValue;
+    if (!make_map_16(&p.wg[e], Wg[e], H, I, kUpBN, false)) return cudaErrorInvalidValue;
+    if (!make_map_16(&p.wu[e], Wu[e], H, I, kUpBN, false)) return cudaErrorInvalidValue;
   }
   auto fn = gateup_tc_kernel<MAXE>;
   cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kUpSmem);
   if (err != cudaSuccess) return err;
   const int n_tiles = (I + kUpBN - 1) / kUpBN;
   fn<<<grid_for(a_rows, g, n_tiles), kTcThreads, kUpSmem, st>>>(
-      p, g, H, I, static_cast<__nv_bfloat16*>(h_out), hdr);
+      p, g, H, I, static_cast<__half*>(h_out), hdr);
   return cudaGetLastError();
 }
 
@@ -527,9 +531,9 @@ static cudaError_t down_impl(const void* h, int64_t a_rows, int H, int I, const 
                              cudaStream_t st) {
   DownParams<MAXE> p;
   memset(&p, 0, sizeof(p));
-  if (!make_map_bf16(&p.a, h, I, a_rows, kTcBM)) return cudaErrorInvalidValue;
+  if (!make_map_16(&p.a, h, I, a_rows, kTcBM, true)) return cudaErrorInvalidValue;
   for (int e = 0; e < g.n_weights; ++e)
-    if (!make_map_bf16(&p.wd[e], Wd[e], I, H, kDownBN)) return cudaErrorInvalidValue;
+    if (!make_map_16(&p.wd[e], Wd[e], I, H, kDownBN, true)) return cudaErrorInvalidValue;
   auto fn = down_tc_kernel<MAXE>;
   cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDnSmem);
   if (err != cudaSuccess) return err;

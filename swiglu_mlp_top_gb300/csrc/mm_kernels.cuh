@@ -63,8 +63,9 @@ cudaError_t launch_dispatch(int dtype, const void* x, int64_t T, int H, int E, i
                             const int32_t* topk_idx, const int32_t* blk_base,
                             const int32_t* offsets, int32_t* perm, void* Xp, cudaStream_t st);
 
-// Tensor-core grouped GEMMs (bf16).  A is [rows, K] row-major; each group e
-// multiplies its rows by its own weight matrices.
+// Tensor-core grouped GEMMs.  A is [rows, K] row-major; each group multiplies
+// its rows by its own weight matrices.  gate/up: bf16 A and weights, fp16 h
+// out.  down: fp16 h and fp16 Wd.
 cudaError_t launch_gateup_tc(const void* A, int64_t a_rows, int H, int I, const GroupRows& g,
                              const void* const* Wg, const void* const* Wu, void* h_out,
                              WsHeader* hdr, cudaStream_t st);
@@ -79,6 +80,11 @@ cudaError_t launch_gateup_simt(int dtype, const void* A, int64_t a_rows, int H, 
 cudaError_t launch_down_simt(int dtype, const void* h, int64_t a_rows, int H, int I,
                              const GroupRows& g, const void* const* Wd, const DownEpilogue& ep,
                              cudaStream_t st);
+
+// bf16 -> fp16 copy of n_mat matrices of per_matrix elements (multiple of 8)
+// into one contiguous destination.
+cudaError_t launch_convert_bf16_to_f16(const void* const* src, int n_mat, int64_t per_matrix,
+                                       void* dst, cudaStream_t st);
 
 cudaError_t launch_watchdog_selftest(WsHeader* hdr, uint32_t limit_us, cudaStream_t st);
 

@@ -24,8 +24,12 @@ template <>
 __device__ __forceinline__ float ld_f32<__nv_bfloat16>(const __nv_bfloat16* p) {
   return __bfloat162float(*p);
 }
+template <>
+__device__ __forceinline__ float ld_f32<__half>(const __half* p) { return __half2float(*p); }
 template <typename T>
 __device__ __forceinline__ T from_f32(float v);
+template <>
+__device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
 template <>
 __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <>
@@ -73,10 +77,10 @@ __device__ __forceinline__ SimtTile simt_tile(int t, const int* s_off, const int
   return st;
 }
 
-template <typename T>
+template <typename T, typename Th>
 __global__ void __launch_bounds__(kSimtThreads)
 gateup_simt_kernel(const T* __restrict__ A, const GroupRows g, const PtrArray wg, const PtrArray wu,
-                   int H, int I, T* __restrict__ hout) {
+                   int H, int I, Th* __restrict__ hout) {
   __shared__ int s_off[kMaxGroups + 1], s_tstart[kMaxGroups + 1];
   __shared__ float As[kSimtBM][kSimtBK + 1];
   __shared__ float Gs[kSimtBN][kSimtBK + 1];
@@ -121,15 +125,15 @@ gateup_simt_kernel(const T* __restrict__ A, const GroupRows g, const PtrArray wg
       for (int j = 0; j < 2; ++j) {
         const int c = ti.n0 + 2 * tx + j;
         if (c < I)
-          hout[static_cast<int64_t>(ti.row0 + r) * I + c] = from_f32<T>(silu_f32(ag[i][j]) * au[i][j]);
+          hout[static_cast<int64_t>(ti.row0 + r) * I + c] = from_f32<Th>(silu_f32(ag[i][j]) * au[i][j]);
       }
     }
   }
 }
 
-template <typename T>
+template <typename T, typename Th>
 __global__ void __launch_bounds__(kSimtThreads)
-down_simt_kernel(const T* __restrict__ Hm, const GroupRows g, const PtrArray wd, int H, int I,
+down_simt_kernel(const Th* __restrict__ Hm, const GroupRows g, const PtrArray wd, int H, int I,
                  const DownEpilogue ep) {
   __shared__ int s_off[kMaxGroups + 1], s_tstart[kMaxGroups + 1];
   __shared__ float As[kSimtBM][kSimtBK + 1];
@@ -212,11 +216,11 @@ cudaError_t launch_gateup_simt(int dtype, const void* A, int64_t a_rows, int H, 
   }
   const int grid = simt_grid(a_rows, g, (I + kSimtBN - 1) / kSimtBN);
   if (dtype == kDtypeBF16)
-    gateup_simt_kernel<__nv_bfloat16><<<grid, kSimtThreads, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(A), g, pg, pu, H, I, static_cast<__nv_bfloat16*>(h_out));
+    gateup_simt_kernel<__nv_bfloat16, __half><<<grid, kSimtThreads, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(A), g, pg, pu, H, I, static_cast<__half*>(h_out));
   else
-    gateup_simt_kernel<float><<<grid, kSimtThreads, 0, st>>>(static_cast<const float*>(A), g, pg,
-                                                              pu, H, I, static_cast<float*>(h_out));
+    gateup_simt_kernel<float, float><<<grid, kSimtThreads, 0, st>>>(
+        static_cast<const float*>(A), g, pg, pu, H, I, static_cast<float*>(h_out));
   return cudaGetLastError();
 }
 
@@ -227,11 +231,48 @@ cudaError_t launch_down_simt(int dtype, const void* h, int64_t a_rows, int H, in
   for (int e = 0; e < g.n_weights; ++e) pd.p[e] = Wd[e];
   const int grid = simt_grid(a_rows, g, (H + kSimtBN - 1) / kSimtBN);
   if (dtype == kDtypeBF16)
-    down_simt_kernel<__nv_bfloat16><<<grid, kSimtThreads, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(h), g, pd, H, I, ep);
+    down_simt_kernel<__nv_bfloat16, __half><<<grid, kSimtThreads, 0, st>>>(
+        static_cast<const __half*>(h), g, pd, H, I, ep);
   else
-    down_simt_kernel<float><<<grid, kSimtThreads, 0, st>>>(static_cast<const float*>(h), g, pd, H,
-                                                            I, ep);
+    down_simt_kernel<float, float><<<grid, kSimtThreads, 0, st>>>(static_cast<const float*>(h), g,
+                                                                   pd, H, I, ep);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ Wd -> fp16
+// Copies each expert's down-projection weights from bf16 to fp16 (exact for
+// |w| >= 2^-14; smaller magnitudes become fp16 subnormals, error <= 2^-25).
+__global__ void convert_bf16_to_f16_kernel(const PtrArray src, __half* __restrict__ dst,
+                                           int64_t per_matrix, int n_mat) {
+  const int64_t nvec = per_matrix / 8;   // per_matrix is a multiple of 8
+  const int64_t total = nvec * n_mat;
+  for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < total;
+       v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int m = static_cast<int>(v / nvec);
+    const int64_t off = (v - m * nvec) * 8;
+    const uint4 raw = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src.p[m]) + off);
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    uint4 out;
+    uint32_t* o = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(b[i]);
+      o[i] = pack_f16x2(f.x, f.y);
+    }
+    *reinterpret_cast<uint4*>(dst + m * per_matrix + off) = out;
+  }
+}
+
+cudaError_t launch_convert_bf16_to_f16(const void* const* src, int n_mat, int64_t per_matrix,
+                                       void* dst, cudaStream_t st) {
+  PtrArray p;
+  for (int m = 0; m < n_mat; ++m) p.p[m] = src[m];
+  const int64_t nvec = per_matrix / 8 * n_mat;
+  int64_t grid = (nvec + 255) / 256;
+  const int64_t cap = 4LL * num_sms();
+  if (grid > cap) grid = cap;
+  convert_bf16_to_f16_kernel<<<static_cast<int>(grid > 0 ? grid : 1), 256, 0, st>>>(
+      p, static_cast<__half*>(dst), per_matrix, n_mat);
   return cudaGetLastError();
 }
 

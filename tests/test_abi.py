@@ -55,7 +55,7 @@ def test_workspace_sizes(lib):
     assert lib.mm_moe_workspace_bytes(T, H, I, E, 9, bf16) == 0         # k > E
     assert lib.mm_moe_workspace_bytes(T, H, I, 65, 2, bf16) == 0        # E > max
     assert lib.mm_swiglu_ffn_workspace_bytes(4096, H, I, bf16) >= 4096 * I * 2
-    assert lib.mm_swiglu_ffn_workspace_bytes(0, H, I, bf16) == 256
+    assert lib.mm_swiglu_ffn_workspace_bytes(0, H, I, bf16) == 256 + H * I * 2   # fp16 Wd copy
     assert lib.mm_moe_route_workspace_bytes(0, 8, 2) == 0
     assert lib.mm_moe_workspace_bytes(T, H, I, 16, 9, bf16) == 0        # k > MM_MAX_TOPK
 
