@@ -133,7 +133,7 @@ def test_dense_empty_input():
 
 
 # ------------------------------------------------------------------ full-size workloads
-def _sample_rows(T, n=256, seed=0):
+def _sample_rows(T, n=2048, seed=0):
     r = np.random.default_rng(seed)
     rows = np.unique(np.concatenate([[0, T - 1], r.choice(T, size=min(n, T), replace=False)]))
     return rows
