@@ -46,116 +46,205 @@ template <>
 __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 // ---------------------------------------------------------------------------
-// Router: one warp per token, kRouteTokensPerBlock tokens per block.
-//   r_e = sum_h x[t,h] Wr[e,h] (+ bias_e)      fp32, lanes split h, xor-tree sum
-//   p = softmax(r)                              fp32, max subtracted
-//   S = k largest p, ties -> lower index        sequential selection
-//   alpha_s = p_S[s] / (sum_S p + 1e-20)
+// Router ([L13] §1.5 equations; chapter 4 §4.3 steps 1-2).  A warp routes
+// TPW = 32 / EP tokens per pass (EP = E rounded up to 8, 16, 32 or 64):
+//   r_{t,e} = sum_h x[t,h] Wr[e,h] (+ bias_e)   fp32; lanes split h into
+//             8-element chunks and hold TPW x EP partial sums, which a
+//             butterfly reduce-scatter (5 shuffle rounds) leaves as one
+//             (token, expert) logit per lane;
+//   p = softmax(r)                              fp32, max subtracted, within
+//                                               the token's lane group;
+//   S = k largest p, equal p -> lower index     k group-wide arg-max rounds;
+//   alpha_s = p_S[s] / (sum_S p + 1e-20).
 // Per block it also records, for every (slot s, expert e) group g = s*E + e,
-// how many of its tokens chose expert e in slot s (blk_cnt[b][g]), and
-// sum_t p_{t,e} over its tokens (blk_prob[b][e]), reduced in a fixed order
-// (token order within a warp, then warp order).
+// how many of its tokens chose e in slot s (blk_cnt[b][g]), and sum_t p_{t,e}
+// over its tokens (blk_prob[b][e]); every sum runs in a fixed order.
 // ---------------------------------------------------------------------------
-template <typename Tin, int MAXE>
+template <typename Tin, int EP>
 __global__ void __launch_bounds__(kRouteThreads)
 router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float* __restrict__ bias,
               int64_t T, int H, int E, int k, int32_t* __restrict__ topk_idx,
               float* __restrict__ topk_w, int32_t* __restrict__ blk_cnt,
               float* __restrict__ blk_prob) {
-  extern __shared__ __align__(16) unsigned char route_smem[];
-  float* w_s = reinterpret_cast<float*>(route_smem);                          // [E][H]
-  int* s_gcnt = reinterpret_cast<int*>(route_smem + sizeof(float) * E * H);   // [k*E]
-  __shared__ float red_p[kRouteThreads / 32][MAXE];
+  constexpr int R = (EP > 32) ? EP / 32 : 1;      // values per lane after the reduction
+  constexpr int NV = 32 * R;                       // partial sums per lane
+  constexpr int TPW = NV / EP;                     // tokens per pass
+  constexpr int GL = (EP < 32) ? EP : 32;          // lanes per token group
+  constexpr int kWarps = kRouteThreads / 32;
+  constexpr int kPerWarp = kRouteTokensPerBlock / kWarps;
+  static_assert(kPerWarp % TPW == 0, "passes cover a warp's tokens");
+
+  extern __shared__ float4 route_smem4[];
+  const int nch = H / 8;                           // 8-element chunks per row
+  float4* w_lo = route_smem4;                      // [E][nch] elements 0..3 of each chunk
+  float4* w_hi = route_smem4 + E * nch;            // [E][nch] elements 4..7
+  int* s_gcnt = reinterpret_cast<int*>(route_smem4 + 2 * E * nch);   // [k*E]
+  __shared__ float red_p[kWarps][EP];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = k * E;
-  for (int i = tid; i < E * H; i += blockDim.x) w_s[i] = to_f32(Wr[i]);
+  for (int i = tid; i < E * nch; i += blockDim.x) {
+    const int e = i / nch, c = i - e * nch;
+    float v[8];
+    load_vec8(Wr + static_cast<int64_t>(e) * H + c * 8, v);
+    w_lo[i] = make_float4(v[0], v[1], v[2], v[3]);
+    w_hi[i] = make_float4(v[4], v[5], v[6], v[7]);
+  }
   for (int i = tid; i < G; i += blockDim.x) s_gcnt[i] = 0;
   __syncthreads();
 
-  constexpr int kWarps = kRouteThreads / 32;
-  constexpr int kPerWarp = kRouteTokensPerBlock / kWarps;
-  // lane e keeps the running probability sum of expert e (and e + 32)
-  float psum0 = 0.f, psum1 = 0.f;
+  // (token, expert) pairs this lane owns after the reduction
+  int e_of[R];
+  const int t_loc = (R == 1) ? lane / EP : 0;
+  const int gbase = t_loc * GL;
+#pragma unroll
+  for (int j = 0; j < R; ++j) e_of[j] = (R == 1) ? (lane % EP) : (lane + 32 * j);
+  float bias_v[R];
+#pragma unroll
+  for (int j = 0; j < R; ++j) bias_v[j] = (bias != nullptr && e_of[j] < E) ? bias[e_of[j]] : 0.f;
+  float psum[R];
+#pragma unroll
+  for (int j = 0; j < R; ++j) psum[j] = 0.f;
 
-  for (int j = 0; j < kPerWarp; ++j) {
-    const int64_t t = static_cast<int64_t>(blockIdx.x) * kRouteTokensPerBlock + warp * kPerWarp + j;
-    if (t >= T) break;   // uniform across the warp
-    float acc[MAXE];
+  for (int pass = 0; pass < kPerWarp / TPW; ++pass) {
+    const int64_t tbase = static_cast<int64_t>(blockIdx.x) * kRouteTokensPerBlock +
+                          warp * kPerWarp + pass * TPW;
+    if (tbase >= T) break;   // uniform across the warp
+    float v[NV];
 #pragma unroll
-    for (int e = 0; e < MAXE; ++e) acc[e] = 0.f;
-    const Tin* xr = x + t * H;
-    for (int h = lane * 8; h < H; h += 256) {
-      float xv[8];
-      load_vec8(xr + h, xv);
+    for (int i = 0; i < NV; ++i) v[i] = 0.f;
+    for (int c = lane; c < nch; c += 32) {
+      float xv[TPW][8];
 #pragma unroll
-      for (int e = 0; e < MAXE; ++e) {
-        if (e < E) {
-          const float* w = w_s + e * H + h;
-          float s = acc[e];
+      for (int t = 0; t < TPW; ++t) {
+        if (tbase + t < T) {
+          load_vec8(x + (tbase + t) * H + c * 8, xv[t]);
+        } else {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) s = fmaf(xv[i], w[i], s);
-          acc[e] = s;
+          for (int i = 0; i < 8; ++i) xv[t][i] = 0.f;
         }
       }
-    }
-    float r[MAXE];
-    float m = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < MAXE; ++e) {
-      if (e < E) {
-        r[e] = warp_sum(acc[e]) + (bias != nullptr ? bias[e] : 0.f);
-        m = fmaxf(m, r[e]);
-      }
-    }
-    float z = 0.f;
+      for (int e = 0; e < EP; ++e) {
+        if (e < E) {
+          const float4 a = w_lo[e * nch + c], b = w_hi[e * nch + c];
 #pragma unroll
-    for (int e = 0; e < MAXE; ++e) {
-      if (e < E) {
-        r[e] = expf(r[e] - m);
-        z += r[e];
-      }
-    }
-    float p[MAXE];
-#pragma unroll
-    for (int e = 0; e < MAXE; ++e) p[e] = (e < E) ? r[e] / z : 0.f;
-
-    // top-k by repeated selection; strict '>' keeps the lowest index on ties.
-    // Pass 1 finds sum_S p; pass 2 repeats the same selection and writes the
-    // slots with alpha = p / (sum_S p + 1e-20).
-    float sel_sum = 0.f;
-    for (int pass = 0; pass < 2; ++pass) {
-      uint64_t taken = 0;
-      for (int s = 0; s < k; ++s) {
-        int best = -1;
-        float bp = 0.f;
-#pragma unroll
-        for (int e = 0; e < MAXE; ++e) {
-          if (e < E && !((taken >> e) & 1ull) && (best < 0 || p[e] > bp)) {
-            best = e;
-            bp = p[e];
+          for (int t = 0; t < TPW; ++t) {
+            float s = v[t * EP + e];
+            s = fmaf(xv[t][0], a.x, s); s = fmaf(xv[t][1], a.y, s);
+            s = fmaf(xv[t][2], a.z, s); s = fmaf(xv[t][3], a.w, s);
+            s = fmaf(xv[t][4], b.x, s); s = fmaf(xv[t][5], b.y, s);
+            s = fmaf(xv[t][6], b.z, s); s = fmaf(xv[t][7], b.w, s);
+            v[t * EP + e] = s;
           }
         }
-        taken |= 1ull << best;
-        if (pass == 0) {
-          sel_sum += bp;
-        } else if (lane == 0) {
-          topk_idx[t * k + s] = best;
-          topk_w[t * k + s] = bp / (sel_sum + 1e-20f);
-          atomicAdd(&s_gcnt[s * E + best], 1);
+      }
+    }
+    // butterfly reduce-scatter: after the round with offset o a lane keeps the
+    // half of its values whose index bit o matches its own lane bit; at the
+    // end lane L holds the full sums of pairs L + 32 j
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+          const float lo = v[j * 32 + i], hi = v[j * 32 + i + o];
+          const float send = up ? lo : hi;
+          const float keep = up ? hi : lo;
+          v[j * 32 + i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
         }
       }
     }
+    const int64_t tok = tbase + t_loc;
+    const bool valid = tok < T;
+    float r[R];
+    float m = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < MAXE; ++e) {
-      if (e < E) {
-        if (e == lane) psum0 += p[e];
-        else if (e == lane + 32) psum1 += p[e];
+    for (int j = 0; j < R; ++j) {
+      r[j] = (e_of[j] < E) ? v[j * 32] + bias_v[j] : -INFINITY;
+      m = fmaxf(m, r[j]);
+    }
+#pragma unroll
+    for (int o = GL / 2; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float z = 0.f;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      r[j] = (e_of[j] < E) ? expf(r[j] - m) : 0.f;
+      z += r[j];
+    }
+#pragma unroll
+    for (int o = GL / 2; o >= 1; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    float p[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j) p[j] = r[j] / z;
+
+    // top-k: k rounds of a group-wide arg-max over (p desc, index asc)
+    float sel_p[MM_MAX_TOPK];
+    int sel_e[MM_MAX_TOPK];
+    unsigned taken = 0;
+    float sel_sum = 0.f;
+#pragma unroll
+    for (int s = 0; s < MM_MAX_TOPK; ++s) {
+      sel_p[s] = 0.f;
+      sel_e[s] = 0;
+      if (s < k) {
+        float bp = -1.f;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+          if (!((taken >> j) & 1u) && e_of[j] < E && (p[j] > bp || (p[j] == bp && e_of[j] < be))) {
+            bp = p[j];
+            be = e_of[j];
+          }
+        }
+#pragma unroll
+        for (int o = GL / 2; o >= 1; o >>= 1) {
+          const float op = __shfl_xor_sync(0xffffffffu, bp, o);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+          if (op > bp || (op == bp && oe < be)) {
+            bp = op;
+            be = oe;
+          }
+        }
+        sel_p[s] = bp;
+        sel_e[s] = be;
+        sel_sum += bp;
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+          if (e_of[j] == be) taken |= 1u << j;
       }
     }
+    const int slot = lane - gbase;
+    if (valid && slot < k) {
+      int we = 0;
+      float wp = 0.f;
+#pragma unroll
+      for (int s = 0; s < MM_MAX_TOPK; ++s)
+        if (s == slot) {
+          we = sel_e[s];
+          wp = sel_p[s];
+        }
+      topk_idx[tok * k + slot] = we;
+      topk_w[tok * k + slot] = wp / (sel_sum + 1e-20f);
+      atomicAdd(&s_gcnt[slot * E + we], 1);
+    }
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+      if (valid) psum[j] += p[j];
   }
-  if (lane < E && lane < MAXE) red_p[warp][lane] = psum0;
-  if (lane + 32 < E && lane + 32 < MAXE) red_p[warp][lane + 32] = psum1;
+  // sum the token groups of the warp (lanes with the same expert), fixed order
+#pragma unroll
+  for (int o = GL; o < 32; o <<= 1) {
+#pragma unroll
+    for (int j = 0; j < R; ++j) psum[j] += __shfl_xor_sync(0xffffffffu, psum[j], o);
+  }
+  if (lane < GL) {
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+      if (e_of[j] < EP) red_p[warp][e_of[j]] = psum[j];
+  }
   __syncthreads();
   if (tid < E) {
     float ps = 0.f;
@@ -168,7 +257,7 @@ router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float
 
 // ---------------------------------------------------------------------------
 // Scan (one block): for every group g = s*E + e
-//   blk_base[b][g] = sum_{b' < b} blk_cnt[b'][g]      (warp scan over blocks)
+//   blk_base[b][g] = sum_{b' < b} blk_cnt[b'][g]    (a lane owns a run of blocks)
 //   tot[g] = sum_b blk_cnt[b][g];  offsets = exclusive scan of tot over g
 // and the aux loss ([L13] §1.6; chapter 4 §4.4):
 //   count_e = sum_s tot[s*E + e];  P_e = sum_b blk_prob[b][e]  (fp64, fixed order)
@@ -187,22 +276,29 @@ route_scan_kernel(int E, int k, int nblk, int64_t T, float coef,
   const int G = k * E;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   constexpr int kWarps = kScanThreads / 32;
+  const int per = (nblk + 31) / 32;
 
   for (int g = warp; g < G; g += kWarps) {
-    int run = 0;
-    for (int b0 = 0; b0 < nblk; b0 += 32) {
-      const int b = b0 + lane;
-      const int v = (b < nblk) ? blk_cnt[static_cast<int64_t>(b) * G + g] : 0;
-      int incl = v;
+    const int b0 = lane * per;
+    const int b1 = min(nblk, b0 + per);
+    int sum = 0;
+    for (int b = b0; b < b1; ++b) sum += blk_cnt[static_cast<int64_t>(b) * G + g];
+    int incl = sum;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-      }
-      if (blk_base != nullptr && b < nblk) blk_base[static_cast<int64_t>(b) * G + g] = run + incl - v;
-      run += __shfl_sync(0xffffffffu, incl, 31);
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
     }
-    if (lane == 0) s_tot[g] = run;
+    if (blk_base != nullptr) {
+      int run = incl - sum;
+      for (int b = b0; b < b1; ++b) {
+        const int64_t i = static_cast<int64_t>(b) * G + g;
+        blk_base[i] = run;
+        run += blk_cnt[i];
+      }
+    }
+    const int tot = __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 0) s_tot[g] = tot;
   }
   for (int e = warp; e < E; e += kWarps) {
     // lane-strided partial sums, then a fixed xor-tree: the order depends only on nblk
@@ -285,15 +381,17 @@ dispatch_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, int k,
     __syncthreads();
   }
 
-  // copy rows: one warp per assignment, 16-byte vectors
+  // copy rows: a flat loop over (assignment, 16-byte vector) pairs
   constexpr int kVec = 16 / sizeof(Tin);
   const int nv = H / kVec;
-  const int nA = ntok * k;
-  for (int a = warp; a < nA; a += kWarps) {
-    const int64_t t = tok0 + a / k;
-    const uint4* src = reinterpret_cast<const uint4*>(x + t * H);
-    uint4* dst = reinterpret_cast<uint4*>(Xp + static_cast<int64_t>(s_pos[a]) * H);
-    for (int v = lane; v < nv; v += 32) dst[v] = src[v];
+  const int total = ntok * k * nv;
+  const uint4* src = reinterpret_cast<const uint4*>(x + tok0 * H);
+  uint4* dst = reinterpret_cast<uint4*>(Xp);
+#pragma unroll 4
+  for (int i = tid; i < total; i += kRouteThreads) {
+    const int a = i / nv;
+    const int v = i - a * nv;
+    dst[static_cast<int64_t>(s_pos[a]) * nv + v] = src[(a / k) * nv + v];
   }
 }
 
@@ -310,9 +408,9 @@ static cudaError_t launch_router_t(const void* x, const void* Wr, const float* b
                                    float* blk_prob, cudaStream_t st) {
   const int nblk = static_cast<int>((T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock);
   const size_t smem = router_smem_bytes(H, E, k);
-#define MM_ROUTER_CASE(ME)                                                                     \
+#define MM_ROUTER_CASE(EPAD)                                                                   \
   {                                                                                            \
-    auto fn = router_kernel<Tin, ME>;                                                          \
+    auto fn = router_kernel<Tin, EPAD>;                                                        \
     cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
                                            static_cast<int>(smem));                            \
     if (err != cudaSuccess) return err;                                                        \
