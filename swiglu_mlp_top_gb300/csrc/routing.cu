@@ -260,7 +260,7 @@ router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float
 //   blk_base[b][g] = sum_{b' < b} blk_cnt[b'][g]    (a lane owns a run of blocks)
 //   tot[g] = sum_b blk_cnt[b][g];  offsets = exclusive scan of tot over g
 // and the aux loss ([L13] §1.6; chapter 4 §4.4):
-//   count_e = sum_s tot[s*E + e];  P_e = sum_b blk_prob[b][e]  (fp64, fixed order)
+//   count_e = sum_s tot[s*E + e];  P_e = sum_b blk_prob[b][e]  (fixed order)
 //   aux = E * coef * sum_e (count_e / T) * (P_e / T)
 // Rows of the dispatched matrix are thus ordered by slot, then expert, then
 // token.  offsets / blk_base may be null (route-only call).
@@ -271,7 +271,7 @@ route_scan_kernel(int E, int k, int nblk, int64_t T, float coef,
                   int32_t* __restrict__ blk_base, int32_t* __restrict__ offsets,
                   int32_t* __restrict__ counts, float* __restrict__ aux_loss) {
   __shared__ int s_tot[kMaxGroups];
-  __shared__ double s_P[MM_MAX_EXPERTS];
+  __shared__ float s_P[MM_MAX_EXPERTS];
   __shared__ int s_cnt[MM_MAX_EXPERTS];
   const int G = k * E;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -282,6 +282,7 @@ route_scan_kernel(int E, int k, int nblk, int64_t T, float coef,
     const int b0 = lane * per;
     const int b1 = min(nblk, b0 + per);
     int sum = 0;
+#pragma unroll 8
     for (int b = b0; b < b1; ++b) sum += blk_cnt[static_cast<int64_t>(b) * G + g];
     int incl = sum;
 #pragma unroll
@@ -302,8 +303,9 @@ route_scan_kernel(int E, int k, int nblk, int64_t T, float coef,
   }
   for (int e = warp; e < E; e += kWarps) {
     // lane-strided partial sums, then a fixed xor-tree: the order depends only on nblk
-    double P = 0.0;
-    for (int b = lane; b < nblk; b += 32) P += static_cast<double>(blk_prob[static_cast<int64_t>(b) * E + e]);
+    float P = 0.f;
+#pragma unroll 8
+    for (int b = lane; b < nblk; b += 32) P += blk_prob[static_cast<int64_t>(b) * E + e];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) P += __shfl_xor_sync(0xffffffffu, P, o);
     if (lane == 0) s_P[e] = P;
@@ -325,11 +327,11 @@ route_scan_kernel(int E, int k, int nblk, int64_t T, float coef,
       }
       offsets[G] = run;
     }
-    double acc = 0.0;
-    for (int e = 0; e < E; ++e)
-      acc += (static_cast<double>(s_cnt[e]) / static_cast<double>(T)) * (s_P[e] / static_cast<double>(T));
-    if (aux_loss != nullptr)
-      *aux_loss = static_cast<float>(static_cast<double>(E) * static_cast<double>(coef) * acc);
+    // E*coef*sum_e (count_e/T)(P_e/T) = (E*coef/T^2) * sum_e count_e * P_e
+    float acc = 0.f;
+    for (int e = 0; e < E; ++e) acc = fmaf(static_cast<float>(s_cnt[e]), s_P[e], acc);
+    const float invT = 1.0f / static_cast<float>(T);
+    if (aux_loss != nullptr) *aux_loss = static_cast<float>(E) * coef * acc * invT * invT;
   }
 }
 
