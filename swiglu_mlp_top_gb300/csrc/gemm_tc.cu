@@ -37,7 +37,12 @@ constexpr int kStages = 6;
 constexpr int kAStage = kTcBM * kTcBK * 2;               // 16 KiB (this CTA's 128 rows)
 constexpr int kBStage = (kN / 2) * kTcBK * 2;            // 16 KiB (this CTA's half of N)
 constexpr int kAccStride = 256;                          // TMEM columns per accumulator
-constexpr int kSmem = kStages * (kAStage + kBStage) + 2048;
+// Epilogue staging: each epilogue thread owns a 128-byte slot (one row piece)
+// at a 144-byte pitch (conflict-free 16-byte stores across a warp); the
+// bulk-copy engine writes the slot to its row in global memory.
+constexpr int kSlotPitch = 144;
+constexpr int kStageEpi = 4 * 32 * kSlotPitch;           // 18 KiB
+constexpr int kSmem = kStages * (kAStage + kBStage) + kStageEpi + 2048;
 constexpr uint32_t kTmemCols = 512;
 static_assert(kSmem <= 232448, "shared memory budget");
 static_assert(kUpBN == 128, "gate/up tiles 128 h columns (g | u = 256)");
@@ -106,37 +111,55 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // ---------------------------------------------------------------- epilogues
-// gate/up: 128 h columns of one row: h = SiLU(g) * u, fp16.
+// Writes one 128-byte row piece through the thread's staging slot: wait for
+// the slot's previous copy to have read it, fill it, hand it to the bulk
+// engine (store or fp32 reduce-add).
+template <bool kReduce>
+__device__ __forceinline__ void emit_piece(uint8_t* slot, void* gdst, const uint32_t (&w)[32]) {
+  bulk_wait_read();
+  uint4* s4 = reinterpret_cast<uint4*>(slot);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) s4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  fence_proxy_async_smem();
+  if (kReduce)
+    bulk_reduce_add_f32(gdst, slot, 128);
+  else
+    bulk_store(gdst, slot, 128);
+  bulk_commit();
+}
+
+// gate/up: 128 h columns of one row: h = SiLU(g) * u, fp16, in two 64-column pieces.
 __device__ __forceinline__ void epilogue_up(uint32_t tb, bool valid, const TileInfo& ti, int I,
-                                            __half* hout, int row) {
+                                            __half* hout, int row, uint8_t* slot) {
   __half* dst = hout + static_cast<int64_t>(ti.row0 + (valid ? row : 0)) * I + ti.n0;
 #pragma unroll 1
-  for (int c = 0; c < kN / 2 / 32; ++c) {
-    uint32_t gr[32], ur[32];
-    tmem_ld_32x32b_x32(tb + c * 32, gr);
-    tmem_ld_32x32b_x32(tb + kN / 2 + c * 32, ur);
-    tmem_ld_wait();
-    if (valid && ti.n0 + c * 32 < I) {
-      uint32_t pk[16];
+  for (int p = 0; p < kN / 2 / 64; ++p) {
+    uint32_t pk[32];
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int c = 2 * p + h2;
+      uint32_t gr[32], ur[32];
+      tmem_ld_32x32b_x32(tb + c * 32, gr);
+      tmem_ld_32x32b_x32(tb + kN / 2 + c * 32, ur);
+      tmem_ld_wait();
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const float g0 = __uint_as_float(gr[2 * j]), g1 = __uint_as_float(gr[2 * j + 1]);
         const float u0 = __uint_as_float(ur[2 * j]), u1 = __uint_as_float(ur[2 * j + 1]);
         const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
         const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
-        pk[j] = pack_f16x2(h0, h1);
+        pk[16 * h2 + j] = pack_f16x2(h0, h1);
       }
-      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
     }
+    if (valid && ti.n0 + p * 64 < I) emit_piece<false>(slot, dst + p * 64, pk);
   }
 }
 
-// down: 256 y columns of one row, scaled by alpha; store / fp32 accumulate.
+// down: 256 y columns of one row, scaled by alpha.  Store / Last: bf16 pieces
+// of 64 columns; First: fp32 pieces of 32 columns stored to acc32; Accum:
+// fp32 pieces reduce-added into acc32; Last adds acc32 (read directly).
 __device__ __forceinline__ void epilogue_down(uint32_t tb, bool valid, const TileInfo& ti, int H,
-                                              const DownEpilogue& ep, int row) {
+                                              const DownEpilogue& ep, int row, uint8_t* slot) {
   int64_t tok = 0;
   float alpha = 1.0f;
   if (valid) {
@@ -151,43 +174,52 @@ __device__ __forceinline__ void epilogue_down(uint32_t tb, bool valid, const Til
   }
   __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(ep.y) + tok * H + ti.n0;
   float* acc32 = ep.acc32 + tok * H + ti.n0;
+  if (ep.mode == kCombineFirst || ep.mode == kCombineAccum) {
 #pragma unroll 1
-  for (int c = 0; c < kN / 32; ++c) {
-    uint32_t r[32];
-    tmem_ld_32x32b_x32(tb + c * 32, r);
-    tmem_ld_wait();
-    if (valid && ti.n0 + c * 32 < H) {
+    for (int c = 0; c < kN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tb + c * 32, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(alpha * __uint_as_float(r[j]));
+      if (valid && ti.n0 + c * 32 < H) {
+        if (ep.mode == kCombineFirst)
+          emit_piece<false>(slot, acc32 + c * 32, r);
+        else
+          emit_piece<true>(slot, acc32 + c * 32, r);
+      }
+    }
+    return;
+  }
+#pragma unroll 1
+  for (int p = 0; p < kN / 64; ++p) {
+    const bool live = valid && ti.n0 + p * 64 < H;
+    float4 pre[16];
+    if (live && ep.mode == kCombineLast) {
+      const float4* a4 = reinterpret_cast<const float4*>(acc32 + p * 64);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) pre[q] = a4[q];
+    }
+    uint32_t pk[32];
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tb + (2 * p + h2) * 32, r);
+      tmem_ld_wait();
       float v[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = alpha * __uint_as_float(r[j]);
-      float4* a4 = reinterpret_cast<float4*>(acc32 + c * 32);
-      if (ep.mode == kCombineFirst) {
+      if (ep.mode == kCombineLast) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          a4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-      } else {
-        if (ep.mode != kCombineStore) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 o = a4[q];
-            v[4 * q] += o.x; v[4 * q + 1] += o.y; v[4 * q + 2] += o.z; v[4 * q + 3] += o.w;
-          }
-        }
-        if (ep.mode == kCombineAccum) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            a4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        } else {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            d4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]),
-                               pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                               pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                               pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+        for (int q = 0; q < 8; ++q) {
+          const float4 o = pre[8 * h2 + q];
+          v[4 * q] += o.x; v[4 * q + 1] += o.y; v[4 * q + 2] += o.z; v[4 * q + 3] += o.w;
         }
       }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) pk[16 * h2 + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
     }
+    if (live) emit_piece<false>(slot, dst + p * 64, pk);
   }
 }
 
@@ -204,7 +236,8 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kAStage;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBStage);
+  uint8_t* sEpi = sB + kStages * kBStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + kStageEpi);
   uint64_t* full = bars;                  // [kStages] even CTA: both CTAs' bytes
   uint64_t* empty = bars + kStages;       // [kStages] each CTA: released by the pair's MMAs
   uint64_t* tfull = bars + 2 * kStages;   // [2] each CTA: accumulator ready
@@ -312,6 +345,7 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
   } else {
     // ------------------------------------------------ epilogue (warps 0-3, both CTAs)
     const int row = warp * 32 + lane;
+    uint8_t* slot = sEpi + row * kSlotPitch;
     const uint32_t te0 = mapa_shared(smem_u32(&tempty[0]), 0);
     const uint32_t te1 = mapa_shared(smem_u32(&tempty[1]), 0);
     int local = 0;
@@ -325,13 +359,14 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
       const uint32_t tb = tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * kAccStride;
       const bool valid = row < ti.rows;
       if constexpr (OP == kOpUp)
-        epilogue_up(tb, valid, ti, NCOLS, hout, row);
+        epilogue_up(tb, valid, ti, NCOLS, hout, row, slot);
       else
-        epilogue_down(tb, valid, ti, NCOLS, ep, row);
+        epilogue_down(tb, valid, ti, NCOLS, ep, row, slot);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc ? te1 : te0);
     }
+    bulk_wait_all();   // this thread's row copies have landed
   }
 
   tc_fence_before();
