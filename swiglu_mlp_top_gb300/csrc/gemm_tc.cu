@@ -37,11 +37,14 @@ constexpr int kStages = 6;
 constexpr int kAStage = kTcBM * kTcBK * 2;               // 16 KiB (this CTA's 128 rows)
 constexpr int kBStage = (kN / 2) * kTcBK * 2;            // 16 KiB (this CTA's half of N)
 constexpr int kAccStride = 256;                          // TMEM columns per accumulator
-// Epilogue staging: each epilogue thread owns a 128-byte slot (one row piece)
-// at a 144-byte pitch (conflict-free 16-byte stores across a warp); the
-// bulk-copy engine writes the slot to its row in global memory.
-constexpr int kSlotPitch = 144;
-constexpr int kStageEpi = 4 * 32 * kSlotPitch;           // 18 KiB
+// Epilogue staging, 4 KiB per epilogue warp: gate/up stages a 32-row x
+// 64-column fp16 piece in the 128-byte-swizzled layout of a TMA box and
+// stores it with one tensor store; down gives each thread a 128-byte slot
+// (144-byte pitch, conflict-free) that the bulk engine copies to the row's
+// token.
+constexpr int kSlotPitch = 128;                          // gate/up staging row
+constexpr int kDownSlotPitch = 144;                      // down per-thread slot
+constexpr int kStageEpi = 4 * 32 * kDownSlotPitch;       // 18 KiB
 constexpr int kSmem = kStages * (kAStage + kBStage) + kStageEpi + 2048;
 constexpr uint32_t kTmemCols = 512;
 static_assert(kSmem <= 232448, "shared memory budget");
@@ -53,6 +56,7 @@ template <> struct OpTraits<kOpDown> { static constexpr int kOutCols = kN; };
 
 template <int MAXW>
 struct TcParams {
+  CUtensorMap out;          // gate/up: h [a_rows, I] fp16, box 64 x 32 (TMA stores)
   CUtensorMap a;            // A [a_rows, K]
   CUtensorMap b0[MAXW];     // gate/up: Wg; down: fp16 Wd  (box rows = N/2)
   CUtensorMap b1[MAXW];     // gate/up: Wu; down: unused
@@ -128,9 +132,16 @@ __device__ __forceinline__ void emit_piece(uint8_t* slot, void* gdst, const uint
   bulk_commit();
 }
 
-// gate/up: 128 h columns of one row: h = SiLU(g) * u, fp16, in two 64-column pieces.
-__device__ __forceinline__ void epilogue_up(uint32_t tb, bool valid, const TileInfo& ti, int I,
-                                            __half* hout, int row, uint8_t* slot) {
+// gate/up: 128 h columns of one row: h = SiLU(g) * u, fp16, in two 64-column
+// pieces.  A warp whose 32 rows are all in the group writes each piece with
+// one TMA tensor store from its swizzled staging tile; a warp holding a
+// group's ragged end stores its valid rows directly (the rows past the end
+// belong to the next group).
+__device__ __forceinline__ void epilogue_up(uint32_t tb, const TileInfo& ti, int I, __half* hout,
+                                            int row, uint8_t* wstage, const CUtensorMap* hmap) {
+  const int lane = row & 31;
+  const bool valid = row < ti.rows;
+  const bool full_warp = (row | 31) < ti.rows;   // warp-uniform
   __half* dst = hout + static_cast<int64_t>(ti.row0 + (valid ? row : 0)) * I + ti.n0;
 #pragma unroll 1
   for (int p = 0; p < kN / 2 / 64; ++p) {
@@ -151,7 +162,26 @@ __device__ __forceinline__ void epilogue_up(uint32_t tb, bool valid, const TileI
         pk[16 * h2 + j] = pack_f16x2(h0, h1);
       }
     }
-    if (valid && ti.n0 + p * 64 < I) emit_piece<false>(slot, dst + p * 64, pk);
+    if (ti.n0 + p * 64 >= I) continue;           // whole piece past the last column
+    if (full_warp) {
+      if (lane == 0) bulk_wait_read();             // previous store has read the tile
+      __syncwarp();
+      uint8_t* r128 = wstage + lane * 128;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(r128 + ((q ^ (lane & 7)) << 4)) =
+            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(hmap, wstage, ti.n0 + p * 64, ti.row0 + (row & ~31));
+        bulk_commit();
+      }
+    } else if (valid) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + p * 64);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
   }
 }
 
@@ -345,7 +375,8 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
   } else {
     // ------------------------------------------------ epilogue (warps 0-3, both CTAs)
     const int row = warp * 32 + lane;
-    uint8_t* slot = sEpi + row * kSlotPitch;
+    uint8_t* slot = sEpi + row * kDownSlotPitch;     // down: this thread's row piece
+    uint8_t* wstage = sEpi + warp * 32 * kSlotPitch;  // gate/up: this warp's staging tile
     const uint32_t te0 = mapa_shared(smem_u32(&tempty[0]), 0);
     const uint32_t te1 = mapa_shared(smem_u32(&tempty[1]), 0);
     int local = 0;
@@ -359,7 +390,7 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
       const uint32_t tb = tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * kAccStride;
       const bool valid = row < ti.rows;
       if constexpr (OP == kOpUp)
-        epilogue_up(tb, valid, ti, NCOLS, hout, row, slot);
+        epilogue_up(tb, ti, NCOLS, hout, row, wstage, &P.out);
       else
         epilogue_down(tb, valid, ti, NCOLS, ep, row, slot);
       tc_fence_before();
@@ -450,6 +481,7 @@ static cudaError_t gateup_impl(const void* A, int64_t a_rows, int H, int I, cons
                                WsHeader* hdr, cudaStream_t st) {
   TcParams<MAXW> p;
   memset(&p, 0, sizeof(p));
+  if (!make_map_16(&p.out, h_out, I, a_rows, 32, true)) return cudaErrorInvalidValue;
   if (!make_map_16(&p.a, A, H, a_rows, kTcBM, false)) return cudaErrorInvalidValue;
   for (int e = 0; e < g.n_weights; ++e) {
     if (!make_map_16(&p.b0[e], Wg[e], H, I, kN / 2, false)) return cudaErrorInvalidValue;

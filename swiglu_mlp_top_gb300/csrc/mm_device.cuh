@@ -278,6 +278,14 @@ __device__ __forceinline__ void bulk_reduce_add_f32(void* gdst, const void* ssrc
                "r"(smem_u32(ssrc)), "r"(bytes)
                : "memory");
 }
+// 2-D tiled TMA store of a box from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d(const void* tmap, const void* smem_src, int32_t c0,
+                                             int32_t c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(smem_u32(smem_src)), "r"(c0), "r"(c1)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
