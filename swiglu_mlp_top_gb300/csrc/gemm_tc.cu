@@ -37,18 +37,17 @@ constexpr int kStages = 6;
 constexpr int kAStage = kTcBM * kTcBK * 2;               // 16 KiB (this CTA's 128 rows)
 constexpr int kBStage = (kN / 2) * kTcBK * 2;            // 16 KiB (this CTA's half of N)
 constexpr int kAccStride = 256;                          // TMEM columns per accumulator
-// Epilogue staging, 4 KiB per epilogue warp: gate/up stages a 32-row x
-// 64-column fp16 piece in the 128-byte-swizzled layout of a TMA box and
-// stores it with one tensor store; down gives each thread a 128-byte slot
-// (144-byte pitch, conflict-free) that the bulk engine copies to the row's
-// token.
-constexpr int kSlotPitch = 128;                          // gate/up staging row
-constexpr int kDownSlotPitch = 144;                      // down per-thread slot
-constexpr int kStageEpi = 4 * 32 * kDownSlotPitch;       // 18 KiB
+// Epilogue: 8 warps; warp w reads TMEM lanes 32*(w%4).. (its rows) and
+// handles half w/4 of the tile's columns.  gate/up stages each 32-row x
+// 32-column fp16 piece in the 64-byte-swizzled layout of a TMA box (2 KiB
+// per warp) and writes it with one tensor store.
+constexpr int kEpiWarps = 8;
+constexpr int kStageEpi = kEpiWarps * 32 * 64;           // 16 KiB
+constexpr int kWarpProducer = kEpiWarps, kWarpMma = kEpiWarps + 1;
+constexpr int kThreads = 32 * (kEpiWarps + 2);
 constexpr int kSmem = kStages * (kAStage + kBStage) + kStageEpi + 2048;
 constexpr uint32_t kTmemCols = 512;
 static_assert(kSmem <= 232448, "shared memory budget");
-static_assert(kUpBN == 128, "gate/up tiles 128 h columns (g | u = 256)");
 
 template <int OP> struct OpTraits;
 template <> struct OpTraits<kOpUp> { static constexpr int kOutCols = kN / 2; };
@@ -56,7 +55,7 @@ template <> struct OpTraits<kOpDown> { static constexpr int kOutCols = kN; };
 
 template <int MAXW>
 struct TcParams {
-  CUtensorMap out;          // gate/up: h [a_rows, I] fp16, box 64 x 32 (TMA stores)
+  CUtensorMap out;          // gate/up: h [a_rows, I] fp16, box 32 x 32 (TMA stores)
   CUtensorMap a;            // A [a_rows, K]
   CUtensorMap b0[MAXW];     // gate/up: Wg; down: fp16 Wd  (box rows = N/2)
   CUtensorMap b1[MAXW];     // gate/up: Wu; down: unused
@@ -115,81 +114,64 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // ---------------------------------------------------------------- epilogues
-// Writes one 128-byte row piece through the thread's staging slot: wait for
-// the slot's previous copy to have read it, fill it, hand it to the bulk
-// engine (store or fp32 reduce-add).
-template <bool kReduce>
-__device__ __forceinline__ void emit_piece(uint8_t* slot, void* gdst, const uint32_t (&w)[32]) {
-  bulk_wait_read();
-  uint4* s4 = reinterpret_cast<uint4*>(slot);
-#pragma unroll
-  for (int q = 0; q < 8; ++q) s4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-  fence_proxy_async_smem();
-  if (kReduce)
-    bulk_reduce_add_f32(gdst, slot, 128);
-  else
-    bulk_store(gdst, slot, 128);
-  bulk_commit();
-}
-
-// gate/up: 128 h columns of one row: h = SiLU(g) * u, fp16, in two 64-column
-// pieces.  A warp whose 32 rows are all in the group writes each piece with
-// one TMA tensor store from its swizzled staging tile; a warp holding a
-// group's ragged end stores its valid rows directly (the rows past the end
-// belong to the next group).
+// gate/up: 64 h columns (half `half` of the tile's 128) of one row:
+// h = SiLU(g) * u, fp16, as two 32-column pieces.  A warp whose 32 rows are
+// all in the group writes each piece with one TMA tensor store from its
+// swizzled staging tile; a warp holding a group's ragged end stores its
+// valid rows directly (the rows past the end belong to the next group).
 __device__ __forceinline__ void epilogue_up(uint32_t tb, const TileInfo& ti, int I, __half* hout,
-                                            int row, uint8_t* wstage, const CUtensorMap* hmap) {
+                                            int row, int half, uint8_t* wstage,
+                                            const CUtensorMap* hmap) {
   const int lane = row & 31;
   const bool valid = row < ti.rows;
   const bool full_warp = (row | 31) < ti.rows;   // warp-uniform
-  __half* dst = hout + static_cast<int64_t>(ti.row0 + (valid ? row : 0)) * I + ti.n0;
+  const int col0 = ti.n0 + half * 64;
+  __half* dst = hout + static_cast<int64_t>(ti.row0 + (valid ? row : 0)) * I + col0;
 #pragma unroll 1
-  for (int p = 0; p < kN / 2 / 64; ++p) {
-    uint32_t pk[32];
+  for (int c = 0; c < 2; ++c) {
+    const int tcol = half * 64 + c * 32;         // TMEM column of g; u is kN/2 further
+    uint32_t gr[32], ur[32];
+    tmem_ld_32x32b_x32(tb + tcol, gr);
+    tmem_ld_32x32b_x32(tb + kN / 2 + tcol, ur);
+    tmem_ld_wait();
+    uint32_t pk[16];
 #pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      const int c = 2 * p + h2;
-      uint32_t gr[32], ur[32];
-      tmem_ld_32x32b_x32(tb + c * 32, gr);
-      tmem_ld_32x32b_x32(tb + kN / 2 + c * 32, ur);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float g0 = __uint_as_float(gr[2 * j]), g1 = __uint_as_float(gr[2 * j + 1]);
-        const float u0 = __uint_as_float(ur[2 * j]), u1 = __uint_as_float(ur[2 * j + 1]);
-        const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
-        const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
-        pk[16 * h2 + j] = pack_f16x2(h0, h1);
-      }
+    for (int j = 0; j < 16; ++j) {
+      const float g0 = __uint_as_float(gr[2 * j]), g1 = __uint_as_float(gr[2 * j + 1]);
+      const float u0 = __uint_as_float(ur[2 * j]), u1 = __uint_as_float(ur[2 * j + 1]);
+      const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+      const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
+      pk[j] = pack_f16x2(h0, h1);
     }
-    if (ti.n0 + p * 64 >= I) continue;           // whole piece past the last column
+    if (col0 + c * 32 >= I) continue;            // piece past the last column
     if (full_warp) {
       if (lane == 0) bulk_wait_read();             // previous store has read the tile
       __syncwarp();
-      uint8_t* r128 = wstage + lane * 128;
+      // 64-byte rows, 16-byte chunk q of row r at chunk q ^ ((r >> 1) & 3)
+      uint8_t* r64 = wstage + lane * 64;
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<uint4*>(r128 + ((q ^ (lane & 7)) << 4)) =
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(r64 + ((q ^ ((lane >> 1) & 3)) << 4)) =
             make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_2d(hmap, wstage, ti.n0 + p * 64, ti.row0 + (row & ~31));
+        tma_store_2d(hmap, wstage, col0 + c * 32, ti.row0 + (row & ~31));
         bulk_commit();
       }
     } else if (valid) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + p * 64);
+      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
     }
   }
 }
 
-// down: 256 y columns of one row, scaled by alpha.  Store / Last: bf16 pieces
-// of 64 columns; First: fp32 pieces of 32 columns stored to acc32; Accum:
-// fp32 pieces reduce-added into acc32; Last adds acc32 (read directly).
+// down: 128 y columns (half `half` of the tile's 256) of one row, scaled by
+// alpha: Store -> y (x's dtype); First -> acc32 = v; Accum -> acc32 += v;
+// Last -> y = round(acc32 + v).
 __device__ __forceinline__ void epilogue_down(uint32_t tb, bool valid, const TileInfo& ti, int H,
-                                              const DownEpilogue& ep, int row, uint8_t* slot) {
+                                              const DownEpilogue& ep, int row, int half) {
   int64_t tok = 0;
   float alpha = 1.0f;
   if (valid) {
@@ -202,54 +184,41 @@ __device__ __forceinline__ void epilogue_down(uint32_t tb, bool valid, const Til
       tok = pos;
     }
   }
-  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(ep.y) + tok * H + ti.n0;
-  float* acc32 = ep.acc32 + tok * H + ti.n0;
-  if (ep.mode == kCombineFirst || ep.mode == kCombineAccum) {
+  const int col0 = ti.n0 + half * (kN / 2);
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(ep.y) + tok * H + col0;
+  float* acc32 = ep.acc32 + tok * H + col0;
 #pragma unroll 1
-    for (int c = 0; c < kN / 32; ++c) {
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(tb + c * 32, r);
-      tmem_ld_wait();
+  for (int c = 0; c < kN / 2 / 32; ++c) {
+    const bool live = valid && col0 + c * 32 < H;
+    float4* a4 = reinterpret_cast<float4*>(acc32 + c * 32);
+    float4 pre[8];
+    if (live && (ep.mode == kCombineAccum || ep.mode == kCombineLast)) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(alpha * __uint_as_float(r[j]));
-      if (valid && ti.n0 + c * 32 < H) {
-        if (ep.mode == kCombineFirst)
-          emit_piece<false>(slot, acc32 + c * 32, r);
-        else
-          emit_piece<true>(slot, acc32 + c * 32, r);
+      for (int q = 0; q < 8; ++q) pre[q] = a4[q];
+    }
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(tb + half * (kN / 2) + c * 32, r);
+    tmem_ld_wait();
+    if (!live) continue;
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = alpha * __uint_as_float(r[j]);
+    if (ep.mode == kCombineAccum || ep.mode == kCombineLast) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        v[4 * q] += pre[q].x; v[4 * q + 1] += pre[q].y; v[4 * q + 2] += pre[q].z; v[4 * q + 3] += pre[q].w;
       }
     }
-    return;
-  }
-#pragma unroll 1
-  for (int p = 0; p < kN / 64; ++p) {
-    const bool live = valid && ti.n0 + p * 64 < H;
-    float4 pre[16];
-    if (live && ep.mode == kCombineLast) {
-      const float4* a4 = reinterpret_cast<const float4*>(acc32 + p * 64);
+    if (ep.mode == kCombineFirst || ep.mode == kCombineAccum) {
 #pragma unroll
-      for (int q = 0; q < 16; ++q) pre[q] = a4[q];
+      for (int q = 0; q < 8; ++q) a4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        d4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
     }
-    uint32_t pk[32];
-#pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(tb + (2 * p + h2) * 32, r);
-      tmem_ld_wait();
-      float v[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = alpha * __uint_as_float(r[j]);
-      if (ep.mode == kCombineLast) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 o = pre[8 * h2 + q];
-          v[4 * q] += o.x; v[4 * q + 1] += o.y; v[4 * q + 2] += o.z; v[4 * q + 3] += o.w;
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) pk[16 * h2 + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-    }
-    if (live) emit_piece<false>(slot, dst + p * 64, pk);
   }
 }
 
@@ -257,7 +226,7 @@ __device__ __forceinline__ void epilogue_down(uint32_t tb, bool valid, const Til
 // K = contraction length (H for gate/up, I for down); NCOLS = output width
 // (I for gate/up, H for down).
 template <int OP, int MAXW>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g, const int K,
                     const int NCOLS, __half* __restrict__ hout, const DownEpilogue ep,
                     WsHeader* hdr) {
@@ -290,15 +259,15 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 2 * 4);     // one arrival per epilogue warp of both CTAs
+      mbar_init(&tempty[a], 2 * kEpiWarps);   // one arrival per epilogue warp of both CTAs
     }
     mbar_init(drained, 1);
     fence_mbar_init();
     s_abort = 0;
     build_schedule(g, n_tiles, s_off, s_tstart);
   }
-  if (warp == 4 && lane == 0) tma_prefetch_desc(&P.a);
-  if (warp == 5) {
+  if (warp == kWarpProducer && lane == 0) tma_prefetch_desc(&P.a);
+  if (warp == kWarpMma) {
     tmem_alloc_cta2(&s_tmem, kTmemCols);
     tmem_relinquish_cta2();
   }
@@ -309,7 +278,7 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
   const int total = s_tstart[g.G];
   volatile int* abort = &s_abort;
 
-  if (warp == 4) {
+  if (warp == kWarpProducer) {
     // ------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       int it = 0;
@@ -339,7 +308,7 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------ MMA issuer (even CTA)
     if (rank == 0 && lane == 0) {
       constexpr uint32_t idesc = (OP == kOpUp) ? idesc_bf16_f32(kPairM, kN) : idesc_f16_f32(kPairM, kN);
@@ -373,10 +342,10 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------ epilogue (warps 0-3, both CTAs)
-    const int row = warp * 32 + lane;
-    uint8_t* slot = sEpi + row * kDownSlotPitch;     // down: this thread's row piece
-    uint8_t* wstage = sEpi + warp * 32 * kSlotPitch;  // gate/up: this warp's staging tile
+    // ------------------------------------------------ epilogue (warps 0-7, both CTAs)
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = quad * 32 + lane;
+    uint8_t* wstage = sEpi + warp * 32 * 64;     // gate/up: this warp's staging tile
     const uint32_t te0 = mapa_shared(smem_u32(&tempty[0]), 0);
     const uint32_t te1 = mapa_shared(smem_u32(&tempty[1]), 0);
     int local = 0;
@@ -387,23 +356,22 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
       const uint32_t aph = (local >> 1) & 1;
       if (!warp_wait(&tfull[acc], aph, abort, hdr, 6)) break;
       tc_fence_after();
-      const uint32_t tb = tmem + (static_cast<uint32_t>(warp * 32) << 16) + acc * kAccStride;
-      const bool valid = row < ti.rows;
+      const uint32_t tb = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * kAccStride;
       if constexpr (OP == kOpUp)
-        epilogue_up(tb, ti, NCOLS, hout, row, wstage, &P.out);
+        epilogue_up(tb, ti, NCOLS, hout, row, half, wstage, &P.out);
       else
-        epilogue_down(tb, valid, ti, NCOLS, ep, row, slot);
+        epilogue_down(tb, row < ti.rows, ti, NCOLS, ep, row, half);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc ? te1 : te0);
     }
-    bulk_wait_all();   // this thread's row copies have landed
+    bulk_wait_all();   // this warp's tensor stores have landed
   }
 
   tc_fence_before();
   cluster_sync();            // no CTA leaves while its peer may still signal it
   tc_fence_after();
-  if (warp == 5) tmem_dealloc_cta2(tmem, kTmemCols);
+  if (warp == kWarpMma) tmem_dealloc_cta2(tmem, kTmemCols);
 }
 
 // =============================================================== host side
@@ -430,11 +398,13 @@ static EncodeTiledFn get_encode_fn() {
 // box_rows (outer), 128-byte swizzle, zero fill outside the matrix.  Cached by
 // (ptr, shape, box, type).
 static bool make_map_16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
-                        uint32_t box_rows, bool is_f16) {
-  using Key = std::tuple<uintptr_t, uint64_t, uint64_t, uint32_t, bool>;
+                        uint32_t box_rows, bool is_f16, uint32_t box_inner = kTcBK,
+                        CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+  using Key = std::tuple<uintptr_t, uint64_t, uint64_t, uint32_t, bool, uint32_t, int>;
   static std::mutex mu;
   static std::map<Key, CUtensorMap> cache;
-  const Key key{reinterpret_cast<uintptr_t>(ptr), inner, outer, box_rows, is_f16};
+  const Key key{reinterpret_cast<uintptr_t>(ptr), inner, outer, box_rows, is_f16, box_inner,
+                static_cast<int>(swz)};
   std::lock_guard<std::mutex> lock(mu);
   auto itc = cache.find(key);
   if (itc != cache.end()) {
@@ -445,11 +415,11 @@ static bool make_map_16(CUtensorMap* out, const void* ptr, uint64_t inner, uint6
   if (enc == nullptr) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBK), box_rows};
+  cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(out, is_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                          2, const_cast<void*>(ptr), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   if (cache.size() > 4096) cache.clear();
@@ -481,7 +451,8 @@ static cudaError_t gateup_impl(const void* A, int64_t a_rows, int H, int I, cons
                                WsHeader* hdr, cudaStream_t st) {
   TcParams<MAXW> p;
   memset(&p, 0, sizeof(p));
-  if (!make_map_16(&p.out, h_out, I, a_rows, 32, true)) return cudaErrorInvalidValue;
+  if (!make_map_16(&p.out, h_out, I, a_rows, 32, true, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
   if (!make_map_16(&p.a, A, H, a_rows, kTcBM, false)) return cudaErrorInvalidValue;
   for (int e = 0; e < g.n_weights; ++e) {
     if (!make_map_16(&p.b0[e], Wg[e], H, I, kN / 2, false)) return cudaErrorInvalidValue;
@@ -492,7 +463,7 @@ static cudaError_t gateup_impl(const void* A, int64_t a_rows, int H, int I, cons
   if (err != cudaSuccess) return err;
   const int n_tiles = (I + kN / 2 - 1) / (kN / 2);
   DownEpilogue none{};
-  fn<<<2 * clusters_for(a_rows, g, n_tiles), kTcThreads, kSmem, st>>>(
+  fn<<<2 * clusters_for(a_rows, g, n_tiles), kThreads, kSmem, st>>>(
       p, g, H, I, static_cast<__half*>(h_out), none, hdr);
   return cudaGetLastError();
 }
@@ -510,7 +481,7 @@ static cudaError_t down_impl(const void* h, int64_t a_rows, int H, int I, const 
   cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (err != cudaSuccess) return err;
   const int n_tiles = (H + kN - 1) / kN;
-  fn<<<2 * clusters_for(a_rows, g, n_tiles), kTcThreads, kSmem, st>>>(p, g, I, H, nullptr, ep,
+  fn<<<2 * clusters_for(a_rows, g, n_tiles), kThreads, kSmem, st>>>(p, g, I, H, nullptr, ep,
                                                                         hdr);
   return cudaGetLastError();
 }

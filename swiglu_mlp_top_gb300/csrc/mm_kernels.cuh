@@ -15,12 +15,9 @@ constexpr int kRouteTokensPerBlock = 64;    // 8 tokens per warp
 constexpr int kScanThreads = 512;
 constexpr int kMaxGroups = MM_MAX_EXPERTS * MM_MAX_TOPK;     // (slot, expert) groups
 
-// Tensor-core GEMM geometry (tcgen05, cta_group::1).
-constexpr int kTcBM = 128;                  // rows per tile (TMEM lanes)
-constexpr int kTcBK = 64;                   // K per stage: one 128-byte swizzle row of bf16
-constexpr int kUpBN = 128;                  // h columns per gate/up tile (MMA N = 256: g | u)
-constexpr int kDownBN = 192;                // y columns per down tile
-constexpr int kTcThreads = 192;             // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer
+// Tensor-core GEMM geometry (tcgen05 over a CTA pair; the rest in gemm_tc.cu).
+constexpr int kTcBM = 128;                  // rows per CTA (TMEM lanes)
+constexpr int kTcBK = 64;                   // K per stage: one 128-byte swizzle row of 16-bit data
 
 // How the down-projection epilogue writes its rows.  With k >= 2 the
 // contributions of a token are summed in fp32 in slot order, one slot per
