@@ -96,6 +96,40 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
                      void* workspace, size_t workspace_bytes, void* stream, int path);
 
 /* ------------------------------------------------------------------------
+ * Dense SwiGLU FFN without caller-provided scratch
+ *
+ * The pages describe no counterpart of this entry point; it exists for
+ * callers that cannot allocate device memory when they run the FFN: code
+ * that enqueues work while a CUDA graph is being captured in a mode that
+ * forbids cudaMalloc, plug-ins of inference runtimes whose enqueue step
+ * must not allocate, and real-time loops that cannot afford the implicit
+ * device synchronisation of cudaMalloc / cudaFree.
+ *
+ * Same arguments and result as mm_swiglu_ffn, minus the workspace: its
+ * scratch is a fixed array of MM_NOALLOC_SCRATCH_BYTES bytes of device
+ * memory that belongs to this library.  The CUDA runtime reserves it on
+ * every GPU where the library is loaded and keeps it until the process
+ * exits.  The call allocates nothing.
+ *
+ *   - Size limit: the call needs mm_swiglu_ffn_workspace_bytes(T, H, I,
+ *     dtype) <= MM_NOALLOC_SCRATCH_BYTES.  Anything larger returns
+ *     MM_ERR_UNSUPPORTED with nothing enqueued.  For example, with H = 768,
+ *     I = 2432 and bf16 this means T <= 2681.
+ *   - The first call on each device looks up the array's device address,
+ *     with that device current.  Make that first call before any stream
+ *     capture starts.
+ *   - All calls share the one array, and it keeps the last call's contents.
+ *     Calls that overlap on the GPU therefore race: order them on one
+ *     stream, or finish one before starting the next.
+ *   - Its device watchdog word is not readable through mm_check_status.
+ *     Stream errors are still reported by the CUDA runtime.
+ * ---------------------------------------------------------------------- */
+#define MM_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+int mm_swiglu_ffn_noalloc(const void* x, const void* Wg, const void* Wu, const void* Wd,
+                          void* y, int64_t T, int H, int I, int dtype, void* stream);
+
+/* ------------------------------------------------------------------------
  * Top-k MoE forward   ([L13] §1.5, §1.6, §3 steps 4-6; [CH4] §4.3, §4.4)
  *
  *   r = Wr x (+ logit_bias);  p = softmax(r)            (fp32)

@@ -15,6 +15,7 @@ MM_DTYPE_F32, MM_DTYPE_BF16 = 0, 1
 MM_PATH_AUTO, MM_PATH_TENSOR, MM_PATH_STREAM, MM_PATH_SIMT = 0, 1, 2, 3
 MM_MAX_EXPERTS = 64
 MM_MAX_TOPK = 8
+MM_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _vp, _i32, _i64, _f32, _sz = C.c_void_p, C.c_int, C.c_int64, C.c_float, C.c_size_t
 _pp = C.POINTER(C.c_void_p)
@@ -28,6 +29,7 @@ SIGNATURES = {
     "mm_swiglu_ffn": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _vp, _sz, _vp]),
     "mm_swiglu_ffn_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _vp, _sz, _vp,
                                 _i32]),
+    "mm_swiglu_ffn_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _vp]),
     "mm_moe_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32, _i32, _i32]),
     "mm_moe_forward": (_i32, [_vp, _vp, _pp, _pp, _pp, _i64, _i32, _i32, _i32, _i32, _f32, _i32,
                               _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),

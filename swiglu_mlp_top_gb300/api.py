@@ -72,6 +72,23 @@ def swiglu_ffn(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Te
     return out
 
 
+def swiglu_ffn_noalloc(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Tensor, *,
+                       out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """mm_swiglu_ffn_noalloc: the dense FFN using the library's fixed device
+    scratch instead of a workspace (for callers that cannot allocate)."""
+    lib = L.load()
+    T, H = x.shape
+    I = Wg.shape[0]
+    dt = _dtype_code(x)
+    if out is None:
+        out = torch.empty_like(x)
+    rc = lib.mm_swiglu_ffn_noalloc(
+        _dev(x, "x"), _dev(Wg, "Wg", x.dtype), _dev(Wu, "Wu", x.dtype), _dev(Wd, "Wd", x.dtype),
+        _dev(out, "out", x.dtype), T, H, I, dt, _stream(stream))
+    L.check(rc, "mm_swiglu_ffn_noalloc")
+    return out
+
+
 def moe_forward(x: torch.Tensor, Wr: torch.Tensor, Wg: Sequence[torch.Tensor],
                 Wu: Sequence[torch.Tensor], Wd: Sequence[torch.Tensor], k: int, coef: float, *,
                 logit_bias: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
