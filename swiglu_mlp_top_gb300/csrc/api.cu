@@ -1,5 +1,6 @@
 // C ABI (include/mm.h): argument checks, workspace layout, kernel sequencing.
 // Every entry point only enqueues work on the caller's stream.
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -54,7 +55,14 @@ MoeLayout moe_layout(int64_t T, int H, int I, int E, int k, int dtype) {
   L.xp = off;       off += align_up(es * rows * H);
   L.h = off;        off += align_up(h_bytes(dtype) * rows * I);
   L.acc32 = off;    if (k >= 2 && dtype == kDtypeBF16) off += align_up(4 * static_cast<size_t>(T) * H);
-  L.wd16 = off;     if (dtype == kDtypeBF16) off += align_up(2 * static_cast<size_t>(E) * H * I);
+  // bf16: fp16 copy of the E down matrices (tensor path) or, for decode-sized
+  // T, the fp32 h of the streaming path; whichever is larger
+  L.wd16 = off;
+  if (dtype == kDtypeBF16) {
+    size_t need = 2 * static_cast<size_t>(E) * H * I;
+    if (T <= kDecodeMaxT) need = std::max(need, 4 * rows * static_cast<size_t>(I));
+    off += align_up(need);
+  }
   L.total = off;
   return L;
 }
@@ -86,13 +94,18 @@ bool valid_dtype(int dtype) { return dtype == kDtypeF32 || dtype == kDtypeBF16; 
 // bf16 tensor-core / streaming kernels tile K and N by 64
 bool tensor_shape_ok(int H, int I) { return H % 64 == 0 && I % 64 == 0; }
 
+// AUTO: fp32 -> CUDA-core kernels; bf16 -> weight streaming for decode-sized
+// T (every weight row read once), tensor cores otherwise.
 int resolve_path(int path, int dtype, int64_t T) {
   if (path == MM_PATH_AUTO) {
     if (dtype == kDtypeF32) return MM_PATH_SIMT;
-    (void)T;
-    return MM_PATH_TENSOR;
+    return T <= kDecodeMaxT ? MM_PATH_STREAM : MM_PATH_TENSOR;
   }
   return path;
+}
+
+bool stream_shape_ok(int64_t T, int H, int I) {
+  return T <= kDecodeMaxT && H <= kDecodeMaxK && I <= kDecodeMaxK;
 }
 
 inline char* ws_at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
@@ -181,14 +194,26 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
   if (!workspace || !aligned16(workspace)) return MM_ERR_WORKSPACE;
   if (workspace_bytes < dense_ws_bytes(T, H, I, dtype)) return MM_ERR_WORKSPACE;
   const int p = resolve_path(path, dtype, T);
-  if ((p == MM_PATH_TENSOR || p == MM_PATH_STREAM) &&
-      (dtype != kDtypeBF16 || !tensor_shape_ok(H, I)))
+  if (p == MM_PATH_TENSOR && (dtype != kDtypeBF16 || !tensor_shape_ok(H, I)))
     return MM_ERR_UNSUPPORTED;
-  if (p == MM_PATH_STREAM) return MM_ERR_UNSUPPORTED;   // decode kernels: not in this build yet
+  if (p == MM_PATH_STREAM && !stream_shape_ok(T, H, I)) return MM_ERR_UNSUPPORTED;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
   void* h = ws_at(workspace, sizeof(WsHeader));
+  if (p == MM_PATH_STREAM) {
+    // fp32 h [T, I] fits in the workspace's h + Wd-copy area for T <= H
+    const void* wg1[1] = {Wg};
+    const void* wu1[1] = {Wu};
+    const void* wd1[1] = {Wd};
+    cudaError_t e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
+      return launch_stream_ffn(dtype, x, wg1, wu1, wd1, nullptr, nullptr, static_cast<int>(T), H,
+                               I, 1, 1, static_cast<float*>(h), y, st);
+    });
+    g_launches.fetch_add(1, std::memory_order_relaxed);   // the stream path launches two kernels
+    if (e != cudaSuccess) return cuda_fail(e, "stream ffn");
+    return MM_OK;
+  }
   GroupRows g{nullptr, 1, static_cast<int>(T), 1};
   DownEpilogue ep{y, nullptr, nullptr, nullptr, 1, kCombineStore};
   const void* wg[1] = {Wg};
@@ -266,10 +291,9 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
   const MoeLayout L = moe_layout(T, H, I, E, k, dtype);
   if (workspace_bytes < L.total) return MM_ERR_WORKSPACE;
   const int p = resolve_path(path, dtype, T);
-  if ((p == MM_PATH_TENSOR || p == MM_PATH_STREAM) &&
-      (dtype != kDtypeBF16 || !tensor_shape_ok(H, I)))
+  if (p == MM_PATH_TENSOR && (dtype != kDtypeBF16 || !tensor_shape_ok(H, I)))
     return MM_ERR_UNSUPPORTED;
-  if (p == MM_PATH_STREAM) return MM_ERR_UNSUPPORTED;   // decode kernels: not in this build yet
+  if (p == MM_PATH_STREAM && !stream_shape_ok(T, H, I)) return MM_ERR_UNSUPPORTED;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
@@ -294,6 +318,18 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
                              aux_loss, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "route_scan");
+  if (p == MM_PATH_STREAM) {
+    // decode-sized: stream the selected experts' weights; fp32 h [T*k, I]
+    // lives in the Xp/h area (fp32) or the fp16 Wd-copy area (bf16)
+    float* hdec = reinterpret_cast<float*>(ws_at(workspace, dtype == kDtypeF32 ? L.h : L.wd16));
+    e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
+      return launch_stream_ffn(dtype, x, Wg, Wu, Wd, topk_idx, topk_w, static_cast<int>(T), H, I,
+                               E, k, hdec, y, st);
+    });
+    g_launches.fetch_add(1, std::memory_order_relaxed);   // the stream path launches two kernels
+    if (e != cudaSuccess) return cuda_fail(e, "stream ffn");
+    return MM_OK;
+  }
   e = counted_launch(MM_KERNEL_DISPATCH, st, [&] {
     return launch_dispatch(dtype, x, T, H, E, k, topk_idx, blk_base, offsets, perm, xp, st);
   });

@@ -15,6 +15,15 @@ constexpr int kRouteTokensPerBlock = 64;    // 8 tokens per warp
 constexpr int kScanThreads = 512;
 constexpr int kMaxGroups = MM_MAX_EXPERTS * MM_MAX_TOPK;     // (slot, expert) groups
 
+// Decode-sized calls (T <= kDecodeMaxT) stream each weight row once.
+constexpr int kDecodeMaxT = 8;
+constexpr int kDecodeMaxK = 4096;           // H and I limits of the streaming kernels
+
+// Per-expert device pointers passed by value to a kernel.
+struct PtrArray {
+  const void* p[MM_MAX_EXPERTS];
+};
+
 // Tensor-core GEMM geometry (tcgen05 over a CTA pair; the rest in gemm_tc.cu).
 constexpr int kTcBM = 128;                  // rows per CTA (TMEM lanes)
 constexpr int kTcBK = 64;                   // K per stage: one 128-byte swizzle row of 16-bit data
@@ -82,6 +91,14 @@ cudaError_t launch_down_simt(int dtype, const void* h, int64_t a_rows, int H, in
 // into one contiguous destination.
 cudaError_t launch_convert_bf16_to_f16(const void* const* src, int n_mat, int64_t per_matrix,
                                        void* dst, cudaStream_t st);
+
+// Decode-sized FFN on the CUDA cores (T <= kDecodeMaxT): gate/up into the
+// fp32 buffer hdec ([T*k, I], or [T, I] dense), then down + slot-ordered
+// combine into y.  topk_idx == nullptr means the dense FFN (one weight set).
+cudaError_t launch_stream_ffn(int dtype, const void* x, const void* const* Wg,
+                              const void* const* Wu, const void* const* Wd,
+                              const int32_t* topk_idx, const float* topk_w, int T, int H, int I,
+                              int E, int k, float* hdec, void* y, cudaStream_t st);
 
 cudaError_t launch_watchdog_selftest(WsHeader* hdr, uint32_t limit_us, cudaStream_t st);
 

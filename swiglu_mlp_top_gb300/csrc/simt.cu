@@ -12,10 +12,6 @@ namespace mm {
 
 constexpr int kSimtBM = 32, kSimtBN = 32, kSimtBK = 32, kSimtThreads = 256;
 
-struct PtrArray {
-  const void* p[MM_MAX_EXPERTS];
-};
-
 template <typename T>
 __device__ __forceinline__ float ld_f32(const T* p);
 template <>

@@ -132,6 +132,47 @@ def test_dense_empty_input():
     assert y.shape == (0, 256)
 
 
+# ------------------------------------------------------------------ decode streaming path
+@pytest.mark.parametrize("T", [1, 3, 8])
+def test_dense_stream_path(T):
+    inp = make_inputs(T, 768, 2432, "bf16", seed=40 + T)
+    g = to_dev(inp)
+    y = mm.swiglu_ffn(g["x"], g["Wg"], g["Wu"], g["Wd"], path="stream")
+    ref = oracle.swiglu_ffn(*[to_f64(inp[n]) for n in ("x", "Wg", "Wu", "Wd")])
+    assert rel_err(y.double().cpu().numpy(), ref) <= Y_TOL["bf16"]
+
+
+@pytest.mark.parametrize("T,E,k,bias", [(1, 8, 2, None), (4, 8, 2, (1.5, 0.5, 0, 0, 0, 0, 0, 0)),
+                                        (8, 4, 1, None), (5, 6, 3, None)])
+def test_moe_stream_path(T, E, k, bias):
+    full_moe_check(moe_inputs(T, 768, 2432, E, "bf16", seed=50 + T, bias=bias), k, 0.01, "bf16",
+                   path="stream")
+
+
+def test_stream_path_f32_tiny():
+    inp = moe_inputs(7, 64, 256, 4, "f32", seed=60)
+    full_moe_check(inp, 2, 0.01, "f32", path="stream")
+    inp = make_inputs(5, 64, 256, "f32", seed=61)
+    g = to_dev(inp)
+    y = mm.swiglu_ffn(g["x"], g["Wg"], g["Wu"], g["Wd"], path="stream")
+    ref = oracle.swiglu_ffn(*[to_f64(inp[n]) for n in ("x", "Wg", "Wu", "Wd")])
+    assert rel_err(y.double().cpu().numpy(), ref) <= Y_TOL["f32"]
+
+
+@pytest.mark.parametrize("T", [1, 4, 16, 64])
+def test_decode_workloads(T):
+    """The decode-shaped workloads at full size, in the launch configuration the
+    benchmark uses (path chosen automatically)."""
+    w = WORKLOADS[f"decode_moe_e8k2_t{T}"]
+    full_moe_check(make_workload_inputs(w), w.k, w.coef, "bf16")
+    w = WORKLOADS[f"decode_dense_t{T}"]
+    inp = make_workload_inputs(w)
+    g = to_dev(inp)
+    y = mm.swiglu_ffn(g["x"], g["Wg"], g["Wu"], g["Wd"])
+    ref = oracle.swiglu_ffn(*[to_f64(inp[n]) for n in ("x", "Wg", "Wu", "Wd")])
+    assert rel_err(y.double().cpu().numpy(), ref) <= Y_TOL["bf16"]
+
+
 # ------------------------------------------------------------------ full-size workloads
 def _sample_rows(T, n=2048, seed=0):
     r = np.random.default_rng(seed)
