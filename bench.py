@@ -36,6 +36,11 @@ METRIC = "MoE/FFN forward tokens/s and TFLOP/s on 1 GB300; % of bf16 tensor or H
 L2_BYTES = 129 * 1024 * 1024
 DECODE_MAX_T = 8          # token counts the library streams weights for
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
+# gate/up GEMM, from an ncu capture of the current kernel on this workload;
+# None where no capture of the current kernel exists.
+GATEUP_TRAFFIC_BYTES = {"moe_e8k2_t16384_skew": 162.850816e6 + 128.985088e6}
+
 
 def algorithmic_flops(w, T=None) -> float:
     """T * (k * 6 * H * I + 2 * H * E): the three GEMMs per assignment plus
@@ -318,7 +323,8 @@ def run_our_arm(args, w):
         achieved = gate_flops / (k_ms / 1e3) / 1e12
         roof = {"kernel": "grouped_gemm_kernel<gate/up> (tcgen05 2-SM GEMM + SwiGLU epilogue)",
                 "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "traffic": GATEUP_TRAFFIC_BYTES.get(w.name),
                 "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)",
                 "kernel_ms": k_ms, "launches_timed": nl.value,
                 "flops_per_launch": gate_flops}
