@@ -104,8 +104,9 @@ int resolve_path(int path, int dtype, int64_t T) {
   return path;
 }
 
-bool stream_shape_ok(int64_t T, int H, int I) {
-  return T <= kDecodeMaxT && H <= kDecodeMaxK && I <= kDecodeMaxK;
+bool stream_shape_ok(int64_t T, int H, int I, int dtype) {
+  return dtype == kDtypeBF16 && T <= kDecodeMaxT &&
+         decode_smem_bytes(static_cast<int>(T), H, I) <= 200 * 1024;
 }
 
 inline char* ws_at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
@@ -196,7 +197,7 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
   const int p = resolve_path(path, dtype, T);
   if (p == MM_PATH_TENSOR && (dtype != kDtypeBF16 || !tensor_shape_ok(H, I)))
     return MM_ERR_UNSUPPORTED;
-  if (p == MM_PATH_STREAM && !stream_shape_ok(T, H, I)) return MM_ERR_UNSUPPORTED;
+  if (p == MM_PATH_STREAM && !stream_shape_ok(T, H, I, dtype)) return MM_ERR_UNSUPPORTED;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
@@ -207,8 +208,8 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
     const void* wu1[1] = {Wu};
     const void* wd1[1] = {Wd};
     cudaError_t e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
-      return launch_stream_ffn(dtype, x, wg1, wu1, wd1, nullptr, nullptr, static_cast<int>(T), H,
-                               I, 1, 1, static_cast<float*>(h), y, st);
+      return launch_decode_ffn(x, nullptr, nullptr, wg1, wu1, wd1, static_cast<int>(T), H, I, 1, 1,
+                               0.f, nullptr, nullptr, nullptr, static_cast<float*>(h), y, hdr, st);
     });
     g_launches.fetch_add(1, std::memory_order_relaxed);   // the stream path launches two kernels
     if (e != cudaSuccess) return cuda_fail(e, "stream ffn");
@@ -293,7 +294,7 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
   const int p = resolve_path(path, dtype, T);
   if (p == MM_PATH_TENSOR && (dtype != kDtypeBF16 || !tensor_shape_ok(H, I)))
     return MM_ERR_UNSUPPORTED;
-  if (p == MM_PATH_STREAM && !stream_shape_ok(T, H, I)) return MM_ERR_UNSUPPORTED;
+  if (p == MM_PATH_STREAM && !stream_shape_ok(T, H, I, dtype)) return MM_ERR_UNSUPPORTED;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
@@ -308,6 +309,18 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
   float* acc32 = (dtype == kDtypeF32) ? static_cast<float*>(y)
                                       : reinterpret_cast<float*>(ws_at(workspace, L.acc32));
 
+  if (p == MM_PATH_STREAM) {
+    // decode-sized: the routing runs inside the two streaming kernels; fp32
+    // h [T*k, I] lives in the fp16 Wd-copy area, which is sized for it
+    float* hdec = reinterpret_cast<float*>(ws_at(workspace, L.wd16));
+    cudaError_t e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
+      return launch_decode_ffn(x, Wr, logit_bias, Wg, Wu, Wd, static_cast<int>(T), H, I, E, k,
+                               coef, topk_idx, topk_w, aux_loss, hdec, y, hdr, st);
+    });
+    g_launches.fetch_add(1, std::memory_order_relaxed);   // the stream path launches two kernels
+    if (e != cudaSuccess) return cuda_fail(e, "decode ffn");
+    return MM_OK;
+  }
   cudaError_t e = counted_launch(MM_KERNEL_ROUTER, st, [&] {
     return launch_router(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w, blk_cnt,
                          blk_prob, st);
@@ -318,18 +331,6 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
                              aux_loss, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "route_scan");
-  if (p == MM_PATH_STREAM) {
-    // decode-sized: stream the selected experts' weights; fp32 h [T*k, I]
-    // lives in the Xp/h area (fp32) or the fp16 Wd-copy area (bf16)
-    float* hdec = reinterpret_cast<float*>(ws_at(workspace, dtype == kDtypeF32 ? L.h : L.wd16));
-    e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
-      return launch_stream_ffn(dtype, x, Wg, Wu, Wd, topk_idx, topk_w, static_cast<int>(T), H, I,
-                               E, k, hdec, y, st);
-    });
-    g_launches.fetch_add(1, std::memory_order_relaxed);   // the stream path launches two kernels
-    if (e != cudaSuccess) return cuda_fail(e, "stream ffn");
-    return MM_OK;
-  }
   e = counted_launch(MM_KERNEL_DISPATCH, st, [&] {
     return launch_dispatch(dtype, x, T, H, E, k, topk_idx, blk_base, offsets, perm, xp, st);
   });

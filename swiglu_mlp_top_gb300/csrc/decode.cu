@@ -1,67 +1,62 @@
-// Decode-sized forward (T <= kDecodeMaxT tokens): weight-streaming kernels
-// on the CUDA cores.  Each weight row is read from HBM exactly once with
-// coalesced 16-byte loads and kept in registers while every token that needs
-// it is applied, so the time is the weights' HBM traffic.  For the MoE only
-// the experts some token selected are read.
+// Decode-sized forward (T <= kDecodeMaxT tokens): weight streaming on the
+// CUDA cores in two kernels.  Every weight row is read from HBM once, by the
+// bulk-copy engine into shared memory, while the previous slice is being used;
+// for the MoE only the experts some token selected are read.
 //
-//   gate/up:  h[a, i] = SiLU(Wg_e[i] . x_t) * (Wu_e[i] . x_t)   for every
-//             assignment a = (t, s) with expert e     (lesson 13 §0/§1.2)
-//   down:     y[t, j] = sum_s alpha_{t,s} * (Wd_{e_s}[j] . h[t, s])  in slot
-//             order, fp32, rounded once (lesson 13 §0 MoE equation, step 5)
+//   A  route (MoE) + gate/up:  h[a, i] = SiLU(Wg_e[i] . x_t) * (Wu_e[i] . x_t)
+//      for every assignment a = (t, s) of expert e          (lesson 13 §0/§1.2)
+//   B  route (MoE) + down + combine:
+//      y[t, j] = sum_s alpha_{t,s} (Wd_{e_s}[j] . h[t, s])  in slot order, fp32,
+//      rounded once                             (lesson 13 §0 MoE equation, step 5)
+//
+// The routing (logits, softmax, top-k, alpha; lesson 13 §1.5, chapter 4 §4.3)
+// is cheap at this size, so every CTA computes it for all T tokens with the
+// same code and order, and all CTAs agree on it; block 0 of kernel A writes
+// topk_idx, topk_w and the aux loss (lesson 13 §1.6).  Kernel B is launched as
+// a programmatic dependent of A: it computes its routing and starts streaming
+// its Wd rows while A runs, and waits for A's h only before using it.
 #include "mm_kernels.cuh"
 
 namespace mm {
 
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kUpRows = 16;                 // Wg / Wu rows per gate/up slice (2 per warp)
+constexpr int kDnRows = 4;                  // output rows per down unit
 
-// 8 consecutive elements of a row, kept packed in registers.
-template <typename T> struct Pack8;
-template <> struct Pack8<__nv_bfloat16> { uint4 r; };
-template <> struct Pack8<float> { uint4 r0, r1; };
+struct DecodeArgs {
+  const void* x;            // [T, H] bf16
+  const void* Wr;           // [E, H] bf16, or nullptr (dense)
+  const float* bias;        // [E] or nullptr
+  PtrArray wg, wu, wd;      // per expert
+  int T, H, I, E, k;
+  float coef;
+  int32_t* topk_idx;        // written by block 0 of kernel A (MoE)
+  float* topk_w;
+  float* aux_loss;
+  float* h;                 // [T*k, I] fp32 scratch (dense: [T, I])
+  void* y;                  // [T, H] bf16
+  WsHeader* hdr;
+};
 
-__device__ __forceinline__ void ld_pack(const __nv_bfloat16* p, Pack8<__nv_bfloat16>& v) {
-  v.r = __ldg(reinterpret_cast<const uint4*>(p));
-}
-__device__ __forceinline__ void ld_pack(const float* p, Pack8<float>& v) {
-  v.r0 = __ldg(reinterpret_cast<const uint4*>(p));
-  v.r1 = __ldg(reinterpret_cast<const uint4*>(p) + 1);
-}
-__device__ __forceinline__ void unpack(const Pack8<__nv_bfloat16>& v, float (&f)[8]) {
-  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v.r);
+// Routing tables shared by the CTA.
+struct DecRoute {
+  int nA;                                   // assignments (MoE: T*k, dense: T)
+  int n_touched;
+  int touched[MM_MAX_EXPERTS];              // ascending expert ids
+  int sel_e[kDecodeMaxT * MM_MAX_TOPK];     // expert of assignment a = t*k + s
+  float sel_a[kDecodeMaxT * MM_MAX_TOPK];   // its alpha
+  float prob[kDecodeMaxT][MM_MAX_EXPERTS];
+};
+
+__device__ __forceinline__ void cvt8(const uint4& raw, float (&f)[8]) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float2 q = __bfloat1622float2(b[i]);
     f[2 * i] = q.x;
     f[2 * i + 1] = q.y;
   }
-}
-__device__ __forceinline__ void unpack(const Pack8<float>& v, float (&f)[8]) {
-  f[0] = __uint_as_float(v.r0.x); f[1] = __uint_as_float(v.r0.y);
-  f[2] = __uint_as_float(v.r0.z); f[3] = __uint_as_float(v.r0.w);
-  f[4] = __uint_as_float(v.r1.x); f[5] = __uint_as_float(v.r1.y);
-  f[6] = __uint_as_float(v.r1.z); f[7] = __uint_as_float(v.r1.w);
-}
-
-template <typename T>
-__device__ __forceinline__ void load8f(const T* p, float (&v)[8]);
-template <>
-__device__ __forceinline__ void load8f<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
-  const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p));
-  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __bfloat1622float2(b[i]);
-    v[2 * i] = f.x;
-    v[2 * i + 1] = f.y;
-  }
-}
-template <>
-__device__ __forceinline__ void load8f<float>(const float* p, float (&v)[8]) {
-  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
 __device__ __forceinline__ float warp_allsum(float v) {
@@ -70,221 +65,370 @@ __device__ __forceinline__ float warp_allsum(float v) {
   return v;
 }
 
-// The experts that some assignment selected, in ascending order (dense: one
-// "expert" 0 with every token).  Written by thread 0 into shared memory.
-struct Touched {
-  int n;
-  int e[MM_MAX_EXPERTS];
-};
+// 1-D bulk copy global -> this CTA's shared memory, completion on `bar`.
+__device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(sdst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
 
-__device__ __forceinline__ void find_touched(const int32_t* topk_idx, int nA, int E, Touched* t) {
-  if (threadIdx.x == 0) {
-    uint64_t m = 0;
-    if (topk_idx == nullptr) {
-      m = 1;
-    } else {
-      for (int a = 0; a < nA; ++a) m |= 1ull << topk_idx[a];
+// Routing of all T tokens from x in shared memory.  Warp t routes token t:
+// fp32 logits (lanes split H, xor-tree sum), softmax with the maximum
+// subtracted, k sequential selections with strict '>' (equal probabilities ->
+// lower index), alpha = p / (sum_S p + 1e-20).  Dense: one weight set, every
+// token with alpha 1.
+__device__ void decode_route(const DecodeArgs& A, const __nv_bfloat16* xs, DecRoute& R) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nch = A.H / 8;
+  if (A.Wr == nullptr) {
+    if (threadIdx.x == 0) {
+      R.nA = A.T;
+      R.n_touched = 1;
+      R.touched[0] = 0;
+      for (int t = 0; t < A.T; ++t) {
+        R.sel_e[t] = 0;
+        R.sel_a[t] = 1.0f;
+      }
     }
+    __syncthreads();
+    return;
+  }
+  const __nv_bfloat16* Wr = static_cast<const __nv_bfloat16*>(A.Wr);
+  for (int t = warp; t < A.T; t += kDecWarps) {
+    for (int e = 0; e < A.E; ++e) {
+      float s = 0.f;
+      for (int c = lane; c < nch; c += 32) {
+        float xv[8], wv[8];
+        cvt8(*reinterpret_cast<const uint4*>(xs + t * A.H + c * 8), xv);
+        cvt8(__ldg(reinterpret_cast<const uint4*>(Wr + static_cast<int64_t>(e) * A.H + c * 8)), wv);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) s = fmaf(xv[q], wv[q], s);
+      }
+      s = warp_allsum(s) + (A.bias != nullptr ? A.bias[e] : 0.f);
+      if (lane == 0) R.prob[t][e] = s;          // logit for now
+    }
+    __syncwarp();
+    if (lane == 0) {
+      float m = -INFINITY;
+      for (int e = 0; e < A.E; ++e) m = fmaxf(m, R.prob[t][e]);
+      float z = 0.f;
+      for (int e = 0; e < A.E; ++e) {
+        const float v = expf(R.prob[t][e] - m);
+        R.prob[t][e] = v;
+        z += v;
+      }
+      for (int e = 0; e < A.E; ++e) R.prob[t][e] = R.prob[t][e] / z;
+      uint64_t taken = 0;
+      float sum = 0.f;
+      for (int s = 0; s < A.k; ++s) {
+        int best = -1;
+        float bp = 0.f;
+        for (int e = 0; e < A.E; ++e) {
+          const float p = R.prob[t][e];
+          if (!((taken >> e) & 1ull) && (best < 0 || p > bp)) {
+            best = e;
+            bp = p;
+          }
+        }
+        taken |= 1ull << best;
+        R.sel_e[t * A.k + s] = best;
+        R.sel_a[t * A.k + s] = bp;
+        sum += bp;
+      }
+      for (int s = 0; s < A.k; ++s) R.sel_a[t * A.k + s] = R.sel_a[t * A.k + s] / (sum + 1e-20f);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    R.nA = A.T * A.k;
+    uint64_t m = 0;
+    for (int a = 0; a < R.nA; ++a) m |= 1ull << R.sel_e[a];
     int n = 0;
-    for (int e = 0; e < E; ++e)
-      if ((m >> e) & 1ull) t->e[n++] = e;
-    t->n = n;
+    for (int e = 0; e < A.E; ++e)
+      if ((m >> e) & 1ull) R.touched[n++] = e;
+    R.n_touched = n;
   }
   __syncthreads();
 }
 
-// ---------------------------------------------------------------- gate/up
-// Work item = (touched expert, block of kDecWarps rows); warp w owns row
-// i = block*kDecWarps + w and holds its Wg / Wu row slices in registers.
-template <typename Tin, int MAXC>
+__device__ __forceinline__ void load_x(const DecodeArgs& A, __nv_bfloat16* xs) {
+  const int n16 = A.T * A.H / 8;
+  for (int i = threadIdx.x; i < n16; i += blockDim.x)
+    reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(A.x) + i);
+}
+
+// ---------------------------------------------------------------- kernel A
+// Work unit = (touched expert, slice of kUpRows rows of Wg / Wu).  The CTA
+// walks its units with two shared-memory buffers: the bulk copy of its next
+// unit is in flight while the current one is computed.  Warp w owns rows
+// 2w, 2w+1 of the slice; lanes split H into 8-element chunks.
 __global__ void __launch_bounds__(kDecThreads)
-stream_gateup_kernel(const Tin* __restrict__ x, const PtrArray wg, const PtrArray wu,
-                     const int32_t* __restrict__ topk_idx, int T, int H, int I, int E, int k,
-                     float* __restrict__ hdec) {
-  __shared__ Touched tch;
-  const int nA = (topk_idx != nullptr) ? T * k : T;
-  find_touched(topk_idx, nA, E, &tch);
+decode_gateup_kernel(const DecodeArgs A) {
+  extern __shared__ __align__(128) unsigned char dsm[];
+  __shared__ DecRoute R;
+  __shared__ __align__(8) uint64_t bar[2];
+  const int H = A.H, I = A.I;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nch = H / 8;
-  const int blocks = (I + kDecWarps - 1) / kDecWarps;
-  const int items = tch.n * blocks;
-  for (int item = blockIdx.x; item < items; item += gridDim.x) {
-    const int e = tch.e[item / blocks];
-    const int i = (item % blocks) * kDecWarps + warp;
-    if (i >= I) continue;                                  // warp-uniform
-    const Tin* g_row = static_cast<const Tin*>(wg.p[e]) + static_cast<int64_t>(i) * H;
-    const Tin* u_row = static_cast<const Tin*>(wu.p[e]) + static_cast<int64_t>(i) * H;
-    Pack8<Tin> gw[MAXC], uw[MAXC];
-#pragma unroll
-    for (int c = 0; c < MAXC; ++c) {
-      const int ch = lane + 32 * c;
-      if (ch < nch) {
-        ld_pack(g_row + ch * 8, gw[c]);
-        ld_pack(u_row + ch * 8, uw[c]);
-      }
+  const size_t slice_bytes = static_cast<size_t>(kUpRows) * H * 2;   // one of Wg / Wu
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(dsm);
+  unsigned char* buf = dsm + ((static_cast<size_t>(A.T) * H * 2 + 127) & ~size_t(127));
+
+  // the dependent grid (kernel B) may start its own prologue now
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+  }
+  load_x(A, xs);
+  __syncthreads();
+  decode_route(A, xs, R);
+
+  if (blockIdx.x == 0 && A.Wr != nullptr) {
+    // routing outputs and aux = E*coef*sum_e (count_e/T)(P_e/T)
+    for (int a = threadIdx.x; a < R.nA; a += blockDim.x) {
+      A.topk_idx[a] = R.sel_e[a];
+      A.topk_w[a] = R.sel_a[a];
     }
-    for (int a = 0; a < nA; ++a) {
-      if (topk_idx != nullptr && topk_idx[a] != e) continue;   // uniform: same a for the warp
-      const int t = (topk_idx != nullptr) ? a / k : a;
-      const Tin* xr = x + static_cast<int64_t>(t) * H;
-      float g = 0.f, u = 0.f;
-#pragma unroll
-      for (int c = 0; c < MAXC; ++c) {
-        const int ch = lane + 32 * c;
-        if (ch < nch) {
-          float xv[8], gf[8], uf[8];
-          load8f(xr + ch * 8, xv);
-          unpack(gw[c], gf);
-          unpack(uw[c], uf);
+    if (threadIdx.x == 0) {
+      float acc = 0.f;
+      for (int e = 0; e < A.E; ++e) {
+        int c = 0;
+        float P = 0.f;
+        for (int a = 0; a < R.nA; ++a) c += (R.sel_e[a] == e);
+        for (int t = 0; t < A.T; ++t) P += R.prob[t][e];
+        acc = fmaf(static_cast<float>(c), P, acc);
+      }
+      const float invT = 1.0f / static_cast<float>(A.T);
+      *A.aux_loss = static_cast<float>(A.E) * A.coef * acc * invT * invT;
+    }
+  }
+
+  const int slices = (I + kUpRows - 1) / kUpRows;
+  const int units = R.n_touched * slices;
+  auto issue = [&](int unit, int b) {
+    const int e = R.touched[unit / slices];
+    const int r0 = (unit % slices) * kUpRows;
+    const int rows = min(kUpRows, I - r0);
+    const uint32_t bytes = static_cast<uint32_t>(rows) * H * 2;
+    unsigned char* dst = buf + b * 2 * slice_bytes;
+    mbar_arrive_expect_tx(&bar[b], 2 * bytes);
+    bulk_load(dst, static_cast<const __nv_bfloat16*>(A.wg.p[e]) + static_cast<int64_t>(r0) * H,
+              bytes, &bar[b]);
+    bulk_load(dst + slice_bytes,
+              static_cast<const __nv_bfloat16*>(A.wu.p[e]) + static_cast<int64_t>(r0) * H, bytes,
+              &bar[b]);
+  };
+  int u = blockIdx.x;
+  bool inflight[2] = {false, false};           // tracked by thread 0, which issues
+  if (threadIdx.x == 0 && u < units) {
+    issue(u, 0);
+    inflight[0] = true;
+  }
+  uint32_t phase[2] = {0, 0};
+  for (int it = 0; u < units; u += gridDim.x, ++it) {
+    const int b = it & 1;
+    const int nxt = u + static_cast<int>(gridDim.x);
+    __syncthreads();                           // buffer b^1 is no longer being read
+    if (threadIdx.x == 0 && nxt < units) {
+      issue(nxt, b ^ 1);
+      inflight[b ^ 1] = true;
+    }
+    const bool ok = mbar_wait(&bar[b], phase[b], nullptr, A.hdr, 20);
+    if (!__syncthreads_and(ok)) break;
+    phase[b] ^= 1;
+    inflight[b] = false;
+    const int e = R.touched[u / slices];
+    const int r0 = (u % slices) * kUpRows;
+    const __nv_bfloat16* gsl = reinterpret_cast<const __nv_bfloat16*>(buf + b * 2 * slice_bytes);
+    const __nv_bfloat16* usl = gsl + kUpRows * H;
+    for (int rr = 0; rr < 2; ++rr) {
+      const int row = 2 * warp + rr;
+      const int i = r0 + row;
+      if (i >= I) break;
+      for (int a = 0; a < R.nA; ++a) {
+        if (R.sel_e[a] != e) continue;         // uniform across the warp
+        const int t = (A.Wr != nullptr) ? a / A.k : a;
+        float g = 0.f, uu = 0.f;
+        for (int c = lane; c < H / 8; c += 32) {
+          float xv[8], gv[8], uv[8];
+          cvt8(*reinterpret_cast<const uint4*>(xs + t * H + c * 8), xv);
+          cvt8(*reinterpret_cast<const uint4*>(gsl + row * H + c * 8), gv);
+          cvt8(*reinterpret_cast<const uint4*>(usl + row * H + c * 8), uv);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            g = fmaf(gf[q], xv[q], g);
-            u = fmaf(uf[q], xv[q], u);
+            g = fmaf(gv[q], xv[q], g);
+            uu = fmaf(uv[q], xv[q], uu);
           }
         }
+        g = warp_allsum(g);
+        uu = warp_allsum(uu);
+        if (lane == 0) A.h[static_cast<int64_t>(a) * I + i] = silu_f32(g) * uu;
       }
-      g = warp_allsum(g);
-      u = warp_allsum(u);
-      if (lane == 0) hdec[static_cast<int64_t>(a) * I + i] = silu_f32(g) * u;
     }
+  }
+  // after a wait gave up, let copies still in flight land before exiting
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b)
+      if (inflight[b]) mbar_wait(&bar[b], phase[b], nullptr, nullptr, 22);
   }
 }
 
-// ---------------------------------------------------------------- down + combine
-// Work item = block of kRowsPerItem output rows j.  For every (touched
-// expert, row) pair a warp streams Wd_e[j, :] once and forms the dot products
-// with the h rows of that expert's assignments; the block then sums each
-// token's slots in order.
-constexpr int kRowsPerItem = 4;
-
-template <typename Tout, int MAXC>
+// ---------------------------------------------------------------- kernel B
+// Unit = kDnRows output rows j.  For each touched expert the CTA bulk-copies
+// Wd_e[j0 : j0 + kDnRows, :] into a double-buffered slot (the first copy is
+// issued before waiting for kernel A) and forms, for every assignment of that
+// expert, the dot products with its h row; the block then sums each token's
+// slots in order and rounds once.
 __global__ void __launch_bounds__(kDecThreads)
-stream_down_kernel(const float* __restrict__ hdec, const PtrArray wd,
-                   const int32_t* __restrict__ topk_idx, const float* __restrict__ topk_w, int T,
-                   int H, int I, int E, int k, Tout* __restrict__ y) {
-  __shared__ Touched tch;
-  __shared__ float part[kDecodeMaxT * MM_MAX_TOPK][kRowsPerItem];
-  const int nA = (topk_idx != nullptr) ? T * k : T;
-  find_touched(topk_idx, nA, E, &tch);
+decode_down_kernel(const DecodeArgs A) {
+  extern __shared__ __align__(128) unsigned char dsm[];
+  __shared__ DecRoute R;
+  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ float part[kDecodeMaxT * MM_MAX_TOPK][kDnRows];
+  const int H = A.H, I = A.I;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nch = I / 8;
-  const int items = (H + kRowsPerItem - 1) / kRowsPerItem;
-  for (int item = blockIdx.x; item < items; item += gridDim.x) {
-    const int j0 = item * kRowsPerItem;
-    const int pairs = tch.n * kRowsPerItem;
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(dsm);
+  unsigned char* buf = dsm + ((static_cast<size_t>(A.T) * H * 2 + 127) & ~size_t(127));
+  const size_t slot_bytes = static_cast<size_t>(kDnRows) * I * 2;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+  }
+  load_x(A, xs);
+  __syncthreads();
+  decode_route(A, xs, R);
+
+  const int units = (H + kDnRows - 1) / kDnRows;
+  const int unit = blockIdx.x;
+  const bool active = unit < units;            // uniform across the block
+  const int j0 = unit * kDnRows;
+  const int rows = active ? min(kDnRows, H - j0) : 0;
+  auto issue = [&](int ti, int b) {
+    const int e = R.touched[ti];
+    const uint32_t bytes = static_cast<uint32_t>(rows) * I * 2;
+    mbar_arrive_expect_tx(&bar[b], bytes);
+    bulk_load(buf + b * slot_bytes,
+              static_cast<const __nv_bfloat16*>(A.wd.p[e]) + static_cast<int64_t>(j0) * I, bytes,
+              &bar[b]);
+  };
+  bool inflight[2] = {false, false};           // tracked by thread 0, which issues
+  if (threadIdx.x == 0 && active) {
+    issue(0, 0);
+    inflight[0] = true;
+  }
+
+  // h comes from kernel A: wait for that grid (and its memory) before reading it
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  uint32_t phase[2] = {0, 0};
+  bool ok = active;
+  for (int ti = 0; ok && ti < R.n_touched; ++ti) {
+    const int b = ti & 1;
+    __syncthreads();                           // buffer b^1 is no longer being read
+    if (threadIdx.x == 0 && ti + 1 < R.n_touched) {
+      issue(ti + 1, b ^ 1);
+      inflight[b ^ 1] = true;
+    }
+    const bool w = mbar_wait(&bar[b], phase[b], nullptr, A.hdr, 21);
+    ok = __syncthreads_and(w);
+    if (!ok) break;
+    phase[b] ^= 1;
+    inflight[b] = false;
+    const int e = R.touched[ti];
+    const __nv_bfloat16* ws = reinterpret_cast<const __nv_bfloat16*>(buf + b * slot_bytes);
+    const int pairs = rows * R.nA;             // (row, assignment) pairs over the warps
     for (int pr = warp; pr < pairs; pr += kDecWarps) {
-      const int e = tch.e[pr / kRowsPerItem];
-      const int jl = pr % kRowsPerItem;
-      const int j = j0 + jl;
-      if (j >= H) continue;
-      const Tout* d_row = static_cast<const Tout*>(wd.p[e]) + static_cast<int64_t>(j) * I;
-      Pack8<Tout> dw[MAXC];
-#pragma unroll
-      for (int c = 0; c < MAXC; ++c) {
-        const int ch = lane + 32 * c;
-        if (ch < nch) ld_pack(d_row + ch * 8, dw[c]);
+      const int jl = pr % rows, a = pr / rows;
+      if (R.sel_e[a] != e) continue;
+      const float* hr = A.h + static_cast<int64_t>(a) * I;
+      float acc = 0.f;
+      for (int c = lane; c < I / 8; c += 32) {
+        float wv[8];
+        cvt8(*reinterpret_cast<const uint4*>(ws + jl * I + c * 8), wv);
+        const float4 h0 = __ldcg(reinterpret_cast<const float4*>(hr + c * 8));
+        const float4 h1 = __ldcg(reinterpret_cast<const float4*>(hr + c * 8) + 1);
+        acc = fmaf(wv[0], h0.x, acc); acc = fmaf(wv[1], h0.y, acc);
+        acc = fmaf(wv[2], h0.z, acc); acc = fmaf(wv[3], h0.w, acc);
+        acc = fmaf(wv[4], h1.x, acc); acc = fmaf(wv[5], h1.y, acc);
+        acc = fmaf(wv[6], h1.z, acc); acc = fmaf(wv[7], h1.w, acc);
       }
-      for (int a = 0; a < nA; ++a) {
-        if (topk_idx != nullptr && topk_idx[a] != e) continue;
-        const float* hr = hdec + static_cast<int64_t>(a) * I;
-        float acc = 0.f;
-#pragma unroll
-        for (int c = 0; c < MAXC; ++c) {
-          const int ch = lane + 32 * c;
-          if (ch < nch) {
-            float hv[8], df[8];
-            load8f(hr + ch * 8, hv);
-            unpack(dw[c], df);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) acc = fmaf(df[q], hv[q], acc);
-          }
-        }
-        acc = warp_allsum(acc);
-        if (lane == 0) part[a][jl] = acc;
-      }
+      acc = warp_allsum(acc);
+      if (lane == 0) part[a][jl] = acc;
     }
-    __syncthreads();
-    const int ntok_rows = T * kRowsPerItem;
-    for (int q = threadIdx.x; q < ntok_rows; q += blockDim.x) {
-      const int t = q / kRowsPerItem, jl = q % kRowsPerItem;
-      const int j = j0 + jl;
-      if (j >= H) continue;
-      float v;
-      if (topk_idx == nullptr) {
-        v = part[t][jl];
-      } else {
-        v = 0.f;
-        for (int s = 0; s < k; ++s) v += topk_w[t * k + s] * part[t * k + s][jl];
-      }
-      y[static_cast<int64_t>(t) * H + j] = static_cast<Tout>(v);
-    }
-    __syncthreads();
+  }
+  __syncthreads();
+  if (!ok) {
+    if (threadIdx.x == 0)
+      for (int b = 0; b < 2; ++b)
+        if (inflight[b]) mbar_wait(&bar[b], phase[b], nullptr, nullptr, 23);
+    return;
+  }
+  const int kk = (A.Wr != nullptr) ? A.k : 1;
+  for (int q = threadIdx.x; q < A.T * rows; q += blockDim.x) {
+    const int t = q / rows, jl = q % rows;
+    float v = 0.f;
+    for (int s = 0; s < kk; ++s) v += R.sel_a[t * kk + s] * part[t * kk + s][jl];
+    static_cast<__nv_bfloat16*>(A.y)[static_cast<int64_t>(t) * H + j0 + jl] = __float2bfloat16_rn(v);
   }
 }
 
-static int decode_grid(int items) {
-  const int cap = 2 * num_sms();
-  return items < cap ? (items > 0 ? items : 1) : cap;
+size_t decode_smem_bytes(int T, int H, int I) {
+  const size_t xs = (static_cast<size_t>(T) * H * 2 + 127) & ~size_t(127);
+  const size_t a = xs + 2 * 2 * static_cast<size_t>(kUpRows) * H * 2;
+  const size_t b = xs + 2 * static_cast<size_t>(kDnRows) * I * 2;
+  return a > b ? a : b;
 }
 
-// Chunks of 8 elements per lane for a reduction length K: ceil(K / 256),
-// rounded up to an instantiated size.
-static int chunks_for(int K) {
-  const int c = (K + 255) / 256;
-  return c <= 1 ? 1 : c <= 2 ? 2 : c <= 4 ? 4 : c <= 8 ? 8 : c <= 12 ? 12 : 16;
-}
-
-template <typename Tx>
-static cudaError_t launch_stream_t(const void* x, const PtrArray& pg, const PtrArray& pu,
-                                   const PtrArray& pd, const int32_t* topk_idx,
-                                   const float* topk_w, int T, int H, int I, int nw, int k,
-                                   float* hdec, void* y, cudaStream_t st) {
-  const int g1 = decode_grid(nw * ((I + kDecWarps - 1) / kDecWarps));
-  const int g2 = decode_grid((H + kRowsPerItem - 1) / kRowsPerItem);
-#define MM_GU(C)                                                                              \
-  stream_gateup_kernel<Tx, C><<<g1, kDecThreads, 0, st>>>(static_cast<const Tx*>(x), pg, pu,    \
-                                                         topk_idx, T, H, I, nw, k, hdec)
-  switch (chunks_for(H)) {
-    case 1: MM_GU(1); break;
-    case 2: MM_GU(2); break;
-    case 4: MM_GU(4); break;
-    case 8: MM_GU(8); break;
-    case 12: MM_GU(12); break;
-    default: MM_GU(16); break;
-  }
-#undef MM_GU
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-#define MM_DN(C)                                                                              \
-  stream_down_kernel<Tx, C><<<g2, kDecThreads, 0, st>>>(hdec, pd, topk_idx, topk_w, T, H, I,   \
-                                                       nw, k, static_cast<Tx*>(y))
-  switch (chunks_for(I)) {
-    case 1: MM_DN(1); break;
-    case 2: MM_DN(2); break;
-    case 4: MM_DN(4); break;
-    case 8: MM_DN(8); break;
-    case 12: MM_DN(12); break;
-    default: MM_DN(16); break;
-  }
-#undef MM_DN
-  return cudaGetLastError();
-}
-
-cudaError_t launch_stream_ffn(int dtype, const void* x, const void* const* Wg,
-                              const void* const* Wu, const void* const* Wd,
-                              const int32_t* topk_idx, const float* topk_w, int T, int H, int I,
-                              int E, int k, float* hdec, void* y, cudaStream_t st) {
-  PtrArray pg, pu, pd;
-  const int nw = (topk_idx != nullptr) ? E : 1;
+cudaError_t launch_decode_ffn(const void* x, const void* Wr, const float* bias,
+                              const void* const* Wg, const void* const* Wu, const void* const* Wd,
+                              int T, int H, int I, int E, int k, float coef, int32_t* topk_idx,
+                              float* topk_w, float* aux_loss, float* hbuf, void* y, WsHeader* hdr,
+                              cudaStream_t st) {
+  DecodeArgs A;
+  memset(&A, 0, sizeof(A));
+  A.x = x;
+  A.Wr = Wr;
+  A.bias = bias;
+  const int nw = (Wr != nullptr) ? E : 1;
   for (int e = 0; e < nw; ++e) {
-    pg.p[e] = Wg[e];
-    pu.p[e] = Wu[e];
-    pd.p[e] = Wd[e];
+    A.wg.p[e] = Wg[e];
+    A.wu.p[e] = Wu[e];
+    A.wd.p[e] = Wd[e];
   }
-  if (dtype == kDtypeBF16)
-    return launch_stream_t<__nv_bfloat16>(x, pg, pu, pd, topk_idx, topk_w, T, H, I, nw, k, hdec,
-                                          y, st);
-  return launch_stream_t<float>(x, pg, pu, pd, topk_idx, topk_w, T, H, I, nw, k, hdec, y, st);
+  A.T = T; A.H = H; A.I = I; A.E = nw; A.k = (Wr != nullptr) ? k : 1; A.coef = coef;
+  A.topk_idx = topk_idx; A.topk_w = topk_w; A.aux_loss = aux_loss;
+  A.h = hbuf; A.y = y; A.hdr = hdr;
+  const size_t smem = decode_smem_bytes(T, H, I);
+  cudaError_t e = cudaFuncSetAttribute(decode_gateup_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int gridA = 2 * num_sms();
+  decode_gateup_kernel<<<gridA, kDecThreads, smem, st>>>(A);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // kernel B as a programmatic dependent of A: its prologue overlaps A
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((H + kDnRows - 1) / kDnRows);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_down_kernel, A);
 }
 
 }  // namespace mm

@@ -92,13 +92,16 @@ cudaError_t launch_down_simt(int dtype, const void* h, int64_t a_rows, int H, in
 cudaError_t launch_convert_bf16_to_f16(const void* const* src, int n_mat, int64_t per_matrix,
                                        void* dst, cudaStream_t st);
 
-// Decode-sized FFN on the CUDA cores (T <= kDecodeMaxT): gate/up into the
-// fp32 buffer hdec ([T*k, I], or [T, I] dense), then down + slot-ordered
-// combine into y.  topk_idx == nullptr means the dense FFN (one weight set).
-cudaError_t launch_stream_ffn(int dtype, const void* x, const void* const* Wg,
-                              const void* const* Wu, const void* const* Wd,
-                              const int32_t* topk_idx, const float* topk_w, int T, int H, int I,
-                              int E, int k, float* hdec, void* y, cudaStream_t st);
+// Decode-sized forward on the CUDA cores (T <= kDecodeMaxT, bf16): kernel A
+// routes (MoE: Wr != nullptr) and computes the fp32 h [T*k, I] (dense: [T, I])
+// into hbuf; kernel B, a programmatic dependent of A, forms y.  Block 0 of A
+// writes topk_idx / topk_w / aux_loss (MoE).
+size_t decode_smem_bytes(int T, int H, int I);
+cudaError_t launch_decode_ffn(const void* x, const void* Wr, const float* bias,
+                              const void* const* Wg, const void* const* Wu, const void* const* Wd,
+                              int T, int H, int I, int E, int k, float coef, int32_t* topk_idx,
+                              float* topk_w, float* aux_loss, float* hbuf, void* y, WsHeader* hdr,
+                              cudaStream_t st);
 
 cudaError_t launch_watchdog_selftest(WsHeader* hdr, uint32_t limit_us, cudaStream_t st);
 
