@@ -406,11 +406,9 @@ cudaError_t launch_decode_ffn(const void* x, const void* Wr, const float* bias,
   A.topk_idx = topk_idx; A.topk_w = topk_w; A.aux_loss = aux_loss;
   A.h = hbuf; A.y = y; A.hdr = hdr;
   const size_t smem = decode_smem_bytes(T, H, I);
-  cudaError_t e = cudaFuncSetAttribute(decode_gateup_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_gateup_kernel), smem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem));
+  e = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_down_kernel), smem);
   if (e != cudaSuccess) return e;
   const int gridA = 2 * num_sms();
   decode_gateup_kernel<<<gridA, kDecThreads, smem, st>>>(A);

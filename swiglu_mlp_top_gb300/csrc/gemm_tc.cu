@@ -428,10 +428,30 @@ static bool make_map_16(CUtensorMap* out, const void* ptr, uint64_t inner, uint6
 }
 
 int num_sms() {
-  int dev = 0, n = 0;
+  constexpr int kMaxDev = 64;
+  static int cached[kMaxDev] = {};
+  int dev = 0;
   cudaGetDevice(&dev);
+  if (dev >= 0 && dev < kMaxDev && cached[dev] > 0) return cached[dev];
+  int n = 0;
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
+  n = n > 0 ? n : 1;
+  if (dev >= 0 && dev < kMaxDev) cached[dev] = n;
+  return n;
+}
+
+cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> done;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = done.find({dev, fn});
+  if (it != done.end() && it->second >= bytes) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) done[{dev, fn}] = bytes;
+  return e;
 }
 
 // Number of CTA pairs: one per tile pair, at most one per co-resident pair.
@@ -459,7 +479,7 @@ static cudaError_t gateup_impl(const void* A, int64_t a_rows, int H, int I, cons
     if (!make_map_16(&p.b1[e], Wu[e], H, I, kN / 2, false)) return cudaErrorInvalidValue;
   }
   auto fn = grouped_gemm_kernel<kOpUp, MAXW>;
-  cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), kSmem);
   if (err != cudaSuccess) return err;
   const int n_tiles = (I + kN / 2 - 1) / (kN / 2);
   DownEpilogue none{};
@@ -478,7 +498,7 @@ static cudaError_t down_impl(const void* h, int64_t a_rows, int H, int I, const 
   for (int e = 0; e < g.n_weights; ++e)
     if (!make_map_16(&p.b0[e], Wd[e], I, H, kN / 2, true)) return cudaErrorInvalidValue;
   auto fn = grouped_gemm_kernel<kOpDown, MAXW>;
-  cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), kSmem);
   if (err != cudaSuccess) return err;
   const int n_tiles = (H + kN - 1) / kN;
   fn<<<2 * clusters_for(a_rows, g, n_tiles), kThreads, kSmem, st>>>(p, g, I, H, nullptr, ep,

@@ -105,6 +105,11 @@ cudaError_t launch_decode_ffn(const void* x, const void* Wr, const float* bias,
 
 cudaError_t launch_watchdog_selftest(WsHeader* hdr, uint32_t limit_us, cudaStream_t st);
 
-int num_sms();
+int num_sms();   // of the current device, looked up once per device
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) for `fn`, skipped when an
+// equal or larger value was already set on the current device (so that calls
+// made during stream capture issue no attribute changes after the first).
+cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes);
 
 }  // namespace mm

@@ -413,8 +413,7 @@ static cudaError_t launch_router_t(const void* x, const void* Wr, const float* b
 #define MM_ROUTER_CASE(EPAD)                                                                   \
   {                                                                                            \
     auto fn = router_kernel<Tin, EPAD>;                                                        \
-    cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
-                                           static_cast<int>(smem));                            \
+    cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem);             \
     if (err != cudaSuccess) return err;                                                        \
     fn<<<nblk, kRouteThreads, smem, st>>>(static_cast<const Tin*>(x),                          \
                                           static_cast<const Tin*>(Wr), bias, T, H, E, k,        \

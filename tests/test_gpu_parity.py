@@ -204,6 +204,38 @@ def test_moe_full_size(name):
     assert np.isfinite(y).all()
 
 
+# ------------------------------------------------------------------ CUDA graphs
+@pytest.mark.parametrize("T", [4, 600])
+def test_moe_forward_graph_capture_replays_identically(T):
+    """The forward allocates nothing and issues only stream work once warmed up,
+    so it can be captured in a CUDA graph; replays reproduce the eager result."""
+    inp = moe_inputs(T, 768, 2432, 8, "bf16", seed=70)
+    g = to_dev(inp)
+    dt = torch.bfloat16
+    ws = mm.new_workspace(mm.moe_workspace_bytes(T, 768, 2432, 8, 2, dt))
+    y = torch.empty(T, 768, dtype=dt, device="cuda")
+    idx = torch.empty(T, 2, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, 2, dtype=torch.float32, device="cuda")
+    aux = torch.empty((), dtype=torch.float32, device="cuda")
+
+    def call():
+        mm.moe_forward(g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], 2, 0.01, out=y, topk_idx=idx,
+                       topk_w=w, aux_loss=aux, workspace=ws)
+
+    call()
+    torch.cuda.synchronize()
+    eager = (y.clone(), idx.clone(), w.clone(), aux.clone())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    y.zero_()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y, eager[0]) and torch.equal(idx, eager[1])
+    assert torch.equal(w, eager[2]) and torch.equal(aux, eager[3])
+
+
 # ------------------------------------------------------------------ watchdog
 def test_watchdog_reports_timeout_and_recovers():
     ws = mm.new_workspace(256)
