@@ -34,7 +34,7 @@ from swiglu_mlp_top_gb300.inputs import WORKLOADS, make_workload_inputs  # noqa:
 DEFAULT_WORKLOAD = "moe_e8k2_t16384_skew"
 METRIC = "MoE/FFN forward tokens/s and TFLOP/s on 1 GB300; % of bf16 tensor or HBM roofline"
 L2_BYTES = 129 * 1024 * 1024
-DECODE_MAX_T = 8          # token counts the library streams weights for
+DECODE_MAX_T = 16         # token counts the library streams weights for
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
 # gate/up GEMM, from an ncu capture of the current kernel on this workload;

@@ -21,8 +21,9 @@ namespace mm {
 
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
-constexpr int kUpRows = 16;                 // Wg / Wu rows per gate/up slice (2 per warp)
+constexpr int kUpRows = kDecWarps;          // Wg / Wu rows per gate/up slice (1 per warp)
 constexpr int kDnRows = 4;                  // output rows per down unit
+constexpr int kTokGroup = 8;                // tokens whose sums a lane keeps at once
 
 struct DecodeArgs {
   const void* x;            // [T, H] bf16
@@ -47,6 +48,8 @@ struct DecRoute {
   int sel_e[kDecodeMaxT * MM_MAX_TOPK];     // expert of assignment a = t*k + s
   float sel_a[kDecodeMaxT * MM_MAX_TOPK];   // its alpha
   float prob[kDecodeMaxT][MM_MAX_EXPERTS];
+  int by_e[kDecodeMaxT * MM_MAX_TOPK];      // assignments grouped by expert, in order
+  int e_start[MM_MAX_EXPERTS + 1];          // expert e's assignments: by_e[e_start[e] ..]
 };
 
 __device__ __forceinline__ void cvt8(const uint4& raw, float (&f)[8]) {
@@ -91,7 +94,10 @@ __device__ void decode_route(const DecodeArgs& A, const __nv_bfloat16* xs, DecRo
       for (int t = 0; t < A.T; ++t) {
         R.sel_e[t] = 0;
         R.sel_a[t] = 1.0f;
+        R.by_e[t] = t;
       }
+      R.e_start[0] = 0;
+      R.e_start[1] = A.T;
     }
     __syncthreads();
     return;
@@ -150,6 +156,13 @@ __device__ void decode_route(const DecodeArgs& A, const __nv_bfloat16* xs, DecRo
     for (int e = 0; e < A.E; ++e)
       if ((m >> e) & 1ull) R.touched[n++] = e;
     R.n_touched = n;
+    int q = 0;
+    for (int e = 0; e < A.E; ++e) {
+      R.e_start[e] = q;
+      for (int a = 0; a < R.nA; ++a)
+        if (R.sel_e[a] == e) R.by_e[q++] = a;
+    }
+    R.e_start[A.E] = q;
   }
   __syncthreads();
 }
@@ -246,28 +259,51 @@ decode_gateup_kernel(const DecodeArgs A) {
     const int r0 = (u % slices) * kUpRows;
     const __nv_bfloat16* gsl = reinterpret_cast<const __nv_bfloat16*>(buf + b * 2 * slice_bytes);
     const __nv_bfloat16* usl = gsl + kUpRows * H;
-    for (int rr = 0; rr < 2; ++rr) {
-      const int row = 2 * warp + rr;
-      const int i = r0 + row;
-      if (i >= I) break;
-      for (int a = 0; a < R.nA; ++a) {
-        if (R.sel_e[a] != e) continue;         // uniform across the warp
-        const int t = (A.Wr != nullptr) ? a / A.k : a;
-        float g = 0.f, uu = 0.f;
+    const int row = warp;                      // one row of Wg and Wu per warp
+    const int i = r0 + row;
+    if (i < I) {
+      const int* list = R.by_e + R.e_start[e];   // the assignments of expert e, in order
+      const int n = R.e_start[e + 1] - R.e_start[e];
+      for (int g0 = 0; g0 < n; g0 += kTokGroup) {
+        // 2*kTokGroup independent partial sums: g_t and u_t of up to 8 tokens
+        float v[2 * kTokGroup];
+#pragma unroll
+        for (int q = 0; q < 2 * kTokGroup; ++q) v[q] = 0.f;
         for (int c = lane; c < H / 8; c += 32) {
-          float xv[8], gv[8], uv[8];
-          cvt8(*reinterpret_cast<const uint4*>(xs + t * H + c * 8), xv);
+          float gv[8], uv[8];
           cvt8(*reinterpret_cast<const uint4*>(gsl + row * H + c * 8), gv);
           cvt8(*reinterpret_cast<const uint4*>(usl + row * H + c * 8), uv);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            g = fmaf(gv[q], xv[q], g);
-            uu = fmaf(uv[q], xv[q], uu);
+          for (int tt = 0; tt < kTokGroup; ++tt) {
+            if (g0 + tt < n) {
+              const int a = list[g0 + tt];
+              const int t = (A.Wr != nullptr) ? a / A.k : a;
+              float xv[8];
+              cvt8(*reinterpret_cast<const uint4*>(xs + t * H + c * 8), xv);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                v[2 * tt] = fmaf(gv[q], xv[q], v[2 * tt]);
+                v[2 * tt + 1] = fmaf(uv[q], xv[q], v[2 * tt + 1]);
+              }
+            }
           }
         }
-        g = warp_allsum(g);
-        uu = warp_allsum(uu);
-        if (lane == 0) A.h[static_cast<int64_t>(a) * I + i] = silu_f32(g) * uu;
+        // butterfly reduce-scatter of the 16 sums: lane L ends with the full
+        // sum of value L >> 1 (value 2t = g_t, 2t + 1 = u_t)
+#pragma unroll
+        for (int o = 16; o >= 2; o >>= 1) {
+          const bool up = (lane & o) != 0;
+#pragma unroll
+          for (int q = 0; q < o / 2; ++q) {
+            const float lo = v[q], hi = v[q + o / 2];
+            v[q] = (up ? hi : lo) + __shfl_xor_sync(0xffffffffu, up ? lo : hi, o);
+          }
+        }
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+        const float u_val = __shfl_down_sync(0xffffffffu, v[0], 2);   // lane L+2 holds u_t
+        const int tt = lane >> 2;
+        if ((lane & 3) == 0 && g0 + tt < n)
+          A.h[static_cast<int64_t>(list[g0 + tt]) * I + i] = silu_f32(v[0]) * u_val;
       }
     }
   }
@@ -343,24 +379,43 @@ decode_down_kernel(const DecodeArgs A) {
     inflight[b] = false;
     const int e = R.touched[ti];
     const __nv_bfloat16* ws = reinterpret_cast<const __nv_bfloat16*>(buf + b * slot_bytes);
-    const int pairs = rows * R.nA;             // (row, assignment) pairs over the warps
-    for (int pr = warp; pr < pairs; pr += kDecWarps) {
-      const int jl = pr % rows, a = pr / rows;
-      if (R.sel_e[a] != e) continue;
-      const float* hr = A.h + static_cast<int64_t>(a) * I;
-      float acc = 0.f;
-      for (int c = lane; c < I / 8; c += 32) {
-        float wv[8];
-        cvt8(*reinterpret_cast<const uint4*>(ws + jl * I + c * 8), wv);
-        const float4 h0 = __ldcg(reinterpret_cast<const float4*>(hr + c * 8));
-        const float4 h1 = __ldcg(reinterpret_cast<const float4*>(hr + c * 8) + 1);
-        acc = fmaf(wv[0], h0.x, acc); acc = fmaf(wv[1], h0.y, acc);
-        acc = fmaf(wv[2], h0.z, acc); acc = fmaf(wv[3], h0.w, acc);
-        acc = fmaf(wv[4], h1.x, acc); acc = fmaf(wv[5], h1.y, acc);
-        acc = fmaf(wv[6], h1.z, acc); acc = fmaf(wv[7], h1.w, acc);
+    const int* list = R.by_e + R.e_start[e];     // the assignments of expert e, in order
+    const int n = R.e_start[e + 1] - R.e_start[e];
+    // warp w: row w % kDnRows, assignment groups of 4 taken round-robin by
+    // the kDecWarps / kDnRows warps of that row
+    constexpr int kWarpsPerRow = kDecWarps / kDnRows;
+    const int jl = warp % kDnRows;
+    if (jl < rows) {
+      for (int g0 = (warp / kDnRows) * 4; g0 < n; g0 += 4 * kWarpsPerRow) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int c = lane; c < I / 8; c += 32) {
+          float wv[8];
+          cvt8(*reinterpret_cast<const uint4*>(ws + jl * I + c * 8), wv);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (g0 + q < n) {
+              const float* hr = A.h + static_cast<int64_t>(list[g0 + q]) * I + c * 8;
+              const float4 h0 = __ldcg(reinterpret_cast<const float4*>(hr));
+              const float4 h1 = __ldcg(reinterpret_cast<const float4*>(hr) + 1);
+              float s2 = acc[q];
+              s2 = fmaf(wv[0], h0.x, s2); s2 = fmaf(wv[1], h0.y, s2);
+              s2 = fmaf(wv[2], h0.z, s2); s2 = fmaf(wv[3], h0.w, s2);
+              s2 = fmaf(wv[4], h1.x, s2); s2 = fmaf(wv[5], h1.y, s2);
+              s2 = fmaf(wv[6], h1.z, s2); s2 = fmaf(wv[7], h1.w, s2);
+              acc[q] = s2;
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[q] = warp_allsum(acc[q]);
+        if (lane < 4 && g0 + lane < n) {
+          float val = acc[0];
+#pragma unroll
+          for (int q = 1; q < 4; ++q)
+            if (lane == q) val = acc[q];
+          part[list[g0 + lane]][jl] = val;
+        }
       }
-      acc = warp_allsum(acc);
-      if (lane == 0) part[a][jl] = acc;
     }
   }
   __syncthreads();

@@ -16,7 +16,7 @@ constexpr int kScanThreads = 512;
 constexpr int kMaxGroups = MM_MAX_EXPERTS * MM_MAX_TOPK;     // (slot, expert) groups
 
 // Decode-sized calls (T <= kDecodeMaxT) stream each weight row once.
-constexpr int kDecodeMaxT = 8;
+constexpr int kDecodeMaxT = 16;
 constexpr int kDecodeMaxK = 4096;           // H and I limits of the streaming kernels
 
 // Per-expert device pointers passed by value to a kernel.
