@@ -14,7 +14,7 @@
  *       Wg, Wu: [I, H]   Wd: [H, I]   Wr: [E, H]   x, y: [T, H].
  *   - dtype selects the element type of x, the weights and y:
  *       MM_DTYPE_BF16 — bf16 storage, fp32 accumulation (tcgen05 tensor
- *                       cores for T > 64, weight streaming for T <= 64);
+ *                       cores for T > 16, weight streaming for T <= 16);
  *       MM_DTYPE_F32  — fp32 storage and fp32 SIMT arithmetic (no TF32).
  *     Router logits, probabilities, alpha and the aux loss are always fp32.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
@@ -22,7 +22,11 @@
  *     the host except mm_check_status().  The library allocates no device
  *     memory: scratch lives in the caller's `workspace`, whose size the
  *     matching *_workspace_bytes() function returns.  Calls that share a
- *     workspace must be ordered on one stream.
+ *     workspace must be ordered on one stream.  The first 256 bytes of a
+ *     workspace hold device-side state (the watchdog word and the counter of
+ *     the streaming kernel's grid barrier): zero them once before the
+ *     workspace's first use (cudaMemset).  Every call leaves them consistent,
+ *     and mm_check_status() zeroes them again after it reports a timeout.
  *   - Argument errors are reported synchronously as a non-zero mm_status
  *     with nothing enqueued.  Device-side watchdog failures (a pipeline wait
  *     that exceeded its time limit) are recorded in the workspace and
@@ -54,7 +58,7 @@ typedef enum { MM_DTYPE_F32 = 0, MM_DTYPE_BF16 = 1 } mm_dtype;
 
 /* Which kernels carry the FFN part of a call (the *_ex entry points). */
 typedef enum {
-  MM_PATH_AUTO = 0,    /* bf16: tensor-core GEMMs if T > 64, else streaming; f32: SIMT */
+  MM_PATH_AUTO = 0,    /* bf16: tensor-core GEMMs if T > 16, else streaming; f32: SIMT */
   MM_PATH_TENSOR = 1,  /* bf16 only: grouped tcgen05/TMEM GEMMs fed by TMA          */
   MM_PATH_STREAM = 2,  /* bf16 only: decode-shaped weight-streaming kernels          */
   MM_PATH_SIMT = 3     /* any dtype: plain fp32-FMA CUDA-core kernels                */

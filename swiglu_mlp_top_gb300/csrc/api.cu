@@ -56,11 +56,11 @@ MoeLayout moe_layout(int64_t T, int H, int I, int E, int k, int dtype) {
   L.h = off;        off += align_up(h_bytes(dtype) * rows * I);
   L.acc32 = off;    if (k >= 2 && dtype == kDtypeBF16) off += align_up(4 * static_cast<size_t>(T) * H);
   // bf16: fp16 copy of the E down matrices (tensor path) or, for decode-sized
-  // T, the fp32 h of the streaming path; whichever is larger
+  // T, the fp16 h of the streaming path; whichever is larger
   L.wd16 = off;
   if (dtype == kDtypeBF16) {
     size_t need = 2 * static_cast<size_t>(E) * H * I;
-    if (T <= kDecodeMaxT) need = std::max(need, 4 * rows * static_cast<size_t>(I));
+    if (T <= kDecodeMaxT) need = std::max(need, 2 * rows * static_cast<size_t>(I));
     off += align_up(need);
   }
   L.total = off;
@@ -104,9 +104,9 @@ int resolve_path(int path, int dtype, int64_t T) {
   return path;
 }
 
-bool stream_shape_ok(int64_t T, int H, int I, int dtype) {
+bool stream_shape_ok(int64_t T, int H, int I, int E, int k, int dtype) {
   return dtype == kDtypeBF16 && T <= kDecodeMaxT &&
-         decode_smem_bytes(static_cast<int>(T), H, I) <= 200 * 1024;
+         decode_smem_bytes(static_cast<int>(T), H, I, E, k) <= 200 * 1024;
 }
 
 inline char* ws_at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
@@ -197,21 +197,20 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
   const int p = resolve_path(path, dtype, T);
   if (p == MM_PATH_TENSOR && (dtype != kDtypeBF16 || !tensor_shape_ok(H, I)))
     return MM_ERR_UNSUPPORTED;
-  if (p == MM_PATH_STREAM && !stream_shape_ok(T, H, I, dtype)) return MM_ERR_UNSUPPORTED;
+  if (p == MM_PATH_STREAM && !stream_shape_ok(T, H, I, 1, 1, dtype)) return MM_ERR_UNSUPPORTED;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
   void* h = ws_at(workspace, sizeof(WsHeader));
   if (p == MM_PATH_STREAM) {
-    // fp32 h [T, I] fits in the workspace's h + Wd-copy area for T <= H
+    // fp16 h [T, I] in the workspace's h area
     const void* wg1[1] = {Wg};
     const void* wu1[1] = {Wu};
     const void* wd1[1] = {Wd};
     cudaError_t e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
       return launch_decode_ffn(x, nullptr, nullptr, wg1, wu1, wd1, static_cast<int>(T), H, I, 1, 1,
-                               0.f, nullptr, nullptr, nullptr, static_cast<float*>(h), y, hdr, st);
+                               0.f, nullptr, nullptr, nullptr, h, y, hdr, st);
     });
-    g_launches.fetch_add(1, std::memory_order_relaxed);   // the stream path launches two kernels
     if (e != cudaSuccess) return cuda_fail(e, "stream ffn");
     return MM_OK;
   }
@@ -294,7 +293,7 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
   const int p = resolve_path(path, dtype, T);
   if (p == MM_PATH_TENSOR && (dtype != kDtypeBF16 || !tensor_shape_ok(H, I)))
     return MM_ERR_UNSUPPORTED;
-  if (p == MM_PATH_STREAM && !stream_shape_ok(T, H, I, dtype)) return MM_ERR_UNSUPPORTED;
+  if (p == MM_PATH_STREAM && !stream_shape_ok(T, H, I, E, k, dtype)) return MM_ERR_UNSUPPORTED;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
@@ -310,14 +309,13 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
                                       : reinterpret_cast<float*>(ws_at(workspace, L.acc32));
 
   if (p == MM_PATH_STREAM) {
-    // decode-sized: the routing runs inside the two streaming kernels; fp32
+    // decode-sized: the routing runs inside the streaming kernel; fp16
     // h [T*k, I] lives in the fp16 Wd-copy area, which is sized for it
-    float* hdec = reinterpret_cast<float*>(ws_at(workspace, L.wd16));
+    void* hdec = ws_at(workspace, L.wd16);
     cudaError_t e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
       return launch_decode_ffn(x, Wr, logit_bias, Wg, Wu, Wd, static_cast<int>(T), H, I, E, k,
                                coef, topk_idx, topk_w, aux_loss, hdec, y, hdr, st);
     });
-    g_launches.fetch_add(1, std::memory_order_relaxed);   // the stream path launches two kernels
     if (e != cudaSuccess) return cuda_fail(e, "decode ffn");
     return MM_OK;
   }

@@ -14,7 +14,9 @@ namespace mm {
 struct WsHeader {
   unsigned int status;        // MM_ERR_* bits set by device code (0 = fine)
   unsigned int where;         // role id of the first wait that gave up
-  unsigned int pad[62];
+  unsigned int bar_count;     // grid barrier: CTAs arrived in the current round (0 between rounds)
+  unsigned int bar_gen;       // grid barrier: completed rounds (wraps)
+  unsigned int pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
@@ -87,6 +89,41 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       }
     }
   }
+}
+
+// Grid-wide barrier for a cooperative launch (every CTA resident).  The last
+// CTA to arrive resets the count and advances the generation; the others wait
+// (bounded) for the generation to change.  Works from any state the header
+// was left in by completed calls.  Returns false if the wait gave up.
+__device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned where) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile unsigned int* gen = &hdr->bar_gen;
+    const unsigned int g0 = *gen;
+    __threadfence();
+    const unsigned int arrived = atomicAdd(&hdr->bar_count, 1u) + 1u;
+    int ok = 1;
+    if (arrived == gridDim.x * gridDim.y * gridDim.z) {
+      hdr->bar_count = 0;
+      __threadfence();
+      atomicAdd(&hdr->bar_gen, 1u);
+    } else {
+      const unsigned long long t0 = globaltimer_ns();
+      uint32_t n = 0;
+      while (*gen == g0) {
+        if ((++n & 63u) == 0u && (globaltimer_ns() - t0 > kWaitLimitNs || n > (1u << 30))) {
+          report_timeout(hdr, where);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
 }
 
 // ---------------------------------------------------------------- TMA

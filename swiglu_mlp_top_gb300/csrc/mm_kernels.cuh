@@ -17,7 +17,6 @@ constexpr int kMaxGroups = MM_MAX_EXPERTS * MM_MAX_TOPK;     // (slot, expert) g
 
 // Decode-sized calls (T <= kDecodeMaxT) stream each weight row once.
 constexpr int kDecodeMaxT = 16;
-constexpr int kDecodeMaxK = 4096;           // H and I limits of the streaming kernels
 
 // Per-expert device pointers passed by value to a kernel.
 struct PtrArray {
@@ -92,15 +91,16 @@ cudaError_t launch_down_simt(int dtype, const void* h, int64_t a_rows, int H, in
 cudaError_t launch_convert_bf16_to_f16(const void* const* src, int n_mat, int64_t per_matrix,
                                        void* dst, cudaStream_t st);
 
-// Decode-sized forward on the CUDA cores (T <= kDecodeMaxT, bf16): kernel A
-// routes (MoE: Wr != nullptr) and computes the fp32 h [T*k, I] (dense: [T, I])
-// into hbuf; kernel B, a programmatic dependent of A, forms y.  Block 0 of A
-// writes topk_idx / topk_w / aux_loss (MoE).
-size_t decode_smem_bytes(int T, int H, int I);
+// Decode-sized forward on the CUDA cores (T <= kDecodeMaxT, bf16): one
+// cooperative kernel routes (MoE: Wr != nullptr), writes the fp16 h [T*k, I]
+// (dense: [T, I]) into hbuf, meets every other CTA at a grid barrier kept in
+// the workspace header, and forms y.  Block 0 writes topk_idx / topk_w /
+// aux_loss (MoE).  decode_smem_bytes is its dynamic shared memory (dense: E = k = 1).
+size_t decode_smem_bytes(int T, int H, int I, int E, int k);
 cudaError_t launch_decode_ffn(const void* x, const void* Wr, const float* bias,
                               const void* const* Wg, const void* const* Wu, const void* const* Wd,
                               int T, int H, int I, int E, int k, float coef, int32_t* topk_idx,
-                              float* topk_w, float* aux_loss, float* hbuf, void* y, WsHeader* hdr,
+                              float* topk_w, float* aux_loss, void* hbuf, void* y, WsHeader* hdr,
                               cudaStream_t st);
 
 cudaError_t launch_watchdog_selftest(WsHeader* hdr, uint32_t limit_us, cudaStream_t st);

@@ -349,7 +349,6 @@ dispatch_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, int k,
                 const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ blk_base,
                 const int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
                 Tin* __restrict__ Xp) {
-  constexpr int kWarps = kRouteThreads / 32;
   __shared__ int s_w0cnt[MM_MAX_EXPERTS];   // per-expert count in warp 0 (tokens 0..31)
   __shared__ int s_pos[kRouteTokensPerBlock * MM_MAX_EXPERTS];
 
