@@ -56,11 +56,11 @@ MoeLayout moe_layout(int64_t T, int H, int I, int E, int k, int dtype) {
   L.h = off;        off += align_up(h_bytes(dtype) * rows * I);
   L.acc32 = off;    if (k >= 2 && dtype == kDtypeBF16) off += align_up(4 * static_cast<size_t>(T) * H);
   // bf16: fp16 copy of the E down matrices (tensor path) or, for decode-sized
-  // T, the fp16 h of the streaming path; whichever is larger
+  // T, the fp32 h of the streaming path; whichever is larger
   L.wd16 = off;
   if (dtype == kDtypeBF16) {
     size_t need = 2 * static_cast<size_t>(E) * H * I;
-    if (T <= kDecodeMaxT) need = std::max(need, 2 * rows * static_cast<size_t>(I));
+    if (T <= kDecodeMaxT) need = std::max(need, 4 * rows * static_cast<size_t>(I));
     off += align_up(need);
   }
   L.total = off;
@@ -80,9 +80,11 @@ RouteLayout route_layout(int64_t T, int E, int k) {
   return L;
 }
 
-// Dense workspace: h [T, I], then (bf16) the fp16 copy of Wd.
+// Dense workspace: h [T, I], then (bf16) the fp16 copy of Wd.  The
+// streaming path (bf16, T <= kDecodeMaxT) keeps h in fp32.
 size_t dense_h_bytes(int64_t T, int I, int dtype) {
-  return align_up(h_bytes(dtype) * static_cast<size_t>(T) * I);
+  const size_t eb = (dtype == kDtypeBF16 && T <= kDecodeMaxT) ? 4 : h_bytes(dtype);
+  return align_up(eb * static_cast<size_t>(T) * I);
 }
 size_t dense_ws_bytes(int64_t T, int H, int I, int dtype) {
   return sizeof(WsHeader) + dense_h_bytes(T, I, dtype) +
@@ -203,7 +205,7 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
   WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
   void* h = ws_at(workspace, sizeof(WsHeader));
   if (p == MM_PATH_STREAM) {
-    // fp16 h [T, I] in the workspace's h area
+    // fp32 h [T, I] in the workspace's h area
     const void* wg1[1] = {Wg};
     const void* wu1[1] = {Wu};
     const void* wd1[1] = {Wd};
@@ -309,7 +311,7 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
                                       : reinterpret_cast<float*>(ws_at(workspace, L.acc32));
 
   if (p == MM_PATH_STREAM) {
-    // decode-sized: the routing runs inside the streaming kernel; fp16
+    // decode-sized: the routing runs inside the streaming kernel; fp32
     // h [T*k, I] lives in the fp16 Wd-copy area, which is sized for it
     void* hdec = ws_at(workspace, L.wd16);
     cudaError_t e = counted_launch(MM_KERNEL_GATEUP, st, [&] {

@@ -4,29 +4,42 @@
 // experts some token selected are read.
 //
 //   route (MoE)  logits, softmax, top-k, alpha (lesson 13 §1.5, chapter 4
-//                §4.3): cheap at this size, so every CTA computes it for all
+//                §4.3): small at this size, so every CTA computes it for all
 //                T tokens with the same code and order, and all CTAs agree;
 //                block 0 writes topk_idx, topk_w and the aux loss (lesson 13 §1.6)
 //   gate/up      h[a, i] = SiLU(Wg_e[i] . x_t) * (Wu_e[i] . x_t) for every
-//                assignment a = (t, s) of expert e, fp16   (lesson 13 §0/§1.2)
+//                assignment a = (t, s) of expert e, fp32  (lesson 13 §0/§1.2)
 //   grid barrier (h complete)
 //   down         y[t, j] = sum_s alpha_{t,s} (Wd_{e_s}[j] . h[t, s]) in slot
 //                order, fp32, rounded once       (lesson 13 §0 MoE equation)
 //
-// Each CTA issues the bulk copies of its first gate/up slice and of its first
-// Wd rows as soon as it knows the touched experts, so the down weights are
-// already in shared memory when the barrier opens.
+// Each CTA issues the bulk copies of its first gate/up slices and of its
+// first Wd rows as soon as it knows the touched experts (dense: at entry), so
+// the down weights are in shared memory by the time the barrier opens.  The
+// products use packed fp32 FMA (two lanes of fp32 per instruction) on
+// operands widened from bf16; every dot product accumulates in fp32.
 #include "mm_kernels.cuh"
 
 namespace mm {
 
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
-constexpr int kUpRows = kDecWarps;          // Wg / Wu rows per gate/up slice (1 per warp)
-constexpr int kDnRows = 4;                  // output rows per down unit
-constexpr int kTokGroup = 8;                // tokens whose sums a lane keeps at once
-constexpr int kHStage = 16;                 // h rows (assignments) staged at once
-constexpr size_t kWrSmemMax = 32 * 1024;    // Wr staged in shared memory up to this size
+constexpr int kUpRows = kDecWarps;          // Wg / Wu rows per gate/up unit (one per warp)
+constexpr int kDnRows = 4;                  // output columns (Wd rows) per down unit
+constexpr int kMaxRing = 6;                 // gate/up stages
+constexpr int kMaxWdSlots = 4;              // Wd buffers
+constexpr int kMaxHRows = 32;               // h rows staged at once
+constexpr size_t kDecSmemBudget = 200 * 1024;
+constexpr size_t kDecSmemTwoPerSm = 100 * 1024;
+
+// Shared-memory plan, chosen on the host.  Phase 1 holds x (fp32) at offset 0
+// and the gate/up ring after it (Wr sits at the ring's start during the
+// routing); phase 2 reuses offset 0 for the staged h rows.  The Wd buffers
+// live above both, since they fill during phase 1.
+struct DecPlan {
+  int ring, wd_slots, h_rows, per_sm;
+  uint32_t ring_off, wd_off, total;
+};
 
 struct DecodeArgs {
   const void* x;            // [T, H] bf16
@@ -38,9 +51,10 @@ struct DecodeArgs {
   int32_t* topk_idx;        // written by block 0 (MoE)
   float* topk_w;
   float* aux_loss;
-  __half* h;                // [T*k, I] fp16 scratch (dense: [T, I])
+  float* h;                 // [T*k, I] fp32 scratch (dense: [T, I])
   void* y;                  // [T, H] bf16
   WsHeader* hdr;
+  DecPlan plan;
 };
 
 // Routing tables shared by the CTA.
@@ -48,36 +62,61 @@ struct DecRoute {
   int nA;                                   // assignments (MoE: T*k, dense: T)
   int n_touched;
   int touched[MM_MAX_EXPERTS];              // ascending expert ids
+  int cnt[MM_MAX_EXPERTS];                  // assignments per expert
+  int e_start[MM_MAX_EXPERTS + 1];          // expert e's assignments: by_e[e_start[e] ..]
   int sel_e[kDecodeMaxT * MM_MAX_TOPK];     // expert of assignment a = t*k + s
   float sel_a[kDecodeMaxT * MM_MAX_TOPK];   // its alpha
-  float prob[kDecodeMaxT][MM_MAX_EXPERTS];  // logits, then probabilities
+  int rank[kDecodeMaxT * MM_MAX_TOPK];      // its place among its expert's assignments
   int by_e[kDecodeMaxT * MM_MAX_TOPK];      // assignments grouped by expert, in order
-  int e_start[MM_MAX_EXPERTS + 1];          // expert e's assignments: by_e[e_start[e] ..]
+  float prob[kDecodeMaxT][MM_MAX_EXPERTS];  // logits, then probabilities
 };
 
-__device__ __forceinline__ void cvt8(const uint4& raw, float (&f)[8]) {
-  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 q = __bfloat1622float2(b[i]);
-    f[2 * i] = q.x;
-    f[2 * i + 1] = q.y;
-  }
-}
-__device__ __forceinline__ void cvt8h(const uint4& raw, float (&f)[8]) {
-  const __half2* b = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 q = __half22float2(b[i]);
-    f[2 * i] = q.x;
-    f[2 * i + 1] = q.y;
-  }
-}
+typedef unsigned long long u64;
 
+// d = a * b + c on two fp32 lanes packed in 64 bits (low word = lane 0).
+__device__ __forceinline__ u64 ffma2(u64 a, u64 b, u64 c) {
+  u64 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// Two bf16 (one 32-bit word, element 0 in the low half) widened to fp32.
+__device__ __forceinline__ u64 bf2(uint32_t w) {
+  return (static_cast<u64>(w & 0xffff0000u) << 32) | static_cast<u64>(w << 16);
+}
+__device__ __forceinline__ float hsum2(u64 v) {
+  return __uint_as_float(static_cast<uint32_t>(v)) + __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
 __device__ __forceinline__ float warp_allsum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
+}
+
+// Sum of NV per-lane values over the warp, scattered: lane L ends with the
+// full sum of value L / (32 / NV).  Each exchange step hands half of the
+// remaining values to the partner lane, so the warp moves NV - 1 + (5 -
+// log2 NV) shuffles instead of 5 * NV.
+template <int NV, int CNT, int O>
+__device__ __forceinline__ void reduce_scatter_step(float (&v)[NV], int lane) {
+  if constexpr (O > 0) {
+    if constexpr (CNT > 1) {
+      const bool up = (lane & O) != 0;
+#pragma unroll
+      for (int q = 0; q < CNT / 2; ++q) {
+        const float lo = v[q], hi = v[q + CNT / 2];
+        v[q] = (up ? hi : lo) + __shfl_xor_sync(0xffffffffu, up ? lo : hi, O);
+      }
+      reduce_scatter_step<NV, CNT / 2, O / 2>(v, lane);
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+      reduce_scatter_step<NV, 1, O / 2>(v, lane);
+    }
+  }
+}
+template <int NV>
+__device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
+  reduce_scatter_step<NV, NV, 16>(v, lane);
+  return v[0];
 }
 
 // 1-D bulk copy global -> this CTA's shared memory, completion on `bar`.
@@ -90,86 +129,137 @@ __device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t
       : "memory");
 }
 
-__host__ __device__ inline size_t round128(size_t v) { return (v + 127) & ~size_t(127); }
-__host__ __device__ inline size_t wr_bytes(int E, int H) { return static_cast<size_t>(E) * H * 2; }
-
-// Shared-memory layout: x | gate/up ring (2 x (Wg, Wu) slices) | Wd slots (2) |
-// h stage (also holds Wr during the routing).
-struct DecLayout {
-  size_t ring, wd, hst, total;
-};
-__host__ __device__ inline DecLayout dec_layout(int T, int H, int I, int E, int nA) {
-  DecLayout L;
-  L.ring = round128(static_cast<size_t>(T) * H * 2);
-  L.wd = L.ring + round128(2 * 2 * static_cast<size_t>(kUpRows) * H * 2);
-  L.hst = L.wd + round128(2 * static_cast<size_t>(kDnRows) * I * 2);
-  const size_t hs = static_cast<size_t>(nA < kHStage ? nA : kHStage) * I * 2;
-  const size_t wr = wr_bytes(E, H) <= kWrSmemMax ? wr_bytes(E, H) : 0;
-  L.total = L.hst + round128(hs > wr ? hs : wr);
-  return L;
+// One gate/up row i of expert e for m <= NT assignments (list): the lanes
+// split H in chunks of 8, the row's Wg and Wu chunks are widened once and
+// applied to every token's fp32 x chunk.
+template <int NT>
+__device__ __forceinline__ void gateup_row(const __nv_bfloat16* grow, const __nv_bfloat16* urow,
+                                           const float* xs, const int* list, int m, int kk, int H,
+                                           int I, int i, float* hout, int lane) {
+  const float* xr[NT];
+#pragma unroll
+  for (int tt = 0; tt < NT; ++tt) xr[tt] = xs + static_cast<size_t>(list[tt < m ? tt : m - 1] / kk) * H;
+  u64 ga[NT], ua[NT];
+#pragma unroll
+  for (int tt = 0; tt < NT; ++tt) ga[tt] = ua[tt] = 0ull;
+  for (int c = lane; c < H / 8; c += 32) {
+    const uint4 gw = *reinterpret_cast<const uint4*>(grow + c * 8);
+    const uint4 uw = *reinterpret_cast<const uint4*>(urow + c * 8);
+    const u64 g0 = bf2(gw.x), g1 = bf2(gw.y), g2 = bf2(gw.z), g3 = bf2(gw.w);
+    const u64 u0 = bf2(uw.x), u1 = bf2(uw.y), u2 = bf2(uw.z), u3 = bf2(uw.w);
+#pragma unroll
+    for (int tt = 0; tt < NT; ++tt) {
+      const ulonglong2 xa = *reinterpret_cast<const ulonglong2*>(xr[tt] + c * 8);
+      const ulonglong2 xb = *reinterpret_cast<const ulonglong2*>(xr[tt] + c * 8 + 4);
+      ga[tt] = ffma2(g0, xa.x, ga[tt]);
+      ua[tt] = ffma2(u0, xa.x, ua[tt]);
+      ga[tt] = ffma2(g1, xa.y, ga[tt]);
+      ua[tt] = ffma2(u1, xa.y, ua[tt]);
+      ga[tt] = ffma2(g2, xb.x, ga[tt]);
+      ua[tt] = ffma2(u2, xb.x, ua[tt]);
+      ga[tt] = ffma2(g3, xb.y, ga[tt]);
+      ua[tt] = ffma2(u3, xb.y, ua[tt]);
+    }
+  }
+  float v[2 * NT];
+#pragma unroll
+  for (int tt = 0; tt < NT; ++tt) {
+    v[2 * tt] = hsum2(ga[tt]);
+    v[2 * tt + 1] = hsum2(ua[tt]);
+  }
+  const float r = reduce_scatter<2 * NT>(v, lane);   // value 2t = g_t, 2t + 1 = u_t
+  constexpr int span = 32 / (2 * NT);                // lanes holding one value
+  const float u = __shfl_down_sync(0xffffffffu, r, span);
+  if (lane % (2 * span) == 0) {
+    const int tt = lane / (2 * span);
+    if (tt < m) hout[static_cast<size_t>(list[tt]) * I + i] = silu_f32(r) * u;
+  }
 }
 
-// Routing of all T tokens.  Logits: (token, expert) pairs spread over the
-// warps, four at a time with independent sums (lanes split H, xor-tree sum),
-// fp32.  Then warp t, lane e: softmax over the experts with the maximum
-// subtracted, and k arg-max rounds over (p desc, index asc) — equal
-// probabilities go to the lower index; alpha = p / (sum_S p + 1e-20).
-__device__ void decode_route(const DecodeArgs& A, const __nv_bfloat16* xs,
-                             const __nv_bfloat16* wrs, DecRoute& R) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nch = A.H / 8;
-  if (A.Wr == nullptr) {                      // dense: one weight set, every token
-    if (threadIdx.x < A.T) {
-      R.sel_e[threadIdx.x] = 0;
-      R.sel_a[threadIdx.x] = 1.0f;
-      R.by_e[threadIdx.x] = threadIdx.x;
+// One Wd row (output column j) against m <= NA staged h rows; the result for
+// staged row sbase + q goes to part[ids[q]][jl].
+template <int NA>
+__device__ __forceinline__ void down_row(const __nv_bfloat16* wrow, const float* hst, int sbase,
+                                         const int* ids, int m, int I, int jl,
+                                         float (*part)[kDnRows], int lane) {
+  const float* hr[NA];
+#pragma unroll
+  for (int q = 0; q < NA; ++q) hr[q] = hst + static_cast<size_t>(sbase + (q < m ? q : m - 1)) * I;
+  u64 acc[NA];
+#pragma unroll
+  for (int q = 0; q < NA; ++q) acc[q] = 0ull;
+  for (int c = lane; c < I / 8; c += 32) {
+    const uint4 w = *reinterpret_cast<const uint4*>(wrow + c * 8);
+    const u64 w0 = bf2(w.x), w1 = bf2(w.y), w2 = bf2(w.z), w3 = bf2(w.w);
+#pragma unroll
+    for (int q = 0; q < NA; ++q) {
+      const ulonglong2 ha = *reinterpret_cast<const ulonglong2*>(hr[q] + c * 8);
+      const ulonglong2 hb = *reinterpret_cast<const ulonglong2*>(hr[q] + c * 8 + 4);
+      acc[q] = ffma2(w0, ha.x, acc[q]);
+      acc[q] = ffma2(w1, ha.y, acc[q]);
+      acc[q] = ffma2(w2, hb.x, acc[q]);
+      acc[q] = ffma2(w3, hb.y, acc[q]);
     }
-    if (threadIdx.x == 0) {
-      R.nA = A.T;
-      R.n_touched = 1;
-      R.touched[0] = 0;
-      R.e_start[0] = 0;
-      R.e_start[1] = A.T;
-    }
-    __syncthreads();
-    return;
   }
-  const __nv_bfloat16* Wr = wrs != nullptr ? wrs : static_cast<const __nv_bfloat16*>(A.Wr);
-  const int E = A.E, k = A.k;
+  float v[NA];
+#pragma unroll
+  for (int q = 0; q < NA; ++q) v[q] = hsum2(acc[q]);
+  const float r = reduce_scatter<NA>(v, lane);
+  constexpr int span = 32 / NA;
+  if (lane % span == 0) {
+    const int q = lane / span;
+    if (q < m) part[ids[q]][jl] = r;
+  }
+}
+
+// MoE routing of all T tokens.  Logits: (token, expert) pairs, four per warp
+// at a time, lanes split H, fp32.  Then warp t, lane e: softmax with the
+// maximum subtracted and k arg-max rounds over (p desc, index asc) — equal
+// probabilities go to the lower index; alpha = p / (sum_S p + 1e-20).  Then
+// warp 0 groups the assignments by expert, keeping token order within each.
+__device__ void decode_route(const DecodeArgs& A, const float* xs, const __nv_bfloat16* Wr,
+                             const float* bias, DecRoute& R) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int E = A.E, k = A.k, H = A.H;
   const int pairs = A.T * E;
   for (int p0 = warp * 4; p0 < pairs; p0 += kDecWarps * 4) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int c = lane; c < nch; c += 32) {
+    const float* xr[4];
+    const __nv_bfloat16* wr[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int p = min(p0 + q, pairs - 1);
+      const int t = p / E;
+      xr[q] = xs + static_cast<size_t>(t) * H;
+      wr[q] = Wr + static_cast<size_t>(p - t * E) * H;
+    }
+    u64 acc[4] = {0ull, 0ull, 0ull, 0ull};
+    for (int c = lane; c < H / 8; c += 32) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const int p = p0 + q;
-        if (p < pairs) {
-          const int t = p / E, e = p - t * E;
-          float xv[8], wv[8];
-          cvt8(*reinterpret_cast<const uint4*>(xs + t * A.H + c * 8), xv);
-          cvt8(*reinterpret_cast<const uint4*>(Wr + static_cast<int64_t>(e) * A.H + c * 8), wv);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) acc[q] = fmaf(xv[j], wv[j], acc[q]);
-        }
+        const uint4 w = *reinterpret_cast<const uint4*>(wr[q] + c * 8);
+        const ulonglong2 xa = *reinterpret_cast<const ulonglong2*>(xr[q] + c * 8);
+        const ulonglong2 xb = *reinterpret_cast<const ulonglong2*>(xr[q] + c * 8 + 4);
+        acc[q] = ffma2(bf2(w.x), xa.x, acc[q]);
+        acc[q] = ffma2(bf2(w.y), xa.y, acc[q]);
+        acc[q] = ffma2(bf2(w.z), xb.x, acc[q]);
+        acc[q] = ffma2(bf2(w.w), xb.y, acc[q]);
       }
     }
+    float v[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[q] = warp_allsum(acc[q]);
-    if (lane < 4 && p0 + lane < pairs) {
-      float v = acc[0];
-#pragma unroll
-      for (int q = 1; q < 4; ++q)
-        if (lane == q) v = acc[q];
-      const int p = p0 + lane;
-      R.prob[p / E][p % E] = v;
+    for (int q = 0; q < 4; ++q) v[q] = hsum2(acc[q]);
+    const float r = reduce_scatter<4>(v, lane);
+    if ((lane & 7) == 0) {
+      const int p = p0 + (lane >> 3);
+      if (p < pairs) R.prob[p / E][p % E] = r;
     }
   }
   __syncthreads();
   for (int t = warp; t < A.T; t += kDecWarps) {
     // lane holds experts lane and lane + 32
     float r0 = -INFINITY, r1 = -INFINITY;
-    if (lane < E) r0 = R.prob[t][lane] + (A.bias != nullptr ? A.bias[lane] : 0.f);
-    if (lane + 32 < E) r1 = R.prob[t][lane + 32] + (A.bias != nullptr ? A.bias[lane + 32] : 0.f);
+    if (lane < E) r0 = R.prob[t][lane] + bias[lane];
+    if (lane + 32 < E) r1 = R.prob[t][lane + 32] + bias[lane + 32];
     float m = fmaxf(r0, r1);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -181,6 +271,8 @@ __device__ void decode_route(const DecodeArgs& A, const __nv_bfloat16* xs,
     if (lane + 32 < E) R.prob[t][lane + 32] = p1;
     bool taken0 = lane >= E, taken1 = lane + 32 >= E;
     float sel_sum = 0.f;
+    float my_p = 0.f;
+    int my_e = 0;
     for (int s = 0; s < k; ++s) {
       float bp = -1.f;
       int be = 0x7fffffff;
@@ -195,39 +287,56 @@ __device__ void decode_route(const DecodeArgs& A, const __nv_bfloat16* xs,
       if (be == lane) taken0 = true;
       if (be == lane + 32) taken1 = true;
       sel_sum += bp;
-      if (lane == 0) {
-        R.sel_e[t * k + s] = be;
-        R.sel_a[t * k + s] = bp;
+      if (lane == s) { my_p = bp; my_e = be; }
+    }
+    if (lane < k) {
+      R.sel_e[t * k + lane] = my_e;
+      R.sel_a[t * k + lane] = my_p / (sel_sum + 1e-20f);
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nA = A.T * k;
+    for (int e = lane; e < E; e += 32) R.cnt[e] = 0;
+    __syncwarp();
+    for (int base = 0; base < nA; base += 32) {
+      const int a = base + lane;
+      const bool valid = a < nA;
+      const int e = valid ? R.sel_e[a] : MM_MAX_EXPERTS + lane;   // idle lanes match no one
+      const unsigned mask = __match_any_sync(0xffffffffu, e);
+      const unsigned below = mask & ((1u << lane) - 1u);
+      const int prior = valid ? R.cnt[e] : 0;
+      __syncwarp();
+      if (valid) {
+        R.rank[a] = prior + __popc(below);
+        if (below == 0u) R.cnt[e] = prior + __popc(mask);
       }
+      __syncwarp();
+    }
+    const unsigned lt = (1u << lane) - 1u;
+    const int c0 = lane < E ? R.cnt[lane] : 0;
+    const int c1 = lane + 32 < E ? R.cnt[lane + 32] : 0;
+    int s0 = c0, s1 = c1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n0 = __shfl_up_sync(0xffffffffu, s0, o);
+      const int n1 = __shfl_up_sync(0xffffffffu, s1, o);
+      if (lane >= o) { s0 += n0; s1 += n1; }
+    }
+    const int tot0 = __shfl_sync(0xffffffffu, s0, 31);
+    if (lane < E) R.e_start[lane] = s0 - c0;
+    if (lane + 32 < E) R.e_start[lane + 32] = tot0 + s1 - c1;
+    const unsigned b0 = __ballot_sync(0xffffffffu, c0 > 0);
+    const unsigned b1 = __ballot_sync(0xffffffffu, c1 > 0);
+    if (c0 > 0) R.touched[__popc(b0 & lt)] = lane;
+    if (c1 > 0) R.touched[__popc(b0) + __popc(b1 & lt)] = lane + 32;
+    if (lane == 0) {
+      R.n_touched = __popc(b0) + __popc(b1);
+      R.nA = nA;
+      R.e_start[E] = nA;
     }
     __syncwarp();
-    if (lane < k) R.sel_a[t * k + lane] = R.sel_a[t * k + lane] / (sel_sum + 1e-20f);
-  }
-  __syncthreads();
-  // per-expert counts, their prefix, and each assignment's place (order kept)
-  const int nA = A.T * k;
-  if (threadIdx.x < E) {
-    int c = 0;
-    for (int a = 0; a < nA; ++a) c += (R.sel_e[a] == static_cast<int>(threadIdx.x));
-    R.e_start[threadIdx.x + 1] = c;                 // count for now
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    R.nA = nA;
-    R.e_start[0] = 0;
-    int n = 0;
-    for (int e = 0; e < E; ++e) {
-      if (R.e_start[e + 1] > 0) R.touched[n++] = e;
-      R.e_start[e + 1] += R.e_start[e];
-    }
-    R.n_touched = n;
-  }
-  __syncthreads();
-  if (threadIdx.x < nA) {
-    const int a = threadIdx.x, e = R.sel_e[a];
-    int rank = 0;
-    for (int b = 0; b < a; ++b) rank += (R.sel_e[b] == e);
-    R.by_e[R.e_start[e] + rank] = a;
+    for (int a = lane; a < nA; a += 32) R.by_e[R.e_start[R.sel_e[a]] + R.rank[a]] = a;
   }
   __syncthreads();
 }
@@ -236,276 +345,308 @@ __global__ void __launch_bounds__(kDecThreads)
 decode_ffn_kernel(const DecodeArgs A) {
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ DecRoute R;
-  __shared__ __align__(8) uint64_t bar[5];     // ring 0, ring 1, Wd slot 0, Wd slot 1, h stage
+  __shared__ __align__(8) uint64_t bar[kMaxRing + kMaxWdSlots + 1];
   __shared__ float part[kDecodeMaxT * MM_MAX_TOPK][kDnRows];
+  __shared__ float s_bias[MM_MAX_EXPERTS];
+  const DecPlan& P = A.plan;
   const int H = A.H, I = A.I;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nA_max = (A.Wr != nullptr) ? A.T * A.k : A.T;
-  const DecLayout Ly = dec_layout(A.T, H, I, A.E, nA_max);
-  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(dsm);
-  unsigned char* ring = dsm + Ly.ring;
-  unsigned char* wdbuf = dsm + Ly.wd;
-  __half* hst = reinterpret_cast<__half*>(dsm + Ly.hst);
-  __nv_bfloat16* wrs = (A.Wr != nullptr && wr_bytes(A.E, H) <= kWrSmemMax)
-                           ? reinterpret_cast<__nv_bfloat16*>(hst) : nullptr;
-  const size_t slice_bytes = static_cast<size_t>(kUpRows) * H * 2;   // one of Wg / Wu
-  const size_t slot_bytes = static_cast<size_t>(kDnRows) * I * 2;
-  uint32_t phase[5] = {0, 0, 0, 0, 0};
-  bool inflight[5] = {false, false, false, false, false};           // thread 0 issues
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = gridDim.x;
+  const bool moe = A.Wr != nullptr;
+  const int kk = moe ? A.k : 1;
+  float* xs = reinterpret_cast<float*>(dsm);
+  unsigned char* ring = dsm + P.ring_off;
+  unsigned char* wdbuf = dsm + P.wd_off;
+  float* hst = reinterpret_cast<float*>(dsm);
+  uint64_t* ring_bar = bar;
+  uint64_t* wd_bar = bar + kMaxRing;
+  uint64_t* h_bar = bar + kMaxRing + kMaxWdSlots;
+  const size_t slice = static_cast<size_t>(kUpRows) * H * 2;   // one of Wg / Wu
+  const size_t stage = 2 * slice;
+  const size_t slot = static_cast<size_t>(kDnRows) * I * 2;
+  const int slices = I / kUpRows;
+  const int dn_units = H / kDnRows;
+  const int my_dn = blockIdx.x < dn_units ? (dn_units - blockIdx.x + G - 1) / G : 0;
 
-  if (threadIdx.x == 0) {
-    for (int q = 0; q < 5; ++q) mbar_init(&bar[q], 1);
+  // copies issued (thread 0) and consumed (every thread)
+  int up_issued = 0, wd_issued = 0, h_issued = 0;
+  int up_used = 0, wd_used = 0, h_used = 0;
+  int n_touched = 1, my_up = 0, my_wd = 0;
+
+  auto issue_up = [&](int it) {
+    const int u = blockIdx.x + it * G;
+    const int e = moe ? R.touched[u / slices] : 0;
+    const int r0 = (u % slices) * kUpRows;
+    const uint32_t bytes = static_cast<uint32_t>(slice);
+    unsigned char* dst = ring + (it % P.ring) * stage;
+    uint64_t* b = &ring_bar[it % P.ring];
+    mbar_arrive_expect_tx(b, 2 * bytes);
+    bulk_load(dst, static_cast<const __nv_bfloat16*>(A.wg.p[e]) + static_cast<size_t>(r0) * H, bytes, b);
+    bulk_load(dst + slice, static_cast<const __nv_bfloat16*>(A.wu.p[e]) + static_cast<size_t>(r0) * H,
+              bytes, b);
+    ++up_issued;
+  };
+  auto issue_wd = [&](int q) {
+    const int r = q / n_touched, ti = q - r * n_touched;
+    const int du = blockIdx.x + r * G;
+    const int e = moe ? R.touched[ti] : 0;
+    uint64_t* b = &wd_bar[q % P.wd_slots];
+    mbar_arrive_expect_tx(b, static_cast<uint32_t>(slot));
+    bulk_load(wdbuf + (q % P.wd_slots) * slot,
+              static_cast<const __nv_bfloat16*>(A.wd.p[e]) + static_cast<size_t>(du) * kDnRows * I,
+              static_cast<uint32_t>(slot), b);
+    ++wd_issued;
+  };
+  auto issue_first = [&]() {
+    for (int it = 0; it < P.ring && it < my_up; ++it) issue_up(it);
+    for (int q = 0; q < P.wd_slots && q < my_wd; ++q) issue_wd(q);
+  };
+
+  if (tid == 0) {
+    for (int q = 0; q < kMaxRing + kMaxWdSlots + 1; ++q) mbar_init(&bar[q], 1);
     fence_mbar_init();
   }
-  {
-    const int nx = A.T * H / 8;
-    const int nw = (wrs != nullptr) ? A.E * H / 8 : 0;
-    for (int i = threadIdx.x; i < nx + nw; i += blockDim.x) {
-      if (i < nx)
-        reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(A.x) + i);
-      else
-        reinterpret_cast<uint4*>(wrs)[i - nx] = __ldg(reinterpret_cast<const uint4*>(A.Wr) + (i - nx));
-    }
-  }
   __syncthreads();
-  decode_route(A, xs, wrs, R);
-
-  if (blockIdx.x == 0 && A.Wr != nullptr) {
-    for (int a = threadIdx.x; a < R.nA; a += blockDim.x) {
-      A.topk_idx[a] = R.sel_e[a];
-      A.topk_w[a] = R.sel_a[a];
-    }
-    if (warp == 0) {
-      // aux = E*coef*sum_e (count_e/T)(P_e/T): lane e sums its expert
-      float acc = 0.f;
-      for (int e = lane; e < A.E; e += 32) {
-        float P = 0.f;
-        for (int t = 0; t < A.T; ++t) P += R.prob[t][e];
-        acc = fmaf(static_cast<float>(R.e_start[e + 1] - R.e_start[e]), P, acc);
+  if (!moe) {                                 // dense: the weights needed are known now
+    my_up = blockIdx.x < slices ? (slices - blockIdx.x + G - 1) / G : 0;
+    my_wd = my_dn;
+    if (tid == 0) issue_first();
+  }
+  {
+    // x as fp32; Wr (bf16) at the ring's start when it fits; logit bias
+    const bool wr_smem = moe && static_cast<size_t>(A.E) * H * 2 <= P.ring * stage;
+    const int nx = A.T * H / 8;
+    const int nw = wr_smem ? A.E * H / 8 : 0;
+    for (int i = tid; i < nx + nw; i += kDecThreads) {
+      if (i < nx) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(A.x) + i);
+        ulonglong2 lo, hi;
+        lo.x = bf2(w.x); lo.y = bf2(w.y); hi.x = bf2(w.z); hi.y = bf2(w.w);
+        reinterpret_cast<ulonglong2*>(xs)[2 * i] = lo;
+        reinterpret_cast<ulonglong2*>(xs)[2 * i + 1] = hi;
+      } else {
+        reinterpret_cast<uint4*>(ring)[i - nx] = __ldg(reinterpret_cast<const uint4*>(A.Wr) + (i - nx));
       }
-      acc = warp_allsum(acc);
-      const float invT = 1.0f / static_cast<float>(A.T);
-      if (lane == 0) *A.aux_loss = static_cast<float>(A.E) * A.coef * acc * invT * invT;
+    }
+    if (tid < MM_MAX_EXPERTS) s_bias[tid] = (moe && A.bias != nullptr && tid < A.E) ? A.bias[tid] : 0.f;
+    __syncthreads();
+    if (moe) {
+      decode_route(A, xs, wr_smem ? reinterpret_cast<const __nv_bfloat16*>(ring)
+                                  : static_cast<const __nv_bfloat16*>(A.Wr), s_bias, R);
+    } else {
+      if (tid < A.T) {
+        R.sel_a[tid] = 1.0f;
+        R.by_e[tid] = tid;
+      }
+      if (tid == 0) {
+        R.nA = A.T;
+        R.n_touched = 1;
+        R.touched[0] = 0;
+        R.e_start[0] = 0;
+        R.e_start[1] = A.T;
+      }
+      __syncthreads();
+    }
+  }
+  if (moe) {
+    n_touched = R.n_touched;
+    const int up_units = n_touched * slices;
+    my_up = blockIdx.x < up_units ? (up_units - blockIdx.x + G - 1) / G : 0;
+    my_wd = my_dn * n_touched;
+    if (blockIdx.x == 0) {
+      for (int a = tid; a < R.nA; a += kDecThreads) {
+        A.topk_idx[a] = R.sel_e[a];
+        A.topk_w[a] = R.sel_a[a];
+      }
+      if (warp == 1) {
+        // aux = E*coef*sum_e (count_e/T)(P_e/T): lane e sums its expert
+        float acc = 0.f;
+        for (int e = lane; e < A.E; e += 32) {
+          float Pe = 0.f;
+          for (int t = 0; t < A.T; ++t) Pe += R.prob[t][e];
+          acc = fmaf(static_cast<float>(R.cnt[e]), Pe, acc);
+        }
+        acc = warp_allsum(acc);
+        const float invT = 1.0f / static_cast<float>(A.T);
+        if (lane == 0) *A.aux_loss = static_cast<float>(A.E) * A.coef * acc * invT * invT;
+      }
+    }
+    __syncthreads();                          // Wr in the ring is no longer read
+    if (tid == 0) {
+      fence_proxy_async_smem();
+      issue_first();
     }
   }
 
-  // ---- work lists
-  const int slices = (I + kUpRows - 1) / kUpRows;
-  const int up_units = R.n_touched * slices;
-  const int dn_units = (H + kDnRows - 1) / kDnRows;
-  auto issue_up = [&](int unit, int b) {
-    fence_proxy_async_smem();
-    const int e = R.touched[unit / slices];
-    const int r0 = (unit % slices) * kUpRows;
-    const int rows = min(kUpRows, I - r0);
-    const uint32_t bytes = static_cast<uint32_t>(rows) * H * 2;
-    unsigned char* dst = ring + b * 2 * slice_bytes;
-    mbar_arrive_expect_tx(&bar[b], 2 * bytes);
-    bulk_load(dst, static_cast<const __nv_bfloat16*>(A.wg.p[e]) + static_cast<int64_t>(r0) * H,
-              bytes, &bar[b]);
-    bulk_load(dst + slice_bytes,
-              static_cast<const __nv_bfloat16*>(A.wu.p[e]) + static_cast<int64_t>(r0) * H, bytes,
-              &bar[b]);
-  };
-  auto issue_wd = [&](int unit, int ti, int b) {
-    fence_proxy_async_smem();
-    const int j0 = unit * kDnRows;
-    const int rows = min(kDnRows, H - j0);
-    const int e = R.touched[ti];
-    const uint32_t bytes = static_cast<uint32_t>(rows) * I * 2;
-    mbar_arrive_expect_tx(&bar[2 + b], bytes);
-    bulk_load(wdbuf + b * slot_bytes,
-              static_cast<const __nv_bfloat16*>(A.wd.p[e]) + static_cast<int64_t>(j0) * I, bytes,
-              &bar[2 + b]);
-  };
-  __syncthreads();                             // Wr in the h stage is no longer read
-  if (threadIdx.x == 0) {
-    if (blockIdx.x < up_units) {
-      issue_up(blockIdx.x, 0);
-      inflight[0] = true;
-    }
-    if (blockIdx.x < dn_units) {               // the first down unit's first two experts
-      for (int q = 0; q < 2 && q < R.n_touched; ++q) {
-        issue_wd(blockIdx.x, q, q);
-        inflight[2 + q] = true;
-      }
-    }
-  }
-
-  // ---- gate/up: units blockIdx.x, + gridDim.x, ...; warp w owns row w
+  // ---- gate/up: this CTA's units blockIdx.x + it*G; warp w owns row w
   bool ok = true;
-  for (int it = 0, u = blockIdx.x; ok && u < up_units; u += gridDim.x, ++it) {
-    const int b = it & 1;
-    const int nxt = u + static_cast<int>(gridDim.x);
-    __syncthreads();                           // buffer b^1 is no longer being read
-    if (threadIdx.x == 0 && nxt < up_units) {
-      issue_up(nxt, b ^ 1);
-      inflight[b ^ 1] = true;
-    }
-    ok = __syncthreads_and(mbar_wait(&bar[b], phase[b], nullptr, A.hdr, 20));
+  for (int it = 0; ok && it < my_up; ++it) {
+    const int s = it % P.ring;
+    ok = __syncthreads_and(mbar_wait(&ring_bar[s], (it / P.ring) & 1, nullptr, A.hdr, 20));
     if (!ok) break;
-    phase[b] ^= 1;
-    inflight[b] = false;
-    const int e = R.touched[u / slices];
+    up_used = it + 1;
+    const int u = blockIdx.x + it * G;
+    const int e = moe ? R.touched[u / slices] : 0;
     const int i = (u % slices) * kUpRows + warp;
-    if (i >= I) continue;
-    const __nv_bfloat16* grow = reinterpret_cast<const __nv_bfloat16*>(ring + b * 2 * slice_bytes) + warp * H;
+    const __nv_bfloat16* grow = reinterpret_cast<const __nv_bfloat16*>(ring + s * stage) + warp * H;
     const __nv_bfloat16* urow = grow + kUpRows * H;
-    const int* list = R.by_e + R.e_start[e];   // the assignments of expert e, in order
+    const int* list = R.by_e + R.e_start[e];  // the assignments of expert e, in order
     const int n = R.e_start[e + 1] - R.e_start[e];
-    for (int g0 = 0; g0 < n; g0 += kTokGroup) {
-      // 2*kTokGroup independent partial sums: g_t and u_t of up to 8 tokens
-      float v[2 * kTokGroup];
-#pragma unroll
-      for (int q = 0; q < 2 * kTokGroup; ++q) v[q] = 0.f;
-      for (int c = lane; c < H / 8; c += 32) {
-        float gv[8], uv[8];
-        cvt8(*reinterpret_cast<const uint4*>(grow + c * 8), gv);
-        cvt8(*reinterpret_cast<const uint4*>(urow + c * 8), uv);
-#pragma unroll
-        for (int tt = 0; tt < kTokGroup; ++tt) {
-          if (g0 + tt < n) {
-            const int a = list[g0 + tt];
-            const int t = (A.Wr != nullptr) ? a / A.k : a;
-            float xv[8];
-            cvt8(*reinterpret_cast<const uint4*>(xs + t * H + c * 8), xv);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              v[2 * tt] = fmaf(gv[q], xv[q], v[2 * tt]);
-              v[2 * tt + 1] = fmaf(uv[q], xv[q], v[2 * tt + 1]);
-            }
-          }
-        }
-      }
-      // butterfly reduce-scatter of the 16 sums: lane L ends with the full
-      // sum of value L >> 1 (value 2t = g_t, 2t + 1 = u_t)
-#pragma unroll
-      for (int o = 16; o >= 2; o >>= 1) {
-        const bool up = (lane & o) != 0;
-#pragma unroll
-        for (int q = 0; q < o / 2; ++q) {
-          const float lo = v[q], hi = v[q + o / 2];
-          v[q] = (up ? hi : lo) + __shfl_xor_sync(0xffffffffu, up ? lo : hi, o);
-        }
-      }
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-      const float u_val = __shfl_down_sync(0xffffffffu, v[0], 2);   // lane L+2 holds u_t
-      const int tt = lane >> 2;
-      if ((lane & 3) == 0 && g0 + tt < n)
-        A.h[static_cast<int64_t>(list[g0 + tt]) * I + i] = __float2half_rn(silu_f32(v[0]) * u_val);
+    for (int g0 = 0; g0 < n; g0 += 8) {
+      const int m = min(8, n - g0);
+      if (m == 1)
+        gateup_row<1>(grow, urow, xs, list + g0, m, kk, H, I, i, A.h, lane);
+      else if (m == 2)
+        gateup_row<2>(grow, urow, xs, list + g0, m, kk, H, I, i, A.h, lane);
+      else if (m <= 4)
+        gateup_row<4>(grow, urow, xs, list + g0, m, kk, H, I, i, A.h, lane);
+      else
+        gateup_row<8>(grow, urow, xs, list + g0, m, kk, H, I, i, A.h, lane);
+    }
+    __syncthreads();                          // stage s is no longer read
+    if (tid == 0 && it + P.ring < my_up) {
+      fence_proxy_async_smem();
+      issue_up(it + P.ring);
     }
   }
 
   // ---- every h row written before any CTA reads it
+  unsigned ticket = 0xffffffffu;
   if (ok) {
     asm volatile("fence.proxy.async.global;" ::: "memory");
-    ok = grid_barrier(A.hdr, 24);
+    ok = grid_barrier(A.hdr, 24, &ticket);
   }
 
-  // ---- down: unit = kDnRows output rows, every touched expert
-  const int kk = (A.Wr != nullptr) ? A.k : 1;
-  for (int du = blockIdx.x, round = 0; ok && du < dn_units; du += gridDim.x, ++round) {
-    const int j0 = du * kDnRows;
-    const int rows = min(kDnRows, H - j0);
-    if (round > 0 && threadIdx.x == 0) {       // later units: fetch their first two experts now
-      for (int q = 0; q < 2 && q < R.n_touched; ++q) {
-        issue_wd(du, q, q);
-        inflight[2 + q] = true;
-      }
-    }
-    bool waited[2] = {false, false};
+  // ---- down: unit = kDnRows output columns, every touched expert
+  const int nA = R.nA;
+  const bool h_once = nA <= P.h_rows;         // one stage serves every unit
+  for (int r = 0; ok && r < my_dn; ++r) {
+    const int j0 = (blockIdx.x + r * G) * kDnRows;
     int ti = 0;
-    for (int q0 = 0; ok && q0 < R.nA;) {
-      const int q1 = min(R.nA, q0 + kHStage);
-      __syncthreads();                         // the previous stage is no longer read
-      if (threadIdx.x == 0) {
-        fence_proxy_async_smem();
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        mbar_arrive_expect_tx(&bar[4], static_cast<uint32_t>(q1 - q0) * I * 2);
-        for (int q = q0; q < q1; ++q)
-          bulk_load(hst + static_cast<size_t>(q - q0) * I, A.h + static_cast<int64_t>(R.by_e[q]) * I,
-                    static_cast<uint32_t>(I) * 2, &bar[4]);
-        inflight[4] = true;
+    __syncthreads();                          // part[] of the previous unit is read
+    for (int q0 = 0; ok && q0 < nA; q0 += P.h_rows) {
+      const int q1 = min(nA, q0 + P.h_rows);
+      if (!(h_once && r > 0)) {
+        __syncthreads();                      // the previous stage is no longer read
+        if (tid == 0) {
+          fence_proxy_async_smem();
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          mbar_arrive_expect_tx(h_bar, static_cast<uint32_t>(q1 - q0) * I * 4);
+          for (int q = q0; q < q1; ++q)
+            bulk_load(hst + static_cast<size_t>(q - q0) * I, A.h + static_cast<size_t>(R.by_e[q]) * I,
+                      static_cast<uint32_t>(I) * 4, h_bar);
+          ++h_issued;
+        }
+        ok = __syncthreads_and(mbar_wait(h_bar, h_used & 1, nullptr, A.hdr, 21));
+        if (!ok) break;
+        ++h_used;
       }
-      ok = __syncthreads_and(mbar_wait(&bar[4], phase[4], nullptr, A.hdr, 21));
-      if (!ok) break;
-      phase[4] ^= 1;
-      inflight[4] = false;
-      while (ti < R.n_touched) {
+      while (ti < n_touched) {
         const int e = R.touched[ti];
-        if (R.e_start[e] >= q1) break;         // its rows come with a later stage
+        if (R.e_start[e] >= q1) break;        // its rows come with a later stage
         const int ea = max(R.e_start[e], q0), eb = min(R.e_start[e + 1], q1);
-        const int b = ti & 1;
-        if (!waited[b]) {
-          ok = __syncthreads_and(mbar_wait(&bar[2 + b], phase[2 + b], nullptr, A.hdr, 22));
+        const int q = r * n_touched + ti;     // Wd copy index
+        const int b = q % P.wd_slots;
+        if (q >= wd_used) {
+          ok = __syncthreads_and(mbar_wait(&wd_bar[b], (q / P.wd_slots) & 1, nullptr, A.hdr, 22));
           if (!ok) break;
-          waited[b] = true;
+          wd_used = q + 1;
         }
-        const __nv_bfloat16* ws = reinterpret_cast<const __nv_bfloat16*>(wdbuf + b * slot_bytes);
-        // warp w: row w % kDnRows; the expert's assignments in this stage four
-        // at a time, round-robin over the warps of that row
-        constexpr int kWarpsPerRow = kDecWarps / kDnRows;
+        // warp w: column w % kDnRows; the expert's staged rows four at a
+        // time, round-robin over the warps of that column
+        constexpr int kWarpsPerCol = kDecWarps / kDnRows;
         const int jl = warp % kDnRows;
-        if (jl < rows) {
-          for (int g0 = ea + (warp / kDnRows) * 4; g0 < eb; g0 += 4 * kWarpsPerRow) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int c = lane; c < I / 8; c += 32) {
-              float wv[8];
-              cvt8(*reinterpret_cast<const uint4*>(ws + jl * I + c * 8), wv);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                if (g0 + q < eb) {
-                  float hv[8];
-                  cvt8h(*reinterpret_cast<const uint4*>(hst + static_cast<size_t>(g0 + q - q0) * I + c * 8), hv);
-#pragma unroll
-                  for (int j = 0; j < 8; ++j) acc[q] = fmaf(wv[j], hv[j], acc[q]);
-                }
-              }
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[q] = warp_allsum(acc[q]);
-            if (lane < 4 && g0 + lane < eb) {
-              float val = acc[0];
-#pragma unroll
-              for (int q = 1; q < 4; ++q)
-                if (lane == q) val = acc[q];
-              part[R.by_e[g0 + lane]][jl] = val;
-            }
-          }
+        const __nv_bfloat16* wrow = reinterpret_cast<const __nv_bfloat16*>(wdbuf + b * slot) + jl * I;
+        for (int g0 = ea + (warp / kDnRows) * 4; g0 < eb; g0 += 4 * kWarpsPerCol) {
+          const int m = min(4, eb - g0);
+          if (m == 1)
+            down_row<1>(wrow, hst, g0 - q0, R.by_e + g0, m, I, jl, part, lane);
+          else if (m == 2)
+            down_row<2>(wrow, hst, g0 - q0, R.by_e + g0, m, I, jl, part, lane);
+          else
+            down_row<4>(wrow, hst, g0 - q0, R.by_e + g0, m, I, jl, part, lane);
         }
-        if (R.e_start[e + 1] > q1) break;      // e continues in the next stage
-        __syncthreads();                       // e is done: its slot takes the expert after next
-        phase[2 + b] ^= 1;
-        waited[b] = false;
-        if (threadIdx.x == 0) {
-          inflight[2 + b] = false;
-          if (ti + 2 < R.n_touched) {
-            issue_wd(du, ti + 2, b);
-            inflight[2 + b] = true;
-          }
+        if (R.e_start[e + 1] > q1) break;     // e continues in the next stage
+        __syncthreads();                      // e is done: its buffer takes a later copy
+        if (tid == 0 && q + P.wd_slots < my_wd) {
+          fence_proxy_async_smem();
+          issue_wd(q + P.wd_slots);
         }
         ++ti;
       }
-      q0 = q1;
     }
     __syncthreads();
     if (!ok) break;
-    for (int q = threadIdx.x; q < A.T * rows; q += blockDim.x) {
-      const int t = q / rows, jl = q % rows;
+    for (int q = tid; q < A.T * kDnRows; q += kDecThreads) {
+      const int t = q / kDnRows, jl = q % kDnRows;
       float v = 0.f;
-      for (int s = 0; s < kk; ++s) v += R.sel_a[t * kk + s] * part[t * kk + s][jl];
-      static_cast<__nv_bfloat16*>(A.y)[static_cast<int64_t>(t) * H + j0 + jl] = __float2bfloat16_rn(v);
+      for (int s = 0; s < kk; ++s) v = fmaf(R.sel_a[t * kk + s], part[t * kk + s][jl], v);
+      static_cast<__nv_bfloat16*>(A.y)[static_cast<size_t>(t) * H + j0 + jl] = __float2bfloat16_rn(v);
     }
   }
-  // let copies still in flight (a unit this CTA did not reach, or a failed
-  // wait) land before the CTA exits
-  if (threadIdx.x == 0)
-    for (int q = 0; q < 5; ++q)
-      if (inflight[q]) mbar_wait(&bar[q], phase[q], nullptr, nullptr, 25);
+  if (tid == 0) {
+    // copies still in flight (a unit not reached after a failed wait) land
+    // before the CTA exits
+    for (int it = up_used; it < up_issued; ++it)
+      mbar_wait(&ring_bar[it % P.ring], (it / P.ring) & 1, nullptr, nullptr, 25);
+    for (int q = wd_used; q < wd_issued; ++q)
+      mbar_wait(&wd_bar[q % P.wd_slots], (q / P.wd_slots) & 1, nullptr, nullptr, 25);
+    if (h_issued > h_used) mbar_wait(h_bar, h_used & 1, nullptr, nullptr, 25);
+    grid_barrier_reset(A.hdr, ticket);
+  }
 }
 
+namespace {
+
+size_t round128(size_t v) { return (v + 127) & ~size_t(127); }
+
+// Shared-memory plan: as many gate/up stages and Wd buffers as fit; two CTAs
+// per SM when the smallest plan leaves room for a second one.
+DecPlan decode_plan(int T, int H, int I, int nA) {
+  const size_t x = round128(static_cast<size_t>(T) * H * 4);
+  const size_t stage = 2 * static_cast<size_t>(kUpRows) * H * 2;
+  const size_t slot = static_cast<size_t>(kDnRows) * I * 2;
+  const size_t hrow = static_cast<size_t>(I) * 4;
+  auto layout = [&](DecPlan& p) {
+    p.ring_off = static_cast<uint32_t>(x);
+    const size_t a = x + p.ring * stage;
+    const size_t b = static_cast<size_t>(p.h_rows) * hrow;
+    p.wd_off = static_cast<uint32_t>(round128(a > b ? a : b));
+    return static_cast<size_t>(p.wd_off) + p.wd_slots * slot;
+  };
+  DecPlan p;
+  p.ring = 2;
+  p.wd_slots = 2;
+  p.h_rows = nA < kMaxHRows ? nA : kMaxHRows;
+  p.per_sm = 1;
+  while (p.h_rows > 1 && layout(p) > kDecSmemBudget) --p.h_rows;
+  size_t total = layout(p);
+  if (total > kDecSmemBudget) {
+    p.total = 0;                              // does not fit
+    return p;
+  }
+  if (total <= kDecSmemTwoPerSm) {
+    p.per_sm = 2;
+  } else {
+    // grow the gate/up ring and the Wd buffers in turn while they fit
+    const int order[6][2] = {{3, 2}, {3, 3}, {4, 3}, {4, 4}, {5, 4}, {6, 4}};
+    for (const auto& o : order) {
+      DecPlan q = p;
+      q.ring = o[0];
+      q.wd_slots = o[1];
+      if (layout(q) <= kDecSmemBudget) p = q;
+    }
+    total = layout(p);
+  }
+  p.total = static_cast<uint32_t>(total);
+  return p;
+}
+
+}  // namespace
+
 size_t decode_smem_bytes(int T, int H, int I, int E, int k) {
-  return dec_layout(T, H, I, E, T * k).total;
+  const DecPlan p = decode_plan(T, H, I, T * (E > 1 ? k : 1));
+  return p.total == 0 ? ~size_t(0) : p.total;
 }
 
 cudaError_t launch_decode_ffn(const void* x, const void* Wr, const float* bias,
@@ -526,16 +667,18 @@ cudaError_t launch_decode_ffn(const void* x, const void* Wr, const float* bias,
   }
   A.T = T; A.H = H; A.I = I; A.E = nw; A.k = (Wr != nullptr) ? k : 1; A.coef = coef;
   A.topk_idx = topk_idx; A.topk_w = topk_w; A.aux_loss = aux_loss;
-  A.h = static_cast<__half*>(hbuf); A.y = y; A.hdr = hdr;
-  const size_t smem = dec_layout(T, H, I, nw, T * A.k).total;
+  A.h = static_cast<float*>(hbuf); A.y = y; A.hdr = hdr;
+  A.plan = decode_plan(T, H, I, T * A.k);
+  if (A.plan.total == 0) return cudaErrorInvalidValue;
+  const size_t smem = A.plan.total;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(decode_ffn_kernel), smem);
   if (e != cudaSuccess) return e;
-  // every CTA must be resident (grid barrier): as many as fit, at most two per SM
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_ffn_kernel, kDecThreads, smem);
+  // every CTA must be resident (grid barrier)
+  int fit = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, decode_ffn_kernel, kDecThreads, smem);
   if (e != cudaSuccess) return e;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  const int grid = num_sms() * (per_sm < 2 ? per_sm : 2);
+  if (fit < 1) return cudaErrorInvalidConfiguration;
+  const int grid = num_sms() * (fit < A.plan.per_sm ? fit : A.plan.per_sm);
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(grid);

@@ -14,8 +14,8 @@ namespace mm {
 struct WsHeader {
   unsigned int status;        // MM_ERR_* bits set by device code (0 = fine)
   unsigned int where;         // role id of the first wait that gave up
-  unsigned int bar_count;     // grid barrier: CTAs arrived in the current round (0 between rounds)
-  unsigned int bar_gen;       // grid barrier: completed rounds (wraps)
+  unsigned int bar_count;     // grid barrier: CTAs arrived (0 between launches)
+  unsigned int bar_leave;     // grid barrier: CTAs released (0 between launches)
   unsigned int pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
@@ -91,39 +91,47 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-// Grid-wide barrier for a cooperative launch (every CTA resident).  The last
-// CTA to arrive resets the count and advances the generation; the others wait
-// (bounded) for the generation to change.  Works from any state the header
-// was left in by completed calls.  Returns false if the wait gave up.
-__device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned where) {
+// One grid-wide barrier per launch for a cooperative grid (every CTA
+// resident).  Arrival is a release add on bar_count; each CTA then polls
+// bar_count with acquire loads until all gridDim.x CTAs have arrived.  Once
+// through, each CTA takes a ticket on bar_leave; the CTA holding the last
+// ticket is the last one that could still read bar_count, and it returns both
+// words to 0 in grid_barrier_reset() at its end, ready for the next launch.
+// The poll gives up after kWaitLimitNs (reported, returns false).
+__device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned where, unsigned* ticket) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
-    volatile unsigned int* gen = &hdr->bar_gen;
-    const unsigned int g0 = *gen;
-    __threadfence();
-    const unsigned int arrived = atomicAdd(&hdr->bar_count, 1u) + 1u;
+    const unsigned int G = gridDim.x * gridDim.y * gridDim.z;
+    unsigned int* cnt = &hdr->bar_count;
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(cnt) : "memory");
     int ok = 1;
-    if (arrived == gridDim.x * gridDim.y * gridDim.z) {
-      hdr->bar_count = 0;
-      __threadfence();
-      atomicAdd(&hdr->bar_gen, 1u);
-    } else {
-      const unsigned long long t0 = globaltimer_ns();
-      uint32_t n = 0;
-      while (*gen == g0) {
-        if ((++n & 63u) == 0u && (globaltimer_ns() - t0 > kWaitLimitNs || n > (1u << 30))) {
-          report_timeout(hdr, where);
-          ok = 0;
-          break;
-        }
+    const unsigned long long t0 = globaltimer_ns();
+    uint32_t n = 0;
+    for (;;) {
+      unsigned int v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+      if (v >= G) break;
+      if ((++n & 63u) == 0u && (globaltimer_ns() - t0 > kWaitLimitNs || n > (1u << 30))) {
+        report_timeout(hdr, where);
+        ok = 0;
+        break;
       }
     }
-    __threadfence();
+    *ticket = ok ? atomicAdd(&hdr->bar_leave, 1u) : 0xffffffffu;
     s_ok = ok;
   }
   __syncthreads();
   return s_ok != 0;
+}
+
+// Called by thread 0 at the very end of the CTA with the ticket from
+// grid_barrier (a failed barrier hands out 0xffffffff, which never resets).
+__device__ __forceinline__ void grid_barrier_reset(WsHeader* hdr, unsigned ticket) {
+  if (ticket + 1u == gridDim.x * gridDim.y * gridDim.z) {
+    hdr->bar_count = 0u;
+    hdr->bar_leave = 0u;
+  }
 }
 
 // ---------------------------------------------------------------- TMA

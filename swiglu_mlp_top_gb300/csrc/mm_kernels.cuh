@@ -92,7 +92,7 @@ cudaError_t launch_convert_bf16_to_f16(const void* const* src, int n_mat, int64_
                                        void* dst, cudaStream_t st);
 
 // Decode-sized forward on the CUDA cores (T <= kDecodeMaxT, bf16): one
-// cooperative kernel routes (MoE: Wr != nullptr), writes the fp16 h [T*k, I]
+// cooperative kernel routes (MoE: Wr != nullptr), writes the fp32 h [T*k, I]
 // (dense: [T, I]) into hbuf, meets every other CTA at a grid barrier kept in
 // the workspace header, and forms y.  Block 0 writes topk_idx / topk_w /
 // aux_loss (MoE).  decode_smem_bytes is its dynamic shared memory (dense: E = k = 1).
