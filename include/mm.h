@@ -14,7 +14,8 @@
  *       Wg, Wu: [I, H]   Wd: [H, I]   Wr: [E, H]   x, y: [T, H].
  *   - dtype selects the element type of x, the weights and y:
  *       MM_DTYPE_BF16 — bf16 storage, fp32 accumulation (tcgen05 tensor
- *                       cores for T > 16, weight streaming for T <= 16);
+ *                       cores; for T <= 64 one weight-streaming kernel
+ *                       that reads every needed weight row once);
  *       MM_DTYPE_F32  — fp32 storage and fp32 SIMT arithmetic (no TF32).
  *     Router logits, probabilities, alpha and the aux loss are always fp32.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
@@ -58,10 +59,11 @@ typedef enum { MM_DTYPE_F32 = 0, MM_DTYPE_BF16 = 1 } mm_dtype;
 
 /* Which kernels carry the FFN part of a call (the *_ex entry points). */
 typedef enum {
-  MM_PATH_AUTO = 0,    /* bf16: tensor-core GEMMs if T > 16, else streaming; f32: SIMT */
+  MM_PATH_AUTO = 0,    /* bf16: streaming up to 64 tokens, tensor-core GEMMs beyond; f32: SIMT */
   MM_PATH_TENSOR = 1,  /* bf16 only: grouped tcgen05/TMEM GEMMs fed by TMA          */
-  MM_PATH_STREAM = 2,  /* bf16 only: decode-shaped weight-streaming kernels          */
-  MM_PATH_SIMT = 3     /* any dtype: plain fp32-FMA CUDA-core kernels                */
+  MM_PATH_STREAM = 2,  /* bf16 only, T <= 16: weight streaming on the CUDA cores       */
+  MM_PATH_SIMT = 3,    /* any dtype: plain fp32-FMA CUDA-core kernels                */
+  MM_PATH_STREAM_TC = 4 /* bf16 only, T <= 64: weight streaming on the tensor cores   */
 } mm_path;
 
 /* Limits of this build. */
@@ -210,7 +212,8 @@ typedef enum {
   MM_KERNEL_DISPATCH = 3,   /* token permute into expert-contiguous rows    */
   MM_KERNEL_GATEUP = 4,     /* gate/up GEMM with the SwiGLU epilogue        */
   MM_KERNEL_DOWN = 5,       /* down GEMM with the alpha-scaled combine      */
-  MM_KERNEL_WCONVERT = 6    /* bf16 -> fp16 copy of the down weights        */
+  MM_KERNEL_WCONVERT = 6,   /* bf16 -> fp16 copy of the down weights        */
+  MM_KERNEL_DECODE = 7      /* decode-sized weight-streaming kernel (whole call) */
 } mm_kernel_id;
 
 /* Number of kernels this library has enqueued since it was loaded. */

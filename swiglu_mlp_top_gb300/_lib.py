@@ -12,7 +12,7 @@ LIB_PATH = os.path.join(_PKG, "libmm.so")
 
 MM_OK, MM_ERR_INVALID_ARG, MM_ERR_UNSUPPORTED, MM_ERR_WORKSPACE, MM_ERR_CUDA, MM_ERR_TIMEOUT = range(6)
 MM_DTYPE_F32, MM_DTYPE_BF16 = 0, 1
-MM_PATH_AUTO, MM_PATH_TENSOR, MM_PATH_STREAM, MM_PATH_SIMT = 0, 1, 2, 3
+MM_PATH_AUTO, MM_PATH_TENSOR, MM_PATH_STREAM, MM_PATH_SIMT, MM_PATH_STREAM_TC = 0, 1, 2, 3, 4
 MM_MAX_EXPERTS = 64
 MM_MAX_TOPK = 8
 MM_NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -44,7 +44,8 @@ SIGNATURES = {
     "mm_profile_start": (_i32, [_i32, _i32]),
     "mm_profile_stop": (_i32, [C.POINTER(C.c_double), C.POINTER(C.c_int)]),
 }
-MM_KERNEL_ROUTER, MM_KERNEL_SCAN, MM_KERNEL_DISPATCH, MM_KERNEL_GATEUP, MM_KERNEL_DOWN, MM_KERNEL_WCONVERT = 1, 2, 3, 4, 5, 6
+(MM_KERNEL_ROUTER, MM_KERNEL_SCAN, MM_KERNEL_DISPATCH, MM_KERNEL_GATEUP, MM_KERNEL_DOWN, MM_KERNEL_WCONVERT,
+ MM_KERNEL_DECODE) = 1, 2, 3, 4, 5, 6, 7
 
 _lib = None
 

@@ -55,14 +55,9 @@ MoeLayout moe_layout(int64_t T, int H, int I, int E, int k, int dtype) {
   L.xp = off;       off += align_up(es * rows * H);
   L.h = off;        off += align_up(h_bytes(dtype) * rows * I);
   L.acc32 = off;    if (k >= 2 && dtype == kDtypeBF16) off += align_up(4 * static_cast<size_t>(T) * H);
-  // bf16: fp16 copy of the E down matrices (tensor path) or, for decode-sized
-  // T, the fp32 h of the streaming path; whichever is larger
+  // bf16: fp16 copy of the E down matrices
   L.wd16 = off;
-  if (dtype == kDtypeBF16) {
-    size_t need = 2 * static_cast<size_t>(E) * H * I;
-    if (T <= kDecodeMaxT) need = std::max(need, 4 * rows * static_cast<size_t>(I));
-    off += align_up(need);
-  }
+  if (dtype == kDtypeBF16) off += align_up(2 * static_cast<size_t>(E) * H * I);
   L.total = off;
   return L;
 }
@@ -80,13 +75,12 @@ RouteLayout route_layout(int64_t T, int E, int k) {
   return L;
 }
 
-// Dense workspace: h [T, I], then (bf16) the fp16 copy of Wd.  The
-// streaming path (bf16, T <= kDecodeMaxT) keeps h in fp32.
+// Dense workspace of the tensor-core and SIMT paths: h [T, I], then (bf16)
+// the fp16 copy of Wd.
 size_t dense_h_bytes(int64_t T, int I, int dtype) {
-  const size_t eb = (dtype == kDtypeBF16 && T <= kDecodeMaxT) ? 4 : h_bytes(dtype);
-  return align_up(eb * static_cast<size_t>(T) * I);
+  return align_up(h_bytes(dtype) * static_cast<size_t>(T) * I);
 }
-size_t dense_ws_bytes(int64_t T, int H, int I, int dtype) {
+size_t dense_tensor_ws_bytes(int64_t T, int H, int I, int dtype) {
   return sizeof(WsHeader) + dense_h_bytes(T, I, dtype) +
          (dtype == kDtypeBF16 ? align_up(2 * static_cast<size_t>(H) * I) : 0);
 }
@@ -96,20 +90,74 @@ bool valid_dtype(int dtype) { return dtype == kDtypeF32 || dtype == kDtypeBF16; 
 // bf16 tensor-core / streaming kernels tile K and N by 64
 bool tensor_shape_ok(int H, int I) { return H % 64 == 0 && I % 64 == 0; }
 
-// AUTO: fp32 -> CUDA-core kernels; bf16 -> weight streaming for decode-sized
-// T (every weight row read once), tensor cores otherwise.
-int resolve_path(int path, int dtype, int64_t T) {
-  if (path == MM_PATH_AUTO) {
-    if (dtype == kDtypeF32) return MM_PATH_SIMT;
-    return T <= kDecodeMaxT ? MM_PATH_STREAM : MM_PATH_TENSOR;
-  }
-  return path;
+// Scratch (after the header) of the two weight-streaming kernels; 0 when the
+// shape is outside the kernel's limits.  E = k = 1 for the dense FFN.
+size_t stream_simt_bytes(int64_t T, int H, int I, int E, int k, int dtype) {
+  if (dtype != kDtypeBF16 || T < 1 || T > kDecodeMaxT) return 0;
+  if (decode_smem_bytes(static_cast<int>(T), H, I, E, k) > 200 * 1024) return 0;
+  return align_up(4 * static_cast<size_t>(T) * k * I);    // fp32 h
+}
+size_t stream_tc_bytes(int64_t T, int H, int I, int E, int k, int dtype) {
+  if (dtype != kDtypeBF16 || T < 1 || T > kDecodeTcMaxT) return 0;
+  return decode_tc_bytes(static_cast<int>(T), H, I, E, k);
 }
 
-bool stream_shape_ok(int64_t T, int H, int I, int E, int k, int dtype) {
-  return dtype == kDtypeBF16 && T <= kDecodeMaxT &&
-         decode_smem_bytes(static_cast<int>(T), H, I, E, k) <= 200 * 1024;
+// Workspace of one path (0: the path does not take this shape), and the
+// workspace that serves every path valid for the shape.
+size_t dense_path_bytes(int64_t T, int H, int I, int dtype, int p) {
+  size_t b = 0;
+  switch (p) {
+    case MM_PATH_STREAM: b = stream_simt_bytes(T, H, I, 1, 1, dtype); break;
+    case MM_PATH_STREAM_TC: b = stream_tc_bytes(T, H, I, 1, 1, dtype); break;
+    default: return dense_tensor_ws_bytes(T, H, I, dtype);
+  }
+  return b ? sizeof(WsHeader) + b : 0;
 }
+size_t dense_ws_bytes(int64_t T, int H, int I, int dtype) {
+  size_t need = dense_tensor_ws_bytes(T, H, I, dtype);
+  need = std::max(need, dense_path_bytes(T, H, I, dtype, MM_PATH_STREAM));
+  need = std::max(need, dense_path_bytes(T, H, I, dtype, MM_PATH_STREAM_TC));
+  return need;
+}
+size_t moe_path_bytes(int64_t T, int H, int I, int E, int k, int dtype, int p) {
+  size_t b = 0;
+  switch (p) {
+    case MM_PATH_STREAM: b = stream_simt_bytes(T, H, I, E, k, dtype); break;
+    case MM_PATH_STREAM_TC: b = stream_tc_bytes(T, H, I, E, k, dtype); break;
+    default: return moe_layout(T, H, I, E, k, dtype).total;
+  }
+  return b ? sizeof(WsHeader) + b : 0;
+}
+size_t moe_ws_bytes(int64_t T, int H, int I, int E, int k, int dtype) {
+  size_t need = moe_layout(T, H, I, E, k, dtype).total;
+  need = std::max(need, moe_path_bytes(T, H, I, E, k, dtype, MM_PATH_STREAM));
+  need = std::max(need, moe_path_bytes(T, H, I, E, k, dtype, MM_PATH_STREAM_TC));
+  return need;
+}
+
+// AUTO: fp32 -> CUDA-core kernels.  bf16 -> weight streaming for decode-sized
+// T (every weight row read once): on the CUDA cores up to kStreamSimtAutoT
+// tokens, on the tensor cores up to kDecodeTcMaxT; tensor-core GEMMs beyond.
+constexpr int64_t kStreamSimtAutoT = 4;
+int resolve_path(int path, int dtype, int64_t T, int H, int I, int E, int k) {
+  if (path != MM_PATH_AUTO) return path;
+  if (dtype == kDtypeF32) return MM_PATH_SIMT;
+  if (T <= kStreamSimtAutoT && stream_simt_bytes(T, H, I, E, k, dtype) > 0) return MM_PATH_STREAM;
+  if (stream_tc_bytes(T, H, I, E, k, dtype) > 0) return MM_PATH_STREAM_TC;
+  if (stream_simt_bytes(T, H, I, E, k, dtype) > 0) return MM_PATH_STREAM;
+  return MM_PATH_TENSOR;
+}
+
+}  // namespace
+
+// Workspace of the path that AUTO (or `path`) resolves to for a dense call; 0
+// when that path does not take the shape.  Used by the no-allocation entry.
+size_t dense_workspace_for_path(int64_t T, int H, int I, int dtype, int path) {
+  if (T < 1 || H < 1 || I < 1 || !valid_dtype(dtype)) return 0;
+  return dense_path_bytes(T, H, I, dtype, resolve_path(path, dtype, T, H, I, 1, 1));
+}
+
+namespace {
 
 inline char* ws_at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
 
@@ -189,29 +237,33 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
   if (!valid_dtype(dtype) || T < 0 || H < 1 || I < 1) return MM_ERR_INVALID_ARG;
   if (H % 8 != 0 || I % 8 != 0) return MM_ERR_UNSUPPORTED;
   if (T > (int64_t{1} << 30)) return MM_ERR_UNSUPPORTED;
-  if (path < MM_PATH_AUTO || path > MM_PATH_SIMT) return MM_ERR_INVALID_ARG;
+  if (path < MM_PATH_AUTO || path > MM_PATH_STREAM_TC) return MM_ERR_INVALID_ARG;
   if (T == 0) return MM_OK;
   if (!x || !Wg || !Wu || !Wd || !y) return MM_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) || !aligned16(y))
     return MM_ERR_INVALID_ARG;
   if (!workspace || !aligned16(workspace)) return MM_ERR_WORKSPACE;
-  if (workspace_bytes < dense_ws_bytes(T, H, I, dtype)) return MM_ERR_WORKSPACE;
-  const int p = resolve_path(path, dtype, T);
+  const int p = resolve_path(path, dtype, T, H, I, 1, 1);
   if (p == MM_PATH_TENSOR && (dtype != kDtypeBF16 || !tensor_shape_ok(H, I)))
     return MM_ERR_UNSUPPORTED;
-  if (p == MM_PATH_STREAM && !stream_shape_ok(T, H, I, 1, 1, dtype)) return MM_ERR_UNSUPPORTED;
+  const size_t need = dense_path_bytes(T, H, I, dtype, p);
+  if (need == 0) return MM_ERR_UNSUPPORTED;
+  if (workspace_bytes < need) return MM_ERR_WORKSPACE;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
   void* h = ws_at(workspace, sizeof(WsHeader));
-  if (p == MM_PATH_STREAM) {
-    // fp32 h [T, I] in the workspace's h area
+  if (p == MM_PATH_STREAM || p == MM_PATH_STREAM_TC) {
+    // scratch (fp32 h, or the tensor-core kernel's buffers) after the header
     const void* wg1[1] = {Wg};
     const void* wu1[1] = {Wu};
     const void* wd1[1] = {Wd};
-    cudaError_t e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
-      return launch_decode_ffn(x, nullptr, nullptr, wg1, wu1, wd1, static_cast<int>(T), H, I, 1, 1,
-                               0.f, nullptr, nullptr, nullptr, h, y, hdr, st);
+    cudaError_t e = counted_launch(MM_KERNEL_DECODE, st, [&] {
+      if (p == MM_PATH_STREAM)
+        return launch_decode_ffn(x, nullptr, nullptr, wg1, wu1, wd1, static_cast<int>(T), H, I, 1,
+                                 1, 0.f, nullptr, nullptr, nullptr, h, y, hdr, st);
+      return launch_decode_tc(x, nullptr, nullptr, wg1, wu1, wd1, static_cast<int>(T), H, I, 1, 1,
+                              0.f, nullptr, nullptr, nullptr, h, y, hdr, st);
     });
     if (e != cudaSuccess) return cuda_fail(e, "stream ffn");
     return MM_OK;
@@ -254,7 +306,7 @@ size_t mm_moe_workspace_bytes(int64_t T, int H, int I, int E, int k, int dtype) 
       !valid_dtype(dtype))
     return 0;
   if (k > MM_MAX_TOPK) return 0;
-  return moe_layout(T, H, I, E, k, dtype).total;
+  return moe_ws_bytes(T, H, I, E, k, dtype);
 }
 
 static int check_route_args(const void* x, const void* Wr, int64_t T, int H, int E, int k,
@@ -283,22 +335,37 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
   if (rc != MM_OK) return rc;
   if (I < 1) return MM_ERR_INVALID_ARG;
   if (I % 8 != 0) return MM_ERR_UNSUPPORTED;
-  if (path < MM_PATH_AUTO || path > MM_PATH_SIMT) return MM_ERR_INVALID_ARG;
+  if (path < MM_PATH_AUTO || path > MM_PATH_STREAM_TC) return MM_ERR_INVALID_ARG;
   if (!Wg || !Wu || !Wd || !y || !aligned16(y)) return MM_ERR_INVALID_ARG;
   for (int e = 0; e < E; ++e) {
     if (!Wg[e] || !Wu[e] || !Wd[e]) return MM_ERR_INVALID_ARG;
     if (!aligned16(Wg[e]) || !aligned16(Wu[e]) || !aligned16(Wd[e])) return MM_ERR_INVALID_ARG;
   }
   if (!workspace || !aligned16(workspace)) return MM_ERR_WORKSPACE;
-  const MoeLayout L = moe_layout(T, H, I, E, k, dtype);
-  if (workspace_bytes < L.total) return MM_ERR_WORKSPACE;
-  const int p = resolve_path(path, dtype, T);
+  const int p = resolve_path(path, dtype, T, H, I, E, k);
   if (p == MM_PATH_TENSOR && (dtype != kDtypeBF16 || !tensor_shape_ok(H, I)))
     return MM_ERR_UNSUPPORTED;
-  if (p == MM_PATH_STREAM && !stream_shape_ok(T, H, I, E, k, dtype)) return MM_ERR_UNSUPPORTED;
+  const size_t need = moe_path_bytes(T, H, I, E, k, dtype, p);
+  if (need == 0) return MM_ERR_UNSUPPORTED;
+  if (workspace_bytes < need) return MM_ERR_WORKSPACE;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
+  if (p == MM_PATH_STREAM || p == MM_PATH_STREAM_TC) {
+    // decode-sized: routing, experts and combine in one streaming kernel,
+    // with its scratch after the header
+    void* scratch = ws_at(workspace, sizeof(WsHeader));
+    cudaError_t e = counted_launch(MM_KERNEL_DECODE, st, [&] {
+      if (p == MM_PATH_STREAM)
+        return launch_decode_ffn(x, Wr, logit_bias, Wg, Wu, Wd, static_cast<int>(T), H, I, E, k,
+                                 coef, topk_idx, topk_w, aux_loss, scratch, y, hdr, st);
+      return launch_decode_tc(x, Wr, logit_bias, Wg, Wu, Wd, static_cast<int>(T), H, I, E, k,
+                              coef, topk_idx, topk_w, aux_loss, scratch, y, hdr, st);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "decode ffn");
+    return MM_OK;
+  }
+  const MoeLayout L = moe_layout(T, H, I, E, k, dtype);
   int32_t* offsets = reinterpret_cast<int32_t*>(ws_at(workspace, L.offsets));
   int32_t* counts = reinterpret_cast<int32_t*>(ws_at(workspace, L.counts));
   int32_t* blk_cnt = reinterpret_cast<int32_t*>(ws_at(workspace, L.blk_cnt));
@@ -310,17 +377,6 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
   float* acc32 = (dtype == kDtypeF32) ? static_cast<float*>(y)
                                       : reinterpret_cast<float*>(ws_at(workspace, L.acc32));
 
-  if (p == MM_PATH_STREAM) {
-    // decode-sized: the routing runs inside the streaming kernel; fp32
-    // h [T*k, I] lives in the fp16 Wd-copy area, which is sized for it
-    void* hdec = ws_at(workspace, L.wd16);
-    cudaError_t e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
-      return launch_decode_ffn(x, Wr, logit_bias, Wg, Wu, Wd, static_cast<int>(T), H, I, E, k,
-                               coef, topk_idx, topk_w, aux_loss, hdec, y, hdr, st);
-    });
-    if (e != cudaSuccess) return cuda_fail(e, "decode ffn");
-    return MM_OK;
-  }
   cudaError_t e = counted_launch(MM_KERNEL_ROUTER, st, [&] {
     return launch_router(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w, blk_cnt,
                          blk_prob, st);
@@ -419,7 +475,7 @@ int mm_moe_route(const void* x, const void* Wr, int64_t T, int H, int E, int k, 
 uint64_t mm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int mm_profile_start(int kernel_id, int max_launches) {
-  if (kernel_id < MM_KERNEL_ROUTER || kernel_id > MM_KERNEL_WCONVERT) return MM_ERR_INVALID_ARG;
+  if (kernel_id < MM_KERNEL_ROUTER || kernel_id > MM_KERNEL_DECODE) return MM_ERR_INVALID_ARG;
   if (max_launches < 1 || max_launches > 100000) return MM_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_prof.mu);
   g_prof.kernel = kernel_id;

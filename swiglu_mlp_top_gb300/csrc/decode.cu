@@ -18,7 +18,7 @@
 // the down weights are in shared memory by the time the barrier opens.  The
 // products use packed fp32 FMA (two lanes of fp32 per instruction) on
 // operands widened from bf16; every dot product accumulates in fp32.
-#include "mm_kernels.cuh"
+#include "route_small.cuh"
 
 namespace mm {
 
@@ -57,19 +57,6 @@ struct DecodeArgs {
   DecPlan plan;
 };
 
-// Routing tables shared by the CTA.
-struct DecRoute {
-  int nA;                                   // assignments (MoE: T*k, dense: T)
-  int n_touched;
-  int touched[MM_MAX_EXPERTS];              // ascending expert ids
-  int cnt[MM_MAX_EXPERTS];                  // assignments per expert
-  int e_start[MM_MAX_EXPERTS + 1];          // expert e's assignments: by_e[e_start[e] ..]
-  int sel_e[kDecodeMaxT * MM_MAX_TOPK];     // expert of assignment a = t*k + s
-  float sel_a[kDecodeMaxT * MM_MAX_TOPK];   // its alpha
-  int rank[kDecodeMaxT * MM_MAX_TOPK];      // its place among its expert's assignments
-  int by_e[kDecodeMaxT * MM_MAX_TOPK];      // assignments grouped by expert, in order
-  float prob[kDecodeMaxT][MM_MAX_EXPERTS];  // logits, then probabilities
-};
 
 typedef unsigned long long u64;
 
@@ -85,11 +72,6 @@ __device__ __forceinline__ u64 bf2(uint32_t w) {
 }
 __device__ __forceinline__ float hsum2(u64 v) {
   return __uint_as_float(static_cast<uint32_t>(v)) + __uint_as_float(static_cast<uint32_t>(v >> 32));
-}
-__device__ __forceinline__ float warp_allsum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
 }
 
 // Sum of NV per-lane values over the warp, scattered: lane L ends with the
@@ -213,12 +195,10 @@ __device__ __forceinline__ void down_row(const __nv_bfloat16* wrow, const float*
 }
 
 // MoE routing of all T tokens.  Logits: (token, expert) pairs, four per warp
-// at a time, lanes split H, fp32.  Then warp t, lane e: softmax with the
-// maximum subtracted and k arg-max rounds over (p desc, index asc) — equal
-// probabilities go to the lower index; alpha = p / (sum_S p + 1e-20).  Then
-// warp 0 groups the assignments by expert, keeping token order within each.
+// at a time, lanes split H, fp32; then softmax / top-k per token and the
+// grouping by expert (route_small.cuh).
 __device__ void decode_route(const DecodeArgs& A, const float* xs, const __nv_bfloat16* Wr,
-                             const float* bias, DecRoute& R) {
+                             const float* bias, SmallRoute<kDecodeMaxT>& R) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int E = A.E, k = A.k, H = A.H;
   const int pairs = A.T * E;
@@ -255,96 +235,16 @@ __device__ void decode_route(const DecodeArgs& A, const float* xs, const __nv_bf
     }
   }
   __syncthreads();
-  for (int t = warp; t < A.T; t += kDecWarps) {
-    // lane holds experts lane and lane + 32
-    float r0 = -INFINITY, r1 = -INFINITY;
-    if (lane < E) r0 = R.prob[t][lane] + bias[lane];
-    if (lane + 32 < E) r1 = R.prob[t][lane + 32] + bias[lane + 32];
-    float m = fmaxf(r0, r1);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float x0 = (lane < E) ? expf(r0 - m) : 0.f;
-    const float x1 = (lane + 32 < E) ? expf(r1 - m) : 0.f;
-    const float z = warp_allsum(x0 + x1);
-    const float p0 = x0 / z, p1 = x1 / z;
-    if (lane < E) R.prob[t][lane] = p0;
-    if (lane + 32 < E) R.prob[t][lane + 32] = p1;
-    bool taken0 = lane >= E, taken1 = lane + 32 >= E;
-    float sel_sum = 0.f;
-    float my_p = 0.f;
-    int my_e = 0;
-    for (int s = 0; s < k; ++s) {
-      float bp = -1.f;
-      int be = 0x7fffffff;
-      if (!taken0) { bp = p0; be = lane; }
-      if (!taken1 && (p1 > bp)) { bp = p1; be = lane + 32; }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float op = __shfl_xor_sync(0xffffffffu, bp, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (op > bp || (op == bp && oe < be)) { bp = op; be = oe; }
-      }
-      if (be == lane) taken0 = true;
-      if (be == lane + 32) taken1 = true;
-      sel_sum += bp;
-      if (lane == s) { my_p = bp; my_e = be; }
-    }
-    if (lane < k) {
-      R.sel_e[t * k + lane] = my_e;
-      R.sel_a[t * k + lane] = my_p / (sel_sum + 1e-20f);
-    }
-  }
+  route_softmax_topk(R, A.T, E, k, bias, warp, kDecWarps, lane);
   __syncthreads();
-  if (warp == 0) {
-    const int nA = A.T * k;
-    for (int e = lane; e < E; e += 32) R.cnt[e] = 0;
-    __syncwarp();
-    for (int base = 0; base < nA; base += 32) {
-      const int a = base + lane;
-      const bool valid = a < nA;
-      const int e = valid ? R.sel_e[a] : MM_MAX_EXPERTS + lane;   // idle lanes match no one
-      const unsigned mask = __match_any_sync(0xffffffffu, e);
-      const unsigned below = mask & ((1u << lane) - 1u);
-      const int prior = valid ? R.cnt[e] : 0;
-      __syncwarp();
-      if (valid) {
-        R.rank[a] = prior + __popc(below);
-        if (below == 0u) R.cnt[e] = prior + __popc(mask);
-      }
-      __syncwarp();
-    }
-    const unsigned lt = (1u << lane) - 1u;
-    const int c0 = lane < E ? R.cnt[lane] : 0;
-    const int c1 = lane + 32 < E ? R.cnt[lane + 32] : 0;
-    int s0 = c0, s1 = c1;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n0 = __shfl_up_sync(0xffffffffu, s0, o);
-      const int n1 = __shfl_up_sync(0xffffffffu, s1, o);
-      if (lane >= o) { s0 += n0; s1 += n1; }
-    }
-    const int tot0 = __shfl_sync(0xffffffffu, s0, 31);
-    if (lane < E) R.e_start[lane] = s0 - c0;
-    if (lane + 32 < E) R.e_start[lane + 32] = tot0 + s1 - c1;
-    const unsigned b0 = __ballot_sync(0xffffffffu, c0 > 0);
-    const unsigned b1 = __ballot_sync(0xffffffffu, c1 > 0);
-    if (c0 > 0) R.touched[__popc(b0 & lt)] = lane;
-    if (c1 > 0) R.touched[__popc(b0) + __popc(b1 & lt)] = lane + 32;
-    if (lane == 0) {
-      R.n_touched = __popc(b0) + __popc(b1);
-      R.nA = nA;
-      R.e_start[E] = nA;
-    }
-    __syncwarp();
-    for (int a = lane; a < nA; a += 32) R.by_e[R.e_start[R.sel_e[a]] + R.rank[a]] = a;
-  }
+  if (warp == 0) route_group(R, A.T * k, E, lane);
   __syncthreads();
 }
 
 __global__ void __launch_bounds__(kDecThreads)
 decode_ffn_kernel(const DecodeArgs A) {
   extern __shared__ __align__(128) unsigned char dsm[];
-  __shared__ DecRoute R;
+  __shared__ SmallRoute<kDecodeMaxT> R;
   __shared__ __align__(8) uint64_t bar[kMaxRing + kMaxWdSlots + 1];
   __shared__ float part[kDecodeMaxT * MM_MAX_TOPK][kDnRows];
   __shared__ float s_bias[MM_MAX_EXPERTS];
@@ -434,17 +334,7 @@ decode_ffn_kernel(const DecodeArgs A) {
       decode_route(A, xs, wr_smem ? reinterpret_cast<const __nv_bfloat16*>(ring)
                                   : static_cast<const __nv_bfloat16*>(A.Wr), s_bias, R);
     } else {
-      if (tid < A.T) {
-        R.sel_a[tid] = 1.0f;
-        R.by_e[tid] = tid;
-      }
-      if (tid == 0) {
-        R.nA = A.T;
-        R.n_touched = 1;
-        R.touched[0] = 0;
-        R.e_start[0] = 0;
-        R.e_start[1] = A.T;
-      }
+      route_dense(R, A.T, tid);
       __syncthreads();
     }
   }
@@ -453,24 +343,8 @@ decode_ffn_kernel(const DecodeArgs A) {
     const int up_units = n_touched * slices;
     my_up = blockIdx.x < up_units ? (up_units - blockIdx.x + G - 1) / G : 0;
     my_wd = my_dn * n_touched;
-    if (blockIdx.x == 0) {
-      for (int a = tid; a < R.nA; a += kDecThreads) {
-        A.topk_idx[a] = R.sel_e[a];
-        A.topk_w[a] = R.sel_a[a];
-      }
-      if (warp == 1) {
-        // aux = E*coef*sum_e (count_e/T)(P_e/T): lane e sums its expert
-        float acc = 0.f;
-        for (int e = lane; e < A.E; e += 32) {
-          float Pe = 0.f;
-          for (int t = 0; t < A.T; ++t) Pe += R.prob[t][e];
-          acc = fmaf(static_cast<float>(R.cnt[e]), Pe, acc);
-        }
-        acc = warp_allsum(acc);
-        const float invT = 1.0f / static_cast<float>(A.T);
-        if (lane == 0) *A.aux_loss = static_cast<float>(A.E) * A.coef * acc * invT * invT;
-      }
-    }
+    if (blockIdx.x == 0)
+      route_outputs(R, A.T, A.E, A.coef, A.topk_idx, A.topk_w, A.aux_loss, tid, kDecThreads, 1);
     __syncthreads();                          // Wr in the ring is no longer read
     if (tid == 0) {
       fence_proxy_async_smem();
@@ -514,7 +388,7 @@ decode_ffn_kernel(const DecodeArgs A) {
   unsigned ticket = 0xffffffffu;
   if (ok) {
     asm volatile("fence.proxy.async.global;" ::: "memory");
-    ok = grid_barrier(A.hdr, 24, &ticket);
+    ok = grid_barrier(A.hdr, 24, 1, &ticket);
   }
 
   // ---- down: unit = kDnRows output columns, every touched expert

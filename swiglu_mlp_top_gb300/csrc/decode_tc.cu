@@ -1,0 +1,618 @@
+// Decode-sized forward on the 5th-generation tensor cores (T <= 64 tokens,
+// bf16): one cooperative kernel that streams every needed weight row once.
+// The weights are the UMMA M operand (tiles of 128 rows x 64 k, TMA-fed,
+// 128-byte swizzle); the T tokens, padded to Np = 16·ceil(T/16) with zero
+// rows, are the N operand; fp32 accumulators live in TMEM.
+//
+//   1  x (all Np rows) -> shared memory once.  MoE: router logits
+//      L = Wr x^T (M = experts, zero-padded to 128) on the tensor core; then
+//      softmax / top-k / alpha per token and the grouping by expert
+//      (route_small.cuh; lesson 13 §1.5, chapter 4 §4.3).  Block 0 writes
+//      topk_idx, topk_w and the aux loss (lesson 13 §1.6).
+//   2  gate/up units (touched expert e, 128 rows of I, k-range):
+//      G = Wg_e x^T, U = Wu_e x^T.  With one k-range per unit the epilogue
+//      forms h = SiLU(G) ⊙ U (lesson 13 §0/§1.2) directly; otherwise it
+//      writes fp32 partial G, U and, after a grid barrier, every CTA reduces
+//      a share of them in k-range order.  Either way the result is stored as
+//      Hp_e[t, i] = alpha_{t,e} h_{t,e}[i] (0 for tokens not routed to e), split
+//      into a bf16 high part and a bf16 remainder: the down product then runs
+//      on bf16 operands with ~16 significant bits of h.
+//   3  grid barrier; down: y^T = sum_e Wd_e Hp_e^T.  The (output m-block,
+//      expert, k-block) tiles are cut into one contiguous range per CTA; each
+//      CTA accumulates its range in TMEM and writes one fp32 partial per
+//      output m-block it touches.  The Wd tiles of a CTA's first tiles are
+//      requested before the barrier, since they do not depend on h.
+//   4  grid barrier; every CTA adds a share of the partials in CTA order and
+//      rounds y to bf16 once (deterministic; the weighted sum over the
+//      selected experts is part of the fp32 accumulation).
+//
+// Warp roles (192 threads): warp 0 lane 0 issues TMA, warp 1 lane 0 issues
+// UMMA and owns TMEM, warps 2-5 are the epilogue (TMEM lane quadrant
+// warp % 4).  All waits are bounded.
+#include <mutex>
+
+#include "route_small.cuh"
+
+namespace mm {
+
+constexpr int kDtThreads = 192;
+constexpr int kDtWarps = kDtThreads / 32;
+constexpr int kDtMaxStages = 6;
+constexpr int kDtTileA = 128 * 64 * 2;          // 16 KiB: 128 weight rows x 64 k
+constexpr int kDtStage = 2 * kDtTileA;          // 32 KiB
+constexpr uint32_t kDtTmemCols = 512;
+constexpr uint32_t kDtColGU = 0;                // two (G, U) buffers, 2 * Np columns each
+constexpr uint32_t kDtColD = 256;               // down accumulator
+constexpr uint32_t kDtColL = 384;               // router logits
+constexpr int kDtMaxSeg = 2;                    // output m-blocks per CTA range
+constexpr int kDtMaxCtas = 160;                 // grid cap (152 SMs on GB300)
+constexpr size_t kDtSmemBudget = 200 * 1024;
+
+template <int MAXW>
+struct DtMaps {
+  CUtensorMap x;                  // x [T, H], box 64 x Np
+  CUtensorMap wr;                 // Wr [E, H], box 64 x 128
+  CUtensorMap hp;                 // Hp [nt_max * 2 * Np, I], box 64 x Np
+  CUtensorMap wg[MAXW], wu[MAXW]; // [I, H], box 64 x 128
+  CUtensorMap wd[MAXW];           // [H, I], box 64 x 128
+};
+
+struct DtArgs {
+  int T, Np, H, I, E, k;          // E = k = 1 for the dense FFN
+  int moe;
+  float coef;
+  const float* bias;
+  int32_t* topk_idx;
+  float* topk_w;
+  float* aux_loss;
+  __nv_bfloat16* hp;              // [nt_max][2][Np][I]
+  float* pgu;                     // [units][2][Np][128]   (split gate/up only)
+  float* pd;                      // [grid][kDtMaxSeg][Np][128]
+  void* y;                        // [T, H] bf16
+  WsHeader* hdr;
+  int stages;
+  uint32_t xs_bytes;              // x operand bytes = ring offset
+  uint32_t alpha_off;             // alpha table [nt_max][Np] fp32
+};
+
+// Work plan derived from the routing; identical in every thread of the grid.
+struct DtPlan {
+  int nt, MB_I, MB_H, KB_H, KB_I;
+  int s_up, n_units;              // gate/up: blocks * k-ranges
+  long long F;                    // down tiles: MB_H * nt * KB_I
+  int per_mb;                     // down tiles per output m-block
+};
+
+__device__ __forceinline__ long long dt_range_start(int c, long long F, int G) {
+  return static_cast<long long>(c) * F / G;
+}
+// CTA whose down range holds tile f (the largest c with start(c) <= f).
+__device__ __forceinline__ int dt_cta_of(long long f, long long F, int G) {
+  return static_cast<int>(((f + 1) * G - 1) / F);
+}
+
+template <int MAXW>
+__global__ void __launch_bounds__(kDtThreads, 1)
+decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
+  extern __shared__ unsigned char smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* xs = smem;                                       // [KB_H][Np rows x 128 B]
+  uint8_t* ring = smem + A.xs_bytes;                        // [stages][32 KiB]
+  float* alpha = reinterpret_cast<float*>(smem + A.alpha_off);
+  __shared__ SmallRoute<kDecodeTcMaxT> R;
+  __shared__ __align__(8) uint64_t full[kDtMaxStages], empty[kDtMaxStages];
+  __shared__ __align__(8) uint64_t xbar, lbar, tfull[2], tempty[2], dfull, dempty, drained;
+  __shared__ uint32_t s_tmem;
+  __shared__ float s_bias[MM_MAX_EXPERTS];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int T = A.T, Np = A.Np, H = A.H, I = A.I, S = A.stages;
+  const uint32_t xtile = static_cast<uint32_t>(Np) * 128;  // bytes of one x / Hp tile
+  const uint32_t idesc = idesc_bf16_f32(128, Np);
+  const bool moe = A.moe != 0;
+  WsHeader* hdr = A.hdr;
+
+  if (tid == 0) {
+    for (int s = 0; s < kDtMaxStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&xbar, 1);
+    mbar_init(&lbar, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(&dfull, 1);
+    mbar_init(&dempty, 4);
+    mbar_init(&drained, 1);
+    fence_mbar_init();
+  }
+  if (tid < MM_MAX_EXPERTS) s_bias[tid] = (moe && A.bias != nullptr && tid < A.E) ? A.bias[tid] : 0.f;
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, kDtTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  // role state: stage uses issued (producer) / consumed (MMA)
+  int p_it = 0, m_it = 0;
+  bool ok = true;
+  auto acquire = [&](int& s) -> bool {      // producer: next ring stage, once it is empty
+    s = p_it % S;
+    return mbar_wait(&empty[s], ((p_it / S) & 1) ^ 1, nullptr, hdr, 40);
+  };
+  auto consume = [&](int& s) -> bool {      // MMA: next ring stage, once it is full
+    s = m_it % S;
+    const bool r = mbar_wait(&full[s], (m_it / S) & 1, nullptr, hdr, 41);
+    tc_fence_after();
+    return r;
+  };
+  auto sdesc = [&](const uint8_t* p) { return smem_desc_sw128(smem_u32(p)); };
+
+  // ------------------------------------------------------------ 1: x, router
+  const int KB_H = H / 64;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&xbar, KB_H * xtile);
+    for (int kb = 0; kb < KB_H; ++kb) tma_load_2d(xs + kb * xtile, &M.x, &xbar, kb * 64, 0);
+    if (moe) {
+      for (int kb = 0; ok && kb < KB_H; ++kb) {
+        int s;
+        if (!acquire(s)) { ok = false; break; }
+        mbar_arrive_expect_tx(&full[s], kDtTileA);
+        tma_load_2d(ring + s * kDtStage, &M.wr, &full[s], kb * 64, 0);
+        ++p_it;
+      }
+    }
+  }
+  if (tid == 32) {
+    ok = mbar_wait(&xbar, 0, nullptr, hdr, 42);
+    tc_fence_after();
+    if (moe && ok) {
+      for (int kb = 0; kb < KB_H; ++kb) {
+        int s;
+        if (!consume(s)) { ok = false; break; }
+        const uint8_t* a = ring + s * kDtStage;
+        const uint8_t* b = xs + kb * xtile;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(tmem + kDtColL, sdesc(a + kk * 32), sdesc(b + kk * 32), idesc, (kb | kk) ? 1u : 0u);
+        umma_commit(&empty[s]);
+        ++m_it;
+      }
+      umma_commit(&lbar);
+    }
+  }
+  if (moe && warp >= 2) {
+    ok = warp_wait(&lbar, 0, nullptr, hdr, 43);
+    tc_fence_after();
+    const int quad = warp & 3, e = quad * 32 + lane;
+    for (int c0 = 0; ok && c0 < Np; c0 += 16) {
+      uint32_t r[16];
+      tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(quad * 32) << 16) + kDtColL + c0, r);
+      tmem_ld_wait();
+      if (e < A.E) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (c0 + j < T) R.prob[c0 + j][e] = __uint_as_float(r[j]);
+      }
+    }
+  }
+  ok = __syncthreads_and(ok);
+
+  // ------------------------------------------------------------ routing
+  if (ok) {
+    if (moe) {
+      route_softmax_topk(R, T, A.E, A.k, s_bias, warp, kDtWarps, lane);
+      __syncthreads();
+      if (warp == 0) route_group(R, T * A.k, A.E, lane);
+    } else {
+      route_dense(R, T, tid);
+    }
+    __syncthreads();
+    for (int q = tid; q < R.n_touched * Np; q += kDtThreads) alpha[q] = 0.f;
+    __syncthreads();
+    for (int a = tid; a < R.nA; a += kDtThreads) {
+      const int t = moe ? a / A.k : a;
+      alpha[R.slot_of[R.sel_e[a]] * Np + t] = R.sel_a[a];
+    }
+    if (moe && cta == 0)
+      route_outputs(R, T, A.E, A.coef, A.topk_idx, A.topk_w, A.aux_loss, tid, kDtThreads, 2);
+    __syncthreads();
+  }
+
+  DtPlan P;
+  P.nt = (ok && R.n_touched > 0) ? R.n_touched : 1;
+  P.MB_I = (I + 127) / 128;
+  P.MB_H = H / 128;
+  P.KB_H = KB_H;
+  P.KB_I = I / 64;
+  {
+    const int blocks = P.nt * P.MB_I;
+    int s_up = (G + blocks - 1) / blocks;
+    s_up = s_up < 1 ? 1 : (s_up > P.KB_H ? P.KB_H : s_up);
+    P.s_up = s_up;
+    P.n_units = blocks * s_up;
+  }
+  P.per_mb = P.nt * P.KB_I;
+  P.F = static_cast<long long>(P.MB_H) * P.per_mb;
+  const long long r0 = dt_range_start(cta, P.F, G), r1 = dt_range_start(cta + 1, P.F, G);
+  const int my_down = static_cast<int>(r1 - r0);
+  const int n_pre = my_down < S ? my_down : S;     // Wd tiles requested before the barrier
+  int pre_it0 = 0;                                 // producer: stage use of the first of them
+
+  // unit u -> (touched index, m-block, k-block range)
+  auto unit_of = [&](int u, int& ti, int& mb, int& kb0, int& kb1) {
+    const int blk = u / P.s_up, kr = u - blk * P.s_up;
+    ti = blk / P.MB_I;
+    mb = blk - ti * P.MB_I;
+    kb0 = kr * P.KB_H / P.s_up;
+    kb1 = (kr + 1) * P.KB_H / P.s_up;
+  };
+  auto tile_of = [&](long long f, int& mbd, int& ti, int& kb) {
+    mbd = static_cast<int>(f / P.per_mb);
+    const int rem = static_cast<int>(f - static_cast<long long>(mbd) * P.per_mb);
+    ti = rem / P.KB_I;
+    kb = rem - ti * P.KB_I;
+  };
+
+  // ------------------------------------------------------------ 2: gate/up
+  if (ok) {
+    if (tid == 0) {
+      for (int u = cta; ok && u < P.n_units; u += G) {
+        int ti, mb, kb0, kb1;
+        unit_of(u, ti, mb, kb0, kb1);
+        const int e = R.touched[ti];
+        for (int kb = kb0; kb < kb1; ++kb) {
+          int s;
+          if (!acquire(s)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[s], 2 * kDtTileA);
+          tma_load_2d(ring + s * kDtStage, &M.wg[e], &full[s], kb * 64, mb * 128);
+          tma_load_2d(ring + s * kDtStage + kDtTileA, &M.wu[e], &full[s], kb * 64, mb * 128);
+          ++p_it;
+        }
+      }
+      pre_it0 = p_it;
+      for (int j = 0; ok && j < n_pre; ++j) {
+        int mbd, ti, kb, s;
+        tile_of(r0 + j, mbd, ti, kb);
+        if (!acquire(s)) { ok = false; break; }
+        mbar_arrive_expect_tx(&full[s], kDtTileA + 2 * xtile);   // the Hp tiles follow later
+        tma_load_2d(ring + s * kDtStage, &M.wd[R.touched[ti]], &full[s], kb * 64, mbd * 128);
+        ++p_it;
+      }
+    }
+    if (tid == 32) {
+      int local = 0;
+      for (int u = cta; ok && u < P.n_units; u += G, ++local) {
+        int ti, mb, kb0, kb1;
+        unit_of(u, ti, mb, kb0, kb1);
+        const int acc = local & 1;
+        if (!mbar_wait(&tempty[acc], ((local >> 1) & 1) ^ 1, nullptr, hdr, 44)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t dg = tmem + kDtColGU + acc * 2 * Np, du = dg + Np;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          int s;
+          if (!consume(s)) { ok = false; break; }
+          const uint8_t* a = ring + s * kDtStage;
+          const uint8_t* b = xs + kb * xtile;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(dg, sdesc(a + kk * 32), sdesc(b + kk * 32), idesc, (kb > kb0 || kk) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(du, sdesc(a + kDtTileA + kk * 32), sdesc(b + kk * 32), idesc,
+                      (kb > kb0 || kk) ? 1u : 0u);
+          umma_commit(&empty[s]);
+          ++m_it;
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+      }
+    }
+    if (warp >= 2) {
+      const int quad = warp & 3, rl = quad * 32 + lane;
+      int local = 0;
+      for (int u = cta; ok && u < P.n_units; u += G, ++local) {
+        int ti, mb, kb0, kb1;
+        unit_of(u, ti, mb, kb0, kb1);
+        const int acc = local & 1;
+        if (!warp_wait(&tfull[acc], (local >> 1) & 1, nullptr, hdr, 45)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tg = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kDtColGU + acc * 2 * Np;
+        const int i = mb * 128 + rl;
+        for (int c0 = 0; c0 < Np; c0 += 16) {
+          uint32_t gr[16], ur[16];
+          tmem_ld_32x32b_x16(tg + c0, gr);
+          tmem_ld_32x32b_x16(tg + Np + c0, ur);
+          tmem_ld_wait();
+          if (P.s_up == 1) {
+            if (i < I) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int t = c0 + j;
+                const float g = __uint_as_float(gr[j]), uu = __uint_as_float(ur[j]);
+                const float v = silu_f32(g) * uu * alpha[ti * Np + t];
+                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+                A.hp[(static_cast<size_t>(ti * 2) * Np + t) * I + i] = hi;
+                A.hp[(static_cast<size_t>(ti * 2 + 1) * Np + t) * I + i] = lo;
+              }
+            }
+          } else {
+            float* pg = A.pgu + static_cast<size_t>(u) * 2 * Np * 128;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              pg[static_cast<size_t>(c0 + j) * 128 + rl] = __uint_as_float(gr[j]);
+              pg[static_cast<size_t>(Np + c0 + j) * 128 + rl] = __uint_as_float(ur[j]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+      }
+    }
+    ok = __syncthreads_and(ok);
+  }
+
+  // ------------------------------------------------------------ h complete
+  unsigned round = 1;
+  if (ok) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    ok = grid_barrier(hdr, 46, round++, nullptr);
+  }
+  if (ok && P.s_up > 1) {
+    // add the k-range partials of G and U in order, then as the direct path
+    const int blocks = P.nt * P.MB_I;
+    const long long total = static_cast<long long>(blocks) * Np * 128;
+    for (long long q = static_cast<long long>(cta) * kDtThreads + tid; q < total;
+         q += static_cast<long long>(G) * kDtThreads) {
+      const int blk = static_cast<int>(q / (Np * 128));
+      const int rem = static_cast<int>(q - static_cast<long long>(blk) * Np * 128);
+      const int t = rem >> 7, rl = rem & 127;
+      const int ti = blk / P.MB_I, mb = blk - ti * P.MB_I;
+      const int i = mb * 128 + rl;
+      if (i >= I) continue;
+      float g = 0.f, uu = 0.f;
+      for (int kr = 0; kr < P.s_up; ++kr) {
+        const float* pg = A.pgu + static_cast<size_t>(blk * P.s_up + kr) * 2 * Np * 128;
+        g += pg[static_cast<size_t>(t) * 128 + rl];
+        uu += pg[static_cast<size_t>(Np + t) * 128 + rl];
+      }
+      const float v = silu_f32(g) * uu * alpha[ti * Np + t];
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+      A.hp[(static_cast<size_t>(ti * 2) * Np + t) * I + i] = hi;
+      A.hp[(static_cast<size_t>(ti * 2 + 1) * Np + t) * I + i] = lo;
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    ok = grid_barrier(hdr, 47, round++, nullptr);
+  }
+
+  // ------------------------------------------------------------ 3: down
+  if (ok) {
+    if (tid == 0) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      for (int j = 0; ok && j < my_down; ++j) {
+        int mbd, ti, kb, s;
+        tile_of(r0 + j, mbd, ti, kb);
+        if (j < n_pre) {
+          s = (pre_it0 + j) % S;                  // Wd already requested, bytes armed
+        } else {
+          if (!acquire(s)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[s], kDtTileA + 2 * xtile);
+          tma_load_2d(ring + s * kDtStage, &M.wd[R.touched[ti]], &full[s], kb * 64, mbd * 128);
+          ++p_it;
+        }
+        uint8_t* b = ring + s * kDtStage + kDtTileA;
+        tma_load_2d(b, &M.hp, &full[s], kb * 64, (ti * 2) * Np);
+        tma_load_2d(b + xtile, &M.hp, &full[s], kb * 64, (ti * 2 + 1) * Np);
+      }
+    }
+    if (tid == 32) {
+      int seg = -1, prev = -1;
+      bool first = true;
+      for (int j = 0; ok && j < my_down; ++j) {
+        int mbd, ti, kb, s;
+        tile_of(r0 + j, mbd, ti, kb);
+        if (mbd != prev) {
+          if (seg >= 0) umma_commit(&dfull);
+          ++seg;
+          prev = mbd;
+          if (!mbar_wait(&dempty, (seg & 1) ^ 1, nullptr, hdr, 48)) { ok = false; break; }
+          tc_fence_after();
+          first = true;
+        }
+        if (!consume(s)) { ok = false; break; }
+        const uint8_t* a = ring + s * kDtStage;
+        const uint8_t* b = a + kDtTileA;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(tmem + kDtColD, sdesc(a + kk * 32), sdesc(b + kk * 32), idesc,
+                    (!first || kk) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(tmem + kDtColD, sdesc(a + kk * 32), sdesc(b + xtile + kk * 32), idesc, 1u);
+        first = false;
+        umma_commit(&empty[s]);
+        ++m_it;
+      }
+      if (ok && seg >= 0) umma_commit(&dfull);
+    }
+    if (warp >= 2) {
+      const int quad = warp & 3, rl = quad * 32 + lane;
+      const int n_seg = my_down > 0 ? static_cast<int>((r1 - 1) / P.per_mb - r0 / P.per_mb) + 1 : 0;
+      for (int seg = 0; ok && seg < n_seg; ++seg) {
+        if (!warp_wait(&dfull, seg & 1, nullptr, hdr, 49)) { ok = false; break; }
+        tc_fence_after();
+        float* pdst = A.pd + (static_cast<size_t>(cta) * kDtMaxSeg + seg) * Np * 128;
+        for (int c0 = 0; c0 < Np; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(quad * 32) << 16) + kDtColD + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pdst[static_cast<size_t>(c0 + j) * 128 + rl] = __uint_as_float(r[j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&dempty);
+      }
+    }
+    ok = __syncthreads_and(ok);
+  }
+
+  // ------------------------------------------------------------ 4: y
+  unsigned ticket = 0xffffffffu;
+  if (ok) ok = grid_barrier(hdr, 50, round, &ticket);
+  if (ok) {
+    const long long total = static_cast<long long>(T) * H;
+    for (long long q = static_cast<long long>(cta) * kDtThreads + tid; q < total;
+         q += static_cast<long long>(G) * kDtThreads) {
+      const int t = static_cast<int>(q / H), j = static_cast<int>(q - static_cast<long long>(t) * H);
+      const int mbd = j >> 7, rl = j & 127;
+      const long long f0 = static_cast<long long>(mbd) * P.per_mb;
+      const int c0 = dt_cta_of(f0, P.F, G), c1 = dt_cta_of(f0 + P.per_mb - 1, P.F, G);
+      float v = 0.f;
+      for (int c = c0; c <= c1; ++c) {
+        const long long s0 = dt_range_start(c, P.F, G);
+        if (dt_range_start(c + 1, P.F, G) == s0) continue;     // empty range
+        const int seg = mbd - static_cast<int>(s0 / P.per_mb);
+        v += A.pd[((static_cast<size_t>(c) * kDtMaxSeg + seg) * Np + t) * 128 + rl];
+      }
+      static_cast<__nv_bfloat16*>(A.y)[q] = __float2bfloat16_rn(v);
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  if (tid == 32) {
+    // every issued UMMA has finished before TMEM is released
+    umma_commit(&drained);
+    mbar_wait(&drained, 0, nullptr, hdr, 51);
+  }
+  if (tid == 0 && !ok) {
+    // copies still in flight land before the CTA exits (bounded)
+    for (int j = 0; j < S && j < p_it; ++j) {
+      const int q = p_it - 1 - j;
+      mbar_wait(&full[q % S], (q / S) & 1, nullptr, nullptr, 52);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kDtTmemCols);
+  if (tid == 0) grid_barrier_reset(hdr, ticket);
+}
+
+// =============================================================== host side
+namespace {
+
+struct DtLayout {
+  int Np, nt_max, stages;
+  size_t xs, alpha_off, smem;           // shared memory
+  size_t hp, pgu, pd, total;            // workspace (after the header)
+};
+
+inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool dt_layout(int T, int H, int I, int E, int k, DtLayout& L) {
+  if (T < 1 || T > kDecodeTcMaxT || H % 128 != 0 || I % 64 != 0) return false;
+  if (E > 1 && (E > MM_MAX_EXPERTS || k < 1 || k > MM_MAX_TOPK || k > E)) return false;
+  L.Np = (T + 15) / 16 * 16;
+  L.nt_max = E > 1 ? (E < T * k ? E : T * k) : 1;
+  L.xs = static_cast<size_t>(L.Np) * 2 * H;
+  const size_t alpha = round_up(static_cast<size_t>(L.nt_max) * L.Np * 4, 1024);
+  const size_t avail = kDtSmemBudget - 1024 - L.xs - alpha;   // 1 KiB: alignment slack
+  if (L.xs + alpha + 2 * kDtStage + 1024 > kDtSmemBudget) return false;
+  L.stages = static_cast<int>(avail / kDtStage);
+  if (L.stages > kDtMaxStages) L.stages = kDtMaxStages;
+  L.alpha_off = L.xs + static_cast<size_t>(L.stages) * kDtStage;
+  L.smem = L.alpha_off + alpha + 1024;
+  const int G = kDtMaxCtas;
+  const int blocks = L.nt_max * ((I + 127) / 128);
+  const int units = blocks + G;                    // blocks * ceil(G / blocks) < blocks + G
+  if (H / 128 > G) return false;
+  L.hp = round_up(static_cast<size_t>(L.nt_max) * 2 * L.Np * I * 2, 256);
+  L.pgu = round_up(static_cast<size_t>(units) * 2 * L.Np * 128 * 4, 256);
+  L.pd = round_up(static_cast<size_t>(G) * kDtMaxSeg * L.Np * 128 * 4, 256);
+  L.total = L.hp + L.pgu + L.pd;
+  return true;
+}
+
+template <int MAXW>
+cudaError_t decode_tc_impl(const DtLayout& L, const void* x, const void* Wr,
+                           const void* const* Wg, const void* const* Wu, const void* const* Wd,
+                           DtArgs& A, cudaStream_t st) {
+  static DtMaps<MAXW> m;                 // host staging, copied into the launch
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  const int T = A.T, H = A.H, I = A.I, nw = A.moe ? A.E : 1;
+  if (!make_map_16(&m.x, x, H, T, L.Np, false)) return cudaErrorInvalidValue;
+  if (A.moe && !make_map_16(&m.wr, Wr, H, A.E, 128, false)) return cudaErrorInvalidValue;
+  if (!make_map_16(&m.hp, A.hp, I, static_cast<uint64_t>(L.nt_max) * 2 * L.Np, L.Np, false))
+    return cudaErrorInvalidValue;
+  for (int e = 0; e < nw; ++e) {
+    if (!make_map_16(&m.wg[e], Wg[e], H, I, 128, false)) return cudaErrorInvalidValue;
+    if (!make_map_16(&m.wu[e], Wu[e], H, I, 128, false)) return cudaErrorInvalidValue;
+    if (!make_map_16(&m.wd[e], Wd[e], I, H, 128, false)) return cudaErrorInvalidValue;
+  }
+  auto fn = decode_tc_kernel<MAXW>;
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), L.smem);
+  if (e != cudaSuccess) return e;
+  int fit = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, fn, kDtThreads, L.smem);
+  if (e != cudaSuccess) return e;
+  if (fit < 1) return cudaErrorInvalidConfiguration;
+  int grid = num_sms();
+  if (grid > kDtMaxCtas) grid = kDtMaxCtas;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kDtThreads);
+  cfg.dynamicSmemBytes = L.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, m, A);
+}
+
+}  // namespace
+
+size_t decode_tc_bytes(int T, int H, int I, int E, int k) {
+  DtLayout L;
+  return dt_layout(T, H, I, E, k, L) ? L.total : 0;
+}
+
+cudaError_t launch_decode_tc(const void* x, const void* Wr, const float* bias,
+                             const void* const* Wg, const void* const* Wu, const void* const* Wd,
+                             int T, int H, int I, int E, int k, float coef, int32_t* topk_idx,
+                             float* topk_w, float* aux_loss, void* scratch, void* y,
+                             WsHeader* hdr, cudaStream_t st) {
+  const bool moe = Wr != nullptr;
+  DtLayout L;
+  if (!dt_layout(T, H, I, moe ? E : 1, moe ? k : 1, L)) return cudaErrorInvalidValue;
+  DtArgs A;
+  memset(&A, 0, sizeof(A));
+  A.T = T; A.Np = L.Np; A.H = H; A.I = I;
+  A.E = moe ? E : 1; A.k = moe ? k : 1; A.moe = moe ? 1 : 0; A.coef = coef; A.bias = bias;
+  A.topk_idx = topk_idx; A.topk_w = topk_w; A.aux_loss = aux_loss;
+  char* base = static_cast<char*>(scratch);
+  A.hp = reinterpret_cast<__nv_bfloat16*>(base);
+  A.pgu = reinterpret_cast<float*>(base + L.hp);
+  A.pd = reinterpret_cast<float*>(base + L.hp + L.pgu);
+  A.y = y; A.hdr = hdr;
+  A.stages = L.stages;
+  A.xs_bytes = static_cast<uint32_t>(L.xs);
+  A.alpha_off = static_cast<uint32_t>(L.alpha_off);
+  if (A.E <= 8) return decode_tc_impl<8>(L, x, Wr, Wg, Wu, Wd, A, st);
+  return decode_tc_impl<MM_MAX_EXPERTS>(L, x, Wr, Wg, Wu, Wd, A, st);
+}
+
+}  // namespace mm

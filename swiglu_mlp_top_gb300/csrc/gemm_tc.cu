@@ -102,17 +102,6 @@ __device__ __forceinline__ void build_schedule(const GroupRows& gr, int n_tiles,
   s_tstart[gr.G] = run;
 }
 
-__device__ __forceinline__ uint8_t* align1024(unsigned char* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
-// Warp-uniform bounded wait: every lane waits, then the warp agrees.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          WsHeader* hdr, unsigned where) {
-  const bool ok = mbar_wait(bar, parity, abort, hdr, where);
-  return __all_sync(0xffffffffu, ok);
-}
-
 // ---------------------------------------------------------------- epilogues
 // gate/up: 64 h columns (half `half` of the tile's 128) of one row:
 // h = SiLU(g) * u, fp16, as two 32-column pieces.  A warp whose 32 rows are
@@ -394,12 +383,11 @@ static EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 16-bit row-major [outer, inner] matrix (bf16 or fp16), box = 64 (inner) x
-// box_rows (outer), 128-byte swizzle, zero fill outside the matrix.  Cached by
-// (ptr, shape, box, type).
-static bool make_map_16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
-                        uint32_t box_rows, bool is_f16, uint32_t box_inner = kTcBK,
-                        CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+// 16-bit row-major [outer, inner] matrix (bf16 or fp16), box = box_inner
+// (inner) x box_rows (outer), zero fill outside the matrix.  Cached by
+// (ptr, shape, box, type, swizzle).
+bool make_map_16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
+                 uint32_t box_rows, bool is_f16, uint32_t box_inner, CUtensorMapSwizzle swz) {
   using Key = std::tuple<uintptr_t, uint64_t, uint64_t, uint32_t, bool, uint32_t, int>;
   static std::mutex mu;
   static std::map<Key, CUtensorMap> cache;

@@ -91,14 +91,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-// One grid-wide barrier per launch for a cooperative grid (every CTA
-// resident).  Arrival is a release add on bar_count; each CTA then polls
-// bar_count with acquire loads until all gridDim.x CTAs have arrived.  Once
-// through, each CTA takes a ticket on bar_leave; the CTA holding the last
-// ticket is the last one that could still read bar_count, and it returns both
-// words to 0 in grid_barrier_reset() at its end, ready for the next launch.
-// The poll gives up after kWaitLimitNs (reported, returns false).
-__device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned where, unsigned* ticket) {
+// Grid-wide barrier for a cooperative grid (every CTA resident), usable
+// several times per launch: round r (1, 2, ...) is a release add on
+// bar_count followed by acquire polls until bar_count reaches r * gridDim.x.
+// After its last round each CTA takes a ticket on bar_leave (pass `ticket`);
+// the CTA holding the last ticket is the last one that could still read
+// bar_count, and it returns both words to 0 in grid_barrier_reset() at its
+// end, ready for the next launch.  The poll gives up after kWaitLimitNs
+// (reported, returns false).
+__device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned where, unsigned round,
+                                             unsigned* ticket) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -111,14 +113,14 @@ __device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned where, unsi
     for (;;) {
       unsigned int v;
       asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
-      if (v >= G) break;
+      if (v >= round * G) break;
       if ((++n & 63u) == 0u && (globaltimer_ns() - t0 > kWaitLimitNs || n > (1u << 30))) {
         report_timeout(hdr, where);
         ok = 0;
         break;
       }
     }
-    *ticket = ok ? atomicAdd(&hdr->bar_leave, 1u) : 0xffffffffu;
+    if (ticket != nullptr) *ticket = ok ? atomicAdd(&hdr->bar_leave, 1u) : 0xffffffffu;
     s_ok = ok;
   }
   __syncthreads();
@@ -132,6 +134,17 @@ __device__ __forceinline__ void grid_barrier_reset(WsHeader* hdr, unsigned ticke
     hdr->bar_count = 0u;
     hdr->bar_leave = 0u;
   }
+}
+
+__device__ __forceinline__ uint8_t* align1024(unsigned char* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Warp-uniform bounded wait: every lane waits, then the warp agrees.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          WsHeader* hdr, unsigned where) {
+  const bool ok = mbar_wait(bar, parity, abort, hdr, where);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // ---------------------------------------------------------------- TMA
@@ -233,6 +246,16 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
         "=r"(r[31])
+      : "r"(taddr));
+}
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() {

@@ -15,8 +15,10 @@ constexpr int kRouteTokensPerBlock = 64;    // 8 tokens per warp
 constexpr int kScanThreads = 512;
 constexpr int kMaxGroups = MM_MAX_EXPERTS * MM_MAX_TOPK;     // (slot, expert) groups
 
-// Decode-sized calls (T <= kDecodeMaxT) stream each weight row once.
+// Decode-sized calls stream each weight row once: on the CUDA cores for
+// T <= kDecodeMaxT, on the tensor cores (decode_tc.cu) for T <= kDecodeTcMaxT.
 constexpr int kDecodeMaxT = 16;
+constexpr int kDecodeTcMaxT = 64;
 
 // Per-expert device pointers passed by value to a kernel.
 struct PtrArray {
@@ -103,7 +105,28 @@ cudaError_t launch_decode_ffn(const void* x, const void* Wr, const float* bias,
                               float* topk_w, float* aux_loss, void* hbuf, void* y, WsHeader* hdr,
                               cudaStream_t st);
 
+// Decode-sized forward on the tensor cores (T <= kDecodeTcMaxT, bf16): one
+// cooperative kernel; weights are the UMMA M operand (128 rows per tile), the
+// T tokens (padded to a multiple of 16) the N operand.  decode_tc_bytes is
+// its workspace after the 256-byte header (0: shape not supported).
+size_t decode_tc_bytes(int T, int H, int I, int E, int k);
+cudaError_t launch_decode_tc(const void* x, const void* Wr, const float* bias,
+                             const void* const* Wg, const void* const* Wu, const void* const* Wd,
+                             int T, int H, int I, int E, int k, float coef, int32_t* topk_idx,
+                             float* topk_w, float* aux_loss, void* scratch, void* y,
+                             WsHeader* hdr, cudaStream_t st);
+
 cudaError_t launch_watchdog_selftest(WsHeader* hdr, uint32_t limit_us, cudaStream_t st);
+
+// Workspace of the path that `path` (AUTO: the automatic choice) resolves to
+// for a dense call of this shape; 0 when that path does not take it.
+size_t dense_workspace_for_path(int64_t T, int H, int I, int dtype, int path);
+
+// TMA tensor map of a 16-bit row-major [outer, inner] matrix, box box_inner x
+// box_rows, zero fill outside; cached by (pointer, shape, box, type, swizzle).
+bool make_map_16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
+                 uint32_t box_rows, bool is_f16, uint32_t box_inner = kTcBK,
+                 CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B);
 
 int num_sms();   // of the current device, looked up once per device
 

@@ -39,12 +39,19 @@ int scratch_for_current_device(void** out) {
 
 extern "C" int mm_swiglu_ffn_noalloc(const void* x, const void* Wg, const void* Wu, const void* Wd,
                                      void* y, int64_t T, int H, int I, int dtype, void* stream) {
-  const size_t need = mm_swiglu_ffn_workspace_bytes(T, H, I, dtype);
-  if (need == 0) return MM_ERR_INVALID_ARG;
-  if (need > kNoAllocScratchBytes) return MM_ERR_UNSUPPORTED;   // beyond the fixed scratch
+  if (mm_swiglu_ffn_workspace_bytes(T, H, I, dtype) == 0) return MM_ERR_INVALID_ARG;
+  if (T == 0) return MM_OK;
+  // the automatic path when its scratch fits, else the tensor-core GEMMs
+  int path = MM_PATH_AUTO;
+  size_t need = mm::dense_workspace_for_path(T, H, I, dtype, path);
+  if (need == 0 || need > kNoAllocScratchBytes) {
+    path = MM_PATH_TENSOR;
+    need = mm::dense_workspace_for_path(T, H, I, dtype, path);
+  }
+  if (need == 0 || need > kNoAllocScratchBytes) return MM_ERR_UNSUPPORTED;   // beyond the scratch
   void* scratch = nullptr;
   const int rc = scratch_for_current_device(&scratch);
   if (rc != MM_OK) return rc;
   return mm_swiglu_ffn_ex(x, Wg, Wu, Wd, y, T, H, I, dtype, scratch, kNoAllocScratchBytes, stream,
-                          MM_PATH_AUTO);
+                          path);
 }

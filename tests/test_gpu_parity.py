@@ -156,6 +156,55 @@ def test_stream_path_is_bf16_only():
         mm.swiglu_ffn(g["x"], g["Wg"], g["Wu"], g["Wd"], path="stream")
 
 
+# ------------------------------------------------------------------ decode on the tensor cores
+@pytest.mark.parametrize("T", [1, 5, 16, 17, 40, 64])
+def test_dense_stream_tc_path(T):
+    inp = make_inputs(T, 768, 2432, "bf16", seed=80 + T)
+    g = to_dev(inp)
+    y = mm.swiglu_ffn(g["x"], g["Wg"], g["Wu"], g["Wd"], path="stream_tc")
+    ref = oracle.swiglu_ffn(*[to_f64(inp[n]) for n in ("x", "Wg", "Wu", "Wd")])
+    assert rel_err(y.double().cpu().numpy(), ref) <= Y_TOL["bf16"]
+
+
+@pytest.mark.parametrize("T,H,I", [(7, 256, 384), (33, 384, 320), (64, 128, 64)])
+def test_dense_stream_tc_small_shapes(T, H, I):
+    """Several output m-blocks, a ragged last block of I (320 = 2.5 x 128) and
+    the smallest admissible shape."""
+    inp = make_inputs(T, H, I, "bf16", seed=90 + T)
+    g = to_dev(inp)
+    y = mm.swiglu_ffn(g["x"], g["Wg"], g["Wu"], g["Wd"], path="stream_tc")
+    ref = oracle.swiglu_ffn(*[to_f64(inp[n]) for n in ("x", "Wg", "Wu", "Wd")])
+    assert rel_err(y.double().cpu().numpy(), ref) <= Y_TOL["bf16"]
+
+
+@pytest.mark.parametrize("T,E,k,bias", [(1, 8, 2, None), (4, 8, 2, (1.5, 0.5, 0, 0, 0, 0, 0, 0)),
+                                        (16, 8, 2, None), (33, 4, 1, None),
+                                        (64, 8, 2, (1.5, 0.5, 0, 0, 0, 0, 0, 0)), (9, 6, 3, None),
+                                        (20, 1, 1, None), (12, 16, 4, None)])
+def test_moe_stream_tc_path(T, E, k, bias):
+    full_moe_check(moe_inputs(T, 768, 2432, E, "bf16", seed=100 + T, bias=bias), k, 0.01, "bf16",
+                   path="stream_tc")
+
+
+def test_moe_stream_tc_deterministic():
+    inp = moe_inputs(40, 768, 2432, 8, "bf16", seed=121)
+    a = run_moe(inp, 2, 0.01, path="stream_tc")
+    b = run_moe(inp, 2, 0.01, path="stream_tc")
+    assert all(np.array_equal(u, v) for u, v in zip(a[:3], b[:3])) and a[3] == b[3]
+
+
+def test_stream_tc_shape_limits():
+    """H must be a multiple of 128 and I of 64; beyond 64 tokens the path is refused."""
+    inp = make_inputs(5, 192, 256, "bf16", seed=122)
+    g = to_dev(inp)
+    with pytest.raises(RuntimeError, match="MM_ERR_UNSUPPORTED"):
+        mm.swiglu_ffn(g["x"], g["Wg"], g["Wu"], g["Wd"], path="stream_tc")
+    inp = make_inputs(65, 256, 256, "bf16", seed=123)
+    g = to_dev(inp)
+    with pytest.raises(RuntimeError, match="MM_ERR_UNSUPPORTED"):
+        mm.swiglu_ffn(g["x"], g["Wg"], g["Wu"], g["Wd"], path="stream_tc")
+
+
 @pytest.mark.parametrize("T", [1, 4, 16, 64])
 def test_decode_workloads(T):
     """The decode-shaped workloads at full size, in the launch configuration the
@@ -205,7 +254,7 @@ def test_moe_full_size(name):
 
 
 # ------------------------------------------------------------------ CUDA graphs
-@pytest.mark.parametrize("T", [4, 600])
+@pytest.mark.parametrize("T", [4, 40, 600])
 def test_moe_forward_graph_capture_replays_identically(T):
     """The forward allocates nothing and issues only stream work once warmed up,
     so it can be captured in a CUDA graph; replays reproduce the eager result."""
