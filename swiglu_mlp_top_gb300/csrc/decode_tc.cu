@@ -5,7 +5,7 @@
 // rows, are the N operand; fp32 accumulators live in TMEM.
 //
 //   1  x (all Np rows) -> shared memory once.  MoE: router logits
-//      L = Wr x^T (M = experts, zero-padded to 128) on the tensor core; then
+//      L = x Wr^T on the tensor core (x rows as M, experts as N); then
 //      softmax / top-k / alpha per token and the grouping by expert
 //      (route_small.cuh; lesson 13 §1.5, chapter 4 §4.3).  Block 0 writes
 //      topk_idx, topk_w and the aux loss (lesson 13 §1.6).
@@ -35,23 +35,25 @@
 
 namespace mm {
 
-constexpr int kDtThreads = 192;
-constexpr int kDtWarps = kDtThreads / 32;
+constexpr int kDtThreads = 320;
+constexpr int kDtEpiWarps = 8;
 constexpr int kDtMaxStages = 6;
 constexpr int kDtTileA = 128 * 64 * 2;          // 16 KiB: 128 weight rows x 64 k
-constexpr int kDtStage = 2 * kDtTileA;          // 32 KiB
 constexpr uint32_t kDtTmemCols = 512;
 constexpr uint32_t kDtColGU = 0;                // two (G, U) buffers, 2 * Np columns each
 constexpr uint32_t kDtColD = 256;               // down accumulator
 constexpr uint32_t kDtColL = 384;               // router logits
 constexpr int kDtMaxSeg = 2;                    // output m-blocks per CTA range
 constexpr int kDtMaxCtas = 160;                 // grid cap (152 SMs on GB300)
-constexpr size_t kDtSmemBudget = 200 * 1024;
+constexpr int kDtMaxMB = 64;                    // output m-blocks (H <= 8192)
+constexpr int kDtMaxSplit = 4;                  // k-ranges per gate/up block at most
+constexpr int kDtReduceChunk = 16;              // partials requested at once in the final sum
+constexpr size_t kDtSmemBudget = 196 * 1024;   // dynamic; static use is ~27 KiB
 
 template <int MAXW>
 struct DtMaps {
-  CUtensorMap x;                  // x [T, H], box 64 x Np
-  CUtensorMap wr;                 // Wr [E, H], box 64 x 128
+  CUtensorMap x;                  // x [T, H], box 64 x Np (rows >= T read as 0)
+  CUtensorMap wr;                 // Wr [E, H], box 64 x Epad
   CUtensorMap hp;                 // Hp [nt_max * 2 * Np, I], box 64 x Np
   CUtensorMap wg[MAXW], wu[MAXW]; // [I, H], box 64 x 128
   CUtensorMap wd[MAXW];           // [H, I], box 64 x 128
@@ -71,7 +73,8 @@ struct DtArgs {
   void* y;                        // [T, H] bf16
   WsHeader* hdr;
   int stages;
-  uint32_t xs_bytes;              // x operand bytes = ring offset
+  int Epad;                       // experts padded to a multiple of 16 (router N)
+  uint32_t stage_bytes;           // 32 KiB of weight tiles + one x tile
   uint32_t alpha_off;             // alpha table [nt_max][Np] fp32
 };
 
@@ -79,16 +82,17 @@ struct DtArgs {
 struct DtPlan {
   int nt, MB_I, MB_H, KB_H, KB_I;
   int s_up, n_units;              // gate/up: blocks * k-ranges
-  long long F;                    // down tiles: MB_H * nt * KB_I
+  int F;                          // down tiles: MB_H * nt * KB_I (F * grid < 2^31)
   int per_mb;                     // down tiles per output m-block
 };
 
-__device__ __forceinline__ long long dt_range_start(int c, long long F, int G) {
-  return static_cast<long long>(c) * F / G;
-}
+__device__ __forceinline__ int dt_range_start(int c, int F, int G) { return c * F / G; }
 // CTA whose down range holds tile f (the largest c with start(c) <= f).
-__device__ __forceinline__ int dt_cta_of(long long f, long long F, int G) {
-  return static_cast<int>(((f + 1) * G - 1) / F);
+__device__ __forceinline__ int dt_cta_of(int f, int F, int G) { return ((f + 1) * G - 1) / F; }
+
+// SiLU(g) * u with the fast exponential; the limit g -> -inf gives -0.
+__device__ __forceinline__ float swiglu_fast(float g, float u) {
+  return g * __frcp_rn(1.0f + __expf(-g)) * u;
 }
 
 template <int MAXW>
@@ -96,36 +100,41 @@ __global__ void __launch_bounds__(kDtThreads, 1)
 decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
   extern __shared__ unsigned char smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* xs = smem;                                       // [KB_H][Np rows x 128 B]
-  uint8_t* ring = smem + A.xs_bytes;                        // [stages][32 KiB]
+  uint8_t* ring = smem;                                     // [stages][A.stage_bytes]
   float* alpha = reinterpret_cast<float*>(smem + A.alpha_off);
   __shared__ SmallRoute<kDecodeTcMaxT> R;
   __shared__ __align__(8) uint64_t full[kDtMaxStages], empty[kDtMaxStages];
-  __shared__ __align__(8) uint64_t xbar, lbar, tfull[2], tempty[2], dfull, dempty, drained;
+  __shared__ __align__(8) uint64_t lbar, tfull[2], tempty[2], dfull, dempty, drained;
   __shared__ uint32_t s_tmem;
   __shared__ float s_bias[MM_MAX_EXPERTS];
+  __shared__ int s_first_mb[kDtMaxCtas];        // first output m-block of each CTA's range (-1: empty)
+  __shared__ int s_c0[kDtMaxMB], s_c1[kDtMaxMB]; // CTAs whose ranges meet output m-block mb
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, cta = blockIdx.x;
   const int T = A.T, Np = A.Np, H = A.H, I = A.I, S = A.stages;
+  const uint32_t SB = A.stage_bytes;
   const uint32_t xtile = static_cast<uint32_t>(Np) * 128;  // bytes of one x / Hp tile
   const uint32_t idesc = idesc_bf16_f32(128, Np);
   const bool moe = A.moe != 0;
   WsHeader* hdr = A.hdr;
+  // epilogue warps 2..9: TMEM lane quadrant warp % 4, column half (warp - 2) / 4
+  const bool epi = warp >= 2;
+  const int quad = warp & 3, half = (warp - 2) >> 2;
+  const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
 
   if (tid == 0) {
     for (int s = 0; s < kDtMaxStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(&xbar, 1);
     mbar_init(&lbar, 1);
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], kDtEpiWarps);
     }
     mbar_init(&dfull, 1);
-    mbar_init(&dempty, 4);
+    mbar_init(&dempty, kDtEpiWarps);
     mbar_init(&drained, 1);
     fence_mbar_init();
   }
@@ -154,51 +163,51 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
   };
   auto sdesc = [&](const uint8_t* p) { return smem_desc_sw128(smem_u32(p)); };
 
-  // ------------------------------------------------------------ 1: x, router
+  // ------------------------------------------------------------ 1: router (MoE)
+  // L[t, e] = x_t . Wr_e per k-block: stage = x tile at 0 (the A operand:
+  // 128 rows are read, rows >= Np are ignored) and the Wr tile (N = Epad) at 16 KiB.
   const int KB_H = H / 64;
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&xbar, KB_H * xtile);
-    for (int kb = 0; kb < KB_H; ++kb) tma_load_2d(xs + kb * xtile, &M.x, &xbar, kb * 64, 0);
-    if (moe) {
+  const uint32_t wtile = static_cast<uint32_t>(A.Epad) * 128;
+  if (moe) {
+    if (tid == 0) {
       for (int kb = 0; ok && kb < KB_H; ++kb) {
         int s;
         if (!acquire(s)) { ok = false; break; }
-        mbar_arrive_expect_tx(&full[s], kDtTileA);
-        tma_load_2d(ring + s * kDtStage, &M.wr, &full[s], kb * 64, 0);
+        uint8_t* st = ring + s * SB;
+        mbar_arrive_expect_tx(&full[s], xtile + wtile);
+        tma_load_2d(st, &M.x, &full[s], kb * 64, 0);
+        tma_load_2d(st + kDtTileA, &M.wr, &full[s], kb * 64, 0);
         ++p_it;
       }
     }
-  }
-  if (tid == 32) {
-    ok = mbar_wait(&xbar, 0, nullptr, hdr, 42);
-    tc_fence_after();
-    if (moe && ok) {
+    if (tid == 32) {
+      const uint32_t idesc_r = idesc_bf16_f32(128, A.Epad);
       for (int kb = 0; kb < KB_H; ++kb) {
         int s;
         if (!consume(s)) { ok = false; break; }
-        const uint8_t* a = ring + s * kDtStage;
-        const uint8_t* b = xs + kb * xtile;
+        const uint8_t* st = ring + s * SB;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          umma_bf16(tmem + kDtColL, sdesc(a + kk * 32), sdesc(b + kk * 32), idesc, (kb | kk) ? 1u : 0u);
+          umma_bf16(tmem + kDtColL, sdesc(st + kk * 32), sdesc(st + kDtTileA + kk * 32), idesc_r,
+                    (kb | kk) ? 1u : 0u);
         umma_commit(&empty[s]);
         ++m_it;
       }
-      umma_commit(&lbar);
+      if (ok) umma_commit(&lbar);
     }
-  }
-  if (moe && warp >= 2) {
-    ok = warp_wait(&lbar, 0, nullptr, hdr, 43);
-    tc_fence_after();
-    const int quad = warp & 3, e = quad * 32 + lane;
-    for (int c0 = 0; ok && c0 < Np; c0 += 16) {
-      uint32_t r[16];
-      tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(quad * 32) << 16) + kDtColL + c0, r);
-      tmem_ld_wait();
-      if (e < A.E) {
+    if (epi && half == 0) {
+      ok = warp_wait(&lbar, 0, nullptr, hdr, 43);
+      tc_fence_after();
+      const int t = quad * 32 + lane;        // TMEM lane = token
+      for (int c0 = 0; ok && c0 < A.Epad; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(tmem + lane_base + kDtColL + c0, r);
+        tmem_ld_wait();
+        if (t < T) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (c0 + j < T) R.prob[c0 + j][e] = __uint_as_float(r[j]);
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < A.E) R.prob[t][c0 + j] = __uint_as_float(r[j]);
+        }
       }
     }
   }
@@ -207,7 +216,7 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
   // ------------------------------------------------------------ routing
   if (ok) {
     if (moe) {
-      route_softmax_topk(R, T, A.E, A.k, s_bias, warp, kDtWarps, lane);
+      route_softmax_topk(R, T, A.E, A.k, s_bias, tid, kDtThreads);
       __syncthreads();
       if (warp == 0) route_group(R, T * A.k, A.E, lane);
     } else {
@@ -232,18 +241,30 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
   P.KB_H = KB_H;
   P.KB_I = I / 64;
   {
+    // split K only as far as needed to occupy the grid, keeping at least
+    // three k-blocks per range (the partials cost traffic of their own)
     const int blocks = P.nt * P.MB_I;
+    const int max_split = P.KB_H / 3 < 1 ? 1 : (P.KB_H / 3 > kDtMaxSplit ? kDtMaxSplit : P.KB_H / 3);
     int s_up = (G + blocks - 1) / blocks;
-    s_up = s_up < 1 ? 1 : (s_up > P.KB_H ? P.KB_H : s_up);
+    s_up = s_up < 1 ? 1 : (s_up > max_split ? max_split : s_up);
     P.s_up = s_up;
     P.n_units = blocks * s_up;
   }
   P.per_mb = P.nt * P.KB_I;
-  P.F = static_cast<long long>(P.MB_H) * P.per_mb;
-  const long long r0 = dt_range_start(cta, P.F, G), r1 = dt_range_start(cta + 1, P.F, G);
-  const int my_down = static_cast<int>(r1 - r0);
+  P.F = P.MB_H * P.per_mb;
+  const int r0 = dt_range_start(cta, P.F, G), r1 = dt_range_start(cta + 1, P.F, G);
+  const int my_down = r1 - r0;
   const int n_pre = my_down < S ? my_down : S;     // Wd tiles requested before the barrier
   int pre_it0 = 0;                                 // producer: stage use of the first of them
+  // contributors of every output m-block, for the final reduction
+  for (int c = tid; c < G; c += kDtThreads) {
+    const int s0 = dt_range_start(c, P.F, G);
+    s_first_mb[c] = dt_range_start(c + 1, P.F, G) > s0 ? s0 / P.per_mb : -1;
+  }
+  for (int mb = tid; mb < P.MB_H; mb += kDtThreads) {
+    s_c0[mb] = dt_cta_of(mb * P.per_mb, P.F, G);
+    s_c1[mb] = dt_cta_of(mb * P.per_mb + P.per_mb - 1, P.F, G);
+  }
 
   // unit u -> (touched index, m-block, k-block range)
   auto unit_of = [&](int u, int& ti, int& mb, int& kb0, int& kb1) {
@@ -253,14 +274,15 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
     kb0 = kr * P.KB_H / P.s_up;
     kb1 = (kr + 1) * P.KB_H / P.s_up;
   };
-  auto tile_of = [&](long long f, int& mbd, int& ti, int& kb) {
-    mbd = static_cast<int>(f / P.per_mb);
-    const int rem = static_cast<int>(f - static_cast<long long>(mbd) * P.per_mb);
+  auto tile_of = [&](int f, int& mbd, int& ti, int& kb) {
+    mbd = f / P.per_mb;
+    const int rem = f - mbd * P.per_mb;
     ti = rem / P.KB_I;
     kb = rem - ti * P.KB_I;
   };
 
   // ------------------------------------------------------------ 2: gate/up
+  // stage = Wg tile at 0, Wu tile at 16 KiB, x tile (B, N = Np) at 32 KiB
   if (ok) {
     if (tid == 0) {
       for (int u = cta; ok && u < P.n_units; u += G) {
@@ -270,9 +292,11 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
         for (int kb = kb0; kb < kb1; ++kb) {
           int s;
           if (!acquire(s)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[s], 2 * kDtTileA);
-          tma_load_2d(ring + s * kDtStage, &M.wg[e], &full[s], kb * 64, mb * 128);
-          tma_load_2d(ring + s * kDtStage + kDtTileA, &M.wu[e], &full[s], kb * 64, mb * 128);
+          uint8_t* st = ring + s * SB;
+          mbar_arrive_expect_tx(&full[s], 2 * kDtTileA + xtile);
+          tma_load_2d(st, &M.wg[e], &full[s], kb * 64, mb * 128);
+          tma_load_2d(st + kDtTileA, &M.wu[e], &full[s], kb * 64, mb * 128);
+          tma_load_2d(st + 2 * kDtTileA, &M.x, &full[s], kb * 64, 0);
           ++p_it;
         }
       }
@@ -282,7 +306,7 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
         tile_of(r0 + j, mbd, ti, kb);
         if (!acquire(s)) { ok = false; break; }
         mbar_arrive_expect_tx(&full[s], kDtTileA + 2 * xtile);   // the Hp tiles follow later
-        tma_load_2d(ring + s * kDtStage, &M.wd[R.touched[ti]], &full[s], kb * 64, mbd * 128);
+        tma_load_2d(ring + s * SB, &M.wd[R.touched[ti]], &full[s], kb * 64, mbd * 128);
         ++p_it;
       }
     }
@@ -298,14 +322,14 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
         for (int kb = kb0; kb < kb1; ++kb) {
           int s;
           if (!consume(s)) { ok = false; break; }
-          const uint8_t* a = ring + s * kDtStage;
-          const uint8_t* b = xs + kb * xtile;
+          const uint8_t* st = ring + s * SB;
+          const uint8_t* b = st + 2 * kDtTileA;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(dg, sdesc(a + kk * 32), sdesc(b + kk * 32), idesc, (kb > kb0 || kk) ? 1u : 0u);
+            umma_bf16(dg, sdesc(st + kk * 32), sdesc(b + kk * 32), idesc, (kb > kb0 || kk) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(du, sdesc(a + kDtTileA + kk * 32), sdesc(b + kk * 32), idesc,
+            umma_bf16(du, sdesc(st + kDtTileA + kk * 32), sdesc(b + kk * 32), idesc,
                       (kb > kb0 || kk) ? 1u : 0u);
           umma_commit(&empty[s]);
           ++m_it;
@@ -314,8 +338,9 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
         umma_commit(&tfull[acc]);
       }
     }
-    if (warp >= 2) {
-      const int quad = warp & 3, rl = quad * 32 + lane;
+    if (epi) {
+      const int rl = quad * 32 + lane;
+      const int cbeg = half * (Np / 2), cend = cbeg + Np / 2;   // this warp's token columns
       int local = 0;
       for (int u = cta; ok && u < P.n_units; u += G, ++local) {
         int ti, mb, kb0, kb1;
@@ -323,20 +348,20 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
         const int acc = local & 1;
         if (!warp_wait(&tfull[acc], (local >> 1) & 1, nullptr, hdr, 45)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t tg = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kDtColGU + acc * 2 * Np;
+        const uint32_t tg = tmem + lane_base + kDtColGU + acc * 2 * Np;
         const int i = mb * 128 + rl;
-        for (int c0 = 0; c0 < Np; c0 += 16) {
-          uint32_t gr[16], ur[16];
-          tmem_ld_32x32b_x16(tg + c0, gr);
-          tmem_ld_32x32b_x16(tg + Np + c0, ur);
+        for (int c0 = cbeg; c0 < cend; c0 += 8) {
+          uint32_t gr[8], ur[8];
+          tmem_ld_32x32b_x8(tg + c0, gr);
+          tmem_ld_32x32b_x8(tg + Np + c0, ur);
           tmem_ld_wait();
           if (P.s_up == 1) {
             if (i < I) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
+              for (int j = 0; j < 8; ++j) {
                 const int t = c0 + j;
-                const float g = __uint_as_float(gr[j]), uu = __uint_as_float(ur[j]);
-                const float v = silu_f32(g) * uu * alpha[ti * Np + t];
+                const float v = swiglu_fast(__uint_as_float(gr[j]), __uint_as_float(ur[j])) *
+                                alpha[ti * Np + t];
                 const __nv_bfloat16 hi = __float2bfloat16_rn(v);
                 const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
                 A.hp[(static_cast<size_t>(ti * 2) * Np + t) * I + i] = hi;
@@ -346,7 +371,7 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
           } else {
             float* pg = A.pgu + static_cast<size_t>(u) * 2 * Np * 128;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < 8; ++j) {
               pg[static_cast<size_t>(c0 + j) * 128 + rl] = __uint_as_float(gr[j]);
               pg[static_cast<size_t>(Np + c0 + j) * 128 + rl] = __uint_as_float(ur[j]);
             }
@@ -367,34 +392,55 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
     ok = grid_barrier(hdr, 46, round++, nullptr);
   }
   if (ok && P.s_up > 1) {
-    // add the k-range partials of G and U in order, then as the direct path
+    // add the k-range partials of G and U in order (zeros past s_up change
+    // nothing), then as the direct path
     const int blocks = P.nt * P.MB_I;
-    const long long total = static_cast<long long>(blocks) * Np * 128;
-    for (long long q = static_cast<long long>(cta) * kDtThreads + tid; q < total;
-         q += static_cast<long long>(G) * kDtThreads) {
-      const int blk = static_cast<int>(q / (Np * 128));
-      const int rem = static_cast<int>(q - static_cast<long long>(blk) * Np * 128);
-      const int t = rem >> 7, rl = rem & 127;
-      const int ti = blk / P.MB_I, mb = blk - ti * P.MB_I;
-      const int i = mb * 128 + rl;
-      if (i >= I) continue;
-      float g = 0.f, uu = 0.f;
-      for (int kr = 0; kr < P.s_up; ++kr) {
-        const float* pg = A.pgu + static_cast<size_t>(blk * P.s_up + kr) * 2 * Np * 128;
-        g += pg[static_cast<size_t>(t) * 128 + rl];
-        uu += pg[static_cast<size_t>(Np + t) * 128 + rl];
+    const int per_blk = Np * 128;
+    const int total = blocks * per_blk;
+    const int stride = G * kDtThreads;
+    for (int q0 = cta * kDtThreads + tid; q0 < total; q0 += 2 * stride) {
+      // every partial of two elements is requested before any is added
+      float pgv[2][kDtMaxSplit], puv[2][kDtMaxSplit];
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        const int q = q0 + w * stride;
+        const int blk = q / per_blk, rem = q - blk * per_blk;
+        const float* pg = A.pgu + static_cast<size_t>(blk * P.s_up) * 2 * per_blk + rem;
+#pragma unroll
+        for (int kr = 0; kr < kDtMaxSplit; ++kr) {
+          const bool live = q < total && kr < P.s_up;
+          pgv[w][kr] = live ? pg[static_cast<size_t>(kr) * 2 * per_blk] : 0.f;
+          puv[w][kr] = live ? pg[static_cast<size_t>(kr) * 2 * per_blk + per_blk] : 0.f;
+        }
       }
-      const float v = silu_f32(g) * uu * alpha[ti * Np + t];
-      const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-      const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-      A.hp[(static_cast<size_t>(ti * 2) * Np + t) * I + i] = hi;
-      A.hp[(static_cast<size_t>(ti * 2 + 1) * Np + t) * I + i] = lo;
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        const int q = q0 + w * stride;
+        if (q >= total) break;
+        float g = 0.f, uu = 0.f;
+#pragma unroll
+        for (int kr = 0; kr < kDtMaxSplit; ++kr) {
+          g += pgv[w][kr];
+          uu += puv[w][kr];
+        }
+        const int blk = q / per_blk, rem = q - blk * per_blk;
+        const int t = rem >> 7, rl = rem & 127;
+        const int ti = blk / P.MB_I, mb = blk - ti * P.MB_I;
+        const int i = mb * 128 + rl;
+        if (i >= I) continue;
+        const float v = swiglu_fast(g, uu) * alpha[ti * Np + t];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+        A.hp[(static_cast<size_t>(ti * 2) * Np + t) * I + i] = hi;
+        A.hp[(static_cast<size_t>(ti * 2 + 1) * Np + t) * I + i] = lo;
+      }
     }
     asm volatile("fence.proxy.async.global;" ::: "memory");
     ok = grid_barrier(hdr, 47, round++, nullptr);
   }
 
   // ------------------------------------------------------------ 3: down
+  // stage = Wd tile at 0, Hp high part at 16 KiB, Hp remainder after it
   if (ok) {
     if (tid == 0) {
       asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -406,10 +452,10 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
         } else {
           if (!acquire(s)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[s], kDtTileA + 2 * xtile);
-          tma_load_2d(ring + s * kDtStage, &M.wd[R.touched[ti]], &full[s], kb * 64, mbd * 128);
+          tma_load_2d(ring + s * SB, &M.wd[R.touched[ti]], &full[s], kb * 64, mbd * 128);
           ++p_it;
         }
-        uint8_t* b = ring + s * kDtStage + kDtTileA;
+        uint8_t* b = ring + s * SB + kDtTileA;
         tma_load_2d(b, &M.hp, &full[s], kb * 64, (ti * 2) * Np);
         tma_load_2d(b + xtile, &M.hp, &full[s], kb * 64, (ti * 2 + 1) * Np);
       }
@@ -429,7 +475,7 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
           first = true;
         }
         if (!consume(s)) { ok = false; break; }
-        const uint8_t* a = ring + s * kDtStage;
+        const uint8_t* a = ring + s * SB;
         const uint8_t* b = a + kDtTileA;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
@@ -444,19 +490,20 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
       }
       if (ok && seg >= 0) umma_commit(&dfull);
     }
-    if (warp >= 2) {
-      const int quad = warp & 3, rl = quad * 32 + lane;
-      const int n_seg = my_down > 0 ? static_cast<int>((r1 - 1) / P.per_mb - r0 / P.per_mb) + 1 : 0;
+    if (epi) {
+      const int rl = quad * 32 + lane;
+      const int cbeg = half * (Np / 2), cend = cbeg + Np / 2;
+      const int n_seg = my_down > 0 ? (r1 - 1) / P.per_mb - r0 / P.per_mb + 1 : 0;
       for (int seg = 0; ok && seg < n_seg; ++seg) {
         if (!warp_wait(&dfull, seg & 1, nullptr, hdr, 49)) { ok = false; break; }
         tc_fence_after();
         float* pdst = A.pd + (static_cast<size_t>(cta) * kDtMaxSeg + seg) * Np * 128;
-        for (int c0 = 0; c0 < Np; c0 += 16) {
-          uint32_t r[16];
-          tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(quad * 32) << 16) + kDtColD + c0, r);
+        for (int c0 = cbeg; c0 < cend; c0 += 8) {
+          uint32_t r[8];
+          tmem_ld_32x32b_x8(tmem + lane_base + kDtColD + c0, r);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) pdst[static_cast<size_t>(c0 + j) * 128 + rl] = __uint_as_float(r[j]);
+          for (int j = 0; j < 8; ++j) pdst[static_cast<size_t>(c0 + j) * 128 + rl] = __uint_as_float(r[j]);
         }
         tc_fence_before();
         __syncwarp();
@@ -470,19 +517,22 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
   unsigned ticket = 0xffffffffu;
   if (ok) ok = grid_barrier(hdr, 50, round, &ticket);
   if (ok) {
-    const long long total = static_cast<long long>(T) * H;
-    for (long long q = static_cast<long long>(cta) * kDtThreads + tid; q < total;
-         q += static_cast<long long>(G) * kDtThreads) {
-      const int t = static_cast<int>(q / H), j = static_cast<int>(q - static_cast<long long>(t) * H);
+    const int total = T * H;
+    for (int q = cta * kDtThreads + tid; q < total; q += G * kDtThreads) {
+      const int t = q / H, j = q - t * H;
       const int mbd = j >> 7, rl = j & 127;
-      const long long f0 = static_cast<long long>(mbd) * P.per_mb;
-      const int c0 = dt_cta_of(f0, P.F, G), c1 = dt_cta_of(f0 + P.per_mb - 1, P.F, G);
       float v = 0.f;
-      for (int c = c0; c <= c1; ++c) {
-        const long long s0 = dt_range_start(c, P.F, G);
-        if (dt_range_start(c + 1, P.F, G) == s0) continue;     // empty range
-        const int seg = mbd - static_cast<int>(s0 / P.per_mb);
-        v += A.pd[((static_cast<size_t>(c) * kDtMaxSeg + seg) * Np + t) * 128 + rl];
+      for (int cb = s_c0[mbd]; cb <= s_c1[mbd]; cb += kDtReduceChunk) {
+        float part[kDtReduceChunk];
+#pragma unroll
+        for (int w = 0; w < kDtReduceChunk; ++w) {
+          const int c = cb + w;
+          const int fm = c <= s_c1[mbd] ? s_first_mb[c] : -1;   // -1: past the end or empty range
+          part[w] = fm >= 0 ? A.pd[((static_cast<size_t>(c) * kDtMaxSeg + (mbd - fm)) * Np + t) * 128 + rl]
+                            : 0.f;
+        }
+#pragma unroll
+        for (int w = 0; w < kDtReduceChunk; ++w) v += part[w];
       }
       static_cast<__nv_bfloat16*>(A.y)[q] = __float2bfloat16_rn(v);
     }
@@ -512,8 +562,8 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
 namespace {
 
 struct DtLayout {
-  int Np, nt_max, stages;
-  size_t xs, alpha_off, smem;           // shared memory
+  int Np, Epad, nt_max, stages;
+  size_t stage, alpha_off, smem;        // shared memory
   size_t hp, pgu, pd, total;            // workspace (after the header)
 };
 
@@ -523,19 +573,25 @@ bool dt_layout(int T, int H, int I, int E, int k, DtLayout& L) {
   if (T < 1 || T > kDecodeTcMaxT || H % 128 != 0 || I % 64 != 0) return false;
   if (E > 1 && (E > MM_MAX_EXPERTS || k < 1 || k > MM_MAX_TOPK || k > E)) return false;
   L.Np = (T + 15) / 16 * 16;
+  L.Epad = (E + 15) / 16 * 16;
   L.nt_max = E > 1 ? (E < T * k ? E : T * k) : 1;
-  L.xs = static_cast<size_t>(L.Np) * 2 * H;
+  // a stage holds two 16 KiB weight tiles and one x tile (gate/up), or the
+  // x and Wr tiles (router), or a Wd tile and the two Hp tiles (down)
+  L.stage = round_up(2 * static_cast<size_t>(kDtTileA) + static_cast<size_t>(L.Np) * 128, 1024);
   const size_t alpha = round_up(static_cast<size_t>(L.nt_max) * L.Np * 4, 1024);
-  const size_t avail = kDtSmemBudget - 1024 - L.xs - alpha;   // 1 KiB: alignment slack
-  if (L.xs + alpha + 2 * kDtStage + 1024 > kDtSmemBudget) return false;
-  L.stages = static_cast<int>(avail / kDtStage);
+  if (kDtSmemBudget < 1024 + alpha + 2 * L.stage) return false;
+  L.stages = static_cast<int>((kDtSmemBudget - 1024 - alpha) / L.stage);
   if (L.stages > kDtMaxStages) L.stages = kDtMaxStages;
-  L.alpha_off = L.xs + static_cast<size_t>(L.stages) * kDtStage;
-  L.smem = L.alpha_off + alpha + 1024;
+  L.alpha_off = static_cast<size_t>(L.stages) * L.stage;
+  L.smem = L.alpha_off + alpha + 1024;               // 1 KiB: alignment slack
   const int G = kDtMaxCtas;
   const int blocks = L.nt_max * ((I + 127) / 128);
-  const int units = blocks + G;                    // blocks * ceil(G / blocks) < blocks + G
-  if (H / 128 > G) return false;
+  const int units = blocks + G;                      // blocks * ceil(G / blocks) < blocks + G
+  if (H / 128 > G || H / 128 > kDtMaxMB) return false;
+  {
+    const long long F = static_cast<long long>(H / 128) * L.nt_max * (I / 64);
+    if ((F + 1) * G >= (1ll << 31)) return false;    // down-range arithmetic in 32 bits
+  }
   L.hp = round_up(static_cast<size_t>(L.nt_max) * 2 * L.Np * I * 2, 256);
   L.pgu = round_up(static_cast<size_t>(units) * 2 * L.Np * 128 * 4, 256);
   L.pd = round_up(static_cast<size_t>(G) * kDtMaxSeg * L.Np * 128 * 4, 256);
@@ -552,7 +608,7 @@ cudaError_t decode_tc_impl(const DtLayout& L, const void* x, const void* Wr,
   std::lock_guard<std::mutex> lock(mu);
   const int T = A.T, H = A.H, I = A.I, nw = A.moe ? A.E : 1;
   if (!make_map_16(&m.x, x, H, T, L.Np, false)) return cudaErrorInvalidValue;
-  if (A.moe && !make_map_16(&m.wr, Wr, H, A.E, 128, false)) return cudaErrorInvalidValue;
+  if (A.moe && !make_map_16(&m.wr, Wr, H, A.E, L.Epad, false)) return cudaErrorInvalidValue;
   if (!make_map_16(&m.hp, A.hp, I, static_cast<uint64_t>(L.nt_max) * 2 * L.Np, L.Np, false))
     return cudaErrorInvalidValue;
   for (int e = 0; e < nw; ++e) {
@@ -609,7 +665,8 @@ cudaError_t launch_decode_tc(const void* x, const void* Wr, const float* bias,
   A.pd = reinterpret_cast<float*>(base + L.hp + L.pgu);
   A.y = y; A.hdr = hdr;
   A.stages = L.stages;
-  A.xs_bytes = static_cast<uint32_t>(L.xs);
+  A.Epad = L.Epad;
+  A.stage_bytes = static_cast<uint32_t>(L.stage);
   A.alpha_off = static_cast<uint32_t>(L.alpha_off);
   if (A.E <= 8) return decode_tc_impl<8>(L, x, Wr, Wg, Wu, Wd, A, st);
   return decode_tc_impl<MM_MAX_EXPERTS>(L, x, Wr, Wg, Wu, Wd, A, st);

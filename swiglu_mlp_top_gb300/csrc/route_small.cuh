@@ -21,7 +21,7 @@ struct SmallRoute {
   float sel_a[MAXT * MM_MAX_TOPK];   // its alpha
   int rank[MAXT * MM_MAX_TOPK];      // its place among its expert's assignments
   int by_e[MAXT * MM_MAX_TOPK];      // assignments grouped by expert, in token order
-  float prob[MAXT][MM_MAX_EXPERTS];  // logits, then probabilities
+  float prob[MAXT][MM_MAX_EXPERTS + 1];  // logits, then probabilities (row padded)
 };
 
 __device__ __forceinline__ float warp_allsum_f(float v) {
@@ -30,51 +30,46 @@ __device__ __forceinline__ float warp_allsum_f(float v) {
   return v;
 }
 
-// Tokens t = first, first + stride, ...: R.prob[t][:] holds the logits on
-// entry and the probabilities on exit.  Lane e holds experts e and e + 32:
-// softmax with the maximum subtracted, then k arg-max rounds over
-// (p desc, index asc) — equal probabilities go to the lower index — and
-// alpha = p / (sum_S p + 1e-20).
+// One thread per token t (t = first, first + stride, ...): R.prob[t][:]
+// holds the logits on entry and the probabilities on exit.  Softmax with the
+// maximum subtracted (fast exponential, one reciprocal); then k arg-max passes in expert order with a strict
+// comparison, so that of equal probabilities the lower expert index is taken
+// first; alpha = p / (sum_S p + 1e-20).
 template <int MAXT>
 __device__ __forceinline__ void route_softmax_topk(SmallRoute<MAXT>& R, int T, int E, int k,
-                                                   const float* bias, int first, int stride,
-                                                   int lane) {
+                                                   const float* bias, int first, int stride) {
   for (int t = first; t < T; t += stride) {
-    float r0 = -INFINITY, r1 = -INFINITY;
-    if (lane < E) r0 = R.prob[t][lane] + bias[lane];
-    if (lane + 32 < E) r1 = R.prob[t][lane + 32] + bias[lane + 32];
-    float m = fmaxf(r0, r1);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float x0 = (lane < E) ? expf(r0 - m) : 0.f;
-    const float x1 = (lane + 32 < E) ? expf(r1 - m) : 0.f;
-    const float z = warp_allsum_f(x0 + x1);
-    const float p0 = x0 / z, p1 = x1 / z;
-    if (lane < E) R.prob[t][lane] = p0;
-    if (lane + 32 < E) R.prob[t][lane + 32] = p1;
-    bool taken0 = lane >= E, taken1 = lane + 32 >= E;
-    float sel_sum = 0.f, my_p = 0.f;
-    int my_e = 0;
+    float* row = R.prob[t];
+    float m = -INFINITY;
+    for (int e = 0; e < E; ++e) {
+      const float r = row[e] + bias[e];
+      row[e] = r;
+      m = fmaxf(m, r);
+    }
+    float z = 0.f;
+    for (int e = 0; e < E; ++e) {
+      const float x = __expf(row[e] - m);
+      row[e] = x;
+      z += x;
+    }
+    const float rz = 1.0f / z;
+    for (int e = 0; e < E; ++e) row[e] *= rz;
+    uint64_t taken = 0;
+    float sel_sum = 0.f;
     for (int s = 0; s < k; ++s) {
       float bp = -1.f;
-      int be = 0x7fffffff;
-      if (!taken0) { bp = p0; be = lane; }
-      if (!taken1 && (p1 > bp)) { bp = p1; be = lane + 32; }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float op = __shfl_xor_sync(0xffffffffu, bp, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (op > bp || (op == bp && oe < be)) { bp = op; be = oe; }
+      int be = 0;
+      for (int e = 0; e < E; ++e) {
+        const float p = row[e];
+        if (!((taken >> e) & 1ull) && p > bp) { bp = p; be = e; }
       }
-      if (be == lane) taken0 = true;
-      if (be == lane + 32) taken1 = true;
+      taken |= 1ull << be;
       sel_sum += bp;
-      if (lane == s) { my_p = bp; my_e = be; }
+      R.sel_e[t * k + s] = be;
+      R.sel_a[t * k + s] = bp;
     }
-    if (lane < k) {
-      R.sel_e[t * k + lane] = my_e;
-      R.sel_a[t * k + lane] = my_p / (sel_sum + 1e-20f);
-    }
+    const float inv = sel_sum + 1e-20f;
+    for (int s = 0; s < k; ++s) R.sel_a[t * k + s] = R.sel_a[t * k + s] / inv;
   }
 }
 
