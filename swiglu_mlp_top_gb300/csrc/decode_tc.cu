@@ -29,6 +29,7 @@
 // Warp roles (192 threads): warp 0 lane 0 issues TMA, warp 1 lane 0 issues
 // UMMA and owns TMEM, warps 2-5 are the epilogue (TMEM lane quadrant
 // warp % 4).  All waits are bounded.
+#include <algorithm>
 #include <mutex>
 
 #include "route_small.cuh"
@@ -47,14 +48,15 @@ constexpr int kDtMaxSeg = 2;                    // output m-blocks per CTA range
 constexpr int kDtMaxCtas = 160;                 // grid cap (152 SMs on GB300)
 constexpr int kDtMaxMB = 64;                    // output m-blocks (H <= 8192)
 constexpr int kDtMaxSplit = 4;                  // k-ranges per gate/up block at most
-constexpr int kDtReduceChunk = 16;              // partials requested at once in the final sum
+constexpr int kDtReduceChunk = 32;              // partials requested at once in the final sum
 constexpr size_t kDtSmemBudget = 196 * 1024;   // dynamic; static use is ~27 KiB
 
 template <int MAXW>
 struct DtMaps {
   CUtensorMap x;                  // x [T, H], box 64 x Np (rows >= T read as 0)
   CUtensorMap wr;                 // Wr [E, H], box 64 x Epad
-  CUtensorMap hp;                 // Hp [nt_max * 2 * Np, I], box 64 x Np
+  CUtensorMap hp;                 // Hp [nt_max * 2 * Np, I], box 64 x Np (loads, 128-byte swizzle)
+  CUtensorMap hps;                // the same matrix, box 128 x Np, no swizzle (stores)
   CUtensorMap wg[MAXW], wu[MAXW]; // [I, H], box 64 x 128
   CUtensorMap wd[MAXW];           // [H, I], box 64 x 128
 };
@@ -75,6 +77,7 @@ struct DtArgs {
   int stages;
   int Epad;                       // experts padded to a multiple of 16 (router N)
   uint32_t stage_bytes;           // 32 KiB of weight tiles + one x tile
+  uint32_t hstage_off;            // Hp staging tile [2][Np][128] bf16 (epilogue -> TMA store)
   uint32_t alpha_off;             // alpha table [nt_max][Np] fp32
 };
 
@@ -90,10 +93,32 @@ __device__ __forceinline__ int dt_range_start(int c, int F, int G) { return c * 
 // CTA whose down range holds tile f (the largest c with start(c) <= f).
 __device__ __forceinline__ int dt_cta_of(int f, int F, int G) { return ((f + 1) * G - 1) / F; }
 
-// SiLU(g) * u with the fast exponential; the limit g -> -inf gives -0.
+// SiLU(g) * u with the fast exponential and division (for g -> -inf the
+// divisor overflows to inf and the quotient is 0).
 __device__ __forceinline__ float swiglu_fast(float g, float u) {
-  return g * __frcp_rn(1.0f + __expf(-g)) * u;
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
+
+constexpr int kDtEpiLeader = 64;                // warp 2, lane 0
+// Barrier among the eight epilogue warps only (named barrier 1), plain and
+// with an AND of one predicate over the 256 threads.
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kDtEpiWarps * 32) : "memory");
+}
+__device__ __forceinline__ bool epi_sync_and(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\t"
+      "setp.ne.u32 a, %1, 0;\n\t"
+      "bar.red.and.pred b, 1, %2, a;\n\t"
+      "selp.u32 %0, 1, 0, b;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p)), "n"(kDtEpiWarps * 32)
+      : "memory");
+  return r != 0;
+}
+
+
 
 template <int MAXW>
 __global__ void __launch_bounds__(kDtThreads, 1)
@@ -102,9 +127,10 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
   uint8_t* smem = align1024(smem_raw);
   uint8_t* ring = smem;                                     // [stages][A.stage_bytes]
   float* alpha = reinterpret_cast<float*>(smem + A.alpha_off);
+  __nv_bfloat16* hstage = reinterpret_cast<__nv_bfloat16*>(smem + A.hstage_off);
   __shared__ SmallRoute<kDecodeTcMaxT> R;
   __shared__ __align__(8) uint64_t full[kDtMaxStages], empty[kDtMaxStages];
-  __shared__ __align__(8) uint64_t lbar, tfull[2], tempty[2], dfull, dempty, drained;
+  __shared__ __align__(8) uint64_t wbar, lbar, tfull[2], tempty[2], dfull, dempty, drained;
   __shared__ uint32_t s_tmem;
   __shared__ float s_bias[MM_MAX_EXPERTS];
   __shared__ int s_first_mb[kDtMaxCtas];        // first output m-block of each CTA's range (-1: empty)
@@ -128,6 +154,7 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
+    mbar_init(&wbar, 1);
     mbar_init(&lbar, 1);
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -164,48 +191,48 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
   auto sdesc = [&](const uint8_t* p) { return smem_desc_sw128(smem_u32(p)); };
 
   // ------------------------------------------------------------ 1: router (MoE)
-  // L[t, e] = x_t . Wr_e per k-block: stage = x tile at 0 (the A operand:
-  // 128 rows are read, rows >= Np are ignored) and the Wr tile (N = Epad) at 16 KiB.
+  // L[t, e] = x_t . Wr_e.  All k-blocks are requested at once into the ring
+  // region (its stages are first used after the routing): the x tiles
+  // (A operand: 128 rows are read from each, rows >= Np are ignored), then
+  // the Wr tiles (B operand, N = Epad).
   const int KB_H = H / 64;
   const uint32_t wtile = static_cast<uint32_t>(A.Epad) * 128;
+  uint8_t* rx = ring;
+  uint8_t* rw = ring + KB_H * xtile;
   if (moe) {
     if (tid == 0) {
-      for (int kb = 0; ok && kb < KB_H; ++kb) {
-        int s;
-        if (!acquire(s)) { ok = false; break; }
-        uint8_t* st = ring + s * SB;
-        mbar_arrive_expect_tx(&full[s], xtile + wtile);
-        tma_load_2d(st, &M.x, &full[s], kb * 64, 0);
-        tma_load_2d(st + kDtTileA, &M.wr, &full[s], kb * 64, 0);
-        ++p_it;
+      mbar_arrive_expect_tx(&wbar, KB_H * (xtile + wtile));
+      for (int kb = 0; kb < KB_H; ++kb) {
+        tma_load_2d(rx + kb * xtile, &M.x, &wbar, kb * 64, 0);
+        tma_load_2d(rw + kb * wtile, &M.wr, &wbar, kb * 64, 0);
       }
     }
     if (tid == 32) {
-      const uint32_t idesc_r = idesc_bf16_f32(128, A.Epad);
-      for (int kb = 0; kb < KB_H; ++kb) {
-        int s;
-        if (!consume(s)) { ok = false; break; }
-        const uint8_t* st = ring + s * SB;
+      ok = mbar_wait(&wbar, 0, nullptr, hdr, 42);
+      tc_fence_after();
+      if (ok) {
+        const uint32_t idesc_r = idesc_bf16_f32(128, A.Epad);
+        for (int kb = 0; kb < KB_H; ++kb) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16(tmem + kDtColL, sdesc(st + kk * 32), sdesc(st + kDtTileA + kk * 32), idesc_r,
-                    (kb | kk) ? 1u : 0u);
-        umma_commit(&empty[s]);
-        ++m_it;
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + kDtColL, sdesc(rx + kb * xtile + kk * 32), sdesc(rw + kb * wtile + kk * 32),
+                      idesc_r, (kb | kk) ? 1u : 0u);
+        }
+        umma_commit(&lbar);
       }
-      if (ok) umma_commit(&lbar);
     }
     if (epi && half == 0) {
       ok = warp_wait(&lbar, 0, nullptr, hdr, 43);
       tc_fence_after();
       const int t = quad * 32 + lane;        // TMEM lane = token
-      for (int c0 = 0; ok && c0 < A.Epad; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld_32x32b_x16(tmem + lane_base + kDtColL + c0, r);
+#pragma unroll 1
+      for (int c0 = 0; ok && c0 < A.Epad; c0 += 8) {
+        uint32_t r[8];
+        tmem_ld_32x32b_x8(tmem + lane_base + kDtColL + c0, r);
         tmem_ld_wait();
         if (t < T) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
+          for (int j = 0; j < 8; ++j)
             if (c0 + j < A.E) R.prob[t][c0 + j] = __uint_as_float(r[j]);
         }
       }
@@ -241,10 +268,11 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
   P.KB_H = KB_H;
   P.KB_I = I / 64;
   {
-    // split K only as far as needed to occupy the grid, keeping at least
-    // three k-blocks per range (the partials cost traffic of their own)
+    // split K only for long rows (>= 24 k-blocks), keeping ranges of at least
+    // 12 k-blocks: a shorter stream finishes sooner than the extra grid
+    // barrier and the partial sums cost
     const int blocks = P.nt * P.MB_I;
-    const int max_split = P.KB_H / 3 < 1 ? 1 : (P.KB_H / 3 > kDtMaxSplit ? kDtMaxSplit : P.KB_H / 3);
+    const int max_split = P.KB_H / 12 < 1 ? 1 : (P.KB_H / 12 > kDtMaxSplit ? kDtMaxSplit : P.KB_H / 12);
     int s_up = (G + blocks - 1) / blocks;
     s_up = s_up < 1 ? 1 : (s_up > max_split ? max_split : s_up);
     P.s_up = s_up;
@@ -252,18 +280,21 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
   }
   P.per_mb = P.nt * P.KB_I;
   P.F = P.MB_H * P.per_mb;
-  const int r0 = dt_range_start(cta, P.F, G), r1 = dt_range_start(cta + 1, P.F, G);
+  // the down tiles go to the first Gd CTAs, at least three per CTA
+  const int Gd = (P.F + 2) / 3 < G ? (P.F + 2) / 3 : G;
+  const int r0 = cta < Gd ? dt_range_start(cta, P.F, Gd) : P.F;
+  const int r1 = cta < Gd ? dt_range_start(cta + 1, P.F, Gd) : P.F;
   const int my_down = r1 - r0;
   const int n_pre = my_down < S ? my_down : S;     // Wd tiles requested before the barrier
   int pre_it0 = 0;                                 // producer: stage use of the first of them
   // contributors of every output m-block, for the final reduction
-  for (int c = tid; c < G; c += kDtThreads) {
-    const int s0 = dt_range_start(c, P.F, G);
-    s_first_mb[c] = dt_range_start(c + 1, P.F, G) > s0 ? s0 / P.per_mb : -1;
+  for (int c = tid; c < Gd; c += kDtThreads) {
+    const int s0 = dt_range_start(c, P.F, Gd);
+    s_first_mb[c] = dt_range_start(c + 1, P.F, Gd) > s0 ? s0 / P.per_mb : -1;
   }
   for (int mb = tid; mb < P.MB_H; mb += kDtThreads) {
-    s_c0[mb] = dt_cta_of(mb * P.per_mb, P.F, G);
-    s_c1[mb] = dt_cta_of(mb * P.per_mb + P.per_mb - 1, P.F, G);
+    s_c0[mb] = dt_cta_of(mb * P.per_mb, P.F, Gd);
+    s_c1[mb] = dt_cta_of(mb * P.per_mb + P.per_mb - 1, P.F, Gd);
   }
 
   // unit u -> (touched index, m-block, k-block range)
@@ -346,30 +377,51 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
         int ti, mb, kb0, kb1;
         unit_of(u, ti, mb, kb0, kb1);
         const int acc = local & 1;
-        if (!warp_wait(&tfull[acc], (local >> 1) & 1, nullptr, hdr, 45)) { ok = false; break; }
+        // all epilogue warps leave together (they meet at named barriers below)
+        if (!epi_sync_and(warp_wait(&tfull[acc], (local >> 1) & 1, nullptr, hdr, 45))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t tg = tmem + lane_base + kDtColGU + acc * 2 * Np;
-        const int i = mb * 128 + rl;
-        for (int c0 = cbeg; c0 < cend; c0 += 8) {
-          uint32_t gr[8], ur[8];
-          tmem_ld_32x32b_x8(tg + c0, gr);
-          tmem_ld_32x32b_x8(tg + Np + c0, ur);
-          tmem_ld_wait();
-          if (P.s_up == 1) {
-            if (i < I) {
+        // compact loops: this code runs once per launch and unit, so its
+        // size (instruction fetch) matters more than its unrolling
+        if (P.s_up == 1) {
+          // h through a shared tile [part][t][row] and two TMA stores (rows
+          // past I are clipped by the store)
+          if (tid == kDtEpiLeader) bulk_wait_read();   // the previous unit's stores read it
+          epi_sync();
+#pragma unroll 1
+          for (int c0 = cbeg; c0 < cend; c0 += 8) {
+            uint32_t gr[8], ur[8];
+            tmem_ld_32x32b_x8(tg + c0, gr);
+            tmem_ld_32x32b_x8(tg + Np + c0, ur);
+            tmem_ld_wait();
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const int t = c0 + j;
-                const float v = swiglu_fast(__uint_as_float(gr[j]), __uint_as_float(ur[j])) *
-                                alpha[ti * Np + t];
-                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-                const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-                A.hp[(static_cast<size_t>(ti * 2) * Np + t) * I + i] = hi;
-                A.hp[(static_cast<size_t>(ti * 2 + 1) * Np + t) * I + i] = lo;
-              }
+            for (int j = 0; j < 8; ++j) {
+              const int t = c0 + j;
+              const float v = swiglu_fast(__uint_as_float(gr[j]), __uint_as_float(ur[j])) *
+                              alpha[ti * Np + t];
+              const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+              hstage[t * 128 + rl] = hi;
+              hstage[(Np + t) * 128 + rl] = __float2bfloat16_rn(v - __bfloat162float(hi));
             }
-          } else {
-            float* pg = A.pgu + static_cast<size_t>(u) * 2 * Np * 128;
+          }
+          fence_proxy_async_smem();
+          epi_sync();
+          if (tid == kDtEpiLeader) {
+            tma_store_2d(&M.hps, hstage, mb * 128, (ti * 2) * Np);
+            tma_store_2d(&M.hps, hstage + Np * 128, mb * 128, (ti * 2 + 1) * Np);
+            bulk_commit();
+          }
+        } else {
+          float* pg = A.pgu + static_cast<size_t>(u) * 2 * Np * 128;
+#pragma unroll 1
+          for (int c0 = cbeg; c0 < cend; c0 += 8) {
+            uint32_t gr[8], ur[8];
+            tmem_ld_32x32b_x8(tg + c0, gr);
+            tmem_ld_32x32b_x8(tg + Np + c0, ur);
+            tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               pg[static_cast<size_t>(c0 + j) * 128 + rl] = __uint_as_float(gr[j]);
@@ -381,6 +433,7 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
       }
+      if (tid == kDtEpiLeader) bulk_wait_all();   // h has reached global memory
     }
     ok = __syncthreads_and(ok);
   }
@@ -498,6 +551,7 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
         if (!warp_wait(&dfull, seg & 1, nullptr, hdr, 49)) { ok = false; break; }
         tc_fence_after();
         float* pdst = A.pd + (static_cast<size_t>(cta) * kDtMaxSeg + seg) * Np * 128;
+#pragma unroll 1
         for (int c0 = cbeg; c0 < cend; c0 += 8) {
           uint32_t r[8];
           tmem_ld_32x32b_x8(tmem + lane_base + kDtColD + c0, r);
@@ -563,7 +617,7 @@ namespace {
 
 struct DtLayout {
   int Np, Epad, nt_max, stages;
-  size_t stage, alpha_off, smem;        // shared memory
+  size_t stage, alpha_off, hstage_off, smem;   // shared memory
   size_t hp, pgu, pd, total;            // workspace (after the header)
 };
 
@@ -579,15 +633,25 @@ bool dt_layout(int T, int H, int I, int E, int k, DtLayout& L) {
   // x and Wr tiles (router), or a Wd tile and the two Hp tiles (down)
   L.stage = round_up(2 * static_cast<size_t>(kDtTileA) + static_cast<size_t>(L.Np) * 128, 1024);
   const size_t alpha = round_up(static_cast<size_t>(L.nt_max) * L.Np * 4, 1024);
-  if (kDtSmemBudget < 1024 + alpha + 2 * L.stage) return false;
-  L.stages = static_cast<int>((kDtSmemBudget - 1024 - alpha) / L.stage);
+  const size_t hstage = static_cast<size_t>(2) * L.Np * 128 * 2;
+  if (kDtSmemBudget < 1024 + alpha + hstage + 2 * L.stage) return false;
+  L.stages = static_cast<int>((kDtSmemBudget - 1024 - alpha - hstage) / L.stage);
   if (L.stages > kDtMaxStages) L.stages = kDtMaxStages;
   L.alpha_off = static_cast<size_t>(L.stages) * L.stage;
-  L.smem = L.alpha_off + alpha + 1024;               // 1 KiB: alignment slack
+  L.hstage_off = L.alpha_off + alpha;
+  L.smem = L.hstage_off + hstage + 1024;             // 1 KiB: alignment slack
   const int G = kDtMaxCtas;
   const int blocks = L.nt_max * ((I + 127) / 128);
   const int units = blocks + G;                      // blocks * ceil(G / blocks) < blocks + G
   if (H / 128 > G || H / 128 > kDtMaxMB) return false;
+  {
+    // MoE router: all x tiles, then all Wr tiles, in the ring region; the A
+    // read of the last x tile spans 128 rows
+    const size_t xt = static_cast<size_t>(L.Np) * 128, wt = static_cast<size_t>(L.Epad) * 128;
+    const size_t kbh = static_cast<size_t>(H / 64);
+    const size_t need = std::max(kbh * (xt + wt), (kbh - 1) * xt + kDtTileA);
+    if (E > 1 && need > static_cast<size_t>(L.stages) * L.stage) return false;
+  }
   {
     const long long F = static_cast<long long>(H / 128) * L.nt_max * (I / 64);
     if ((F + 1) * G >= (1ll << 31)) return false;    // down-range arithmetic in 32 bits
@@ -610,6 +674,9 @@ cudaError_t decode_tc_impl(const DtLayout& L, const void* x, const void* Wr,
   if (!make_map_16(&m.x, x, H, T, L.Np, false)) return cudaErrorInvalidValue;
   if (A.moe && !make_map_16(&m.wr, Wr, H, A.E, L.Epad, false)) return cudaErrorInvalidValue;
   if (!make_map_16(&m.hp, A.hp, I, static_cast<uint64_t>(L.nt_max) * 2 * L.Np, L.Np, false))
+    return cudaErrorInvalidValue;
+  if (!make_map_16(&m.hps, A.hp, I, static_cast<uint64_t>(L.nt_max) * 2 * L.Np, L.Np, false, 128,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   for (int e = 0; e < nw; ++e) {
     if (!make_map_16(&m.wg[e], Wg[e], H, I, 128, false)) return cudaErrorInvalidValue;
@@ -667,6 +734,7 @@ cudaError_t launch_decode_tc(const void* x, const void* Wr, const float* bias,
   A.stages = L.stages;
   A.Epad = L.Epad;
   A.stage_bytes = static_cast<uint32_t>(L.stage);
+  A.hstage_off = static_cast<uint32_t>(L.hstage_off);
   A.alpha_off = static_cast<uint32_t>(L.alpha_off);
   if (A.E <= 8) return decode_tc_impl<8>(L, x, Wr, Wg, Wu, Wd, A, st);
   return decode_tc_impl<MM_MAX_EXPERTS>(L, x, Wr, Wg, Wu, Wd, A, st);
