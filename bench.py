@@ -34,7 +34,15 @@ from swiglu_mlp_top_gb300.inputs import WORKLOADS, make_workload_inputs  # noqa:
 DEFAULT_WORKLOAD = "moe_e8k2_t16384_skew"
 METRIC = "MoE/FFN forward tokens/s and TFLOP/s on 1 GB300; % of bf16 tensor or HBM roofline"
 L2_BYTES = 129 * 1024 * 1024
-DECODE_MAX_T = 16         # token counts the library streams weights for
+DECODE_MAX_T = 64         # token counts the library streams weights for (bf16)
+
+
+def decode_kernel_name(w):
+    """The streaming kernel the automatic path picks for this workload: CUDA
+    cores up to 8 tokens (dense) or 2 tokens (MoE), tensor cores beyond."""
+    simt = w.T <= (8 if w.kind == "dense" else 2)
+    return ("decode_ffn_kernel (CUDA-core weight streaming)" if simt
+            else "decode_tc_kernel (tcgen05 weight streaming)")
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
 # gate/up GEMM, from an ncu capture of the current kernel on this workload;
@@ -275,7 +283,8 @@ def run_our_arm(args, w):
 
     use_graph = args.graph == "on" or (args.graph == "auto" and w.T <= 64)
     # ---- timed region: K steps, device events on the launching stream
-    dominant = L.MM_KERNEL_GATEUP
+    dominant = (L.MM_KERNEL_DECODE if (w.T <= DECODE_MAX_T and w.dtype == "bf16")
+                else L.MM_KERNEL_GATEUP)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     if use_graph:
@@ -330,13 +339,13 @@ def run_our_arm(args, w):
     peaks, peak_src = measured_peaks()
     k_ms = tot.value / max(1, nl.value)
     if w.T <= DECODE_MAX_T and w.dtype == "bf16":
-        # weight streaming (gate/up + down kernels, timed together): HBM-bound;
-        # algorithmic bytes = the weights of the experts some token selected
+        # weight streaming (one kernel per step): HBM-bound; algorithmic bytes =
+        # the weights of the experts some token selected, x read and y written
         touched = 1 if w.kind == "dense" else int(torch.unique(step.idx).numel())
         wbytes = touched * 3.0 * w.H * w.I * 2 + 2.0 * w.T * w.H * 2
         achieved = wbytes / (k_ms / 1e3) / 1e9
-        roof = {"kernel": "decode_gateup_kernel + decode_down_kernel (weight streaming"
-                          + (", CUDA-graph replay of the whole step)" if use_graph else ")"),
+        roof = {"kernel": decode_kernel_name(w)
+                          + (", CUDA-graph replay of the whole step" if use_graph else ""),
                 "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": None,
                 "peak_source": f"{peak_src} HBM copy bandwidth (MEASURED_PEAKS.json)",

@@ -136,13 +136,16 @@ size_t moe_ws_bytes(int64_t T, int H, int I, int E, int k, int dtype) {
 }
 
 // AUTO: fp32 -> CUDA-core kernels.  bf16 -> weight streaming for decode-sized
-// T (every weight row read once): on the CUDA cores up to kStreamSimtAutoT
-// tokens, on the tensor cores up to kDecodeTcMaxT; tensor-core GEMMs beyond.
-constexpr int64_t kStreamSimtAutoT = 4;
+// T (every weight row read once): on the CUDA cores for the smallest T (up to
+// 8 tokens dense, 2 tokens MoE: their cost grows with the tokens and the
+// touched experts), on the tensor cores up to kDecodeTcMaxT (a fixed cost of
+// two grid barriers and the partial sums); tensor-core GEMMs beyond.
+inline int64_t stream_simt_auto_max_t(int E) { return E == 1 ? 8 : 2; }
 int resolve_path(int path, int dtype, int64_t T, int H, int I, int E, int k) {
   if (path != MM_PATH_AUTO) return path;
   if (dtype == kDtypeF32) return MM_PATH_SIMT;
-  if (T <= kStreamSimtAutoT && stream_simt_bytes(T, H, I, E, k, dtype) > 0) return MM_PATH_STREAM;
+  if (T <= stream_simt_auto_max_t(E) && stream_simt_bytes(T, H, I, E, k, dtype) > 0)
+    return MM_PATH_STREAM;
   if (stream_tc_bytes(T, H, I, E, k, dtype) > 0) return MM_PATH_STREAM_TC;
   if (stream_simt_bytes(T, H, I, E, k, dtype) > 0) return MM_PATH_STREAM;
   return MM_PATH_TENSOR;
