@@ -142,8 +142,9 @@ int mm_swiglu_ffn_noalloc(const void* x, const void* Wg, const void* Wu, const v
  *   S = TopK(p, k): descending p, equal p -> lower expert index first
  *   alpha_e = p_e / (sum_{j in S} p_j + 1e-20)
  *   y = sum_{e in S} alpha_e · SwiGLU_e(x)   — the k terms are added in fp32
- *       in slot order and rounded once to y's dtype (deterministic; the
- *       pages' index_add_ into y rounds every term, which costs accuracy)
+ *       and rounded once to y's dtype, in a fixed order per path (results are
+ *       deterministic; the pages' index_add_ into y rounds every term, which
+ *       costs accuracy)
  *   count_e = #{(t,s): S_t[s] = e},  P_e = sum_t p_{t,e}
  *   aux_loss = E · coef · sum_e (count_e / T) · (P_e / T)
  *
