@@ -48,6 +48,9 @@ def decode_kernel_name(w):
 # gate/up GEMM, from an ncu capture of the current kernel on this workload;
 # None where no capture of the current kernel exists.
 GATEUP_TRAFFIC_BYTES = {"moe_e8k2_t16384_skew": 162.850816e6 + 128.985088e6}
+# The same for the decode kernel that streams the weights (one launch per step).
+DECODE_TRAFFIC_BYTES = {"decode_moe_e8k2_t64": 89.886976e6 + 3.358208e6,
+                        "decode_dense_t1": 11.30624e6}
 
 
 def algorithmic_flops(w, T=None) -> float:
@@ -347,7 +350,7 @@ def run_our_arm(args, w):
         roof = {"kernel": decode_kernel_name(w)
                           + (", CUDA-graph replay of the whole step" if use_graph else ""),
                 "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "frac": achieved / peaks["hbm_gbs"], "traffic": DECODE_TRAFFIC_BYTES.get(w.name),
                 "peak_source": f"{peak_src} HBM copy bandwidth (MEASURED_PEAKS.json)",
                 "kernel_ms": k_ms, "launches_timed": nl.value, "bytes_per_launch": wbytes,
                 "experts_touched": touched}
