@@ -29,7 +29,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 // ----------------------------------------------------------------- layouts
 struct MoeLayout {
-  size_t offsets, counts, blk_cnt, blk_base, blk_prob, perm, xp, h, acc32, wd16, total;
+  size_t offsets, counts, blk_cnt, blk_prob, perm, xp, h, acc32, wd16, total;
 };
 
 // h is stored in fp16 for bf16 inputs (see gemm_tc.cu) and in fp32 for fp32.
@@ -49,7 +49,6 @@ MoeLayout moe_layout(int64_t T, int H, int I, int E, int k, int dtype) {
   L.offsets = off;  off += align_up(4 * (G + 1));
   L.counts = off;   off += align_up(4 * static_cast<size_t>(E));
   L.blk_cnt = off;  off += align_up(4 * nblk * G);
-  L.blk_base = off; off += align_up(4 * nblk * G);
   L.blk_prob = off; off += align_up(4 * nblk * E);
   L.perm = off;     off += align_up(4 * rows);
   L.xp = off;       off += align_up(es * rows * H);
@@ -372,7 +371,6 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
   int32_t* offsets = reinterpret_cast<int32_t*>(ws_at(workspace, L.offsets));
   int32_t* counts = reinterpret_cast<int32_t*>(ws_at(workspace, L.counts));
   int32_t* blk_cnt = reinterpret_cast<int32_t*>(ws_at(workspace, L.blk_cnt));
-  int32_t* blk_base = reinterpret_cast<int32_t*>(ws_at(workspace, L.blk_base));
   float* blk_prob = reinterpret_cast<float*>(ws_at(workspace, L.blk_prob));
   int32_t* perm = reinterpret_cast<int32_t*>(ws_at(workspace, L.perm));
   void* xp = ws_at(workspace, L.xp);
@@ -380,31 +378,25 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
   float* acc32 = (dtype == kDtypeF32) ? static_cast<float*>(y)
                                       : reinterpret_cast<float*>(ws_at(workspace, L.acc32));
 
+  // router + scan, with the fp16 copy of Wd made by extra blocks of the same
+  // grid (tensor path)
+  const int64_t rows = T * k;
+  const void* wd16p[MM_MAX_EXPERTS];
+  char* wd16 = ws_at(workspace, L.wd16);
+  if (p == MM_PATH_TENSOR)
+    for (int q = 0; q < E; ++q) wd16p[q] = wd16 + static_cast<size_t>(q) * H * I * 2;
+  const RouteOut ro{nullptr, nullptr, nullptr, nullptr, coef, 0};
   cudaError_t e = counted_launch(MM_KERNEL_ROUTER, st, [&] {
-    return launch_router(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w, blk_cnt,
-                         blk_prob, st);
+    return launch_router(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w, blk_cnt, blk_prob,
+                         ro, p == MM_PATH_TENSOR ? Wd : nullptr, I, wd16, hdr, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "router");
-  e = counted_launch(MM_KERNEL_SCAN, st, [&] {
-    return launch_route_scan(E, k, T, coef, blk_cnt, blk_prob, blk_base, offsets, counts,
-                             aux_loss, st);
-  });
-  if (e != cudaSuccess) return cuda_fail(e, "route_scan");
+  const DispatchOut dout{offsets, counts, aux_loss, coef, hdr};
   e = counted_launch(MM_KERNEL_DISPATCH, st, [&] {
-    return launch_dispatch(dtype, x, T, H, E, k, topk_idx, blk_base, offsets, perm, xp, st);
+    return launch_dispatch(dtype, x, T, H, E, k, topk_idx, blk_cnt, blk_prob, dout, perm, xp, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "dispatch");
 
-  const int64_t rows = T * k;
-  const void* wd16p[MM_MAX_EXPERTS];
-  if (p == MM_PATH_TENSOR) {
-    char* wd16 = ws_at(workspace, L.wd16);
-    for (int q = 0; q < E; ++q) wd16p[q] = wd16 + static_cast<size_t>(q) * H * I * 2;
-    e = counted_launch(MM_KERNEL_WCONVERT, st, [&] {
-      return launch_convert_bf16_to_f16(Wd, E, static_cast<int64_t>(H) * I, wd16, st);
-    });
-    if (e != cudaSuccess) return cuda_fail(e, "wd convert");
-  }
   // gate/up over all k*E (slot, expert) groups at once
   GroupRows gu{offsets, k * E, 0, E};
   if (p == MM_PATH_TENSOR)
@@ -462,16 +454,13 @@ int mm_moe_route(const void* x, const void* Wr, int64_t T, int H, int E, int k, 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int32_t* blk_cnt = reinterpret_cast<int32_t*>(ws_at(workspace, L.blk_cnt));
   float* blk_prob = reinterpret_cast<float*>(ws_at(workspace, L.blk_prob));
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
+  const RouteOut ro{nullptr, nullptr, expert_counts, aux_loss, coef, 1};
   cudaError_t e = counted_launch(MM_KERNEL_ROUTER, st, [&] {
-    return launch_router(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w, blk_cnt,
-                         blk_prob, st);
+    return launch_router(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w, blk_cnt, blk_prob,
+                         ro, nullptr, 0, nullptr, hdr, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "router");
-  e = counted_launch(MM_KERNEL_SCAN, st, [&] {
-    return launch_route_scan(E, k, T, coef, blk_cnt, blk_prob, nullptr, nullptr, expert_counts,
-                             aux_loss, st);
-  });
-  if (e != cudaSuccess) return cuda_fail(e, "route_scan");
   return MM_OK;
 }
 

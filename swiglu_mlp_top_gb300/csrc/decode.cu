@@ -58,22 +58,6 @@ struct DecodeArgs {
 };
 
 
-typedef unsigned long long u64;
-
-// d = a * b + c on two fp32 lanes packed in 64 bits (low word = lane 0).
-__device__ __forceinline__ u64 ffma2(u64 a, u64 b, u64 c) {
-  u64 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-// Two bf16 (one 32-bit word, element 0 in the low half) widened to fp32.
-__device__ __forceinline__ u64 bf2(uint32_t w) {
-  return (static_cast<u64>(w & 0xffff0000u) << 32) | static_cast<u64>(w << 16);
-}
-__device__ __forceinline__ float hsum2(u64 v) {
-  return __uint_as_float(static_cast<uint32_t>(v)) + __uint_as_float(static_cast<uint32_t>(v >> 32));
-}
-
 // Sum of NV per-lane values over the warp, scattered: lane L ends with the
 // full sum of value L / (32 / NV).  Each exchange step hands half of the
 // remaining values to the partner lane, so the warp moves NV - 1 + (5 -

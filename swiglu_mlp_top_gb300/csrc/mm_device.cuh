@@ -16,7 +16,8 @@ struct WsHeader {
   unsigned int where;         // role id of the first wait that gave up
   unsigned int bar_count;     // grid barrier: CTAs arrived (0 between launches)
   unsigned int bar_leave;     // grid barrier: CTAs released (0 between launches)
-  unsigned int pad[60];
+  unsigned int route_done;    // router blocks finished (0 between launches)
+  unsigned int pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
@@ -145,6 +146,23 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
                                           WsHeader* hdr, unsigned where) {
   const bool ok = mbar_wait(bar, parity, abort, hdr, where);
   return __all_sync(0xffffffffu, ok);
+}
+
+// ---------------------------------------------------------------- packed fp32
+typedef unsigned long long u64;
+
+// d = a * b + c on two fp32 lanes packed in 64 bits (low word = lane 0).
+__device__ __forceinline__ u64 ffma2(u64 a, u64 b, u64 c) {
+  u64 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// Two bf16 (one 32-bit word, element 0 in the low half) widened to fp32.
+__device__ __forceinline__ u64 bf2(uint32_t w) {
+  return (static_cast<u64>(w & 0xffff0000u) << 32) | static_cast<u64>(w << 16);
+}
+__device__ __forceinline__ float hsum2(u64 v) {
+  return __uint_as_float(static_cast<uint32_t>(v)) + __uint_as_float(static_cast<uint32_t>(v >> 32));
 }
 
 // ---------------------------------------------------------------- TMA

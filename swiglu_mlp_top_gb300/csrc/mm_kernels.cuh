@@ -59,16 +59,52 @@ struct DownEpilogue {
   int mode;                 // CombineMode
 };
 
+// Router grid (routing.cu): per 64-token block logits, softmax, top-k, alpha
+// and partial counts / probability sums; the block that finishes last runs
+// the scan (group offsets, per-block bases, counts, aux loss; the counter
+// lives in the workspace header).  With wd_src set, num_sms() further blocks
+// copy the E down matrices [H, I] to fp16 at wd16 meanwhile.
+struct RouteOut {
+  int32_t* blk_base;     // [nblk, k*E] or null
+  int32_t* offsets;      // [k*E + 1] or null
+  int32_t* counts;       // [E] or null
+  float* aux_loss;       // scalar or null
+  float coef;
+  int do_scan;           // 0: the dispatch kernel derives bases, offsets, counts, aux
+};
+struct RouteExtras {
+  int32_t* blk_base;
+  int32_t* offsets;
+  int32_t* counts;
+  float* aux_loss;
+  float coef;
+  WsHeader* hdr;
+  PtrArray conv_src;     // Wd per expert (bf16)
+  __half* conv_dst;      // [E, H, I] fp16
+  int64_t conv_per;      // H * I
+  int conv_n;            // E, or 0: no conversion
+  int n_conv;            // conversion blocks (the grid's first)
+  int stage_x;           // x rows staged in shared memory at byte x_off
+  uint32_t x_off;
+  int do_scan;
+};
 cudaError_t launch_router(int dtype, const void* x, const void* Wr, const float* bias, int64_t T,
                           int H, int E, int k, int32_t* topk_idx, float* topk_w, int32_t* blk_cnt,
-                          float* blk_prob, cudaStream_t st);
+                          float* blk_prob, const RouteOut& out, const void* const* wd_src, int I,
+                          void* wd16, WsHeader* hdr, cudaStream_t st);
 size_t router_smem_bytes(int H, int E, int k);
-cudaError_t launch_route_scan(int E, int k, int64_t T, float coef, const int32_t* blk_cnt,
-                              const float* blk_prob, int32_t* blk_base, int32_t* offsets,
-                              int32_t* counts, float* aux_loss, cudaStream_t st);
+// Dispatch (routing.cu): group bases, offsets, expert counts and the aux
+// loss from the router's per-block partials, then the token permute.
+struct DispatchOut {
+  int32_t* offsets;      // [k*E + 1]
+  int32_t* counts;       // [E] or null
+  float* aux_loss;
+  float coef;
+  WsHeader* hdr;
+};
 cudaError_t launch_dispatch(int dtype, const void* x, int64_t T, int H, int E, int k,
-                            const int32_t* topk_idx, const int32_t* blk_base,
-                            const int32_t* offsets, int32_t* perm, void* Xp, cudaStream_t st);
+                            const int32_t* topk_idx, const int32_t* blk_cnt, const float* blk_prob,
+                            const DispatchOut& D, int32_t* perm, void* Xp, cudaStream_t st);
 
 // Tensor-core grouped GEMMs.  A is [rows, K] row-major; each group multiplies
 // its rows by its own weight matrices.  gate/up: bf16 A and weights, fp16 h

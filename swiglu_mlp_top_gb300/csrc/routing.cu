@@ -38,6 +38,21 @@ __device__ __forceinline__ void load_vec8<float>(const float* p, float (&v)[8]) 
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
+// 8 consecutive elements as four packed fp32 pairs (element 2i in the low word).
+template <typename Tin>
+__device__ __forceinline__ void load_pairs8(const Tin* p, u64 (&q)[4]);
+template <>
+__device__ __forceinline__ void load_pairs8<__nv_bfloat16>(const __nv_bfloat16* p, u64 (&q)[4]) {
+  const uint4 raw = *reinterpret_cast<const uint4*>(p);
+  q[0] = bf2(raw.x); q[1] = bf2(raw.y); q[2] = bf2(raw.z); q[3] = bf2(raw.w);
+}
+template <>
+__device__ __forceinline__ void load_pairs8<float>(const float* p, u64 (&q)[4]) {
+  const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(p);
+  const ulonglong2 b = *reinterpret_cast<const ulonglong2*>(p + 4);
+  q[0] = a.x; q[1] = a.y; q[2] = b.x; q[3] = b.y;
+}
+
 template <typename T>
 __device__ __forceinline__ float to_f32(T v);
 template <>
@@ -60,12 +75,17 @@ __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return
 // how many of its tokens chose e in slot s (blk_cnt[b][g]), and sum_t p_{t,e}
 // over its tokens (blk_prob[b][e]); every sum runs in a fixed order.
 // ---------------------------------------------------------------------------
+__device__ void scan_block(int E, int k, int nblk, int64_t T, const RouteExtras& X,
+                           const int32_t* __restrict__ blk_cnt, const float* __restrict__ blk_prob);
+__device__ void convert_role(const RouteExtras& X, int blk, int nblk_conv);
+
 template <typename Tin, int EP>
 __global__ void __launch_bounds__(kRouteThreads)
 router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float* __restrict__ bias,
               int64_t T, int H, int E, int k, int32_t* __restrict__ topk_idx,
               float* __restrict__ topk_w, int32_t* __restrict__ blk_cnt,
-              float* __restrict__ blk_prob) {
+              float* __restrict__ blk_prob, const RouteExtras X) {
+
   constexpr int R = (EP > 32) ? EP / 32 : 1;      // values per lane after the reduction
   constexpr int NV = 32 * R;                       // partial sums per lane
   constexpr int TPW = NV / EP;                     // tokens per pass
@@ -74,24 +94,53 @@ router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float
   constexpr int kPerWarp = kRouteTokensPerBlock / kWarps;
   static_assert(kPerWarp % TPW == 0, "passes cover a warp's tokens");
 
+  // the grid's first X.n_conv blocks copy Wd to fp16, the rest route
+  if (static_cast<int>(blockIdx.x) < X.n_conv) {
+    convert_role(X, blockIdx.x, X.n_conv);
+    return;
+  }
+  const int rblk = blockIdx.x - X.n_conv;          // router block: tokens [64 rblk, +64)
+  const int nblk = static_cast<int>((T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock);
+
   extern __shared__ float4 route_smem4[];
   const int nch = H / 8;                           // 8-element chunks per row
-  float4* w_lo = route_smem4;                      // [E][nch] elements 0..3 of each chunk
-  float4* w_hi = route_smem4 + E * nch;            // [E][nch] elements 4..7
-  int* s_gcnt = reinterpret_cast<int*>(route_smem4 + 2 * E * nch);   // [k*E]
+  // Wr [E][H] as stored, then the group counters; x rows at X.x_off
+  Tin* wsm = reinterpret_cast<Tin*>(route_smem4);
+  int* s_gcnt = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(route_smem4) +
+                                       static_cast<size_t>(E) * H * sizeof(Tin));   // [k*E]
   __shared__ float red_p[kWarps][EP];
+  __shared__ __align__(8) uint64_t xbar;
+  __shared__ int s_last;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = k * E;
-  for (int i = tid; i < E * nch; i += blockDim.x) {
-    const int e = i / nch, c = i - e * nch;
-    float v[8];
-    load_vec8(Wr + static_cast<int64_t>(e) * H + c * 8, v);
-    w_lo[i] = make_float4(v[0], v[1], v[2], v[3]);
-    w_hi[i] = make_float4(v[4], v[5], v[6], v[7]);
+  // Wr and (when X.stage_x) this block's x rows come into shared memory by
+  // bulk copies
+  const int64_t t0 = static_cast<int64_t>(rblk) * kRouteTokensPerBlock;
+  const int ntok = static_cast<int>(T - t0 < kRouteTokensPerBlock ? T - t0 : kRouteTokensPerBlock);
+  const Tin* xsrc = x + t0 * H;                    // row t of the block at xsrc + t * H
+  Tin* xs = reinterpret_cast<Tin*>(reinterpret_cast<unsigned char*>(route_smem4) + X.x_off);
+  if (tid == 0) {
+    mbar_init(&xbar, 1);
+    fence_mbar_init();
+    const uint32_t wbytes = static_cast<uint32_t>(E) * H * sizeof(Tin);
+    const uint32_t xbytes = X.stage_x ? static_cast<uint32_t>(ntok) * H * sizeof(Tin) : 0u;
+    mbar_arrive_expect_tx(&xbar, wbytes + xbytes);
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(wsm)), "l"(Wr), "r"(wbytes), "r"(smem_u32(&xbar))
+        : "memory");
+    if (xbytes)
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+          ::"r"(smem_u32(xs)), "l"(xsrc), "r"(xbytes), "r"(smem_u32(&xbar))
+          : "memory");
   }
+  if (X.stage_x) xsrc = xs;
+
   for (int i = tid; i < G; i += blockDim.x) s_gcnt[i] = 0;
   __syncthreads();
+  if (!__syncthreads_and(mbar_wait(&xbar, 0, nullptr, X.hdr, 60))) return;
 
   // (token, expert) pairs this lane owns after the reduction
   int e_of[R];
@@ -107,39 +156,40 @@ router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float
   for (int j = 0; j < R; ++j) psum[j] = 0.f;
 
   for (int pass = 0; pass < kPerWarp / TPW; ++pass) {
-    const int64_t tbase = static_cast<int64_t>(blockIdx.x) * kRouteTokensPerBlock +
-                          warp * kPerWarp + pass * TPW;
+    const int lbase = warp * kPerWarp + pass * TPW;      // token within the block
+    const int64_t tbase = t0 + lbase;
     if (tbase >= T) break;   // uniform across the warp
-    float v[NV];
+    // packed fp32 partial sums (even / odd elements), folded before the reduction
+    u64 acc[NV];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) v[i] = 0.f;
+    for (int i = 0; i < NV; ++i) acc[i] = 0ull;
     for (int c = lane; c < nch; c += 32) {
-      float xv[TPW][8];
+      u64 xv[TPW][4];
 #pragma unroll
       for (int t = 0; t < TPW; ++t) {
         if (tbase + t < T) {
-          load_vec8(x + (tbase + t) * H + c * 8, xv[t]);
+          load_pairs8(xsrc + static_cast<int64_t>(lbase + t) * H + c * 8, xv[t]);
         } else {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) xv[t][i] = 0.f;
+          for (int i = 0; i < 4; ++i) xv[t][i] = 0ull;
         }
       }
 #pragma unroll
       for (int e = 0; e < EP; ++e) {
         if (e < E) {
-          const float4 a = w_lo[e * nch + c], b = w_hi[e * nch + c];
+          u64 wv[4];
+          load_pairs8(wsm + static_cast<int64_t>(e) * H + c * 8, wv);
 #pragma unroll
           for (int t = 0; t < TPW; ++t) {
-            float s = v[t * EP + e];
-            s = fmaf(xv[t][0], a.x, s); s = fmaf(xv[t][1], a.y, s);
-            s = fmaf(xv[t][2], a.z, s); s = fmaf(xv[t][3], a.w, s);
-            s = fmaf(xv[t][4], b.x, s); s = fmaf(xv[t][5], b.y, s);
-            s = fmaf(xv[t][6], b.z, s); s = fmaf(xv[t][7], b.w, s);
-            v[t * EP + e] = s;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[t * EP + e] = ffma2(xv[t][q], wv[q], acc[t * EP + e]);
           }
         }
       }
     }
+    float v[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = hsum2(acc[i]);
     // butterfly reduce-scatter: after the round with offset o a lane keeps the
     // half of its values whose index bit o matches its own lane bit; at the
     // end lane L holds the full sums of pairs L + 32 j
@@ -249,53 +299,81 @@ router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float
   if (tid < E) {
     float ps = 0.f;
     for (int w = 0; w < kWarps; ++w) ps += red_p[w][tid];
-    blk_prob[static_cast<int64_t>(blockIdx.x) * E + tid] = ps;
+    blk_prob[static_cast<int64_t>(rblk) * E + tid] = ps;
   }
   for (int g = tid; g < G; g += blockDim.x)
-    blk_cnt[static_cast<int64_t>(blockIdx.x) * G + g] = s_gcnt[g];
+    blk_cnt[static_cast<int64_t>(rblk) * G + g] = s_gcnt[g];
+
+  // route-only calls: the router block that finishes last runs the scan
+  // (partials, fence, count: whoever brings the count to nblk sees every
+  // block's partials); it resets the counter for the next launch.  The MoE
+  // forward leaves this to the dispatch kernel.
+  if (!X.do_scan) return;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(&X.hdr->route_done, 1u) == static_cast<unsigned>(nblk - 1));
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    scan_block(E, k, nblk, T, X, blk_cnt, blk_prob);
+    if (tid == 0) X.hdr->route_done = 0u;
+  }
 }
 
+
 // ---------------------------------------------------------------------------
-// Scan (one block): for every group g = s*E + e
+// Scan, run by the router block that finishes last: for every group
+// g = s*E + e
 //   blk_base[b][g] = sum_{b' < b} blk_cnt[b'][g]    (a lane owns a run of blocks)
 //   tot[g] = sum_b blk_cnt[b][g];  offsets = exclusive scan of tot over g
 // and the aux loss ([L13] §1.6; chapter 4 §4.4):
 //   count_e = sum_s tot[s*E + e];  P_e = sum_b blk_prob[b][e]  (fixed order)
 //   aux = E * coef * sum_e (count_e / T) * (P_e / T)
 // Rows of the dispatched matrix are thus ordered by slot, then expert, then
-// token.  offsets / blk_base may be null (route-only call).
+// token.  offsets / blk_base may be null (route-only call).  The other
+// blocks' partials are read through L2 (ld.global.cg).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kScanThreads)
-route_scan_kernel(int E, int k, int nblk, int64_t T, float coef,
-                  const int32_t* __restrict__ blk_cnt, const float* __restrict__ blk_prob,
-                  int32_t* __restrict__ blk_base, int32_t* __restrict__ offsets,
-                  int32_t* __restrict__ counts, float* __restrict__ aux_loss) {
+__device__ void scan_block(int E, int k, int nblk, int64_t T, const RouteExtras& X,
+                           const int32_t* __restrict__ blk_cnt, const float* __restrict__ blk_prob) {
   __shared__ int s_tot[kMaxGroups];
   __shared__ float s_P[MM_MAX_EXPERTS];
   __shared__ int s_cnt[MM_MAX_EXPERTS];
   const int G = k * E;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int kWarps = kScanThreads / 32;
+  constexpr int kWarps = kRouteThreads / 32;
   const int per = (nblk + 31) / 32;
 
   for (int g = warp; g < G; g += kWarps) {
     const int b0 = lane * per;
     const int b1 = min(nblk, b0 + per);
     int sum = 0;
-#pragma unroll 8
-    for (int b = b0; b < b1; ++b) sum += blk_cnt[static_cast<int64_t>(b) * G + g];
+    for (int b = b0; b < b1; b += 8) {
+      int c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        c[j] = (b + j < b1) ? __ldcg(blk_cnt + static_cast<int64_t>(b + j) * G + g) : 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sum += c[j];
+    }
     int incl = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int n = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += n;
     }
-    if (blk_base != nullptr) {
+    if (X.blk_base != nullptr) {
+      // every count of a run of 8 is requested before the running sum uses it
       int run = incl - sum;
-      for (int b = b0; b < b1; ++b) {
-        const int64_t i = static_cast<int64_t>(b) * G + g;
-        blk_base[i] = run;
-        run += blk_cnt[i];
+      for (int b = b0; b < b1; b += 8) {
+        int c[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          c[j] = (b + j < b1) ? __ldcg(blk_cnt + static_cast<int64_t>(b + j) * G + g) : 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (b + j < b1) X.blk_base[static_cast<int64_t>(b + j) * G + g] = run;
+          run += c[j];
+        }
       }
     }
     const int tot = __shfl_sync(0xffffffffu, incl, 31);
@@ -305,9 +383,8 @@ route_scan_kernel(int E, int k, int nblk, int64_t T, float coef,
     // lane-strided partial sums, then a fixed xor-tree: the order depends only on nblk
     float P = 0.f;
 #pragma unroll 8
-    for (int b = lane; b < nblk; b += 32) P += blk_prob[static_cast<int64_t>(b) * E + e];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) P += __shfl_xor_sync(0xffffffffu, P, o);
+    for (int b = lane; b < nblk; b += 32) P += __ldcg(blk_prob + static_cast<int64_t>(b) * E + e);
+    P = warp_sum(P);
     if (lane == 0) s_P[e] = P;
   }
   __syncthreads();
@@ -315,49 +392,188 @@ route_scan_kernel(int E, int k, int nblk, int64_t T, float coef,
     int c = 0;
     for (int s = 0; s < k; ++s) c += s_tot[s * E + threadIdx.x];
     s_cnt[threadIdx.x] = c;
-    if (counts != nullptr) counts[threadIdx.x] = c;
+    if (X.counts != nullptr) X.counts[threadIdx.x] = c;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    if (offsets != nullptr) {
+    if (X.offsets != nullptr) {
       int run = 0;
       for (int g = 0; g < G; ++g) {
-        offsets[g] = run;
+        X.offsets[g] = run;
         run += s_tot[g];
       }
-      offsets[G] = run;
+      X.offsets[G] = run;
     }
     // E*coef*sum_e (count_e/T)(P_e/T) = (E*coef/T^2) * sum_e count_e * P_e
     float acc = 0.f;
     for (int e = 0; e < E; ++e) acc = fmaf(static_cast<float>(s_cnt[e]), s_P[e], acc);
     const float invT = 1.0f / static_cast<float>(T);
-    if (aux_loss != nullptr) *aux_loss = static_cast<float>(E) * coef * acc * invT * invT;
+    if (X.aux_loss != nullptr) *X.aux_loss = static_cast<float>(E) * X.coef * acc * invT * invT;
+  }
+}
+
+// Copy of the E down-projection matrices from bf16 to fp16 (exact for
+// |w| >= 2^-14; smaller magnitudes become fp16 subnormals, error <= 2^-25),
+// by the router grid's first X.n_conv blocks.  The E matrices form one index
+// space of 16-byte vectors cut into one contiguous range per block (a range
+// meets at most a few matrices, so the matrix index is stepped, not divided);
+// each thread keeps kInFlight vectors in flight.
+__device__ void convert_role(const RouteExtras& X, int blk, int nblk_conv) {
+  constexpr int kInFlight = 8;
+  const int nvec = static_cast<int>(X.conv_per / 8);      // per matrix
+  const int total = nvec * X.conv_n;                      // < 2^31 (checked by the launcher)
+  const int r0 = static_cast<int>(static_cast<long long>(total) * blk / nblk_conv);
+  const int r1 = static_cast<int>(static_cast<long long>(total) * (blk + 1) / nblk_conv);
+  int m = r0 / nvec;                                      // matrix of this thread's next vector
+  int off = r0 - m * nvec + static_cast<int>(threadIdx.x);
+  while (off >= nvec) { off -= nvec; ++m; }
+  uint4* dst = reinterpret_cast<uint4*>(X.conv_dst);
+  for (int v0 = r0 + static_cast<int>(threadIdx.x); v0 < r1; v0 += kInFlight * kRouteThreads) {
+    uint4 raw[kInFlight];
+    int mm_[kInFlight], oo[kInFlight];
+#pragma unroll
+    for (int j = 0; j < kInFlight; ++j) {
+      mm_[j] = m;
+      oo[j] = off;
+      if (v0 + j * kRouteThreads < r1)
+        raw[j] = __ldcs(static_cast<const uint4*>(X.conv_src.p[m]) + off);
+      off += kRouteThreads;
+      while (off >= nvec) { off -= nvec; ++m; }   // more than once only when nvec < 256
+    }
+#pragma unroll
+    for (int j = 0; j < kInFlight; ++j) {
+      if (v0 + j * kRouteThreads < r1) {
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw[j]);
+        uint4 out;
+        uint32_t* o = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = __bfloat1622float2(b[q]);
+          o[q] = pack_f16x2(f.x, f.y);
+        }
+        __stcs(dst + static_cast<int64_t>(mm_[j]) * nvec + oo[j], out);
+      }
+    }
   }
 }
 
 // ---------------------------------------------------------------------------
-// Dispatch: block b owns the same tokens as router block b.  Assignment
-// (t, s) with expert e goes to group g = s*E + e and gets the row
-//   pos = offsets[g] + blk_base[b][g] + rank of t among the block's tokens
-//         that chose e in slot s (token order),
-// so every group's rows are in ascending token order.  perm[pos] = t*k + s,
-// and x[t] is copied to Xp[pos].
+// Dispatch: block b owns the same tokens as router block b.  From the
+// router's per-block counts it derives, for every (slot s, expert e) group
+// g = s*E + e, the rows before its own block (base) and the group totals;
+// block 0 also writes the group offsets, the expert counts and the aux loss
+// ([L13] §1.6; chapter 4 §4.4: aux = E*coef*sum_e (count_e/T)(P_e/T), with
+// P_e = sum_b blk_prob[b][e] in a fixed order).  Assignment (t, s) with
+// expert e gets the row
+//   pos = offset[g] + base[g] + rank of t among the block's tokens that chose
+//         e in slot s (token order),
+// so every group's rows are in ascending token order; perm[pos] = t*k + s and
+// x[t] is copied to Xp[pos] — staged in shared memory by one bulk copy and
+// written back by one bulk copy per row when the block's rows fit.
 // ---------------------------------------------------------------------------
 template <typename Tin>
 __global__ void __launch_bounds__(kRouteThreads)
 dispatch_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, int k,
-                const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ blk_base,
-                const int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
-                Tin* __restrict__ Xp) {
+                const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ blk_cnt,
+                const float* __restrict__ blk_prob, const DispatchOut D,
+                int32_t* __restrict__ perm, Tin* __restrict__ Xp, int stage_x) {
+  extern __shared__ __align__(128) unsigned char disp_smem[];
   __shared__ int s_w0cnt[MM_MAX_EXPERTS];   // per-expert count in warp 0 (tokens 0..31)
-  __shared__ int s_pos[kRouteTokensPerBlock * MM_MAX_EXPERTS];
+  __shared__ int s_pos[kRouteTokensPerBlock * MM_MAX_TOPK];
+  __shared__ int s_base[kMaxGroups], s_tot[kMaxGroups], s_off[kMaxGroups + 1];
+  __shared__ __align__(8) uint64_t xbar;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kWarps = kRouteThreads / 32;
   const int b = blockIdx.x;
+  const int nblk = gridDim.x;
   const int G = k * E;
   const int64_t tok0 = static_cast<int64_t>(b) * kRouteTokensPerBlock;
   const int ntok = static_cast<int>((T - tok0) < kRouteTokensPerBlock ? (T - tok0) : kRouteTokensPerBlock);
   static_assert(kRouteTokensPerBlock == 64, "two ranking warps cover one slot of a block");
+  Tin* xs = reinterpret_cast<Tin*>(disp_smem);
+  const uint32_t rowb = static_cast<uint32_t>(H) * sizeof(Tin);
+
+  if (tid == 0 && stage_x) {
+    mbar_init(&xbar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&xbar, static_cast<uint32_t>(ntok) * rowb);
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(xs)), "l"(x + tok0 * H), "r"(static_cast<uint32_t>(ntok) * rowb),
+        "r"(smem_u32(&xbar))
+        : "memory");
+  }
+
+  // group totals and this block's bases: a warp per group, lanes over runs of
+  // router blocks, every count of a run requested at once
+  const int per = (nblk + 31) / 32;
+  for (int g = warp; g < G; g += kWarps) {
+    const int b0 = lane * per, b1 = min(nblk, b0 + per);
+    int all = 0, before = 0;
+    for (int bb = b0; bb < b1; bb += 8) {
+      int c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) c[j] = (bb + j < b1) ? blk_cnt[static_cast<int64_t>(bb + j) * G + g] : 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        all += c[j];
+        before += (bb + j < b) ? c[j] : 0;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      all += __shfl_xor_sync(0xffffffffu, all, o);
+      before += __shfl_xor_sync(0xffffffffu, before, o);
+    }
+    if (lane == 0) {
+      s_tot[g] = all;
+      s_base[g] = before;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive scan of the group totals: a lane owns a run of groups
+    const int gper = (G + 31) / 32;
+    const int g0 = lane * gper, g1 = min(G, g0 + gper);
+    int sum = 0;
+    for (int g = g0; g < g1; ++g) sum += s_tot[g];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    int run = incl - sum;
+    for (int g = g0; g < g1; ++g) {
+      s_off[g] = run;
+      run += s_tot[g];
+    }
+    if (lane == 31) s_off[G] = incl;
+  }
+  __syncthreads();
+  if (b == 0) {
+    for (int g = tid; g <= G; g += kRouteThreads) D.offsets[g] = s_off[g];
+    for (int e = tid; e < E; e += kRouteThreads) {
+      int c = 0;
+      for (int s = 0; s < k; ++s) c += s_tot[s * E + e];
+      if (D.counts != nullptr) D.counts[e] = c;
+    }
+    if (warp == 0) {
+      // aux: lane-strided partial sums over the router blocks, fixed xor tree
+      float acc = 0.f;
+      for (int e = 0; e < E; ++e) {
+        float P = 0.f;
+        for (int bb = lane; bb < nblk; bb += 32) P += blk_prob[static_cast<int64_t>(bb) * E + e];
+        P = warp_sum(P);
+        int c = 0;
+        for (int s = 0; s < k; ++s) c += s_tot[s * E + e];
+        acc = fmaf(static_cast<float>(c), P, acc);
+      }
+      const float invT = 1.0f / static_cast<float>(T);
+      if (lane == 0) *D.aux_loss = static_cast<float>(E) * D.coef * acc * invT * invT;
+    }
+  }
 
   for (int s = 0; s < k; ++s) {
     for (int i = tid; i < E; i += kRouteThreads) s_w0cnt[i] = 0;
@@ -374,25 +590,33 @@ dispatch_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, int k,
     if (warp < 2 && e >= 0) {
       const int tl = warp * 32 + lane;
       const int g = s * E + e;
-      const int pos = offsets[g] + blk_base[static_cast<int64_t>(b) * G + g] +
-                      (warp == 1 ? s_w0cnt[e] : 0) + rank;
+      const int pos = s_off[g] + s_base[g] + (warp == 1 ? s_w0cnt[e] : 0) + rank;
       perm[pos] = static_cast<int32_t>((tok0 + tl) * k + s);
       s_pos[tl * k + s] = pos;
     }
     __syncthreads();
   }
 
-  // copy rows: a flat loop over (assignment, 16-byte vector) pairs
-  constexpr int kVec = 16 / sizeof(Tin);
-  const int nv = H / kVec;
-  const int total = ntok * k * nv;
-  const uint4* src = reinterpret_cast<const uint4*>(x + tok0 * H);
-  uint4* dst = reinterpret_cast<uint4*>(Xp);
+  const int na = ntok * k;
+  if (stage_x) {
+    // one bulk copy per assignment row, shared -> global
+    if (!__syncthreads_and(mbar_wait(&xbar, 0, nullptr, D.hdr, 61))) return;
+    if (tid < na) {
+      for (int a = tid; a < na; a += kRouteThreads)
+        bulk_store(Xp + static_cast<int64_t>(s_pos[a]) * H, xs + static_cast<int64_t>(a / k) * H, rowb);
+      bulk_commit();
+      bulk_wait_all();
+    }
+  } else {
+    // a warp per row, 16-byte vectors
+    constexpr int kVec = 16 / sizeof(Tin);
+    const int nv = H / kVec;
+    for (int a = warp; a < na; a += kWarps) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (tok0 + a / k) * H);
+      uint4* dst = reinterpret_cast<uint4*>(Xp + static_cast<int64_t>(s_pos[a]) * H);
 #pragma unroll 4
-  for (int i = tid; i < total; i += kRouteThreads) {
-    const int a = i / nv;
-    const int v = i - a * nv;
-    dst[static_cast<int64_t>(s_pos[a]) * nv + v] = src[(a / k) * nv + v];
+      for (int v = lane; v < nv; v += 32) dst[v] = src[v];
+    }
   }
 }
 
@@ -403,20 +627,28 @@ size_t router_smem_bytes(int H, int E, int k) {
   return static_cast<size_t>(E) * H * sizeof(float) + static_cast<size_t>(k) * E * sizeof(int);
 }
 
+// Router grid: X.n_conv conversion blocks (when Wd is given), then one block
+// per 64 tokens.  x is staged in shared memory when the block's rows and Wr
+// fit in 110 KiB together (two blocks per SM).
 template <typename Tin>
 static cudaError_t launch_router_t(const void* x, const void* Wr, const float* bias, int64_t T, int H,
                                    int E, int k, int32_t* topk_idx, float* topk_w, int32_t* blk_cnt,
-                                   float* blk_prob, cudaStream_t st) {
+                                   float* blk_prob, RouteExtras X, cudaStream_t st) {
   const int nblk = static_cast<int>((T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock);
-  const size_t smem = router_smem_bytes(H, E, k);
+  size_t smem = static_cast<size_t>(E) * H * sizeof(Tin) + static_cast<size_t>(k) * E * sizeof(int);
+  X.x_off = static_cast<uint32_t>((smem + 127) & ~size_t(127));
+  const size_t xbytes = static_cast<size_t>(kRouteTokensPerBlock) * H * sizeof(Tin);
+  X.stage_x = X.x_off + xbytes <= 110 * 1024 ? 1 : 0;
+  if (X.stage_x) smem = X.x_off + xbytes;
 #define MM_ROUTER_CASE(EPAD)                                                                   \
   {                                                                                            \
     auto fn = router_kernel<Tin, EPAD>;                                                        \
     cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem);             \
     if (err != cudaSuccess) return err;                                                        \
-    fn<<<nblk, kRouteThreads, smem, st>>>(static_cast<const Tin*>(x),                          \
-                                          static_cast<const Tin*>(Wr), bias, T, H, E, k,        \
-                                          topk_idx, topk_w, blk_cnt, blk_prob);                \
+    fn<<<X.n_conv + nblk, kRouteThreads, smem, st>>>(static_cast<const Tin*>(x),               \
+                                                     static_cast<const Tin*>(Wr), bias, T, H,   \
+                                                     E, k, topk_idx, topk_w, blk_cnt,          \
+                                                     blk_prob, X);                             \
     return cudaGetLastError();                                                                 \
   }
   if (E <= 8) MM_ROUTER_CASE(8)
@@ -428,34 +660,57 @@ static cudaError_t launch_router_t(const void* x, const void* Wr, const float* b
 
 cudaError_t launch_router(int dtype, const void* x, const void* Wr, const float* bias, int64_t T,
                           int H, int E, int k, int32_t* topk_idx, float* topk_w, int32_t* blk_cnt,
-                          float* blk_prob, cudaStream_t st) {
+                          float* blk_prob, const RouteOut& out, const void* const* wd_src, int I,
+                          void* wd16, WsHeader* hdr, cudaStream_t st) {
+  RouteExtras X;
+  memset(&X, 0, sizeof(X));
+  X.blk_base = out.blk_base;
+  X.offsets = out.offsets;
+  X.counts = out.counts;
+  X.aux_loss = out.aux_loss;
+  X.coef = out.coef;
+  X.do_scan = out.do_scan;
+  X.hdr = hdr;
+  if (wd_src != nullptr) {
+    // one 32-bit index space of 16-byte vectors over the E matrices
+    if (static_cast<long long>(H) * I / 8 * E + 16LL * num_sms() * kRouteThreads >= (1LL << 31))
+      return cudaErrorInvalidValue;
+    for (int m = 0; m < E; ++m) X.conv_src.p[m] = wd_src[m];
+    X.conv_dst = static_cast<__half*>(wd16);
+    X.conv_per = static_cast<int64_t>(H) * I;
+    X.conv_n = E;
+    X.n_conv = num_sms();
+  }
   if (dtype == kDtypeBF16)
     return launch_router_t<__nv_bfloat16>(x, Wr, bias, T, H, E, k, topk_idx, topk_w, blk_cnt,
-                                          blk_prob, st);
-  return launch_router_t<float>(x, Wr, bias, T, H, E, k, topk_idx, topk_w, blk_cnt, blk_prob, st);
-}
-
-cudaError_t launch_route_scan(int E, int k, int64_t T, float coef, const int32_t* blk_cnt,
-                              const float* blk_prob, int32_t* blk_base, int32_t* offsets,
-                              int32_t* counts, float* aux_loss, cudaStream_t st) {
-  const int nblk = static_cast<int>((T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock);
-  route_scan_kernel<<<1, kScanThreads, 0, st>>>(E, k, nblk, T, coef, blk_cnt, blk_prob, blk_base,
-                                                offsets, counts, aux_loss);
-  return cudaGetLastError();
+                                          blk_prob, X, st);
+  return launch_router_t<float>(x, Wr, bias, T, H, E, k, topk_idx, topk_w, blk_cnt, blk_prob, X,
+                                st);
 }
 
 cudaError_t launch_dispatch(int dtype, const void* x, int64_t T, int H, int E, int k,
-                            const int32_t* topk_idx, const int32_t* blk_base,
-                            const int32_t* offsets, int32_t* perm, void* Xp, cudaStream_t st) {
+                            const int32_t* topk_idx, const int32_t* blk_cnt, const float* blk_prob,
+                            const DispatchOut& D, int32_t* perm, void* Xp, cudaStream_t st) {
   const int nblk = static_cast<int>((T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock);
+  const size_t rows = static_cast<size_t>(kRouteTokensPerBlock) * H;
   if (dtype == kDtypeBF16) {
-    dispatch_kernel<__nv_bfloat16><<<nblk, kRouteThreads, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(x), T, H, E, k, topk_idx, blk_base, offsets, perm,
-        static_cast<__nv_bfloat16*>(Xp));
+    const size_t smem = rows * 2;
+    const int stage = smem <= 110 * 1024 ? 1 : 0;
+    auto fn = dispatch_kernel<__nv_bfloat16>;
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), stage ? smem : 0);
+    if (e != cudaSuccess) return e;
+    fn<<<nblk, kRouteThreads, stage ? smem : 0, st>>>(
+        static_cast<const __nv_bfloat16*>(x), T, H, E, k, topk_idx, blk_cnt, blk_prob, D, perm,
+        static_cast<__nv_bfloat16*>(Xp), stage);
   } else {
-    dispatch_kernel<float><<<nblk, kRouteThreads, 0, st>>>(
-        static_cast<const float*>(x), T, H, E, k, topk_idx, blk_base, offsets, perm,
-        static_cast<float*>(Xp));
+    const size_t smem = rows * 4;
+    const int stage = smem <= 110 * 1024 ? 1 : 0;
+    auto fn = dispatch_kernel<float>;
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), stage ? smem : 0);
+    if (e != cudaSuccess) return e;
+    fn<<<nblk, kRouteThreads, stage ? smem : 0, st>>>(static_cast<const float*>(x), T, H, E, k,
+                                                       topk_idx, blk_cnt, blk_prob, D, perm,
+                                                       static_cast<float*>(Xp), stage);
   }
   return cudaGetLastError();
 }
