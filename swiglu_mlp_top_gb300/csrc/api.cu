@@ -163,6 +163,46 @@ namespace {
 
 inline char* ws_at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
 
+// A second stream per device for work that may overlap the caller's stream
+// within one call: forked from and joined back into the caller's stream with
+// events (also inside a CUDA graph capture, where it becomes a parallel
+// branch).  Created on first use; never destroyed.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+cudaError_t side_fork(cudaStream_t st, SideStream** out) {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static SideStream per_dev[kMaxDev];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  SideStream& s = per_dev[dev];
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (s.stream == nullptr) {
+      e = cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
+      if (e != cudaSuccess) {
+        s.stream = nullptr;
+        return e;
+      }
+    }
+  }
+  e = cudaEventRecord(s.fork, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s.stream, s.fork, 0);
+  *out = &s;
+  return e;
+}
+cudaError_t side_join(cudaStream_t st, SideStream* s) {
+  cudaError_t e = cudaEventRecord(s->join, s->stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, s->join, 0);
+  return e;
+}
+
 // ----------------------------------------------------------- measurement hooks
 std::atomic<uint64_t> g_launches{0};
 
@@ -378,8 +418,6 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
   float* acc32 = (dtype == kDtypeF32) ? static_cast<float*>(y)
                                       : reinterpret_cast<float*>(ws_at(workspace, L.acc32));
 
-  // router + scan, with the fp16 copy of Wd made by extra blocks of the same
-  // grid (tensor path)
   const int64_t rows = T * k;
   const void* wd16p[MM_MAX_EXPERTS];
   char* wd16 = ws_at(workspace, L.wd16);
@@ -388,7 +426,7 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
   const RouteOut ro{nullptr, nullptr, nullptr, nullptr, coef, 0};
   cudaError_t e = counted_launch(MM_KERNEL_ROUTER, st, [&] {
     return launch_router(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w, blk_cnt, blk_prob,
-                         ro, p == MM_PATH_TENSOR ? Wd : nullptr, I, wd16, hdr, st);
+                         ro, hdr, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "router");
   const DispatchOut dout{offsets, counts, aux_loss, coef, hdr};
@@ -397,6 +435,21 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
   });
   if (e != cudaSuccess) return cuda_fail(e, "dispatch");
 
+  // tensor path: the fp16 copy of Wd runs on the library's side stream,
+  // concurrently with the gate/up GEMM (tensor-bound, HBM mostly idle), and
+  // is joined before the down GEMM
+  SideStream* side = nullptr;
+  if (p == MM_PATH_TENSOR) {
+    e = side_fork(st, &side);
+    if (e != cudaSuccess) return cuda_fail(e, "side stream fork");
+    e = counted_launch(MM_KERNEL_WCONVERT, side->stream, [&] {
+      return launch_convert_bf16_to_f16(Wd, E, static_cast<int64_t>(H) * I, wd16, side->stream);
+    });
+    if (e != cudaSuccess) {
+      side_join(st, side);
+      return cuda_fail(e, "wd convert");
+    }
+  }
   // gate/up over all k*E (slot, expert) groups at once
   GroupRows gu{offsets, k * E, 0, E};
   if (p == MM_PATH_TENSOR)
@@ -407,6 +460,10 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
     e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
       return launch_gateup_simt(dtype, xp, rows, H, I, gu, Wg, Wu, h, st);
     });
+  if (side != nullptr) {
+    const cudaError_t ej = side_join(st, side);
+    if (e == cudaSuccess) e = ej;
+  }
   if (e != cudaSuccess) return cuda_fail(e, "gateup");
   // down: one phase per slot; the k contributions of a token are summed in
   // fp32 in slot order and rounded once
@@ -458,7 +515,7 @@ int mm_moe_route(const void* x, const void* Wr, int64_t T, int H, int E, int k, 
   const RouteOut ro{nullptr, nullptr, expert_counts, aux_loss, coef, 1};
   cudaError_t e = counted_launch(MM_KERNEL_ROUTER, st, [&] {
     return launch_router(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w, blk_cnt, blk_prob,
-                         ro, nullptr, 0, nullptr, hdr, st);
+                         ro, hdr, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "router");
   return MM_OK;

@@ -60,10 +60,9 @@ struct DownEpilogue {
 };
 
 // Router grid (routing.cu): per 64-token block logits, softmax, top-k, alpha
-// and partial counts / probability sums; the block that finishes last runs
-// the scan (group offsets, per-block bases, counts, aux loss; the counter
-// lives in the workspace header).  With wd_src set, num_sms() further blocks
-// copy the E down matrices [H, I] to fp16 at wd16 meanwhile.
+// and partial counts / probability sums; with do_scan the block that
+// finishes last runs the scan (counts, aux loss; its counter lives in the
+// workspace header).
 struct RouteOut {
   int32_t* blk_base;     // [nblk, k*E] or null
   int32_t* offsets;      // [k*E + 1] or null
@@ -79,19 +78,13 @@ struct RouteExtras {
   float* aux_loss;
   float coef;
   WsHeader* hdr;
-  PtrArray conv_src;     // Wd per expert (bf16)
-  __half* conv_dst;      // [E, H, I] fp16
-  int64_t conv_per;      // H * I
-  int conv_n;            // E, or 0: no conversion
-  int n_conv;            // conversion blocks (the grid's first)
   int stage_x;           // x rows staged in shared memory at byte x_off
   uint32_t x_off;
   int do_scan;
 };
 cudaError_t launch_router(int dtype, const void* x, const void* Wr, const float* bias, int64_t T,
                           int H, int E, int k, int32_t* topk_idx, float* topk_w, int32_t* blk_cnt,
-                          float* blk_prob, const RouteOut& out, const void* const* wd_src, int I,
-                          void* wd16, WsHeader* hdr, cudaStream_t st);
+                          float* blk_prob, const RouteOut& out, WsHeader* hdr, cudaStream_t st);
 size_t router_smem_bytes(int H, int E, int k);
 // Dispatch (routing.cu): group bases, offsets, expert counts and the aux
 // loss from the router's per-block partials, then the token permute.

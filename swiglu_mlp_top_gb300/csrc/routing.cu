@@ -77,7 +77,6 @@ __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return
 // ---------------------------------------------------------------------------
 __device__ void scan_block(int E, int k, int nblk, int64_t T, const RouteExtras& X,
                            const int32_t* __restrict__ blk_cnt, const float* __restrict__ blk_prob);
-__device__ void convert_role(const RouteExtras& X, int blk, int nblk_conv);
 
 template <typename Tin, int EP>
 __global__ void __launch_bounds__(kRouteThreads)
@@ -94,12 +93,7 @@ router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float
   constexpr int kPerWarp = kRouteTokensPerBlock / kWarps;
   static_assert(kPerWarp % TPW == 0, "passes cover a warp's tokens");
 
-  // the grid's first X.n_conv blocks copy Wd to fp16, the rest route
-  if (static_cast<int>(blockIdx.x) < X.n_conv) {
-    convert_role(X, blockIdx.x, X.n_conv);
-    return;
-  }
-  const int rblk = blockIdx.x - X.n_conv;          // router block: tokens [64 rblk, +64)
+  const int rblk = blockIdx.x;                     // router block: tokens [64 rblk, +64)
   const int nblk = static_cast<int>((T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock);
 
   extern __shared__ float4 route_smem4[];
@@ -412,50 +406,6 @@ __device__ void scan_block(int E, int k, int nblk, int64_t T, const RouteExtras&
   }
 }
 
-// Copy of the E down-projection matrices from bf16 to fp16 (exact for
-// |w| >= 2^-14; smaller magnitudes become fp16 subnormals, error <= 2^-25),
-// by the router grid's first X.n_conv blocks.  The E matrices form one index
-// space of 16-byte vectors cut into one contiguous range per block (a range
-// meets at most a few matrices, so the matrix index is stepped, not divided);
-// each thread keeps kInFlight vectors in flight.
-__device__ void convert_role(const RouteExtras& X, int blk, int nblk_conv) {
-  constexpr int kInFlight = 8;
-  const int nvec = static_cast<int>(X.conv_per / 8);      // per matrix
-  const int total = nvec * X.conv_n;                      // < 2^31 (checked by the launcher)
-  const int r0 = static_cast<int>(static_cast<long long>(total) * blk / nblk_conv);
-  const int r1 = static_cast<int>(static_cast<long long>(total) * (blk + 1) / nblk_conv);
-  int m = r0 / nvec;                                      // matrix of this thread's next vector
-  int off = r0 - m * nvec + static_cast<int>(threadIdx.x);
-  while (off >= nvec) { off -= nvec; ++m; }
-  uint4* dst = reinterpret_cast<uint4*>(X.conv_dst);
-  for (int v0 = r0 + static_cast<int>(threadIdx.x); v0 < r1; v0 += kInFlight * kRouteThreads) {
-    uint4 raw[kInFlight];
-    int mm_[kInFlight], oo[kInFlight];
-#pragma unroll
-    for (int j = 0; j < kInFlight; ++j) {
-      mm_[j] = m;
-      oo[j] = off;
-      if (v0 + j * kRouteThreads < r1)
-        raw[j] = __ldcs(static_cast<const uint4*>(X.conv_src.p[m]) + off);
-      off += kRouteThreads;
-      while (off >= nvec) { off -= nvec; ++m; }   // more than once only when nvec < 256
-    }
-#pragma unroll
-    for (int j = 0; j < kInFlight; ++j) {
-      if (v0 + j * kRouteThreads < r1) {
-        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw[j]);
-        uint4 out;
-        uint32_t* o = reinterpret_cast<uint32_t*>(&out);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 f = __bfloat1622float2(b[q]);
-          o[q] = pack_f16x2(f.x, f.y);
-        }
-        __stcs(dst + static_cast<int64_t>(mm_[j]) * nvec + oo[j], out);
-      }
-    }
-  }
-}
 
 // ---------------------------------------------------------------------------
 // Dispatch: block b owns the same tokens as router block b.  From the
@@ -627,8 +577,7 @@ size_t router_smem_bytes(int H, int E, int k) {
   return static_cast<size_t>(E) * H * sizeof(float) + static_cast<size_t>(k) * E * sizeof(int);
 }
 
-// Router grid: X.n_conv conversion blocks (when Wd is given), then one block
-// per 64 tokens.  x is staged in shared memory when the block's rows and Wr
+// Router grid: one block per 64 tokens.  x is staged in shared memory when the block's rows and Wr
 // fit in 110 KiB together (two blocks per SM).
 template <typename Tin>
 static cudaError_t launch_router_t(const void* x, const void* Wr, const float* bias, int64_t T, int H,
@@ -645,7 +594,7 @@ static cudaError_t launch_router_t(const void* x, const void* Wr, const float* b
     auto fn = router_kernel<Tin, EPAD>;                                                        \
     cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem);             \
     if (err != cudaSuccess) return err;                                                        \
-    fn<<<X.n_conv + nblk, kRouteThreads, smem, st>>>(static_cast<const Tin*>(x),               \
+    fn<<<nblk, kRouteThreads, smem, st>>>(static_cast<const Tin*>(x),               \
                                                      static_cast<const Tin*>(Wr), bias, T, H,   \
                                                      E, k, topk_idx, topk_w, blk_cnt,          \
                                                      blk_prob, X);                             \
@@ -660,8 +609,7 @@ static cudaError_t launch_router_t(const void* x, const void* Wr, const float* b
 
 cudaError_t launch_router(int dtype, const void* x, const void* Wr, const float* bias, int64_t T,
                           int H, int E, int k, int32_t* topk_idx, float* topk_w, int32_t* blk_cnt,
-                          float* blk_prob, const RouteOut& out, const void* const* wd_src, int I,
-                          void* wd16, WsHeader* hdr, cudaStream_t st) {
+                          float* blk_prob, const RouteOut& out, WsHeader* hdr, cudaStream_t st) {
   RouteExtras X;
   memset(&X, 0, sizeof(X));
   X.blk_base = out.blk_base;
@@ -671,16 +619,6 @@ cudaError_t launch_router(int dtype, const void* x, const void* Wr, const float*
   X.coef = out.coef;
   X.do_scan = out.do_scan;
   X.hdr = hdr;
-  if (wd_src != nullptr) {
-    // one 32-bit index space of 16-byte vectors over the E matrices
-    if (static_cast<long long>(H) * I / 8 * E + 16LL * num_sms() * kRouteThreads >= (1LL << 31))
-      return cudaErrorInvalidValue;
-    for (int m = 0; m < E; ++m) X.conv_src.p[m] = wd_src[m];
-    X.conv_dst = static_cast<__half*>(wd16);
-    X.conv_per = static_cast<int64_t>(H) * I;
-    X.conv_n = E;
-    X.n_conv = num_sms();
-  }
   if (dtype == kDtypeBF16)
     return launch_router_t<__nv_bfloat16>(x, Wr, bias, T, H, E, k, topk_idx, topk_w, blk_cnt,
                                           blk_prob, X, st);
