@@ -218,7 +218,7 @@ template <int OP, int MAXW>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g, const int K,
                     const int NCOLS, __half* __restrict__ hout, const DownEpilogue ep,
-                    WsHeader* hdr) {
+                    WsHeader* hdr, const int dep_mainloop) {
   constexpr int kOutCols = OpTraits<OP>::kOutCols;
   extern __shared__ unsigned char smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -267,9 +267,19 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
   const int total = s_tstart[g.G];
   volatile int* abort = &s_abort;
 
+  // Programmatic dependent launch: with dep_mainloop the operands come from
+  // the previous kernel, so the producer waits for it before the first load
+  // and only then lets the next kernel launch (which may then rely on this
+  // kernel's inputs being complete); otherwise the next kernel may launch at
+  // once.  griddepcontrol is a no-op for a launch without the attribute.
+  if (!dep_mainloop && threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (warp == kWarpProducer) {
     // ------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
+      if (dep_mainloop) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+      }
       int it = 0;
       bool ok = true;
       for (int tile = cluster; ok && tile < total; tile += n_clusters) {
@@ -337,6 +347,9 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
     uint8_t* wstage = sEpi + warp * 32 * 64;     // gate/up: this warp's staging tile
     const uint32_t te0 = mapa_shared(smem_u32(&tempty[0]), 0);
     const uint32_t te1 = mapa_shared(smem_u32(&tempty[1]), 0);
+    // the running fp32 sum is the previous kernel's output
+    if (OP == kOpDown && (ep.mode == kCombineAccum || ep.mode == kCombineLast))
+      asm volatile("griddepcontrol.wait;" ::: "memory");
     int local = 0;
     for (int tile = cluster; tile < total; tile += n_clusters, ++local) {
       const TileInfo ti = decode_tile(tile, s_off, s_tstart, g.G, g.n_weights, n_tiles, kOutCols,
@@ -442,6 +455,24 @@ cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes) {
   return e;
 }
 
+// Launch with programmatic stream serialisation (the kernel may start while
+// the previous kernel of the stream finishes; see griddepcontrol in it).
+template <typename Kern, typename... Args>
+static cudaError_t launch_pdl(Kern fn, int grid, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, args...);
+}
+
 // Number of CTA pairs: one per tile pair, at most one per co-resident pair.
 static int clusters_for(int64_t a_rows, const GroupRows& g, int n_tiles) {
   int64_t tiles;
@@ -471,9 +502,8 @@ static cudaError_t gateup_impl(const void* A, int64_t a_rows, int H, int I, cons
   if (err != cudaSuccess) return err;
   const int n_tiles = (I + kN / 2 - 1) / (kN / 2);
   DownEpilogue none{};
-  fn<<<2 * clusters_for(a_rows, g, n_tiles), kThreads, kSmem, st>>>(
-      p, g, H, I, static_cast<__half*>(h_out), none, hdr);
-  return cudaGetLastError();
+  return launch_pdl(fn, 2 * clusters_for(a_rows, g, n_tiles), st, p, g, H, I,
+                    static_cast<__half*>(h_out), none, hdr, 1);
 }
 
 template <int MAXW>
@@ -489,9 +519,11 @@ static cudaError_t down_impl(const void* h, int64_t a_rows, int H, int I, const 
   cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), kSmem);
   if (err != cudaSuccess) return err;
   const int n_tiles = (H + kN - 1) / kN;
-  fn<<<2 * clusters_for(a_rows, g, n_tiles), kThreads, kSmem, st>>>(p, g, I, H, nullptr, ep,
-                                                                        hdr);
-  return cudaGetLastError();
+  // a later slot's operands (h, fp16 Wd) were complete before the previous
+  // slot's launch let it start: only its epilogue waits (for the fp32 sum)
+  const int dep = (ep.mode == kCombineAccum || ep.mode == kCombineLast) ? 0 : 1;
+  return launch_pdl(fn, 2 * clusters_for(a_rows, g, n_tiles), st, p, g, I, H,
+                    static_cast<__half*>(nullptr), ep, hdr, dep);
 }
 
 cudaError_t launch_gateup_tc(const void* A, int64_t a_rows, int H, int I, const GroupRows& g,
