@@ -5,6 +5,8 @@
 // Follows MiniMind lesson 13 "FFN 与 MoE" §1.5 (router equations), §1.6 and
 // step 6 (aux loss), step 4-5 (top-k, renormalisation, per-expert dispatch
 // and index_add_ into y), and minimind3.com chapter 4 §4.3-§4.4.
+#include <cstring>
+
 #include "mm_kernels.cuh"
 
 namespace mm {
@@ -93,6 +95,9 @@ router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float
   constexpr int kPerWarp = kRouteTokensPerBlock / kWarps;
   static_assert(kPerWarp % TPW == 0, "passes cover a warp's tokens");
 
+  // the dispatch kernel may launch as soon as router blocks start to leave
+  // (it waits for this grid before reading the routing results)
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int rblk = blockIdx.x;                     // router block: tokens [64 rblk, +64)
   const int nblk = static_cast<int>((T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock);
 
@@ -431,6 +436,7 @@ dispatch_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, int k,
   __shared__ int s_w0cnt[MM_MAX_EXPERTS];   // per-expert count in warp 0 (tokens 0..31)
   __shared__ int s_pos[kRouteTokensPerBlock * MM_MAX_TOPK];
   __shared__ int s_base[kMaxGroups], s_tot[kMaxGroups], s_off[kMaxGroups + 1];
+  __shared__ int s_part[kRouteThreads / 32][32][2];
   __shared__ __align__(8) uint64_t xbar;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -455,30 +461,47 @@ dispatch_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, int k,
         : "memory");
   }
 
-  // group totals and this block's bases: a warp per group, lanes over runs of
-  // router blocks, every count of a run requested at once
-  const int per = (nblk + 31) / 32;
-  for (int g = warp; g < G; g += kWarps) {
-    const int b0 = lane * per, b1 = min(nblk, b0 + per);
-    int all = 0, before = 0;
-    for (int bb = b0; bb < b1; bb += 8) {
-      int c[8];
+  // the routing results come from the router grid, launched just before
+  // (x is the caller's input and may be read at once)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // group totals and this block's bases: warp w sums a run of router blocks,
+  // lane g its group (all counts of the run requested at once), then the
+  // warps' partial sums are added in warp order
+  {
+    const int per = (nblk + kWarps - 1) / kWarps;
+    const int b0 = warp * per, b1 = min(nblk, b0 + per);
+    for (int g0 = 0; g0 < G; g0 += 32) {
+      const int g = g0 + lane;
+      int all = 0, before = 0;
+      if (g < G) {
+        for (int bb = b0; bb < b1; bb += 8) {
+          int c[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) c[j] = (bb + j < b1) ? blk_cnt[static_cast<int64_t>(bb + j) * G + g] : 0;
+          for (int j = 0; j < 8; ++j) c[j] = (bb + j < b1) ? blk_cnt[static_cast<int64_t>(bb + j) * G + g] : 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        all += c[j];
-        before += (bb + j < b) ? c[j] : 0;
+          for (int j = 0; j < 8; ++j) {
+            all += c[j];
+            before += (bb + j < b) ? c[j] : 0;
+          }
+        }
       }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      all += __shfl_xor_sync(0xffffffffu, all, o);
-      before += __shfl_xor_sync(0xffffffffu, before, o);
-    }
-    if (lane == 0) {
-      s_tot[g] = all;
-      s_base[g] = before;
+      __syncthreads();                       // s_part of the previous round is read
+      if (g < G) {
+        s_part[warp][lane][0] = all;
+        s_part[warp][lane][1] = before;
+      }
+      __syncthreads();
+      if (tid < 32 && g0 + tid < G) {
+        int a = 0, bf = 0;
+        for (int w = 0; w < kWarps; ++w) {
+          a += s_part[w][tid][0];
+          bf += s_part[w][tid][1];
+        }
+        s_tot[g0 + tid] = a;
+        s_base[g0 + tid] = bf;
+      }
     }
   }
   __syncthreads();
@@ -509,19 +532,25 @@ dispatch_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, int k,
       for (int s = 0; s < k; ++s) c += s_tot[s * E + e];
       if (D.counts != nullptr) D.counts[e] = c;
     }
-    if (warp == 0) {
-      // aux: lane-strided partial sums over the router blocks, fixed xor tree
+    // aux: P_e by warp e % 8 (lane-strided partial sums over the router
+    // blocks, a fixed xor tree), then one thread adds count_e * P_e in order
+    __shared__ float s_P[MM_MAX_EXPERTS];
+    for (int e = warp; e < E; e += kWarps) {
+      float P = 0.f;
+      for (int bb = lane; bb < nblk; bb += 32) P += blk_prob[static_cast<int64_t>(bb) * E + e];
+      P = warp_sum(P);
+      if (lane == 0) s_P[e] = P;
+    }
+    __syncthreads();
+    if (tid == 0) {
       float acc = 0.f;
       for (int e = 0; e < E; ++e) {
-        float P = 0.f;
-        for (int bb = lane; bb < nblk; bb += 32) P += blk_prob[static_cast<int64_t>(bb) * E + e];
-        P = warp_sum(P);
         int c = 0;
         for (int s = 0; s < k; ++s) c += s_tot[s * E + e];
-        acc = fmaf(static_cast<float>(c), P, acc);
+        acc = fmaf(static_cast<float>(c), s_P[e], acc);
       }
       const float invT = 1.0f / static_cast<float>(T);
-      if (lane == 0) *D.aux_loss = static_cast<float>(E) * D.coef * acc * invT * invT;
+      *D.aux_loss = static_cast<float>(E) * D.coef * acc * invT * invT;
     }
   }
 
@@ -626,31 +655,43 @@ cudaError_t launch_router(int dtype, const void* x, const void* Wr, const float*
                                 st);
 }
 
+// Launch with programmatic stream serialisation: the dispatch blocks may
+// start while the router grid finishes (they wait for it before reading its
+// results).
+template <typename Tin>
+static cudaError_t launch_dispatch_t(const Tin* x, int64_t T, int H, int E, int k,
+                                     const int32_t* topk_idx, const int32_t* blk_cnt,
+                                     const float* blk_prob, const DispatchOut& D, int32_t* perm,
+                                     Tin* Xp, cudaStream_t st) {
+  const int nblk = static_cast<int>((T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock);
+  const size_t smem = static_cast<size_t>(kRouteTokensPerBlock) * H * sizeof(Tin);
+  const int stage = smem <= 110 * 1024 ? 1 : 0;
+  auto fn = dispatch_kernel<Tin>;
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), stage ? smem : 0);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(nblk);
+  cfg.blockDim = dim3(kRouteThreads);
+  cfg.dynamicSmemBytes = stage ? smem : 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, x, T, H, E, k, topk_idx, blk_cnt, blk_prob, D, perm, Xp,
+                            stage);
+}
+
 cudaError_t launch_dispatch(int dtype, const void* x, int64_t T, int H, int E, int k,
                             const int32_t* topk_idx, const int32_t* blk_cnt, const float* blk_prob,
                             const DispatchOut& D, int32_t* perm, void* Xp, cudaStream_t st) {
-  const int nblk = static_cast<int>((T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock);
-  const size_t rows = static_cast<size_t>(kRouteTokensPerBlock) * H;
-  if (dtype == kDtypeBF16) {
-    const size_t smem = rows * 2;
-    const int stage = smem <= 110 * 1024 ? 1 : 0;
-    auto fn = dispatch_kernel<__nv_bfloat16>;
-    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), stage ? smem : 0);
-    if (e != cudaSuccess) return e;
-    fn<<<nblk, kRouteThreads, stage ? smem : 0, st>>>(
-        static_cast<const __nv_bfloat16*>(x), T, H, E, k, topk_idx, blk_cnt, blk_prob, D, perm,
-        static_cast<__nv_bfloat16*>(Xp), stage);
-  } else {
-    const size_t smem = rows * 4;
-    const int stage = smem <= 110 * 1024 ? 1 : 0;
-    auto fn = dispatch_kernel<float>;
-    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), stage ? smem : 0);
-    if (e != cudaSuccess) return e;
-    fn<<<nblk, kRouteThreads, stage ? smem : 0, st>>>(static_cast<const float*>(x), T, H, E, k,
-                                                       topk_idx, blk_cnt, blk_prob, D, perm,
-                                                       static_cast<float*>(Xp), stage);
-  }
-  return cudaGetLastError();
+  if (dtype == kDtypeBF16)
+    return launch_dispatch_t(static_cast<const __nv_bfloat16*>(x), T, H, E, k, topk_idx, blk_cnt,
+                             blk_prob, D, perm, static_cast<__nv_bfloat16*>(Xp), st);
+  return launch_dispatch_t(static_cast<const float*>(x), T, H, E, k, topk_idx, blk_cnt, blk_prob,
+                           D, perm, static_cast<float*>(Xp), st);
 }
 
 }  // namespace mm
