@@ -158,55 +158,88 @@ __device__ __forceinline__ void epilogue_up(uint32_t tb, const TileInfo& ti, int
 
 // down: 128 y columns (half `half` of the tile's 256) of one row, scaled by
 // alpha: Store -> y (x's dtype); First -> acc32 = v; Accum -> acc32 += v;
-// Last -> y = round(acc32 + v).
-__device__ __forceinline__ void epilogue_down(uint32_t tb, bool valid, const TileInfo& ti, int H,
-                                              const DownEpilogue& ep, int row, int half) {
-  int64_t tok = 0;
-  float alpha = 1.0f;
-  if (valid) {
+// Last -> y = round(acc32 + v).  The row's token and alpha (two dependent
+// global loads) and the first chunk of the running fp32 sum are requested
+// before the tile's accumulator is ready; each later chunk of the sum is
+// requested while the previous chunk is being processed.
+struct DownRow {
+  int64_t tok;
+  float alpha;
+  bool valid;
+};
+
+__device__ __forceinline__ DownRow down_row_info(const TileInfo& ti, const DownEpilogue& ep,
+                                                 int row) {
+  DownRow d{0, 1.0f, row < ti.rows};
+  if (d.valid) {
     const int pos = ti.row0 + row;
     if (ep.perm != nullptr) {
       const int a = ep.perm[pos];
-      alpha = ep.topk_w != nullptr ? ep.topk_w[a] : 1.0f;
-      tok = a / ep.k;
+      d.alpha = ep.topk_w != nullptr ? ep.topk_w[a] : 1.0f;
+      d.tok = a / ep.k;
     } else {
-      tok = pos;
+      d.tok = pos;
     }
   }
-  const int col0 = ti.n0 + half * (kN / 2);
-  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(ep.y) + tok * H + col0;
-  float* acc32 = ep.acc32 + tok * H + col0;
-#pragma unroll 1
-  for (int c = 0; c < kN / 2 / 32; ++c) {
-    const bool live = valid && col0 + c * 32 < H;
-    float4* a4 = reinterpret_cast<float4*>(acc32 + c * 32);
-    float4 pre[8];
-    if (live && (ep.mode == kCombineAccum || ep.mode == kCombineLast)) {
+  return d;
+}
+
+__device__ __forceinline__ bool down_reads_sum(const DownEpilogue& ep) {
+  return ep.mode == kCombineAccum || ep.mode == kCombineLast;
+}
+
+// chunk c (32 columns) of the running sum for this row, if the mode reads it
+__device__ __forceinline__ void down_prefetch(const DownRow& d, const TileInfo& ti, int H,
+                                              const DownEpilogue& ep, int half, int c,
+                                              float4 (&pre)[8]) {
+  const int col0 = ti.n0 + half * (kN / 2) + c * 32;
+  if (d.valid && col0 < H && down_reads_sum(ep)) {
+    const float4* a4 = reinterpret_cast<const float4*>(ep.acc32 + d.tok * H + col0);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) pre[q] = a4[q];
-    }
+    for (int q = 0; q < 8; ++q) pre[q] = a4[q];
+  }
+}
+
+__device__ __forceinline__ void epilogue_down(uint32_t tb, const DownRow& d, const TileInfo& ti,
+                                              int H, const DownEpilogue& ep, int half,
+                                              float4 (&pre)[8]) {
+  const int col0 = ti.n0 + half * (kN / 2);
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(ep.y) + d.tok * H + col0;
+  float* acc32 = ep.acc32 + d.tok * H + col0;
+  constexpr int kChunks = kN / 2 / 32;
+#pragma unroll 1
+  for (int c = 0; c < kChunks; ++c) {
+    const bool live = d.valid && col0 + c * 32 < H;
+    float4 nxt[8];
+    if (c + 1 < kChunks) down_prefetch(d, ti, H, ep, half, c + 1, nxt);
     uint32_t r[32];
     tmem_ld_32x32b_x32(tb + half * (kN / 2) + c * 32, r);
     tmem_ld_wait();
-    if (!live) continue;
-    float v[32];
+    if (live) {
+      float v[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = alpha * __uint_as_float(r[j]);
-    if (ep.mode == kCombineAccum || ep.mode == kCombineLast) {
+      for (int j = 0; j < 32; ++j) v[j] = d.alpha * __uint_as_float(r[j]);
+      if (down_reads_sum(ep)) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        v[4 * q] += pre[q].x; v[4 * q + 1] += pre[q].y; v[4 * q + 2] += pre[q].z; v[4 * q + 3] += pre[q].w;
+        for (int q = 0; q < 8; ++q) {
+          v[4 * q] += pre[q].x; v[4 * q + 1] += pre[q].y; v[4 * q + 2] += pre[q].z; v[4 * q + 3] += pre[q].w;
+        }
+      }
+      if (ep.mode == kCombineFirst || ep.mode == kCombineAccum) {
+        float4* a4 = reinterpret_cast<float4*>(acc32 + c * 32);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) a4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      } else {
+        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          d4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                             pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
       }
     }
-    if (ep.mode == kCombineFirst || ep.mode == kCombineAccum) {
+    if (c + 1 < kChunks) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) a4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-    } else {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        d4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+      for (int q = 0; q < 8; ++q) pre[q] = nxt[q];
     }
   }
 }
@@ -356,13 +389,20 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
                                       static_cast<int>(rank));
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
+      DownRow dr{0, 1.0f, false};
+      float4 pre[8];
+      if constexpr (OP == kOpDown) {
+        // independent of the MMAs: requested while they run
+        dr = down_row_info(ti, ep, row);
+        down_prefetch(dr, ti, NCOLS, ep, half, 0, pre);
+      }
       if (!warp_wait(&tfull[acc], aph, abort, hdr, 6)) break;
       tc_fence_after();
       const uint32_t tb = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * kAccStride;
       if constexpr (OP == kOpUp)
         epilogue_up(tb, ti, NCOLS, hout, row, half, wstage, &P.out);
       else
-        epilogue_down(tb, row < ti.rows, ti, NCOLS, ep, row, half);
+        epilogue_down(tb, dr, ti, NCOLS, ep, half, pre);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc ? te1 : te0);
