@@ -58,33 +58,6 @@ struct DecodeArgs {
 };
 
 
-// Sum of NV per-lane values over the warp, scattered: lane L ends with the
-// full sum of value L / (32 / NV).  Each exchange step hands half of the
-// remaining values to the partner lane, so the warp moves NV - 1 + (5 -
-// log2 NV) shuffles instead of 5 * NV.
-template <int NV, int CNT, int O>
-__device__ __forceinline__ void reduce_scatter_step(float (&v)[NV], int lane) {
-  if constexpr (O > 0) {
-    if constexpr (CNT > 1) {
-      const bool up = (lane & O) != 0;
-#pragma unroll
-      for (int q = 0; q < CNT / 2; ++q) {
-        const float lo = v[q], hi = v[q + CNT / 2];
-        v[q] = (up ? hi : lo) + __shfl_xor_sync(0xffffffffu, up ? lo : hi, O);
-      }
-      reduce_scatter_step<NV, CNT / 2, O / 2>(v, lane);
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
-      reduce_scatter_step<NV, 1, O / 2>(v, lane);
-    }
-  }
-}
-template <int NV>
-__device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
-  reduce_scatter_step<NV, NV, 16>(v, lane);
-  return v[0];
-}
-
 // 1-D bulk copy global -> this CTA's shared memory, completion on `bar`.
 __device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes,
                                           uint64_t* bar) {

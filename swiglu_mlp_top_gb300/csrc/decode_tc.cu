@@ -50,6 +50,9 @@ constexpr int kDtMaxMB = 64;                    // output m-blocks (H <= 8192)
 constexpr int kDtMaxSplit = 4;                  // k-ranges per gate/up block at most
 constexpr int kDtReduceChunk = 32;              // partials requested at once in the final sum
 constexpr size_t kDtSmemBudget = 196 * 1024;   // dynamic; static use is ~27 KiB
+constexpr int kDtFusedMinUnits = 64;            // fused variant: (expert, I-block) units at least
+constexpr int kDtMaxSlices = 8;                 // fused: partial sums per output quad at most
+constexpr int kDtSumChunk = 8;                  // fused: partials requested at once
 
 template <int MAXW>
 struct DtMaps {
@@ -75,6 +78,7 @@ struct DtArgs {
   void* y;                        // [T, H] bf16
   WsHeader* hdr;
   int stages;
+  int gu_bufs;                    // fused: (G, U) TMEM buffers (1 or 2)
   int Epad;                       // experts padded to a multiple of 16 (router N)
   uint32_t stage_bytes;           // 32 KiB of weight tiles + one x tile
   uint32_t hstage_off;            // Hp staging tile [2][Np][128] bf16 (epilogue -> TMA store)
@@ -120,7 +124,12 @@ __device__ __forceinline__ bool epi_sync_and(bool p) {
 
 
 
-template <int MAXW>
+// kFused: every unit (expert, 128 rows of I) also runs its share of the
+// down product in the same CTA, from h kept in shared memory; each CTA
+// writes one fp32 partial of y and the partials are added after one grid
+// barrier.  Otherwise h goes through global memory (split-K gate/up, down
+// ranges over output m-blocks, two or three grid barriers).
+template <int MAXW, bool kFused>
 __global__ void __launch_bounds__(kDtThreads, 1)
 decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
   extern __shared__ unsigned char smem_raw[];
@@ -131,6 +140,7 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
   __shared__ SmallRoute<kDecodeTcMaxT> R;
   __shared__ __align__(8) uint64_t full[kDtMaxStages], empty[kDtMaxStages];
   __shared__ __align__(8) uint64_t wbar, lbar, tfull[2], tempty[2], dfull, dempty, drained;
+  __shared__ __align__(8) uint64_t hfull, hempty;      // fused: h tiles written / read
   __shared__ uint32_t s_tmem;
   __shared__ float s_bias[MM_MAX_EXPERTS];
   __shared__ int s_first_mb[kDtMaxCtas];        // first output m-block of each CTA's range (-1: empty)
@@ -163,6 +173,8 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
     mbar_init(&dfull, 1);
     mbar_init(&dempty, kDtEpiWarps);
     mbar_init(&drained, 1);
+    mbar_init(&hfull, kDtEpiWarps);
+    mbar_init(&hempty, 1);
     fence_mbar_init();
   }
   if (tid < MM_MAX_EXPERTS) s_bias[tid] = (moe && A.bias != nullptr && tid < A.E) ? A.bias[tid] : 0.f;
@@ -238,7 +250,9 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
       }
     }
   }
+  tc_fence_before();
   ok = __syncthreads_and(ok);
+  tc_fence_after();
 
   // ------------------------------------------------------------ routing
   if (ok) {
@@ -261,136 +275,108 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
     __syncthreads();
   }
 
-  DtPlan P;
-  P.nt = (ok && R.n_touched > 0) ? R.n_touched : 1;
-  P.MB_I = (I + 127) / 128;
-  P.MB_H = H / 128;
-  P.KB_H = KB_H;
-  P.KB_I = I / 64;
-  {
-    // split K only for long rows (>= 24 k-blocks), keeping ranges of at least
-    // 12 k-blocks: a shorter stream finishes sooner than the extra grid
-    // barrier and the partial sums cost
-    const int blocks = P.nt * P.MB_I;
-    const int max_split = P.KB_H / 12 < 1 ? 1 : (P.KB_H / 12 > kDtMaxSplit ? kDtMaxSplit : P.KB_H / 12);
-    int s_up = (G + blocks - 1) / blocks;
-    s_up = s_up < 1 ? 1 : (s_up > max_split ? max_split : s_up);
-    P.s_up = s_up;
-    P.n_units = blocks * s_up;
-  }
-  P.per_mb = P.nt * P.KB_I;
-  P.F = P.MB_H * P.per_mb;
-  // the down tiles go to the first Gd CTAs, at least three per CTA
-  const int Gd = (P.F + 2) / 3 < G ? (P.F + 2) / 3 : G;
-  const int r0 = cta < Gd ? dt_range_start(cta, P.F, Gd) : P.F;
-  const int r1 = cta < Gd ? dt_range_start(cta + 1, P.F, Gd) : P.F;
-  const int my_down = r1 - r0;
-  const int n_pre = my_down < S ? my_down : S;     // Wd tiles requested before the barrier
-  int pre_it0 = 0;                                 // producer: stage use of the first of them
-  // contributors of every output m-block, for the final reduction
-  for (int c = tid; c < Gd; c += kDtThreads) {
-    const int s0 = dt_range_start(c, P.F, Gd);
-    s_first_mb[c] = dt_range_start(c + 1, P.F, Gd) > s0 ? s0 / P.per_mb : -1;
-  }
-  for (int mb = tid; mb < P.MB_H; mb += kDtThreads) {
-    s_c0[mb] = dt_cta_of(mb * P.per_mb, P.F, Gd);
-    s_c1[mb] = dt_cta_of(mb * P.per_mb + P.per_mb - 1, P.F, Gd);
-  }
-
-  // unit u -> (touched index, m-block, k-block range)
-  auto unit_of = [&](int u, int& ti, int& mb, int& kb0, int& kb1) {
-    const int blk = u / P.s_up, kr = u - blk * P.s_up;
-    ti = blk / P.MB_I;
-    mb = blk - ti * P.MB_I;
-    kb0 = kr * P.KB_H / P.s_up;
-    kb1 = (kr + 1) * P.KB_H / P.s_up;
-  };
-  auto tile_of = [&](int f, int& mbd, int& ti, int& kb) {
-    mbd = f / P.per_mb;
-    const int rem = f - mbd * P.per_mb;
-    ti = rem / P.KB_I;
-    kb = rem - ti * P.KB_I;
-  };
-
-  // ------------------------------------------------------------ 2: gate/up
-  // stage = Wg tile at 0, Wu tile at 16 KiB, x tile (B, N = Np) at 32 KiB
-  if (ok) {
-    if (tid == 0) {
-      for (int u = cta; ok && u < P.n_units; u += G) {
-        int ti, mb, kb0, kb1;
-        unit_of(u, ti, mb, kb0, kb1);
-        const int e = R.touched[ti];
-        for (int kb = kb0; kb < kb1; ++kb) {
-          int s;
-          if (!acquire(s)) { ok = false; break; }
-          uint8_t* st = ring + s * SB;
-          mbar_arrive_expect_tx(&full[s], 2 * kDtTileA + xtile);
-          tma_load_2d(st, &M.wg[e], &full[s], kb * 64, mb * 128);
-          tma_load_2d(st + kDtTileA, &M.wu[e], &full[s], kb * 64, mb * 128);
-          tma_load_2d(st + 2 * kDtTileA, &M.x, &full[s], kb * 64, 0);
-          ++p_it;
+  unsigned ticket = 0xffffffffu;
+  if constexpr (kFused) {
+    // ---------------------------------------------------------- 2+3: units
+    // unit u = (touched expert ti, I-block mb): stages of Wg|Wu|x tiles
+    // (gate/up, K = H), then stages of two Wd tiles (output m-block mbd,
+    // K = the unit's 128 values of I).  h = SiLU(G) * U * alpha goes from
+    // TMEM into four shared tiles (bf16 high part and remainder, two k-halves;
+    // Np rows x 128 bytes, 128-byte swizzle): the B operand of the down MMAs,
+    // which accumulate y^T for all H rows in TMEM across the CTA's units.
+    const int nt = (ok && R.n_touched > 0) ? R.n_touched : 1;
+    const int MB_I = (I + 127) / 128, MB_H = H / 128;
+    const int n_units = nt * MB_I;
+    const int nb = A.gu_bufs;
+    const uint32_t colD = 2u * static_cast<uint32_t>(Np * nb);
+    uint8_t* hs = reinterpret_cast<uint8_t*>(hstage);      // tile (part, k-half) at (2 part + kh) * xtile
+    if (ok) {
+      if (tid == 0) {
+        for (int u = cta; ok && u < n_units; u += G) {
+          const int ti = u / MB_I, mb = u - ti * MB_I, e = R.touched[ti];
+          for (int kb = 0; kb < KB_H; ++kb) {
+            int s;
+            if (!acquire(s)) { ok = false; break; }
+            uint8_t* st = ring + s * SB;
+            mbar_arrive_expect_tx(&full[s], 2 * kDtTileA + xtile);
+            tma_load_2d(st, &M.wg[e], &full[s], kb * 64, mb * 128);
+            tma_load_2d(st + kDtTileA, &M.wu[e], &full[s], kb * 64, mb * 128);
+            tma_load_2d(st + 2 * kDtTileA, &M.x, &full[s], kb * 64, 0);
+            ++p_it;
+          }
+          for (int mbd = 0; ok && mbd < MB_H; ++mbd) {
+            int s;
+            if (!acquire(s)) { ok = false; break; }
+            uint8_t* st = ring + s * SB;
+            mbar_arrive_expect_tx(&full[s], 2 * kDtTileA);
+            tma_load_2d(st, &M.wd[e], &full[s], mb * 128, mbd * 128);
+            tma_load_2d(st + kDtTileA, &M.wd[e], &full[s], mb * 128 + 64, mbd * 128);
+            ++p_it;
+          }
         }
       }
-      pre_it0 = p_it;
-      for (int j = 0; ok && j < n_pre; ++j) {
-        int mbd, ti, kb, s;
-        tile_of(r0 + j, mbd, ti, kb);
-        if (!acquire(s)) { ok = false; break; }
-        mbar_arrive_expect_tx(&full[s], kDtTileA + 2 * xtile);   // the Hp tiles follow later
-        tma_load_2d(ring + s * SB, &M.wd[R.touched[ti]], &full[s], kb * 64, mbd * 128);
-        ++p_it;
-      }
-    }
-    if (tid == 32) {
-      int local = 0;
-      for (int u = cta; ok && u < P.n_units; u += G, ++local) {
-        int ti, mb, kb0, kb1;
-        unit_of(u, ti, mb, kb0, kb1);
-        const int acc = local & 1;
-        if (!mbar_wait(&tempty[acc], ((local >> 1) & 1) ^ 1, nullptr, hdr, 44)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t dg = tmem + kDtColGU + acc * 2 * Np, du = dg + Np;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          int s;
-          if (!consume(s)) { ok = false; break; }
-          const uint8_t* st = ring + s * SB;
-          const uint8_t* b = st + 2 * kDtTileA;
+      if (tid == 32) {
+        int j = 0;
+        for (int u = cta; ok && u < n_units; u += G, ++j) {
+          const int acc = nb == 2 ? (j & 1) : 0, use = nb == 2 ? (j >> 1) : j;
+          if (!mbar_wait(&tempty[acc], (use & 1) ^ 1, nullptr, hdr, 44)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t dg = tmem + kDtColGU + acc * 2 * Np, du = dg + Np;
+          for (int kb = 0; kb < KB_H; ++kb) {
+            int s;
+            if (!consume(s)) { ok = false; break; }
+            const uint8_t* st = ring + s * SB;
+            const uint8_t* b = st + 2 * kDtTileA;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(dg, sdesc(st + kk * 32), sdesc(b + kk * 32), idesc, (kb > kb0 || kk) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(dg, sdesc(st + kk * 32), sdesc(b + kk * 32), idesc, (kb || kk) ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(du, sdesc(st + kDtTileA + kk * 32), sdesc(b + kk * 32), idesc,
-                      (kb > kb0 || kk) ? 1u : 0u);
-          umma_commit(&empty[s]);
-          ++m_it;
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(du, sdesc(st + kDtTileA + kk * 32), sdesc(b + kk * 32), idesc, (kb || kk) ? 1u : 0u);
+            umma_commit(&empty[s]);
+            ++m_it;
+          }
+          if (!ok) break;
+          umma_commit(&tfull[acc]);
+          if (!mbar_wait(&hfull, j & 1, nullptr, hdr, 53)) { ok = false; break; }
+          tc_fence_after();
+          for (int mbd = 0; mbd < MB_H; ++mbd) {
+            int s;
+            if (!consume(s)) { ok = false; break; }
+            const uint8_t* st = ring + s * SB;
+            const uint32_t d = tmem + colD + mbd * Np;
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {           // (k-half, part) = (q >> 1, q & 1)
+              const uint8_t* a = st + (q >> 1) * kDtTileA;
+              const uint8_t* b = hs + (2 * (q & 1) + (q >> 1)) * xtile;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_bf16(d, sdesc(a + kk * 32), sdesc(b + kk * 32), idesc, (j || q || kk) ? 1u : 0u);
+            }
+            umma_commit(&empty[s]);
+            ++m_it;
+          }
+          if (!ok) break;
+          umma_commit(&hempty);
         }
-        if (!ok) break;
-        umma_commit(&tfull[acc]);
+        if (ok && j > 0) umma_commit(&dfull);
       }
-    }
-    if (epi) {
-      const int rl = quad * 32 + lane;
-      const int cbeg = half * (Np / 2), cend = cbeg + Np / 2;   // this warp's token columns
-      int local = 0;
-      for (int u = cta; ok && u < P.n_units; u += G, ++local) {
-        int ti, mb, kb0, kb1;
-        unit_of(u, ti, mb, kb0, kb1);
-        const int acc = local & 1;
-        // all epilogue warps leave together (they meet at named barriers below)
-        if (!epi_sync_and(warp_wait(&tfull[acc], (local >> 1) & 1, nullptr, hdr, 45))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t tg = tmem + lane_base + kDtColGU + acc * 2 * Np;
-        // compact loops: this code runs once per launch and unit, so its
-        // size (instruction fetch) matters more than its unrolling
-        if (P.s_up == 1) {
-          // h through a shared tile [part][t][row] and two TMA stores (rows
-          // past I are clipped by the store)
-          if (tid == kDtEpiLeader) bulk_wait_read();   // the previous unit's stores read it
-          epi_sync();
+      if (epi) {
+        const int rl = quad * 32 + lane;
+        const int cbeg = half * (Np / 2), cend = cbeg + Np / 2;   // this warp's token columns
+        // element (t, rl) of the h tiles: k-half rl / 64, column rl % 64 of
+        // row t, 16-byte chunks swizzled by t % 8
+        const int col = rl & 63;
+        uint8_t* hhi = hs + (rl >> 6) * xtile;
+        uint8_t* hlo = hhi + 2 * xtile;
+        int j = 0;
+        for (int u = cta; ok && u < n_units; u += G, ++j) {
+          const int ti = u / MB_I;
+          const int acc = nb == 2 ? (j & 1) : 0, use = nb == 2 ? (j >> 1) : j;
+          if (!warp_wait(&tfull[acc], use & 1, nullptr, hdr, 45)) { ok = false; break; }
+          if (j > 0 && !warp_wait(&hempty, (j - 1) & 1, nullptr, hdr, 54)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t tg = tmem + lane_base + kDtColGU + acc * 2 * Np;
 #pragma unroll 1
           for (int c0 = cbeg; c0 < cend; c0 += 8) {
             uint32_t gr[8], ur[8];
@@ -398,198 +384,431 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
             tmem_ld_32x32b_x8(tg + Np + c0, ur);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int t = c0 + j;
-              const float v = swiglu_fast(__uint_as_float(gr[j]), __uint_as_float(ur[j])) *
+            for (int jj = 0; jj < 8; ++jj) {
+              const int t = c0 + jj;
+              const float v = swiglu_fast(__uint_as_float(gr[jj]), __uint_as_float(ur[jj])) *
                               alpha[ti * Np + t];
               const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-              hstage[t * 128 + rl] = hi;
-              hstage[(Np + t) * 128 + rl] = __float2bfloat16_rn(v - __bfloat162float(hi));
+              const int off = t * 128 + ((((col >> 3) ^ (t & 7)) << 4) | ((col & 7) << 1));
+              *reinterpret_cast<__nv_bfloat16*>(hhi + off) = hi;
+              *reinterpret_cast<__nv_bfloat16*>(hlo + off) = __float2bfloat16_rn(v - __bfloat162float(hi));
             }
           }
           fence_proxy_async_smem();
-          epi_sync();
-          if (tid == kDtEpiLeader) {
-            tma_store_2d(&M.hps, hstage, mb * 128, (ti * 2) * Np);
-            tma_store_2d(&M.hps, hstage + Np * 128, mb * 128, (ti * 2 + 1) * Np);
-            bulk_commit();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&hfull);
+            mbar_arrive(&tempty[acc]);
           }
-        } else {
-          float* pg = A.pgu + static_cast<size_t>(u) * 2 * Np * 128;
+        }
+        // the CTA's partial of y: pd[cta][t][row], tokens t < T only
+        if (ok && j > 0) {
+          if (!warp_wait(&dfull, 0, nullptr, hdr, 49)) {
+            ok = false;
+          } else {
+            tc_fence_after();
+            float* pdst = A.pd + static_cast<size_t>(cta) * T * H + rl;
+            const int cstop = cend < T ? cend : T;
 #pragma unroll 1
-          for (int c0 = cbeg; c0 < cend; c0 += 8) {
-            uint32_t gr[8], ur[8];
-            tmem_ld_32x32b_x8(tg + c0, gr);
-            tmem_ld_32x32b_x8(tg + Np + c0, ur);
-            tmem_ld_wait();
+            for (int mbd = 0; mbd < MB_H; ++mbd) {
+#pragma unroll 1
+              for (int c0 = cbeg; c0 < cstop; c0 += 8) {
+                uint32_t r[8];
+                tmem_ld_32x32b_x8(tmem + lane_base + colD + mbd * Np + c0, r);
+                tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              pg[static_cast<size_t>(c0 + j) * 128 + rl] = __uint_as_float(gr[j]);
-              pg[static_cast<size_t>(Np + c0 + j) * 128 + rl] = __uint_as_float(ur[j]);
+                for (int jj = 0; jj < 8; ++jj)
+                  if (c0 + jj < T) pdst[static_cast<size_t>(c0 + jj) * H + mbd * 128] = __uint_as_float(r[jj]);
+              }
             }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
       }
-      if (tid == kDtEpiLeader) bulk_wait_all();   // h has reached global memory
+      tc_fence_before();
+      ok = __syncthreads_and(ok);
+      tc_fence_after();
     }
-    ok = __syncthreads_and(ok);
-  }
 
-  // ------------------------------------------------------------ h complete
-  unsigned round = 1;
-  if (ok) {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    ok = grid_barrier(hdr, 46, round++, nullptr);
-  }
-  if (ok && P.s_up > 1) {
-    // add the k-range partials of G and U in order (zeros past s_up change
-    // nothing), then as the direct path
-    const int blocks = P.nt * P.MB_I;
-    const int per_blk = Np * 128;
-    const int total = blocks * per_blk;
-    const int stride = G * kDtThreads;
-    for (int q0 = cta * kDtThreads + tid; q0 < total; q0 += 2 * stride) {
-      // every partial of two elements is requested before any is added
-      float pgv[2][kDtMaxSplit], puv[2][kDtMaxSplit];
+    // ---------------------------------------------------------- 4: y
+    // y = the partials of CTAs 0 .. Gp-1 added in CTA order.  Each CTA takes
+    // a contiguous range of 4-element quads of y; up to kDtMaxSlices threads
+    // share a quad (contiguous CTA slices), their sums added in slice order.
+    if (ok) ok = grid_barrier(hdr, 50, 1, &ticket);
+    if (ok) {
+      const int Gp = n_units < G ? n_units : G;
+      const int nq_all = T * H / 4;
+      const int q0 = static_cast<int>(static_cast<long long>(cta) * nq_all / G);
+      const int nq = static_cast<int>(static_cast<long long>(cta + 1) * nq_all / G) - q0;
+      if (nq > 0) {
+        int ns = kDtThreads / nq;
+        ns = ns < 1 ? 1 : (ns > kDtMaxSlices ? kDtMaxSlices : ns);
+        ns = ns > Gp ? Gp : ns;
+        float4* red = reinterpret_cast<float4*>(ring);        // [ns][nq]; the ring is idle now
+        const float4* pd4 = reinterpret_cast<const float4*>(A.pd) + q0;
+        for (int w = tid; w < nq * ns; w += kDtThreads) {
+          const int sl = w / nq, qi = w - sl * nq;
+          const int c0 = sl * Gp / ns, c1 = (sl + 1) * Gp / ns;
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int cb = c0; cb < c1; cb += kDtSumChunk) {
+            float4 part[kDtSumChunk];
 #pragma unroll
-      for (int w = 0; w < 2; ++w) {
-        const int q = q0 + w * stride;
-        const int blk = q / per_blk, rem = q - blk * per_blk;
-        const float* pg = A.pgu + static_cast<size_t>(blk * P.s_up) * 2 * per_blk + rem;
+            for (int w2 = 0; w2 < kDtSumChunk; ++w2)
+              part[w2] = cb + w2 < c1 ? __ldcg(pd4 + static_cast<size_t>(cb + w2) * nq_all + qi)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int kr = 0; kr < kDtMaxSplit; ++kr) {
-          const bool live = q < total && kr < P.s_up;
-          pgv[w][kr] = live ? pg[static_cast<size_t>(kr) * 2 * per_blk] : 0.f;
-          puv[w][kr] = live ? pg[static_cast<size_t>(kr) * 2 * per_blk + per_blk] : 0.f;
+            for (int w2 = 0; w2 < kDtSumChunk; ++w2) {
+              v.x += part[w2].x; v.y += part[w2].y; v.z += part[w2].z; v.w += part[w2].w;
+            }
+          }
+          red[w] = v;
+        }
+        __syncthreads();
+        for (int qi = tid; qi < nq; qi += kDtThreads) {
+          float4 v = red[qi];
+          for (int sl = 1; sl < ns; ++sl) {
+            const float4 o = red[sl * nq + qi];
+            v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+          }
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+          uint2 pk;
+          pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+          pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+          reinterpret_cast<uint2*>(A.y)[q0 + qi] = pk;
         }
       }
-#pragma unroll
-      for (int w = 0; w < 2; ++w) {
-        const int q = q0 + w * stride;
-        if (q >= total) break;
-        float g = 0.f, uu = 0.f;
-#pragma unroll
-        for (int kr = 0; kr < kDtMaxSplit; ++kr) {
-          g += pgv[w][kr];
-          uu += puv[w][kr];
-        }
-        const int blk = q / per_blk, rem = q - blk * per_blk;
-        const int t = rem >> 7, rl = rem & 127;
-        const int ti = blk / P.MB_I, mb = blk - ti * P.MB_I;
-        const int i = mb * 128 + rl;
-        if (i >= I) continue;
-        const float v = swiglu_fast(g, uu) * alpha[ti * Np + t];
-        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-        A.hp[(static_cast<size_t>(ti * 2) * Np + t) * I + i] = hi;
-        A.hp[(static_cast<size_t>(ti * 2 + 1) * Np + t) * I + i] = lo;
-      }
     }
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    ok = grid_barrier(hdr, 47, round++, nullptr);
-  }
+  } else {
+    DtPlan P;
+    P.nt = (ok && R.n_touched > 0) ? R.n_touched : 1;
+    P.MB_I = (I + 127) / 128;
+    P.MB_H = H / 128;
+    P.KB_H = KB_H;
+    P.KB_I = I / 64;
+    {
+      // split K only for long rows (>= 24 k-blocks), keeping ranges of at least
+      // 12 k-blocks: a shorter stream finishes sooner than the extra grid
+      // barrier and the partial sums cost
+      const int blocks = P.nt * P.MB_I;
+      const int max_split = P.KB_H / 12 < 1 ? 1 : (P.KB_H / 12 > kDtMaxSplit ? kDtMaxSplit : P.KB_H / 12);
+      int s_up = (G + blocks - 1) / blocks;
+      s_up = s_up < 1 ? 1 : (s_up > max_split ? max_split : s_up);
+      P.s_up = s_up;
+      P.n_units = blocks * s_up;
+    }
+    P.per_mb = P.nt * P.KB_I;
+    P.F = P.MB_H * P.per_mb;
+    // the down tiles go to the first Gd CTAs, at least three per CTA
+    const int Gd = (P.F + 2) / 3 < G ? (P.F + 2) / 3 : G;
+    const int r0 = cta < Gd ? dt_range_start(cta, P.F, Gd) : P.F;
+    const int r1 = cta < Gd ? dt_range_start(cta + 1, P.F, Gd) : P.F;
+    const int my_down = r1 - r0;
+    const int n_pre = my_down < S ? my_down : S;     // Wd tiles requested before the barrier
+    int pre_it0 = 0;                                 // producer: stage use of the first of them
+    // contributors of every output m-block, for the final reduction
+    for (int c = tid; c < Gd; c += kDtThreads) {
+      const int s0 = dt_range_start(c, P.F, Gd);
+      s_first_mb[c] = dt_range_start(c + 1, P.F, Gd) > s0 ? s0 / P.per_mb : -1;
+    }
+    for (int mb = tid; mb < P.MB_H; mb += kDtThreads) {
+      s_c0[mb] = dt_cta_of(mb * P.per_mb, P.F, Gd);
+      s_c1[mb] = dt_cta_of(mb * P.per_mb + P.per_mb - 1, P.F, Gd);
+    }
 
-  // ------------------------------------------------------------ 3: down
-  // stage = Wd tile at 0, Hp high part at 16 KiB, Hp remainder after it
-  if (ok) {
-    if (tid == 0) {
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      for (int j = 0; ok && j < my_down; ++j) {
-        int mbd, ti, kb, s;
-        tile_of(r0 + j, mbd, ti, kb);
-        if (j < n_pre) {
-          s = (pre_it0 + j) % S;                  // Wd already requested, bytes armed
-        } else {
+    // unit u -> (touched index, m-block, k-block range)
+    auto unit_of = [&](int u, int& ti, int& mb, int& kb0, int& kb1) {
+      const int blk = u / P.s_up, kr = u - blk * P.s_up;
+      ti = blk / P.MB_I;
+      mb = blk - ti * P.MB_I;
+      kb0 = kr * P.KB_H / P.s_up;
+      kb1 = (kr + 1) * P.KB_H / P.s_up;
+    };
+    auto tile_of = [&](int f, int& mbd, int& ti, int& kb) {
+      mbd = f / P.per_mb;
+      const int rem = f - mbd * P.per_mb;
+      ti = rem / P.KB_I;
+      kb = rem - ti * P.KB_I;
+    };
+
+    // ------------------------------------------------------------ 2: gate/up
+    // stage = Wg tile at 0, Wu tile at 16 KiB, x tile (B, N = Np) at 32 KiB
+    if (ok) {
+      if (tid == 0) {
+        for (int u = cta; ok && u < P.n_units; u += G) {
+          int ti, mb, kb0, kb1;
+          unit_of(u, ti, mb, kb0, kb1);
+          const int e = R.touched[ti];
+          for (int kb = kb0; kb < kb1; ++kb) {
+            int s;
+            if (!acquire(s)) { ok = false; break; }
+            uint8_t* st = ring + s * SB;
+            mbar_arrive_expect_tx(&full[s], 2 * kDtTileA + xtile);
+            tma_load_2d(st, &M.wg[e], &full[s], kb * 64, mb * 128);
+            tma_load_2d(st + kDtTileA, &M.wu[e], &full[s], kb * 64, mb * 128);
+            tma_load_2d(st + 2 * kDtTileA, &M.x, &full[s], kb * 64, 0);
+            ++p_it;
+          }
+        }
+        pre_it0 = p_it;
+        for (int j = 0; ok && j < n_pre; ++j) {
+          int mbd, ti, kb, s;
+          tile_of(r0 + j, mbd, ti, kb);
           if (!acquire(s)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[s], kDtTileA + 2 * xtile);
+          mbar_arrive_expect_tx(&full[s], kDtTileA + 2 * xtile);   // the Hp tiles follow later
           tma_load_2d(ring + s * SB, &M.wd[R.touched[ti]], &full[s], kb * 64, mbd * 128);
           ++p_it;
         }
-        uint8_t* b = ring + s * SB + kDtTileA;
-        tma_load_2d(b, &M.hp, &full[s], kb * 64, (ti * 2) * Np);
-        tma_load_2d(b + xtile, &M.hp, &full[s], kb * 64, (ti * 2 + 1) * Np);
       }
-    }
-    if (tid == 32) {
-      int seg = -1, prev = -1;
-      bool first = true;
-      for (int j = 0; ok && j < my_down; ++j) {
-        int mbd, ti, kb, s;
-        tile_of(r0 + j, mbd, ti, kb);
-        if (mbd != prev) {
-          if (seg >= 0) umma_commit(&dfull);
-          ++seg;
-          prev = mbd;
-          if (!mbar_wait(&dempty, (seg & 1) ^ 1, nullptr, hdr, 48)) { ok = false; break; }
+      if (tid == 32) {
+        int local = 0;
+        for (int u = cta; ok && u < P.n_units; u += G, ++local) {
+          int ti, mb, kb0, kb1;
+          unit_of(u, ti, mb, kb0, kb1);
+          const int acc = local & 1;
+          if (!mbar_wait(&tempty[acc], ((local >> 1) & 1) ^ 1, nullptr, hdr, 44)) { ok = false; break; }
           tc_fence_after();
-          first = true;
+          const uint32_t dg = tmem + kDtColGU + acc * 2 * Np, du = dg + Np;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            int s;
+            if (!consume(s)) { ok = false; break; }
+            const uint8_t* st = ring + s * SB;
+            const uint8_t* b = st + 2 * kDtTileA;
+  #pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(dg, sdesc(st + kk * 32), sdesc(b + kk * 32), idesc, (kb > kb0 || kk) ? 1u : 0u);
+  #pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(du, sdesc(st + kDtTileA + kk * 32), sdesc(b + kk * 32), idesc,
+                        (kb > kb0 || kk) ? 1u : 0u);
+            umma_commit(&empty[s]);
+            ++m_it;
+          }
+          if (!ok) break;
+          umma_commit(&tfull[acc]);
         }
-        if (!consume(s)) { ok = false; break; }
-        const uint8_t* a = ring + s * SB;
-        const uint8_t* b = a + kDtTileA;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16(tmem + kDtColD, sdesc(a + kk * 32), sdesc(b + kk * 32), idesc,
-                    (!first || kk) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16(tmem + kDtColD, sdesc(a + kk * 32), sdesc(b + xtile + kk * 32), idesc, 1u);
-        first = false;
-        umma_commit(&empty[s]);
-        ++m_it;
       }
-      if (ok && seg >= 0) umma_commit(&dfull);
-    }
-    if (epi) {
-      const int rl = quad * 32 + lane;
-      const int cbeg = half * (Np / 2), cend = cbeg + Np / 2;
-      const int n_seg = my_down > 0 ? (r1 - 1) / P.per_mb - r0 / P.per_mb + 1 : 0;
-      for (int seg = 0; ok && seg < n_seg; ++seg) {
-        if (!warp_wait(&dfull, seg & 1, nullptr, hdr, 49)) { ok = false; break; }
-        tc_fence_after();
-        float* pdst = A.pd + (static_cast<size_t>(cta) * kDtMaxSeg + seg) * Np * 128;
-#pragma unroll 1
-        for (int c0 = cbeg; c0 < cend; c0 += 8) {
-          uint32_t r[8];
-          tmem_ld_32x32b_x8(tmem + lane_base + kDtColD + c0, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 8; ++j) pdst[static_cast<size_t>(c0 + j) * 128 + rl] = __uint_as_float(r[j]);
+      if (epi) {
+        const int rl = quad * 32 + lane;
+        const int cbeg = half * (Np / 2), cend = cbeg + Np / 2;   // this warp's token columns
+        int local = 0;
+        for (int u = cta; ok && u < P.n_units; u += G, ++local) {
+          int ti, mb, kb0, kb1;
+          unit_of(u, ti, mb, kb0, kb1);
+          const int acc = local & 1;
+          // all epilogue warps leave together (they meet at named barriers below)
+          if (!epi_sync_and(warp_wait(&tfull[acc], (local >> 1) & 1, nullptr, hdr, 45))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t tg = tmem + lane_base + kDtColGU + acc * 2 * Np;
+          // compact loops: this code runs once per launch and unit, so its
+          // size (instruction fetch) matters more than its unrolling
+          if (P.s_up == 1) {
+            // h through a shared tile [part][t][row] and two TMA stores (rows
+            // past I are clipped by the store)
+            if (tid == kDtEpiLeader) bulk_wait_read();   // the previous unit's stores read it
+            epi_sync();
+  #pragma unroll 1
+            for (int c0 = cbeg; c0 < cend; c0 += 8) {
+              uint32_t gr[8], ur[8];
+              tmem_ld_32x32b_x8(tg + c0, gr);
+              tmem_ld_32x32b_x8(tg + Np + c0, ur);
+              tmem_ld_wait();
+  #pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int t = c0 + j;
+                const float v = swiglu_fast(__uint_as_float(gr[j]), __uint_as_float(ur[j])) *
+                                alpha[ti * Np + t];
+                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+                hstage[t * 128 + rl] = hi;
+                hstage[(Np + t) * 128 + rl] = __float2bfloat16_rn(v - __bfloat162float(hi));
+              }
+            }
+            fence_proxy_async_smem();
+            epi_sync();
+            if (tid == kDtEpiLeader) {
+              tma_store_2d(&M.hps, hstage, mb * 128, (ti * 2) * Np);
+              tma_store_2d(&M.hps, hstage + Np * 128, mb * 128, (ti * 2 + 1) * Np);
+              bulk_commit();
+            }
+          } else {
+            float* pg = A.pgu + static_cast<size_t>(u) * 2 * Np * 128;
+  #pragma unroll 1
+            for (int c0 = cbeg; c0 < cend; c0 += 8) {
+              uint32_t gr[8], ur[8];
+              tmem_ld_32x32b_x8(tg + c0, gr);
+              tmem_ld_32x32b_x8(tg + Np + c0, ur);
+              tmem_ld_wait();
+  #pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                pg[static_cast<size_t>(c0 + j) * 128 + rl] = __uint_as_float(gr[j]);
+                pg[static_cast<size_t>(Np + c0 + j) * 128 + rl] = __uint_as_float(ur[j]);
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[acc]);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&dempty);
+        if (tid == kDtEpiLeader) bulk_wait_all();   // h has reached global memory
       }
+      ok = __syncthreads_and(ok);
     }
-    ok = __syncthreads_and(ok);
-  }
 
-  // ------------------------------------------------------------ 4: y
-  unsigned ticket = 0xffffffffu;
-  if (ok) ok = grid_barrier(hdr, 50, round, &ticket);
-  if (ok) {
-    const int total = T * H;
-    for (int q = cta * kDtThreads + tid; q < total; q += G * kDtThreads) {
-      const int t = q / H, j = q - t * H;
-      const int mbd = j >> 7, rl = j & 127;
-      float v = 0.f;
-      for (int cb = s_c0[mbd]; cb <= s_c1[mbd]; cb += kDtReduceChunk) {
-        float part[kDtReduceChunk];
-#pragma unroll
-        for (int w = 0; w < kDtReduceChunk; ++w) {
-          const int c = cb + w;
-          const int fm = c <= s_c1[mbd] ? s_first_mb[c] : -1;   // -1: past the end or empty range
-          part[w] = fm >= 0 ? A.pd[((static_cast<size_t>(c) * kDtMaxSeg + (mbd - fm)) * Np + t) * 128 + rl]
-                            : 0.f;
-        }
-#pragma unroll
-        for (int w = 0; w < kDtReduceChunk; ++w) v += part[w];
-      }
-      static_cast<__nv_bfloat16*>(A.y)[q] = __float2bfloat16_rn(v);
+    // ------------------------------------------------------------ h complete
+    unsigned round = 1;
+    if (ok) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      ok = grid_barrier(hdr, 46, round++, nullptr);
     }
+    if (ok && P.s_up > 1) {
+      // add the k-range partials of G and U in order (zeros past s_up change
+      // nothing), then as the direct path
+      const int blocks = P.nt * P.MB_I;
+      const int per_blk = Np * 128;
+      const int total = blocks * per_blk;
+      const int stride = G * kDtThreads;
+      for (int q0 = cta * kDtThreads + tid; q0 < total; q0 += 2 * stride) {
+        // every partial of two elements is requested before any is added
+        float pgv[2][kDtMaxSplit], puv[2][kDtMaxSplit];
+  #pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          const int q = q0 + w * stride;
+          const int blk = q / per_blk, rem = q - blk * per_blk;
+          const float* pg = A.pgu + static_cast<size_t>(blk * P.s_up) * 2 * per_blk + rem;
+  #pragma unroll
+          for (int kr = 0; kr < kDtMaxSplit; ++kr) {
+            const bool live = q < total && kr < P.s_up;
+            pgv[w][kr] = live ? pg[static_cast<size_t>(kr) * 2 * per_blk] : 0.f;
+            puv[w][kr] = live ? pg[static_cast<size_t>(kr) * 2 * per_blk + per_blk] : 0.f;
+          }
+        }
+  #pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          const int q = q0 + w * stride;
+          if (q >= total) break;
+          float g = 0.f, uu = 0.f;
+  #pragma unroll
+          for (int kr = 0; kr < kDtMaxSplit; ++kr) {
+            g += pgv[w][kr];
+            uu += puv[w][kr];
+          }
+          const int blk = q / per_blk, rem = q - blk * per_blk;
+          const int t = rem >> 7, rl = rem & 127;
+          const int ti = blk / P.MB_I, mb = blk - ti * P.MB_I;
+          const int i = mb * 128 + rl;
+          if (i >= I) continue;
+          const float v = swiglu_fast(g, uu) * alpha[ti * Np + t];
+          const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+          A.hp[(static_cast<size_t>(ti * 2) * Np + t) * I + i] = hi;
+          A.hp[(static_cast<size_t>(ti * 2 + 1) * Np + t) * I + i] = lo;
+        }
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      ok = grid_barrier(hdr, 47, round++, nullptr);
+    }
+
+    // ------------------------------------------------------------ 3: down
+    // stage = Wd tile at 0, Hp high part at 16 KiB, Hp remainder after it
+    if (ok) {
+      if (tid == 0) {
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        for (int j = 0; ok && j < my_down; ++j) {
+          int mbd, ti, kb, s;
+          tile_of(r0 + j, mbd, ti, kb);
+          if (j < n_pre) {
+            s = (pre_it0 + j) % S;                  // Wd already requested, bytes armed
+          } else {
+            if (!acquire(s)) { ok = false; break; }
+            mbar_arrive_expect_tx(&full[s], kDtTileA + 2 * xtile);
+            tma_load_2d(ring + s * SB, &M.wd[R.touched[ti]], &full[s], kb * 64, mbd * 128);
+            ++p_it;
+          }
+          uint8_t* b = ring + s * SB + kDtTileA;
+          tma_load_2d(b, &M.hp, &full[s], kb * 64, (ti * 2) * Np);
+          tma_load_2d(b + xtile, &M.hp, &full[s], kb * 64, (ti * 2 + 1) * Np);
+        }
+      }
+      if (tid == 32) {
+        int seg = -1, prev = -1;
+        bool first = true;
+        for (int j = 0; ok && j < my_down; ++j) {
+          int mbd, ti, kb, s;
+          tile_of(r0 + j, mbd, ti, kb);
+          if (mbd != prev) {
+            if (seg >= 0) umma_commit(&dfull);
+            ++seg;
+            prev = mbd;
+            if (!mbar_wait(&dempty, (seg & 1) ^ 1, nullptr, hdr, 48)) { ok = false; break; }
+            tc_fence_after();
+            first = true;
+          }
+          if (!consume(s)) { ok = false; break; }
+          const uint8_t* a = ring + s * SB;
+          const uint8_t* b = a + kDtTileA;
+  #pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + kDtColD, sdesc(a + kk * 32), sdesc(b + kk * 32), idesc,
+                      (!first || kk) ? 1u : 0u);
+  #pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + kDtColD, sdesc(a + kk * 32), sdesc(b + xtile + kk * 32), idesc, 1u);
+          first = false;
+          umma_commit(&empty[s]);
+          ++m_it;
+        }
+        if (ok && seg >= 0) umma_commit(&dfull);
+      }
+      if (epi) {
+        const int rl = quad * 32 + lane;
+        const int cbeg = half * (Np / 2), cend = cbeg + Np / 2;
+        const int n_seg = my_down > 0 ? (r1 - 1) / P.per_mb - r0 / P.per_mb + 1 : 0;
+        for (int seg = 0; ok && seg < n_seg; ++seg) {
+          if (!warp_wait(&dfull, seg & 1, nullptr, hdr, 49)) { ok = false; break; }
+          tc_fence_after();
+          float* pdst = A.pd + (static_cast<size_t>(cta) * kDtMaxSeg + seg) * Np * 128;
+  #pragma unroll 1
+          for (int c0 = cbeg; c0 < cend; c0 += 8) {
+            uint32_t r[8];
+            tmem_ld_32x32b_x8(tmem + lane_base + kDtColD + c0, r);
+            tmem_ld_wait();
+  #pragma unroll
+            for (int j = 0; j < 8; ++j) pdst[static_cast<size_t>(c0 + j) * 128 + rl] = __uint_as_float(r[j]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&dempty);
+        }
+      }
+      ok = __syncthreads_and(ok);
+    }
+
+    // ------------------------------------------------------------ 4: y
+    if (ok) ok = grid_barrier(hdr, 50, round, &ticket);
+    if (ok) {
+      const int total = T * H;
+      for (int q = cta * kDtThreads + tid; q < total; q += G * kDtThreads) {
+        const int t = q / H, j = q - t * H;
+        const int mbd = j >> 7, rl = j & 127;
+        float v = 0.f;
+        for (int cb = s_c0[mbd]; cb <= s_c1[mbd]; cb += kDtReduceChunk) {
+          float part[kDtReduceChunk];
+  #pragma unroll
+          for (int w = 0; w < kDtReduceChunk; ++w) {
+            const int c = cb + w;
+            const int fm = c <= s_c1[mbd] ? s_first_mb[c] : -1;   // -1: past the end or empty range
+            part[w] = fm >= 0 ? A.pd[((static_cast<size_t>(c) * kDtMaxSeg + (mbd - fm)) * Np + t) * 128 + rl]
+                              : 0.f;
+          }
+  #pragma unroll
+          for (int w = 0; w < kDtReduceChunk; ++w) v += part[w];
+        }
+        static_cast<__nv_bfloat16*>(A.y)[q] = __float2bfloat16_rn(v);
+      }
+    }
+
   }
 
   // ------------------------------------------------------------ teardown
@@ -617,6 +836,7 @@ namespace {
 
 struct DtLayout {
   int Np, Epad, nt_max, stages;
+  int fused, gu_bufs;                   // down product per unit in the same CTA
   size_t stage, alpha_off, hstage_off, smem;   // shared memory
   size_t hp, pgu, pd, total;            // workspace (after the header)
 };
@@ -642,6 +862,12 @@ bool dt_layout(int T, int H, int I, int E, int k, DtLayout& L) {
   L.smem = L.hstage_off + hstage + 1024;             // 1 KiB: alignment slack
   const int G = kDtMaxCtas;
   const int blocks = L.nt_max * ((I + 127) / 128);
+  // fused: the (G, U) accumulators and y^T for all H rows fit in TMEM, and
+  // there are units enough to keep most SMs streaming (a fused unit cannot be
+  // split along K; the dense FFN at H = 768 has only I / 128 of them)
+  const int MB_H = H / 128;
+  L.fused = ((MB_H + 2) * L.Np <= static_cast<int>(kDtTmemCols) && blocks >= kDtFusedMinUnits) ? 1 : 0;
+  L.gu_bufs = (MB_H + 4) * L.Np <= static_cast<int>(kDtTmemCols) ? 2 : 1;
   const int units = blocks + G;                      // blocks * ceil(G / blocks) < blocks + G
   if (H / 128 > G || H / 128 > kDtMaxMB) return false;
   {
@@ -656,9 +882,15 @@ bool dt_layout(int T, int H, int I, int E, int k, DtLayout& L) {
     const long long F = static_cast<long long>(H / 128) * L.nt_max * (I / 64);
     if ((F + 1) * G >= (1ll << 31)) return false;    // down-range arithmetic in 32 bits
   }
-  L.hp = round_up(static_cast<size_t>(L.nt_max) * 2 * L.Np * I * 2, 256);
-  L.pgu = round_up(static_cast<size_t>(units) * 2 * L.Np * 128 * 4, 256);
-  L.pd = round_up(static_cast<size_t>(G) * kDtMaxSeg * L.Np * 128 * 4, 256);
+  if (L.fused) {
+    L.hp = 0;
+    L.pgu = 0;
+    L.pd = round_up(static_cast<size_t>(G) * T * H * 4, 256);   // one partial of y per CTA
+  } else {
+    L.hp = round_up(static_cast<size_t>(L.nt_max) * 2 * L.Np * I * 2, 256);
+    L.pgu = round_up(static_cast<size_t>(units) * 2 * L.Np * 128 * 4, 256);
+    L.pd = round_up(static_cast<size_t>(G) * kDtMaxSeg * L.Np * 128 * 4, 256);
+  }
   L.total = L.hp + L.pgu + L.pd;
   return true;
 }
@@ -673,17 +905,19 @@ cudaError_t decode_tc_impl(const DtLayout& L, const void* x, const void* Wr,
   const int T = A.T, H = A.H, I = A.I, nw = A.moe ? A.E : 1;
   if (!make_map_16(&m.x, x, H, T, L.Np, false)) return cudaErrorInvalidValue;
   if (A.moe && !make_map_16(&m.wr, Wr, H, A.E, L.Epad, false)) return cudaErrorInvalidValue;
-  if (!make_map_16(&m.hp, A.hp, I, static_cast<uint64_t>(L.nt_max) * 2 * L.Np, L.Np, false))
-    return cudaErrorInvalidValue;
-  if (!make_map_16(&m.hps, A.hp, I, static_cast<uint64_t>(L.nt_max) * 2 * L.Np, L.Np, false, 128,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
-    return cudaErrorInvalidValue;
+  if (!L.fused) {
+    if (!make_map_16(&m.hp, A.hp, I, static_cast<uint64_t>(L.nt_max) * 2 * L.Np, L.Np, false))
+      return cudaErrorInvalidValue;
+    if (!make_map_16(&m.hps, A.hp, I, static_cast<uint64_t>(L.nt_max) * 2 * L.Np, L.Np, false, 128,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  }
   for (int e = 0; e < nw; ++e) {
     if (!make_map_16(&m.wg[e], Wg[e], H, I, 128, false)) return cudaErrorInvalidValue;
     if (!make_map_16(&m.wu[e], Wu[e], H, I, 128, false)) return cudaErrorInvalidValue;
     if (!make_map_16(&m.wd[e], Wd[e], I, H, 128, false)) return cudaErrorInvalidValue;
   }
-  auto fn = decode_tc_kernel<MAXW>;
+  auto fn = L.fused ? decode_tc_kernel<MAXW, true> : decode_tc_kernel<MAXW, false>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), L.smem);
   if (e != cudaSuccess) return e;
   int fit = 0;
@@ -732,6 +966,7 @@ cudaError_t launch_decode_tc(const void* x, const void* Wr, const float* bias,
   A.pd = reinterpret_cast<float*>(base + L.hp + L.pgu);
   A.y = y; A.hdr = hdr;
   A.stages = L.stages;
+  A.gu_bufs = L.gu_bufs;
   A.Epad = L.Epad;
   A.stage_bytes = static_cast<uint32_t>(L.stage);
   A.hstage_off = static_cast<uint32_t>(L.hstage_off);

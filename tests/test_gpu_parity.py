@@ -166,7 +166,8 @@ def test_dense_stream_tc_path(T):
     assert rel_err(y.double().cpu().numpy(), ref) <= Y_TOL["bf16"]
 
 
-@pytest.mark.parametrize("T,H,I", [(7, 256, 384), (33, 384, 320), (64, 128, 64)])
+@pytest.mark.parametrize("T,H,I", [(7, 256, 384), (33, 384, 320), (64, 128, 64), (64, 1024, 256),
+                                   (20, 2048, 192)])
 def test_dense_stream_tc_small_shapes(T, H, I):
     """Several output m-blocks, a ragged last block of I (320 = 2.5 x 128) and
     the smallest admissible shape."""
@@ -180,10 +181,23 @@ def test_dense_stream_tc_small_shapes(T, H, I):
 @pytest.mark.parametrize("T,E,k,bias", [(1, 8, 2, None), (4, 8, 2, (1.5, 0.5, 0, 0, 0, 0, 0, 0)),
                                         (16, 8, 2, None), (33, 4, 1, None),
                                         (64, 8, 2, (1.5, 0.5, 0, 0, 0, 0, 0, 0)), (9, 6, 3, None),
-                                        (20, 1, 1, None), (12, 16, 4, None)])
+                                        (20, 1, 1, None), (12, 16, 4, None), (64, 16, 4, None),
+                                        (16, 8, 2, (8.0, 8.0, 0, 0, 0, 0, 0, 0))])
 def test_moe_stream_tc_path(T, E, k, bias):
+    """The last case routes every token to experts 0 and 1: the experts
+    streamed before the routing is known but never selected add nothing."""
     full_moe_check(moe_inputs(T, 768, 2432, E, "bf16", seed=100 + T, bias=bias), k, 0.01, "bf16",
                    path="stream_tc")
+
+
+@pytest.mark.parametrize("T,H,I,E,k", [(64, 1024, 256, 4, 2), (48, 1152, 256, 4, 2),
+                                       (16, 256, 192, 32, 4)])
+def test_moe_stream_tc_shapes(T, H, I, E, k):
+    """The first two: y^T does not fit in TMEM beside the gate/up accumulators,
+    so h goes through global memory between the two products.  The last: the
+    down product runs per (expert, I-block) unit, with a half-empty last
+    I-block (192 = 1.5 x 128)."""
+    full_moe_check(moe_inputs(T, H, I, E, "bf16", seed=130 + T), k, 0.01, "bf16", path="stream_tc")
 
 
 def test_moe_stream_tc_deterministic():
