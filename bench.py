@@ -39,8 +39,8 @@ DECODE_MAX_T = 64         # token counts the library streams weights for (bf16)
 
 def decode_kernel_name(w):
     """The streaming kernel the automatic path picks for this workload: CUDA
-    cores up to 8 tokens (dense) or 2 tokens (MoE), tensor cores beyond."""
-    simt = w.T <= (8 if w.kind == "dense" else 2)
+    cores up to 6 tokens (dense) or 2 tokens (MoE), tensor cores beyond."""
+    simt = w.T <= (6 if w.kind == "dense" else 2)
     return ("decode_ffn_kernel (CUDA-core weight streaming)" if simt
             else "decode_tc_kernel (tcgen05 weight streaming)")
 

@@ -136,10 +136,10 @@ size_t moe_ws_bytes(int64_t T, int H, int I, int E, int k, int dtype) {
 
 // AUTO: fp32 -> CUDA-core kernels.  bf16 -> weight streaming for decode-sized
 // T (every weight row read once): on the CUDA cores for the smallest T (up to
-// 8 tokens dense, 2 tokens MoE: their cost grows with the tokens and the
+// 6 tokens dense, 2 tokens MoE: their cost grows with the tokens and the
 // touched experts), on the tensor cores up to kDecodeTcMaxT (a fixed cost of
-// two grid barriers and the partial sums); tensor-core GEMMs beyond.
-inline int64_t stream_simt_auto_max_t(int E) { return E == 1 ? 8 : 2; }
+// one to three grid barriers and the partial sums); tensor-core GEMMs beyond.
+inline int64_t stream_simt_auto_max_t(int E) { return E == 1 ? 6 : 2; }
 int resolve_path(int path, int dtype, int64_t T, int H, int I, int E, int k) {
   if (path != MM_PATH_AUTO) return path;
   if (dtype == kDtypeF32) return MM_PATH_SIMT;

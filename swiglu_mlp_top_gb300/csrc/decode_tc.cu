@@ -26,9 +26,16 @@
 //      rounds y to bf16 once (deterministic; the weighted sum over the
 //      selected experts is part of the fp32 accumulation).
 //
-// Warp roles (192 threads): warp 0 lane 0 issues TMA, warp 1 lane 0 issues
-// UMMA and owns TMEM, warps 2-5 are the epilogue (TMEM lane quadrant
-// warp % 4).  All waits are bounded.
+// Fused variant (many (expert, I-block) units, few tokens, y^T for all H rows
+// fits in TMEM beside the gate/up accumulators): each unit also streams its
+// 128 columns of Wd_e and multiplies them by its own h, kept in shared memory
+// as the B operand; a CTA's units accumulate y^T in TMEM, the CTA writes one
+// fp32 partial of y, and after a single grid barrier the partials are added in
+// CTA order.  h never reaches global memory.
+//
+// Warp roles (320 threads): warp 0 lane 0 issues TMA, warp 1 lane 0 issues
+// UMMA and owns TMEM, warps 2-9 are the epilogue (TMEM lane quadrant
+// warp % 4, token-column half (warp - 2) / 4).  All waits are bounded.
 #include <algorithm>
 #include <mutex>
 
@@ -51,6 +58,7 @@ constexpr int kDtMaxSplit = 4;                  // k-ranges per gate/up block at
 constexpr int kDtReduceChunk = 32;              // partials requested at once in the final sum
 constexpr size_t kDtSmemBudget = 196 * 1024;   // dynamic; static use is ~27 KiB
 constexpr int kDtFusedMinUnits = 64;            // fused variant: (expert, I-block) units at least
+constexpr int kDtFusedMaxNp = 32;               // fused variant: padded tokens at most
 constexpr int kDtMaxSlices = 8;                 // fused: partial sums per output quad at most
 constexpr int kDtSumChunk = 8;                  // fused: partials requested at once
 
@@ -486,11 +494,13 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
     P.KB_H = KB_H;
     P.KB_I = I / 64;
     {
-      // split K only for long rows (>= 24 k-blocks), keeping ranges of at least
-      // 12 k-blocks: a shorter stream finishes sooner than the extra grid
+      // split K when fewer than half the CTAs would stream (ranges of at
+      // least 3 k-blocks), else only for long rows (ranges of at least 12
+      // k-blocks): a shorter stream finishes sooner than the extra grid
       // barrier and the partial sums cost
       const int blocks = P.nt * P.MB_I;
-      const int max_split = P.KB_H / 12 < 1 ? 1 : (P.KB_H / 12 > kDtMaxSplit ? kDtMaxSplit : P.KB_H / 12);
+      const int kmin = blocks * 2 <= G ? 3 : 12;
+      const int max_split = P.KB_H / kmin < 1 ? 1 : (P.KB_H / kmin > kDtMaxSplit ? kDtMaxSplit : P.KB_H / kmin);
       int s_up = (G + blocks - 1) / blocks;
       s_up = s_up < 1 ? 1 : (s_up > max_split ? max_split : s_up);
       P.s_up = s_up;
@@ -862,11 +872,14 @@ bool dt_layout(int T, int H, int I, int E, int k, DtLayout& L) {
   L.smem = L.hstage_off + hstage + 1024;             // 1 KiB: alignment slack
   const int G = kDtMaxCtas;
   const int blocks = L.nt_max * ((I + 127) / 128);
-  // fused: the (G, U) accumulators and y^T for all H rows fit in TMEM, and
-  // there are units enough to keep most SMs streaming (a fused unit cannot be
-  // split along K; the dense FFN at H = 768 has only I / 128 of them)
+  // fused: the (G, U) accumulators and y^T for all H rows fit in TMEM, there
+  // are units enough to keep most SMs streaming (a fused unit cannot be split
+  // along K; the dense FFN at H = 768 has only I / 128 of them), and the
+  // per-CTA partials of y (T * H * 4 bytes each) stay small: at 64 tokens
+  // writing and adding them costs more than h's round trip through memory
   const int MB_H = H / 128;
-  L.fused = ((MB_H + 2) * L.Np <= static_cast<int>(kDtTmemCols) && blocks >= kDtFusedMinUnits) ? 1 : 0;
+  L.fused = ((MB_H + 2) * L.Np <= static_cast<int>(kDtTmemCols) && blocks >= kDtFusedMinUnits &&
+             L.Np <= kDtFusedMaxNp) ? 1 : 0;
   L.gu_bufs = (MB_H + 4) * L.Np <= static_cast<int>(kDtTmemCols) ? 2 : 1;
   const int units = blocks + G;                      // blocks * ceil(G / blocks) < blocks + G
   if (H / 128 > G || H / 128 > kDtMaxMB) return false;

@@ -167,10 +167,11 @@ def test_dense_stream_tc_path(T):
 
 
 @pytest.mark.parametrize("T,H,I", [(7, 256, 384), (33, 384, 320), (64, 128, 64), (64, 1024, 256),
-                                   (20, 2048, 192)])
+                                   (20, 2048, 192), (17, 1792, 8192)])
 def test_dense_stream_tc_small_shapes(T, H, I):
-    """Several output m-blocks, a ragged last block of I (320 = 2.5 x 128) and
-    the smallest admissible shape."""
+    """Several output m-blocks, a ragged last block of I (320 = 2.5 x 128),
+    the smallest admissible shape, split gate/up ranges, and (the last) the
+    down product per I-block with one (G, U) TMEM buffer."""
     inp = make_inputs(T, H, I, "bf16", seed=90 + T)
     g = to_dev(inp)
     y = mm.swiglu_ffn(g["x"], g["Wg"], g["Wu"], g["Wd"], path="stream_tc")
