@@ -49,7 +49,9 @@ def decode_kernel_name(w):
 # None where no capture of the current kernel exists.
 GATEUP_TRAFFIC_BYTES = {"moe_e8k2_t16384_skew": 163.401216e6 + 128.745472e6}
 # The same for the decode kernel that streams the weights (one launch per step).
-DECODE_TRAFFIC_BYTES = {"decode_moe_e8k2_t64": 89.886976e6 + 3.358208e6,
+DECODE_TRAFFIC_BYTES = {"decode_moe_e8k2_t64": 89.88672e6 + 3.149824e6,
+                        "decode_moe_e8k2_t16": 89.779456e6 + 2.938368e6,
+                        "decode_dense_t16": 11.350272e6,
                         "decode_dense_t1": 11.30624e6}
 
 
