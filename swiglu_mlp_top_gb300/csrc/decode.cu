@@ -68,6 +68,16 @@ __device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t
       : "memory");
 }
 
+// The same with an L2 cache policy (the streamed weights: evict first).
+__device__ __forceinline__ void bulk_load_hint(void* sdst, const void* gsrc, uint32_t bytes,
+                                               uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(sdst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // One gate/up row i of expert e for m <= NT assignments (list): the lanes
 // split H in chunks of 8, the row's Wg and Wu chunks are widened once and
 // applied to every token's fp32 x chunk.
@@ -230,6 +240,7 @@ decode_ffn_kernel(const DecodeArgs A) {
   int up_used = 0, wd_used = 0, h_used = 0;
   int n_touched = 1, my_up = 0, my_wd = 0;
 
+  const uint64_t pol = l2_evict_first_policy();     // weights: read once per launch
   auto issue_up = [&](int it) {
     const int u = blockIdx.x + it * G;
     const int e = moe ? R.touched[u / slices] : 0;
@@ -238,9 +249,10 @@ decode_ffn_kernel(const DecodeArgs A) {
     unsigned char* dst = ring + (it % P.ring) * stage;
     uint64_t* b = &ring_bar[it % P.ring];
     mbar_arrive_expect_tx(b, 2 * bytes);
-    bulk_load(dst, static_cast<const __nv_bfloat16*>(A.wg.p[e]) + static_cast<size_t>(r0) * H, bytes, b);
-    bulk_load(dst + slice, static_cast<const __nv_bfloat16*>(A.wu.p[e]) + static_cast<size_t>(r0) * H,
-              bytes, b);
+    bulk_load_hint(dst, static_cast<const __nv_bfloat16*>(A.wg.p[e]) + static_cast<size_t>(r0) * H,
+                   bytes, b, pol);
+    bulk_load_hint(dst + slice, static_cast<const __nv_bfloat16*>(A.wu.p[e]) + static_cast<size_t>(r0) * H,
+                   bytes, b, pol);
     ++up_issued;
   };
   auto issue_wd = [&](int q) {
@@ -249,9 +261,9 @@ decode_ffn_kernel(const DecodeArgs A) {
     const int e = moe ? R.touched[ti] : 0;
     uint64_t* b = &wd_bar[q % P.wd_slots];
     mbar_arrive_expect_tx(b, static_cast<uint32_t>(slot));
-    bulk_load(wdbuf + (q % P.wd_slots) * slot,
-              static_cast<const __nv_bfloat16*>(A.wd.p[e]) + static_cast<size_t>(du) * kDnRows * I,
-              static_cast<uint32_t>(slot), b);
+    bulk_load_hint(wdbuf + (q % P.wd_slots) * slot,
+                   static_cast<const __nv_bfloat16*>(A.wd.p[e]) + static_cast<size_t>(du) * kDnRows * I,
+                   static_cast<uint32_t>(slot), b, pol);
     ++wd_issued;
   };
   auto issue_first = [&]() {

@@ -45,7 +45,7 @@ namespace mm {
 
 constexpr int kDtThreads = 320;
 constexpr int kDtEpiWarps = 8;
-constexpr int kDtMaxStages = 6;
+constexpr int kDtMaxStages = 4;
 constexpr int kDtTileA = 128 * 64 * 2;          // 16 KiB: 128 weight rows x 64 k
 constexpr uint32_t kDtTmemCols = 512;
 constexpr uint32_t kDtColGU = 0;                // two (G, U) buffers, 2 * Np columns each
@@ -87,6 +87,8 @@ struct DtArgs {
   WsHeader* hdr;
   int stages;
   int gu_bufs;                    // fused: (G, U) TMEM buffers (1 or 2)
+  int spec;                       // fused MoE: every expert streamed from the start, routed meanwhile
+  int router_stages;              // ring stages the router's x and Wr tiles cover
   int Epad;                       // experts padded to a multiple of 16 (router N)
   uint32_t stage_bytes;           // 32 KiB of weight tiles + one x tile
   uint32_t hstage_off;            // Hp staging tile [2][Np][128] bf16 (epilogue -> TMA store)
@@ -209,6 +211,7 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
     return r;
   };
   auto sdesc = [&](const uint8_t* p) { return smem_desc_sw128(smem_u32(p)); };
+  const uint64_t pol = l2_evict_first_policy();     // weights: read once per launch
 
   // ------------------------------------------------------------ 1: router (MoE)
   // L[t, e] = x_t . Wr_e.  All k-blocks are requested at once into the ring
@@ -219,51 +222,56 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
   const uint32_t wtile = static_cast<uint32_t>(A.Epad) * 128;
   uint8_t* rx = ring;
   uint8_t* rw = ring + KB_H * xtile;
-  if (moe) {
-    if (tid == 0) {
-      mbar_arrive_expect_tx(&wbar, KB_H * (xtile + wtile));
-      for (int kb = 0; kb < KB_H; ++kb) {
-        tma_load_2d(rx + kb * xtile, &M.x, &wbar, kb * 64, 0);
-        tma_load_2d(rw + kb * wtile, &M.wr, &wbar, kb * 64, 0);
-      }
+  auto router_issue = [&]() {               // thread 0
+    mbar_arrive_expect_tx(&wbar, KB_H * (xtile + wtile));
+    for (int kb = 0; kb < KB_H; ++kb) {
+      tma_load_2d(rx + kb * xtile, &M.x, &wbar, kb * 64, 0);
+      tma_load_2d(rw + kb * wtile, &M.wr, &wbar, kb * 64, 0);
     }
-    if (tid == 32) {
-      ok = mbar_wait(&wbar, 0, nullptr, hdr, 42);
-      tc_fence_after();
-      if (ok) {
-        const uint32_t idesc_r = idesc_bf16_f32(128, A.Epad);
-        for (int kb = 0; kb < KB_H; ++kb) {
+  };
+  auto router_mma = [&]() -> bool {         // thread 32
+    if (!mbar_wait(&wbar, 0, nullptr, hdr, 42)) return false;
+    tc_fence_after();
+    const uint32_t idesc_r = idesc_bf16_f32(128, A.Epad);
+    for (int kb = 0; kb < KB_H; ++kb) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + kDtColL, sdesc(rx + kb * xtile + kk * 32), sdesc(rw + kb * wtile + kk * 32),
-                      idesc_r, (kb | kk) ? 1u : 0u);
-        }
-        umma_commit(&lbar);
-      }
+      for (int kk = 0; kk < 4; ++kk)
+        umma_bf16(tmem + kDtColL, sdesc(rx + kb * xtile + kk * 32), sdesc(rw + kb * wtile + kk * 32),
+                  idesc_r, (kb | kk) ? 1u : 0u);
     }
-    if (epi && half == 0) {
-      ok = warp_wait(&lbar, 0, nullptr, hdr, 43);
-      tc_fence_after();
-      const int t = quad * 32 + lane;        // TMEM lane = token
+    umma_commit(&lbar);
+    return true;
+  };
+  auto router_read = [&]() -> bool {        // epilogue warps of column half 0 (TMEM lane = token)
+    const bool r = warp_wait(&lbar, 0, nullptr, hdr, 43);
+    tc_fence_after();
+    const int t = quad * 32 + lane;
 #pragma unroll 1
-      for (int c0 = 0; ok && c0 < A.Epad; c0 += 8) {
-        uint32_t r[8];
-        tmem_ld_32x32b_x8(tmem + lane_base + kDtColL + c0, r);
-        tmem_ld_wait();
-        if (t < T) {
+    for (int c0 = 0; r && c0 < A.Epad; c0 += 8) {
+      uint32_t v[8];
+      tmem_ld_32x32b_x8(tmem + lane_base + kDtColL + c0, v);
+      tmem_ld_wait();
+      if (t < T) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (c0 + j < A.E) R.prob[t][c0 + j] = __uint_as_float(r[j]);
-        }
+        for (int j = 0; j < 8; ++j)
+          if (c0 + j < A.E) R.prob[t][c0 + j] = __uint_as_float(v[j]);
       }
     }
+    return r;
+  };
+  // speculative (fused MoE only): the router runs inside the unit phase
+  const bool spec = kFused && A.spec != 0;
+  if (moe && !spec) {
+    if (tid == 0) router_issue();
+    if (tid == 32) ok = router_mma();
+    if (epi && half == 0) ok = router_read();
   }
   tc_fence_before();
   ok = __syncthreads_and(ok);
   tc_fence_after();
 
   // ------------------------------------------------------------ routing
-  if (ok) {
+  if (ok && !spec) {
     if (moe) {
       route_softmax_topk(R, T, A.E, A.k, s_bias, tid, kDtThreads);
       __syncthreads();
@@ -292,7 +300,11 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
     // TMEM into four shared tiles (bf16 high part and remainder, two k-halves;
     // Np rows x 128 bytes, 128-byte swizzle): the B operand of the down MMAs,
     // which accumulate y^T for all H rows in TMEM across the CTA's units.
-    const int nt = (ok && R.n_touched > 0) ? R.n_touched : 1;
+    // speculative: every expert is a unit (alpha indexed by expert); the
+    // router's tiles take the first A.router_stages ring stages, whose first
+    // use is completed by hand (full: a plain arrival; empty: a commit after
+    // the router MMAs), so that the ring then runs as if they had been used
+    const int nt = spec ? A.E : ((ok && R.n_touched > 0) ? R.n_touched : 1);
     const int MB_I = (I + 127) / 128, MB_H = H / 128;
     const int n_units = nt * MB_I;
     const int nb = A.gu_bufs;
@@ -300,15 +312,20 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
     uint8_t* hs = reinterpret_cast<uint8_t*>(hstage);      // tile (part, k-half) at (2 part + kh) * xtile
     if (ok) {
       if (tid == 0) {
+        if (spec) {
+          router_issue();
+          for (int q = 0; q < A.router_stages; ++q) mbar_arrive(&full[q]);
+          p_it = A.router_stages;
+        }
         for (int u = cta; ok && u < n_units; u += G) {
-          const int ti = u / MB_I, mb = u - ti * MB_I, e = R.touched[ti];
+          const int ti = u / MB_I, mb = u - ti * MB_I, e = spec ? ti : R.touched[ti];
           for (int kb = 0; kb < KB_H; ++kb) {
             int s;
             if (!acquire(s)) { ok = false; break; }
             uint8_t* st = ring + s * SB;
             mbar_arrive_expect_tx(&full[s], 2 * kDtTileA + xtile);
-            tma_load_2d(st, &M.wg[e], &full[s], kb * 64, mb * 128);
-            tma_load_2d(st + kDtTileA, &M.wu[e], &full[s], kb * 64, mb * 128);
+            tma_load_2d_hint(st, &M.wg[e], &full[s], kb * 64, mb * 128, pol);
+            tma_load_2d_hint(st + kDtTileA, &M.wu[e], &full[s], kb * 64, mb * 128, pol);
             tma_load_2d(st + 2 * kDtTileA, &M.x, &full[s], kb * 64, 0);
             ++p_it;
           }
@@ -317,13 +334,18 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
             if (!acquire(s)) { ok = false; break; }
             uint8_t* st = ring + s * SB;
             mbar_arrive_expect_tx(&full[s], 2 * kDtTileA);
-            tma_load_2d(st, &M.wd[e], &full[s], mb * 128, mbd * 128);
-            tma_load_2d(st + kDtTileA, &M.wd[e], &full[s], mb * 128 + 64, mbd * 128);
+            tma_load_2d_hint(st, &M.wd[e], &full[s], mb * 128, mbd * 128, pol);
+            tma_load_2d_hint(st + kDtTileA, &M.wd[e], &full[s], mb * 128 + 64, mbd * 128, pol);
             ++p_it;
           }
         }
       }
       if (tid == 32) {
+        if (spec) {
+          ok = router_mma();
+          for (int q = 0; q < A.router_stages; ++q) umma_commit(&empty[q]);
+          m_it = A.router_stages;
+        }
         int j = 0;
         for (int u = cta; ok && u < n_units; u += G, ++j) {
           const int acc = nb == 2 ? (j & 1) : 0, use = nb == 2 ? (j >> 1) : j;
@@ -377,6 +399,22 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
         const int col = rl & 63;
         uint8_t* hhi = hs + (rl >> 6) * xtile;
         uint8_t* hlo = hhi + 2 * xtile;
+        if (spec) {
+          // routing on the epilogue warps (named barrier 1) while the weights stream
+          bool r = true;
+          if (half == 0) r = router_read();
+          ok = epi_sync_and(r);
+          if (ok) {
+            const int etid = tid - 64, en = kDtEpiWarps * 32;
+            route_softmax_topk(R, T, A.E, A.k, s_bias, etid, en);
+            for (int q = etid; q < A.E * Np; q += en) alpha[q] = 0.f;
+            epi_sync();
+            if (warp == 2) route_group(R, T * A.k, A.E, lane);
+            for (int a = etid; a < T * A.k; a += en) alpha[R.sel_e[a] * Np + a / A.k] = R.sel_a[a];
+            epi_sync();
+            if (cta == 0) route_outputs(R, T, A.E, A.coef, A.topk_idx, A.topk_w, A.aux_loss, etid, en, 0);
+          }
+        }
         int j = 0;
         for (int u = cta; ok && u < n_units; u += G, ++j) {
           const int ti = u / MB_I;
@@ -553,8 +591,8 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
             if (!acquire(s)) { ok = false; break; }
             uint8_t* st = ring + s * SB;
             mbar_arrive_expect_tx(&full[s], 2 * kDtTileA + xtile);
-            tma_load_2d(st, &M.wg[e], &full[s], kb * 64, mb * 128);
-            tma_load_2d(st + kDtTileA, &M.wu[e], &full[s], kb * 64, mb * 128);
+            tma_load_2d_hint(st, &M.wg[e], &full[s], kb * 64, mb * 128, pol);
+            tma_load_2d_hint(st + kDtTileA, &M.wu[e], &full[s], kb * 64, mb * 128, pol);
             tma_load_2d(st + 2 * kDtTileA, &M.x, &full[s], kb * 64, 0);
             ++p_it;
           }
@@ -565,7 +603,7 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
           tile_of(r0 + j, mbd, ti, kb);
           if (!acquire(s)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[s], kDtTileA + 2 * xtile);   // the Hp tiles follow later
-          tma_load_2d(ring + s * SB, &M.wd[R.touched[ti]], &full[s], kb * 64, mbd * 128);
+          tma_load_2d_hint(ring + s * SB, &M.wd[R.touched[ti]], &full[s], kb * 64, mbd * 128, pol);
           ++p_it;
         }
       }
@@ -733,7 +771,7 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
           } else {
             if (!acquire(s)) { ok = false; break; }
             mbar_arrive_expect_tx(&full[s], kDtTileA + 2 * xtile);
-            tma_load_2d(ring + s * SB, &M.wd[R.touched[ti]], &full[s], kb * 64, mbd * 128);
+            tma_load_2d_hint(ring + s * SB, &M.wd[R.touched[ti]], &full[s], kb * 64, mbd * 128, pol);
             ++p_it;
           }
           uint8_t* b = ring + s * SB + kDtTileA;
@@ -847,6 +885,7 @@ namespace {
 struct DtLayout {
   int Np, Epad, nt_max, stages;
   int fused, gu_bufs;                   // down product per unit in the same CTA
+  int spec, router_stages;              // fused MoE streaming every expert before the routing
   size_t stage, alpha_off, hstage_off, smem;   // shared memory
   size_t hp, pgu, pd, total;            // workspace (after the header)
 };
@@ -883,6 +922,8 @@ bool dt_layout(int T, int H, int I, int E, int k, DtLayout& L) {
   L.gu_bufs = (MB_H + 4) * L.Np <= static_cast<int>(kDtTmemCols) ? 2 : 1;
   const int units = blocks + G;                      // blocks * ceil(G / blocks) < blocks + G
   if (H / 128 > G || H / 128 > kDtMaxMB) return false;
+  L.spec = 0;
+  L.router_stages = 0;
   {
     // MoE router: all x tiles, then all Wr tiles, in the ring region; the A
     // read of the last x tile spans 128 rows
@@ -890,6 +931,16 @@ bool dt_layout(int T, int H, int I, int E, int k, DtLayout& L) {
     const size_t kbh = static_cast<size_t>(H / 64);
     const size_t need = std::max(kbh * (xt + wt), (kbh - 1) * xt + kDtTileA);
     if (E > 1 && need > static_cast<size_t>(L.stages) * L.stage) return false;
+    // speculative streaming (fused MoE with at least two assignments per
+    // expert, so that nearly every expert is touched): every expert's units
+    // stream from the start while the router and the routing run; the
+    // router's stages must leave one free, and the gate/up and y^T columns of
+    // TMEM must stay clear of the router's logits
+    L.router_stages = static_cast<int>((need + L.stage - 1) / L.stage);
+    const int colD = 2 * L.Np * L.gu_bufs;
+    if (L.fused && E > 1 && T * k >= 2 * E && L.router_stages < L.stages &&
+        colD + MB_H * L.Np <= static_cast<int>(kDtColL))
+      L.spec = 1;                                    // (nt_max is already E here)
   }
   {
     const long long F = static_cast<long long>(H / 128) * L.nt_max * (I / 64);
@@ -980,6 +1031,8 @@ cudaError_t launch_decode_tc(const void* x, const void* Wr, const float* bias,
   A.y = y; A.hdr = hdr;
   A.stages = L.stages;
   A.gu_bufs = L.gu_bufs;
+  A.spec = L.spec;
+  A.router_stages = L.router_stages;
   A.Epad = L.Epad;
   A.stage_bytes = static_cast<uint32_t>(L.stage);
   A.hstage_off = static_cast<uint32_t>(L.hstage_off);
