@@ -59,8 +59,8 @@ constexpr int kDtReduceChunk = 32;              // partials requested at once in
 constexpr size_t kDtSmemBudget = 196 * 1024;   // dynamic; static use is ~27 KiB
 constexpr int kDtFusedMinUnits = 64;            // fused variant: (expert, I-block) units at least
 constexpr int kDtFusedMaxNp = 32;               // fused variant: padded tokens at most
-constexpr int kDtMaxSlices = 8;                 // fused: partial sums per output quad at most
-constexpr int kDtSumChunk = 8;                  // fused: partials requested at once
+constexpr int kDtMaxSlices = 16;                // fused: partial sums per output quad at most
+constexpr int kDtSumChunk = 16;                 // fused: partials requested at once
 
 template <int MAXW>
 struct DtMaps {
@@ -456,16 +456,24 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
             tc_fence_after();
             float* pdst = A.pd + static_cast<size_t>(cta) * T * H + rl;
             const int cstop = cend < T ? cend : T;
+            // four output m-blocks per TMEM wait
 #pragma unroll 1
-            for (int mbd = 0; mbd < MB_H; ++mbd) {
+            for (int c0 = cbeg; c0 < cstop; c0 += 8) {
 #pragma unroll 1
-              for (int c0 = cbeg; c0 < cstop; c0 += 8) {
-                uint32_t r[8];
-                tmem_ld_32x32b_x8(tmem + lane_base + colD + mbd * Np + c0, r);
+              for (int m0 = 0; m0 < MB_H; m0 += 4) {
+                uint32_t r[4][8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  if (m0 + q < MB_H) tmem_ld_32x32b_x8(tmem + lane_base + colD + (m0 + q) * Np + c0, r[q]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj)
-                  if (c0 + jj < T) pdst[static_cast<size_t>(c0 + jj) * H + mbd * 128] = __uint_as_float(r[jj]);
+                for (int q = 0; q < 4; ++q) {
+                  if (m0 + q >= MB_H) break;
+#pragma unroll
+                  for (int jj = 0; jj < 8; ++jj)
+                    if (c0 + jj < T)
+                      pdst[static_cast<size_t>(c0 + jj) * H + (m0 + q) * 128] = __uint_as_float(r[q][jj]);
+                }
               }
             }
           }
