@@ -50,7 +50,7 @@ constexpr int kDtTileA = 128 * 64 * 2;          // 16 KiB: 128 weight rows x 64 
 constexpr uint32_t kDtTmemCols = 512;
 constexpr uint32_t kDtColGU = 0;                // two (G, U) buffers, 2 * Np columns each
 constexpr uint32_t kDtColD = 256;               // down accumulator
-constexpr uint32_t kDtColL = 384;               // router logits
+constexpr uint32_t kDtColL = 384;               // router logits (speculative: the last Epad columns)
 constexpr int kDtMaxSeg = 2;                    // output m-blocks per CTA range
 constexpr int kDtMaxCtas = 160;                 // grid cap (152 SMs on GB300)
 constexpr int kDtMaxMB = 64;                    // output m-blocks (H <= 8192)
@@ -58,7 +58,6 @@ constexpr int kDtMaxSplit = 4;                  // k-ranges per gate/up block at
 constexpr int kDtReduceChunk = 32;              // partials requested at once in the final sum
 constexpr size_t kDtSmemBudget = 196 * 1024;   // dynamic; static use is ~27 KiB
 constexpr int kDtFusedMinUnits = 64;            // fused variant: (expert, I-block) units at least
-constexpr int kDtFusedMaxNp = 32;               // fused variant: padded tokens at most
 constexpr int kDtMaxSlices = 16;                // fused: partial sums per output quad at most
 constexpr int kDtSumChunk = 16;                 // fused: partials requested at once
 
@@ -222,6 +221,12 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
   const uint32_t wtile = static_cast<uint32_t>(A.Epad) * 128;
   uint8_t* rx = ring;
   uint8_t* rw = ring + KB_H * xtile;
+  // speculative (fused MoE only): the router runs inside the unit phase, its
+  // logits in the last Epad TMEM columns.  Those may be y^T's last columns:
+  // the first down MMA of the CTA waits for h, which the epilogue writes only
+  // after it has read the logits and routed.
+  const bool spec = kFused && A.spec != 0;
+  const uint32_t colL = spec ? kDtTmemCols - static_cast<uint32_t>(A.Epad) : kDtColL;
   auto router_issue = [&]() {               // thread 0
     mbar_arrive_expect_tx(&wbar, KB_H * (xtile + wtile));
     for (int kb = 0; kb < KB_H; ++kb) {
@@ -236,7 +241,7 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
     for (int kb = 0; kb < KB_H; ++kb) {
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        umma_bf16(tmem + kDtColL, sdesc(rx + kb * xtile + kk * 32), sdesc(rw + kb * wtile + kk * 32),
+        umma_bf16(tmem + colL, sdesc(rx + kb * xtile + kk * 32), sdesc(rw + kb * wtile + kk * 32),
                   idesc_r, (kb | kk) ? 1u : 0u);
     }
     umma_commit(&lbar);
@@ -249,7 +254,7 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
 #pragma unroll 1
     for (int c0 = 0; r && c0 < A.Epad; c0 += 8) {
       uint32_t v[8];
-      tmem_ld_32x32b_x8(tmem + lane_base + kDtColL + c0, v);
+      tmem_ld_32x32b_x8(tmem + lane_base + colL + c0, v);
       tmem_ld_wait();
       if (t < T) {
 #pragma unroll
@@ -259,8 +264,6 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
     }
     return r;
   };
-  // speculative (fused MoE only): the router runs inside the unit phase
-  const bool spec = kFused && A.spec != 0;
   if (moe && !spec) {
     if (tid == 0) router_issue();
     if (tid == 32) ok = router_mma();
@@ -919,14 +922,11 @@ bool dt_layout(int T, int H, int I, int E, int k, DtLayout& L) {
   L.smem = L.hstage_off + hstage + 1024;             // 1 KiB: alignment slack
   const int G = kDtMaxCtas;
   const int blocks = L.nt_max * ((I + 127) / 128);
-  // fused: the (G, U) accumulators and y^T for all H rows fit in TMEM, there
-  // are units enough to keep most SMs streaming (a fused unit cannot be split
-  // along K; the dense FFN at H = 768 has only I / 128 of them), and the
-  // per-CTA partials of y (T * H * 4 bytes each) stay small: at 64 tokens
-  // writing and adding them costs more than h's round trip through memory
+  // fused: the (G, U) accumulators and y^T for all H rows fit in TMEM, and
+  // there are units enough to keep most SMs streaming (a fused unit cannot be
+  // split along K; the dense FFN at H = 768 has only I / 128 of them)
   const int MB_H = H / 128;
-  L.fused = ((MB_H + 2) * L.Np <= static_cast<int>(kDtTmemCols) && blocks >= kDtFusedMinUnits &&
-             L.Np <= kDtFusedMaxNp) ? 1 : 0;
+  L.fused = ((MB_H + 2) * L.Np <= static_cast<int>(kDtTmemCols) && blocks >= kDtFusedMinUnits) ? 1 : 0;
   L.gu_bufs = (MB_H + 4) * L.Np <= static_cast<int>(kDtTmemCols) ? 2 : 1;
   const int units = blocks + G;                      // blocks * ceil(G / blocks) < blocks + G
   if (H / 128 > G || H / 128 > kDtMaxMB) return false;
@@ -942,12 +942,11 @@ bool dt_layout(int T, int H, int I, int E, int k, DtLayout& L) {
     // speculative streaming (fused MoE with at least two assignments per
     // expert, so that nearly every expert is touched): every expert's units
     // stream from the start while the router and the routing run; the
-    // router's stages must leave one free, and the gate/up and y^T columns of
-    // TMEM must stay clear of the router's logits
+    // router's stages must leave one free, and the gate/up columns of TMEM
+    // must stay clear of the router's logits (the last Epad columns)
     L.router_stages = static_cast<int>((need + L.stage - 1) / L.stage);
-    const int colD = 2 * L.Np * L.gu_bufs;
     if (L.fused && E > 1 && T * k >= 2 * E && L.router_stages < L.stages &&
-        colD + MB_H * L.Np <= static_cast<int>(kDtColL))
+        2 * L.Np * L.gu_bufs + L.Epad <= static_cast<int>(kDtTmemCols))
       L.spec = 1;                                    // (nt_max is already E here)
   }
   {
