@@ -34,15 +34,25 @@ from swiglu_mlp_top_gb300.inputs import WORKLOADS, make_workload_inputs  # noqa:
 DEFAULT_WORKLOAD = "moe_e8k2_t16384_skew"
 METRIC = "MoE/FFN forward tokens/s and TFLOP/s on 1 GB300; % of bf16 tensor or HBM roofline"
 L2_BYTES = 129 * 1024 * 1024
-DECODE_MAX_T = 64         # token counts the library streams weights for (bf16)
+DECODE_MAX_T = 64         # token counts the library streams weights for (bf16 MoE)
+DENSE_STREAM_MAX_T = 128  # the same for the dense FFN
+
+
+def streams_weights(w):
+    """Whether the automatic path runs this workload as one weight-streaming
+    kernel (bf16; up to 128 tokens dense, 64 MoE)."""
+    return w.dtype == "bf16" and w.T <= (DENSE_STREAM_MAX_T if w.kind == "dense" else DECODE_MAX_T)
 
 
 def decode_kernel_name(w):
     """The streaming kernel the automatic path picks for this workload: CUDA
-    cores up to 6 tokens (dense) or 2 tokens (MoE), tensor cores beyond."""
-    simt = w.T <= (6 if w.kind == "dense" else 2)
-    return ("decode_ffn_kernel (CUDA-core weight streaming)" if simt
-            else "decode_tc_kernel (tcgen05 weight streaming)")
+    cores up to 6 tokens (dense) or 2 tokens (MoE), tensor cores beyond (the
+    dense FFN with the tokens as the UMMA M operand)."""
+    if w.T <= (6 if w.kind == "dense" else 2):
+        return "decode_ffn_kernel (CUDA-core weight streaming)"
+    if w.kind == "dense":
+        return "decode_sw_kernel (tcgen05 weight streaming, tokens as M)"
+    return "decode_tc_kernel (tcgen05 weight streaming)"
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
 # gate/up GEMM, from an ncu capture of the current kernel on this workload;
@@ -298,10 +308,9 @@ def run_our_arm(args, w):
     torch.cuda.synchronize()
     assert mm.check_status(step.ws) == 0
 
-    use_graph = args.graph == "on" or (args.graph == "auto" and w.T <= 64)
+    use_graph = args.graph == "on" or (args.graph == "auto" and streams_weights(w))
     # ---- timed region: K steps, device events on the launching stream
-    dominant = (L.MM_KERNEL_DECODE if (w.T <= DECODE_MAX_T and w.dtype == "bf16")
-                else L.MM_KERNEL_GATEUP)
+    dominant = L.MM_KERNEL_DECODE if streams_weights(w) else L.MM_KERNEL_GATEUP
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     if use_graph:
@@ -355,7 +364,7 @@ def run_our_arm(args, w):
     # ---- dominant kernel roofline
     peaks, peak_src = measured_peaks()
     k_ms = tot.value / max(1, nl.value)
-    if w.T <= DECODE_MAX_T and w.dtype == "bf16":
+    if streams_weights(w):
         # weight streaming (one kernel per step): HBM-bound; algorithmic bytes =
         # the weights of the experts some token selected, x read and y written
         touched = 1 if w.kind == "dense" else int(torch.unique(step.idx).numel())

@@ -14,8 +14,9 @@
  *       Wg, Wu: [I, H]   Wd: [H, I]   Wr: [E, H]   x, y: [T, H].
  *   - dtype selects the element type of x, the weights and y:
  *       MM_DTYPE_BF16 — bf16 storage, fp32 accumulation (tcgen05 tensor
- *                       cores; for T <= 64 one weight-streaming kernel
- *                       that reads every needed weight row once);
+ *                       cores; for T <= 128 (dense FFN) or T <= 64 (MoE)
+ *                       one weight-streaming kernel that reads every
+ *                       needed weight row once);
  *       MM_DTYPE_F32  — fp32 storage and fp32 SIMT arithmetic (no TF32).
  *     Router logits, probabilities, alpha and the aux loss are always fp32.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
@@ -59,11 +60,11 @@ typedef enum { MM_DTYPE_F32 = 0, MM_DTYPE_BF16 = 1 } mm_dtype;
 
 /* Which kernels carry the FFN part of a call (the *_ex entry points). */
 typedef enum {
-  MM_PATH_AUTO = 0,    /* bf16: streaming up to 64 tokens, tensor-core GEMMs beyond; f32: SIMT */
+  MM_PATH_AUTO = 0,    /* bf16: streaming up to 128 (dense) / 64 (MoE) tokens, tensor-core GEMMs beyond; f32: SIMT */
   MM_PATH_TENSOR = 1,  /* bf16 only: grouped tcgen05/TMEM GEMMs fed by TMA          */
   MM_PATH_STREAM = 2,  /* bf16 only, T <= 16: weight streaming on the CUDA cores       */
   MM_PATH_SIMT = 3,    /* any dtype: plain fp32-FMA CUDA-core kernels                */
-  MM_PATH_STREAM_TC = 4 /* bf16 only, T <= 64: weight streaming on the tensor cores   */
+  MM_PATH_STREAM_TC = 4 /* bf16 only, T <= 128 dense / 64 MoE: weight streaming on the tensor cores */
 } mm_path;
 
 /* Limits of this build. */

@@ -100,6 +100,14 @@ size_t stream_tc_bytes(int64_t T, int H, int I, int E, int k, int dtype) {
   if (dtype != kDtypeBF16 || T < 1 || T > kDecodeTcMaxT) return 0;
   return decode_tc_bytes(static_cast<int>(T), H, I, E, k);
 }
+// The dense FFN streams on the tensor cores with the tokens as the M operand
+// (decode_sw.cu, up to kDecodeSwMaxT tokens) where that kernel takes the
+// shape, else with the weights as the M operand (decode_tc.cu).
+size_t dense_stream_tc_bytes(int64_t T, int H, int I, int dtype) {
+  if (dtype != kDtypeBF16 || T < 1 || T > kDecodeSwMaxT) return 0;
+  const size_t sw = decode_sw_bytes(static_cast<int>(T), H, I);
+  return sw ? sw : stream_tc_bytes(T, H, I, 1, 1, dtype);
+}
 
 // Workspace of one path (0: the path does not take this shape), and the
 // workspace that serves every path valid for the shape.
@@ -107,7 +115,7 @@ size_t dense_path_bytes(int64_t T, int H, int I, int dtype, int p) {
   size_t b = 0;
   switch (p) {
     case MM_PATH_STREAM: b = stream_simt_bytes(T, H, I, 1, 1, dtype); break;
-    case MM_PATH_STREAM_TC: b = stream_tc_bytes(T, H, I, 1, 1, dtype); break;
+    case MM_PATH_STREAM_TC: b = dense_stream_tc_bytes(T, H, I, dtype); break;
     default: return dense_tensor_ws_bytes(T, H, I, dtype);
   }
   return b ? sizeof(WsHeader) + b : 0;
@@ -137,15 +145,17 @@ size_t moe_ws_bytes(int64_t T, int H, int I, int E, int k, int dtype) {
 // AUTO: fp32 -> CUDA-core kernels.  bf16 -> weight streaming for decode-sized
 // T (every weight row read once): on the CUDA cores for the smallest T (up to
 // 6 tokens dense, 2 tokens MoE: their cost grows with the tokens and the
-// touched experts), on the tensor cores up to kDecodeTcMaxT (a fixed cost of
-// one to three grid barriers and the partial sums); tensor-core GEMMs beyond.
+// touched experts), on the tensor cores up to kDecodeSwMaxT tokens (dense) or
+// kDecodeTcMaxT (MoE) (a fixed cost of one to three grid barriers and the
+// partial sums); tensor-core GEMMs beyond.
 inline int64_t stream_simt_auto_max_t(int E) { return E == 1 ? 6 : 2; }
-int resolve_path(int path, int dtype, int64_t T, int H, int I, int E, int k) {
+int resolve_path(int path, int dtype, int64_t T, int H, int I, int E, int k, bool dense) {
   if (path != MM_PATH_AUTO) return path;
   if (dtype == kDtypeF32) return MM_PATH_SIMT;
   if (T <= stream_simt_auto_max_t(E) && stream_simt_bytes(T, H, I, E, k, dtype) > 0)
     return MM_PATH_STREAM;
-  if (stream_tc_bytes(T, H, I, E, k, dtype) > 0) return MM_PATH_STREAM_TC;
+  if (dense ? dense_stream_tc_bytes(T, H, I, dtype) > 0 : stream_tc_bytes(T, H, I, E, k, dtype) > 0)
+    return MM_PATH_STREAM_TC;
   if (stream_simt_bytes(T, H, I, E, k, dtype) > 0) return MM_PATH_STREAM;
   return MM_PATH_TENSOR;
 }
@@ -156,7 +166,7 @@ int resolve_path(int path, int dtype, int64_t T, int H, int I, int E, int k) {
 // when that path does not take the shape.  Used by the no-allocation entry.
 size_t dense_workspace_for_path(int64_t T, int H, int I, int dtype, int path) {
   if (T < 1 || H < 1 || I < 1 || !valid_dtype(dtype)) return 0;
-  return dense_path_bytes(T, H, I, dtype, resolve_path(path, dtype, T, H, I, 1, 1));
+  return dense_path_bytes(T, H, I, dtype, resolve_path(path, dtype, T, H, I, 1, 1, true));
 }
 
 namespace {
@@ -285,7 +295,7 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
   if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) || !aligned16(y))
     return MM_ERR_INVALID_ARG;
   if (!workspace || !aligned16(workspace)) return MM_ERR_WORKSPACE;
-  const int p = resolve_path(path, dtype, T, H, I, 1, 1);
+  const int p = resolve_path(path, dtype, T, H, I, 1, 1, true);
   if (p == MM_PATH_TENSOR && (dtype != kDtypeBF16 || !tensor_shape_ok(H, I)))
     return MM_ERR_UNSUPPORTED;
   const size_t need = dense_path_bytes(T, H, I, dtype, p);
@@ -304,6 +314,8 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
       if (p == MM_PATH_STREAM)
         return launch_decode_ffn(x, nullptr, nullptr, wg1, wu1, wd1, static_cast<int>(T), H, I, 1,
                                  1, 0.f, nullptr, nullptr, nullptr, h, y, hdr, st);
+      if (decode_sw_bytes(static_cast<int>(T), H, I) > 0)
+        return launch_decode_sw(x, Wg, Wu, Wd, static_cast<int>(T), H, I, h, y, hdr, st);
       return launch_decode_tc(x, nullptr, nullptr, wg1, wu1, wd1, static_cast<int>(T), H, I, 1, 1,
                               0.f, nullptr, nullptr, nullptr, h, y, hdr, st);
     });
@@ -384,7 +396,7 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
     if (!aligned16(Wg[e]) || !aligned16(Wu[e]) || !aligned16(Wd[e])) return MM_ERR_INVALID_ARG;
   }
   if (!workspace || !aligned16(workspace)) return MM_ERR_WORKSPACE;
-  const int p = resolve_path(path, dtype, T, H, I, E, k);
+  const int p = resolve_path(path, dtype, T, H, I, E, k, false);
   if (p == MM_PATH_TENSOR && (dtype != kDtypeBF16 || !tensor_shape_ok(H, I)))
     return MM_ERR_UNSUPPORTED;
   const size_t need = moe_path_bytes(T, H, I, E, k, dtype, p);

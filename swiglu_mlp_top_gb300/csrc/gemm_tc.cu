@@ -468,6 +468,35 @@ bool make_map_16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t out
   return true;
 }
 
+bool make_map_3d(CUtensorMap* out, const void* ptr, const uint64_t dims[3],
+                 const uint64_t strides[2], const uint32_t box[3]) {
+  using Key = std::tuple<uintptr_t, uint64_t, uint64_t, uint64_t, uint64_t, uint64_t, uint32_t,
+                         uint32_t, uint32_t>;
+  static std::mutex mu;
+  static std::map<Key, CUtensorMap> cache;
+  const Key key{reinterpret_cast<uintptr_t>(ptr), dims[0], dims[1], dims[2], strides[0],
+                strides[1], box[0], box[1], box[2]};
+  std::lock_guard<std::mutex> lock(mu);
+  auto itc = cache.find(key);
+  if (itc != cache.end()) {
+    *out = itc->second;
+    return true;
+  }
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  cuuint64_t st[2] = {strides[0], strides[1]};
+  cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), d, st, bx,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  if (cache.size() > 4096) cache.clear();
+  cache.emplace(key, *out);
+  return true;
+}
+
 int num_sms() {
   constexpr int kMaxDev = 64;
   static int cached[kMaxDev] = {};

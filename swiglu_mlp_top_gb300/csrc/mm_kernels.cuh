@@ -19,6 +19,7 @@ constexpr int kMaxGroups = MM_MAX_EXPERTS * MM_MAX_TOPK;     // (slot, expert) g
 // T <= kDecodeMaxT, on the tensor cores (decode_tc.cu) for T <= kDecodeTcMaxT.
 constexpr int kDecodeMaxT = 16;
 constexpr int kDecodeTcMaxT = 64;
+constexpr int kDecodeSwMaxT = 128;          // dense FFN with the tokens as the M operand
 
 // Per-expert device pointers passed by value to a kernel.
 struct PtrArray {
@@ -145,6 +146,15 @@ cudaError_t launch_decode_tc(const void* x, const void* Wr, const float* bias,
                              float* topk_w, float* aux_loss, void* scratch, void* y,
                              WsHeader* hdr, cudaStream_t st);
 
+// Dense FFN on the tensor cores with the tokens as the M operand (T <=
+// kDecodeSwMaxT, bf16; decode_sw.cu): one cooperative kernel, units of 64
+// rows of I each run gate/up, SwiGLU and their share of the down product,
+// unit partials of y added after one grid barrier.  decode_sw_bytes is its
+// workspace after the 256-byte header (0: shape not supported).
+size_t decode_sw_bytes(int T, int H, int I);
+cudaError_t launch_decode_sw(const void* x, const void* Wg, const void* Wu, const void* Wd, int T,
+                             int H, int I, void* scratch, void* y, WsHeader* hdr, cudaStream_t st);
+
 cudaError_t launch_watchdog_selftest(WsHeader* hdr, uint32_t limit_us, cudaStream_t st);
 
 // Workspace of the path that `path` (AUTO: the automatic choice) resolves to
@@ -156,6 +166,12 @@ size_t dense_workspace_for_path(int64_t T, int H, int I, int dtype, int path);
 bool make_map_16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t outer,
                  uint32_t box_rows, bool is_f16, uint32_t box_inner = kTcBK,
                  CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B);
+
+// TMA tensor map of a bf16 tensor viewed in three dimensions (element
+// strides 1, strides[0], strides[1] bytes), box box[0] x box[1] x box[2],
+// 128-byte swizzle, zero fill outside; cached like make_map_16.
+bool make_map_3d(CUtensorMap* out, const void* ptr, const uint64_t dims[3],
+                 const uint64_t strides[2], const uint32_t box[3]);
 
 int num_sms();   // of the current device, looked up once per device
 

@@ -157,7 +157,7 @@ def test_stream_path_is_bf16_only():
 
 
 # ------------------------------------------------------------------ decode on the tensor cores
-@pytest.mark.parametrize("T", [1, 5, 16, 17, 40, 64])
+@pytest.mark.parametrize("T", [1, 5, 16, 17, 40, 64, 100, 128])
 def test_dense_stream_tc_path(T):
     inp = make_inputs(T, 768, 2432, "bf16", seed=80 + T)
     g = to_dev(inp)
@@ -209,15 +209,18 @@ def test_moe_stream_tc_deterministic():
 
 
 def test_stream_tc_shape_limits():
-    """H must be a multiple of 128 and I of 64; beyond 64 tokens the path is refused."""
+    """H must be a multiple of 128 and I of 64; the dense FFN streams up to 128
+    tokens, the MoE layer up to 64; beyond that the path is refused."""
     inp = make_inputs(5, 192, 256, "bf16", seed=122)
     g = to_dev(inp)
     with pytest.raises(RuntimeError, match="MM_ERR_UNSUPPORTED"):
         mm.swiglu_ffn(g["x"], g["Wg"], g["Wu"], g["Wd"], path="stream_tc")
-    inp = make_inputs(65, 256, 256, "bf16", seed=123)
+    inp = make_inputs(129, 256, 256, "bf16", seed=123)
     g = to_dev(inp)
     with pytest.raises(RuntimeError, match="MM_ERR_UNSUPPORTED"):
         mm.swiglu_ffn(g["x"], g["Wg"], g["Wu"], g["Wd"], path="stream_tc")
+    with pytest.raises(RuntimeError, match="MM_ERR_UNSUPPORTED"):
+        run_moe(moe_inputs(65, 256, 256, 4, "bf16", seed=124), 2, 0.01, path="stream_tc")
 
 
 @pytest.mark.parametrize("T", [1, 4, 16, 64])
