@@ -59,10 +59,11 @@ def decode_kernel_name(w):
 # None where no capture of the current kernel exists.
 GATEUP_TRAFFIC_BYTES = {"moe_e8k2_t16384_skew": 163.401216e6 + 128.745472e6}
 # The same for the decode kernel that streams the weights (one launch per step).
-DECODE_TRAFFIC_BYTES = {"decode_moe_e8k2_t64": 89.88672e6 + 3.149824e6,
-                        "decode_moe_e8k2_t16": 89.779456e6 + 2.938368e6,
-                        "decode_dense_t16": 11.350272e6,
-                        "decode_dense_t1": 11.30624e6}
+DECODE_TRAFFIC_BYTES = {"decode_moe_e8k2_t64": 89.896704e6 + 3.152384e6,
+                        "decode_moe_e8k2_t16": 89.822464e6 + 2.980096e6,
+                        "decode_dense_t16": 11.282432e6,
+                        "dense_t100": 11.417856e6,
+                        "decode_dense_t1": 11.307008e6}
 
 
 def algorithmic_flops(w, T=None) -> float:
