@@ -57,7 +57,7 @@ def decode_kernel_name(w):
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
 # gate/up GEMM, from an ncu capture of the current kernel on this workload;
 # None where no capture of the current kernel exists.
-GATEUP_TRAFFIC_BYTES = {"moe_e8k2_t16384_skew": 163.401216e6 + 128.745472e6}
+GATEUP_TRAFFIC_BYTES = {}
 # The same for the decode kernel that streams the weights (one launch per step).
 DECODE_TRAFFIC_BYTES = {"decode_moe_e8k2_t64": 89.896704e6 + 3.152384e6,
                         "decode_moe_e8k2_t16": 89.822464e6 + 2.980096e6,

@@ -33,9 +33,13 @@ namespace mm {
 constexpr int kOpUp = 0, kOpDown = 1;
 constexpr int kPairM = 2 * kTcBM;                        // rows per tile pair
 constexpr int kN = 256;                                  // UMMA N (both ops)
-constexpr int kStages = 6;
-constexpr int kAStage = kTcBM * kTcBK * 2;               // 16 KiB (this CTA's 128 rows)
-constexpr int kBStage = (kN / 2) * kTcBK * 2;            // 16 KiB (this CTA's half of N)
+// The operand ring holds six k-blocks of A and B (16 KiB each per CTA),
+// grouped into stages of kKb k-blocks fetched by one 3-D TMA box each:
+// gate/up measured 163 us with stages of two k-blocks against 170 with one,
+// the down GEMM 61 against 60, so each takes its own.
+constexpr int kATile = kTcBM * kTcBK * 2;                // 16 KiB: 128 rows x one k-block
+constexpr int kBTile = (kN / 2) * kTcBK * 2;             // 16 KiB: this CTA's half of N x one k-block
+constexpr int kRingKb = 6;                               // k-blocks in the ring
 constexpr int kAccStride = 256;                          // TMEM columns per accumulator
 // Epilogue: 8 warps; warp w reads TMEM lanes 32*(w%4).. (its rows) and
 // handles half w/4 of the tile's columns.  gate/up stages each 32-row x
@@ -45,13 +49,13 @@ constexpr int kEpiWarps = 8;
 constexpr int kStageEpi = kEpiWarps * 32 * 64;           // 16 KiB
 constexpr int kWarpProducer = kEpiWarps, kWarpMma = kEpiWarps + 1;
 constexpr int kThreads = 32 * (kEpiWarps + 2);
-constexpr int kSmem = kStages * (kAStage + kBStage) + kStageEpi + 2048;
+constexpr int kSmem = kRingKb * (kATile + kBTile) + kStageEpi + 2048;
 constexpr uint32_t kTmemCols = 512;
 static_assert(kSmem <= 232448, "shared memory budget");
 
 template <int OP> struct OpTraits;
-template <> struct OpTraits<kOpUp> { static constexpr int kOutCols = kN / 2; };
-template <> struct OpTraits<kOpDown> { static constexpr int kOutCols = kN; };
+template <> struct OpTraits<kOpUp> { static constexpr int kOutCols = kN / 2, kKb = 2; };
+template <> struct OpTraits<kOpDown> { static constexpr int kOutCols = kN, kKb = 1; };
 
 template <int MAXW>
 struct TcParams {
@@ -256,6 +260,10 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
   extern __shared__ unsigned char smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
+  constexpr int kKbStage = OpTraits<OP>::kKb;
+  constexpr int kStages = kRingKb / kKbStage;
+  constexpr int kAStage = kKbStage * kATile;
+  constexpr int kBStage = kKbStage * kBTile;
   uint8_t* sB = smem + kStages * kAStage;
   uint8_t* sEpi = sB + kStages * kBStage;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + kStageEpi);
@@ -320,14 +328,14 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
                                         kOutCols, static_cast<int>(rank));
         const CUtensorMap* bmap = (OP == kOpUp && rank == 1) ? &P.b1[ti.w] : &P.b0[ti.w];
         const int bcoord = (OP == kOpUp) ? ti.n0 : ti.n0 + static_cast<int>(rank) * (kN / 2);
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+        for (int kb = 0; kb < nkb; kb += kKbStage, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, abort, hdr, 1)) { ok = false; break; }
           const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
           if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (kAStage + kBStage));
-          tma_load_2d_cta2(sA + s * kAStage, &P.a, fb, kb * kTcBK, ti.row0);
-          tma_load_2d_cta2(sB + s * kBStage, bmap, fb, kb * kTcBK, bcoord);
+          tma_load_3d_cta2(sA + s * kAStage, &P.a, fb, 0, ti.row0, kb);
+          tma_load_3d_cta2(sB + s * kBStage, bmap, fb, 0, bcoord, kb);
         }
       }
       if (!ok && rank == 0) {
@@ -352,17 +360,21 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
         if (!mbar_wait(&tempty[acc], aph ^ 1, abort, hdr, 3)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + acc * kAccStride;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
+        for (int kb = 0; kb < nkb; kb += kKbStage, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
           if (!mbar_wait(&full[s], ph, abort, hdr, 4)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + s * kAStage);
-          const uint32_t b0 = smem_u32(sB + s * kBStage);
 #pragma unroll
-          for (int kk = 0; kk < kTcBK / 16; ++kk)
-            umma_f16_cta2(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
-                          (kb > 0 || kk > 0) ? 1u : 0u);
+          for (int kl = 0; kl < kKbStage; ++kl) {
+            if (kb + kl >= nkb) break;               // a box past K was zero-filled
+            const uint32_t a0 = smem_u32(sA + s * kAStage + kl * kATile);
+            const uint32_t b0 = smem_u32(sB + s * kBStage + kl * kBTile);
+#pragma unroll
+            for (int kk = 0; kk < kTcBK / 16; ++kk)
+              umma_f16_cta2(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
+                            (kb + kl > 0 || kk > 0) ? 1u : 0u);
+          }
           umma_commit_cta2_mc(&empty[s], 0x3);
         }
         if (!ok) break;
@@ -469,13 +481,13 @@ bool make_map_16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t out
 }
 
 bool make_map_3d(CUtensorMap* out, const void* ptr, const uint64_t dims[3],
-                 const uint64_t strides[2], const uint32_t box[3]) {
+                 const uint64_t strides[2], const uint32_t box[3], bool is_f16) {
   using Key = std::tuple<uintptr_t, uint64_t, uint64_t, uint64_t, uint64_t, uint64_t, uint32_t,
-                         uint32_t, uint32_t>;
+                         uint32_t, uint32_t, bool>;
   static std::mutex mu;
   static std::map<Key, CUtensorMap> cache;
   const Key key{reinterpret_cast<uintptr_t>(ptr), dims[0], dims[1], dims[2], strides[0],
-                strides[1], box[0], box[1], box[2]};
+                strides[1], box[0], box[1], box[2], is_f16};
   std::lock_guard<std::mutex> lock(mu);
   auto itc = cache.find(key);
   if (itc != cache.end()) {
@@ -488,7 +500,8 @@ bool make_map_3d(CUtensorMap* out, const void* ptr, const uint64_t dims[3],
   cuuint64_t st[2] = {strides[0], strides[1]};
   cuuint32_t bx[3] = {box[0], box[1], box[2]};
   cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), d, st, bx,
+  const CUresult r = enc(out, is_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         3, const_cast<void*>(ptr), d, st, bx,
                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
@@ -542,6 +555,17 @@ static cudaError_t launch_pdl(Kern fn, int grid, cudaStream_t st, Args... args) 
   return cudaLaunchKernelEx(&cfg, fn, args...);
 }
 
+// Operand map of a 16-bit row-major [rows, K] matrix (K a multiple of 64) as
+// (64 elements, rows, K / 64): box 64 x box_rows x kb, i.e. kb consecutive
+// 128-byte-swizzled k-block tiles per TMA.
+static bool kblock_map(CUtensorMap* out, const void* ptr, int K, int64_t rows, int box_rows,
+                       bool is_f16, int kb) {
+  const uint64_t dims[3] = {64, static_cast<uint64_t>(rows), static_cast<uint64_t>(K / 64)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(K) * 2, 128};
+  const uint32_t box[3] = {64, static_cast<uint32_t>(box_rows), static_cast<uint32_t>(kb)};
+  return make_map_3d(out, ptr, dims, strides, box, is_f16);
+}
+
 // Number of CTA pairs: one per tile pair, at most one per co-resident pair.
 static int clusters_for(int64_t a_rows, const GroupRows& g, int n_tiles) {
   int64_t tiles;
@@ -561,10 +585,11 @@ static cudaError_t gateup_impl(const void* A, int64_t a_rows, int H, int I, cons
   memset(&p, 0, sizeof(p));
   if (!make_map_16(&p.out, h_out, I, a_rows, 32, true, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  if (!make_map_16(&p.a, A, H, a_rows, kTcBM, false)) return cudaErrorInvalidValue;
+  constexpr int kb = OpTraits<kOpUp>::kKb;
+  if (!kblock_map(&p.a, A, H, a_rows, kTcBM, false, kb)) return cudaErrorInvalidValue;
   for (int e = 0; e < g.n_weights; ++e) {
-    if (!make_map_16(&p.b0[e], Wg[e], H, I, kN / 2, false)) return cudaErrorInvalidValue;
-    if (!make_map_16(&p.b1[e], Wu[e], H, I, kN / 2, false)) return cudaErrorInvalidValue;
+    if (!kblock_map(&p.b0[e], Wg[e], H, I, kN / 2, false, kb)) return cudaErrorInvalidValue;
+    if (!kblock_map(&p.b1[e], Wu[e], H, I, kN / 2, false, kb)) return cudaErrorInvalidValue;
   }
   auto fn = grouped_gemm_kernel<kOpUp, MAXW>;
   cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), kSmem);
@@ -581,9 +606,10 @@ static cudaError_t down_impl(const void* h, int64_t a_rows, int H, int I, const 
                              cudaStream_t st) {
   TcParams<MAXW> p;
   memset(&p, 0, sizeof(p));
-  if (!make_map_16(&p.a, h, I, a_rows, kTcBM, true)) return cudaErrorInvalidValue;
+  constexpr int kb = OpTraits<kOpDown>::kKb;
+  if (!kblock_map(&p.a, h, I, a_rows, kTcBM, true, kb)) return cudaErrorInvalidValue;
   for (int e = 0; e < g.n_weights; ++e)
-    if (!make_map_16(&p.b0[e], Wd[e], I, H, kN / 2, true)) return cudaErrorInvalidValue;
+    if (!kblock_map(&p.b0[e], Wd[e], I, H, kN / 2, true, kb)) return cudaErrorInvalidValue;
   auto fn = grouped_gemm_kernel<kOpDown, MAXW>;
   cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), kSmem);
   if (err != cudaSuccess) return err;
