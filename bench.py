@@ -46,9 +46,9 @@ def streams_weights(w):
 
 def decode_kernel_name(w):
     """The streaming kernel the automatic path picks for this workload: CUDA
-    cores up to 6 tokens (dense) or 2 tokens (MoE), tensor cores beyond (the
+    cores up to 4 tokens (dense) or 2 tokens (MoE), tensor cores beyond (the
     dense FFN with the tokens as the UMMA M operand)."""
-    if w.T <= (6 if w.kind == "dense" else 2):
+    if w.T <= (4 if w.kind == "dense" else 2):
         return "decode_ffn_kernel (CUDA-core weight streaming)"
     if w.kind == "dense":
         return "decode_sw_kernel (tcgen05 weight streaming, tokens as M)"

@@ -144,11 +144,11 @@ size_t moe_ws_bytes(int64_t T, int H, int I, int E, int k, int dtype) {
 
 // AUTO: fp32 -> CUDA-core kernels.  bf16 -> weight streaming for decode-sized
 // T (every weight row read once): on the CUDA cores for the smallest T (up to
-// 6 tokens dense, 2 tokens MoE: their cost grows with the tokens and the
+// 4 tokens dense, 2 tokens MoE: their cost grows with the tokens and the
 // touched experts), on the tensor cores up to kDecodeSwMaxT tokens (dense) or
 // kDecodeTcMaxT (MoE) (a fixed cost of one to three grid barriers and the
 // partial sums); tensor-core GEMMs beyond.
-inline int64_t stream_simt_auto_max_t(int E) { return E == 1 ? 6 : 2; }
+inline int64_t stream_simt_auto_max_t(int E) { return E == 1 ? 4 : 2; }
 int resolve_path(int path, int dtype, int64_t T, int H, int I, int E, int k, bool dense) {
   if (path != MM_PATH_AUTO) return path;
   if (dtype == kDtypeF32) return MM_PATH_SIMT;

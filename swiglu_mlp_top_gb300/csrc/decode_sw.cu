@@ -1,20 +1,21 @@
 // Dense SwiGLU FFN for up to 128 tokens on the 5th-generation tensor cores,
 // with the operands swapped against decode_tc.cu: the tokens are the UMMA M
 // operand (TMEM lane = token; rows past T are never stored), the weights the
-// N operand.  A unit is 64 rows of I, so a dense FFN has I / 64 units (38 for
-// I = 2432) where decode_tc.cu's 128-row M tiles give it only 19.
+// N operand.  A unit is R rows of I (R = 32 up to 64 tokens, else 64), so a
+// dense FFN has 76 or 38 units at I = 2432 where decode_tc.cu's 128-row M
+// tiles give it only 19.
 //
 // Per unit (MiniMind lesson 13 §0 / §1.2; minimind3.com chapter 4 §4.2):
-//   gate/up   G, U [T x 64] = x [T x H] . Wg/Wu[64 rows, H]^T, K = H in
+//   gate/up   G, U [T x R] = x [T x H] . Wg/Wu[R rows, H]^T, K = H in
 //             stages of nkb 64-wide k-blocks of x, Wg and Wu, each fetched by
 //             one 3-D TMA box (a box of 8 KiB moves ~30 GB/s per SM, one of
-//             32 KiB ~95 GB/s); TMEM, N = 64 each
+//             32 KiB ~95 GB/s); TMEM, N = R each
 //   epilogue  h = SiLU(G) * U, split into a bf16 high part and a bf16
 //             remainder, written as two 128-row A tiles (128-byte swizzle)
-//   down      y_u [T x H] = h . Wd[:, unit's 64 columns]^T, N = 128 output
+//   down      y_u [T x H] = h . Wd[:, unit's R columns]^T, N = 128 output
 //             columns per MMA, two 128-column blocks of y per TMEM pass and
-//             per 32 KiB box of Wd; two TMEM buffers, so that the epilogue
-//             drains one pass while the next accumulates
+//             per box of Wd; two TMEM buffers, so that the epilogue drains
+//             one pass while the next accumulates
 //   partial   y_u (fp32, tokens < T) to global memory, 4-column groups in
 //             token order so that the lanes of a store write one run
 // then one grid barrier and every CTA adds a share of the unit partials in
@@ -30,10 +31,22 @@
 namespace mm {
 
 constexpr int kSwThreads = 320;
-constexpr int kSwRows = 64;                      // rows of I per unit (N of gate/up, K of down)
+
 constexpr int kSwMaxStages = 8;
-constexpr int kSwWTile = kSwRows * 128;          // 8 KiB: 64 weight rows x 64 k
-constexpr int kSwDTile = 128 * 128;              // 16 KiB: 128 rows of Wd x 64 k, or 128 rows of h
+// Unit geometry for R rows of I per unit (R = 32 or 64): h and Wd tiles are
+// K-major with K = R, rows of 2R bytes, 128-byte swizzle for R = 64 and
+// 64-byte swizzle for R = 32.
+template <int R>
+struct SwUnit {
+  static_assert(R == 32 || R == 64, "unit rows");
+  static constexpr int kWTile = R * 128;         // one k-block of the unit's Wg (or Wu) rows
+  static constexpr int kHRow = R * 2;
+  static constexpr int kDTile = 128 * kHRow;     // 128 rows of h, or 128 rows of Wd x R
+  static constexpr int kKSteps = R / 16;         // UMMA k-steps of the down product
+  __device__ static __forceinline__ uint64_t desc(uint32_t saddr) {
+    return R == 64 ? smem_desc_sw128(saddr) : smem_desc_sw64(saddr);
+  }
+};
 constexpr uint32_t kSwTmemCols = 512;
 constexpr uint32_t kSwColG = 0, kSwColU = 64;    // gate/up accumulators
 constexpr uint32_t kSwBufCols = 256;             // y: two buffers of two 128-column blocks
@@ -46,8 +59,8 @@ constexpr size_t kSwSmemBudget = 200 * 1024;
 
 struct SwMaps {
   CUtensorMap x;                  // x as (64, T, H / 64), box 64 x Np x nkb (rows >= T read as 0)
-  CUtensorMap wg, wu;             // [I, H] as (64, I, H / 64), box 64 x 64 x nkb
-  CUtensorMap wd;                 // [H, I] as (I, 128, H / 128), box 64 x 128 x 2
+  CUtensorMap wg, wu;             // [I, H] as (64, I, H / 64), box 64 x R x nkb
+  CUtensorMap wd;                 // [H, I] as (I, 128, H / 128), box R x 128 x 2
 };
 
 struct SwArgs {
@@ -55,7 +68,7 @@ struct SwArgs {
   int nkb;                        // k-blocks per gate/up stage
   uint32_t stage_bytes;           // nkb x tiles + nkb Wg tiles + nkb Wu tiles, or three Wd tiles
   uint32_t xtile;                 // Np * 128 bytes
-  uint32_t h_off;                 // two h tiles (high part, remainder), 16 KiB each
+  uint32_t h_off;                 // two h tiles (high part, remainder), 256 R bytes each
   float* pd;                      // [n_units][H / 4][T][4] fp32 partials
   void* y;                        // [T, H] bf16
   WsHeader* hdr;
@@ -65,8 +78,15 @@ __device__ __forceinline__ float sw_swiglu(float g, float u) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
+template <int R>
 __global__ void __launch_bounds__(kSwThreads, 1)
 decode_sw_kernel(const __grid_constant__ SwMaps M, const SwArgs A) {
+  using U = SwUnit<R>;
+  constexpr int kSwRows = R;
+  constexpr int kSwWTile = U::kWTile;
+  constexpr int kSwHRow = U::kHRow;
+  constexpr int kSwDTile = U::kDTile;
+  constexpr int kSwKSteps = U::kKSteps;
   extern __shared__ unsigned char smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* ring = smem;
@@ -199,11 +219,12 @@ decode_sw_kernel(const __grid_constant__ SwMaps M, const SwArgs A) {
           const uint32_t d = tmem + b * kSwBufCols + q * 128;
           const uint8_t* wd = st + q * kSwDTile;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d, sdesc(hhi + kk * 32), sdesc(wd + kk * 32), idesc_dn, kk ? 1u : 0u);
+          for (int kk = 0; kk < kSwKSteps; ++kk)
+            umma_bf16(d, U::desc(smem_u32(hhi + kk * 32)), U::desc(smem_u32(wd + kk * 32)), idesc_dn,
+                      kk ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d, sdesc(hlo + kk * 32), sdesc(wd + kk * 32), idesc_dn, 1u);
+          for (int kk = 0; kk < kSwKSteps; ++kk)
+            umma_bf16(d, U::desc(smem_u32(hlo + kk * 32)), U::desc(smem_u32(wd + kk * 32)), idesc_dn, 1u);
         }
         umma_commit(&empty[s]);
         ++m_it;
@@ -225,12 +246,13 @@ decode_sw_kernel(const __grid_constant__ SwMaps M, const SwArgs A) {
       if (!warp_wait(&tfull, j & 1, nullptr, hdr, 65)) { ok = false; break; }
       if (j > 0 && !warp_wait(&hempty, (j - 1) & 1, nullptr, hdr, 66)) { ok = false; break; }
       tc_fence_after();
-      // row t of the two h tiles: 64 values = eight 16-byte chunks, chunk c
-      // stored at chunk position c ^ (t % 8); this warp writes chunks
-      // 4 half .. 4 half + 3
+      // row t of the two h tiles: R values in 16-byte chunks, chunk c stored
+      // at chunk position c ^ (t % 8) (128-byte rows) or c ^ ((t / 2) % 4)
+      // (64-byte rows); this warp writes the chunks of columns
+      // half * R / 2 .. (half + 1) * R / 2
       if (quad_live) {
 #pragma unroll 1
-        for (int c0 = half * 32; c0 < half * 32 + 32; c0 += 16) {
+        for (int c0 = half * (kSwRows / 2); c0 < (half + 1) * (kSwRows / 2); c0 += 16) {
           uint32_t gr[16], ur[16];
           tmem_ld_32x32b_x16(tmem + lane_base + kSwColG + c0, gr);
           tmem_ld_32x32b_x16(tmem + lane_base + kSwColU + c0, ur);
@@ -249,7 +271,8 @@ decode_sw_kernel(const __grid_constant__ SwMaps M, const SwArgs A) {
               lo[q] = pack_bf16x2(v0 - __bfloat162float(h0), v1 - __bfloat162float(h1));
             }
             const int chunk = (c0 >> 3) + hc;
-            const uint32_t off = static_cast<uint32_t>(t) * 128 + ((chunk ^ (t & 7)) << 4);
+            const int pos = kSwRows == 64 ? (chunk ^ (t & 7)) : (chunk ^ ((t >> 1) & 3));
+            const uint32_t off = static_cast<uint32_t>(t) * kSwHRow + (pos << 4);
             *reinterpret_cast<uint4*>(hhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             *reinterpret_cast<uint4*>(hlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
@@ -375,16 +398,22 @@ decode_sw_kernel(const __grid_constant__ SwMaps M, const SwArgs A) {
 namespace {
 
 struct SwLayout {
-  int Np, stages, n_units, nkb;
+  int R, Np, stages, n_units, nkb;
   size_t xtile, stage, h_off, smem, pd;
 };
 
 inline size_t sw_round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool sw_layout(int T, int H, int I, SwLayout& L) {
-  if (T < 1 || T > kDecodeSwMaxT || H % 128 != 0 || I % kSwRows != 0) return false;
+  if (T < 1 || T > kDecodeSwMaxT || H % 128 != 0 || I % 64 != 0) return false;
   L.Np = (T + 15) / 16 * 16;
-  L.n_units = I / kSwRows;
+  // 32-row units: twice the streaming CTAs; 64-row units: half the partials
+  // of y, which pays from about 100 tokens (measured: T = 16 / 64 / 100 took
+  // 14.7 / 17.2 / 21.2 us with 32 rows, 15.6 / 17.7 / 20.6 with 64)
+  L.R = L.Np <= 64 ? 32 : 64;
+  const int kSwWTile = L.R * 128;
+  const int kSwDTile = 128 * L.R * 2;
+  L.n_units = I / L.R;
   L.xtile = static_cast<size_t>(L.Np) * 128;
   // the most k-blocks per gate/up stage (larger TMA boxes stream faster)
   // that leave three stages (else two); a stage also holds one pass of Wd
@@ -432,14 +461,16 @@ cudaError_t launch_decode_sw(const void* x, const void* Wg, const void* Wu, cons
     const uint32_t bx[3] = {64, static_cast<uint32_t>(L.Np), static_cast<uint32_t>(L.nkb)};
     if (!make_map_3d(&m.x, x, dx, sx, bx)) return cudaErrorInvalidValue;
     const uint64_t dw[3] = {64, static_cast<uint64_t>(I), static_cast<uint64_t>(H / 64)};
-    const uint32_t bw[3] = {64, static_cast<uint32_t>(kSwRows), static_cast<uint32_t>(L.nkb)};
+    const uint32_t bw[3] = {64, static_cast<uint32_t>(L.R), static_cast<uint32_t>(L.nkb)};
     if (!make_map_3d(&m.wg, Wg, dw, sx, bw)) return cudaErrorInvalidValue;
     if (!make_map_3d(&m.wu, Wu, dw, sx, bw)) return cudaErrorInvalidValue;
     // Wd [H, I] as (i, row within a 128-row block, block)
     const uint64_t sd[2] = {static_cast<uint64_t>(I) * 2, static_cast<uint64_t>(I) * 2 * 128};
     const uint64_t dd[3] = {static_cast<uint64_t>(I), 128, static_cast<uint64_t>(H / 128)};
-    const uint32_t bd[3] = {64, 128, static_cast<uint32_t>(kSwPassBlocks)};
-    if (!make_map_3d(&m.wd, Wd, dd, sd, bd)) return cudaErrorInvalidValue;
+    const uint32_t bd[3] = {static_cast<uint32_t>(L.R), 128, static_cast<uint32_t>(kSwPassBlocks)};
+    if (!make_map_3d(&m.wd, Wd, dd, sd, bd, false,
+                     L.R == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
   }
   SwArgs A;
   memset(&A, 0, sizeof(A));
@@ -451,7 +482,7 @@ cudaError_t launch_decode_sw(const void* x, const void* Wg, const void* Wu, cons
   A.pd = static_cast<float*>(scratch);
   A.y = y;
   A.hdr = hdr;
-  auto fn = decode_sw_kernel;
+  auto fn = L.R == 64 ? decode_sw_kernel<64> : decode_sw_kernel<32>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), L.smem);
   if (e != cudaSuccess) return e;
   int fit = 0;

@@ -481,13 +481,14 @@ bool make_map_16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t out
 }
 
 bool make_map_3d(CUtensorMap* out, const void* ptr, const uint64_t dims[3],
-                 const uint64_t strides[2], const uint32_t box[3], bool is_f16) {
+                 const uint64_t strides[2], const uint32_t box[3], bool is_f16,
+                 CUtensorMapSwizzle swz) {
   using Key = std::tuple<uintptr_t, uint64_t, uint64_t, uint64_t, uint64_t, uint64_t, uint32_t,
-                         uint32_t, uint32_t, bool>;
+                         uint32_t, uint32_t, bool, int>;
   static std::mutex mu;
   static std::map<Key, CUtensorMap> cache;
   const Key key{reinterpret_cast<uintptr_t>(ptr), dims[0], dims[1], dims[2], strides[0],
-                strides[1], box[0], box[1], box[2], is_f16};
+                strides[1], box[0], box[1], box[2], is_f16, static_cast<int>(swz)};
   std::lock_guard<std::mutex> lock(mu);
   auto itc = cache.find(key);
   if (itc != cache.end()) {
@@ -502,7 +503,7 @@ bool make_map_3d(CUtensorMap* out, const void* ptr, const uint64_t dims[3],
   cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = enc(out, is_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                          3, const_cast<void*>(ptr), d, st, bx,
-                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   if (cache.size() > 4096) cache.clear();

@@ -294,6 +294,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same for a tile written with 64-byte swizzle: rows of 64 B (32 16-bit
+// elements), 8-row groups 512 B apart.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address
+  d |= static_cast<uint64_t>(1u) << 16;                    // leading byte offset (unused)
+  d |= static_cast<uint64_t>(512u >> 4) << 32;             // stride byte offset
+  d |= static_cast<uint64_t>(1u) << 46;                    // descriptor version
+  d |= static_cast<uint64_t>(4u) << 61;                    // 64-byte swizzle
+  return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                                   // D format: f32

@@ -169,9 +169,10 @@ bool make_map_16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t out
 
 // TMA tensor map of a 16-bit tensor (bf16, or fp16) viewed in three dimensions (element
 // strides 1, strides[0], strides[1] bytes), box box[0] x box[1] x box[2],
-// 128-byte swizzle, zero fill outside; cached like make_map_16.
+// 128-byte swizzle unless given, zero fill outside; cached like make_map_16.
 bool make_map_3d(CUtensorMap* out, const void* ptr, const uint64_t dims[3],
-                 const uint64_t strides[2], const uint32_t box[3], bool is_f16 = false);
+                 const uint64_t strides[2], const uint32_t box[3], bool is_f16 = false,
+                 CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B);
 
 int num_sms();   // of the current device, looked up once per device
 
