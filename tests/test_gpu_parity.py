@@ -82,6 +82,14 @@ def test_moe_bf16_tensor(T, H, I, E, k, bias):
     full_moe_check(moe_inputs(T, H, I, E, "bf16", seed=7, bias=bias), k, 0.01, "bf16", path="tensor")
 
 
+@pytest.mark.parametrize("T,path", [(300, "tensor"), (300, "simt"), (16, "auto"), (40, "stream_tc"),
+                                    (3, "stream")])
+def test_moe_max_experts_and_topk(T, path):
+    """The build's limits: 64 experts, top-8 (k * E = 512 groups on the
+    tensor path), with every path that takes the shape."""
+    full_moe_check(moe_inputs(T, 256, 192, 64, "bf16", seed=150 + T), 8, 0.01, "bf16", path=path)
+
+
 @pytest.mark.parametrize("T,E,k", [(300, 4, 1), (257, 8, 2)])
 def test_moe_bf16_simt_second_path(T, E, k):
     full_moe_check(moe_inputs(T, 128, 192, E, "bf16", seed=9), k, 0.01, "bf16", path="simt")
