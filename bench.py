@@ -191,15 +191,33 @@ class Step:
         per_expert = 3 * w.H * w.I * (2 if w.dtype == "bf16" else 4)
         return min(self.input_bytes(), min(w.E, w.T * w.k) * per_expert)
 
-    def __call__(self, i, x=None):
+    def outputs(self):
+        """The device tensors a step writes (y, and for MoE topk_idx, topk_w, aux)."""
+        return [self.y] + ([self.idx, self.tw, self.aux] if self.w.kind == "moe" else [])
+
+    def new_outputs(self):
+        """A fresh set of output tensors, views into one contiguous byte buffer
+        (returned too), so that one copy moves all of a step's results."""
+        views, offs, off = [], [], 0
+        for t in self.outputs():
+            offs.append(off)
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        buf = torch.empty(off, dtype=torch.uint8, device=self.y.device)
+        for t, o in zip(self.outputs(), offs):
+            nb = t.numel() * t.element_size()
+            views.append(buf[o:o + nb].view(t.dtype).view(t.shape))
+        return views, buf
+
+    def __call__(self, i, x=None, outs=None):
         s = self.sets[i % len(self.sets)]
         x = s["x"] if x is None else x
+        o = self.outputs() if outs is None else outs
         if self.w.kind == "moe":
             self.mm.moe_forward(x, s["Wr"], s["Wg"], s["Wu"], s["Wd"], self.w.k, self.w.coef,
-                                logit_bias=s.get("logit_bias"), out=self.y, topk_idx=self.idx,
-                                topk_w=self.tw, aux_loss=self.aux, workspace=self.ws)
+                                logit_bias=s.get("logit_bias"), out=o[0], topk_idx=o[1],
+                                topk_w=o[2], aux_loss=o[3], workspace=self.ws)
         else:
-            self.mm.swiglu_ffn(x, s["Wg"], s["Wu"], s["Wd"], out=self.y, workspace=self.ws)
+            self.mm.swiglu_ffn(x, s["Wg"], s["Wu"], s["Wd"], out=o[0], workspace=self.ws)
 
 
 def dist_setup():
@@ -391,42 +409,84 @@ def run_our_arm(args, w):
                 "kernel_ms": k_ms, "launches_timed": nl.value,
                 "flops_per_launch": gate_flops}
 
-    # ---- end to end through the public API: pinned host x in, y/idx/w/aux out
+    # ---- end to end through the public API: pinned host x in, y/idx/w/aux out.
+    # Every step copies its x in and its outputs out; the copies run on their
+    # own streams, double-buffered, so that step i's outputs leave and step
+    # i + 1's input arrives while step i + 1 / step i compute.
     e2e = None
     if args.e2e_steps > 0:
+        nbuf = 2
         x_host = step.cpu["x"].pin_memory()
-        x_dev = torch.empty_like(step.sets[0]["x"])
-        y_host = torch.empty(step.y.shape, dtype=step.y.dtype).pin_memory()
-        outs = [y_host]
-        if w.kind == "moe":
-            outs += [torch.empty(step.idx.shape, dtype=torch.int32).pin_memory(),
-                     torch.empty(step.tw.shape, dtype=torch.float32).pin_memory(),
-                     torch.empty((), dtype=torch.float32).pin_memory()]
-        devs = [step.y] + ([step.idx, step.tw, step.aux] if w.kind == "moe" else [])
+        x_dev = [torch.empty_like(step.sets[0]["x"]) for _ in range(nbuf)]
+        d_sets = [step.new_outputs() for _ in range(nbuf)]
+        d_outs = [v for v, _ in d_sets]
+        d_bufs = [b for _, b in d_sets]
+        h_bufs = [torch.empty(b.shape, dtype=torch.uint8).pin_memory() for b in d_bufs]
         h2d = x_host.numel() * x_host.element_size()
-        d2h = sum(t.numel() * t.element_size() for t in outs)
+        d2h = sum(t.numel() * t.element_size() for t in d_outs[0])
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+        ev_comp = [torch.cuda.Event() for _ in range(nbuf)]
+        ev_out = [torch.cuda.Event() for _ in range(nbuf)]
 
-        def e2e_step(i):
-            x_dev.copy_(x_host, non_blocking=True)
-            step(i, x=x_dev)
-            for hst, d in zip(outs, devs):
-                hst.copy_(d, non_blocking=True)
+        ev_fork = torch.cuda.Event()
 
-        for i in range(3):
-            e2e_step(i)
+        def e2e_step(i, comp):
+            b = i % nbuf
+            if i >= nbuf:
+                s_in.wait_event(ev_comp[b])           # step i - nbuf has read x_dev[b]
+            with torch.cuda.stream(s_in):
+                x_dev[b].copy_(x_host, non_blocking=True)
+                ev_in[b].record(s_in)
+            comp.wait_event(ev_in[b])
+            if i >= nbuf:
+                comp.wait_event(ev_out[b])            # step i - nbuf's outputs have left
+            with torch.cuda.stream(comp):
+                step(i, x=x_dev[b], outs=d_outs[b])
+            ev_comp[b].record(comp)
+            s_out.wait_event(ev_comp[b])
+            with torch.cuda.stream(s_out):
+                h_bufs[b].copy_(d_bufs[b], non_blocking=True)   # all outputs in one copy
+                ev_out[b].record(s_out)
+
+        def e2e_loop(n, comp):
+            ev_fork.record(comp)                      # the copy streams start after this point
+            s_in.wait_event(ev_fork)
+            s_out.wait_event(ev_fork)
+            for i in range(n):
+                e2e_step(i, comp)
+            for b in range(min(nbuf, n)):
+                comp.wait_event(ev_out[b])            # every copy has landed
+
+        e2e_loop(3, stream)
         torch.cuda.synchronize()
+        e2e_graph = None
+        if use_graph:
+            # decode-sized steps: the K steps, their copies and the stream
+            # dependencies captured into one CUDA graph, as for the device timing
+            e2e_graph = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream()
+            cap.wait_stream(stream)
+            with torch.cuda.graph(e2e_graph, stream=cap):
+                e2e_loop(args.e2e_steps, cap)
+            e2e_graph.replay()
+            torch.cuda.synchronize()
         barrier(ws)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for i in range(args.e2e_steps):
-            e2e_step(i)
+        if e2e_graph is not None:
+            e2e_graph.replay()
+        else:
+            e2e_loop(args.e2e_steps, stream)
         e1.record(stream)
         torch.cuda.synchronize()
         ems = max_over_ranks(e0.elapsed_time(e1), ws, dev)
         e2e = {"value": ws * w.T * args.e2e_steps / (ems / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": ems / args.e2e_steps}
+               "ms_per_step": ems / args.e2e_steps,
+               "pipelining": f"copies on their own streams, {nbuf} buffers, one copy each way",
+               "timing": "cuda_graph_replay" if e2e_graph is not None else "stream_launches"}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
