@@ -58,6 +58,7 @@ constexpr int kDtMaxSplit = 4;                  // k-ranges per gate/up block at
 constexpr int kDtReduceChunk = 32;              // partials requested at once in the final sum
 constexpr size_t kDtSmemBudget = 196 * 1024;   // dynamic; static use is ~27 KiB
 constexpr int kDtFusedMinUnits = 64;            // fused variant: (expert, I-block) units at least
+constexpr int kDtMaxLocalUnits = 64;            // speculative: units per CTA at most (cut table)
 constexpr int kDtMaxSlices = 16;                // fused: partial sums per output quad at most
 constexpr int kDtSumChunk = 16;                 // fused: partials requested at once
 
@@ -150,6 +151,12 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
   __shared__ __align__(8) uint64_t full[kDtMaxStages], empty[kDtMaxStages];
   __shared__ __align__(8) uint64_t wbar, lbar, tfull[2], tempty[2], dfull, dempty, drained;
   __shared__ __align__(8) uint64_t hfull, hempty;      // fused: h tiles written / read
+  // speculative streaming: the routing once known (flag, selected experts)
+  // and, per local unit, the stages the producer issued before it dropped
+  // the unit of an unselected expert (-1: not dropped)
+  __shared__ volatile int s_routed;
+  __shared__ volatile unsigned long long s_selected;
+  __shared__ volatile int s_cut[kDtMaxLocalUnits];
   __shared__ uint32_t s_tmem;
   __shared__ float s_bias[MM_MAX_EXPERTS];
   __shared__ int s_first_mb[kDtMaxCtas];        // first output m-block of each CTA's range (-1: empty)
@@ -185,6 +192,9 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
     mbar_init(&hfull, kDtEpiWarps);
     mbar_init(&hempty, 1);
     fence_mbar_init();
+    s_routed = 0;
+    s_selected = 0ull;
+    for (int q = 0; q < kDtMaxLocalUnits; ++q) s_cut[q] = -1;
   }
   if (tid < MM_MAX_EXPERTS) s_bias[tid] = (moe && A.bias != nullptr && tid < A.E) ? A.bias[tid] : 0.f;
   if (warp == 1) {
@@ -313,6 +323,42 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
     const int nb = A.gu_bufs;
     const uint32_t colD = 2u * static_cast<uint32_t>(Np * nb);
     uint8_t* hs = reinterpret_cast<uint8_t*>(hstage);      // tile (part, k-half) at (2 part + kh) * xtile
+    // speculative: expert e's units are dropped once the routing is known
+    // and no token selected e
+    auto dropped = [&](int e) -> bool {
+      if (!s_routed) return false;
+      __threadfence_block();
+      return ((s_selected >> e) & 1ull) == 0ull;
+    };
+    auto wait_routed = [&]() -> bool {
+      const unsigned long long t0 = globaltimer_ns();
+      for (uint32_t n = 0; !s_routed; ++n)
+        if ((n & 63u) == 63u && (globaltimer_ns() - t0 > kWaitLimitNs || n > (1u << 30))) {
+          report_timeout(hdr, 56);
+          return false;
+        }
+      __threadfence_block();
+      return true;
+    };
+    // MMA: stage q of local unit j, once it is full (1), or 0 when the
+    // producer dropped the unit before issuing it; -1 on time-out
+    auto take = [&](int j, int q, int& s) -> int {
+      s = m_it % S;
+      const uint32_t addr = smem_u32(&full[s]), par = (m_it / S) & 1;
+      const unsigned long long t0 = globaltimer_ns();
+      for (uint32_t n = 0;; ++n) {
+        if (mbar_try_wait(addr, par)) {
+          tc_fence_after();
+          return 1;
+        }
+        const int c = s_cut[j];
+        if (c >= 0 && q >= c) return 0;
+        if ((n & 63u) == 63u && (globaltimer_ns() - t0 > kWaitLimitNs || n > (1u << 30))) {
+          report_timeout(hdr, 55);
+          return -1;
+        }
+      }
+    };
     if (ok) {
       if (tid == 0) {
         if (spec) {
@@ -320,25 +366,28 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
           for (int q = 0; q < A.router_stages; ++q) mbar_arrive(&full[q]);
           p_it = A.router_stages;
         }
-        for (int u = cta; ok && u < n_units; u += G) {
+        int j = 0;
+        for (int u = cta; ok && u < n_units; u += G, ++j) {
           const int ti = u / MB_I, mb = u - ti * MB_I, e = spec ? ti : R.touched[ti];
-          for (int kb = 0; kb < KB_H; ++kb) {
+          for (int q = 0; q < KB_H + MB_H; ++q) {
+            if (spec && dropped(e)) {                 // stop; the MMA consumes what was issued
+              s_cut[j] = q;
+              break;
+            }
             int s;
             if (!acquire(s)) { ok = false; break; }
             uint8_t* st = ring + s * SB;
-            mbar_arrive_expect_tx(&full[s], 2 * kDtTileA + xtile);
-            tma_load_2d_hint(st, &M.wg[e], &full[s], kb * 64, mb * 128, pol);
-            tma_load_2d_hint(st + kDtTileA, &M.wu[e], &full[s], kb * 64, mb * 128, pol);
-            tma_load_2d(st + 2 * kDtTileA, &M.x, &full[s], kb * 64, 0);
-            ++p_it;
-          }
-          for (int mbd = 0; ok && mbd < MB_H; ++mbd) {
-            int s;
-            if (!acquire(s)) { ok = false; break; }
-            uint8_t* st = ring + s * SB;
-            mbar_arrive_expect_tx(&full[s], 2 * kDtTileA);
-            tma_load_2d_hint(st, &M.wd[e], &full[s], mb * 128, mbd * 128, pol);
-            tma_load_2d_hint(st + kDtTileA, &M.wd[e], &full[s], mb * 128 + 64, mbd * 128, pol);
+            if (q < KB_H) {
+              mbar_arrive_expect_tx(&full[s], 2 * kDtTileA + xtile);
+              tma_load_2d_hint(st, &M.wg[e], &full[s], q * 64, mb * 128, pol);
+              tma_load_2d_hint(st + kDtTileA, &M.wu[e], &full[s], q * 64, mb * 128, pol);
+              tma_load_2d(st + 2 * kDtTileA, &M.x, &full[s], q * 64, 0);
+            } else {
+              const int mbd = q - KB_H;
+              mbar_arrive_expect_tx(&full[s], 2 * kDtTileA);
+              tma_load_2d_hint(st, &M.wd[e], &full[s], mb * 128, mbd * 128, pol);
+              tma_load_2d_hint(st + kDtTileA, &M.wd[e], &full[s], mb * 128 + 64, mbd * 128, pol);
+            }
             ++p_it;
           }
         }
@@ -349,29 +398,47 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
           for (int q = 0; q < A.router_stages; ++q) umma_commit(&empty[q]);
           m_it = A.router_stages;
         }
-        int j = 0;
+        // j: local unit; jj: units kept (their (G, U), h and y^T protocol)
+        int j = 0, jj = 0;
         for (int u = cta; ok && u < n_units; u += G, ++j) {
-          const int acc = nb == 2 ? (j & 1) : 0, use = nb == 2 ? (j >> 1) : j;
+          const int ti = u / MB_I, e = spec ? ti : 0;
+          const int acc = nb == 2 ? (jj & 1) : 0, use = nb == 2 ? (jj >> 1) : jj;
           if (!mbar_wait(&tempty[acc], (use & 1) ^ 1, nullptr, hdr, 44)) { ok = false; break; }
           tc_fence_after();
           const uint32_t dg = tmem + kDtColGU + acc * 2 * Np, du = dg + Np;
-          for (int kb = 0; kb < KB_H; ++kb) {
+          int q = 0;
+          for (; q < KB_H; ++q) {
             int s;
-            if (!consume(s)) { ok = false; break; }
+            const int r = take(j, q, s);
+            if (r <= 0) { ok = r == 0; break; }
             const uint8_t* st = ring + s * SB;
             const uint8_t* b = st + 2 * kDtTileA;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(dg, sdesc(st + kk * 32), sdesc(b + kk * 32), idesc, (kb || kk) ? 1u : 0u);
+              umma_bf16(dg, sdesc(st + kk * 32), sdesc(b + kk * 32), idesc, (q || kk) ? 1u : 0u);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              umma_bf16(du, sdesc(st + kDtTileA + kk * 32), sdesc(b + kk * 32), idesc, (kb || kk) ? 1u : 0u);
+              umma_bf16(du, sdesc(st + kDtTileA + kk * 32), sdesc(b + kk * 32), idesc, (q || kk) ? 1u : 0u);
             umma_commit(&empty[s]);
             ++m_it;
           }
           if (!ok) break;
+          // keep the unit?  (speculative: once the routing is known)
+          if (spec && !wait_routed()) { ok = false; break; }
+          if (spec && dropped(e)) {
+            // release the unit's remaining issued stages without using them
+            for (; q < KB_H + MB_H; ++q) {
+              int s;
+              const int r = take(j, q, s);
+              if (r <= 0) { ok = r == 0; break; }
+              umma_commit(&empty[s]);
+              ++m_it;
+            }
+            if (!ok) break;
+            continue;
+          }
           umma_commit(&tfull[acc]);
-          if (!mbar_wait(&hfull, j & 1, nullptr, hdr, 53)) { ok = false; break; }
+          if (!mbar_wait(&hfull, jj & 1, nullptr, hdr, 53)) { ok = false; break; }
           tc_fence_after();
           for (int mbd = 0; mbd < MB_H; ++mbd) {
             int s;
@@ -379,20 +446,21 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
             const uint8_t* st = ring + s * SB;
             const uint32_t d = tmem + colD + mbd * Np;
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {           // (k-half, part) = (q >> 1, q & 1)
-              const uint8_t* a = st + (q >> 1) * kDtTileA;
-              const uint8_t* b = hs + (2 * (q & 1) + (q >> 1)) * xtile;
+            for (int h4 = 0; h4 < 4; ++h4) {        // (k-half, part) = (h4 >> 1, h4 & 1)
+              const uint8_t* a = st + (h4 >> 1) * kDtTileA;
+              const uint8_t* b = hs + (2 * (h4 & 1) + (h4 >> 1)) * xtile;
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                umma_bf16(d, sdesc(a + kk * 32), sdesc(b + kk * 32), idesc, (j || q || kk) ? 1u : 0u);
+                umma_bf16(d, sdesc(a + kk * 32), sdesc(b + kk * 32), idesc, (jj || h4 || kk) ? 1u : 0u);
             }
             umma_commit(&empty[s]);
             ++m_it;
           }
           if (!ok) break;
           umma_commit(&hempty);
+          ++jj;
         }
-        if (ok && j > 0) umma_commit(&dfull);
+        if (ok && jj > 0) umma_commit(&dfull);
       }
       if (epi) {
         const int rl = quad * 32 + lane;
@@ -415,15 +483,25 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
             if (warp == 2) route_group(R, T * A.k, A.E, lane);
             for (int a = etid; a < T * A.k; a += en) alpha[R.sel_e[a] * Np + a / A.k] = R.sel_a[a];
             epi_sync();
+            if (etid == 0) {
+              // publish the routing to the producer and the MMA issuer
+              unsigned long long sel = 0ull;
+              for (int e = 0; e < A.E; ++e)
+                if (R.slot_of[e] >= 0) sel |= 1ull << e;
+              s_selected = sel;
+              __threadfence_block();
+              s_routed = 1;
+            }
             if (cta == 0) route_outputs(R, T, A.E, A.coef, A.topk_idx, A.topk_w, A.aux_loss, etid, en, 0);
           }
         }
-        int j = 0;
-        for (int u = cta; ok && u < n_units; u += G, ++j) {
+        int jj = 0;                                   // units kept
+        for (int u = cta; ok && u < n_units; u += G) {
           const int ti = u / MB_I;
-          const int acc = nb == 2 ? (j & 1) : 0, use = nb == 2 ? (j >> 1) : j;
+          if (spec && R.slot_of[ti] < 0) continue;    // unselected expert: dropped
+          const int acc = nb == 2 ? (jj & 1) : 0, use = nb == 2 ? (jj >> 1) : jj;
           if (!warp_wait(&tfull[acc], use & 1, nullptr, hdr, 45)) { ok = false; break; }
-          if (j > 0 && !warp_wait(&hempty, (j - 1) & 1, nullptr, hdr, 54)) { ok = false; break; }
+          if (jj > 0 && !warp_wait(&hempty, (jj - 1) & 1, nullptr, hdr, 54)) { ok = false; break; }
           tc_fence_after();
           const uint32_t tg = tmem + lane_base + kDtColGU + acc * 2 * Np;
 #pragma unroll 1
@@ -450,9 +528,16 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
             mbar_arrive(&hfull);
             mbar_arrive(&tempty[acc]);
           }
+          ++jj;
         }
-        // the CTA's partial of y: pd[cta][t][row], tokens t < T only
-        if (ok && j > 0) {
+        // the CTA's partial of y: pd[cta][t][row], tokens t < T only (zeros
+        // when every unit of the CTA was dropped)
+        if (ok && jj == 0 && cta < n_units) {
+          float* pdst = A.pd + static_cast<size_t>(cta) * T * H + rl;
+          for (int c0 = cbeg; c0 < cend && c0 < T; ++c0)
+            for (int mbd = 0; mbd < MB_H; ++mbd) pdst[static_cast<size_t>(c0) * H + mbd * 128] = 0.f;
+        }
+        if (ok && jj > 0) {
           if (!warp_wait(&dfull, 0, nullptr, hdr, 49)) {
             ok = false;
           } else {
@@ -908,7 +993,9 @@ bool dt_layout(int T, int H, int I, int E, int k, DtLayout& L) {
   if (E > 1 && (E > MM_MAX_EXPERTS || k < 1 || k > MM_MAX_TOPK || k > E)) return false;
   L.Np = (T + 15) / 16 * 16;
   L.Epad = (E + 15) / 16 * 16;
-  L.nt_max = E > 1 ? (E < T * k ? E : T * k) : 1;
+  // MoE: the alpha table has a row per expert (speculative streaming indexes
+  // it by expert), h at most one per expert
+  L.nt_max = E > 1 ? E : 1;
   // a stage holds two 16 KiB weight tiles and one x tile (gate/up), or the
   // x and Wr tiles (router), or a Wd tile and the two Hp tiles (down)
   L.stage = round_up(2 * static_cast<size_t>(kDtTileA) + static_cast<size_t>(L.Np) * 128, 1024);
@@ -939,15 +1026,15 @@ bool dt_layout(int T, int H, int I, int E, int k, DtLayout& L) {
     const size_t kbh = static_cast<size_t>(H / 64);
     const size_t need = std::max(kbh * (xt + wt), (kbh - 1) * xt + kDtTileA);
     if (E > 1 && need > static_cast<size_t>(L.stages) * L.stage) return false;
-    // speculative streaming (fused MoE with at least two assignments per
-    // expert, so that nearly every expert is touched): every expert's units
-    // stream from the start while the router and the routing run; the
+    // speculative streaming (fused MoE): every expert's units stream from
+    // the start while the router and the routing run, and the units of the
+    // experts no token selected are dropped once the routing is known; the
     // router's stages must leave one free, and the gate/up columns of TMEM
     // must stay clear of the router's logits (the last Epad columns)
     L.router_stages = static_cast<int>((need + L.stage - 1) / L.stage);
-    if (L.fused && E > 1 && T * k >= 2 * E && L.router_stages < L.stages &&
+    if (L.fused && E > 1 && L.router_stages < L.stages &&
         2 * L.Np * L.gu_bufs + L.Epad <= static_cast<int>(kDtTmemCols))
-      L.spec = 1;                                    // (nt_max is already E here)
+      L.spec = 1;
   }
   {
     const long long F = static_cast<long long>(H / 128) * L.nt_max * (I / 64);
@@ -997,6 +1084,8 @@ cudaError_t decode_tc_impl(const DtLayout& L, const void* x, const void* Wr,
   if (fit < 1) return cudaErrorInvalidConfiguration;
   int grid = num_sms();
   if (grid > kDtMaxCtas) grid = kDtMaxCtas;
+  // the speculative cut table holds kDtMaxLocalUnits units per CTA
+  if (A.spec && (A.E * ((I + 127) / 128) + grid - 1) / grid > kDtMaxLocalUnits) A.spec = 0;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(grid);
