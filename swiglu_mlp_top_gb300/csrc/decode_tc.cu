@@ -26,12 +26,16 @@
 //      rounds y to bf16 once (deterministic; the weighted sum over the
 //      selected experts is part of the fp32 accumulation).
 //
-// Fused variant (many (expert, I-block) units, few tokens, y^T for all H rows
-// fits in TMEM beside the gate/up accumulators): each unit also streams its
-// 128 columns of Wd_e and multiplies them by its own h, kept in shared memory
-// as the B operand; a CTA's units accumulate y^T in TMEM, the CTA writes one
+// Fused variant (many (expert, I-block) units, y^T for all H rows fits in
+// TMEM beside the gate/up accumulators): each unit also streams its 128
+// columns of Wd_e and multiplies them by its own h, kept in shared memory as
+// the B operand; a CTA's units accumulate y^T in TMEM, the CTA writes one
 // fp32 partial of y, and after a single grid barrier the partials are added in
-// CTA order.  h never reaches global memory.
+// CTA order.  h never reaches global memory.  MoE calls stream speculatively:
+// every expert's units start at once, the router runs on stages the ring
+// then skips and the epilogue warps route meanwhile; once the routing is
+// published, units of experts no token selected stop (the producer records
+// how many of their stages it issued, the MMA issuer releases exactly those).
 //
 // Warp roles (320 threads): warp 0 lane 0 issues TMA, warp 1 lane 0 issues
 // UMMA and owns TMEM, warps 2-9 are the epilogue (TMEM lane quadrant
