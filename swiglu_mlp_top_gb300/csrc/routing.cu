@@ -5,7 +5,9 @@
 // Follows MiniMind lesson 13 "FFN 与 MoE" §1.5 (router equations), §1.6 and
 // step 6 (aux loss), step 4-5 (top-k, renormalisation, per-expert dispatch
 // and index_add_ into y), and minimind3.com chapter 4 §4.3-§4.4.
+#include <algorithm>
 #include <cstring>
+#include <mutex>
 
 #include "mm_kernels.cuh"
 
@@ -599,6 +601,201 @@ dispatch_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, int k,
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Router on the tensor cores (bf16, E <= 64): the same outputs as
+// router_kernel for one 64-token block per CTA.  L = x Wr^T by tcgen05 (x
+// rows as the M operand: 128 rows are read from each x tile, rows past the
+// block's 64 land in TMEM lanes that are never read; Wr padded to EP rows as
+// N), the x and Wr k-blocks fetched as 3-D TMA boxes of nkb k-blocks through
+// a two-stage ring.  Warps 0 and 1 (TMEM lanes 0-63: one token per thread)
+// then take softmax, top-k, alpha, the block's group counts and
+// probability sums (fixed-order reductions) exactly as router_kernel does.
+// ---------------------------------------------------------------------------
+constexpr int kRtStages = 2;
+struct RtMaps {
+  CUtensorMap x;                 // x as (64, T, H / 64), box 64 x 64 x nkb
+  CUtensorMap wr;                // Wr as (64, E, H / 64), box 64 x EP x nkb (rows >= E read as 0)
+};
+
+template <int EP>
+__global__ void __launch_bounds__(kRouteThreads)
+router_tc_kernel(const __grid_constant__ RtMaps M, int64_t T, int H, int E, int k,
+                 const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
+                 float* __restrict__ topk_w, int32_t* __restrict__ blk_cnt,
+                 float* __restrict__ blk_prob, const RouteExtras X, int nkb, uint32_t stage_bytes) {
+  // the dispatch kernel may launch as soon as router blocks start to leave
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ unsigned char rt_raw[];
+  uint8_t* smem = align1024(rt_raw);
+  __shared__ __align__(8) uint64_t full[kRtStages], empty[kRtStages], lbar, drained;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_gcnt[kMaxGroups];
+  __shared__ float s_red[2][EP];
+  __shared__ int s_last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rblk = blockIdx.x;
+  const int nblk = static_cast<int>((T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock);
+  const int64_t t0 = static_cast<int64_t>(rblk) * kRouteTokensPerBlock;
+  const int ntok = static_cast<int>(T - t0 < kRouteTokensPerBlock ? T - t0 : kRouteTokensPerBlock);
+  const int G = k * E;
+  const int nst = (H / 64) / nkb;
+  constexpr uint32_t kXTile = 64 * 128;          // 64 rows x one k-block
+  constexpr uint32_t kWTile = EP * 128;
+  WsHeader* hdr = X.hdr;
+
+  if (tid == 0) {
+    for (int q = 0; q < kRtStages; ++q) {
+      mbar_init(&full[q], 1);
+      mbar_init(&empty[q], 1);
+    }
+    mbar_init(&lbar, 1);
+    mbar_init(&drained, 1);
+    fence_mbar_init();
+  }
+  for (int g = tid; g < G; g += kRouteThreads) s_gcnt[g] = 0;
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, 64);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  bool ok = true;
+
+  if (tid == 0) {
+    // producer: stage q = nkb x tiles, then nkb Wr tiles
+    for (int q = 0; ok && q < nst; ++q) {
+      const int sl = q % kRtStages;
+      if (!mbar_wait(&empty[sl], ((q / kRtStages) & 1) ^ 1, nullptr, hdr, 62)) { ok = false; break; }
+      uint8_t* st = smem + sl * stage_bytes;
+      mbar_arrive_expect_tx(&full[sl], static_cast<uint32_t>(nkb) * (kXTile + kWTile));
+      tma_load_3d(st, &M.x, &full[sl], 0, static_cast<int32_t>(t0), q * nkb);
+      tma_load_3d(st + nkb * kXTile, &M.wr, &full[sl], 0, 0, q * nkb);
+    }
+  }
+  if (tid == 32) {
+    // MMA issuer: L[t, e] += x_t . Wr_e over the k-blocks
+    const uint32_t idesc = idesc_bf16_f32(128, EP);
+    for (int q = 0; ok && q < nst; ++q) {
+      const int sl = q % kRtStages;
+      if (!mbar_wait(&full[sl], (q / kRtStages) & 1, nullptr, hdr, 63)) { ok = false; break; }
+      tc_fence_after();
+      const uint8_t* st = smem + sl * stage_bytes;
+      for (int kl = 0; kl < nkb; ++kl) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(tmem, smem_desc_sw128(smem_u32(st + kl * kXTile + kk * 32)),
+                    smem_desc_sw128(smem_u32(st + nkb * kXTile + kl * kWTile + kk * 32)), idesc,
+                    (q | kl | kk) ? 1u : 0u);
+      }
+      umma_commit(&empty[sl]);
+    }
+    if (ok) umma_commit(&lbar);
+  }
+  if (warp < 2) {
+    const int t = warp * 32 + lane;              // TMEM lane = token of the block
+    const bool valid = t < ntok;
+    ok = warp_wait(&lbar, 0, nullptr, hdr, 64) && ok;
+    tc_fence_after();
+    float p[EP];
+    if (ok) {
+#pragma unroll
+      for (int c0 = 0; c0 < EP; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) p[c0 + j] = __uint_as_float(r[j]);
+      }
+      float m = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < EP; ++e) {
+        if (e < E) {
+          p[e] += bias != nullptr ? bias[e] : 0.f;
+          m = fmaxf(m, p[e]);
+        }
+      }
+      float z = 0.f;
+#pragma unroll
+      for (int e = 0; e < EP; ++e) {
+        p[e] = e < E ? expf(p[e] - m) : 0.f;
+        z += p[e];
+      }
+#pragma unroll
+      for (int e = 0; e < EP; ++e) p[e] = p[e] / z;
+      // top-k: k arg-max passes in expert order, strict comparison (lower index first)
+      uint64_t taken = 0;
+      float sel_sum = 0.f;
+      int sel_e[MM_MAX_TOPK];
+      float sel_p[MM_MAX_TOPK];
+#pragma unroll
+      for (int sl = 0; sl < MM_MAX_TOPK; ++sl) {
+        sel_e[sl] = 0;
+        sel_p[sl] = 0.f;
+        if (sl < k) {
+          float bp = -1.f;
+          int be = 0;
+#pragma unroll
+          for (int e = 0; e < EP; ++e)
+            if (e < E && !((taken >> e) & 1ull) && p[e] > bp) {
+              bp = p[e];
+              be = e;
+            }
+          taken |= 1ull << be;
+          sel_sum += bp;
+          sel_e[sl] = be;
+          sel_p[sl] = bp;
+        }
+      }
+      if (valid) {
+        const float inv = sel_sum + 1e-20f;
+#pragma unroll
+        for (int sl = 0; sl < MM_MAX_TOPK; ++sl) {
+          if (sl < k) {
+            topk_idx[(t0 + t) * k + sl] = sel_e[sl];
+            topk_w[(t0 + t) * k + sl] = sel_p[sl] / inv;
+            atomicAdd(&s_gcnt[sl * E + sel_e[sl]], 1);
+          }
+        }
+      }
+      // the block's probability sums per expert: fixed butterfly order
+#pragma unroll
+      for (int e = 0; e < EP; ++e) {
+        float v = valid ? p[e] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) s_red[warp][e] = v;
+      }
+    }
+  }
+  ok = __syncthreads_and(ok);
+  if (ok) {
+    if (tid < E) blk_prob[static_cast<int64_t>(rblk) * E + tid] = s_red[0][tid] + s_red[1][tid];
+    for (int g = tid; g < G; g += kRouteThreads) blk_cnt[static_cast<int64_t>(rblk) * G + g] = s_gcnt[g];
+  }
+  if (tid == 32) {
+    umma_commit(&drained);                       // every issued UMMA has finished
+    mbar_wait(&drained, 0, nullptr, hdr, 65);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 64);
+  // route-only calls: as router_kernel
+  if (!X.do_scan || !ok) return;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(&X.hdr->route_done, 1u) == static_cast<unsigned>(nblk - 1));
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    scan_block(E, k, nblk, T, X, blk_cnt, blk_prob);
+    if (tid == 0) X.hdr->route_done = 0u;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
@@ -636,6 +833,40 @@ static cudaError_t launch_router_t(const void* x, const void* Wr, const float* b
 #undef MM_ROUTER_CASE
 }
 
+// Tensor-core router for bf16 (H a multiple of 64, E <= 64): nkb k-blocks
+// per stage (the most, up to 4, that divide H / 64).
+template <int EP>
+static cudaError_t launch_router_tc(const void* x, const void* Wr, const float* bias, int64_t T,
+                                    int H, int E, int k, int32_t* topk_idx, float* topk_w,
+                                    int32_t* blk_cnt, float* blk_prob, const RouteExtras& X,
+                                    cudaStream_t st) {
+  const int KB = H / 64;
+  int nkb = 4;
+  while (KB % nkb != 0) --nkb;
+  const size_t xt = 64 * 128, wt = static_cast<size_t>(EP) * 128;
+  // the A read of a stage's last x tile spans 128 rows
+  size_t stage = std::max(nkb * (xt + wt), (nkb - 1) * xt + 2 * xt);
+  stage = (stage + 1023) / 1024 * 1024;
+  const size_t smem = kRtStages * stage + 1024;
+  static RtMaps m;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  const uint64_t sx[2] = {static_cast<uint64_t>(H) * 2, 128};
+  const uint64_t dx[3] = {64, static_cast<uint64_t>(T), static_cast<uint64_t>(KB)};
+  const uint32_t bx[3] = {64, static_cast<uint32_t>(kRouteTokensPerBlock), static_cast<uint32_t>(nkb)};
+  if (!make_map_3d(&m.x, x, dx, sx, bx)) return cudaErrorInvalidValue;
+  const uint64_t dw[3] = {64, static_cast<uint64_t>(E), static_cast<uint64_t>(KB)};
+  const uint32_t bw[3] = {64, static_cast<uint32_t>(EP), static_cast<uint32_t>(nkb)};
+  if (!make_map_3d(&m.wr, Wr, dw, sx, bw)) return cudaErrorInvalidValue;
+  auto fn = router_tc_kernel<EP>;
+  cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem);
+  if (err != cudaSuccess) return err;
+  const int nblk = static_cast<int>((T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock);
+  fn<<<nblk, kRouteThreads, smem, st>>>(m, T, H, E, k, bias, topk_idx, topk_w, blk_cnt, blk_prob, X,
+                                        nkb, static_cast<uint32_t>(stage));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_router(int dtype, const void* x, const void* Wr, const float* bias, int64_t T,
                           int H, int E, int k, int32_t* topk_idx, float* topk_w, int32_t* blk_cnt,
                           float* blk_prob, const RouteOut& out, WsHeader* hdr, cudaStream_t st) {
@@ -648,6 +879,15 @@ cudaError_t launch_router(int dtype, const void* x, const void* Wr, const float*
   X.coef = out.coef;
   X.do_scan = out.do_scan;
   X.hdr = hdr;
+  const bool tc_ok = dtype == kDtypeBF16 && H % 64 == 0 && E <= 64 &&
+                     (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && (reinterpret_cast<uintptr_t>(Wr) & 15u) == 0;
+  if (tc_ok) {
+    if (E <= 16)
+      return launch_router_tc<16>(x, Wr, bias, T, H, E, k, topk_idx, topk_w, blk_cnt, blk_prob, X, st);
+    if (E <= 32)
+      return launch_router_tc<32>(x, Wr, bias, T, H, E, k, topk_idx, topk_w, blk_cnt, blk_prob, X, st);
+    return launch_router_tc<64>(x, Wr, bias, T, H, E, k, topk_idx, topk_w, blk_cnt, blk_prob, X, st);
+  }
   if (dtype == kDtypeBF16)
     return launch_router_t<__nv_bfloat16>(x, Wr, bias, T, H, E, k, topk_idx, topk_w, blk_cnt,
                                           blk_prob, X, st);
