@@ -468,6 +468,10 @@ dispatch_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, int k,
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+  // this block's selections, requested together with the counts below
+  __shared__ int s_sel[kRouteTokensPerBlock * MM_MAX_TOPK];
+  for (int a = tid; a < ntok * k; a += kRouteThreads) s_sel[a] = topk_idx[tok0 * k + a];
+
   // group totals and this block's bases: warp w sums a run of router blocks,
   // lane g its group (all counts of the run requested at once), then the
   // warps' partial sums are added in warp order
@@ -478,12 +482,12 @@ dispatch_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, int k,
       const int g = g0 + lane;
       int all = 0, before = 0;
       if (g < G) {
-        for (int bb = b0; bb < b1; bb += 8) {
-          int c[8];
+        for (int bb = b0; bb < b1; bb += 32) {
+          int c[32];                         // one round of requests for a run of 32 blocks
 #pragma unroll
-          for (int j = 0; j < 8; ++j) c[j] = (bb + j < b1) ? blk_cnt[static_cast<int64_t>(bb + j) * G + g] : 0;
+          for (int j = 0; j < 32; ++j) c[j] = (bb + j < b1) ? blk_cnt[static_cast<int64_t>(bb + j) * G + g] : 0;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int j = 0; j < 32; ++j) {
             all += c[j];
             before += (bb + j < b) ? c[j] : 0;
           }
@@ -562,7 +566,7 @@ dispatch_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, int k,
     int e = -1, rank = 0;
     if (warp < 2) {
       const int tl = warp * 32 + lane;
-      e = (tl < ntok) ? topk_idx[(tok0 + tl) * k + s] : -1;
+      e = (tl < ntok) ? s_sel[tl * k + s] : -1;
       const unsigned peers = __match_any_sync(0xffffffffu, e);
       rank = __popc(peers & ((1u << lane) - 1u));
       if (warp == 0 && e >= 0 && lane == __ffs(peers) - 1) s_w0cnt[e] = __popc(peers);
@@ -632,6 +636,7 @@ router_tc_kernel(const __grid_constant__ RtMaps M, int64_t T, int H, int E, int 
   __shared__ uint32_t s_tmem;
   __shared__ int s_gcnt[kMaxGroups];
   __shared__ float s_red[2][EP];
+  __shared__ float s_bias[EP];
   __shared__ int s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rblk = blockIdx.x;
@@ -654,6 +659,7 @@ router_tc_kernel(const __grid_constant__ RtMaps M, int64_t T, int H, int E, int 
     fence_mbar_init();
   }
   for (int g = tid; g < G; g += kRouteThreads) s_gcnt[g] = 0;
+  if (tid < EP) s_bias[tid] = (bias != nullptr && tid < E) ? bias[tid] : 0.f;
   if (warp == 1) {
     tmem_alloc(&s_tmem, 64);
     tmem_relinquish();
@@ -713,7 +719,7 @@ router_tc_kernel(const __grid_constant__ RtMaps M, int64_t T, int H, int E, int 
 #pragma unroll
       for (int e = 0; e < EP; ++e) {
         if (e < E) {
-          p[e] += bias != nullptr ? bias[e] : 0.f;
+          p[e] += s_bias[e];
           m = fmaxf(m, p[e]);
         }
       }
