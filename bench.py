@@ -57,7 +57,7 @@ def decode_kernel_name(w):
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
 # gate/up GEMM, from an ncu capture of the current kernel on this workload;
 # None where no capture of the current kernel exists.
-GATEUP_TRAFFIC_BYTES = {"moe_e8k2_t16384_skew": 163.404032e6 + 129.638144e6}
+GATEUP_TRAFFIC_BYTES = {"moe_e8k2_t16384_skew": 163.514112e6 + 129.354752e6}
 # The same for the decode kernel that streams the weights (one launch per step).
 DECODE_TRAFFIC_BYTES = {"decode_moe_e8k2_t64": 89.903104e6 + 2.921728e6,
                         "decode_moe_e8k2_t16": 89.82784e6 + 2.927104e6,
