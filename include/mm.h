@@ -214,7 +214,8 @@ typedef enum {
   MM_KERNEL_DISPATCH = 3,   /* token permute into expert-contiguous rows    */
   MM_KERNEL_GATEUP = 4,     /* gate/up GEMM with the SwiGLU epilogue        */
   MM_KERNEL_DOWN = 5,       /* down GEMM with the alpha-scaled combine      */
-  MM_KERNEL_WCONVERT = 6,   /* bf16 -> fp16 copy of the down weights        */
+  MM_KERNEL_WCONVERT = 6,   /* unused: the fp16 copy of the down weights is
+                               made inside the gate/up kernel                */
   MM_KERNEL_DECODE = 7      /* decode-sized weight-streaming kernel (whole call) */
 } mm_kernel_id;
 

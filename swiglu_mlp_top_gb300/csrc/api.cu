@@ -173,46 +173,6 @@ namespace {
 
 inline char* ws_at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
 
-// A second stream per device for work that may overlap the caller's stream
-// within one call: forked from and joined back into the caller's stream with
-// events (also inside a CUDA graph capture, where it becomes a parallel
-// branch).  Created on first use; never destroyed.
-struct SideStream {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-};
-cudaError_t side_fork(cudaStream_t st, SideStream** out) {
-  constexpr int kMaxDev = 64;
-  static std::mutex mu;
-  static SideStream per_dev[kMaxDev];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-  SideStream& s = per_dev[dev];
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (s.stream == nullptr) {
-      e = cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking);
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
-      if (e != cudaSuccess) {
-        s.stream = nullptr;
-        return e;
-      }
-    }
-  }
-  e = cudaEventRecord(s.fork, st);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(s.stream, s.fork, 0);
-  *out = &s;
-  return e;
-}
-cudaError_t side_join(cudaStream_t st, SideStream* s) {
-  cudaError_t e = cudaEventRecord(s->join, s->stream);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, s->join, 0);
-  return e;
-}
-
 // ----------------------------------------------------------- measurement hooks
 std::atomic<uint64_t> g_launches{0};
 
@@ -329,13 +289,12 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
   const void* wd[1] = {Wd};
   cudaError_t e;
   if (p == MM_PATH_TENSOR) {
+    // the gate/up kernel also makes the fp16 copy of Wd that the down GEMM reads
     void* wd16 = ws_at(workspace, sizeof(WsHeader) + dense_h_bytes(T, I, dtype));
     const void* wd16p[1] = {wd16};
-    e = counted_launch(MM_KERNEL_WCONVERT, st, [&] {
-      return launch_convert_bf16_to_f16(wd, 1, static_cast<int64_t>(H) * I, wd16, st);
+    e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
+      return launch_gateup_tc(x, T, H, I, g, wg, wu, h, wd, 1, wd16, hdr, st);
     });
-    if (e != cudaSuccess) return cuda_fail(e, "wd convert");
-    e = counted_launch(MM_KERNEL_GATEUP, st, [&] { return launch_gateup_tc(x, T, H, I, g, wg, wu, h, hdr, st); });
     if (e != cudaSuccess) return cuda_fail(e, "gateup_tc");
     e = counted_launch(MM_KERNEL_DOWN, st, [&] { return launch_down_tc(h, T, H, I, g, wd16p, ep, hdr, st); });
     if (e != cudaSuccess) return cuda_fail(e, "down_tc");
@@ -447,35 +406,18 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
   });
   if (e != cudaSuccess) return cuda_fail(e, "dispatch");
 
-  // tensor path: the fp16 copy of Wd runs on the library's side stream,
-  // concurrently with the gate/up GEMM (tensor-bound, HBM mostly idle), and
-  // is joined before the down GEMM
-  SideStream* side = nullptr;
-  if (p == MM_PATH_TENSOR) {
-    e = side_fork(st, &side);
-    if (e != cudaSuccess) return cuda_fail(e, "side stream fork");
-    e = counted_launch(MM_KERNEL_WCONVERT, side->stream, [&] {
-      return launch_convert_bf16_to_f16(Wd, E, static_cast<int64_t>(H) * I, wd16, side->stream);
-    });
-    if (e != cudaSuccess) {
-      side_join(st, side);
-      return cuda_fail(e, "wd convert");
-    }
-  }
-  // gate/up over all k*E (slot, expert) groups at once
+  // gate/up over all k*E (slot, expert) groups at once; on the tensor path
+  // the same kernel makes the fp16 copy of Wd that the down GEMM reads, with
+  // its epilogue warps while the tensor pipe runs (HBM is mostly idle then)
   GroupRows gu{offsets, k * E, 0, E};
   if (p == MM_PATH_TENSOR)
     e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
-      return launch_gateup_tc(xp, rows, H, I, gu, Wg, Wu, h, hdr, st);
+      return launch_gateup_tc(xp, rows, H, I, gu, Wg, Wu, h, Wd, E, wd16, hdr, st);
     });
   else
     e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
       return launch_gateup_simt(dtype, xp, rows, H, I, gu, Wg, Wu, h, st);
     });
-  if (side != nullptr) {
-    const cudaError_t ej = side_join(st, side);
-    if (e == cudaSuccess) e = ej;
-  }
   if (e != cudaSuccess) return cuda_fail(e, "gateup");
   // down: one phase per slot; the k contributions of a token are summed in
   // fp32 in slot order and rounded once

@@ -42,9 +42,10 @@ constexpr int kBTile = (kN / 2) * kTcBK * 2;             // 16 KiB: this CTA's h
 constexpr int kRingKb = 6;                               // k-blocks in the ring
 constexpr int kAccStride = 256;                          // TMEM columns per accumulator
 // Epilogue: 8 warps; warp w reads TMEM lanes 32*(w%4).. (its rows) and
-// handles half w/4 of the tile's columns.  gate/up stages each 32-row x
-// 32-column fp16 piece in the 64-byte-swizzled layout of a TMA box (2 KiB
-// per warp) and writes it with one tensor store.
+// handles half w/4 of the tile's columns, through a 2 KiB staging tile per
+// warp: gate/up stages each 32-row x 32-column fp16 piece in the
+// 64-byte-swizzled layout of a TMA box and writes it with one tensor store;
+// down transposes 32-row x 16-column fp32 pieces through it.
 constexpr int kEpiWarps = 8;
 constexpr int kStageEpi = kEpiWarps * 32 * 64;           // 16 KiB
 constexpr int kWarpProducer = kEpiWarps, kWarpMma = kEpiWarps + 1;
@@ -160,12 +161,15 @@ __device__ __forceinline__ void epilogue_up(uint32_t tb, const TileInfo& ti, int
   }
 }
 
-// down: 128 y columns (half `half` of the tile's 256) of one row, scaled by
-// alpha: Store -> y (x's dtype); First -> acc32 = v; Accum -> acc32 += v;
-// Last -> y = round(acc32 + v).  The row's token and alpha (two dependent
-// global loads) and the first chunk of the running fp32 sum are requested
-// before the tile's accumulator is ready; each later chunk of the sum is
-// requested while the previous chunk is being processed.
+// down: 128 y columns (half `half` of the tile's 256) of the warp's 32 rows,
+// scaled by each row's alpha: Store -> y (x's dtype); First -> acc32 = v;
+// Accum -> acc32 += v; Last -> y = round(acc32 + v).  The rows are tokens
+// scattered over y / acc32, so a thread-per-row store would touch 32 lines
+// per instruction.  Instead each 16-column piece goes TMEM -> registers
+// (thread = row) -> the warp's 64-byte-row staging tile -> back out with
+// lane l on row 8i + l/4, columns 4(l%4)..+3: every global access of the
+// warp then covers 8 rows x 64 contiguous bytes.  The running sum of the
+// next piece is requested before the current piece is processed.
 struct DownRow {
   int64_t tok;
   float alpha;
@@ -192,59 +196,139 @@ __device__ __forceinline__ bool down_reads_sum(const DownEpilogue& ep) {
   return ep.mode == kCombineAccum || ep.mode == kCombineLast;
 }
 
-// chunk c (32 columns) of the running sum for this row, if the mode reads it
-__device__ __forceinline__ void down_prefetch(const DownRow& d, const TileInfo& ti, int H,
-                                              const DownEpilogue& ep, int half, int c,
-                                              float4 (&pre)[8]) {
-  const int col0 = ti.n0 + half * (kN / 2) + c * 32;
-  if (d.valid && col0 < H && down_reads_sum(ep)) {
-    const float4* a4 = reinterpret_cast<const float4*>(ep.acc32 + d.tok * H + col0);
+constexpr int kDnPiece = 16;                    // columns per staged piece
+
+// Rows this lane serves in the transposed phase: 8i + lane/4, i = 0..3.
+struct DownLanes {
+  int64_t off[4];     // element offset of the row's first column of the tile half
+  uint32_t valid;     // bit i: row 8i + lane/4 holds an assignment
+};
+
+__device__ __forceinline__ DownLanes down_lanes(const DownRow& d, const TileInfo& ti, int H,
+                                                int half, int lane) {
+  DownLanes L;
+  const uint32_t vmask = __ballot_sync(0xffffffffu, d.valid);
+  const int col0 = ti.n0 + half * (kN / 2);
+  L.valid = 0;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) pre[q] = a4[q];
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + (lane >> 2);
+    const long long tok = __shfl_sync(0xffffffffu, static_cast<long long>(d.tok), r);
+    L.off[i] = tok * H + col0 + 4 * (lane & 3);
+    L.valid |= ((vmask >> r) & 1u) << i;
+  }
+  return L;
+}
+
+// the running sum at piece c for the lane's four rows, if the mode reads it
+__device__ __forceinline__ void down_prefetch(const DownLanes& L, const DownEpilogue& ep, int c,
+                                              float4 (&pre)[4]) {
+  if (!down_reads_sum(ep)) return;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if ((L.valid >> i) & 1u)
+      pre[i] = __ldcg(reinterpret_cast<const float4*>(ep.acc32 + L.off[i] + c * kDnPiece));
+}
+
+__device__ __forceinline__ void epilogue_down(uint32_t tb, const DownRow& d, const DownLanes& L,
+                                              const TileInfo& ti, int H, const DownEpilogue& ep,
+                                              int half, int lane, uint8_t* wstage,
+                                              float4 (&pre)[4]) {
+  const int col0 = ti.n0 + half * (kN / 2);
+  constexpr int kPieces = kN / 2 / kDnPiece;
+  const uint32_t st0 = smem_u32(wstage);
+#pragma unroll 1
+  for (int c = 0; c < kPieces; ++c) {
+    if (col0 + c * kDnPiece >= H) break;         // warp-uniform: past the last column
+    uint32_t r[16];
+    tmem_ld_32x32b_x16(tb + half * (kN / 2) + c * kDnPiece, r);
+    float4 nxt[4];
+    if (c + 1 < kPieces && col0 + (c + 1) * kDnPiece < H) down_prefetch(L, ep, c + 1, nxt);
+    tmem_ld_wait();
+    __syncwarp();                                // the previous piece has been read back
+    // row `lane`: 64 bytes, 16-byte chunk q at q ^ ((lane >> 1) & 3)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t a = st0 + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4);
+      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                   "f"(d.alpha * __uint_as_float(r[4 * q])), "f"(d.alpha * __uint_as_float(r[4 * q + 1])),
+                   "f"(d.alpha * __uint_as_float(r[4 * q + 2])), "f"(d.alpha * __uint_as_float(r[4 * q + 3]))
+                   : "memory");
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = 8 * i + (lane >> 2);
+      const uint32_t a = st0 + row * 64 + (((lane & 3) ^ ((row >> 1) & 3)) << 4);
+      float4 v;
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a) : "memory");
+      if (!((L.valid >> i) & 1u)) continue;
+      if (down_reads_sum(ep)) {
+        v.x += pre[i].x; v.y += pre[i].y; v.z += pre[i].z; v.w += pre[i].w;
+      }
+      const int64_t o = L.off[i] + c * kDnPiece;
+      if (ep.mode == kCombineFirst || ep.mode == kCombineAccum) {
+        __stcg(reinterpret_cast<float4*>(ep.acc32 + o), v);
+      } else {
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(ep.y) + o) =
+            make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pre[i] = nxt[i];
   }
 }
 
-__device__ __forceinline__ void epilogue_down(uint32_t tb, const DownRow& d, const TileInfo& ti,
-                                              int H, const DownEpilogue& ep, int half,
-                                              float4 (&pre)[8]) {
-  const int col0 = ti.n0 + half * (kN / 2);
-  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(ep.y) + d.tok * H + col0;
-  float* acc32 = ep.acc32 + d.tok * H + col0;
-  constexpr int kChunks = kN / 2 / 32;
+// --------------------------------------------------------- fp16 copy of Wd
+// The copy works in batches of four 16-byte vectors per epilogue thread
+// (16 KiB per CTA): vectors v + t + j * 256 of one index space over the
+// matrices, below v1.  A tile's first batch is requested before the
+// epilogue waits for the tile's accumulator and written after its epilogue,
+// so the load latency hides behind the wait; the bf16 weights are read once
+// (evict-first), the fp16 copy stays in L2 for the down GEMM.
+constexpr int kCvStride = kEpiWarps * 32;
+constexpr int kCvBatch = 4 * kCvStride;
+
+__device__ __forceinline__ void cv_load(const WdConvert& cv, int64_t v, int64_t v1, int t,
+                                        uint4 (&raw)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int64_t u = v + t + j * kCvStride;
+    if (u < v1) {
+      const int64_t m = u / cv.nvec;
+      raw[j] = __ldcs(static_cast<const uint4*>(cv.src.p[m]) + (u - m * cv.nvec));
+    }
+  }
+}
+
+__device__ __forceinline__ void cv_store(const WdConvert& cv, int64_t v, int64_t v1, int t,
+                                         const uint4 (&raw)[4]) {
+  uint4* dst = reinterpret_cast<uint4*>(cv.dst);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int64_t u = v + t + j * kCvStride;
+    if (u < v1) {
+      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw[j]);
+      uint4 out;
+      uint32_t* o = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(b[q]);
+        o[q] = pack_f16x2(f.x, f.y);
+      }
+      __stcg(dst + u, out);
+    }
+  }
+}
+
+// the batches of [v0, v1) from v onwards, one after the other
+__device__ __forceinline__ void cv_rest(const WdConvert& cv, int64_t v, int64_t v1, int t) {
 #pragma unroll 1
-  for (int c = 0; c < kChunks; ++c) {
-    const bool live = d.valid && col0 + c * 32 < H;
-    float4 nxt[8];
-    if (c + 1 < kChunks) down_prefetch(d, ti, H, ep, half, c + 1, nxt);
-    uint32_t r[32];
-    tmem_ld_32x32b_x32(tb + half * (kN / 2) + c * 32, r);
-    tmem_ld_wait();
-    if (live) {
-      float v[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = d.alpha * __uint_as_float(r[j]);
-      if (down_reads_sum(ep)) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          v[4 * q] += pre[q].x; v[4 * q + 1] += pre[q].y; v[4 * q + 2] += pre[q].z; v[4 * q + 3] += pre[q].w;
-        }
-      }
-      if (ep.mode == kCombineFirst || ep.mode == kCombineAccum) {
-        float4* a4 = reinterpret_cast<float4*>(acc32 + c * 32);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) a4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-      } else {
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          d4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                             pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-      }
-    }
-    if (c + 1 < kChunks) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q) pre[q] = nxt[q];
-    }
+  for (; v < v1; v += kCvBatch) {
+    uint4 raw[4];
+    cv_load(cv, v, v1, t, raw);
+    cv_store(cv, v, v1, t, raw);
   }
 }
 
@@ -255,7 +339,7 @@ template <int OP, int MAXW>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g, const int K,
                     const int NCOLS, __half* __restrict__ hout, const DownEpilogue ep,
-                    WsHeader* hdr, const int dep_mainloop) {
+                    const WdConvert cv, WsHeader* hdr, const int dep_mainloop) {
   constexpr int kOutCols = OpTraits<OP>::kOutCols;
   extern __shared__ unsigned char smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -389,12 +473,25 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
     // ------------------------------------------------ epilogue (warps 0-7, both CTAs)
     const int quad = warp & 3, half = warp >> 2;
     const int row = quad * 32 + lane;
-    uint8_t* wstage = sEpi + warp * 32 * 64;     // gate/up: this warp's staging tile
+    uint8_t* wstage = sEpi + warp * 32 * 64;     // this warp's staging tile
     const uint32_t te0 = mapa_shared(smem_u32(&tempty[0]), 0);
     const uint32_t te1 = mapa_shared(smem_u32(&tempty[1]), 0);
     // the running fp32 sum is the previous kernel's output
     if (OP == kOpDown && (ep.mode == kCombineAccum || ep.mode == kCombineLast))
       asm volatile("griddepcontrol.wait;" ::: "memory");
+    // gate/up: this CTA's share of the fp16 Wd copy, one piece before each
+    // of its tiles (all of it if it has none).  The previous kernel (and so
+    // any earlier reader of the copy) has finished first.
+    int64_t cv0 = 0, cv1 = 0;
+    int n_local = 0;
+    if (OP == kOpUp && cv.n_mat > 0) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      const int64_t nv = cv.nvec * cv.n_mat;
+      cv0 = nv * blockIdx.x / gridDim.x;
+      cv1 = nv * (blockIdx.x + 1) / gridDim.x;
+      n_local = cluster < total ? (total - cluster + n_clusters - 1) / n_clusters : 0;
+      if (n_local == 0) cv_rest(cv, cv0, cv1, threadIdx.x);
+    }
     int local = 0;
     for (int tile = cluster; tile < total; tile += n_clusters, ++local) {
       const TileInfo ti = decode_tile(tile, s_off, s_tstart, g.G, g.n_weights, n_tiles, kOutCols,
@@ -402,11 +499,20 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       DownRow dr{0, 1.0f, false};
-      float4 pre[8];
+      DownLanes dl;
+      float4 pre[4];
       if constexpr (OP == kOpDown) {
         // independent of the MMAs: requested while they run
         dr = down_row_info(ti, ep, row);
-        down_prefetch(dr, ti, NCOLS, ep, half, 0, pre);
+        dl = down_lanes(dr, ti, NCOLS, half, lane);
+        if (ti.n0 + half * (kN / 2) < NCOLS) down_prefetch(dl, ep, 0, pre);
+      }
+      int64_t ca = 0, cb = 0;           // this tile's piece of the Wd copy
+      uint4 craw[4];
+      if (OP == kOpUp && n_local > 0) {
+        ca = cv0 + (cv1 - cv0) * local / n_local;
+        cb = cv0 + (cv1 - cv0) * (local + 1) / n_local;
+        cv_load(cv, ca, cb, threadIdx.x, craw);
       }
       if (!warp_wait(&tfull[acc], aph, abort, hdr, 6)) break;
       tc_fence_after();
@@ -414,10 +520,14 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
       if constexpr (OP == kOpUp)
         epilogue_up(tb, ti, NCOLS, hout, row, half, wstage, &P.out);
       else
-        epilogue_down(tb, dr, ti, NCOLS, ep, half, pre);
+        epilogue_down(tb, dr, dl, ti, NCOLS, ep, half, lane, wstage, pre);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc ? te1 : te0);
+      if (OP == kOpUp && ca < cb) {
+        cv_store(cv, ca, cb, threadIdx.x, craw);
+        cv_rest(cv, ca + kCvBatch, cb, threadIdx.x);
+      }
     }
     bulk_wait_all();   // this warp's tensor stores have landed
   }
@@ -581,7 +691,7 @@ static int clusters_for(int64_t a_rows, const GroupRows& g, int n_tiles) {
 template <int MAXW>
 static cudaError_t gateup_impl(const void* A, int64_t a_rows, int H, int I, const GroupRows& g,
                                const void* const* Wg, const void* const* Wu, void* h_out,
-                               WsHeader* hdr, cudaStream_t st) {
+                               const WdConvert& cv, WsHeader* hdr, cudaStream_t st) {
   TcParams<MAXW> p;
   memset(&p, 0, sizeof(p));
   if (!make_map_16(&p.out, h_out, I, a_rows, 32, true, 32, CU_TENSOR_MAP_SWIZZLE_64B))
@@ -598,7 +708,7 @@ static cudaError_t gateup_impl(const void* A, int64_t a_rows, int H, int I, cons
   const int n_tiles = (I + kN / 2 - 1) / (kN / 2);
   DownEpilogue none{};
   return launch_pdl(fn, 2 * clusters_for(a_rows, g, n_tiles), st, p, g, H, I,
-                    static_cast<__half*>(h_out), none, hdr, 1);
+                    static_cast<__half*>(h_out), none, cv, hdr, 1);
 }
 
 template <int MAXW>
@@ -618,15 +728,26 @@ static cudaError_t down_impl(const void* h, int64_t a_rows, int H, int I, const 
   // a later slot's operands (h, fp16 Wd) were complete before the previous
   // slot's launch let it start: only its epilogue waits (for the fp32 sum)
   const int dep = (ep.mode == kCombineAccum || ep.mode == kCombineLast) ? 0 : 1;
+  WdConvert no_cv{};
   return launch_pdl(fn, 2 * clusters_for(a_rows, g, n_tiles), st, p, g, I, H,
-                    static_cast<__half*>(nullptr), ep, hdr, dep);
+                    static_cast<__half*>(nullptr), ep, no_cv, hdr, dep);
 }
 
 cudaError_t launch_gateup_tc(const void* A, int64_t a_rows, int H, int I, const GroupRows& g,
                              const void* const* Wg, const void* const* Wu, void* h_out,
-                             WsHeader* hdr, cudaStream_t st) {
-  if (g.n_weights <= 8) return gateup_impl<8>(A, a_rows, H, I, g, Wg, Wu, h_out, hdr, st);
-  return gateup_impl<MM_MAX_EXPERTS>(A, a_rows, H, I, g, Wg, Wu, h_out, hdr, st);
+                             const void* const* wd_src, int n_wd, void* wd16, WsHeader* hdr,
+                             cudaStream_t st) {
+  WdConvert cv{};
+  if (n_wd > 0) {
+    if (n_wd > MM_MAX_EXPERTS || (static_cast<int64_t>(H) * I) % 8 != 0 || wd16 == nullptr)
+      return cudaErrorInvalidValue;
+    for (int m = 0; m < n_wd; ++m) cv.src.p[m] = wd_src[m];
+    cv.dst = static_cast<__half*>(wd16);
+    cv.nvec = static_cast<int64_t>(H) * I / 8;
+    cv.n_mat = n_wd;
+  }
+  if (g.n_weights <= 8) return gateup_impl<8>(A, a_rows, H, I, g, Wg, Wu, h_out, cv, hdr, st);
+  return gateup_impl<MM_MAX_EXPERTS>(A, a_rows, H, I, g, Wg, Wu, h_out, cv, hdr, st);
 }
 
 cudaError_t launch_down_tc(const void* h, int64_t a_rows, int H, int I, const GroupRows& g,

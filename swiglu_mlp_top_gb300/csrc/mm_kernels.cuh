@@ -60,6 +60,18 @@ struct DownEpilogue {
   int mode;                 // CombineMode
 };
 
+// fp16 copy of the down matrices, made by the epilogue warps of the gate/up
+// GEMM while its tensor pipe runs (HBM is mostly idle then): n_mat bf16
+// matrices of nvec 16-byte vectors each -> dst [n_mat][8 * nvec] fp16.
+// The conversion is exact for |w| >= 2^-14 (smaller magnitudes become fp16
+// subnormals, error <= 2^-25).  n_mat = 0: nothing to convert.
+struct WdConvert {
+  PtrArray src;
+  __half* dst;
+  int64_t nvec;
+  int n_mat;
+};
+
 // Router grid (routing.cu): per 64-token block logits, softmax, top-k, alpha
 // and partial counts / probability sums; with do_scan the block that
 // finishes last runs the scan (counts, aux loss; its counter lives in the
@@ -103,9 +115,11 @@ cudaError_t launch_dispatch(int dtype, const void* x, int64_t T, int H, int E, i
 // Tensor-core grouped GEMMs.  A is [rows, K] row-major; each group multiplies
 // its rows by its own weight matrices.  gate/up: bf16 A and weights, fp16 h
 // out.  down: fp16 h and fp16 Wd.
+// wd_src / n_wd: the down matrices to copy to fp16 at wd16 (n_wd = 0: none).
 cudaError_t launch_gateup_tc(const void* A, int64_t a_rows, int H, int I, const GroupRows& g,
                              const void* const* Wg, const void* const* Wu, void* h_out,
-                             WsHeader* hdr, cudaStream_t st);
+                             const void* const* wd_src, int n_wd, void* wd16, WsHeader* hdr,
+                             cudaStream_t st);
 cudaError_t launch_down_tc(const void* h, int64_t a_rows, int H, int I, const GroupRows& g,
                            const void* const* Wd, const DownEpilogue& ep, WsHeader* hdr,
                            cudaStream_t st);
@@ -117,11 +131,6 @@ cudaError_t launch_gateup_simt(int dtype, const void* A, int64_t a_rows, int H, 
 cudaError_t launch_down_simt(int dtype, const void* h, int64_t a_rows, int H, int I,
                              const GroupRows& g, const void* const* Wd, const DownEpilogue& ep,
                              cudaStream_t st);
-
-// bf16 -> fp16 copy of n_mat matrices of per_matrix elements (multiple of 8)
-// into one contiguous destination.
-cudaError_t launch_convert_bf16_to_f16(const void* const* src, int n_mat, int64_t per_matrix,
-                                       void* dst, cudaStream_t st);
 
 // Decode-sized forward on the CUDA cores (T <= kDecodeMaxT, bf16): one
 // cooperative kernel routes (MoE: Wr != nullptr), writes the fp32 h [T*k, I]

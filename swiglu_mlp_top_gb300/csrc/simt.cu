@@ -235,66 +235,6 @@ cudaError_t launch_down_simt(int dtype, const void* h, int64_t a_rows, int H, in
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------------------ Wd -> fp16
-// Copies each expert's down-projection weights from bf16 to fp16 (exact for
-// |w| >= 2^-14; smaller magnitudes become fp16 subnormals, error <= 2^-25).
-// The n_mat matrices form one index space of 16-byte vectors cut into one
-// contiguous range per block (a range meets at most a few matrices, so the
-// matrix index is stepped, not divided); each thread keeps kInFlight vectors
-// in flight and the stores bypass L1 and stream through L2.
-constexpr int kConvThreads = 256;
-__global__ void __launch_bounds__(kConvThreads)
-convert_bf16_to_f16_kernel(const PtrArray src, __half* __restrict__ dst_h, int nvec, int n_mat) {
-  constexpr int kInFlight = 8;
-  const int total = nvec * n_mat;                          // < 2^31 (checked by the launcher)
-  const int r0 = static_cast<int>(static_cast<long long>(total) * blockIdx.x / gridDim.x);
-  const int r1 = static_cast<int>(static_cast<long long>(total) * (blockIdx.x + 1) / gridDim.x);
-  int m = r0 / nvec;                                       // matrix of this thread's next vector
-  int off = r0 - m * nvec + static_cast<int>(threadIdx.x);
-  while (off >= nvec) { off -= nvec; ++m; }
-  uint4* dst = reinterpret_cast<uint4*>(dst_h);
-  for (int v0 = r0 + static_cast<int>(threadIdx.x); v0 < r1; v0 += kInFlight * kConvThreads) {
-    uint4 raw[kInFlight];
-    int mj[kInFlight], oj[kInFlight];
-#pragma unroll
-    for (int j = 0; j < kInFlight; ++j) {
-      mj[j] = m;
-      oj[j] = off;
-      if (v0 + j * kConvThreads < r1) raw[j] = __ldcs(static_cast<const uint4*>(src.p[m]) + off);
-      off += kConvThreads;
-      while (off >= nvec) { off -= nvec; ++m; }            // more than once only when nvec < 256
-    }
-#pragma unroll
-    for (int j = 0; j < kInFlight; ++j) {
-      if (v0 + j * kConvThreads < r1) {
-        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&raw[j]);
-        uint4 out;
-        uint32_t* o = reinterpret_cast<uint32_t*>(&out);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 f = __bfloat1622float2(b[q]);
-          o[q] = pack_f16x2(f.x, f.y);
-        }
-        __stcg(dst + static_cast<int64_t>(mj[j]) * nvec + oj[j], out);
-      }
-    }
-  }
-}
-
-cudaError_t launch_convert_bf16_to_f16(const void* const* src, int n_mat, int64_t per_matrix,
-                                       void* dst, cudaStream_t st) {
-  PtrArray p;
-  for (int m = 0; m < n_mat; ++m) p.p[m] = src[m];
-  const int64_t nvec = per_matrix / 8;                     // per_matrix is a multiple of 8
-  if (nvec * n_mat + 8LL * kConvThreads * num_sms() >= (1LL << 31)) return cudaErrorInvalidValue;
-  int grid = num_sms();
-  if (static_cast<int64_t>(grid) * kConvThreads > nvec * n_mat)
-    grid = static_cast<int>((nvec * n_mat + kConvThreads - 1) / kConvThreads);
-  convert_bf16_to_f16_kernel<<<grid > 0 ? grid : 1, kConvThreads, 0, st>>>(
-      p, static_cast<__half*>(dst), static_cast<int>(nvec), n_mat);
-  return cudaGetLastError();
-}
-
 // ------------------------------------------------------------------ watchdog
 // One thread waits on an mbarrier that nothing arrives on; the bounded wait
 // gives up after limit_us, records MM_ERR_TIMEOUT and the kernel returns.
