@@ -168,8 +168,8 @@ __device__ __forceinline__ void epilogue_up(uint32_t tb, const TileInfo& ti, int
 // per instruction.  Instead each 16-column piece goes TMEM -> registers
 // (thread = row) -> the warp's 64-byte-row staging tile -> back out with
 // lane l on row 8i + l/4, columns 4(l%4)..+3: every global access of the
-// warp then covers 8 rows x 64 contiguous bytes.  The running sum of the
-// next piece is requested before the current piece is processed.
+// warp then covers 8 rows x 64 contiguous bytes.  The running sum is
+// requested two pieces ahead of its use.
 struct DownRow {
   int64_t tok;
   float alpha;
@@ -233,7 +233,7 @@ __device__ __forceinline__ void down_prefetch(const DownLanes& L, const DownEpil
 __device__ __forceinline__ void epilogue_down(uint32_t tb, const DownRow& d, const DownLanes& L,
                                               const TileInfo& ti, int H, const DownEpilogue& ep,
                                               int half, int lane, uint8_t* wstage,
-                                              float4 (&pre)[4]) {
+                                              float4 (&pre)[4], float4 (&pre2)[4]) {
   const int col0 = ti.n0 + half * (kN / 2);
   constexpr int kPieces = kN / 2 / kDnPiece;
   const uint32_t st0 = smem_u32(wstage);
@@ -243,7 +243,7 @@ __device__ __forceinline__ void epilogue_down(uint32_t tb, const DownRow& d, con
     uint32_t r[16];
     tmem_ld_32x32b_x16(tb + half * (kN / 2) + c * kDnPiece, r);
     float4 nxt[4];
-    if (c + 1 < kPieces && col0 + (c + 1) * kDnPiece < H) down_prefetch(L, ep, c + 1, nxt);
+    if (c + 2 < kPieces && col0 + (c + 2) * kDnPiece < H) down_prefetch(L, ep, c + 2, nxt);
     tmem_ld_wait();
     __syncwarp();                                // the previous piece has been read back
     // row `lane`: 64 bytes, 16-byte chunk q at q ^ ((lane >> 1) & 3)
@@ -276,7 +276,10 @@ __device__ __forceinline__ void epilogue_down(uint32_t tb, const DownRow& d, con
       }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) pre[i] = nxt[i];
+    for (int i = 0; i < 4; ++i) {
+      pre[i] = pre2[i];
+      pre2[i] = nxt[i];
+    }
   }
 }
 
@@ -500,12 +503,22 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
       const uint32_t aph = (local >> 1) & 1;
       DownRow dr{0, 1.0f, false};
       DownLanes dl;
-      float4 pre[4];
+      float4 pre[4], pre2[4];
       if constexpr (OP == kOpDown) {
         // independent of the MMAs: requested while they run
         dr = down_row_info(ti, ep, row);
+        // the running sum of this row's 128 columns: pulled into L2 while the
+        // MMAs run, so the epilogue's reads of it do not wait on DRAM
+        if (down_reads_sum(ep) && dr.valid && ti.n0 + half * (kN / 2) < NCOLS) {
+          const float* a = ep.acc32 + dr.tok * NCOLS + ti.n0 + half * (kN / 2);
+#pragma unroll
+          for (int j = 0; j < kN / 2 / 32; ++j)
+            if (ti.n0 + half * (kN / 2) + j * 32 < NCOLS)
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(a + j * 32) : "memory");
+        }
         dl = down_lanes(dr, ti, NCOLS, half, lane);
         if (ti.n0 + half * (kN / 2) < NCOLS) down_prefetch(dl, ep, 0, pre);
+        if (ti.n0 + half * (kN / 2) + kDnPiece < NCOLS) down_prefetch(dl, ep, 1, pre2);
       }
       int64_t ca = 0, cb = 0;           // this tile's piece of the Wd copy
       uint4 craw[4];
@@ -520,7 +533,7 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
       if constexpr (OP == kOpUp)
         epilogue_up(tb, ti, NCOLS, hout, row, half, wstage, &P.out);
       else
-        epilogue_down(tb, dr, dl, ti, NCOLS, ep, half, lane, wstage, pre);
+        epilogue_down(tb, dr, dl, ti, NCOLS, ep, half, lane, wstage, pre, pre2);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc ? te1 : te0);
