@@ -60,7 +60,8 @@ template <> struct OpTraits<kOpDown> { static constexpr int kOutCols = kN, kKb =
 
 template <int MAXW>
 struct TcParams {
-  CUtensorMap out;          // gate/up: h [a_rows, I] fp16, box 32 x 32 (TMA stores)
+  CUtensorMap out;          // gate/up: h [a_rows, I] fp16; down of a dense FFN: y [a_rows, H]
+                            // bf16; box 32 x 32, 64-byte swizzle (TMA stores)
   CUtensorMap a;            // A [a_rows, K]
   CUtensorMap b0[MAXW];     // gate/up: Wg; down: fp16 Wd  (box rows = N/2)
   CUtensorMap b1[MAXW];     // gate/up: Wu; down: unused
@@ -230,6 +231,44 @@ __device__ __forceinline__ void down_prefetch(const DownLanes& L, const DownEpil
       pre[i] = __ldcg(reinterpret_cast<const float4*>(ep.acc32 + L.off[i] + c * kDnPiece));
 }
 
+// down, dense FFN (rows are tokens in order, alpha = 1, plain store) and a
+// warp whose 32 rows are all in the problem: 32-column pieces of bf16 y go
+// through the warp's 64-byte-swizzled staging tile and out with one tensor
+// store each, like h in the gate/up epilogue.
+__device__ __forceinline__ void epilogue_down_dense(uint32_t tb, const TileInfo& ti, int H,
+                                                    int half, int lane, int row_base,
+                                                    uint8_t* wstage, const CUtensorMap* ymap) {
+  const int col0 = ti.n0 + half * (kN / 2);
+#pragma unroll 1
+  for (int c = 0; c < kN / 2 / 32; ++c) {
+    if (col0 + c * 32 >= H) break;               // warp-uniform: past the last column
+    uint32_t r0[16], r1[16];
+    tmem_ld_32x32b_x16(tb + half * (kN / 2) + c * 32, r0);
+    tmem_ld_32x32b_x16(tb + half * (kN / 2) + c * 32 + 16, r1);
+    tmem_ld_wait();
+    uint32_t pk[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      pk[j] = pack_bf16x2(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]));
+      pk[8 + j] = pack_bf16x2(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]));
+    }
+    if (lane == 0) bulk_wait_read();             // the previous store has read the tile
+    __syncwarp();
+    // 64-byte rows, 16-byte chunk q of row r at chunk q ^ ((r >> 1) & 3)
+    uint8_t* r64 = wstage + lane * 64;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(r64 + ((q ^ ((lane >> 1) & 3)) << 4)) =
+          make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(ymap, wstage, col0 + c * 32, row_base);
+      bulk_commit();
+    }
+  }
+}
+
 __device__ __forceinline__ void epilogue_down(uint32_t tb, const DownRow& d, const DownLanes& L,
                                               const TileInfo& ti, int H, const DownEpilogue& ep,
                                               int half, int lane, uint8_t* wstage,
@@ -237,6 +276,8 @@ __device__ __forceinline__ void epilogue_down(uint32_t tb, const DownRow& d, con
   const int col0 = ti.n0 + half * (kN / 2);
   constexpr int kPieces = kN / 2 / kDnPiece;
   const uint32_t st0 = smem_u32(wstage);
+  if (lane == 0) bulk_wait_read();               // a dense tile's tensor stores used the tile
+  __syncwarp();
 #pragma unroll 1
   for (int c = 0; c < kPieces; ++c) {
     if (col0 + c * kDnPiece >= H) break;         // warp-uniform: past the last column
@@ -532,6 +573,8 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
       const uint32_t tb = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * kAccStride;
       if constexpr (OP == kOpUp)
         epilogue_up(tb, ti, NCOLS, hout, row, half, wstage, &P.out);
+      else if (ep.perm == nullptr && ep.mode == kCombineStore && (row | 31) < ti.rows)
+        epilogue_down_dense(tb, ti, NCOLS, half, lane, ti.row0 + (row & ~31), wstage, &P.out);
       else
         epilogue_down(tb, dr, dl, ti, NCOLS, ep, half, lane, wstage, pre, pre2);
       tc_fence_before();
@@ -734,6 +777,10 @@ static cudaError_t down_impl(const void* h, int64_t a_rows, int H, int I, const 
   if (!kblock_map(&p.a, h, I, a_rows, kTcBM, true, kb)) return cudaErrorInvalidValue;
   for (int e = 0; e < g.n_weights; ++e)
     if (!kblock_map(&p.b0[e], Wd[e], I, H, kN / 2, true, kb)) return cudaErrorInvalidValue;
+  // dense FFN: y is written with tensor stores (32 x 32 boxes, 64-byte swizzle)
+  if (ep.perm == nullptr && ep.mode == kCombineStore &&
+      !make_map_16(&p.out, ep.y, H, a_rows, 32, false, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
   auto fn = grouped_gemm_kernel<kOpDown, MAXW>;
   cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), kSmem);
   if (err != cudaSuccess) return err;
