@@ -51,6 +51,14 @@ constexpr int kStageEpi = kEpiWarps * 32 * 64;           // 16 KiB
 constexpr int kWarpProducer = kEpiWarps, kWarpMma = kEpiWarps + 1;
 constexpr int kThreads = 32 * (kEpiWarps + 2);
 constexpr int kSmem = kRingKb * (kATile + kBTile) + kStageEpi + 2048;
+// Wide down tile (N = 384 as two MMAs of N = 192, one 384-column
+// accumulator): taken when it makes every tile pair fit in one wave.  Each
+// CTA stages 192 rows of Wd per k-block (two boxes of 96), so the ring holds
+// five k-blocks.
+constexpr int kNWide = 384;
+constexpr int kRingKbWide = 5;
+constexpr int kSmemWide = kRingKbWide * (kATile + (kNWide / 2) * kTcBK * 2) + kStageEpi + 2048;
+static_assert(kSmemWide <= 232448 - 8192, "shared memory budget (wide down tile)");
 constexpr uint32_t kTmemCols = 512;
 static_assert(kSmem <= 232448, "shared memory budget");
 
@@ -206,10 +214,10 @@ struct DownLanes {
 };
 
 __device__ __forceinline__ DownLanes down_lanes(const DownRow& d, const TileInfo& ti, int H,
-                                                int half, int lane) {
+                                                int half, int lane, int hc) {
   DownLanes L;
   const uint32_t vmask = __ballot_sync(0xffffffffu, d.valid);
-  const int col0 = ti.n0 + half * (kN / 2);
+  const int col0 = ti.n0 + half * hc;
   L.valid = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -235,16 +243,17 @@ __device__ __forceinline__ void down_prefetch(const DownLanes& L, const DownEpil
 // warp whose 32 rows are all in the problem: 32-column pieces of bf16 y go
 // through the warp's 64-byte-swizzled staging tile and out with one tensor
 // store each, like h in the gate/up epilogue.
+template <int HC>
 __device__ __forceinline__ void epilogue_down_dense(uint32_t tb, const TileInfo& ti, int H,
                                                     int half, int lane, int row_base,
                                                     uint8_t* wstage, const CUtensorMap* ymap) {
-  const int col0 = ti.n0 + half * (kN / 2);
+  const int col0 = ti.n0 + half * HC;
 #pragma unroll 1
-  for (int c = 0; c < kN / 2 / 32; ++c) {
+  for (int c = 0; c < HC / 32; ++c) {
     if (col0 + c * 32 >= H) break;               // warp-uniform: past the last column
     uint32_t r0[16], r1[16];
-    tmem_ld_32x32b_x16(tb + half * (kN / 2) + c * 32, r0);
-    tmem_ld_32x32b_x16(tb + half * (kN / 2) + c * 32 + 16, r1);
+    tmem_ld_32x32b_x16(tb + half * HC + c * 32, r0);
+    tmem_ld_32x32b_x16(tb + half * HC + c * 32 + 16, r1);
     tmem_ld_wait();
     uint32_t pk[16];
 #pragma unroll
@@ -269,12 +278,13 @@ __device__ __forceinline__ void epilogue_down_dense(uint32_t tb, const TileInfo&
   }
 }
 
+template <int HC>
 __device__ __forceinline__ void epilogue_down(uint32_t tb, const DownRow& d, const DownLanes& L,
                                               const TileInfo& ti, int H, const DownEpilogue& ep,
                                               int half, int lane, uint8_t* wstage,
                                               float4 (&pre)[4], float4 (&pre2)[4]) {
-  const int col0 = ti.n0 + half * (kN / 2);
-  constexpr int kPieces = kN / 2 / kDnPiece;
+  const int col0 = ti.n0 + half * HC;
+  constexpr int kPieces = HC / kDnPiece;
   const uint32_t st0 = smem_u32(wstage);
   if (lane == 0) bulk_wait_read();               // a dense tile's tensor stores used the tile
   __syncwarp();
@@ -282,7 +292,7 @@ __device__ __forceinline__ void epilogue_down(uint32_t tb, const DownRow& d, con
   for (int c = 0; c < kPieces; ++c) {
     if (col0 + c * kDnPiece >= H) break;         // warp-uniform: past the last column
     uint32_t r[16];
-    tmem_ld_32x32b_x16(tb + half * (kN / 2) + c * kDnPiece, r);
+    tmem_ld_32x32b_x16(tb + half * HC + c * kDnPiece, r);
     float4 nxt[4];
     if (c + 2 < kPieces && col0 + (c + 2) * kDnPiece < H) down_prefetch(L, ep, c + 2, nxt);
     tmem_ld_wait();
@@ -378,20 +388,25 @@ __device__ __forceinline__ void cv_rest(const WdConvert& cv, int64_t v, int64_t 
 
 // =============================================================== kernel
 // K = contraction length (H for gate/up, I for down); NCOLS = output width
-// (I for gate/up, H for down).
-template <int OP, int MAXW>
+// (I for gate/up, H for down).  NW = N of a down tile pair: 256 (two TMEM
+// accumulators), or kNWide (one accumulator; tiles that fit one wave).
+template <int OP, int MAXW, int NW = kN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g, const int K,
                     const int NCOLS, __half* __restrict__ hout, const DownEpilogue ep,
                     const WdConvert cv, WsHeader* hdr, const int dep_mainloop) {
-  constexpr int kOutCols = OpTraits<OP>::kOutCols;
+  static_assert(NW == kN || (OP == kOpDown && NW == kNWide), "tile width");
+  constexpr bool kWide = NW == kNWide;
+  constexpr int kOutCols = OP == kOpUp ? OpTraits<OP>::kOutCols : NW;
+  constexpr int kHC = NW / 2;                     // down: columns per epilogue warp half
   extern __shared__ unsigned char smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
   constexpr int kKbStage = OpTraits<OP>::kKb;
-  constexpr int kStages = kRingKb / kKbStage;
+  constexpr int kStages = (kWide ? kRingKbWide : kRingKb) / kKbStage;
   constexpr int kAStage = kKbStage * kATile;
-  constexpr int kBStage = kKbStage * kBTile;
+  constexpr int kBTileK = (OP == kOpUp ? kN / 2 : NW / 2) * kTcBK * 2;   // B rows of this CTA, one k-block
+  constexpr int kBStage = kKbStage * kBTileK;
   uint8_t* sB = smem + kStages * kAStage;
   uint8_t* sEpi = sB + kStages * kBStage;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + kStageEpi);
@@ -455,7 +470,11 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
         const TileInfo ti = decode_tile(tile, s_off, s_tstart, g.G, g.n_weights, n_tiles,
                                         kOutCols, static_cast<int>(rank));
         const CUtensorMap* bmap = (OP == kOpUp && rank == 1) ? &P.b1[ti.w] : &P.b0[ti.w];
-        const int bcoord = (OP == kOpUp) ? ti.n0 : ti.n0 + static_cast<int>(rank) * (kN / 2);
+        // wide tile: this CTA's B rows are two boxes of 96, Wd rows
+        // n0 + 96 rank .. and n0 + 192 + 96 rank .., so that the first MMA
+        // (N = 192) yields y columns n0 .. n0 + 191 and the second the rest
+        const int bcoord = (OP == kOpUp) ? ti.n0
+                                         : ti.n0 + static_cast<int>(rank) * (kWide ? kHC / 2 : kHC);
         for (int kb = 0; kb < nkb; kb += kKbStage, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
@@ -464,6 +483,8 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
           if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (kAStage + kBStage));
           tma_load_3d_cta2(sA + s * kAStage, &P.a, fb, 0, ti.row0, kb);
           tma_load_3d_cta2(sB + s * kBStage, bmap, fb, 0, bcoord, kb);
+          if constexpr (kWide)
+            tma_load_3d_cta2(sB + s * kBStage + kBStage / 2, bmap, fb, 0, bcoord + NW / 2, kb);
         }
       }
       if (!ok && rank == 0) {
@@ -479,12 +500,14 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
   } else if (warp == kWarpMma) {
     // ------------------------------------------------ MMA issuer (even CTA)
     if (rank == 0 && lane == 0) {
-      constexpr uint32_t idesc = (OP == kOpUp) ? idesc_bf16_f32(kPairM, kN) : idesc_f16_f32(kPairM, kN);
+      constexpr uint32_t idesc = (OP == kOpUp) ? idesc_bf16_f32(kPairM, kN)
+                                 : idesc_f16_f32(kPairM, kWide ? NW / 2 : NW);
       int it = 0, local = 0;
       bool ok = true;
       for (int tile = cluster; ok && tile < total; tile += n_clusters, ++local) {
-        const int acc = local & 1;
-        const uint32_t aph = (local >> 1) & 1;
+        // wide tiles: one accumulator, so tile i + 1 waits for tile i's epilogue
+        const int acc = kWide ? 0 : (local & 1);
+        const uint32_t aph = kWide ? (local & 1) : ((local >> 1) & 1);
         if (!mbar_wait(&tempty[acc], aph ^ 1, abort, hdr, 3)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + acc * kAccStride;
@@ -497,11 +520,15 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
           for (int kl = 0; kl < kKbStage; ++kl) {
             if (kb + kl >= nkb) break;               // a box past K was zero-filled
             const uint32_t a0 = smem_u32(sA + s * kAStage + kl * kATile);
-            const uint32_t b0 = smem_u32(sB + s * kBStage + kl * kBTile);
+            const uint32_t b0 = smem_u32(sB + s * kBStage + kl * kBTileK);
 #pragma unroll
-            for (int kk = 0; kk < kTcBK / 16; ++kk)
-              umma_f16_cta2(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc,
-                            (kb + kl > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kTcBK / 16; ++kk) {
+              const uint32_t accf = (kb + kl > 0 || kk > 0) ? 1u : 0u;
+              umma_f16_cta2(d, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc, accf);
+              if constexpr (kWide)   // the second box: accumulator columns 192 .. 383
+                umma_f16_cta2(d + NW / 2, smem_desc_sw128(a0 + kk * 32),
+                              smem_desc_sw128(b0 + kBStage / 2 + kk * 32), idesc, accf);
+            }
           }
           umma_commit_cta2_mc(&empty[s], 0x3);
         }
@@ -540,8 +567,8 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
     for (int tile = cluster; tile < total; tile += n_clusters, ++local) {
       const TileInfo ti = decode_tile(tile, s_off, s_tstart, g.G, g.n_weights, n_tiles, kOutCols,
                                       static_cast<int>(rank));
-      const int acc = local & 1;
-      const uint32_t aph = (local >> 1) & 1;
+      const int acc = kWide ? 0 : (local & 1);
+      const uint32_t aph = kWide ? (local & 1) : ((local >> 1) & 1);
       DownRow dr{0, 1.0f, false};
       DownLanes dl;
       float4 pre[4], pre2[4];
@@ -550,16 +577,16 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
         dr = down_row_info(ti, ep, row);
         // the running sum of this row's 128 columns: pulled into L2 while the
         // MMAs run, so the epilogue's reads of it do not wait on DRAM
-        if (down_reads_sum(ep) && dr.valid && ti.n0 + half * (kN / 2) < NCOLS) {
-          const float* a = ep.acc32 + dr.tok * NCOLS + ti.n0 + half * (kN / 2);
+        if (down_reads_sum(ep) && dr.valid && ti.n0 + half * kHC < NCOLS) {
+          const float* a = ep.acc32 + dr.tok * NCOLS + ti.n0 + half * kHC;
 #pragma unroll
-          for (int j = 0; j < kN / 2 / 32; ++j)
-            if (ti.n0 + half * (kN / 2) + j * 32 < NCOLS)
+          for (int j = 0; j < kHC / 32; ++j)
+            if (ti.n0 + half * kHC + j * 32 < NCOLS)
               asm volatile("prefetch.global.L2 [%0];" ::"l"(a + j * 32) : "memory");
         }
-        dl = down_lanes(dr, ti, NCOLS, half, lane);
-        if (ti.n0 + half * (kN / 2) < NCOLS) down_prefetch(dl, ep, 0, pre);
-        if (ti.n0 + half * (kN / 2) + kDnPiece < NCOLS) down_prefetch(dl, ep, 1, pre2);
+        dl = down_lanes(dr, ti, NCOLS, half, lane, kHC);
+        if (ti.n0 + half * kHC < NCOLS) down_prefetch(dl, ep, 0, pre);
+        if (ti.n0 + half * kHC + kDnPiece < NCOLS) down_prefetch(dl, ep, 1, pre2);
       }
       int64_t ca = 0, cb = 0;           // this tile's piece of the Wd copy
       uint4 craw[4];
@@ -574,9 +601,9 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
       if constexpr (OP == kOpUp)
         epilogue_up(tb, ti, NCOLS, hout, row, half, wstage, &P.out);
       else if (ep.perm == nullptr && ep.mode == kCombineStore && (row | 31) < ti.rows)
-        epilogue_down_dense(tb, ti, NCOLS, half, lane, ti.row0 + (row & ~31), wstage, &P.out);
+        epilogue_down_dense<kHC>(tb, ti, NCOLS, half, lane, ti.row0 + (row & ~31), wstage, &P.out);
       else
-        epilogue_down(tb, dr, dl, ti, NCOLS, ep, half, lane, wstage, pre, pre2);
+        epilogue_down<kHC>(tb, dr, dl, ti, NCOLS, ep, half, lane, wstage, pre, pre2);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc ? te1 : te0);
@@ -707,12 +734,12 @@ cudaError_t ensure_dynamic_smem(const void* fn, size_t bytes) {
 // Launch with programmatic stream serialisation (the kernel may start while
 // the previous kernel of the stream finishes; see griddepcontrol in it).
 template <typename Kern, typename... Args>
-static cudaError_t launch_pdl(Kern fn, int grid, cudaStream_t st, Args... args) {
+static cudaError_t launch_pdl(Kern fn, int grid, size_t smem, cudaStream_t st, Args... args) {
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -733,13 +760,17 @@ static bool kblock_map(CUtensorMap* out, const void* ptr, int K, int64_t rows, i
   return make_map_3d(out, ptr, dims, strides, box, is_f16);
 }
 
+// Upper bound on the tile pairs of a grouped problem with n_tiles column
+// tiles (the group sizes are only known on the device).
+static int64_t tiles_bound(int64_t a_rows, const GroupRows& g, int n_tiles) {
+  if (g.offsets == nullptr)
+    return ((g.dense_rows + kPairM - 1) / kPairM) * static_cast<int64_t>(n_tiles);
+  return ((a_rows + kPairM - 1) / kPairM + g.G) * static_cast<int64_t>(n_tiles);
+}
+
 // Number of CTA pairs: one per tile pair, at most one per co-resident pair.
 static int clusters_for(int64_t a_rows, const GroupRows& g, int n_tiles) {
-  int64_t tiles;
-  if (g.offsets == nullptr)
-    tiles = ((g.dense_rows + kPairM - 1) / kPairM) * static_cast<int64_t>(n_tiles);
-  else
-    tiles = ((a_rows + kPairM - 1) / kPairM + g.G) * static_cast<int64_t>(n_tiles);
+  const int64_t tiles = tiles_bound(a_rows, g, n_tiles);
   const int pairs = num_sms() / 2;
   return static_cast<int>(tiles < pairs ? (tiles > 0 ? tiles : 1) : pairs);
 }
@@ -763,7 +794,7 @@ static cudaError_t gateup_impl(const void* A, int64_t a_rows, int H, int I, cons
   if (err != cudaSuccess) return err;
   const int n_tiles = (I + kN / 2 - 1) / (kN / 2);
   DownEpilogue none{};
-  return launch_pdl(fn, 2 * clusters_for(a_rows, g, n_tiles), st, p, g, H, I,
+  return launch_pdl(fn, 2 * clusters_for(a_rows, g, n_tiles), kSmem, st, p, g, H, I,
                     static_cast<__half*>(h_out), none, cv, hdr, 1);
 }
 
@@ -771,25 +802,34 @@ template <int MAXW>
 static cudaError_t down_impl(const void* h, int64_t a_rows, int H, int I, const GroupRows& g,
                              const void* const* Wd, const DownEpilogue& ep, WsHeader* hdr,
                              cudaStream_t st) {
+  // 384-wide tiles where they put every tile pair in one wave and 256-wide
+  // ones do not (e.g. 8192 top-1 rows over 4 experts at H = 768: ~100 tile
+  // pairs in two waves against ~70 in one)
+  const int pairs = num_sms() / 2;
+  const bool wide = tiles_bound(a_rows, g, (H + kNWide - 1) / kNWide) <= pairs &&
+                    tiles_bound(a_rows, g, (H + kN - 1) / kN) > pairs;
+  const int nw = wide ? kNWide : kN;
   TcParams<MAXW> p;
   memset(&p, 0, sizeof(p));
   constexpr int kb = OpTraits<kOpDown>::kKb;
   if (!kblock_map(&p.a, h, I, a_rows, kTcBM, true, kb)) return cudaErrorInvalidValue;
   for (int e = 0; e < g.n_weights; ++e)
-    if (!kblock_map(&p.b0[e], Wd[e], I, H, kN / 2, true, kb)) return cudaErrorInvalidValue;
+    if (!kblock_map(&p.b0[e], Wd[e], I, H, wide ? kNWide / 4 : kN / 2, true, kb))
+      return cudaErrorInvalidValue;
   // dense FFN: y is written with tensor stores (32 x 32 boxes, 64-byte swizzle)
   if (ep.perm == nullptr && ep.mode == kCombineStore &&
       !make_map_16(&p.out, ep.y, H, a_rows, 32, false, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  auto fn = grouped_gemm_kernel<kOpDown, MAXW>;
-  cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), kSmem);
+  auto fn = wide ? grouped_gemm_kernel<kOpDown, MAXW, kNWide> : grouped_gemm_kernel<kOpDown, MAXW>;
+  const size_t smem = wide ? kSmemWide : kSmem;
+  cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem);
   if (err != cudaSuccess) return err;
-  const int n_tiles = (H + kN - 1) / kN;
+  const int n_tiles = (H + nw - 1) / nw;
   // a later slot's operands (h, fp16 Wd) were complete before the previous
   // slot's launch let it start: only its epilogue waits (for the fp32 sum)
   const int dep = (ep.mode == kCombineAccum || ep.mode == kCombineLast) ? 0 : 1;
   WdConvert no_cv{};
-  return launch_pdl(fn, 2 * clusters_for(a_rows, g, n_tiles), st, p, g, I, H,
+  return launch_pdl(fn, 2 * clusters_for(a_rows, g, n_tiles), smem, st, p, g, I, H,
                     static_cast<__half*>(nullptr), ep, no_cv, hdr, dep);
 }
 

@@ -70,6 +70,25 @@ def test_dense_bf16_tensor(T):
     assert rel_err(y.double().cpu().numpy(), ref) <= Y_TOL["bf16"]
 
 
+@pytest.mark.parametrize("T,H,I", [(3500, 1536, 512), (3400, 1408, 320)])
+def test_dense_bf16_tensor_wide_down_tiles(T, H, I):
+    """Shapes whose down GEMM takes 384-wide tiles (256-wide ones would need a
+    second wave): two N = 192 MMAs per k-step into one accumulator; the
+    second case ends in a tile with 256 valid columns."""
+    inp = make_inputs(T, H, I, "bf16", seed=T + 17)
+    g = to_dev(inp)
+    y = mm.swiglu_ffn(g["x"], g["Wg"], g["Wu"], g["Wd"], path="tensor")
+    torch.cuda.synchronize()
+    ref = oracle.swiglu_ffn(*[to_f64(inp[n]) for n in ("x", "Wg", "Wu", "Wd")])
+    assert rel_err(y.double().cpu().numpy(), ref) <= Y_TOL["bf16"]
+
+
+def test_moe_top1_wide_down_tiles():
+    """Top-1 over 4 experts at T = 6000, H = 768: 384-wide down tiles with
+    the rows scattered back to their tokens."""
+    full_moe_check(moe_inputs(6000, 768, 384, 4, "bf16", seed=19), 1, 0.01, "bf16", path="tensor")
+
+
 @pytest.mark.parametrize("T,H,I,E,k,bias", [
     (1000, 256, 384, 4, 1, None),
     (777, 256, 320, 8, 2, (1.5, 0.5, 0, 0, 0, 0, 0, 0)),
