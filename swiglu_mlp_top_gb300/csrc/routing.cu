@@ -659,11 +659,15 @@ router_tc_kernel(const __grid_constant__ RtMaps M, int64_t T, int H, int E, int 
     fence_mbar_init();
   }
   for (int g = tid; g < G; g += kRouteThreads) s_gcnt[g] = 0;
-  if (tid < EP) s_bias[tid] = (bias != nullptr && tid < E) ? bias[tid] : 0.f;
   if (warp == 1) {
     tmem_alloc(&s_tmem, 64);
     tmem_relinquish();
   }
+  // launched as a programmatic dependent: the set-up above overlaps the
+  // previous kernel of the stream, whose outputs (x, Wr, the bias, or the
+  // buffers written here) are touched only once it has finished
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid < EP) s_bias[tid] = (bias != nullptr && tid < E) ? bias[tid] : 0.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -868,9 +872,19 @@ static cudaError_t launch_router_tc(const void* x, const void* Wr, const float* 
   cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem);
   if (err != cudaSuccess) return err;
   const int nblk = static_cast<int>((T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock);
-  fn<<<nblk, kRouteThreads, smem, st>>>(m, T, H, E, k, bias, topk_idx, topk_w, blk_cnt, blk_prob, X,
-                                        nkb, static_cast<uint32_t>(stage));
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(nblk);
+  cfg.blockDim = dim3(kRouteThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, m, T, H, E, k, bias, topk_idx, topk_w, blk_cnt, blk_prob, X,
+                            nkb, static_cast<uint32_t>(stage));
 }
 
 cudaError_t launch_router(int dtype, const void* x, const void* Wr, const float* bias, int64_t T,
