@@ -719,22 +719,27 @@ router_tc_kernel(const __grid_constant__ RtMaps M, int64_t T, int H, int E, int 
 #pragma unroll
         for (int j = 0; j < 16; ++j) p[c0 + j] = __uint_as_float(r[j]);
       }
+      // loops over the E experts only (E is uniform; the padded columns past
+      // E are never read)
       float m = -INFINITY;
 #pragma unroll
       for (int e = 0; e < EP; ++e) {
-        if (e < E) {
-          p[e] += s_bias[e];
-          m = fmaxf(m, p[e]);
-        }
+        if (e >= E) break;
+        p[e] += s_bias[e];
+        m = fmaxf(m, p[e]);
       }
       float z = 0.f;
 #pragma unroll
       for (int e = 0; e < EP; ++e) {
-        p[e] = e < E ? expf(p[e] - m) : 0.f;
+        if (e >= E) break;
+        p[e] = expf(p[e] - m);
         z += p[e];
       }
 #pragma unroll
-      for (int e = 0; e < EP; ++e) p[e] = p[e] / z;
+      for (int e = 0; e < EP; ++e) {
+        if (e >= E) break;
+        p[e] = p[e] / z;
+      }
       // top-k: k arg-max passes in expert order, strict comparison (lower index first)
       uint64_t taken = 0;
       float sel_sum = 0.f;
@@ -748,11 +753,13 @@ router_tc_kernel(const __grid_constant__ RtMaps M, int64_t T, int H, int E, int 
           float bp = -1.f;
           int be = 0;
 #pragma unroll
-          for (int e = 0; e < EP; ++e)
-            if (e < E && !((taken >> e) & 1ull) && p[e] > bp) {
+          for (int e = 0; e < EP; ++e) {
+            if (e >= E) break;
+            if (!((taken >> e) & 1ull) && p[e] > bp) {
               bp = p[e];
               be = e;
             }
+          }
           taken |= 1ull << be;
           sel_sum += bp;
           sel_e[sl] = be;
@@ -773,6 +780,7 @@ router_tc_kernel(const __grid_constant__ RtMaps M, int64_t T, int H, int E, int 
       // the block's probability sums per expert: fixed butterfly order
 #pragma unroll
       for (int e = 0; e < EP; ++e) {
+        if (e >= E) break;
         float v = valid ? p[e] : 0.f;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
