@@ -162,7 +162,7 @@ __device__ __forceinline__ void down_row(const __nv_bfloat16* wrow, const float*
 }
 
 // MoE routing of all T tokens.  Logits: (token, expert) pairs, four per warp
-// at a time, lanes split H, fp32; then softmax / top-k (one thread per token)
+// at a time, lanes split H, fp32; then softmax / top-k (one warp per token)
 // and the grouping by expert (route_small.cuh).
 __device__ void decode_route(const DecodeArgs& A, const float* xs, const __nv_bfloat16* Wr,
                              const float* bias, SmallRoute<kDecodeMaxT>& R) {
@@ -202,7 +202,7 @@ __device__ void decode_route(const DecodeArgs& A, const float* xs, const __nv_bf
     }
   }
   __syncthreads();
-  route_softmax_topk(R, A.T, E, k, bias, static_cast<int>(threadIdx.x), kDecThreads);
+  route_softmax_topk_warp(R, A.T, E, k, bias, warp, kDecWarps, lane);
   __syncthreads();
   if (warp == 0) route_group(R, A.T * k, E, lane);
   __syncthreads();

@@ -73,6 +73,59 @@ __device__ __forceinline__ void route_softmax_topk(SmallRoute<MAXT>& R, int T, i
   }
 }
 
+// The same on one warp per token (t = first_warp, first_warp + nwarps, ...):
+// lane l holds experts l and l + 32 in registers; the maximum and the sum of
+// the exponentials are warp reductions, and each of the k selections is a
+// warp arg-max (larger probability, else lower expert index).  Latency-bound
+// calls (a few tokens) take this form; the sum runs in a different order from
+// route_softmax_topk's, so probabilities can differ in their last bits.
+template <int MAXT>
+__device__ __forceinline__ void route_softmax_topk_warp(SmallRoute<MAXT>& R, int T, int E, int k,
+                                                        const float* bias, int first_warp,
+                                                        int nwarps, int lane) {
+  for (int t = first_warp; t < T; t += nwarps) {
+    float* row = R.prob[t];
+    const bool v0 = lane < E, v1 = lane + 32 < E;
+    const float r0 = v0 ? row[lane] + bias[lane] : -INFINITY;
+    const float r1 = v1 ? row[lane + 32] + bias[lane + 32] : -INFINITY;
+    float m = fmaxf(r0, r1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float x0 = v0 ? __expf(r0 - m) : 0.f;
+    const float x1 = v1 ? __expf(r1 - m) : 0.f;
+    const float rz = 1.0f / warp_allsum_f(x0 + x1);
+    const float p0 = x0 * rz, p1 = x1 * rz;
+    if (v0) row[lane] = p0;
+    if (v1) row[lane + 32] = p1;
+    bool took0 = false, took1 = false;
+    float sel_sum = 0.f;
+    for (int s = 0; s < k; ++s) {
+      // this lane's best unselected expert (the lower index on a tie)
+      float bp = -1.f;
+      int be = 2 * MM_MAX_EXPERTS;
+      if (v0 && !took0) { bp = p0; be = lane; }
+      if (v1 && !took1 && p1 > bp) { bp = p1; be = lane + 32; }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float op = __shfl_xor_sync(0xffffffffu, bp, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (op > bp || (op == bp && oe < be)) { bp = op; be = oe; }
+      }
+      took0 = took0 || be == lane;
+      took1 = took1 || be == lane + 32;
+      sel_sum += bp;
+      if (lane == 0) {
+        R.sel_e[t * k + s] = be;
+        R.sel_a[t * k + s] = bp;
+      }
+    }
+    __syncwarp();
+    const float inv = sel_sum + 1e-20f;
+    if (lane < k) R.sel_a[t * k + lane] = R.sel_a[t * k + lane] / inv;
+    __syncwarp();
+  }
+}
+
 // One warp: per-expert counts, their prefix, the touched experts in
 // ascending order and the assignments grouped by expert (token order kept).
 template <int MAXT>
