@@ -134,25 +134,33 @@ __device__ __forceinline__ void down_row(const __nv_bfloat16* wrow, const float*
   const float* hr[NA];
 #pragma unroll
   for (int q = 0; q < NA; ++q) hr[q] = hst + static_cast<size_t>(sbase + (q < m ? q : m - 1)) * I;
-  u64 acc[NA];
+  // two 8-element chunks per step into two accumulator sets, so that the
+  // loads of one overlap the products of the other (fixed order: the sets are
+  // added at the end)
+  u64 acc[2][NA];
 #pragma unroll
-  for (int q = 0; q < NA; ++q) acc[q] = 0ull;
-  for (int c = lane; c < I / 8; c += 32) {
-    const uint4 w = *reinterpret_cast<const uint4*>(wrow + c * 8);
-    const u64 w0 = bf2(w.x), w1 = bf2(w.y), w2 = bf2(w.z), w3 = bf2(w.w);
+  for (int q = 0; q < NA; ++q) acc[0][q] = acc[1][q] = 0ull;
+  for (int c0 = lane; c0 < I / 8; c0 += 64) {
 #pragma unroll
-    for (int q = 0; q < NA; ++q) {
-      const ulonglong2 ha = *reinterpret_cast<const ulonglong2*>(hr[q] + c * 8);
-      const ulonglong2 hb = *reinterpret_cast<const ulonglong2*>(hr[q] + c * 8 + 4);
-      acc[q] = ffma2(w0, ha.x, acc[q]);
-      acc[q] = ffma2(w1, ha.y, acc[q]);
-      acc[q] = ffma2(w2, hb.x, acc[q]);
-      acc[q] = ffma2(w3, hb.y, acc[q]);
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int c = c0 + 32 * h2;
+      if (c >= I / 8) break;
+      const uint4 w = *reinterpret_cast<const uint4*>(wrow + c * 8);
+      const u64 w0 = bf2(w.x), w1 = bf2(w.y), w2 = bf2(w.z), w3 = bf2(w.w);
+#pragma unroll
+      for (int q = 0; q < NA; ++q) {
+        const ulonglong2 ha = *reinterpret_cast<const ulonglong2*>(hr[q] + c * 8);
+        const ulonglong2 hb = *reinterpret_cast<const ulonglong2*>(hr[q] + c * 8 + 4);
+        acc[h2][q] = ffma2(w0, ha.x, acc[h2][q]);
+        acc[h2][q] = ffma2(w1, ha.y, acc[h2][q]);
+        acc[h2][q] = ffma2(w2, hb.x, acc[h2][q]);
+        acc[h2][q] = ffma2(w3, hb.y, acc[h2][q]);
+      }
     }
   }
   float v[NA];
 #pragma unroll
-  for (int q = 0; q < NA; ++q) v[q] = hsum2(acc[q]);
+  for (int q = 0; q < NA; ++q) v[q] = hsum2(acc[0][q]) + hsum2(acc[1][q]);
   const float r = reduce_scatter<NA>(v, lane);
   constexpr int span = 32 / NA;
   if (lane % span == 0) {
