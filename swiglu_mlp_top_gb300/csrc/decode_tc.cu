@@ -290,7 +290,7 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
   // ------------------------------------------------------------ routing
   if (ok && !spec) {
     if (moe) {
-      route_softmax_topk(R, T, A.E, A.k, s_bias, tid, kDtThreads);
+      route_softmax_topk_warp(R, T, A.E, A.k, s_bias, warp, kDtThreads / 32, lane);
       __syncthreads();
       if (warp == 0) route_group(R, T * A.k, A.E, lane);
     } else {
@@ -481,7 +481,7 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
           ok = epi_sync_and(r);
           if (ok) {
             const int etid = tid - 64, en = kDtEpiWarps * 32;
-            route_softmax_topk(R, T, A.E, A.k, s_bias, etid, en);
+            route_softmax_topk_warp(R, T, A.E, A.k, s_bias, etid >> 5, en >> 5, lane);
             for (int q = etid; q < A.E * Np; q += en) alpha[q] = 0.f;
             epi_sync();
             if (warp == 2) route_group(R, T * A.k, A.E, lane);
