@@ -59,12 +59,12 @@ def decode_kernel_name(w):
 # None where no capture of the current kernel exists.
 GATEUP_TRAFFIC_BYTES = {"moe_e8k2_t16384_skew": 195.55968e6 + 155.473408e6}
 # The same for the decode kernel that streams the weights (one launch per step).
-DECODE_TRAFFIC_BYTES = {"decode_moe_e8k2_t64": 89.903104e6 + 2.921728e6,
-                        "decode_moe_e8k2_t16": 89.82784e6 + 2.927104e6,
-                        "decode_moe_e8k2_t4": 87.951616e6 + 2.358784e6,
+DECODE_TRAFFIC_BYTES = {"decode_moe_e8k2_t64": 89.885696e6 + 3.497984e6,
+                        "decode_moe_e8k2_t16": 89.806336e6 + 2.620416e6,
+                        "decode_moe_e8k2_t4": 87.923712e6 + 2.422528e6,
                         "decode_dense_t16": 11.281152e6,
                         "dense_t100": 11.417856e6,
-                        "decode_dense_t1": 11.307008e6}
+                        "decode_dense_t1": 11.295744e6}
 
 
 def algorithmic_flops(w, T=None) -> float:
