@@ -86,7 +86,9 @@ def measured_peaks():
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running:
+    one sample before the region starts, every 200 ms inside it, and one
+    after it ends."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -106,12 +108,28 @@ class ClockSampler:
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
+            # the first sample is taken before the timed region starts
+            self._wait_lines(1, 3.0)
         except Exception:
             self.proc = None
         return self
 
+    def _lines(self):
+        try:
+            with open(self.path) as f:
+                return sum(1 for _ in f)
+        except OSError:
+            return 0
+
+    def _wait_lines(self, n, timeout_s):
+        t_end = time.time() + timeout_s
+        while self._lines() < n and time.time() < t_end and self.proc.poll() is None:
+            time.sleep(0.01)
+
     def __exit__(self, *a):
         if self.proc is not None:
+            # and one more after it ends, so the samples bracket a short region
+            self._wait_lines(self._lines() + 1, 1.0)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)

@@ -109,6 +109,21 @@ def test_moe_max_experts_and_topk(T, path):
     full_moe_check(moe_inputs(T, 256, 192, 64, "bf16", seed=150 + T), 8, 0.01, "bf16", path=path)
 
 
+@pytest.mark.parametrize("T,path", [(2000, "tensor"), (300, "simt"), (40, "stream_tc"), (3, "stream")])
+def test_moe_all_tokens_to_one_expert(T, path):
+    """Degenerate routing: a logit bias of +8 on expert 3 makes it every
+    token's first choice and -8 on experts 5-7 keeps them unselected, so the
+    slot-0 group of expert 3 holds all T rows and eleven of the sixteen
+    (slot, expert) groups are empty."""
+    bias = (0.0, 0.0, 0.0, 8.0, 0.0, -8.0, -8.0, -8.0)
+    inp = moe_inputs(T, 256, 320, 8, "bf16", seed=170 + T, bias=bias)
+    full_moe_check(inp, 2, 0.01, "bf16", path=path)
+    _, idx, _, _ = run_moe(inp, 2, 0.01, path)
+    idx = np.asarray(idx)
+    assert (idx[:, 0] == 3).all()
+    assert not np.isin(idx, (5, 6, 7)).any()
+
+
 @pytest.mark.parametrize("T,E,k", [(300, 4, 1), (257, 8, 2)])
 def test_moe_bf16_simt_second_path(T, E, k):
     full_moe_check(moe_inputs(T, 128, 192, E, "bf16", seed=9), k, 0.01, "bf16", path="simt")
