@@ -58,7 +58,8 @@ def decode_kernel_name(w):
 # gate/up GEMM, from an ncu capture of the current kernel on this workload;
 # None where no capture of the current kernel exists.
 GATEUP_TRAFFIC_BYTES = {"moe_e8k2_t16384_skew": 195.55968e6 + 155.473408e6,
-                        "moe_e4k1_t8192": 57.545472e6 + 12.62976e6}
+                        "moe_e4k1_t8192": 57.545472e6 + 12.62976e6,
+                        "dense_t4096": 17.554432e6 + 0.0}
 # The same for the decode kernel that streams the weights (one launch per step).
 DECODE_TRAFFIC_BYTES = {"decode_moe_e8k2_t64": 89.885696e6 + 3.497984e6,
                         "decode_moe_e8k2_t16": 89.806336e6 + 2.620416e6,
