@@ -267,22 +267,30 @@ def max_over_ranks(v: float, ws: int, dev) -> float:
     return float(t.item())
 
 
-def cpu_baseline(w, budget_s: float = 12.0):
-    """The fp64 oracle as it stands, on a bounded token sample of the workload."""
+def cpu_baseline(w, budget_s: float = 12.0, gpu_out=None):
+    """The fp64 oracle as it stands, on a bounded token sample of the workload.
+
+    With ``gpu_out`` (the GPU's outputs of one step on the same seed-0
+    inputs, copied to the host before the timed region) the sample the
+    oracle computed is also compared with them, after the timing: the
+    routing of every sampled token (near-ties, a top-k probability gap below
+    1e-6, counted apart), every sampled row of y, and aux_loss when the
+    sample is the whole workload."""
     import oracle
     from swiglu_mlp_top_gb300.inputs import to_f64
     probe_T = max(1, min(w.T, 64))
     cpu = make_workload_inputs(w, seed=0)
     x = to_f64(cpu["x"])
     args = {n: to_f64(cpu[n]) for n in ("Wg", "Wu", "Wd")}
+    last = {}
 
     def run(T):
         t0 = time.perf_counter()
         if w.kind == "moe":
-            oracle.moe_forward(x[:T], to_f64(cpu["Wr"]), args["Wg"], args["Wu"], args["Wd"], w.k,
-                               w.coef, to_f64(cpu.get("logit_bias")))
+            last["ref"] = oracle.moe_forward(x[:T], to_f64(cpu["Wr"]), args["Wg"], args["Wu"],
+                                             args["Wd"], w.k, w.coef, to_f64(cpu.get("logit_bias")))
         else:
-            oracle.swiglu_ffn(x[:T], args["Wg"], args["Wu"], args["Wd"])
+            last["ref"] = {"y": oracle.swiglu_ffn(x[:T], args["Wg"], args["Wu"], args["Wd"])}
         return time.perf_counter() - t0
 
     dt = run(probe_T)
@@ -290,9 +298,70 @@ def cpu_baseline(w, budget_s: float = 12.0):
     while T < w.T and dt < budget_s / 4:
         T = min(w.T, T * 4)
         dt = run(T)
-    return {"value": T / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{T} of {w.T} tokens of {w.name} (fp64 numpy, one pass, {dt:.2f} s)",
-            "tflops": algorithmic_flops(w, T) / dt / 1e12}
+    out = {"value": T / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+           "sample": f"{T} of {w.T} tokens of {w.name} (fp64 numpy, one pass, {dt:.2f} s)",
+           "tflops": algorithmic_flops(w, T) / dt / 1e12}
+    if gpu_out is not None:
+        out["parity"] = compare_with_oracle(w, gpu_out, last["ref"], T, x, args, oracle)
+    return out
+
+
+def compare_with_oracle(w, gpu_out, ref, T, x, args, oracle):
+    """Parity of one GPU step against the oracle on the first T tokens."""
+    y = gpu_out["y"][:T].astype(np.float64)
+    res = {"tokens": T, "of": w.T}
+    yref = ref["y"].copy()
+    if w.kind == "moe":
+        idx = gpu_out["topk_idx"][:T]
+        tie = oracle.near_tie_tokens(ref["probs"], w.k, 1e-6)
+        diff = (idx != ref["topk_idx"]).any(axis=-1)
+        res["near_ties"] = int(tie.sum())
+        res["near_tie_flips"] = int((diff & tie).sum())
+        res["idx_mismatch_non_tie"] = int((diff & ~tie).sum())
+        agree = ~diff
+        res["topk_w_max_abs_err"] = (float(np.abs(gpu_out["topk_w"][:T][agree]
+                                                   - ref["topk_w"][agree]).max())
+                                     if agree.any() else 0.0)
+        # rows the GPU routed differently (near-ties): the oracle's y on the GPU's choice
+        rows = np.nonzero(diff)[0]
+        if rows.size:
+            sel = idx[rows].astype(np.int64)
+            alpha = oracle.renormalise(np.take_along_axis(ref["probs"][rows], sel, axis=-1))
+            yref[rows] = oracle.combine(x[rows], args["Wg"], args["Wu"], args["Wd"], sel, alpha)
+        res["aux_abs_err"] = (abs(float(gpu_out["aux_loss"]) - ref["aux_loss"])
+                              if T == w.T else None)
+    rms = float(np.sqrt(np.mean(yref ** 2)))
+    res["y_rel_err"] = float(np.abs(y - yref).max() / rms)
+    res["y_tolerance"] = 1e-4 if w.dtype == "f32" else 2e-2
+    res["ok"] = bool(res["y_rel_err"] <= res["y_tolerance"]
+                     and res.get("idx_mismatch_non_tie", 0) == 0
+                     and res.get("topk_w_max_abs_err", 0.0) <= 1e-5
+                     and (res.get("aux_abs_err") is None or res["aux_abs_err"] <= 1e-5))
+    return res
+
+
+def workload_config(w, ws):
+    """The config object of a bench line; both arms print the same one."""
+    n_sets, per_set, floor = l2_rotation(w)
+    return {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "k": w.k,
+            "coef": w.coef, "logit_bias": list(w.logit_bias) if w.logit_bias else None,
+            "parallelism": f"replicas{ws}" if ws > 1 else "single",
+            "l2": f"{n_sets} rotating input sets of {per_set / 2**20:.0f} MiB, of which a step "
+                  f"reads at least {floor / 2**20:.0f} MiB (> 2x L2 over the rotation)"}
+
+
+def l2_rotation(w):
+    """(sets, bytes per set, bytes a step reads at least): enough distinct
+    copies of the inputs that the bytes a step reads, summed over the
+    rotation, are twice L2, so no step finds the last ones' lines in L2.  A
+    decode-sized MoE step reads only its touched experts, at least min(E, T*k)."""
+    es = 2 if w.dtype == "bf16" else 4
+    per_expert = 3 * w.H * w.I * es
+    n_exp = w.E if w.kind == "moe" else 1
+    per_set = w.T * w.H * es + n_exp * per_expert + (w.E * w.H * es if w.kind == "moe" else 0)
+    floor = per_set if w.kind != "moe" else min(per_set, min(w.E, w.T * w.k) * per_expert)
+    n_sets = max(1, min(64, int(np.ceil(2.0 * L2_BYTES / floor))))
+    return n_sets, per_set, floor
 
 
 def run_reference_arm(args, w):
@@ -312,8 +381,8 @@ def run_reference_arm(args, w):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * w.T / v, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "k": w.k,
-                       "note": "the fp64 CPU oracle timed on a token sample per step"},
+            "config": workload_config(w, args.gpus),
+            "note": "the fp64 CPU oracle timed on a token sample per step",
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": os.cpu_count(),
                              "kind": "oracle", "sample": samples[-1]},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -321,126 +390,192 @@ def run_reference_arm(args, w):
     print(json.dumps(line), flush=True)
 
 
-def run_our_arm(args, w):
-    ws, rank, local = dist_setup()
-    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    import swiglu_mlp_top_gb300 as mm
-    from swiglu_mlp_top_gb300 import _lib as L
-    lib = L.load()
-
-    probe = Step(w, dev, 1)
-    per_set = probe.input_bytes()
-    # enough distinct copies that the bytes a step reads, summed over the
-    # rotation, are twice L2: no step finds the last ones' lines in L2
-    read_floor = probe.read_bytes_floor()
-    n_sets = max(1, min(64, int(np.ceil(2.0 * L2_BYTES / read_floor))))
-    if n_sets > 1:
-        del probe
-        step = Step(w, dev, n_sets)
-    else:
-        step = probe
-    stream = torch.cuda.current_stream()
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    assert mm.check_status(step.ws) == 0
-
-    use_graph = args.graph == "on" or (args.graph == "auto" and streams_weights(w))
-    # ---- timed region: K steps, device events on the launching stream
-    dominant = L.MM_KERNEL_DECODE if streams_weights(w) else L.MM_KERNEL_GATEUP
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    if use_graph:
-        # decode-sized steps are launch-bound: capture the K steps into one CUDA
-        # graph (the library allocates nothing and issues no attribute changes
-        # once warmed up) and time one replay of it
-        graph = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream()
-        cap.wait_stream(torch.cuda.current_stream())
-        launches0 = lib.mm_launch_count()
-        with torch.cuda.graph(graph, stream=cap):
-            for i in range(args.steps):
-                step(i)
-        launches = int(lib.mm_launch_count() - launches0)
-        graph.replay()                      # warm replay
-        torch.cuda.synchronize()
-    barrier(ws)
-    torch.cuda.synchronize()
-    import ctypes as C
-    tot = C.c_double(0)
-    nl = C.c_int(0)
-    with ClockSampler(local) as clk:
-        if use_graph:
-            ev0.record(stream)
-            graph.replay()
-            ev1.record(stream)
-        else:
-            launches0 = lib.mm_launch_count()
-            ev0.record(stream)
-            for i in range(args.steps):
-                step(i)
-            ev1.record(stream)
-            launches = int(lib.mm_launch_count() - launches0)
-        torch.cuda.synchronize()
-        ms = ev0.elapsed_time(ev1)
-        if not use_graph:
-            # the dominant kernel's launches, timed by events around each on
-            # its stream, in a second run of the same K steps: events between
-            # the kernels of a step stop the next kernel from launching early
-            # (programmatic dependent launch), so the step time above is taken
-            # without them
-            lib.mm_profile_start(dominant, args.steps)
-            for i in range(args.steps):
-                step(i)
-            torch.cuda.synchronize()
-            lib.mm_profile_stop(C.byref(tot), C.byref(nl))
-    barrier(ws)
-    if use_graph:
-        # the graph holds only this library's kernels: the step time is the kernels' time
-        tot.value, nl.value = ms, args.steps
-    ms = max_over_ranks(ms, ws, dev)
-    status = mm.check_status(step.ws)
-    assert status == 0, f"device watchdog status {status}"
-    ms_per_step = ms / args.steps
-    value = ws * w.T * args.steps / (ms / 1e3)
-    flops = algorithmic_flops(w)
-    tflops = flops / (ms_per_step / 1e3) / 1e12
-
-    # ---- dominant kernel roofline
+def roofline(w, step, k_ms, n_launches, use_graph):
+    """The dominant kernel's roofline: achieved = its algorithmic work per
+    launch / its average launch time."""
     peaks, peak_src = measured_peaks()
-    k_ms = tot.value / max(1, nl.value)
     if streams_weights(w):
         # weight streaming (one kernel per step): HBM-bound; algorithmic bytes =
         # the weights of the experts some token selected, x read and y written
         touched = 1 if w.kind == "dense" else int(torch.unique(step.idx).numel())
         wbytes = touched * 3.0 * w.H * w.I * 2 + 2.0 * w.T * w.H * 2
         achieved = wbytes / (k_ms / 1e3) / 1e9
-        roof = {"kernel": decode_kernel_name(w)
+        return {"kernel": decode_kernel_name(w)
                           + (", CUDA-graph replay of the whole step" if use_graph else ""),
                 "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": DECODE_TRAFFIC_BYTES.get(w.name),
                 "peak_source": f"{peak_src} HBM copy bandwidth (MEASURED_PEAKS.json)",
-                "kernel_ms": k_ms, "launches_timed": nl.value, "bytes_per_launch": wbytes,
+                "kernel_ms": k_ms, "launches_timed": n_launches, "bytes_per_launch": wbytes,
                 "experts_touched": touched}
-    else:
-        # grouped gate/up GEMM: 4*H*I flops per assignment
-        gate_flops = float(w.T) * w.k * 4.0 * w.H * w.I
-        achieved = gate_flops / (k_ms / 1e3) / 1e12
-        roof = {"kernel": ("grouped_gemm_kernel<gate/up> (tcgen05 2-SM GEMM + SwiGLU epilogue)"
-                           if not use_graph else "whole step (CUDA-graph replay)"),
-                "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                "traffic": GATEUP_TRAFFIC_BYTES.get(w.name),
-                "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)",
-                "kernel_ms": k_ms, "launches_timed": nl.value,
-                "flops_per_launch": gate_flops}
+    # grouped gate/up GEMM: 4*H*I flops per assignment
+    gate_flops = float(w.T) * w.k * 4.0 * w.H * w.I
+    achieved = gate_flops / (k_ms / 1e3) / 1e12
+    return {"kernel": ("grouped_gemm_kernel<gate/up> (tcgen05 2-SM GEMM + SwiGLU epilogue)"
+                       if not use_graph else "whole step (CUDA-graph replay)"),
+            "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+            "traffic": GATEUP_TRAFFIC_BYTES.get(w.name),
+            "peak_source": f"{peak_src} bf16 dense burst (MEASURED_PEAKS.json)",
+            "kernel_ms": k_ms, "launches_timed": n_launches, "flops_per_launch": gate_flops,
+            "kernel_timing": "CUDA events around each launch of the kernel on its stream, "
+                             "in a separate run of K steps"}
 
-    if not use_graph:
-        roof["kernel_timing"] = ("CUDA events around each launch of the kernel on its stream, "
-                                 "in a second run of the K timed steps")
+
+def measure(step, lib, steps, warmup, ws, local, use_graph, dominant,
+            min_total_s=0.5, min_repeats=5):
+    """Time one workload: W warm-up steps, then repeats of a region of exactly
+    `steps` steps (barrier + synchronize on both sides of each, CUDA events
+    on the launching stream), until the regions cover min_total_s and there
+    are at least min_repeats of them; the clock sampler runs over all of
+    them.  Returns the median region time (max over ranks) and the rest."""
+    import ctypes as C
+    mm = step.mm
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert mm.check_status(step.ws) == 0
+    graph = None
+    launches = 0
+    if use_graph:
+        # decode-sized steps are launch-bound: capture the K steps into one CUDA
+        # graph (the library allocates nothing and issues no attribute changes
+        # once warmed up) and time replays of it
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        l0 = lib.mm_launch_count()
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(steps):
+                step(i)
+        launches = int(lib.mm_launch_count() - l0)
+        graph.replay()                      # warm replay
+        torch.cuda.synchronize()
+    regions = []
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t_start = time.perf_counter()
+        while len(regions) < min_repeats or sum(regions) / 1e3 < min_total_s:
+            barrier(ws)
+            torch.cuda.synchronize()
+            if graph is not None:
+                ev0.record(stream)
+                graph.replay()
+                ev1.record(stream)
+            else:
+                l0 = lib.mm_launch_count()
+                ev0.record(stream)
+                for i in range(steps):
+                    step(i)
+                ev1.record(stream)
+                launches = int(lib.mm_launch_count() - l0)
+            torch.cuda.synchronize()
+            regions.append(ev0.elapsed_time(ev1))
+            if len(regions) >= 2000 or time.perf_counter() - t_start > 30.0:
+                break
+    clocks = clk.summary()
+    barrier(ws)
+    med = statistics.median(regions)
+    med = max_over_ranks(med, ws, step.y.device)
+    if graph is not None:
+        # the graph holds only this library's kernels: the step time is the kernels' time
+        k_ms, nl = med / steps, steps
+    else:
+        # the dominant kernel's launches, timed by events around each on its
+        # stream, in a separate run of K steps: events between the kernels of
+        # a step stop the next kernel from launching early (programmatic
+        # dependent launch), so the step time above is taken without them
+        tot, n = C.c_double(0), C.c_int(0)
+        lib.mm_profile_start(dominant, steps)
+        for i in range(steps):
+            step(i)
+        torch.cuda.synchronize()
+        lib.mm_profile_stop(C.byref(tot), C.byref(n))
+        k_ms, nl = tot.value / max(1, n.value), n.value
+    status = mm.check_status(step.ws)
+    assert status == 0, f"device watchdog status {status}"
+    return {"region_ms": med, "ms_per_step": med / steps, "repeats": len(regions),
+            "region_ms_min": min(regions), "region_ms_max": max(regions),
+            "timed_s": sum(regions) / 1e3, "launches": launches, "clocks": clocks,
+            "kernel_ms": k_ms, "kernel_launches": nl, "timing":
+            "cuda_graph_replay" if graph is not None else "stream_launches"}
+
+
+def make_step(w, dev):
+    n_sets, _, _ = l2_rotation(w)
+    return Step(w, dev, n_sets)
+
+
+#: Workloads measured after the headline one, one entry each in the line's
+#: per_workload object (each the configuration a parity test covers).
+PER_WORKLOADS = ["dense_t4096", "dense_t100", "moe_e4k1_t8192"] + \
+    [f"decode_{kind}_t{T}" for kind in ("dense", "moe_e8k2") for T in (1, 4, 16, 64)]
+
+
+def per_workload_entry(name, lib, ws, local, dev, warmup):
+    w = WORKLOADS[name]
+    step = make_step(w, dev)
+    use_graph = streams_weights(w)
+    dominant = 7 if use_graph else 4          # MM_KERNEL_DECODE / MM_KERNEL_GATEUP
+    # calibrate: K steps per region so that one region takes about 20 ms
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(10):
+        step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    est = e0.elapsed_time(e1) / 10
+    steps = int(min(1000, max(10, 20.0 / max(est, 1e-3))))
+    m = measure(step, lib, steps, warmup, ws, local, use_graph, dominant)
+    roof = roofline(w, step, m["kernel_ms"], m["kernel_launches"], use_graph)
+    flops = algorithmic_flops(w)
+    out = {"ms_per_step": m["ms_per_step"], "tokens_per_s": ws * w.T / (m["ms_per_step"] / 1e3),
+           "tflops": flops / (m["ms_per_step"] / 1e3) / 1e12,
+           "frac_of_bf16_peak_whole_step": flops / (m["ms_per_step"] / 1e3) / 1e12
+           / measured_peaks()[0]["bf16_tflops"],
+           "steps_per_region": steps, "repeats": m["repeats"], "timed_s": m["timed_s"],
+           "region_ms_min": m["region_ms_min"], "region_ms_max": m["region_ms_max"],
+           "timing": m["timing"], "roofline": {k: roof[k] for k in
+                                               ("kernel", "bound", "achieved", "peak", "unit",
+                                                "frac", "kernel_ms")},
+           "clocks": m["clocks"], "l2": workload_config(w, ws)["l2"]}
+    del step
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_our_arm(args, w):
+    ws, rank, local = dist_setup()
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import swiglu_mlp_top_gb300 as mm  # noqa: F401
+    from swiglu_mlp_top_gb300 import _lib as L
+    lib = L.load()
+
+    step = make_step(w, dev)
+    stream = torch.cuda.current_stream()
+    use_graph = args.graph == "on" or (args.graph == "auto" and streams_weights(w))
+    dominant = L.MM_KERNEL_DECODE if streams_weights(w) else L.MM_KERNEL_GATEUP
+
+    # one step on the seed-0 inputs, kept for the parity check of the CPU-baseline leg
+    step(0)
+    torch.cuda.synchronize()
+    gpu_out = {"y": step.y.float().cpu().numpy()}
+    if w.kind == "moe":
+        gpu_out.update(topk_idx=step.idx.cpu().numpy(), topk_w=step.tw.cpu().numpy(),
+                       aux_loss=float(step.aux))
+
+    m = measure(step, lib, args.steps, args.warmup, ws, local, use_graph, dominant)
+    ms_per_step = m["ms_per_step"]
+    value = ws * w.T / (ms_per_step / 1e3)
+    flops = algorithmic_flops(w)
+    tflops = flops / (ms_per_step / 1e3) / 1e12
+    roof = roofline(w, step, m["kernel_ms"], m["kernel_launches"], use_graph)
 
     # ---- end to end through the public API: pinned host x in, y/idx/w/aux out.
     # Every step copies its x in and its outputs out; the copies run on their
@@ -520,26 +655,36 @@ def run_our_arm(args, w):
                "ms_per_step": ems / args.e2e_steps,
                "pipelining": f"copies on their own streams, {nbuf} buffers, one copy each way",
                "timing": "cuda_graph_replay" if e2e_graph is not None else "stream_launches"}
+    del step
+    torch.cuda.empty_cache()
+
+    per = None
+    if not args.no_per_workload:
+        per = {}
+        for name in PER_WORKLOADS:
+            if name != w.name:
+                per[name] = per_workload_entry(name, lib, ws, local, dev, args.warmup)
 
     cpu = None
+    parity = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w)
+        cpu = cpu_baseline(w, gpu_out=gpu_out)
+        parity = cpu.pop("parity", None)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": w.dtype, "data": "synthetic",
-                "config": {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E,
-                           "k": w.k, "coef": w.coef,
-                           "logit_bias": list(w.logit_bias) if w.logit_bias else None,
-                           "parallelism": f"replicas{ws}" if ws > 1 else "single",
-                           "l2": f"{len(step.sets)} rotating input sets of "
-                                 f"{per_set / 2**20:.0f} MiB, of which a step reads at least "
-                                 f"{read_floor / 2**20:.0f} MiB (> 2x L2 over the rotation)"},
-                "tflops": tflops, "timing": "cuda_graph_replay" if use_graph else "stream_launches",
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": launches, "clocks": clk.summary()}
+                "config": workload_config(w, ws),
+                "tflops": tflops, "timing": m["timing"],
+                "repeats": {"n": m["repeats"], "steps_each": args.steps,
+                            "region_ms_median": m["region_ms"], "region_ms_min": m["region_ms_min"],
+                            "region_ms_max": m["region_ms_max"], "timed_s": m["timed_s"],
+                            "note": "value and ms_per_step are from the median region"},
+                "roofline": roof, "cpu_baseline": cpu, "parity": parity, "e2e": e2e,
+                "gpu_launches": m["launches"], "clocks": m["clocks"],
+                "per_workload": per}
         print(json.dumps(line), flush=True)
 
 
@@ -552,6 +697,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="measure only the selected workload")
     ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                     help="time a CUDA-graph replay of the K steps (auto: T <= 64)")
     args = ap.parse_args()

@@ -21,10 +21,12 @@
  *     Router logits, probabilities, alpha and the aux loss are always fp32.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
  *     call only enqueues work on that stream and returns; none synchronises
- *     the host except mm_check_status().  The library allocates no device
- *     memory: scratch lives in the caller's `workspace`, whose size the
- *     matching *_workspace_bytes() function returns.  Calls that share a
- *     workspace must be ordered on one stream.  The first 256 bytes of a
+ *     the host except mm_check_status().  No call allocates device memory:
+ *     scratch lives in the caller's `workspace`, whose size the matching
+ *     *_workspace_bytes() function returns.  The one exception is a fixed
+ *     array of MM_NOALLOC_SCRATCH_BYTES that the library's module reserves
+ *     on every GPU where it is loaded (used only by mm_swiglu_ffn_noalloc).
+ *     Calls that share a workspace must be ordered on one stream.  The first 256 bytes of a
  *     workspace hold device-side state (the watchdog word and the counter of
  *     the streaming kernel's grid barrier): zero them once before the
  *     workspace's first use (cudaMemset).  Every call leaves them consistent,
@@ -128,8 +130,12 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
  *   - All calls share the one array, and it keeps the last call's contents.
  *     Calls that overlap on the GPU therefore race: order them on one
  *     stream, or finish one before starting the next.
- *   - Its device watchdog word is not readable through mm_check_status.
- *     Stream errors are still reported by the CUDA runtime.
+ *   - Each call first zeroes the array's 256-byte state header on `stream`
+ *     (grid-barrier counters and the watchdog word), so a call whose
+ *     pipeline wait gave up leaves no state behind for the next one.  That
+ *     watchdog word is not readable through mm_check_status: a timed-out
+ *     call is not reported.  Stream errors are still reported by the CUDA
+ *     runtime.
  * ---------------------------------------------------------------------- */
 #define MM_NOALLOC_SCRATCH_BYTES (16u << 20)
 
@@ -210,12 +216,9 @@ int mm_watchdog_selftest(void* workspace, size_t workspace_bytes,
  * ---------------------------------------------------------------------- */
 typedef enum {
   MM_KERNEL_ROUTER = 1,     /* logits/softmax/top-k/alpha/aux partials      */
-  MM_KERNEL_SCAN = 2,       /* group offsets + aux loss finalisation        */
-  MM_KERNEL_DISPATCH = 3,   /* token permute into expert-contiguous rows    */
+  MM_KERNEL_DISPATCH = 3,   /* aux finalisation, group offsets, token permute */
   MM_KERNEL_GATEUP = 4,     /* gate/up GEMM with the SwiGLU epilogue        */
   MM_KERNEL_DOWN = 5,       /* down GEMM with the alpha-scaled combine      */
-  MM_KERNEL_WCONVERT = 6,   /* unused: the fp16 copy of the down weights is
-                               made inside the gate/up kernel                */
   MM_KERNEL_DECODE = 7      /* decode-sized weight-streaming kernel (whole call) */
 } mm_kernel_id;
 

@@ -148,6 +148,9 @@ def aux_loss_from_stats(load, prob, E, coef):
 
 
 def aux_loss(topk_idx, p, coef):
+    """L_aux from the selections and the probabilities directly ([L13] §1.6;
+    [CH4] §4.4): E is the number of probability columns, load_e counts every
+    slot (the [k, E] one-hot mean summed over k)."""
     p = _f64(p)
     E = p.shape[1]
     load, _ = expert_load(topk_idx, E)

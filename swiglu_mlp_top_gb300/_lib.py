@@ -44,8 +44,7 @@ SIGNATURES = {
     "mm_profile_start": (_i32, [_i32, _i32]),
     "mm_profile_stop": (_i32, [C.POINTER(C.c_double), C.POINTER(C.c_int)]),
 }
-(MM_KERNEL_ROUTER, MM_KERNEL_SCAN, MM_KERNEL_DISPATCH, MM_KERNEL_GATEUP, MM_KERNEL_DOWN, MM_KERNEL_WCONVERT,
- MM_KERNEL_DECODE) = 1, 2, 3, 4, 5, 6, 7
+MM_KERNEL_ROUTER, MM_KERNEL_DISPATCH, MM_KERNEL_GATEUP, MM_KERNEL_DOWN, MM_KERNEL_DECODE = 1, 3, 4, 5, 7
 
 _lib = None
 

@@ -478,7 +478,11 @@ int mm_moe_route(const void* x, const void* Wr, int64_t T, int H, int E, int k, 
 uint64_t mm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int mm_profile_start(int kernel_id, int max_launches) {
-  if (kernel_id < MM_KERNEL_ROUTER || kernel_id > MM_KERNEL_DECODE) return MM_ERR_INVALID_ARG;
+  switch (kernel_id) {
+    case MM_KERNEL_ROUTER: case MM_KERNEL_DISPATCH: case MM_KERNEL_GATEUP: case MM_KERNEL_DOWN:
+    case MM_KERNEL_DECODE: break;
+    default: return MM_ERR_INVALID_ARG;
+  }
   if (max_launches < 1 || max_launches > 100000) return MM_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_prof.mu);
   g_prof.kernel = kernel_id;

@@ -52,6 +52,14 @@ extern "C" int mm_swiglu_ffn_noalloc(const void* x, const void* Wg, const void* 
   void* scratch = nullptr;
   const int rc = scratch_for_current_device(&scratch);
   if (rc != MM_OK) return rc;
+  // The array's first 256 bytes hold the streaming kernels' grid-barrier
+  // counters and the watchdog word.  A call whose wait gave up leaves them
+  // non-zero, and nobody can read or clear them through mm_check_status, so
+  // every call zeroes them first, in order on its own stream (a memset
+  // allocates nothing).
+  const cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(mm::WsHeader),
+                                        static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return MM_ERR_CUDA;
   return mm_swiglu_ffn_ex(x, Wg, Wu, Wd, y, T, H, I, dtype, scratch, kNoAllocScratchBytes, stream,
                           path);
 }

@@ -297,6 +297,40 @@ def test_aux_coef_zero_is_zero():
     assert out["aux_loss"] == 0.0
 
 
+def test_aux_loss_wrapper_extremes_table():
+    """aux_loss(topk_idx, p, coef) on selections and probabilities built to
+    give chapter 4 §4.4's two rows (E = 4, top-1, coef = 1): balanced load and
+    mean probability 1/4 -> 1.0; every token on expert 0 with mean
+    probabilities (0.7, 0.1, 0.1, 0.1) -> 2.8."""
+    g = golden("aux_loss_tables.json")
+    bal, col = g["extremes"]
+    T = 8
+    idx = (np.arange(T) % 4)[:, None]                         # 2 tokens per expert
+    p = np.full((T, 4), 0.25)
+    assert abs(O.aux_loss(idx, p, 1.0) - bal["times_E"]) < 1e-14
+    idx = np.zeros((T, 1), dtype=np.int64)                     # collapsed on expert 0
+    p = np.tile(np.array(col["prob"]), (T, 1))
+    p[:4] += np.array([0.1, -0.1, 0.0, 0.0])                   # rows differ, the mean does not
+    p[4:] -= np.array([0.1, -0.1, 0.0, 0.0])
+    assert abs(O.aux_loss(idx, p, 1.0) - col["times_E"]) < 1e-14
+
+
+def test_aux_loss_wrapper_counts_every_slot_and_every_expert():
+    """k = 2 with a uniform router: load_e = count_e / T summed over both slots
+    (sum_e load_e = k), prob_e = 1/E, so aux = E*coef*k/E = k*coef (lesson 13
+    §1.6 / step 6 summed [k, E] one-hot mean).  The highest expert is never
+    selected: E must come from the probabilities, not from the indices."""
+    E, k, T, coef = 6, 2, 10, 0.01
+    idx = np.tile(np.arange(k), (T, 1))                        # experts 0, 1 only
+    p = np.full((T, E), 1.0 / E)
+    assert abs(O.aux_loss(idx, p, coef) - k * coef) < 1e-17
+    # agrees with the routing path's own value on a random router
+    r = rng(10)
+    x, Wr = r.normal(size=(T, 7)), r.normal(size=(E, 7))
+    out = O.moe_route(x, Wr, k, coef)
+    assert abs(O.aux_loss(out["topk_idx"], out["probs"], coef) - out["aux_loss"]) < 1e-17
+
+
 # --------------------------------------------------------------------------
 # MoE layer: special cases that reduce to known forms
 # --------------------------------------------------------------------------

@@ -86,3 +86,7 @@ def test_reference_arm_prints_once_under_two_ranks():
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+    # the same config object as the GPU arm prints for this workload
+    sys.path.insert(0, ROOT)
+    import bench
+    assert line["config"] == bench.workload_config(bench.WORKLOADS["tiny_moe_f32"], 2)

@@ -2,14 +2,12 @@
 device memory, running on the library's fixed device scratch.
 
 It must give the same output as mm_swiglu_ffn with a caller-owned
-workspace, on two calls in a row, so the scratch is reused correctly.
+workspace, bit for bit, on two calls in a row, so the scratch is reused
+correctly, for every kernel family the automatic path picks.
 This file is collected last so that a run stopping at its first failure has
 already run every other test.  It passes on its own in a fresh process and
 after the other tests.
 """
-import ctypes as C
-
-import numpy as np
 import pytest
 import torch
 
@@ -17,8 +15,6 @@ from swiglu_mlp_top_gb300 import _lib as L
 from swiglu_mlp_top_gb300.inputs import make_inputs
 
 pytestmark = pytest.mark.gpu
-
-Y_TOL_BF16 = 2e-2     # the bf16 tolerance of the parity tests (max |dy| / rms)
 
 
 def _call_noalloc(lib, g, y, T, H, I):
@@ -39,27 +35,28 @@ def _call_workspace(lib, g, y, T, H, I):
     return rc
 
 
-def _rel(a, b):
-    a = a.double().cpu().numpy()
-    b = b.double().cpu().numpy()
-    return float(np.abs(a - b).max() / np.sqrt((b ** 2).mean()))
-
-
-def test_noalloc_matches_workspace_entry_point_twice():
+# Token counts that take each kernel family the automatic path picks: the
+# CUDA-core streaming kernel (1, 4 tokens), the tensor-core streaming kernel
+# with the tokens as the M operand (64, 100), and the tensor-core GEMMs (300,
+# 1000).  The streaming kernels keep grid-barrier counters in the scratch
+# header, so each case runs twice in a row on the same array.
+@pytest.mark.parametrize("T", [1, 4, 64, 100, 300, 1000])
+def test_noalloc_matches_workspace_entry_point_twice(T):
     import __graft_entry__
     __graft_entry__.build()
     lib = L.load()
     H, I = 768, 2432
-    for seed, T in ((21, 300), (22, 1000)):            # two calls in a row, new inputs each
-        inp = make_inputs(T, H, I, "bf16", seed=seed)
+    for call in range(2):                                # two calls in a row, new inputs each
+        inp = make_inputs(T, H, I, "bf16", seed=20 + 2 * T + call)
         g = {n: v.cuda() for n, v in inp.items()}
         y_ref = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
         assert _call_workspace(lib, g, y_ref, T, H, I) == L.MM_OK
         y = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device="cuda")
         assert _call_noalloc(lib, g, y, T, H, I) == L.MM_OK
         torch.cuda.synchronize()
-        assert torch.isfinite(y.float()).all()
-        assert _rel(y, y_ref) <= Y_TOL_BF16
+        # the same kernels on the same inputs: every kernel is deterministic,
+        # so the two results agree bit for bit
+        assert torch.equal(y, y_ref), f"T={T} call {call}: noalloc result differs"
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
