@@ -73,16 +73,41 @@ def swiglu_ffn(x, Wg, Wu, Wd):
 # --------------------------------------------------------------------------
 # Router: logits, softmax, top-k, renormalisation
 # --------------------------------------------------------------------------
-def router_logits(x, Wr, logit_bias=None):
+def router_logits(x, Wr, logit_bias=None, logit_noise=None):
     """r = W_router x  ([L13] §1.5; [CH4] §4.3 "gate" = nn.Linear(H, E, bias=False)).
 
     ``logit_bias`` ([E] or None) is added to every token's logits; None gives
-    the pages' bias-free router exactly.
+    the pages' bias-free router exactly.  ``logit_noise`` ([T, E] or None) is
+    the router noise of NOTE08 §10's table ("add noise to the router to
+    encourage exploration"), read as an additive perturbation of each
+    token's logits; its random draws are an input.
     """
     r = _f64(x) @ _f64(Wr).T                      # [T, E]
     if logit_bias is not None:
         r = r + _f64(logit_bias)[None, :]
+    if logit_noise is not None:
+        r = r + _f64(logit_noise)
     return r
+
+
+def logsumexp(r):
+    """lse_t = log sum_e exp(r_{t,e}), with the row maximum taken out first
+    (lse = m + log sum_e exp(r_e - m), the same value)."""
+    r = _f64(r)
+    m = r.max(axis=-1)
+    return m + np.log(np.exp(r - m[:, None]).sum(axis=-1))
+
+
+def z_loss(r, z_coef):
+    """Router z-loss: L_z = z_coef * (1/T) * sum_t (lse_t)^2.
+
+    NOTE08 §10's table names z-loss as the mechanism that keeps the router
+    logits from growing too large and gives no formula; this is the
+    standard definition (the mean squared log-partition function of the
+    router's softmax), the plainest reading.
+    """
+    lse = logsumexp(r)
+    return F64(z_coef) * float(np.mean(lse ** 2))
 
 
 def softmax(r):
@@ -183,35 +208,31 @@ def combine(x, Wg, Wu, Wd, topk_idx, alpha):
     return y
 
 
-def moe_forward(x, Wr, Wg, Wu, Wd, k, coef, logit_bias=None):
+def moe_forward(x, Wr, Wg, Wu, Wd, k, coef, logit_bias=None, logit_noise=None, z_coef=0.0):
     """The MoE layer forward ([L13] step 4-6; [CH4] §4.3-4.4).
 
     Returns a dict with y [T, H], topk_idx [T, k], topk_w (alpha) [T, k],
-    aux_loss (float), probs p [T, E] and the per-expert counts [E].
+    aux_loss (float), probs p [T, E], the per-expert counts [E], the
+    logsumexp of each token's logits lse [T] and the router z-loss.
     """
-    x = _f64(x)
-    E = len(Wg)
-    p = softmax(router_logits(x, Wr, logit_bias))
-    idx, val = topk(p, k)
-    alpha = renormalise(val)
-    y = combine(x, Wg, Wu, Wd, idx, alpha)
-    load, counts = expert_load(idx, E)
-    aux = aux_loss_from_stats(load, mean_prob(p), E, coef)
-    return {"y": y, "topk_idx": idx, "topk_w": alpha, "aux_loss": aux,
-            "probs": p, "counts": counts}
+    out = moe_route(x, Wr, k, coef, logit_bias, logit_noise, z_coef)
+    out["y"] = combine(x, Wg, Wu, Wd, out["topk_idx"], out["topk_w"])
+    return out
 
 
-def moe_route(x, Wr, k, coef, logit_bias=None):
-    """Router half of :func:`moe_forward` (no experts): idx, alpha, aux, probs."""
+def moe_route(x, Wr, k, coef, logit_bias=None, logit_noise=None, z_coef=0.0):
+    """Router half of :func:`moe_forward` (no experts): idx, alpha, aux, probs,
+    counts, lse, z_loss."""
     x = _f64(x)
-    p = softmax(router_logits(x, Wr, logit_bias))
+    r = router_logits(x, Wr, logit_bias, logit_noise)
+    p = softmax(r)
     E = p.shape[1]
     idx, val = topk(p, k)
     alpha = renormalise(val)
     load, counts = expert_load(idx, E)
     aux = aux_loss_from_stats(load, mean_prob(p), E, coef)
     return {"topk_idx": idx, "topk_w": alpha, "aux_loss": aux, "probs": p,
-            "counts": counts}
+            "counts": counts, "lse": logsumexp(r), "z_loss": z_loss(r, z_coef)}
 
 
 def near_tie_tokens(p, k, gap=1e-6):

@@ -142,7 +142,7 @@ def _logits_for_probs(p, H=6):
     return x, Wr
 
 
-@pytest.mark.parametrize("via", ["weights", "bias"])
+@pytest.mark.parametrize("via", ["weights", "bias", "noise"])
 def test_routing_worked_example(via):
     """Lesson 13 §1.5: p = [0.05, 0.10, 0.80, 0.05]."""
     g = golden("routing_worked_example.json")
@@ -150,12 +150,15 @@ def test_routing_worked_example(via):
     if via == "weights":
         x, Wr = _logits_for_probs(p)
         bias = None
-    else:
+    elif via == "bias":
         x, Wr, bias = np.ones((1, 3)), np.zeros((4, 3)), np.log(p)
-    probs = O.softmax(O.router_logits(x, Wr, bias))
+    noise = None
+    if via == "noise":                         # the logits arrive as router noise
+        x, Wr, bias, noise = np.ones((1, 3)), np.zeros((4, 3)), None, np.log(p)[None, :]
+    probs = O.softmax(O.router_logits(x, Wr, bias, noise))
     np.testing.assert_allclose(probs[0], p, rtol=1e-14)
     for key, k in (("top1", 1), ("top2", 2)):
-        r = O.moe_route(x, Wr, k, 0.0, bias)
+        r = O.moe_route(x, Wr, k, 0.0, bias, noise)
         assert r["topk_idx"][0].tolist() == g[key]["idx"]
         np.testing.assert_allclose(r["topk_w"][0], g[key]["alpha"], rtol=1e-14)
 
@@ -475,3 +478,86 @@ def test_config_intermediate_size():
     from swiglu_mlp_top_gb300.inputs import intermediate_size
     g = golden("minimind_config.json")
     assert intermediate_size(g["hidden_size"]) == g["intermediate_size"]
+
+
+# --------------------------------------------------------------------------
+# Router variants (p-chao.com note 08 §10 table: router noise, z-loss)
+# --------------------------------------------------------------------------
+def _lse_bruteforce(row):
+    """log of the plain sum of exponentials (no maximum taken out), summed
+    exactly with math.fsum: fine for the small logits it is used on."""
+    return math.log(math.fsum(math.exp(v) for v in row))
+
+
+def test_logsumexp_closed_forms():
+    # two experts: log(e^a + e^b); all-equal logits c: c + log E
+    for a, b in ((0.3, -1.2), (2.0, 2.0), (-5.0, 1.0)):
+        assert abs(O.logsumexp(np.array([[a, b]]))[0] - math.log(math.exp(a) + math.exp(b))) < 1e-15
+    for E, c in ((1, 0.7), (4, 0.0), (8, -3.0)):
+        assert abs(O.logsumexp(np.full((1, E), c))[0] - (c + math.log(E))) < 1e-14
+    # a dominant logit: lse = max + log(1 + e^{-1000}) = 1000 exactly in fp64
+    # (a plain exp of the logits would overflow)
+    assert O.logsumexp(np.array([[1000.0, 0.0]]))[0] == 1000.0
+
+
+def test_logsumexp_bruteforce():
+    r = rng(11).normal(size=(9, 6)) * 2
+    for t in range(r.shape[0]):
+        assert abs(O.logsumexp(r[t:t + 1])[0] - _lse_bruteforce(r[t].tolist())) < 1e-13
+
+
+def test_z_loss_closed_forms():
+    """Uniform router (Wr = 0): lse = log E for every token, so
+    L_z = z_coef (log E)^2; one expert: lse = r, L_z = z_coef mean r^2;
+    z_coef = 0 gives 0."""
+    x = rng(12).normal(size=(10, 5))
+    for E in (2, 4, 8):
+        out = O.moe_route(x, np.zeros((E, 5)), 1, 0.0, z_coef=1e-3)
+        assert abs(out["z_loss"] - 1e-3 * math.log(E) ** 2) < 1e-17
+    Wr = rng(13).normal(size=(1, 5))
+    r = x @ Wr.T
+    assert abs(O.z_loss(r, 0.5) - 0.5 * float(np.mean(r[:, 0] ** 2))) < 1e-14
+    assert O.moe_route(x, rng(14).normal(size=(4, 5)), 2, 0.01)["z_loss"] == 0.0
+
+
+def test_z_loss_bruteforce():
+    r = rng(15).normal(size=(7, 5))
+    ref = 0.02 * math.fsum(_lse_bruteforce(r[t].tolist()) ** 2 for t in range(7)) / 7
+    assert abs(O.z_loss(r, 0.02) - ref) < 1e-15
+
+
+def test_noise_equal_rows_is_a_logit_bias():
+    """Noise that is the same vector b for every token routes exactly as
+    logit_bias = b (two independent code paths of the oracle)."""
+    r = rng(16)
+    x, Wr = r.normal(size=(20, 6)), r.normal(size=(5, 6)) * 0.5
+    b = r.normal(size=5)
+    a = O.moe_route(x, Wr, 2, 0.01, logit_bias=b, z_coef=1e-2)
+    n = O.moe_route(x, Wr, 2, 0.01, logit_noise=np.tile(b, (20, 1)), z_coef=1e-2)
+    for key in ("topk_idx", "topk_w", "probs", "lse"):
+        np.testing.assert_allclose(a[key], n[key], rtol=0, atol=1e-15)
+    assert abs(a["aux_loss"] - n["aux_loss"]) < 1e-17 and abs(a["z_loss"] - n["z_loss"]) < 1e-16
+
+
+def test_per_token_constant_noise_moves_only_the_partition_function():
+    """Softmax is shift invariant: noise c_t on every expert of token t leaves
+    p, the selection, alpha and aux unchanged and moves lse_t by c_t."""
+    r = rng(17)
+    x, Wr = r.normal(size=(12, 4)), r.normal(size=(6, 4))
+    c = r.normal(size=12)
+    a = O.moe_route(x, Wr, 3, 0.01, z_coef=1.0)
+    n = O.moe_route(x, Wr, 3, 0.01, logit_noise=np.repeat(c[:, None], 6, axis=1), z_coef=1.0)
+    np.testing.assert_allclose(n["probs"], a["probs"], rtol=1e-13)
+    assert np.array_equal(n["topk_idx"], a["topk_idx"])
+    np.testing.assert_allclose(n["lse"], a["lse"] + c, rtol=0, atol=1e-13)
+    assert abs(n["z_loss"] - float(np.mean((a["lse"] + c) ** 2))) < 1e-13
+
+
+def test_noise_changes_the_choice():
+    """A noise large enough on one expert takes top-1 for every token."""
+    r = rng(18)
+    x, Wr = r.normal(size=(8, 4)), r.normal(size=(5, 4)) * 0.1
+    noise = np.zeros((8, 5))
+    noise[:, 3] = 50.0
+    out = O.moe_route(x, Wr, 1, 0.0, logit_noise=noise)
+    assert (out["topk_idx"][:, 0] == 3).all()
