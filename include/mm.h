@@ -55,7 +55,12 @@ typedef enum {
   MM_ERR_UNSUPPORTED = 2,   /* valid but outside this build's limits          */
   MM_ERR_WORKSPACE = 3,     /* workspace null or smaller than required        */
   MM_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed              */
-  MM_ERR_TIMEOUT = 5        /* a device pipeline wait hit its time limit      */
+  MM_ERR_TIMEOUT = 5,       /* a device pipeline wait hit its time limit      */
+  MM_ERR_RANGE = 6          /* bf16 tensor-core prefill path: a value of h, or
+                               of Wd, is beyond the fp16 range (|v| >= 65520)
+                               of its intermediate copy; y may hold inf/NaN.
+                               Recorded on the device, reported by
+                               mm_check_status()                              */
 } mm_status;
 
 typedef enum { MM_DTYPE_F32 = 0, MM_DTYPE_BF16 = 1 } mm_dtype;
@@ -89,8 +94,11 @@ const char* mm_last_error(void);
  *   u = Wu x,  g = Wg x,  h = SiLU(g) ⊙ u,  y = Wd h,  SiLU(z) = z·sigmoid(z)
  *
  * x [T,H], Wg/Wu [I,H], Wd [H,I] in; y [T,H] out (overwritten).  g and u
- * never reach memory; h ([T,I]) lives in the workspace, in fp16 for bf16
- * inputs (|h| must stay below 65504) and fp32 for fp32 inputs.
+ * never reach memory; h ([T,I]) lives in the workspace, in fp16 on the bf16
+ * tensor-core path (with Wd converted to fp16) and fp32 for fp32 inputs.  A
+ * value of h or Wd at or beyond the fp16 range (|v| >= 65520) is recorded
+ * on the device and reported by mm_check_status() as MM_ERR_RANGE (the
+ * weight-streaming paths keep h in fp32 or as a bf16 pair and need no check).
  * Limits: T >= 0 (T = 0 enqueues nothing); H, I >= 1; bf16 tensor and
  * streaming paths need H and I to be multiples of 64.
  * ---------------------------------------------------------------------- */
@@ -184,6 +192,42 @@ int mm_moe_forward_ex(const void* x, const void* Wr,
                       void* y, int32_t* topk_idx, float* topk_w, float* aux_loss,
                       void* workspace, size_t workspace_bytes, void* stream, int path);
 
+/* ------------------------------------------------------------------------
+ * Router variants and saved router statistics   (p-chao.com "MiniMind 学习笔记
+ * 08：FeedForward 与 MoE" §10, table of large-scale MoE mechanisms: "router
+ * noise" and "z-loss"; §7: the router gradient flows through topk_weight)
+ *
+ * The table names the two mechanisms without formulas; this build reads
+ * them as:
+ *   router noise:  r_{t,e} = W_router x_t + logit_bias_e + noise_{t,e}, with
+ *                  the caller's draws noise [T, E] (scale included); the
+ *                  noisy logits feed softmax, top-k, alpha and aux;
+ *   z-loss:        z_loss = z_coef * (1/T) * sum_t lse_t^2,
+ *                  lse_t = log sum_e exp(r_{t,e}).
+ * router_probs / router_lse return p [T, E] and lse [T] as computed, the
+ * statistics a backward pass needs.
+ *
+ * Every pointer is nullable (NULL: off / not written); an options struct of
+ * zeros is the plain mm_moe_forward_ex with path AUTO.  Every path (tensor,
+ * streaming, SIMT) takes every option.  Pointers must be 4-byte aligned.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int path;                   /* mm_path of the FFN part (MM_PATH_AUTO = 0)        */
+  const float* logit_noise;   /* device fp32 [T, E]: router noise, or NULL         */
+  float z_coef;               /* z-loss coefficient                                */
+  float* z_loss;              /* device fp32 scalar out, or NULL (not computed)    */
+  float* router_probs;        /* device fp32 [T, E] out: softmax p, or NULL        */
+  float* router_lse;          /* device fp32 [T] out: logsumexp of the logits, or NULL */
+} mm_moe_options;
+
+int mm_moe_forward_opts(const void* x, const void* Wr,
+                        const void* const* Wg, const void* const* Wu, const void* const* Wd,
+                        int64_t T, int H, int I, int E, int k, float coef, int dtype,
+                        const float* logit_bias,
+                        void* y, int32_t* topk_idx, float* topk_w, float* aux_loss,
+                        void* workspace, size_t workspace_bytes, void* stream,
+                        const mm_moe_options* opts);
+
 /* Router half of the MoE forward only (logits, softmax, top-k, alpha, aux):
  * same arguments and meaning as mm_moe_forward without the experts and y.
  * expert_counts (device int32 [E], nullable) receives count_e. */
@@ -195,13 +239,23 @@ int mm_moe_route(const void* x, const void* Wr, int64_t T, int H, int E, int k,
                  int32_t* expert_counts,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same with router variants (opts->path is ignored). */
+int mm_moe_route_opts(const void* x, const void* Wr, int64_t T, int H, int E, int k,
+                      float coef, int dtype, const float* logit_bias,
+                      int32_t* topk_idx, float* topk_w, float* aux_loss,
+                      int32_t* expert_counts,
+                      void* workspace, size_t workspace_bytes, void* stream,
+                      const mm_moe_options* opts);
+
 /* ------------------------------------------------------------------------
  * Status
  * ---------------------------------------------------------------------- */
-/* Synchronises `stream`, reads and clears the device watchdog word kept at
+/* Synchronises `stream`, reads and clears the device status word kept at
  * the start of `workspace` (any workspace used by the calls above), and
  * returns MM_ERR_TIMEOUT if a kernel gave up on a pipeline wait since the
- * last check, MM_ERR_CUDA if the stream reported an error, else MM_OK. */
+ * last check, MM_ERR_RANGE if an fp16 intermediate overflowed (the first
+ * failure recorded wins), MM_ERR_CUDA if the stream reported an error, else
+ * MM_OK. */
 int mm_check_status(void* workspace, void* stream);
 
 /* Self-test of the watchdog: launches one block that waits on a barrier no

@@ -10,7 +10,8 @@ import os
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmm.so")
 
-MM_OK, MM_ERR_INVALID_ARG, MM_ERR_UNSUPPORTED, MM_ERR_WORKSPACE, MM_ERR_CUDA, MM_ERR_TIMEOUT = range(6)
+(MM_OK, MM_ERR_INVALID_ARG, MM_ERR_UNSUPPORTED, MM_ERR_WORKSPACE, MM_ERR_CUDA, MM_ERR_TIMEOUT,
+ MM_ERR_RANGE) = range(7)
 MM_DTYPE_F32, MM_DTYPE_BF16 = 0, 1
 MM_PATH_AUTO, MM_PATH_TENSOR, MM_PATH_STREAM, MM_PATH_SIMT, MM_PATH_STREAM_TC = 0, 1, 2, 3, 4
 MM_MAX_EXPERTS = 64
@@ -19,6 +20,16 @@ MM_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _vp, _i32, _i64, _f32, _sz = C.c_void_p, C.c_int, C.c_int64, C.c_float, C.c_size_t
 _pp = C.POINTER(C.c_void_p)
+
+
+class MoeOptions(C.Structure):
+    """mm_moe_options (include/mm.h), field for field."""
+    _fields_ = [("path", C.c_int), ("logit_noise", C.c_void_p), ("z_coef", C.c_float),
+                ("z_loss", C.c_void_p), ("router_probs", C.c_void_p),
+                ("router_lse", C.c_void_p)]
+
+
+_opt = C.POINTER(MoeOptions)
 
 # name -> (restype, argtypes); mirrors include/mm.h
 SIGNATURES = {
@@ -35,7 +46,11 @@ SIGNATURES = {
                               _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "mm_moe_forward_ex": (_i32, [_vp, _vp, _pp, _pp, _pp, _i64, _i32, _i32, _i32, _i32, _f32,
                                  _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _i32]),
+    "mm_moe_forward_opts": (_i32, [_vp, _vp, _pp, _pp, _pp, _i64, _i32, _i32, _i32, _i32, _f32,
+                                   _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _opt]),
     "mm_moe_route_workspace_bytes": (_sz, [_i64, _i32, _i32]),
+    "mm_moe_route_opts": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _f32, _i32, _vp, _vp, _vp, _vp,
+                                 _vp, _vp, _sz, _vp, _opt]),
     "mm_moe_route": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _f32, _i32, _vp, _vp, _vp, _vp,
                             _vp, _vp, _sz, _vp]),
     "mm_check_status": (_i32, [_vp, _vp]),

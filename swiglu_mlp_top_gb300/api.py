@@ -5,6 +5,7 @@ computation runs in the CUDA kernels of libmm.so.  Nothing here computes.
 """
 from __future__ import annotations
 
+import ctypes as C
 from typing import Optional, Sequence
 
 import torch
@@ -89,15 +90,40 @@ def swiglu_ffn_noalloc(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: 
     return out
 
 
+def _router_options(T: int, E: int, dev, path: str, logit_noise, z_coef, stats):
+    """mm_moe_options for the router variants; fills `stats` (a dict) with the
+    output tensors it asks for: z_loss [], probs [T, E], lse [T] (fp32)."""
+    o = L.MoeOptions()
+    o.path = _PATHS[path]
+    if logit_noise is not None:
+        if tuple(logit_noise.shape) != (T, E):
+            raise ValueError(f"logit_noise must be [{T}, {E}]")
+        o.logit_noise = _dev(logit_noise, "logit_noise", torch.float32)
+    o.z_coef = float(z_coef or 0.0)
+    if stats is not None:
+        shapes = {"z_loss": (), "probs": (T, E), "lse": (T,)}
+        for name, shape in shapes.items():
+            if stats.get(name) is None:
+                stats[name] = torch.empty(shape, dtype=torch.float32, device=dev)
+        o.z_loss = _dev(stats["z_loss"], "z_loss", torch.float32)
+        o.router_probs = _dev(stats["probs"], "probs", torch.float32)
+        o.router_lse = _dev(stats["lse"], "lse", torch.float32)
+    return o
+
+
 def moe_forward(x: torch.Tensor, Wr: torch.Tensor, Wg: Sequence[torch.Tensor],
                 Wu: Sequence[torch.Tensor], Wd: Sequence[torch.Tensor], k: int, coef: float, *,
                 logit_bias: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
                 topk_idx: Optional[torch.Tensor] = None, topk_w: Optional[torch.Tensor] = None,
                 aux_loss: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                path: str = "auto", stream=None):
-    """Top-k MoE forward (mm_moe_forward).
+                path: str = "auto", stream=None, logit_noise: Optional[torch.Tensor] = None,
+                z_coef: float = 0.0, stats: Optional[dict] = None):
+    """Top-k MoE forward (mm_moe_forward; mm_moe_forward_opts when router
+    noise, z-loss or router statistics are asked for).
 
     Returns (y [T,H], topk_idx [T,k] int32, topk_w [T,k] fp32, aux_loss [] fp32).
+    With a dict `stats`, it also receives z_loss [] (z_coef * mean_t lse_t^2),
+    probs [T, E] and lse [T] (fp32 device tensors).
     """
     lib = L.load()
     T, H = x.shape
@@ -116,12 +142,16 @@ def moe_forward(x: torch.Tensor, Wr: torch.Tensor, Wg: Sequence[torch.Tensor],
     pu, au = L.ptr_array([_dev(w, "Wu", x.dtype) for w in Wu])
     pd, ad = L.ptr_array([_dev(w, "Wd", x.dtype) for w in Wd])
     bias_ptr = None if logit_bias is None else _dev(logit_bias, "logit_bias", torch.float32)
-    rc = lib.mm_moe_forward_ex(
-        _dev(x, "x"), _dev(Wr, "Wr", x.dtype), pg, pu, pd, T, H, I, E, k, float(coef), dt,
-        bias_ptr, _dev(out, "out", x.dtype), _dev(topk_idx, "topk_idx", torch.int32),
-        _dev(topk_w, "topk_w", torch.float32), _dev(aux_loss, "aux_loss", torch.float32),
-        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
-        _stream(stream), _PATHS[path])
+    args = (_dev(x, "x"), _dev(Wr, "Wr", x.dtype), pg, pu, pd, T, H, I, E, k, float(coef), dt,
+            bias_ptr, _dev(out, "out", x.dtype), _dev(topk_idx, "topk_idx", torch.int32),
+            _dev(topk_w, "topk_w", torch.float32), _dev(aux_loss, "aux_loss", torch.float32),
+            _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+            _stream(stream))
+    if logit_noise is None and not z_coef and stats is None:
+        rc = lib.mm_moe_forward_ex(*args, _PATHS[path])
+    else:
+        o = _router_options(T, E, dev, path, logit_noise, z_coef, stats)
+        rc = lib.mm_moe_forward_opts(*args, C.byref(o))
     del ag, au, ad
     L.check(rc, "mm_moe_forward")
     return out, topk_idx, topk_w, aux_loss
@@ -129,8 +159,10 @@ def moe_forward(x: torch.Tensor, Wr: torch.Tensor, Wg: Sequence[torch.Tensor],
 
 def moe_route(x: torch.Tensor, Wr: torch.Tensor, k: int, coef: float, *,
               logit_bias: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-              stream=None):
-    """Router only (mm_moe_route): (topk_idx, topk_w, aux_loss, expert_counts)."""
+              stream=None, logit_noise: Optional[torch.Tensor] = None, z_coef: float = 0.0,
+              stats: Optional[dict] = None):
+    """Router only (mm_moe_route / mm_moe_route_opts): (topk_idx, topk_w,
+    aux_loss, expert_counts); router variants and `stats` as moe_forward."""
     lib = L.load()
     T, H = x.shape
     E = Wr.shape[0]
@@ -144,10 +176,15 @@ def moe_route(x: torch.Tensor, Wr: torch.Tensor, k: int, coef: float, *,
     if workspace is None:
         workspace = new_workspace(need, dev)
     bias_ptr = None if logit_bias is None else _dev(logit_bias, "logit_bias", torch.float32)
-    rc = lib.mm_moe_route(_dev(x, "x"), _dev(Wr, "Wr", x.dtype), T, H, E, k, float(coef), dt,
-                          bias_ptr, idx.data_ptr(), w.data_ptr(), aux.data_ptr(),
-                          counts.data_ptr(), _dev(workspace, "workspace"),
-                          workspace.numel() * workspace.element_size(), _stream(stream))
+    args = (_dev(x, "x"), _dev(Wr, "Wr", x.dtype), T, H, E, k, float(coef), dt,
+            bias_ptr, idx.data_ptr(), w.data_ptr(), aux.data_ptr(),
+            counts.data_ptr(), _dev(workspace, "workspace"),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+    if logit_noise is None and not z_coef and stats is None:
+        rc = lib.mm_moe_route(*args)
+    else:
+        o = _router_options(T, E, dev, "auto", logit_noise, z_coef, stats)
+        rc = lib.mm_moe_route_opts(*args, C.byref(o))
     L.check(rc, "mm_moe_route")
     return idx, w, aux, counts
 

@@ -29,7 +29,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 // ----------------------------------------------------------------- layouts
 struct MoeLayout {
-  size_t offsets, counts, blk_cnt, blk_prob, perm, xp, h, acc32, wd16, total;
+  size_t offsets, counts, blk_cnt, blk_prob, blk_z, perm, xp, h, acc32, wd16, total;
 };
 
 // h is stored in fp16 for bf16 inputs (see gemm_tc.cu) and in fp32 for fp32.
@@ -50,6 +50,7 @@ MoeLayout moe_layout(int64_t T, int H, int I, int E, int k, int dtype) {
   L.counts = off;   off += align_up(4 * static_cast<size_t>(E));
   L.blk_cnt = off;  off += align_up(4 * nblk * G);
   L.blk_prob = off; off += align_up(4 * nblk * E);
+  L.blk_z = off;    off += align_up(4 * nblk);
   L.perm = off;     off += align_up(4 * rows);
   L.xp = off;       off += align_up(es * rows * H);
   L.h = off;        off += align_up(h_bytes(dtype) * rows * I);
@@ -62,7 +63,7 @@ MoeLayout moe_layout(int64_t T, int H, int I, int E, int k, int dtype) {
 }
 
 struct RouteLayout {
-  size_t blk_cnt, blk_prob, total;
+  size_t blk_cnt, blk_prob, blk_z, total;
 };
 RouteLayout route_layout(int64_t T, int E, int k) {
   RouteLayout L;
@@ -70,6 +71,7 @@ RouteLayout route_layout(int64_t T, int E, int k) {
   size_t off = sizeof(WsHeader);
   L.blk_cnt = off;  off += align_up(4 * nblk * static_cast<size_t>(k) * E);
   L.blk_prob = off; off += align_up(4 * nblk * E);
+  L.blk_z = off;    off += align_up(4 * nblk);
   L.total = off;
   return L;
 }
@@ -230,6 +232,7 @@ const char* mm_status_string(int status) {
     case MM_ERR_WORKSPACE: return "MM_ERR_WORKSPACE";
     case MM_ERR_CUDA: return "MM_ERR_CUDA";
     case MM_ERR_TIMEOUT: return "MM_ERR_TIMEOUT";
+    case MM_ERR_RANGE: return "MM_ERR_RANGE";
     default: return "MM_ERR_UNKNOWN";
   }
 }
@@ -339,11 +342,29 @@ static int check_route_args(const void* x, const void* Wr, int64_t T, int H, int
   return MM_OK;
 }
 
-int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
-                      const void* const* Wu, const void* const* Wd, int64_t T, int H, int I, int E,
-                      int k, float coef, int dtype, const float* logit_bias, void* y,
-                      int32_t* topk_idx, float* topk_w, float* aux_loss, void* workspace,
-                      size_t workspace_bytes, void* stream, int path) {
+// Router variants of an options struct as the kernels take them (the
+// per-block z sums live in the workspace at blk_z).
+static int router_variant(const mm_moe_options* o, void* blk_z, RouterVariant* rv) {
+  memset(rv, 0, sizeof(*rv));
+  if (o == nullptr) return MM_OK;
+  auto a4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  if (!a4(o->logit_noise) || !a4(o->z_loss) || !a4(o->router_probs) || !a4(o->router_lse))
+    return MM_ERR_INVALID_ARG;
+  rv->noise = o->logit_noise;
+  rv->z_coef = o->z_coef;
+  rv->z_loss = o->z_loss;
+  rv->probs = o->router_probs;
+  rv->lse = o->router_lse;
+  rv->blk_z = o->z_loss != nullptr ? static_cast<float*>(blk_z) : nullptr;
+  return MM_OK;
+}
+
+static int moe_forward_impl(const void* x, const void* Wr, const void* const* Wg,
+                            const void* const* Wu, const void* const* Wd, int64_t T, int H, int I,
+                            int E, int k, float coef, int dtype, const float* logit_bias, void* y,
+                            int32_t* topk_idx, float* topk_w, float* aux_loss, void* workspace,
+                            size_t workspace_bytes, void* stream, const mm_moe_options* opts) {
+  const int path = opts ? opts->path : MM_PATH_AUTO;
   int rc = check_route_args(x, Wr, T, H, E, k, dtype, logit_bias, topk_idx, topk_w, aux_loss);
   if (rc != MM_OK) return rc;
   if (I < 1) return MM_ERR_INVALID_ARG;
@@ -368,12 +389,15 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
     // decode-sized: routing, experts and combine in one streaming kernel,
     // with its scratch after the header
     void* scratch = ws_at(workspace, sizeof(WsHeader));
+    RouterVariant rv;
+    rc = router_variant(opts, nullptr, &rv);
+    if (rc != MM_OK) return rc;
     cudaError_t e = counted_launch(MM_KERNEL_DECODE, st, [&] {
       if (p == MM_PATH_STREAM)
         return launch_decode_ffn(x, Wr, logit_bias, Wg, Wu, Wd, static_cast<int>(T), H, I, E, k,
-                                 coef, topk_idx, topk_w, aux_loss, scratch, y, hdr, st);
+                                 coef, topk_idx, topk_w, aux_loss, scratch, y, hdr, st, &rv);
       return launch_decode_tc(x, Wr, logit_bias, Wg, Wu, Wd, static_cast<int>(T), H, I, E, k,
-                              coef, topk_idx, topk_w, aux_loss, scratch, y, hdr, st);
+                              coef, topk_idx, topk_w, aux_loss, scratch, y, hdr, st, &rv);
     });
     if (e != cudaSuccess) return cuda_fail(e, "decode ffn");
     return MM_OK;
@@ -394,13 +418,16 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
   char* wd16 = ws_at(workspace, L.wd16);
   if (p == MM_PATH_TENSOR)
     for (int q = 0; q < E; ++q) wd16p[q] = wd16 + static_cast<size_t>(q) * H * I * 2;
-  const RouteOut ro{nullptr, nullptr, nullptr, nullptr, coef, 0};
+  RouterVariant rv;
+  rc = router_variant(opts, ws_at(workspace, L.blk_z), &rv);
+  if (rc != MM_OK) return rc;
+  const RouteOut ro{nullptr, nullptr, nullptr, nullptr, coef, 0, rv};
   cudaError_t e = counted_launch(MM_KERNEL_ROUTER, st, [&] {
     return launch_router(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w, blk_cnt, blk_prob,
                          ro, hdr, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "router");
-  const DispatchOut dout{offsets, counts, aux_loss, coef, hdr};
+  const DispatchOut dout{offsets, counts, aux_loss, coef, hdr, rv};
   e = counted_launch(MM_KERNEL_DISPATCH, st, [&] {
     return launch_dispatch(dtype, x, T, H, E, k, topk_idx, blk_cnt, blk_prob, dout, perm, xp, st);
   });
@@ -439,6 +466,27 @@ int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
   return MM_OK;
 }
 
+int mm_moe_forward_ex(const void* x, const void* Wr, const void* const* Wg,
+                      const void* const* Wu, const void* const* Wd, int64_t T, int H, int I, int E,
+                      int k, float coef, int dtype, const float* logit_bias, void* y,
+                      int32_t* topk_idx, float* topk_w, float* aux_loss, void* workspace,
+                      size_t workspace_bytes, void* stream, int path) {
+  mm_moe_options o;
+  memset(&o, 0, sizeof(o));
+  o.path = path;
+  return moe_forward_impl(x, Wr, Wg, Wu, Wd, T, H, I, E, k, coef, dtype, logit_bias, y, topk_idx,
+                          topk_w, aux_loss, workspace, workspace_bytes, stream, &o);
+}
+
+int mm_moe_forward_opts(const void* x, const void* Wr, const void* const* Wg,
+                        const void* const* Wu, const void* const* Wd, int64_t T, int H, int I,
+                        int E, int k, float coef, int dtype, const float* logit_bias, void* y,
+                        int32_t* topk_idx, float* topk_w, float* aux_loss, void* workspace,
+                        size_t workspace_bytes, void* stream, const mm_moe_options* opts) {
+  return moe_forward_impl(x, Wr, Wg, Wu, Wd, T, H, I, E, k, coef, dtype, logit_bias, y, topk_idx,
+                          topk_w, aux_loss, workspace, workspace_bytes, stream, opts);
+}
+
 int mm_moe_forward(const void* x, const void* Wr, const void* const* Wg, const void* const* Wu,
                    const void* const* Wd, int64_t T, int H, int I, int E, int k, float coef,
                    int dtype, const float* logit_bias, void* y, int32_t* topk_idx, float* topk_w,
@@ -456,6 +504,14 @@ int mm_moe_route(const void* x, const void* Wr, int64_t T, int H, int E, int k, 
                  int dtype, const float* logit_bias, int32_t* topk_idx, float* topk_w,
                  float* aux_loss, int32_t* expert_counts, void* workspace, size_t workspace_bytes,
                  void* stream) {
+  return mm_moe_route_opts(x, Wr, T, H, E, k, coef, dtype, logit_bias, topk_idx, topk_w, aux_loss,
+                           expert_counts, workspace, workspace_bytes, stream, nullptr);
+}
+
+int mm_moe_route_opts(const void* x, const void* Wr, int64_t T, int H, int E, int k, float coef,
+                      int dtype, const float* logit_bias, int32_t* topk_idx, float* topk_w,
+                      float* aux_loss, int32_t* expert_counts, void* workspace,
+                      size_t workspace_bytes, void* stream, const mm_moe_options* opts) {
   int rc = check_route_args(x, Wr, T, H, E, k, dtype, logit_bias, topk_idx, topk_w, aux_loss);
   if (rc != MM_OK) return rc;
   if (expert_counts && (reinterpret_cast<uintptr_t>(expert_counts) & 3u)) return MM_ERR_INVALID_ARG;
@@ -466,7 +522,10 @@ int mm_moe_route(const void* x, const void* Wr, int64_t T, int H, int E, int k, 
   int32_t* blk_cnt = reinterpret_cast<int32_t*>(ws_at(workspace, L.blk_cnt));
   float* blk_prob = reinterpret_cast<float*>(ws_at(workspace, L.blk_prob));
   WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
-  const RouteOut ro{nullptr, nullptr, expert_counts, aux_loss, coef, 1};
+  RouterVariant rv;
+  rc = router_variant(opts, ws_at(workspace, L.blk_z), &rv);
+  if (rc != MM_OK) return rc;
+  const RouteOut ro{nullptr, nullptr, expert_counts, aux_loss, coef, 1, rv};
   cudaError_t e = counted_launch(MM_KERNEL_ROUTER, st, [&] {
     return launch_router(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w, blk_cnt, blk_prob,
                          ro, hdr, st);

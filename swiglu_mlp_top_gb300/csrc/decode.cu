@@ -55,6 +55,7 @@ struct DecodeArgs {
   void* y;                  // [T, H] bf16
   WsHeader* hdr;
   DecPlan plan;
+  RouterVariant rv;         // router noise, z-loss, saved statistics (MoE)
 };
 
 
@@ -210,7 +211,7 @@ __device__ void decode_route(const DecodeArgs& A, const float* xs, const __nv_bf
     }
   }
   __syncthreads();
-  route_softmax_topk_warp(R, A.T, E, k, bias, warp, kDecWarps, lane);
+  route_softmax_topk_warp(R, A.T, E, k, bias, warp, kDecWarps, lane, A.rv.noise);
   __syncthreads();
   if (warp == 0) route_group(R, A.T * k, E, lane);
   __syncthreads();
@@ -321,7 +322,8 @@ decode_ffn_kernel(const DecodeArgs A) {
     my_up = blockIdx.x < up_units ? (up_units - blockIdx.x + G - 1) / G : 0;
     my_wd = my_dn * n_touched;
     if (blockIdx.x == 0)
-      route_outputs(R, A.T, A.E, A.coef, A.topk_idx, A.topk_w, A.aux_loss, tid, kDecThreads, 1);
+      route_outputs(R, A.T, A.E, A.coef, A.topk_idx, A.topk_w, A.aux_loss, tid, kDecThreads, 1,
+                    &A.rv);
     __syncthreads();                          // Wr in the ring is no longer read
     if (tid == 0) {
       fence_proxy_async_smem();
@@ -504,9 +506,10 @@ cudaError_t launch_decode_ffn(const void* x, const void* Wr, const float* bias,
                               const void* const* Wg, const void* const* Wu, const void* const* Wd,
                               int T, int H, int I, int E, int k, float coef, int32_t* topk_idx,
                               float* topk_w, float* aux_loss, void* hbuf, void* y, WsHeader* hdr,
-                              cudaStream_t st) {
+                              cudaStream_t st, const RouterVariant* rv) {
   DecodeArgs A;
   memset(&A, 0, sizeof(A));
+  if (rv != nullptr) A.rv = *rv;
   A.x = x;
   A.Wr = Wr;
   A.bias = bias;

@@ -97,6 +97,7 @@ struct DtArgs {
   uint32_t stage_bytes;           // 32 KiB of weight tiles + one x tile
   uint32_t hstage_off;            // Hp staging tile [2][Np][128] bf16 (epilogue -> TMA store)
   uint32_t alpha_off;             // alpha table [nt_max][Np] fp32
+  RouterVariant rv;               // router noise, z-loss, saved statistics (MoE)
 };
 
 // Work plan derived from the routing; identical in every thread of the grid.
@@ -290,7 +291,7 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
   // ------------------------------------------------------------ routing
   if (ok && !spec) {
     if (moe) {
-      route_softmax_topk_warp(R, T, A.E, A.k, s_bias, warp, kDtThreads / 32, lane);
+      route_softmax_topk_warp(R, T, A.E, A.k, s_bias, warp, kDtThreads / 32, lane, A.rv.noise);
       __syncthreads();
       if (warp == 0) route_group(R, T * A.k, A.E, lane);
     } else {
@@ -304,7 +305,8 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
       alpha[R.slot_of[R.sel_e[a]] * Np + t] = R.sel_a[a];
     }
     if (moe && cta == 0)
-      route_outputs(R, T, A.E, A.coef, A.topk_idx, A.topk_w, A.aux_loss, tid, kDtThreads, 2);
+      route_outputs(R, T, A.E, A.coef, A.topk_idx, A.topk_w, A.aux_loss, tid, kDtThreads, 2,
+                    &A.rv);
     __syncthreads();
   }
 
@@ -481,7 +483,7 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
           ok = epi_sync_and(r);
           if (ok) {
             const int etid = tid - 64, en = kDtEpiWarps * 32;
-            route_softmax_topk_warp(R, T, A.E, A.k, s_bias, etid >> 5, en >> 5, lane);
+            route_softmax_topk_warp(R, T, A.E, A.k, s_bias, etid >> 5, en >> 5, lane, A.rv.noise);
             for (int q = etid; q < A.E * Np; q += en) alpha[q] = 0.f;
             epi_sync();
             if (warp == 2) route_group(R, T * A.k, A.E, lane);
@@ -496,7 +498,8 @@ decode_tc_kernel(const __grid_constant__ DtMaps<MAXW> M, const DtArgs A) {
               __threadfence_block();
               s_routed = 1;
             }
-            if (cta == 0) route_outputs(R, T, A.E, A.coef, A.topk_idx, A.topk_w, A.aux_loss, etid, en, 0);
+            if (cta == 0)
+              route_outputs(R, T, A.E, A.coef, A.topk_idx, A.topk_w, A.aux_loss, etid, en, 0, &A.rv);
           }
         }
         int jj = 0;                                   // units kept
@@ -1115,12 +1118,13 @@ cudaError_t launch_decode_tc(const void* x, const void* Wr, const float* bias,
                              const void* const* Wg, const void* const* Wu, const void* const* Wd,
                              int T, int H, int I, int E, int k, float coef, int32_t* topk_idx,
                              float* topk_w, float* aux_loss, void* scratch, void* y,
-                             WsHeader* hdr, cudaStream_t st) {
+                             WsHeader* hdr, cudaStream_t st, const RouterVariant* rv) {
   const bool moe = Wr != nullptr;
   DtLayout L;
   if (!dt_layout(T, H, I, moe ? E : 1, moe ? k : 1, L)) return cudaErrorInvalidValue;
   DtArgs A;
   memset(&A, 0, sizeof(A));
+  if (rv != nullptr && moe) A.rv = *rv;
   A.T = T; A.Np = L.Np; A.H = H; A.I = I;
   A.E = moe ? E : 1; A.k = moe ? k : 1; A.moe = moe ? 1 : 0; A.coef = coef; A.bias = bias;
   A.topk_idx = topk_idx; A.topk_w = topk_w; A.aux_loss = aux_loss;

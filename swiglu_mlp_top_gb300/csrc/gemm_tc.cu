@@ -31,6 +31,8 @@ namespace mm {
 
 // ------------------------------------------------------------------ geometry
 constexpr int kOpUp = 0, kOpDown = 1;
+// Smallest magnitude that rounds to infinity in fp16 (65504 + half an ulp).
+constexpr float kF16Overflow = 65520.0f;
 constexpr int kPairM = 2 * kTcBM;                        // rows per tile pair
 constexpr int kN = 256;                                  // UMMA N (both ops)
 // The operand ring holds six k-blocks of A and B (16 KiB each per CTA),
@@ -122,10 +124,13 @@ __device__ __forceinline__ void build_schedule(const GroupRows& gr, int n_tiles,
 // all in the group writes each piece with one TMA tensor store from its
 // swizzled staging tile; a warp holding a group's ragged end stores its
 // valid rows directly (the rows past the end belong to the next group).
-__device__ __forceinline__ void epilogue_up(uint32_t tb, const TileInfo& ti, int I, __half* hout,
+// Returns true when some value of the lane's pieces is not representable in
+// fp16 (|h| >= 65520 rounds to infinity; a NaN or an infinite g or u).
+__device__ __forceinline__ bool epilogue_up(uint32_t tb, const TileInfo& ti, int I, __half* hout,
                                             int row, int half, uint8_t* wstage,
                                             const CUtensorMap* hmap) {
   const int lane = row & 31;
+  bool out_of_range = false;
   const bool valid = row < ti.rows;
   const bool full_warp = (row | 31) < ti.rows;   // warp-uniform
   const int col0 = ti.n0 + half * 64;
@@ -145,6 +150,8 @@ __device__ __forceinline__ void epilogue_up(uint32_t tb, const TileInfo& ti, int
       const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
       const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
       pk[j] = pack_f16x2(h0, h1);
+      // false for NaN as well
+      out_of_range |= !(fabsf(h0) < kF16Overflow) | !(fabsf(h1) < kF16Overflow);
     }
     if (col0 + c * 32 >= I) continue;            // piece past the last column
     if (full_warp) {
@@ -168,6 +175,7 @@ __device__ __forceinline__ void epilogue_up(uint32_t tb, const TileInfo& ti, int
       for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
     }
   }
+  return out_of_range && valid;
 }
 
 // down: 128 y columns (half `half` of the tile's 256) of the warp's 32 rows,
@@ -356,9 +364,10 @@ __device__ __forceinline__ void cv_load(const WdConvert& cv, int64_t v, int64_t 
   }
 }
 
-__device__ __forceinline__ void cv_store(const WdConvert& cv, int64_t v, int64_t v1, int t,
+__device__ __forceinline__ bool cv_store(const WdConvert& cv, int64_t v, int64_t v1, int t,
                                          const uint4 (&raw)[4]) {
   uint4* dst = reinterpret_cast<uint4*>(cv.dst);
+  bool out_of_range = false;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int64_t u = v + t + j * kCvStride;
@@ -370,19 +379,31 @@ __device__ __forceinline__ void cv_store(const WdConvert& cv, int64_t v, int64_t
       for (int q = 0; q < 4; ++q) {
         const float2 f = __bfloat1622float2(b[q]);
         o[q] = pack_f16x2(f.x, f.y);
+        out_of_range |= !(fabsf(f.x) < kF16Overflow) | !(fabsf(f.y) < kF16Overflow);
       }
       __stcg(dst + u, out);
     }
   }
+  return out_of_range;
 }
 
 // the batches of [v0, v1) from v onwards, one after the other
-__device__ __forceinline__ void cv_rest(const WdConvert& cv, int64_t v, int64_t v1, int t) {
+__device__ __forceinline__ bool cv_rest(const WdConvert& cv, int64_t v, int64_t v1, int t) {
+  bool out_of_range = false;
 #pragma unroll 1
   for (; v < v1; v += kCvBatch) {
     uint4 raw[4];
     cv_load(cv, v, v1, t, raw);
-    cv_store(cv, v, v1, t, raw);
+    out_of_range |= cv_store(cv, v, v1, t, raw);
+  }
+  return out_of_range;
+}
+
+// Records MM_ERR_RANGE in the workspace header (first failure wins) when any
+// lane of the warp saw a value that fp16 cannot hold.
+__device__ __forceinline__ void report_range(WsHeader* hdr, bool bad) {
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0 && hdr != nullptr) {
+    if (atomicCAS(&hdr->status, 0u, kStatusRange) == 0u) hdr->where = 100;
   }
 }
 
@@ -437,6 +458,11 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
     mbar_init(drained, 1);
     fence_mbar_init();
     s_abort = 0;
+    // The group offsets of a grouped problem are written by the previous
+    // kernel (the dispatch), which lets this one launch before it writes
+    // them: with dep_mainloop the schedule is built only once that kernel
+    // has completed.  (The barrier set-up above still overlaps it.)
+    if (dep_mainloop && g.offsets != nullptr) asm volatile("griddepcontrol.wait;" ::: "memory");
     build_schedule(g, n_tiles, s_off, s_tstart);
   }
   if (warp == kWarpProducer && lane == 0) tma_prefetch_desc(&P.a);
@@ -555,13 +581,14 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
     // any earlier reader of the copy) has finished first.
     int64_t cv0 = 0, cv1 = 0;
     int n_local = 0;
+    bool range_bad = false;     // gate/up: an h or Wd value beyond the fp16 range
     if (OP == kOpUp && cv.n_mat > 0) {
       asm volatile("griddepcontrol.wait;" ::: "memory");
       const int64_t nv = cv.nvec * cv.n_mat;
       cv0 = nv * blockIdx.x / gridDim.x;
       cv1 = nv * (blockIdx.x + 1) / gridDim.x;
       n_local = cluster < total ? (total - cluster + n_clusters - 1) / n_clusters : 0;
-      if (n_local == 0) cv_rest(cv, cv0, cv1, threadIdx.x);
+      if (n_local == 0) range_bad |= cv_rest(cv, cv0, cv1, threadIdx.x);
     }
     int local = 0;
     for (int tile = cluster; tile < total; tile += n_clusters, ++local) {
@@ -599,7 +626,7 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
       tc_fence_after();
       const uint32_t tb = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * kAccStride;
       if constexpr (OP == kOpUp)
-        epilogue_up(tb, ti, NCOLS, hout, row, half, wstage, &P.out);
+        range_bad |= epilogue_up(tb, ti, NCOLS, hout, row, half, wstage, &P.out);
       else if (ep.perm == nullptr && ep.mode == kCombineStore && (row | 31) < ti.rows)
         epilogue_down_dense<kHC>(tb, ti, NCOLS, half, lane, ti.row0 + (row & ~31), wstage, &P.out);
       else
@@ -608,10 +635,11 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc ? te1 : te0);
       if (OP == kOpUp && ca < cb) {
-        cv_store(cv, ca, cb, threadIdx.x, craw);
-        cv_rest(cv, ca + kCvBatch, cb, threadIdx.x);
+        range_bad |= cv_store(cv, ca, cb, threadIdx.x, craw);
+        range_bad |= cv_rest(cv, ca + kCvBatch, cb, threadIdx.x);
       }
     }
+    if constexpr (OP == kOpUp) report_range(hdr, range_bad);
     bulk_wait_all();   // this warp's tensor stores have landed
   }
 

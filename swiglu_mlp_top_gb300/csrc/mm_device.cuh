@@ -22,6 +22,7 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
 constexpr unsigned kStatusTimeout = 5u;      // == MM_ERR_TIMEOUT
+constexpr unsigned kStatusRange = 6u;        // == MM_ERR_RANGE
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s per wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -72,6 +72,21 @@ struct WdConvert {
   int n_mat;
 };
 
+// Router variants and saved router statistics, all optional (null / 0:
+// off).  noise: router noise, added to each token's logits after the bias;
+// z-loss = z_coef * (1/T) sum_t lse_t^2 with lse_t the logsumexp of the
+// token's logits; probs / lse: the softmax probabilities [T, E] and lse [T]
+// as computed, for a backward pass.  blk_z is workspace: per router block,
+// the sum of its tokens' lse^2, added in a fixed order by the finaliser.
+struct RouterVariant {
+  const float* noise;    // [T, E] fp32
+  float z_coef;
+  float* z_loss;         // fp32 scalar
+  float* probs;          // [T, E] fp32
+  float* lse;            // [T] fp32
+  float* blk_z;          // [nblk] fp32 (prefill router)
+};
+
 // Router grid (routing.cu): per 64-token block logits, softmax, top-k, alpha
 // and partial counts / probability sums; with do_scan the block that
 // finishes last runs the scan (counts, aux loss; its counter lives in the
@@ -83,6 +98,7 @@ struct RouteOut {
   float* aux_loss;       // scalar or null
   float coef;
   int do_scan;           // 0: the dispatch kernel derives bases, offsets, counts, aux
+  RouterVariant rv;
 };
 struct RouteExtras {
   int32_t* blk_base;
@@ -94,6 +110,7 @@ struct RouteExtras {
   int stage_x;           // x rows staged in shared memory at byte x_off
   uint32_t x_off;
   int do_scan;
+  RouterVariant rv;
 };
 cudaError_t launch_router(int dtype, const void* x, const void* Wr, const float* bias, int64_t T,
                           int H, int E, int k, int32_t* topk_idx, float* topk_w, int32_t* blk_cnt,
@@ -107,6 +124,7 @@ struct DispatchOut {
   float* aux_loss;
   float coef;
   WsHeader* hdr;
+  RouterVariant rv;      // block 0 finalises the z-loss from rv.blk_z
 };
 cudaError_t launch_dispatch(int dtype, const void* x, int64_t T, int H, int E, int k,
                             const int32_t* topk_idx, const int32_t* blk_cnt, const float* blk_prob,
@@ -142,7 +160,7 @@ cudaError_t launch_decode_ffn(const void* x, const void* Wr, const float* bias,
                               const void* const* Wg, const void* const* Wu, const void* const* Wd,
                               int T, int H, int I, int E, int k, float coef, int32_t* topk_idx,
                               float* topk_w, float* aux_loss, void* hbuf, void* y, WsHeader* hdr,
-                              cudaStream_t st);
+                              cudaStream_t st, const RouterVariant* rv = nullptr);
 
 // Decode-sized forward on the tensor cores (T <= kDecodeTcMaxT, bf16): one
 // cooperative kernel; weights are the UMMA M operand (128 rows per tile), the
@@ -153,7 +171,7 @@ cudaError_t launch_decode_tc(const void* x, const void* Wr, const float* bias,
                              const void* const* Wg, const void* const* Wu, const void* const* Wd,
                              int T, int H, int I, int E, int k, float coef, int32_t* topk_idx,
                              float* topk_w, float* aux_loss, void* scratch, void* y,
-                             WsHeader* hdr, cudaStream_t st);
+                             WsHeader* hdr, cudaStream_t st, const RouterVariant* rv = nullptr);
 
 // Dense FFN on the tensor cores with the tokens as the M operand (T <=
 // kDecodeSwMaxT, bf16; decode_sw.cu): one cooperative kernel, units of 64

@@ -22,6 +22,7 @@ struct SmallRoute {
   int rank[MAXT * MM_MAX_TOPK];      // its place among its expert's assignments
   int by_e[MAXT * MM_MAX_TOPK];      // assignments grouped by expert, in token order
   float prob[MAXT][MM_MAX_EXPERTS + 1];  // logits, then probabilities (row padded)
+  float lse[MAXT];                       // logsumexp of each token's logits
 };
 
 __device__ __forceinline__ float warp_allsum_f(float v) {
@@ -30,70 +31,36 @@ __device__ __forceinline__ float warp_allsum_f(float v) {
   return v;
 }
 
-// One thread per token t (t = first, first + stride, ...): R.prob[t][:]
-// holds the logits on entry and the probabilities on exit.  Softmax with the
-// maximum subtracted (fast exponential, one reciprocal); then k arg-max passes in expert order with a strict
-// comparison, so that of equal probabilities the lower expert index is taken
-// first; alpha = p / (sum_S p + 1e-20).
-template <int MAXT>
-__device__ __forceinline__ void route_softmax_topk(SmallRoute<MAXT>& R, int T, int E, int k,
-                                                   const float* bias, int first, int stride) {
-  for (int t = first; t < T; t += stride) {
-    float* row = R.prob[t];
-    float m = -INFINITY;
-    for (int e = 0; e < E; ++e) {
-      const float r = row[e] + bias[e];
-      row[e] = r;
-      m = fmaxf(m, r);
-    }
-    float z = 0.f;
-    for (int e = 0; e < E; ++e) {
-      const float x = __expf(row[e] - m);
-      row[e] = x;
-      z += x;
-    }
-    const float rz = 1.0f / z;
-    for (int e = 0; e < E; ++e) row[e] *= rz;
-    uint64_t taken = 0;
-    float sel_sum = 0.f;
-    for (int s = 0; s < k; ++s) {
-      float bp = -1.f;
-      int be = 0;
-      for (int e = 0; e < E; ++e) {
-        const float p = row[e];
-        if (!((taken >> e) & 1ull) && p > bp) { bp = p; be = e; }
-      }
-      taken |= 1ull << be;
-      sel_sum += bp;
-      R.sel_e[t * k + s] = be;
-      R.sel_a[t * k + s] = bp;
-    }
-    const float inv = sel_sum + 1e-20f;
-    for (int s = 0; s < k; ++s) R.sel_a[t * k + s] = R.sel_a[t * k + s] / inv;
-  }
-}
-
-// The same on one warp per token (t = first_warp, first_warp + nwarps, ...):
-// lane l holds experts l and l + 32 in registers; the maximum and the sum of
-// the exponentials are warp reductions, and each of the k selections is a
-// warp arg-max (larger probability, else lower expert index).  Latency-bound
-// calls (a few tokens) take this form; the sum runs in a different order from
-// route_softmax_topk's, so probabilities can differ in their last bits.
+// One warp per token (t = first_warp, first_warp + nwarps, ...): R.prob[t][:]
+// holds the logits on entry and the probabilities on exit.  Lane l holds
+// experts l and l + 32 in registers; the logits get the bias and, if given,
+// the router noise of the token; the maximum and the sum of the
+// exponentials are warp reductions (softmax with the maximum subtracted),
+// and each of the k selections is a warp arg-max (larger probability, else
+// lower expert index); alpha = p / (sum_S p + 1e-20).  R.lse[t] receives
+// the logsumexp of the token's logits, m + log(sum).
 template <int MAXT>
 __device__ __forceinline__ void route_softmax_topk_warp(SmallRoute<MAXT>& R, int T, int E, int k,
                                                         const float* bias, int first_warp,
-                                                        int nwarps, int lane) {
+                                                        int nwarps, int lane,
+                                                        const float* noise = nullptr) {
   for (int t = first_warp; t < T; t += nwarps) {
     float* row = R.prob[t];
     const bool v0 = lane < E, v1 = lane + 32 < E;
-    const float r0 = v0 ? row[lane] + bias[lane] : -INFINITY;
-    const float r1 = v1 ? row[lane + 32] + bias[lane + 32] : -INFINITY;
+    float r0 = v0 ? row[lane] + bias[lane] : -INFINITY;
+    float r1 = v1 ? row[lane + 32] + bias[lane + 32] : -INFINITY;
+    if (noise != nullptr) {
+      if (v0) r0 += noise[t * E + lane];
+      if (v1) r1 += noise[t * E + lane + 32];
+    }
     float m = fmaxf(r0, r1);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     const float x0 = v0 ? __expf(r0 - m) : 0.f;
     const float x1 = v1 ? __expf(r1 - m) : 0.f;
-    const float rz = 1.0f / warp_allsum_f(x0 + x1);
+    const float zsum = warp_allsum_f(x0 + x1);
+    const float rz = 1.0f / zsum;
+    if (lane == 0) R.lse[t] = m + logf(zsum);
     const float p0 = x0 * rz, p1 = x1 * rz;
     if (v0) row[lane] = p0;
     if (v1) row[lane + 32] = p1;
@@ -195,14 +162,30 @@ __device__ __forceinline__ void route_dense(SmallRoute<MAXT>& R, int T, int tid)
 }
 
 // Block 0's routing outputs: topk_idx, topk_w and
-// aux = E * coef * sum_e (count_e / T)(P_e / T)  (lesson 13 §1.6), by one warp.
+// aux = E * coef * sum_e (count_e / T)(P_e / T)  (lesson 13 §1.6), by one warp;
+// with a router variant also the probabilities, lse and
+// z-loss = z_coef * (1/T) sum_t lse_t^2 (fixed summation order).
 template <int MAXT>
 __device__ __forceinline__ void route_outputs(const SmallRoute<MAXT>& R, int T, int E, float coef,
                                               int32_t* topk_idx, float* topk_w, float* aux_loss,
-                                              int tid, int nthreads, int aux_warp) {
+                                              int tid, int nthreads, int aux_warp,
+                                              const RouterVariant* rv = nullptr) {
   for (int a = tid; a < R.nA; a += nthreads) {
     topk_idx[a] = R.sel_e[a];
     topk_w[a] = R.sel_a[a];
+  }
+  if (rv != nullptr) {
+    if (rv->probs != nullptr)
+      for (int i = tid; i < T * E; i += nthreads) rv->probs[i] = R.prob[i / E][i % E];
+    if (rv->lse != nullptr)
+      for (int t = tid; t < T; t += nthreads) rv->lse[t] = R.lse[t];
+    if (rv->z_loss != nullptr && (tid >> 5) == aux_warp) {
+      const int lane = tid & 31;
+      float zs = 0.f;
+      for (int t = lane; t < T; t += 32) zs = fmaf(R.lse[t], R.lse[t], zs);
+      zs = warp_allsum_f(zs);
+      if (lane == 0) *rv->z_loss = rv->z_coef * zs / static_cast<float>(T);
+    }
   }
   if ((tid >> 5) == aux_warp) {
     const int lane = tid & 31;

@@ -82,6 +82,17 @@ __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return
 __device__ void scan_block(int E, int k, int nblk, int64_t T, const RouteExtras& X,
                            const int32_t* __restrict__ blk_cnt, const float* __restrict__ blk_prob);
 
+// z-loss = z_coef * (1/T) * sum_t lse_t^2 from the router blocks' sums of
+// lse^2, by one warp: lane-strided partial sums over the blocks, then a
+// fixed xor tree (the order depends only on nblk).
+__device__ __forceinline__ void finalize_z_loss(const RouterVariant& rv, int nblk, int64_t T,
+                                                int lane) {
+  float zs = 0.f;
+  for (int b = lane; b < nblk; b += 32) zs += __ldcg(rv.blk_z + b);
+  zs = warp_sum(zs);
+  if (lane == 0) *rv.z_loss = rv.z_coef * zs / static_cast<float>(T);
+}
+
 template <typename Tin, int EP>
 __global__ void __launch_bounds__(kRouteThreads)
 router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float* __restrict__ bias,
@@ -110,8 +121,10 @@ router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float
   int* s_gcnt = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(route_smem4) +
                                        static_cast<size_t>(E) * H * sizeof(Tin));   // [k*E]
   __shared__ float red_p[kWarps][EP];
+  __shared__ float red_z[kWarps];
   __shared__ __align__(8) uint64_t xbar;
   __shared__ int s_last;
+  const RouterVariant& rv = X.rv;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = k * E;
@@ -155,6 +168,7 @@ router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float
   float psum[R];
 #pragma unroll
   for (int j = 0; j < R; ++j) psum[j] = 0.f;
+  float zsum = 0.f;                                // lse^2 of the lane group's tokens (slot-0 lane)
 
   for (int pass = 0; pass < kPerWarp / TPW; ++pass) {
     const int lbase = warp * kPerWarp + pass * TPW;      // token within the block
@@ -215,6 +229,7 @@ router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float
 #pragma unroll
     for (int j = 0; j < R; ++j) {
       r[j] = (e_of[j] < E) ? v[j * 32] + bias_v[j] : -INFINITY;
+      if (rv.noise != nullptr && valid && e_of[j] < E) r[j] += rv.noise[tok * E + e_of[j]];
       m = fmaxf(m, r[j]);
     }
 #pragma unroll
@@ -230,6 +245,18 @@ router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float
     float p[R];
 #pragma unroll
     for (int j = 0; j < R; ++j) p[j] = r[j] / z;
+    const float lse = m + logf(z);
+    if (valid) {
+      if (rv.probs != nullptr) {
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+          if (e_of[j] < E) rv.probs[tok * E + e_of[j]] = p[j];
+      }
+      if (lane == gbase) {
+        if (rv.lse != nullptr) rv.lse[tok] = lse;
+        zsum = fmaf(lse, lse, zsum);
+      }
+    }
 
     // top-k: k rounds of a group-wide arg-max over (p desc, index asc)
     float sel_p[MM_MAX_TOPK];
@@ -296,11 +323,18 @@ router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float
     for (int j = 0; j < R; ++j)
       if (e_of[j] < EP) red_p[warp][e_of[j]] = psum[j];
   }
+  zsum = warp_sum(zsum);
+  if (lane == 0) red_z[warp] = zsum;
   __syncthreads();
   if (tid < E) {
     float ps = 0.f;
     for (int w = 0; w < kWarps; ++w) ps += red_p[w][tid];
     blk_prob[static_cast<int64_t>(rblk) * E + tid] = ps;
+  }
+  if (tid == 0 && rv.blk_z != nullptr) {
+    float zs = 0.f;
+    for (int w = 0; w < kWarps; ++w) zs += red_z[w];
+    rv.blk_z[rblk] = zs;
   }
   for (int g = tid; g < G; g += blockDim.x)
     blk_cnt[static_cast<int64_t>(rblk) * G + g] = s_gcnt[g];
@@ -411,6 +445,8 @@ __device__ void scan_block(int E, int k, int nblk, int64_t T, const RouteExtras&
     const float invT = 1.0f / static_cast<float>(T);
     if (X.aux_loss != nullptr) *X.aux_loss = static_cast<float>(E) * X.coef * acc * invT * invT;
   }
+  if (warp == kWarps - 1 && X.rv.z_loss != nullptr)
+    finalize_z_loss(X.rv, nblk, T, lane);
 }
 
 
@@ -558,6 +594,7 @@ dispatch_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, int k,
       const float invT = 1.0f / static_cast<float>(T);
       *D.aux_loss = static_cast<float>(E) * D.coef * acc * invT * invT;
     }
+    if (warp == kWarps - 1 && D.rv.z_loss != nullptr) finalize_z_loss(D.rv, nblk, T, lane);
   }
 
   for (int s = 0; s < k; ++s) {
@@ -636,8 +673,10 @@ router_tc_kernel(const __grid_constant__ RtMaps M, int64_t T, int H, int E, int 
   __shared__ uint32_t s_tmem;
   __shared__ int s_gcnt[kMaxGroups];
   __shared__ float s_red[2][EP];
+  __shared__ float s_redz[2];
   __shared__ float s_bias[EP];
   __shared__ int s_last;
+  const RouterVariant& rv = X.rv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rblk = blockIdx.x;
   const int nblk = static_cast<int>((T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock);
@@ -722,10 +761,12 @@ router_tc_kernel(const __grid_constant__ RtMaps M, int64_t T, int H, int E, int 
       // loops over the E experts only (E is uniform; the padded columns past
       // E are never read)
       float m = -INFINITY;
+      const float* nz = (rv.noise != nullptr && valid) ? rv.noise + (t0 + t) * E : nullptr;
 #pragma unroll
       for (int e = 0; e < EP; ++e) {
         if (e >= E) break;
         p[e] += s_bias[e];
+        if (nz != nullptr) p[e] += nz[e];
         m = fmaxf(m, p[e]);
       }
       float z = 0.f;
@@ -739,6 +780,24 @@ router_tc_kernel(const __grid_constant__ RtMaps M, int64_t T, int H, int E, int 
       for (int e = 0; e < EP; ++e) {
         if (e >= E) break;
         p[e] = p[e] / z;
+      }
+      const float lse = m + logf(z);
+      if (valid) {
+        if (rv.probs != nullptr) {
+          float* pr = rv.probs + (t0 + t) * E;
+#pragma unroll
+          for (int e = 0; e < EP; ++e) {
+            if (e >= E) break;
+            pr[e] = p[e];
+          }
+        }
+        if (rv.lse != nullptr) rv.lse[t0 + t] = lse;
+      }
+      {
+        float v = valid ? lse * lse : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) s_redz[warp] = v;
       }
       // top-k: k arg-max passes in expert order, strict comparison (lower index first)
       uint64_t taken = 0;
@@ -791,6 +850,7 @@ router_tc_kernel(const __grid_constant__ RtMaps M, int64_t T, int H, int E, int 
   ok = __syncthreads_and(ok);
   if (ok) {
     if (tid < E) blk_prob[static_cast<int64_t>(rblk) * E + tid] = s_red[0][tid] + s_red[1][tid];
+    if (tid == 0 && rv.blk_z != nullptr) rv.blk_z[rblk] = s_redz[0] + s_redz[1];
     for (int g = tid; g < G; g += kRouteThreads) blk_cnt[static_cast<int64_t>(rblk) * G + g] = s_gcnt[g];
   }
   if (tid == 32) {
@@ -907,6 +967,7 @@ cudaError_t launch_router(int dtype, const void* x, const void* Wr, const float*
   X.coef = out.coef;
   X.do_scan = out.do_scan;
   X.hdr = hdr;
+  X.rv = out.rv;
   const bool tc_ok = dtype == kDtypeBF16 && H % 64 == 0 && E <= 64 &&
                      (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && (reinterpret_cast<uintptr_t>(Wr) & 15u) == 0;
   if (tc_ok) {

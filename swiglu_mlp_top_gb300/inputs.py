@@ -132,3 +132,11 @@ def to_f64(t) -> "numpy.ndarray":  # noqa: F821
     if t is None:
         return None
     return t.detach().to("cpu", torch.float64).numpy()
+
+
+def make_router_noise(T: int, E: int, std: float, seed: int = 1) -> torch.Tensor:
+    """Router noise draws: [T, E] float32 ~ N(0, std^2) from its own seeded
+    CPU generator.  The method adds them to the logits; the draw itself is
+    an input, shared by the CUDA path and the oracle."""
+    gen = torch.Generator().manual_seed(seed)
+    return (torch.randn(T, E, generator=gen, dtype=torch.float32) * std).contiguous()

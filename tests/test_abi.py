@@ -43,6 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings(lib):
     assert lib.mm_status_string(0) == b"MM_OK"
     assert lib.mm_status_string(5) == b"MM_ERR_TIMEOUT"
+    assert lib.mm_status_string(6) == b"MM_ERR_RANGE"
     assert lib.mm_version() >= 100
 
 

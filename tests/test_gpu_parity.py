@@ -280,6 +280,33 @@ def test_decode_workloads(T):
     assert rel_err(y.double().cpu().numpy(), ref) <= Y_TOL["bf16"]
 
 
+@pytest.mark.parametrize("E,k", [(64, 8), (8, 2), (32, 4)])
+def test_moe_back_to_back_calls(E, k):
+    """Calls issued back to back on the tensor path, on fresh zeroed
+    workspaces and then on one reused workspace with new inputs (so new
+    routing) each call: every result matches the oracle.  The grouped GEMMs
+    launch before the dispatch kernel has written the group offsets
+    (programmatic dependent launch), so this catches a kernel that reads
+    them before waiting for it."""
+    T, H, I = 300, 256, 192
+    ws = mm.new_workspace(mm.moe_workspace_bytes(T, H, I, E, k, torch.bfloat16))
+    for call in range(6):
+        inp = moe_inputs(T, H, I, E, "bf16", seed=300 + 10 * E + call)
+        g = to_dev(inp)
+        y, idx, w, aux = mm.moe_forward(g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], k, 0.01,
+                                        path="tensor", workspace=ws if call >= 3 else None)
+        torch.cuda.synchronize()
+        i64 = inputs64(inp)
+        ref = oracle.moe_forward(i64["x"], i64["Wr"], i64["Wg"], i64["Wu"], i64["Wd"], k, 0.01)
+        tie, diff = check_route(idx.cpu().numpy(), w.cpu().numpy(), float(aux), ref, k)
+        yref = ref["y"].copy()
+        if diff.any():
+            rows = np.nonzero(diff)[0]
+            yref[rows] = ref_y_rows(i64, ref, idx.cpu().numpy(), rows, k)
+        err = rel_err(y.double().cpu().numpy(), yref)
+        assert err <= Y_TOL["bf16"], f"call {call}: y rel err {err}"
+
+
 # ------------------------------------------------------------------ full-size workloads
 @pytest.mark.parametrize("name", ["dense_t4096", "dense_t100"])
 def test_dense_full_size(name):
@@ -333,6 +360,33 @@ def test_moe_forward_graph_capture_replays_identically(T):
     torch.cuda.synchronize()
     assert torch.equal(y, eager[0]) and torch.equal(idx, eager[1])
     assert torch.equal(w, eager[2]) and torch.equal(aux, eager[3])
+
+
+# ------------------------------------------------------------------ fp16 range of h
+@pytest.mark.parametrize("scale,expect", [(1.0, 0), (2000.0, 6)])
+def test_fp16_h_overflow_is_reported(scale, expect):
+    """The bf16 prefill path keeps h = SiLU(g) * u in fp16.  With x scaled by
+    2000 (weights N(0, 0.02), H = 256) g and u are ~ 600, so |h| reaches
+    ~ 3e5, beyond fp16's 65504: the call must report MM_ERR_RANGE through
+    mm_check_status instead of leaving a silent inf in y.  Unscaled inputs
+    report nothing; the status clears once read."""
+    inp = make_inputs(300, 256, 384, "bf16", seed=31)
+    x = (inp["x"].float() * scale).to(torch.bfloat16)
+    g = to_dev(inp)
+    ws = mm.new_workspace(mm.ffn_workspace_bytes(300, 256, 384, torch.bfloat16))
+    mm.swiglu_ffn(x.cuda(), g["Wg"], g["Wu"], g["Wd"], workspace=ws, path="tensor")
+    assert mm.check_status(ws) == expect
+    assert mm.check_status(ws) == 0
+
+
+def test_fp16_h_overflow_is_reported_by_the_moe_forward():
+    inp = moe_inputs(400, 256, 320, 4, "bf16", seed=32)
+    inp["x"] = (inp["x"].float() * 2000.0).to(torch.bfloat16)
+    g = to_dev(inp)
+    ws = mm.new_workspace(mm.moe_workspace_bytes(400, 256, 320, 4, 2, torch.bfloat16))
+    mm.moe_forward(g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], 2, 0.01, workspace=ws,
+                   path="tensor")
+    assert mm.check_status(ws) == 6
 
 
 # ------------------------------------------------------------------ watchdog
