@@ -248,3 +248,95 @@ def near_tie_tokens(p, k, gap=1e-6):
         return np.zeros(q.shape[0], dtype=bool)
     gaps = q[:, :jmax] - q[:, 1:jmax + 1]
     return (gaps < gap).any(axis=-1)
+
+
+# --------------------------------------------------------------------------
+# Backward pass (training: L_train = L_lm + L_aux, lesson 13 step 8)
+# --------------------------------------------------------------------------
+def swiglu_ffn_backward(x, Wg, Wu, Wd, dy):
+    """Gradients of the dense SwiGLU FFN for an upstream gradient dy = dL/dy
+    (the chain rule through [L13] §0 / §1.2's equations):
+
+        g = Wg x, u = Wu x, s = sigmoid(g), h = g s u, y = Wd h
+        dWd = dy^T h,  dh = dy Wd
+        du = dh * SiLU(g),  dg = dh * u * SiLU'(g),  SiLU'(g) = s (1 + g (1 - s))
+        dx = dg Wg + du Wu,  dWg = dg^T x,  dWu = du^T x
+
+    Returns (dx [T, H], dWg [I, H], dWu [I, H], dWd [H, I]).
+    """
+    x, Wg, Wu, Wd, dy = _f64(x), _f64(Wg), _f64(Wu), _f64(Wd), _f64(dy)
+    g = x @ Wg.T
+    u = x @ Wu.T
+    sg = 1.0 / (1.0 + np.exp(-g))
+    h = g * sg * u
+    dWd = dy.T @ h
+    dh = dy @ Wd
+    du = dh * (g * sg)
+    dg = dh * u * (sg * (1.0 + g * (1.0 - sg)))
+    dx = dg @ Wg + du @ Wu
+    return dx, dg.T @ x, du.T @ x, dWd
+
+
+def moe_backward(x, Wr, Wg, Wu, Wd, k, coef, dy, d_aux=1.0, logit_bias=None,
+                 logit_noise=None, z_coef=0.0, d_z=1.0):
+    """Gradients of L = <dy, y> + d_aux * aux_loss + d_z * z_loss for the MoE
+    layer (the scalar upstream gradients d_aux, d_z are 1 for L_lm + L_aux).
+
+    Routing is recomputed as in :func:`moe_forward`; the selection S is a
+    discrete choice with no gradient, so (p-chao.com note 08 §7) the router
+    receives gradient only through the selected weights alpha, and the
+    experts a token did not select receive none from it.  In aux, the load
+    f_e is a count with no gradient and the mean probability P_e carries it
+    ([CH4] §4.4: f_i is not differentiable, P_i is).  Steps:
+
+      o_{t,s} = Expert_{S_s}(x_t);   y_t = sum_s alpha_{t,s} o_{t,s}
+      dalpha_{t,s} = <dy_t, o_{t,s}>;  expert backward with upstream alpha dy_t
+      alpha_s = p_s / Z, Z = sum_S p + 1e-20:
+          dp_{S_s} += dalpha_s / Z - (sum_j dalpha_j p_{S_j}) / Z^2
+      aux = E coef sum_e (count_e / T)(sum_t p_{t,e} / T):
+          dp_{t,e} += d_aux * E * coef * count_e / T^2
+      softmax: dr_{t,e} = p_{t,e} (dp_{t,e} - sum_j p_{t,j} dp_{t,j})
+      z-loss = z_coef / T * sum_t lse_t^2:  dr_{t,e} += d_z * 2 z_coef lse_t p_{t,e} / T
+      dWr = dr^T x;  dx += dr Wr;  d_bias = sum_t dr_t (the logit bias as a parameter)
+
+    Returns a dict: dx [T, H], dWr [E, H], dWg / dWu / dWd (lists of E),
+    d_bias [E], dalpha [T, k], dlogits [T, E].
+    """
+    x, Wr, dy = _f64(x), _f64(Wr), _f64(dy)
+    T, H = x.shape
+    E = len(Wg)
+    r = router_logits(x, Wr, logit_bias, logit_noise)
+    p = softmax(r)
+    idx, val = topk(p, k)
+    alpha = renormalise(val)
+    _, counts = expert_load(idx, E)
+    dx = np.zeros((T, H))
+    dWg = [np.zeros_like(_f64(w)) for w in Wg]
+    dWu = [np.zeros_like(_f64(w)) for w in Wu]
+    dWd = [np.zeros_like(_f64(w)) for w in Wd]
+    dalpha = np.zeros((T, k))
+    for e in range(E):
+        for s in range(k):
+            tok = np.nonzero(idx[:, s] == e)[0]
+            if tok.size == 0:
+                continue
+            o = swiglu_ffn(x[tok], Wg[e], Wu[e], Wd[e])
+            dalpha[tok, s] = np.sum(dy[tok] * o, axis=1)
+            up = dy[tok] * alpha[tok, s][:, None]
+            gx, gg, gu, gd = swiglu_ffn_backward(x[tok], Wg[e], Wu[e], Wd[e], up)
+            dx[tok] += gx
+            dWg[e] += gg
+            dWu[e] += gu
+            dWd[e] += gd
+    dp = np.zeros((T, E))
+    Z = val.sum(axis=1) + RENORM_EPS
+    c = np.sum(dalpha * val, axis=1)
+    for s in range(k):
+        dp[np.arange(T), idx[:, s]] += dalpha[:, s] / Z - c / Z ** 2
+    dp += F64(d_aux) * F64(E) * F64(coef) * counts[None, :].astype(F64) / F64(T) ** 2
+    dr = p * (dp - np.sum(p * dp, axis=1, keepdims=True))
+    lse = logsumexp(r)
+    dr += F64(d_z) * 2.0 * F64(z_coef) * lse[:, None] * p / F64(T)
+    dx += dr @ Wr
+    return {"dx": dx, "dWr": dr.T @ x, "dWg": dWg, "dWu": dWu, "dWd": dWd,
+            "d_bias": dr.sum(axis=0), "dalpha": dalpha, "dlogits": dr}

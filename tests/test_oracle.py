@@ -561,3 +561,117 @@ def test_noise_changes_the_choice():
     noise[:, 3] = 50.0
     out = O.moe_route(x, Wr, 1, 0.0, logit_noise=noise)
     assert (out["topk_idx"][:, 0] == 3).all()
+
+
+# --------------------------------------------------------------------------
+# Backward pass: finite differences of the oracle's own forward (itself
+# pinned above) and the special cases the pages fix
+# --------------------------------------------------------------------------
+def _fd_grad(f, a, eps=1e-5):
+    """Central differences of the scalar f() with respect to every element of a."""
+    g = np.zeros_like(a)
+    it = np.nditer(a, flags=["multi_index"])
+    for _ in it:
+        i = it.multi_index
+        old = a[i]
+        a[i] = old + eps
+        fp = f()
+        a[i] = old - eps
+        fm = f()
+        a[i] = old
+        g[i] = (fp - fm) / (2 * eps)
+    return g
+
+
+def test_swiglu_backward_finite_differences():
+    r = rng(30)
+    x, dy = r.normal(size=(3, 4)), r.normal(size=(3, 4))
+    Wg, Wu, Wd = r.normal(size=(5, 4)), r.normal(size=(5, 4)), r.normal(size=(4, 5))
+    loss = lambda: float(np.sum(dy * O.swiglu_ffn(x, Wg, Wu, Wd)))
+    dx, dWg, dWu, dWd = O.swiglu_ffn_backward(x, Wg, Wu, Wd, dy)
+    for got, a in ((dx, x), (dWg, Wg), (dWu, Wu), (dWd, Wd)):
+        np.testing.assert_allclose(got, _fd_grad(loss, a), rtol=0, atol=1e-7)
+
+
+def _moe_case(seed, T=6, H=5, I=4, E=4):
+    r = rng(seed)
+    return (r.normal(size=(T, H)), r.normal(size=(E, H)) * 0.7,
+            [r.normal(size=(I, H)) for _ in range(E)], [r.normal(size=(I, H)) for _ in range(E)],
+            [r.normal(size=(H, I)) for _ in range(E)], r.normal(size=(T, H)))
+
+
+@pytest.mark.parametrize("k,with_noise", [(1, False), (2, False), (2, True), (3, True)])
+def test_moe_backward_finite_differences(k, with_noise):
+    """dL/d(every input) for L = <dy, y> + d_aux aux + d_z z: the router's
+    gradient through alpha, P_e and lse, the experts' through alpha dy."""
+    coef, zc, d_aux, d_z = 0.05, 0.02, 1.3, 0.7
+    # finite differences are valid only away from a change of selection:
+    # take the first draw with no top-k gap below 1e-3
+    for seed in range(31, 81):
+        x, Wr, Wg, Wu, Wd, dy = _moe_case(seed + 100 * k)
+        T, E = x.shape[0], Wr.shape[0]
+        bias = rng(seed).normal(size=E) * 0.3
+        noise = rng(seed + 1).normal(size=(T, E)) * 0.5 if with_noise else None
+        p = O.moe_route(x, Wr, k, coef, bias, noise)["probs"]
+        if not O.near_tie_tokens(p, k, gap=1e-3).any():
+            break
+
+    def loss():
+        f = O.moe_forward(x, Wr, Wg, Wu, Wd, k, coef, bias, noise, zc)
+        return float(np.sum(dy * f["y"])) + d_aux * f["aux_loss"] + d_z * f["z_loss"]
+
+    assert not O.near_tie_tokens(p, k, gap=1e-3).any()
+    g = O.moe_backward(x, Wr, Wg, Wu, Wd, k, coef, dy, d_aux, bias, noise, zc, d_z)
+    np.testing.assert_allclose(g["dx"], _fd_grad(loss, x), rtol=0, atol=1e-7)
+    np.testing.assert_allclose(g["dWr"], _fd_grad(loss, Wr), rtol=0, atol=1e-7)
+    np.testing.assert_allclose(g["d_bias"], _fd_grad(loss, bias), rtol=0, atol=1e-7)
+    for e in range(E):
+        np.testing.assert_allclose(g["dWg"][e], _fd_grad(loss, Wg[e]), rtol=0, atol=1e-7)
+        np.testing.assert_allclose(g["dWu"][e], _fd_grad(loss, Wu[e]), rtol=0, atol=1e-7)
+        np.testing.assert_allclose(g["dWd"][e], _fd_grad(loss, Wd[e]), rtol=0, atol=1e-7)
+
+
+def test_moe_backward_top1_router_learns_only_from_aux():
+    """Top-1 with renormalisation: alpha = p / p = 1 is constant, so <dy, y>
+    sends the router no gradient (note 08 §7: the router learns through
+    topk_weight; here that weight is 1) - only aux and z-loss reach it."""
+    x, Wr, Wg, Wu, Wd, dy = _moe_case(50)
+    g = O.moe_backward(x, Wr, Wg, Wu, Wd, 1, 0.0, dy, z_coef=0.0)
+    assert np.abs(g["dWr"]).max() < 1e-12 and np.abs(g["d_bias"]).max() < 1e-12
+    g = O.moe_backward(x, Wr, Wg, Wu, Wd, 1, 0.05, dy, z_coef=0.0)
+    assert np.abs(g["dWr"]).max() > 1e-4
+
+
+def test_moe_backward_unselected_expert_gets_no_gradient():
+    x, Wr, Wg, Wu, Wd, dy = _moe_case(51)
+    noise = np.zeros((x.shape[0], 4))
+    noise[:, 2] = -50.0                       # expert 2 is never selected
+    g = O.moe_backward(x, Wr, Wg, Wu, Wd, 2, 0.01, dy, logit_noise=noise)
+    assert np.all(g["dWg"][2] == 0) and np.all(g["dWu"][2] == 0) and np.all(g["dWd"][2] == 0)
+    assert np.abs(g["dWg"][0]).max() > 0
+
+
+def test_moe_backward_single_expert_is_dense_backward():
+    """E = 1, k = 1: alpha = 1, y = FFN(x), so the expert's gradients and dx
+    are the dense FFN's; with coef = z = 0 the router gets nothing."""
+    x, Wr, Wg, Wu, Wd, dy = _moe_case(52, E=1)
+    g = O.moe_backward(x, Wr, Wg, Wu, Wd, 1, 0.0, dy)
+    dx, dWg, dWu, dWd = O.swiglu_ffn_backward(x, Wg[0], Wu[0], Wd[0], dy)
+    np.testing.assert_allclose(g["dx"], dx, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(g["dWg"][0], dWg, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(g["dWd"][0], dWd, rtol=0, atol=1e-13)
+    assert np.abs(g["dWr"]).max() < 1e-12
+
+
+def test_moe_backward_all_experts_identical_and_k_equal_E():
+    """k = E with identical experts: y = sum_e p_e FFN(x) = FFN(x) does not
+    depend on the router, so with coef = z = 0 dWr = 0 and dx is the dense
+    FFN's dx; the weight gradient of each expert is p_e times the dense one."""
+    x, Wr, Wg, Wu, Wd, dy = _moe_case(53)
+    E = 4
+    Wg, Wu, Wd = [Wg[0]] * E, [Wu[0]] * E, [Wd[0]] * E
+    g = O.moe_backward(x, Wr, Wg, Wu, Wd, E, 0.0, dy)
+    dx, dWg, _, _ = O.swiglu_ffn_backward(x, Wg[0], Wu[0], Wd[0], dy)
+    np.testing.assert_allclose(g["dx"], dx, rtol=0, atol=1e-12)
+    assert np.abs(g["dWr"]).max() < 1e-12
+    np.testing.assert_allclose(sum(g["dWg"]), dWg, rtol=0, atol=1e-12)
