@@ -248,6 +248,52 @@ int mm_moe_route_opts(const void* x, const void* Wr, int64_t T, int H, int E, in
                       const mm_moe_options* opts);
 
 /* ------------------------------------------------------------------------
+ * Backward pass   (training objective L_train = L_lm + L_aux, [L13] step 8;
+ * the router's gradient flows only through the selected weights alpha,
+ * p-chao.com "MiniMind 学习笔记 08" §7; in aux only P_e carries gradient,
+ * [CH4] §4.4)
+ *
+ * bf16 only, on the tensor cores; H and I multiples of 64.  Inputs and
+ * outputs are device memory; every gradient is OVERWRITTEN (not added to).
+ *
+ * Dense FFN: for dy = dL/dy [T, H] (bf16),
+ *   dx [T, H] (bf16) and dWg, dWu [I, H], dWd [H, I] (fp32) with
+ *   dWd = dy^T h, dh = dy Wd, dU = dh SiLU(g), dG = dh u SiLU'(g),
+ *   dx = dG Wg + dU Wu, dWg = dG^T x, dWu = dU^T x  (g and u recomputed).
+ * T = 0 zeroes the weight gradients.
+ * ---------------------------------------------------------------------- */
+size_t mm_swiglu_ffn_backward_workspace_bytes(int64_t T, int H, int I, int dtype);
+
+int mm_swiglu_ffn_backward(const void* x, const void* Wg, const void* Wu, const void* Wd,
+                           const void* dy, int64_t T, int H, int I, int dtype,
+                           void* dx, float* dWg, float* dWu, float* dWd,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* MoE layer: gradients of L = <dy, y> + d_aux * aux_loss + d_z * z_loss
+ * (d_aux = d_z = 1 for L_lm + L_aux + L_z), given the forward's saved routing:
+ * topk_idx, topk_w (alpha) and router_probs [T, E] from mm_moe_forward_opts
+ * (router_lse [T] too when z_coef and d_z are non-zero, else nullable).
+ * The router noise and logit bias of the forward are already inside those
+ * probabilities.  Outputs:
+ *   dx [T, H] (bf16), dWr [E, H] (fp32), dWg[e], dWu[e] [I, H] and dWd[e]
+ *   [H, I] (HOST arrays of E device fp32 pointers; an expert no token chose
+ *   gets zeros), d_bias [E] (fp32, nullable): the gradient of the logit bias
+ *   as a parameter (= sum_t dL/dlogits).
+ * Deterministic: every sum runs in a fixed order.
+ * ---------------------------------------------------------------------- */
+size_t mm_moe_backward_workspace_bytes(int64_t T, int H, int I, int E, int k, int dtype);
+
+int mm_moe_backward(const void* x, const void* Wr,
+                    const void* const* Wg, const void* const* Wu, const void* const* Wd,
+                    int64_t T, int H, int I, int E, int k, float coef, int dtype,
+                    const int32_t* topk_idx, const float* topk_w,
+                    const float* router_probs, const float* router_lse,
+                    const void* dy, float d_aux, float z_coef, float d_z,
+                    void* dx, float* dWr, float* const* dWg, float* const* dWu,
+                    float* const* dWd, float* d_bias,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * Status
  * ---------------------------------------------------------------------- */
 /* Synchronises `stream`, reads and clears the device status word kept at
@@ -273,7 +319,11 @@ typedef enum {
   MM_KERNEL_DISPATCH = 3,   /* aux finalisation, group offsets, token permute */
   MM_KERNEL_GATEUP = 4,     /* gate/up GEMM with the SwiGLU epilogue        */
   MM_KERNEL_DOWN = 5,       /* down GEMM with the alpha-scaled combine      */
-  MM_KERNEL_DECODE = 7      /* decode-sized weight-streaming kernel (whole call) */
+  MM_KERNEL_DECODE = 7,     /* decode-sized weight-streaming kernel (whole call) */
+  MM_KERNEL_BWD_DGRAD = 8,  /* backward: dh = dy Wd and dx = dG Wg + dU Wu GEMMs */
+  MM_KERNEL_BWD_SWIGLU = 9, /* backward: gate/up recomputed, SwiGLU derivative */
+  MM_KERNEL_BWD_WGRAD = 10, /* backward: weight-gradient GEMMs                */
+  MM_KERNEL_BWD_ROUTER = 11 /* backward: dispatch, router gradient, dx combine */
 } mm_kernel_id;
 
 /* Number of kernels this library has enqueued since it was loaded. */

@@ -278,7 +278,7 @@ def swiglu_ffn_backward(x, Wg, Wu, Wd, dy):
 
 
 def moe_backward(x, Wr, Wg, Wu, Wd, k, coef, dy, d_aux=1.0, logit_bias=None,
-                 logit_noise=None, z_coef=0.0, d_z=1.0):
+                 logit_noise=None, z_coef=0.0, d_z=1.0, topk_idx=None):
     """Gradients of L = <dy, y> + d_aux * aux_loss + d_z * z_loss for the MoE
     layer (the scalar upstream gradients d_aux, d_z are 1 for L_lm + L_aux).
 
@@ -299,6 +299,10 @@ def moe_backward(x, Wr, Wg, Wu, Wd, k, coef, dy, d_aux=1.0, logit_bias=None,
       z-loss = z_coef / T * sum_t lse_t^2:  dr_{t,e} += d_z * 2 z_coef lse_t p_{t,e} / T
       dWr = dr^T x;  dx += dr Wr;  d_bias = sum_t dr_t (the logit bias as a parameter)
 
+    ``topk_idx`` (optional) replaces the selection: on a near-tie token both
+    selections are correct forwards, and a backward is compared on the one
+    the forward took.
+
     Returns a dict: dx [T, H], dWr [E, H], dWg / dWu / dWd (lists of E),
     d_bias [E], dalpha [T, k], dlogits [T, E].
     """
@@ -308,6 +312,9 @@ def moe_backward(x, Wr, Wg, Wu, Wd, k, coef, dy, d_aux=1.0, logit_bias=None,
     r = router_logits(x, Wr, logit_bias, logit_noise)
     p = softmax(r)
     idx, val = topk(p, k)
+    if topk_idx is not None:
+        idx = np.asarray(topk_idx).astype(np.int64)
+        val = np.take_along_axis(p, idx, axis=-1)
     alpha = renormalise(val)
     _, counts = expert_load(idx, E)
     dx = np.zeros((T, H))

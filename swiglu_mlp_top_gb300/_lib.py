@@ -53,6 +53,13 @@ SIGNATURES = {
                                  _vp, _vp, _sz, _vp, _opt]),
     "mm_moe_route": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _f32, _i32, _vp, _vp, _vp, _vp,
                             _vp, _vp, _sz, _vp]),
+    "mm_swiglu_ffn_backward_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32]),
+    "mm_swiglu_ffn_backward": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _vp, _vp,
+                                      _vp, _vp, _vp, _sz, _vp]),
+    "mm_moe_backward_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32, _i32, _i32]),
+    "mm_moe_backward": (_i32, [_vp, _vp, _pp, _pp, _pp, _i64, _i32, _i32, _i32, _i32, _f32, _i32,
+                               _vp, _vp, _vp, _vp, _vp, _f32, _f32, _f32, _vp, _vp, _pp, _pp, _pp,
+                               _vp, _vp, _sz, _vp]),
     "mm_check_status": (_i32, [_vp, _vp]),
     "mm_watchdog_selftest": (_i32, [_vp, _sz, C.c_uint32, _vp]),
     "mm_launch_count": (C.c_uint64, []),
@@ -60,6 +67,7 @@ SIGNATURES = {
     "mm_profile_stop": (_i32, [C.POINTER(C.c_double), C.POINTER(C.c_int)]),
 }
 MM_KERNEL_ROUTER, MM_KERNEL_DISPATCH, MM_KERNEL_GATEUP, MM_KERNEL_DOWN, MM_KERNEL_DECODE = 1, 3, 4, 5, 7
+MM_KERNEL_BWD_DGRAD, MM_KERNEL_BWD_SWIGLU, MM_KERNEL_BWD_WGRAD, MM_KERNEL_BWD_ROUTER = 8, 9, 10, 11
 
 _lib = None
 

@@ -189,6 +189,79 @@ def moe_route(x: torch.Tensor, Wr: torch.Tensor, k: int, coef: float, *,
     return idx, w, aux, counts
 
 
+def swiglu_ffn_backward(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Tensor,
+                        dy: torch.Tensor, *, workspace: Optional[torch.Tensor] = None,
+                        stream=None):
+    """Backward of the dense FFN (mm_swiglu_ffn_backward, bf16): returns
+    (dx [T, H] bf16, dWg [I, H], dWu [I, H], dWd [H, I] fp32)."""
+    lib = L.load()
+    T, H = x.shape
+    I = Wg.shape[0]
+    dt = _dtype_code(x)
+    dev = x.device
+    dx = torch.empty_like(x)
+    dWg = torch.empty(I, H, dtype=torch.float32, device=dev)
+    dWu = torch.empty(I, H, dtype=torch.float32, device=dev)
+    dWd = torch.empty(H, I, dtype=torch.float32, device=dev)
+    need = lib.mm_swiglu_ffn_backward_workspace_bytes(T, H, I, dt)
+    if workspace is None:
+        workspace = new_workspace(need, dev)
+    rc = lib.mm_swiglu_ffn_backward(
+        _dev(x, "x"), _dev(Wg, "Wg", x.dtype), _dev(Wu, "Wu", x.dtype), _dev(Wd, "Wd", x.dtype),
+        _dev(dy, "dy", x.dtype), T, H, I, dt, dx.data_ptr(), dWg.data_ptr(), dWu.data_ptr(),
+        dWd.data_ptr(), _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    L.check(rc, "mm_swiglu_ffn_backward")
+    return dx, dWg, dWu, dWd
+
+
+def moe_backward(x: torch.Tensor, Wr: torch.Tensor, Wg: Sequence[torch.Tensor],
+                 Wu: Sequence[torch.Tensor], Wd: Sequence[torch.Tensor], k: int, coef: float,
+                 topk_idx: torch.Tensor, topk_w: torch.Tensor, probs: torch.Tensor,
+                 dy: torch.Tensor, *, d_aux: float = 1.0, lse: Optional[torch.Tensor] = None,
+                 z_coef: float = 0.0, d_z: float = 1.0, bias_grad: bool = False,
+                 workspace: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """Backward of the MoE layer (mm_moe_backward, bf16) from the forward's
+    saved routing (topk_idx, topk_w, and the `stats` probs / lse of
+    moe_forward).  Returns a dict: dx, dWr, dWg / dWu / dWd (lists of E
+    fp32 tensors) and, with bias_grad, d_bias."""
+    lib = L.load()
+    T, H = x.shape
+    E = len(Wg)
+    I = Wg[0].shape[0]
+    dt = _dtype_code(x)
+    dev = x.device
+    dx = torch.empty_like(x)
+    dWr = torch.empty(E, H, dtype=torch.float32, device=dev)
+    dWg = [torch.empty(I, H, dtype=torch.float32, device=dev) for _ in range(E)]
+    dWu = [torch.empty(I, H, dtype=torch.float32, device=dev) for _ in range(E)]
+    dWd = [torch.empty(H, I, dtype=torch.float32, device=dev) for _ in range(E)]
+    d_bias = torch.empty(E, dtype=torch.float32, device=dev) if bias_grad else None
+    need = lib.mm_moe_backward_workspace_bytes(T, H, I, E, k, dt)
+    if workspace is None:
+        workspace = new_workspace(need, dev)
+    pg, ag = L.ptr_array([_dev(w, "Wg", x.dtype) for w in Wg])
+    pu, au = L.ptr_array([_dev(w, "Wu", x.dtype) for w in Wu])
+    pd, ad = L.ptr_array([_dev(w, "Wd", x.dtype) for w in Wd])
+    qg, bg = L.ptr_array([t.data_ptr() for t in dWg])
+    qu, bu = L.ptr_array([t.data_ptr() for t in dWu])
+    qd, bd = L.ptr_array([t.data_ptr() for t in dWd])
+    rc = lib.mm_moe_backward(
+        _dev(x, "x"), _dev(Wr, "Wr", x.dtype), pg, pu, pd, T, H, I, E, k, float(coef), dt,
+        _dev(topk_idx, "topk_idx", torch.int32), _dev(topk_w, "topk_w", torch.float32),
+        _dev(probs, "probs", torch.float32),
+        None if lse is None else _dev(lse, "lse", torch.float32), _dev(dy, "dy", x.dtype),
+        float(d_aux), float(z_coef), float(d_z), dx.data_ptr(), dWr.data_ptr(), qg, qu, qd,
+        None if d_bias is None else d_bias.data_ptr(), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    del ag, au, ad, bg, bu, bd
+    L.check(rc, "mm_moe_backward")
+    out = {"dx": dx, "dWr": dWr, "dWg": dWg, "dWu": dWu, "dWd": dWd}
+    if d_bias is not None:
+        out["d_bias"] = d_bias
+    return out
+
+
 def check_status(workspace: torch.Tensor, stream=None) -> int:
     """Synchronise and return the device watchdog status (0 = fine); clears it."""
     return int(L.load().mm_check_status(_dev(workspace, "workspace"), _stream(stream)))

@@ -76,6 +76,58 @@ RouteLayout route_layout(int64_t T, int E, int k) {
   return L;
 }
 
+// Backward of the dense FFN (bf16): dh = dy Wd [T, I] (fp32: only the
+// SwiGLU-backward epilogue reads it), dG | dU [T, 2I] and h [T, I] (bf16:
+// operands of the tensor-core GEMMs).
+struct DenseBwdLayout {
+  size_t dh, dgu, h, total;
+};
+DenseBwdLayout dense_bwd_layout(int64_t T, int I) {
+  DenseBwdLayout L;
+  const size_t ti = static_cast<size_t>(T) * I;
+  size_t off = sizeof(WsHeader);
+  L.dh = off;  off += align_up(4 * ti);
+  L.dgu = off; off += align_up(4 * ti);
+  L.h = off;   off += align_up(2 * ti);
+  L.total = off;
+  return L;
+}
+
+// Backward of the MoE layer (bf16).  Rows are the T*k assignments grouped by
+// expert, each group padded to a multiple of kBwAlign rows: at most
+// T*k + E*(kBwAlign - 1) rows.
+struct MoeBwdLayout {
+  int64_t rows;                    // row capacity of the padded buffers
+  int n_parts;                     // dalpha partials per row
+  size_t blk_cnt, offsets, counts, pos, perm, xp, dyp, dhu, dgu, ha, dpart, dxp, dr, dwr_part,
+      dbias_part, total;
+};
+MoeBwdLayout moe_bwd_layout(int64_t T, int H, int I, int E, int k) {
+  MoeBwdLayout L;
+  const size_t nblk = static_cast<size_t>(route_blocks(T));
+  L.rows = T * k + static_cast<int64_t>(E) * (kBwAlign - 1);
+  L.n_parts = 2 * ((I + 127) / 128);
+  const size_t R = static_cast<size_t>(L.rows);
+  size_t off = sizeof(WsHeader);
+  L.blk_cnt = off;    off += align_up(4 * nblk * E);
+  L.offsets = off;    off += align_up(4 * (static_cast<size_t>(E) + 1));
+  L.counts = off;     off += align_up(4 * static_cast<size_t>(E));
+  L.pos = off;        off += align_up(4 * static_cast<size_t>(T) * k);
+  L.perm = off;       off += align_up(4 * R);
+  L.xp = off;         off += align_up(2 * R * H);
+  L.dyp = off;        off += align_up(2 * R * H);
+  L.dhu = off;        off += align_up(4 * R * I);
+  L.dgu = off;        off += align_up(4 * R * I);
+  L.ha = off;         off += align_up(2 * R * I);
+  L.dpart = off;      off += align_up(4 * R * L.n_parts);
+  L.dxp = off;        off += align_up(4 * R * H);
+  L.dr = off;         off += align_up(4 * static_cast<size_t>(T) * E);
+  L.dwr_part = off;   off += align_up(4 * nblk * E * H);
+  L.dbias_part = off; off += align_up(4 * nblk * E);
+  L.total = off;
+  return L;
+}
+
 // Dense workspace of the tensor-core and SIMT paths: h [T, I], then (bf16)
 // the fp16 copy of Wd.
 size_t dense_h_bytes(int64_t T, int I, int dtype) {
@@ -534,12 +586,194 @@ int mm_moe_route_opts(const void* x, const void* Wr, int64_t T, int H, int E, in
   return MM_OK;
 }
 
+// ------------------------------------------------------------------ backward
+size_t mm_swiglu_ffn_backward_workspace_bytes(int64_t T, int H, int I, int dtype) {
+  if (T < 0 || H < 1 || I < 1 || dtype != kDtypeBF16) return 0;
+  return dense_bwd_layout(T, I).total;
+}
+
+static bool bwd_shape_ok(int H, int I) { return H % 64 == 0 && I % 64 == 0; }
+
+int mm_swiglu_ffn_backward(const void* x, const void* Wg, const void* Wu, const void* Wd,
+                           const void* dy, int64_t T, int H, int I, int dtype, void* dx,
+                           float* dWg, float* dWu, float* dWd, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (!valid_dtype(dtype) || T < 0 || H < 1 || I < 1) return MM_ERR_INVALID_ARG;
+  if (dtype != kDtypeBF16 || !bwd_shape_ok(H, I)) return MM_ERR_UNSUPPORTED;
+  if (T > (int64_t{1} << 30)) return MM_ERR_UNSUPPORTED;
+  if (!x || !Wg || !Wu || !Wd || !dy || !dx || !dWg || !dWu || !dWd) return MM_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, Wg, Wu, Wd, dy, dx, dWg, dWu, dWd};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MM_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return MM_ERR_WORKSPACE;
+  const DenseBwdLayout L = dense_bwd_layout(T, I);
+  if (workspace_bytes < L.total) return MM_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
+  if (T == 0) {
+    // no tokens: the weight gradients are zero
+    const size_t wb = 4 * static_cast<size_t>(H) * I;
+    for (float* q : {dWg, dWu, dWd}) {
+      cudaError_t e = cudaMemsetAsync(q, 0, wb, st);
+      if (e != cudaSuccess) return cuda_fail(e, "zero dW");
+    }
+    return MM_OK;
+  }
+  void* dh = ws_at(workspace, L.dh);
+  void* dgu = ws_at(workspace, L.dgu);
+  void* h = ws_at(workspace, L.h);
+  const int Ti = static_cast<int>(T);
+  // dh = dy Wd
+  const void* wd1[1] = {Wd};
+  cudaError_t e = counted_launch(MM_KERNEL_BWD_DGRAD, st, [&] {
+    return launch_bw_dgrad(dy, T, H, nullptr, 1, Ti, wd1, wd1, H / 64, I, dh, I, 0, hdr, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "bwd dh");
+  // g, u again; dG, dU, h
+  const void* wg1[1] = {Wg};
+  const void* wu1[1] = {Wu};
+  UpBwd ub{static_cast<const float*>(dh), nullptr, nullptr,
+           static_cast<__nv_bfloat16*>(dgu), static_cast<__nv_bfloat16*>(h), nullptr, 0};
+  GroupRows gr{nullptr, 1, Ti, 1};
+  e = counted_launch(MM_KERNEL_BWD_SWIGLU, st, [&] {
+    return launch_gateup_bwd_tc(x, T, H, I, gr, wg1, wu1, ub, hdr, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "bwd swiglu");
+  // dx = dG Wg + dU Wu
+  e = counted_launch(MM_KERNEL_BWD_DGRAD, st, [&] {
+    return launch_bw_dgrad(dgu, T, 2 * I, nullptr, 1, Ti, wg1, wu1, I / 64, H, dx, H, 1, hdr, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "bwd dx");
+  // dWd = dy^T h, dWg = dG^T x, dWu = dU^T x
+  const void* am[2] = {dy, dgu};
+  const int64_t ac[2] = {H, 2 * static_cast<int64_t>(I)};
+  const void* bm[2] = {h, x};
+  const int64_t bc[2] = {I, H};
+  const BwProblem pr[3] = {{dWd, H, I, 0, 0, 0, 0}, {dWg, I, H, 0, 1, 1, 0}, {dWu, I, H, 0, 1, 1, I}};
+  e = counted_launch(MM_KERNEL_BWD_WGRAD, st, [&] {
+    return launch_bw_wgrad(am, ac, 2, bm, bc, 2, T, pr, 3, nullptr, 1, Ti, hdr, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "bwd wgrad");
+  return MM_OK;
+}
+
+size_t mm_moe_backward_workspace_bytes(int64_t T, int H, int I, int E, int k, int dtype) {
+  if (T < 1 || H < 1 || I < 1 || E < 1 || E > MM_MAX_EXPERTS || k < 1 || k > E ||
+      k > MM_MAX_TOPK || dtype != kDtypeBF16)
+    return 0;
+  return moe_bwd_layout(T, H, I, E, k).total;
+}
+
+int mm_moe_backward(const void* x, const void* Wr, const void* const* Wg, const void* const* Wu,
+                    const void* const* Wd, int64_t T, int H, int I, int E, int k, float coef,
+                    int dtype, const int32_t* topk_idx, const float* topk_w,
+                    const float* router_probs, const float* router_lse, const void* dy,
+                    float d_aux, float z_coef, float d_z, void* dx, float* dWr,
+                    float* const* dWg, float* const* dWu, float* const* dWd, float* d_bias,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (!valid_dtype(dtype) || T < 1 || H < 1 || I < 1 || E < 1 || k < 1 || k > E)
+    return MM_ERR_INVALID_ARG;
+  if (E > MM_MAX_EXPERTS || k > MM_MAX_TOPK) return MM_ERR_UNSUPPORTED;
+  if (dtype != kDtypeBF16 || !bwd_shape_ok(H, I)) return MM_ERR_UNSUPPORTED;
+  if (T > (int64_t{1} << 30) / k) return MM_ERR_UNSUPPORTED;
+  if (!x || !Wr || !Wg || !Wu || !Wd || !topk_idx || !topk_w || !router_probs || !dy || !dx ||
+      !dWr || !dWg || !dWu || !dWd)
+    return MM_ERR_INVALID_ARG;
+  if (z_coef != 0.f && d_z != 0.f && router_lse == nullptr) return MM_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, Wr, dy, dx, dWr};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MM_ERR_INVALID_ARG;
+  for (int e = 0; e < E; ++e) {
+    const void* w[] = {Wg[e], Wu[e], Wd[e], dWg[e], dWu[e], dWd[e]};
+    for (const void* q : w)
+      if (!q || !aligned16(q)) return MM_ERR_INVALID_ARG;
+  }
+  auto a4 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 3u) == 0; };
+  if (!a4(topk_idx) || !a4(topk_w) || !a4(router_probs) || !a4(router_lse) || !a4(d_bias))
+    return MM_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return MM_ERR_WORKSPACE;
+  const MoeBwdLayout L = moe_bwd_layout(T, H, I, E, k);
+  if (workspace_bytes < L.total) return MM_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
+  auto i32 = [&](size_t off) { return reinterpret_cast<int32_t*>(ws_at(workspace, off)); };
+  auto f32 = [&](size_t off) { return reinterpret_cast<float*>(ws_at(workspace, off)); };
+  int32_t* offsets = i32(L.offsets);
+  void* xp = ws_at(workspace, L.xp);
+  void* dyp = ws_at(workspace, L.dyp);
+  void* dhu = ws_at(workspace, L.dhu);
+  void* dgu = ws_at(workspace, L.dgu);
+  void* ha = ws_at(workspace, L.ha);
+  const int nblk = route_blocks(T);
+  const int64_t R = L.rows;
+
+  // 1. group the assignments by expert (padded), gather x and dy rows
+  cudaError_t e = counted_launch(MM_KERNEL_BWD_ROUTER, st, [&] {
+    return launch_bwd_count(topk_idx, T, E, k, i32(L.blk_cnt), st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "bwd count");
+  const BwdDispatchOut dout{offsets, i32(L.counts), i32(L.perm), i32(L.pos), xp, dyp};
+  e = counted_launch(MM_KERNEL_BWD_ROUTER, st, [&] {
+    return launch_bwd_dispatch(x, dy, topk_idx, T, H, E, k, i32(L.blk_cnt), dout, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "bwd dispatch");
+  // 2. dhu = dy Wd_e (unscaled by alpha), per expert group
+  e = counted_launch(MM_KERNEL_BWD_DGRAD, st, [&] {
+    return launch_bw_dgrad(dyp, R, H, offsets, E, 0, Wd, Wd, H / 64, I, dhu, I, 0, hdr, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "bwd dhu");
+  // 3. g, u again: dG, dU, alpha h, dalpha partials
+  const UpBwd ub{static_cast<const float*>(dhu), i32(L.perm), topk_w,
+                 static_cast<__nv_bfloat16*>(dgu), static_cast<__nv_bfloat16*>(ha), f32(L.dpart),
+                 L.n_parts};
+  const GroupRows gr{offsets, E, 0, E};
+  e = counted_launch(MM_KERNEL_BWD_SWIGLU, st, [&] {
+    return launch_gateup_bwd_tc(xp, R, H, I, gr, Wg, Wu, ub, hdr, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "bwd swiglu");
+  // 4. per-assignment dx rows (fp32) = dG Wg_e + dU Wu_e
+  e = counted_launch(MM_KERNEL_BWD_DGRAD, st, [&] {
+    return launch_bw_dgrad(dgu, R, 2 * I, offsets, E, 0, Wg, Wu, I / 64, H, f32(L.dxp), H, 0, hdr,
+                           st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "bwd dxp");
+  // 5. weight gradients over each expert's rows
+  const void* am[2] = {dyp, dgu};
+  const int64_t ac[2] = {H, 2 * static_cast<int64_t>(I)};
+  const void* bm[2] = {ha, xp};
+  const int64_t bc[2] = {I, H};
+  BwProblem pr[kBwMaxGroups];
+  for (int q = 0; q < E; ++q) {
+    pr[3 * q + 0] = BwProblem{dWd[q], H, I, q, 0, 0, 0};
+    pr[3 * q + 1] = BwProblem{dWg[q], I, H, q, 1, 1, 0};
+    pr[3 * q + 2] = BwProblem{dWu[q], I, H, q, 1, 1, I};
+  }
+  e = counted_launch(MM_KERNEL_BWD_WGRAD, st, [&] {
+    return launch_bw_wgrad(am, ac, 2, bm, bc, 2, R, pr, 3 * E, offsets, E, 0, hdr, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "bwd wgrad");
+  // 6. router: dr, dx (slot-ordered sum + dr Wr), dWr / d_bias partials, then their sums
+  const RouterBwd rb{topk_idx, topk_w, router_probs, (z_coef != 0.f && d_z != 0.f) ? router_lse : nullptr,
+                     i32(L.counts), i32(L.pos), f32(L.dpart), L.n_parts, f32(L.dxp), coef, d_aux,
+                     z_coef, d_z, f32(L.dr), dx, f32(L.dwr_part), f32(L.dbias_part)};
+  e = counted_launch(MM_KERNEL_BWD_ROUTER, st, [&] {
+    return launch_router_bwd(x, Wr, T, H, E, k, rb, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "bwd router");
+  e = counted_launch(MM_KERNEL_BWD_ROUTER, st, [&] {
+    return launch_router_bwd_reduce(f32(L.dwr_part), f32(L.dbias_part), nblk, E, H, dWr, d_bias, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "bwd router reduce");
+  return MM_OK;
+}
+
 uint64_t mm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int mm_profile_start(int kernel_id, int max_launches) {
   switch (kernel_id) {
     case MM_KERNEL_ROUTER: case MM_KERNEL_DISPATCH: case MM_KERNEL_GATEUP: case MM_KERNEL_DOWN:
-    case MM_KERNEL_DECODE: break;
+    case MM_KERNEL_DECODE: case MM_KERNEL_BWD_DGRAD: case MM_KERNEL_BWD_SWIGLU:
+    case MM_KERNEL_BWD_WGRAD: case MM_KERNEL_BWD_ROUTER: break;
     default: return MM_ERR_INVALID_ARG;
   }
   if (max_launches < 1 || max_launches > 100000) return MM_ERR_INVALID_ARG;

@@ -1,0 +1,293 @@
+// Backward pass of the MoE layer outside the GEMMs: the dispatch of the
+// assignments into expert groups, and the router backward.
+//
+// The router gradient follows p-chao.com "MiniMind 学习笔记 08" §7 (the
+// selection has no gradient; the router learns through the selected
+// weights) and chapter 4 §4.4 of minimind3.com (in aux, the load f_e is not
+// differentiable, the mean probability P_e is):
+//   alpha_s = p_{S_s} / Z, Z = sum_S p + 1e-20
+//       dp_{S_s} += (dalpha_s - sum_j dalpha_j alpha_j) / Z
+//   aux = E coef sum_e (count_e / T)(sum_t p_{t,e} / T)
+//       dp_{t,e} += d_aux E coef count_e / T^2
+//   softmax:  dr_e = p_e (dp_e - sum_j p_j dp_j)
+//   z-loss = z_coef / T sum_t lse_t^2:  dr_e += d_z 2 z_coef lse_t p_e / T
+//   dx_t = sum_s dx_{t,s} (slot order) + sum_e dr_e Wr_e;  dWr = dr^T x;  d_bias = sum_t dr_t
+// Every sum runs in a fixed order; the results are deterministic.
+#include <algorithm>
+#include <cstring>
+
+#include "mm_kernels.cuh"
+
+namespace mm {
+
+constexpr int kBwdTok = 64;           // tokens per block (count, dispatch, router backward)
+constexpr int kBwdThreads = 256;
+
+__device__ __forceinline__ float bw_warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Per block of 64 tokens: assignments per expert.
+__global__ void __launch_bounds__(kBwdThreads)
+bwd_count_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int E, int k,
+                 int32_t* __restrict__ blk_cnt) {
+  __shared__ int cnt[MM_MAX_EXPERTS];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kBwdTok;
+  const int na = static_cast<int>(T - t0 < kBwdTok ? T - t0 : kBwdTok) * k;
+  for (int a = threadIdx.x; a < na; a += blockDim.x) atomicAdd(&cnt[topk_idx[t0 * k + a]], 1);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) blk_cnt[static_cast<int64_t>(blockIdx.x) * E + e] = cnt[e];
+}
+
+// Block b owns the assignments of tokens [64 b, 64 b + 64).  From every
+// block's counts it derives the expert totals, the padded group offsets
+// (each group starts on a multiple of kBwAlign rows) and its own base in
+// each group; an assignment's row is offset[e] + base[e] + its rank among
+// the block's assignments to e in (token, slot) order.  It writes perm /
+// pos and copies the x and dy rows; block 0 also writes offsets and counts
+// and zeroes the padding rows.
+template <typename Tin>
+__global__ void __launch_bounds__(kBwdThreads)
+bwd_dispatch_kernel(const Tin* __restrict__ x, const Tin* __restrict__ dy,
+                    const int32_t* __restrict__ topk_idx, int64_t T, int H, int E, int k,
+                    const int32_t* __restrict__ blk_cnt, BwdDispatchOut o) {
+  __shared__ int s_tot[MM_MAX_EXPERTS], s_base[MM_MAX_EXPERTS], s_off[MM_MAX_EXPERTS + 1];
+  __shared__ int s_run[MM_MAX_EXPERTS];
+  __shared__ int s_pos[kBwdTok * MM_MAX_TOPK];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x, nblk = gridDim.x;
+  const int64_t t0 = static_cast<int64_t>(b) * kBwdTok;
+  const int na = static_cast<int>(T - t0 < kBwdTok ? T - t0 : kBwdTok) * k;
+  // totals and this block's base per expert (thread e sums the blocks in order)
+  for (int e = tid; e < E; e += blockDim.x) {
+    int all = 0, before = 0;
+    for (int bb = 0; bb < nblk; ++bb) {
+      const int c = blk_cnt[static_cast<int64_t>(bb) * E + e];
+      all += c;
+      before += bb < b ? c : 0;
+    }
+    s_tot[e] = all;
+    s_base[e] = before;
+    s_run[e] = 0;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int e = 0; e < E; ++e) {
+      s_off[e] = run;
+      run += (s_tot[e] + kBwAlign - 1) / kBwAlign * kBwAlign;
+    }
+    s_off[E] = run;
+  }
+  __syncthreads();
+  // ranks: warp 0 walks the block's assignments 32 at a time in order
+  if (warp == 0) {
+    for (int base = 0; base < na; base += 32) {
+      const int a = base + lane;
+      const bool valid = a < na;
+      const int e = valid ? topk_idx[t0 * k + a] : MM_MAX_EXPERTS + lane;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const unsigned below = peers & ((1u << lane) - 1u);
+      const int prior = valid ? s_run[e] : 0;
+      __syncwarp();
+      if (valid) {
+        s_pos[a] = s_off[e] + s_base[e] + prior + __popc(below);
+        if (below == 0u) s_run[e] = prior + __popc(peers);
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  for (int a = tid; a < na; a += blockDim.x) {
+    o.perm[s_pos[a]] = static_cast<int32_t>(t0 * k + a);
+    o.pos[t0 * k + a] = s_pos[a];
+  }
+  // rows: a warp per assignment, 16-byte vectors
+  constexpr int kVec = 16 / sizeof(Tin);
+  const int nv = H / kVec;
+  for (int a = warp; a < na; a += kBwdThreads / 32) {
+    const int64_t t = t0 + a / k;
+    const uint4* sx = reinterpret_cast<const uint4*>(x + t * H);
+    const uint4* sd = reinterpret_cast<const uint4*>(dy + t * H);
+    uint4* dx4 = reinterpret_cast<uint4*>(static_cast<Tin*>(o.xp) + static_cast<int64_t>(s_pos[a]) * H);
+    uint4* dd4 = reinterpret_cast<uint4*>(static_cast<Tin*>(o.dyp) + static_cast<int64_t>(s_pos[a]) * H);
+    for (int v = lane; v < nv; v += 32) {
+      dx4[v] = sx[v];
+      dd4[v] = sd[v];
+    }
+  }
+  if (b == 0) {
+    for (int e = tid; e <= E; e += blockDim.x) o.offsets[e] = s_off[e];
+    for (int e = tid; e < E; e += blockDim.x) o.counts[e] = s_tot[e];
+    // padding rows of every group: zero x and dy rows, perm -1
+    for (int e = 0; e < E; ++e) {
+      const int p0 = s_off[e] + s_tot[e], p1 = s_off[e + 1];
+      for (int r = p0 + warp; r < p1; r += kBwdThreads / 32) {
+        if (lane == 0) o.perm[r] = -1;
+        uint4* dx4 = reinterpret_cast<uint4*>(static_cast<Tin*>(o.xp) + static_cast<int64_t>(r) * H);
+        uint4* dd4 = reinterpret_cast<uint4*>(static_cast<Tin*>(o.dyp) + static_cast<int64_t>(r) * H);
+        for (int v = lane; v < nv; v += 32) {
+          dx4[v] = make_uint4(0u, 0u, 0u, 0u);
+          dd4[v] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+    }
+  }
+}
+
+// Router backward, one block per 64 tokens, one warp per token at a time
+// (lane l holds experts l and l + 32).  Writes dr [T, E], dx [T, H] (the k
+// per-assignment rows in slot order plus dr Wr), and the block's partials of
+// dWr = dr^T x and d_bias = sum_t dr_t.
+template <typename Tin>
+__global__ void __launch_bounds__(kBwdThreads)
+router_bwd_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, int64_t T, int H, int E,
+                  int k, const RouterBwd rb) {
+  extern __shared__ float s_dr[];              // [64][E] this block's dr
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kWarps = kBwdThreads / 32;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kBwdTok;
+  const int ntok = static_cast<int>(T - t0 < kBwdTok ? T - t0 : kBwdTok);
+  const float invT = 1.0f / static_cast<float>(T);
+  const bool v0 = lane < E, v1 = lane + 32 < E;
+  const float aux0 = v0 ? rb.d_aux * static_cast<float>(E) * rb.coef * static_cast<float>(rb.counts[lane]) * invT * invT : 0.f;
+  const float aux1 = v1 ? rb.d_aux * static_cast<float>(E) * rb.coef * static_cast<float>(rb.counts[lane + 32]) * invT * invT : 0.f;
+  for (int tl = warp; tl < ntok; tl += kWarps) {
+    const int64_t t = t0 + tl;
+    const float p0 = v0 ? rb.probs[t * E + lane] : 0.f;
+    const float p1 = v1 ? rb.probs[t * E + lane + 32] : 0.f;
+    float dp0 = aux0, dp1 = aux1;
+    // dalpha_s = sum of the row's partials (lane-strided, then a fixed tree)
+    float Z = 0.f, c = 0.f;
+    float da[MM_MAX_TOPK];
+#pragma unroll
+    for (int s = 0; s < MM_MAX_TOPK; ++s) {
+      da[s] = 0.f;
+      if (s < k) {
+        const float* part = rb.dalpha_part + static_cast<int64_t>(rb.pos[t * k + s]) * rb.n_parts;
+        float v = 0.f;
+        for (int j = lane; j < rb.n_parts; j += 32) v += part[j];
+        da[s] = bw_warp_sum(v);
+        const int e = rb.topk_idx[t * k + s];
+        Z += __shfl_sync(0xffffffffu, e < 32 ? p0 : p1, e & 31);
+        c = fmaf(da[s], rb.topk_w[t * k + s], c);
+      }
+    }
+    Z += 1e-20f;
+#pragma unroll
+    for (int s = 0; s < MM_MAX_TOPK; ++s) {
+      if (s < k) {
+        const int e = rb.topk_idx[t * k + s];
+        const float g = (da[s] - c) / Z;
+        if (e == lane) dp0 += g;
+        if (e == lane + 32) dp1 += g;
+      }
+    }
+    const float S = bw_warp_sum(p0 * dp0 + p1 * dp1);
+    float dr0 = p0 * (dp0 - S), dr1 = p1 * (dp1 - S);
+    if (rb.lse != nullptr) {
+      const float zf = rb.d_z * 2.0f * rb.z_coef * rb.lse[t] * invT;
+      dr0 = fmaf(zf, p0, dr0);
+      dr1 = fmaf(zf, p1, dr1);
+    }
+    if (v0) { rb.dr[t * E + lane] = dr0; s_dr[tl * E + lane] = dr0; }
+    if (v1) { rb.dr[t * E + lane + 32] = dr1; s_dr[tl * E + lane + 32] = dr1; }
+    __syncwarp();
+    // dx_t = sum_s dxp[pos(t, s)] (slot order) + sum_e dr_e Wr_e
+    for (int h = lane * 4; h < H; h += 128) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = 0; s < k; ++s) {
+        const float4 v = *reinterpret_cast<const float4*>(rb.dxp + static_cast<int64_t>(rb.pos[t * k + s]) * H + h);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      for (int e = 0; e < E; ++e) {
+        const float d = s_dr[tl * E + e];
+        const Tin* w = Wr + static_cast<int64_t>(e) * H + h;
+        acc.x = fmaf(d, static_cast<float>(w[0]), acc.x);
+        acc.y = fmaf(d, static_cast<float>(w[1]), acc.y);
+        acc.z = fmaf(d, static_cast<float>(w[2]), acc.z);
+        acc.w = fmaf(d, static_cast<float>(w[3]), acc.w);
+      }
+      Tin* out = static_cast<Tin*>(rb.dx) + t * H + h;
+      out[0] = static_cast<Tin>(acc.x);
+      out[1] = static_cast<Tin>(acc.y);
+      out[2] = static_cast<Tin>(acc.z);
+      out[3] = static_cast<Tin>(acc.w);
+    }
+  }
+  __syncthreads();
+  // the block's dWr partial: element (e, h) = sum_t dr[t][e] x[t][h], token order
+  for (int i = tid; i < E * H; i += blockDim.x) {
+    const int e = i / H, h = i - e * H;
+    float acc = 0.f;
+    for (int tl = 0; tl < ntok; ++tl) acc = fmaf(s_dr[tl * E + e], static_cast<float>(x[(t0 + tl) * H + h]), acc);
+    rb.dwr_part[static_cast<int64_t>(blockIdx.x) * E * H + i] = acc;
+  }
+  for (int e = tid; e < E; e += blockDim.x) {
+    float acc = 0.f;
+    for (int tl = 0; tl < ntok; ++tl) acc += s_dr[tl * E + e];
+    rb.dbias_part[static_cast<int64_t>(blockIdx.x) * E + e] = acc;
+  }
+}
+
+// dWr[e][h] = sum_b dwr_part[b][e][h] and d_bias[e] = sum_b dbias_part[b][e],
+// blocks in order.
+__global__ void router_bwd_reduce_kernel(const float* __restrict__ dwr_part,
+                                         const float* __restrict__ dbias_part, int nblk, int E,
+                                         int H, float* __restrict__ dWr, float* __restrict__ d_bias) {
+  const int64_t n = static_cast<int64_t>(E) * H;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n + E;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float acc = 0.f;
+    if (i < n) {
+      for (int b = 0; b < nblk; ++b) acc += dwr_part[static_cast<int64_t>(b) * n + i];
+      dWr[i] = acc;
+    } else if (d_bias != nullptr) {
+      const int e = static_cast<int>(i - n);
+      for (int b = 0; b < nblk; ++b) acc += dbias_part[static_cast<int64_t>(b) * E + e];
+      d_bias[e] = acc;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- launchers
+static int bwd_blocks(int64_t T) { return static_cast<int>((T + kBwdTok - 1) / kBwdTok); }
+
+cudaError_t launch_bwd_count(const int32_t* topk_idx, int64_t T, int E, int k, int32_t* blk_cnt,
+                             cudaStream_t st) {
+  bwd_count_kernel<<<bwd_blocks(T), kBwdThreads, 0, st>>>(topk_idx, T, E, k, blk_cnt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dispatch(const void* x, const void* dy, const int32_t* topk_idx, int64_t T,
+                                int H, int E, int k, const int32_t* blk_cnt,
+                                const BwdDispatchOut& o, cudaStream_t st) {
+  if (H % 8 != 0) return cudaErrorInvalidValue;
+  bwd_dispatch_kernel<__nv_bfloat16><<<bwd_blocks(T), kBwdThreads, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(dy), topk_idx, T, H,
+      E, k, blk_cnt, o);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_bwd(const void* x, const void* Wr, int64_t T, int H, int E, int k,
+                              const RouterBwd& rb, cudaStream_t st) {
+  if (H % 4 != 0) return cudaErrorInvalidValue;
+  const size_t smem = static_cast<size_t>(kBwdTok) * E * sizeof(float);
+  router_bwd_kernel<__nv_bfloat16><<<bwd_blocks(T), kBwdThreads, smem, st>>>(
+      static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(Wr), T, H, E, k, rb);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_bwd_reduce(const float* dwr_part, const float* dbias_part, int nblk,
+                                     int E, int H, float* dWr, float* d_bias, cudaStream_t st) {
+  const int64_t n = static_cast<int64_t>(E) * H + E;
+  const int grid = static_cast<int>(std::min<int64_t>((n + 255) / 256, 1024));
+  router_bwd_reduce_kernel<<<grid, 256, 0, st>>>(dwr_part, dbias_part, nblk, E, H, dWr, d_bias);
+  return cudaGetLastError();
+}
+
+}  // namespace mm

@@ -31,6 +31,9 @@ namespace mm {
 
 // ------------------------------------------------------------------ geometry
 constexpr int kOpUp = 0, kOpDown = 1;
+// The gate/up GEMM run again in the backward pass: same operands and tiles,
+// an epilogue that differentiates the SwiGLU (UpBwd) instead of storing h.
+constexpr int kOpUpBwd = 2;
 // Smallest magnitude that rounds to infinity in fp16 (65504 + half an ulp).
 constexpr float kF16Overflow = 65520.0f;
 constexpr int kPairM = 2 * kTcBM;                        // rows per tile pair
@@ -66,6 +69,7 @@ static_assert(kSmem <= 232448, "shared memory budget");
 
 template <int OP> struct OpTraits;
 template <> struct OpTraits<kOpUp> { static constexpr int kOutCols = kN / 2, kKb = 2; };
+template <> struct OpTraits<kOpUpBwd> { static constexpr int kOutCols = kN / 2, kKb = 2; };
 template <> struct OpTraits<kOpDown> { static constexpr int kOutCols = kN, kKb = 1; };
 
 template <int MAXW>
@@ -176,6 +180,84 @@ __device__ __forceinline__ bool epilogue_up(uint32_t tb, const TileInfo& ti, int
     }
   }
   return out_of_range && valid;
+}
+
+// gate/up of the backward: the warp's 32 rows x 64 columns (half `half` of
+// the tile's 128) of g and u from TMEM; per element, with s = sigmoid(g):
+//   h = g s u;  dalpha += h * dhu;  dh = alpha dhu;  dU = dh g s;
+//   dG = dh u s (1 + g (1 - s))
+// (the chain rule through lesson 13 §0's h = SiLU(g) ⊙ u).  dG, dU and
+// alpha h go out as bf16, 64 contiguous bytes per row and piece; the row's
+// dalpha partial over these 64 columns goes to dalpha_part[row][2 nb + half].
+// Every lane takes part in the TMEM loads (warp-collective); only the rows
+// of the group (`valid`) read dhu and store.
+__device__ __forceinline__ void epilogue_up_bwd(uint32_t tb, const TileInfo& ti, int I, int row,
+                                                int half, const UpBwd& ub) {
+  const bool valid = row < ti.rows;              // else: past the group, the next group's row
+  const int64_t r = ti.row0 + (valid ? row : 0);
+  float alpha = 1.0f;
+  if (valid && ub.perm != nullptr) {
+    const int a = ub.perm[r];
+    alpha = a >= 0 ? ub.topk_w[a] : 0.0f;        // padding rows: zero gradient
+  }
+  const int col0 = ti.n0 + half * 64;
+  float dpart = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < 2; ++c) {
+    const int col = col0 + c * 32;
+    const int tcol = half * 64 + c * 32;         // TMEM column of g; u is kN/2 further
+    uint32_t gr[32], ur[32];
+    tmem_ld_32x32b_x32(tb + tcol, gr);
+    tmem_ld_32x32b_x32(tb + kN / 2 + tcol, ur);
+    tmem_ld_wait();
+    if (col >= I) continue;                      // warp-uniform
+    float dv[32];
+#pragma unroll
+    for (int q = 0; q < 32; ++q) dv[q] = 0.f;
+    if (valid) {
+      const float4* dsrc = reinterpret_cast<const float4*>(ub.dhu + r * I + col);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 v = dsrc[q];
+        dv[4 * q] = v.x; dv[4 * q + 1] = v.y; dv[4 * q + 2] = v.z; dv[4 * q + 3] = v.w;
+      }
+    }
+    uint32_t pg[16], pu[16], ph[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float o_g[2], o_u[2], o_h[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float g = __uint_as_float(gr[2 * j + e]);
+        const float u = __uint_as_float(ur[2 * j + e]);
+        const float d = dv[2 * j + e];
+        const float sg = 1.0f / (1.0f + __expf(-g));
+        const float silu = g * sg;
+        const float h = silu * u;
+        dpart = fmaf(h, d, dpart);
+        const float dh = alpha * d;
+        o_u[e] = dh * silu;
+        o_g[e] = dh * u * (sg * (1.0f + g * (1.0f - sg)));
+        o_h[e] = alpha * h;
+      }
+      pg[j] = pack_bf16x2(o_g[0], o_g[1]);
+      pu[j] = pack_bf16x2(o_u[0], o_u[1]);
+      ph[j] = pack_bf16x2(o_h[0], o_h[1]);
+    }
+    if (valid) {
+      uint4* dg = reinterpret_cast<uint4*>(ub.dgu + r * (2 * static_cast<int64_t>(I)) + col);
+      uint4* du = reinterpret_cast<uint4*>(ub.dgu + r * (2 * static_cast<int64_t>(I)) + I + col);
+      uint4* dh4 = reinterpret_cast<uint4*>(ub.ha + r * I + col);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        dg[q] = make_uint4(pg[4 * q], pg[4 * q + 1], pg[4 * q + 2], pg[4 * q + 3]);
+        du[q] = make_uint4(pu[4 * q], pu[4 * q + 1], pu[4 * q + 2], pu[4 * q + 3]);
+        dh4[q] = make_uint4(ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]);
+      }
+    }
+  }
+  if (valid && ub.dalpha_part != nullptr)
+    ub.dalpha_part[r * ub.n_parts + (ti.n0 / (kN / 2)) * 2 + half] = dpart;
 }
 
 // down: 128 y columns (half `half` of the tile's 256) of the warp's 32 rows,
@@ -415,10 +497,11 @@ template <int OP, int MAXW, int NW = kN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g, const int K,
                     const int NCOLS, __half* __restrict__ hout, const DownEpilogue ep,
-                    const WdConvert cv, WsHeader* hdr, const int dep_mainloop) {
+                    const WdConvert cv, WsHeader* hdr, const int dep_mainloop, const UpBwd ub) {
   static_assert(NW == kN || (OP == kOpDown && NW == kNWide), "tile width");
   constexpr bool kWide = NW == kNWide;
-  constexpr int kOutCols = OP == kOpUp ? OpTraits<OP>::kOutCols : NW;
+  constexpr bool kUpLike = OP != kOpDown;       // gate/up tiles (forward or backward)
+  constexpr int kOutCols = kUpLike ? OpTraits<OP>::kOutCols : NW;
   constexpr int kHC = NW / 2;                     // down: columns per epilogue warp half
   extern __shared__ unsigned char smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -426,7 +509,7 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
   constexpr int kKbStage = OpTraits<OP>::kKb;
   constexpr int kStages = (kWide ? kRingKbWide : kRingKb) / kKbStage;
   constexpr int kAStage = kKbStage * kATile;
-  constexpr int kBTileK = (OP == kOpUp ? kN / 2 : NW / 2) * kTcBK * 2;   // B rows of this CTA, one k-block
+  constexpr int kBTileK = (kUpLike ? kN / 2 : NW / 2) * kTcBK * 2;   // B rows of this CTA, one k-block
   constexpr int kBStage = kKbStage * kBTileK;
   uint8_t* sB = smem + kStages * kAStage;
   uint8_t* sEpi = sB + kStages * kBStage;
@@ -495,11 +578,11 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
       for (int tile = cluster; ok && tile < total; tile += n_clusters) {
         const TileInfo ti = decode_tile(tile, s_off, s_tstart, g.G, g.n_weights, n_tiles,
                                         kOutCols, static_cast<int>(rank));
-        const CUtensorMap* bmap = (OP == kOpUp && rank == 1) ? &P.b1[ti.w] : &P.b0[ti.w];
+        const CUtensorMap* bmap = (kUpLike && rank == 1) ? &P.b1[ti.w] : &P.b0[ti.w];
         // wide tile: this CTA's B rows are two boxes of 96, Wd rows
         // n0 + 96 rank .. and n0 + 192 + 96 rank .., so that the first MMA
         // (N = 192) yields y columns n0 .. n0 + 191 and the second the rest
-        const int bcoord = (OP == kOpUp) ? ti.n0
+        const int bcoord = kUpLike ? ti.n0
                                          : ti.n0 + static_cast<int>(rank) * (kWide ? kHC / 2 : kHC);
         for (int kb = 0; kb < nkb; kb += kKbStage, ++it) {
           const int s = it % kStages;
@@ -526,7 +609,7 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
   } else if (warp == kWarpMma) {
     // ------------------------------------------------ MMA issuer (even CTA)
     if (rank == 0 && lane == 0) {
-      constexpr uint32_t idesc = (OP == kOpUp) ? idesc_bf16_f32(kPairM, kN)
+      constexpr uint32_t idesc = kUpLike ? idesc_bf16_f32(kPairM, kN)
                                  : idesc_f16_f32(kPairM, kWide ? NW / 2 : NW);
       int it = 0, local = 0;
       bool ok = true;
@@ -627,6 +710,8 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
       const uint32_t tb = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * kAccStride;
       if constexpr (OP == kOpUp)
         range_bad |= epilogue_up(tb, ti, NCOLS, hout, row, half, wstage, &P.out);
+      else if constexpr (OP == kOpUpBwd)
+        epilogue_up_bwd(tb, ti, NCOLS, row, half, ub);
       else if (ep.perm == nullptr && ep.mode == kCombineStore && (row | 31) < ti.rows)
         epilogue_down_dense<kHC>(tb, ti, NCOLS, half, lane, ti.row0 + (row & ~31), wstage, &P.out);
       else
@@ -823,7 +908,37 @@ static cudaError_t gateup_impl(const void* A, int64_t a_rows, int H, int I, cons
   const int n_tiles = (I + kN / 2 - 1) / (kN / 2);
   DownEpilogue none{};
   return launch_pdl(fn, 2 * clusters_for(a_rows, g, n_tiles), kSmem, st, p, g, H, I,
-                    static_cast<__half*>(h_out), none, cv, hdr, 1);
+                    static_cast<__half*>(h_out), none, cv, hdr, 1, UpBwd{});
+}
+
+template <int MAXW>
+static cudaError_t gateup_bwd_impl(const void* A, int64_t a_rows, int H, int I, const GroupRows& g,
+                                   const void* const* Wg, const void* const* Wu, const UpBwd& ub,
+                                   WsHeader* hdr, cudaStream_t st) {
+  TcParams<MAXW> p;
+  memset(&p, 0, sizeof(p));
+  constexpr int kb = OpTraits<kOpUpBwd>::kKb;
+  if (!kblock_map(&p.a, A, H, a_rows, kTcBM, false, kb)) return cudaErrorInvalidValue;
+  for (int e = 0; e < g.n_weights; ++e) {
+    if (!kblock_map(&p.b0[e], Wg[e], H, I, kN / 2, false, kb)) return cudaErrorInvalidValue;
+    if (!kblock_map(&p.b1[e], Wu[e], H, I, kN / 2, false, kb)) return cudaErrorInvalidValue;
+  }
+  auto fn = grouped_gemm_kernel<kOpUpBwd, MAXW>;
+  cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), kSmem);
+  if (err != cudaSuccess) return err;
+  const int n_tiles = (I + kN / 2 - 1) / (kN / 2);
+  DownEpilogue none{};
+  WdConvert no_cv{};
+  return launch_pdl(fn, 2 * clusters_for(a_rows, g, n_tiles), kSmem, st, p, g, H, I,
+                    static_cast<__half*>(nullptr), none, no_cv, hdr, 1, ub);
+}
+
+cudaError_t launch_gateup_bwd_tc(const void* A, int64_t a_rows, int H, int I, const GroupRows& g,
+                                 const void* const* Wg, const void* const* Wu, const UpBwd& ub,
+                                 WsHeader* hdr, cudaStream_t st) {
+  if (I % 64 != 0) return cudaErrorInvalidValue;
+  if (g.n_weights <= 8) return gateup_bwd_impl<8>(A, a_rows, H, I, g, Wg, Wu, ub, hdr, st);
+  return gateup_bwd_impl<MM_MAX_EXPERTS>(A, a_rows, H, I, g, Wg, Wu, ub, hdr, st);
 }
 
 template <int MAXW>
@@ -858,7 +973,7 @@ static cudaError_t down_impl(const void* h, int64_t a_rows, int H, int I, const 
   const int dep = (ep.mode == kCombineAccum || ep.mode == kCombineLast) ? 0 : 1;
   WdConvert no_cv{};
   return launch_pdl(fn, 2 * clusters_for(a_rows, g, n_tiles), smem, st, p, g, I, H,
-                    static_cast<__half*>(nullptr), ep, no_cv, hdr, dep);
+                    static_cast<__half*>(nullptr), ep, no_cv, hdr, dep, UpBwd{});
 }
 
 cudaError_t launch_gateup_tc(const void* A, int64_t a_rows, int H, int I, const GroupRows& g,

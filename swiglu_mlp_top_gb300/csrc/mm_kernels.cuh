@@ -184,6 +184,104 @@ cudaError_t launch_decode_sw(const void* x, const void* Wg, const void* Wu, cons
 
 cudaError_t launch_watchdog_selftest(WsHeader* hdr, uint32_t limit_us, cudaStream_t st);
 
+// ----------------------------------------------------------- backward pass
+// Tensor-core GEMMs of the backward (gemm_bwd.cu).  kSchedRows: row groups
+// of a K-major A (dgrad: dh = dy Wd, dx = [dG | dU] [Wg; Wu]); kSchedKGrp:
+// weight gradients whose K runs over a group's rows (A and B MN-major).
+constexpr int kSchedRows = 0, kSchedKGrp = 1;
+constexpr int kBwMaxMaps = 2;                            // A matrices of the K-grouped GEMM
+constexpr int kBwMaxGroups = 3 * MM_MAX_EXPERTS;         // problems (K-grouped) / groups (rows)
+
+// One weight gradient: out [M, N] fp32 = A[:, a_col0 .. a_col0 + M)^T B over
+// the rows of group grp; A = a_map-th A matrix, B = b_map-th B matrix.
+struct BwProblem {
+  float* out;
+  int M, N;
+  int grp;
+  int a_map, b_map;
+  int a_col0;
+};
+
+struct BwParams {
+  CUtensorMap a[kBwMaxMaps];            // rows: A [rows, K] (box 64 x 128); K-grouped: A matrices (64 x 64)
+  CUtensorMap b_lo[MM_MAX_EXPERTS];     // rows: per group, B for k-blocks < kb_split; K-grouped: B matrices
+  CUtensorMap b_hi[MM_MAX_EXPERTS];     // rows: per group, B for k-blocks >= kb_split
+  BwProblem prob[kBwMaxGroups];         // K-grouped problems
+  const int32_t* offsets;               // group row offsets [G+1] (rows) / [n_groups+1], or null
+  int G;                                // groups (rows) / problems (K-grouped)
+  int n_groups;                         // K-grouped: groups of rows
+  int dense_rows;                       // offsets == null: one group [0, dense_rows)
+  int K, N, kb_split;                   // rows schedule
+  void* out;                            // rows schedule: [rows, ldo]
+  int64_t ldo;
+  int out_bf16;
+};
+
+cudaError_t launch_bw_dgrad(const void* A, int64_t a_rows, int K, const int32_t* offsets, int G,
+                            int dense_rows, const void* const* b_lo, const void* const* b_hi,
+                            int kb_split, int N, void* out, int64_t ldo, int out_bf16,
+                            WsHeader* hdr, cudaStream_t st);
+cudaError_t launch_bw_wgrad(const void* const* a_mats, const int64_t* a_cols, int n_a,
+                            const void* const* b_mats, const int64_t* b_cols, int n_b,
+                            int64_t k_rows, const BwProblem* probs, int n_probs,
+                            const int32_t* offsets, int n_groups, int dense_rows, WsHeader* hdr,
+                            cudaStream_t st);
+
+// Epilogue of the gate/up GEMM run again in the backward (recomputing g and
+// u): with dhu = dy Wd (unscaled by alpha) of the row, alpha of the row,
+//   h = SiLU(g) u;  dalpha partial = sum over the tile's columns of h * dhu;
+//   dh = alpha dhu;  dU = dh SiLU(g);  dG = dh u SiLU'(g);  out: dG | dU, alpha h.
+struct UpBwd {
+  const float* dhu;           // [rows, I] fp32 (not an MMA operand: kept unrounded)
+  const int32_t* perm;        // row -> assignment t*k + s, -1 for padding; null: alpha = 1
+  const float* topk_w;        // [T*k] alpha
+  __nv_bfloat16* dgu;         // [rows, 2I]: dG in columns [0, I), dU in [I, 2I)
+  __nv_bfloat16* ha;          // [rows, I]: alpha * h
+  float* dalpha_part;         // [rows, n_parts] or null
+  int n_parts;                // 2 * ceil(I / 128)
+};
+cudaError_t launch_gateup_bwd_tc(const void* A, int64_t a_rows, int H, int I, const GroupRows& g,
+                                 const void* const* Wg, const void* const* Wu, const UpBwd& ub,
+                                 WsHeader* hdr, cudaStream_t st);
+
+// Backward dispatch and router backward (backward.cu).  Rows of the backward
+// are grouped by expert (token order, then slot), each group starting on a
+// multiple of 64 rows; padding rows are zero in Xp and dYp and have perm -1.
+constexpr int kBwAlign = 64;
+cudaError_t launch_bwd_count(const int32_t* topk_idx, int64_t T, int E, int k, int32_t* blk_cnt,
+                             cudaStream_t st);
+struct BwdDispatchOut {
+  int32_t* offsets;           // [E + 1] padded group offsets
+  int32_t* counts;            // [E] assignments per expert
+  int32_t* perm;              // [rows_pad] row -> assignment, -1 padding
+  int32_t* pos;               // [T*k] assignment -> row
+  void* xp;                   // [rows_pad, H] x rows
+  void* dyp;                  // [rows_pad, H] dy rows
+};
+cudaError_t launch_bwd_dispatch(const void* x, const void* dy, const int32_t* topk_idx, int64_t T,
+                                int H, int E, int k, const int32_t* blk_cnt,
+                                const BwdDispatchOut& o, cudaStream_t st);
+struct RouterBwd {
+  const int32_t* topk_idx;    // [T, k]
+  const float* topk_w;        // [T, k] alpha
+  const float* probs;         // [T, E]
+  const float* lse;           // [T] or null (z term off)
+  const int32_t* counts;      // [E]
+  const int32_t* pos;         // [T*k]
+  const float* dalpha_part;   // [rows_pad, n_parts]
+  int n_parts;
+  const float* dxp;           // [rows_pad, H] fp32 per-assignment dx
+  float coef, d_aux, z_coef, d_z;
+  float* dr;                  // [T, E] out: dL/dlogits
+  void* dx;                   // [T, H] out, x's dtype
+  float* dwr_part;            // [nblk, E, H] out
+  float* dbias_part;          // [nblk, E] out
+};
+cudaError_t launch_router_bwd(const void* x, const void* Wr, int64_t T, int H, int E, int k,
+                              const RouterBwd& rb, cudaStream_t st);
+cudaError_t launch_router_bwd_reduce(const float* dwr_part, const float* dbias_part, int nblk,
+                                     int E, int H, float* dWr, float* d_bias, cudaStream_t st);
+
 // Workspace of the path that `path` (AUTO: the automatic choice) resolves to
 // for a dense call of this shape; 0 when that path does not take it.
 size_t dense_workspace_for_path(int64_t T, int H, int I, int dtype, int path);
