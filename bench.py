@@ -507,13 +507,58 @@ def make_step(w, dev):
     return Step(w, dev, n_sets)
 
 
+class BwdStep(Step):
+    """One backward pass of the workload (mm_swiglu_ffn_backward /
+    mm_moe_backward) on device inputs: an upstream gradient dy per input
+    set; the MoE backward takes the routing its forward saved (run once per
+    set before timing)."""
+
+    def __init__(self, w, dev, n_sets):
+        super().__init__(w, dev, n_sets)
+        gen = torch.Generator().manual_seed(123)
+        dy = torch.randn(w.T, w.H, generator=gen).to(torch.bfloat16)
+        self.saved = []
+        for s in self.sets:
+            s["dy"] = dy.to(dev)
+            if w.kind == "moe":
+                st = {}
+                _, idx, tw, _ = self.mm.moe_forward(s["x"], s["Wr"], s["Wg"], s["Wu"], s["Wd"],
+                                                    w.k, w.coef, logit_bias=s.get("logit_bias"),
+                                                    stats=st)
+                self.saved.append((idx, tw, st))
+        from swiglu_mlp_top_gb300 import _lib as L
+        if w.kind == "moe":
+            nbytes = L.load().mm_moe_backward_workspace_bytes(w.T, w.H, w.I, w.E, w.k,
+                                                              L.MM_DTYPE_BF16)
+        else:
+            nbytes = L.load().mm_swiglu_ffn_backward_workspace_bytes(w.T, w.H, w.I,
+                                                                     L.MM_DTYPE_BF16)
+        self.ws = self.mm.new_workspace(nbytes, dev)
+        self.y = self.sets[0]["x"]
+        self.idx = None
+
+    def __call__(self, i, x=None, outs=None):
+        s = self.sets[i % len(self.sets)]
+        if self.w.kind == "moe":
+            idx, tw, st = self.saved[i % len(self.sets)]
+            self.mm.moe_backward(s["x"], s["Wr"], s["Wg"], s["Wu"], s["Wd"], self.w.k,
+                                 self.w.coef, idx, tw, st["probs"], s["dy"], lse=st["lse"],
+                                 workspace=self.ws)
+        else:
+            self.mm.swiglu_ffn_backward(s["x"], s["Wg"], s["Wu"], s["Wd"], s["dy"],
+                                        workspace=self.ws)
+
+
 #: Workloads measured after the headline one, one entry each in the line's
 #: per_workload object (each the configuration a parity test covers).
 PER_WORKLOADS = ["dense_t4096", "dense_t100", "moe_e4k1_t8192"] + \
-    [f"decode_{kind}_t{T}" for kind in ("dense", "moe_e8k2") for T in (1, 4, 16, 64)]
+    [f"decode_{kind}_t{T}" for kind in ("dense", "moe_e8k2") for T in (1, 4, 16, 64)] + \
+    ["backward:dense_t4096", "backward:moe_e4k1_t8192", "backward:moe_e8k2_t16384_skew"]
 
 
 def per_workload_entry(name, lib, ws, local, dev, warmup):
+    if name.startswith("backward:"):
+        return backward_entry(WORKLOADS[name.split(":", 1)[1]], lib, ws, local, dev, warmup)
     w = WORKLOADS[name]
     step = make_step(w, dev)
     use_graph = streams_weights(w)
@@ -543,6 +588,46 @@ def per_workload_entry(name, lib, ws, local, dev, warmup):
                                                ("kernel", "bound", "achieved", "peak", "unit",
                                                 "frac", "kernel_ms")},
            "clocks": m["clocks"], "l2": workload_config(w, ws)["l2"]}
+    del step
+    torch.cuda.empty_cache()
+    return out
+
+
+def backward_entry(w, lib, ws, local, dev, warmup):
+    """The backward pass of a prefill workload: tokens/s, TFLOP/s over the
+    algorithmic 12*H*I flops per assignment (dh, dx and the three weight
+    gradients; the recomputed gate/up is extra work, not counted), and the
+    weight-gradient GEMM (6*H*I per assignment) against the bf16 peak."""
+    n_sets, _, _ = l2_rotation(w)
+    step = BwdStep(w, dev, n_sets)
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(5):
+        step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    est = e0.elapsed_time(e1) / 5
+    steps = int(min(200, max(5, 20.0 / max(est, 1e-3))))
+    m = measure(step, lib, steps, warmup, ws, local, False, 10)   # MM_KERNEL_BWD_WGRAD
+    flops = float(w.T) * w.k * 12.0 * w.H * w.I
+    wg_flops = float(w.T) * w.k * 6.0 * w.H * w.I
+    peaks, src = measured_peaks()
+    achieved = wg_flops / (m["kernel_ms"] / 1e3) / 1e12
+    out = {"ms_per_step": m["ms_per_step"], "tokens_per_s": ws * w.T / (m["ms_per_step"] / 1e3),
+           "tflops": flops / (m["ms_per_step"] / 1e3) / 1e12,
+           "frac_of_bf16_peak_whole_step": flops / (m["ms_per_step"] / 1e3) / 1e12
+           / peaks["bf16_tflops"],
+           "steps_per_region": steps, "repeats": m["repeats"], "timed_s": m["timed_s"],
+           "region_ms_min": m["region_ms_min"], "region_ms_max": m["region_ms_max"],
+           "timing": m["timing"],
+           "roofline": {"kernel": "bw_gemm_kernel<K-grouped> (weight gradients)", "bound": "tensor",
+                        "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                        "frac": achieved / peaks["bf16_tflops"], "kernel_ms": m["kernel_ms"]},
+           "clocks": m["clocks"], "l2": workload_config(w, ws)["l2"],
+           "flops_note": "12*H*I per assignment (2x the forward's GEMMs)"}
     del step
     torch.cuda.empty_cache()
     return out
@@ -661,7 +746,8 @@ def run_our_arm(args, w):
     per = None
     if not args.no_per_workload:
         per = {}
-        for name in PER_WORKLOADS:
+        names = PER_WORKLOADS if not args.per_workload else args.per_workload.split(",")
+        for name in names:
             if name != w.name:
                 per[name] = per_workload_entry(name, lib, ws, local, dev, args.warmup)
 
@@ -699,6 +785,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="measure only the selected workload")
+    ap.add_argument("--per-workload", default="",
+                    help="comma-separated subset of the per-workload entries")
     ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                     help="time a CUDA-graph replay of the K steps (auto: T <= 64)")
     args = ap.parse_args()

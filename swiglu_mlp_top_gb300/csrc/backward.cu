@@ -62,17 +62,26 @@ bwd_dispatch_kernel(const Tin* __restrict__ x, const Tin* __restrict__ dy,
   const int b = blockIdx.x, nblk = gridDim.x;
   const int64_t t0 = static_cast<int64_t>(b) * kBwdTok;
   const int na = static_cast<int>(T - t0 < kBwdTok ? T - t0 : kBwdTok) * k;
-  // totals and this block's base per expert (thread e sums the blocks in order)
-  for (int e = tid; e < E; e += blockDim.x) {
+  // totals and this block's base per expert: warp w takes experts w, w + 8,
+  // ...; its lanes split the blocks (all loads in flight together) and a
+  // warp reduction adds them (integers: any order gives the same sums)
+  for (int e = warp; e < E; e += kBwdThreads / 32) {
     int all = 0, before = 0;
-    for (int bb = 0; bb < nblk; ++bb) {
+    for (int bb = lane; bb < nblk; bb += 32) {
       const int c = blk_cnt[static_cast<int64_t>(bb) * E + e];
       all += c;
       before += bb < b ? c : 0;
     }
-    s_tot[e] = all;
-    s_base[e] = before;
-    s_run[e] = 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      all += __shfl_xor_sync(0xffffffffu, all, o);
+      before += __shfl_xor_sync(0xffffffffu, before, o);
+    }
+    if (lane == 0) {
+      s_tot[e] = all;
+      s_base[e] = before;
+      s_run[e] = 0;
+    }
   }
   __syncthreads();
   if (tid == 0) {
@@ -106,19 +115,18 @@ bwd_dispatch_kernel(const Tin* __restrict__ x, const Tin* __restrict__ dy,
     o.perm[s_pos[a]] = static_cast<int32_t>(t0 * k + a);
     o.pos[t0 * k + a] = s_pos[a];
   }
-  // rows: a warp per assignment, 16-byte vectors
+  // rows: one flat loop over (assignment, 16-byte vector) items, four in
+  // flight per thread
   constexpr int kVec = 16 / sizeof(Tin);
   const int nv = H / kVec;
-  for (int a = warp; a < na; a += kBwdThreads / 32) {
+  const int items = na * nv;
+#pragma unroll 4
+  for (int i = tid; i < items; i += kBwdThreads) {
+    const int a = i / nv, v = i - a * nv;
     const int64_t t = t0 + a / k;
-    const uint4* sx = reinterpret_cast<const uint4*>(x + t * H);
-    const uint4* sd = reinterpret_cast<const uint4*>(dy + t * H);
-    uint4* dx4 = reinterpret_cast<uint4*>(static_cast<Tin*>(o.xp) + static_cast<int64_t>(s_pos[a]) * H);
-    uint4* dd4 = reinterpret_cast<uint4*>(static_cast<Tin*>(o.dyp) + static_cast<int64_t>(s_pos[a]) * H);
-    for (int v = lane; v < nv; v += 32) {
-      dx4[v] = sx[v];
-      dd4[v] = sd[v];
-    }
+    const int64_t d = static_cast<int64_t>(s_pos[a]) * nv + v;
+    reinterpret_cast<uint4*>(o.xp)[d] = reinterpret_cast<const uint4*>(x)[t * nv + v];
+    reinterpret_cast<uint4*>(o.dyp)[d] = reinterpret_cast<const uint4*>(dy)[t * nv + v];
   }
   if (b == 0) {
     for (int e = tid; e <= E; e += blockDim.x) o.offsets[e] = s_off[e];
@@ -137,6 +145,18 @@ bwd_dispatch_kernel(const Tin* __restrict__ x, const Tin* __restrict__ dy,
       }
     }
   }
+}
+
+// Four consecutive bf16 (8-byte aligned) as fp32, and back.
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(p);
+  v[0] = __uint_as_float(raw.x << 16);
+  v[1] = __uint_as_float(raw.x & 0xffff0000u);
+  v[2] = __uint_as_float(raw.y << 16);
+  v[3] = __uint_as_float(raw.y & 0xffff0000u);
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* p, const float4& a) {
+  *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
 }
 
 // Router backward, one block per 64 tokens, one warp per token at a time
@@ -197,35 +217,58 @@ router_bwd_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, int64_t
     if (v0) { rb.dr[t * E + lane] = dr0; s_dr[tl * E + lane] = dr0; }
     if (v1) { rb.dr[t * E + lane + 32] = dr1; s_dr[tl * E + lane + 32] = dr1; }
     __syncwarp();
-    // dx_t = sum_s dxp[pos(t, s)] (slot order) + sum_e dr_e Wr_e
-    for (int h = lane * 4; h < H; h += 128) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s = 0; s < k; ++s) {
-        const float4 v = *reinterpret_cast<const float4*>(rb.dxp + static_cast<int64_t>(rb.pos[t * k + s]) * H + h);
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-      }
-      for (int e = 0; e < E; ++e) {
-        const float d = s_dr[tl * E + e];
-        const Tin* w = Wr + static_cast<int64_t>(e) * H + h;
-        acc.x = fmaf(d, static_cast<float>(w[0]), acc.x);
-        acc.y = fmaf(d, static_cast<float>(w[1]), acc.y);
-        acc.z = fmaf(d, static_cast<float>(w[2]), acc.z);
-        acc.w = fmaf(d, static_cast<float>(w[3]), acc.w);
-      }
-      Tin* out = static_cast<Tin*>(rb.dx) + t * H + h;
-      out[0] = static_cast<Tin>(acc.x);
-      out[1] = static_cast<Tin>(acc.y);
-      out[2] = static_cast<Tin>(acc.z);
-      out[3] = static_cast<Tin>(acc.w);
-    }
   }
   __syncthreads();
-  // the block's dWr partial: element (e, h) = sum_t dr[t][e] x[t][h], token order
-  for (int i = tid; i < E * H; i += blockDim.x) {
-    const int e = i / H, h = i - e * H;
-    float acc = 0.f;
-    for (int tl = 0; tl < ntok; ++tl) acc = fmaf(s_dr[tl * E + e], static_cast<float>(x[(t0 + tl) * H + h]), acc);
-    rb.dwr_part[static_cast<int64_t>(blockIdx.x) * E * H + i] = acc;
+  // dx_t = sum_s dxp[pos(t, s)] (slot order) + sum_e dr_e Wr_e: one flat
+  // loop over (token, 4-column group) items of the block
+  const int nc4 = H / 4;
+#pragma unroll 2
+  for (int i = tid; i < ntok * nc4; i += blockDim.x) {
+    const int tl = i / nc4, h = 4 * (i - tl * nc4);
+    const int64_t t = t0 + tl;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < k; ++s) {
+      const float4 v = *reinterpret_cast<const float4*>(rb.dxp + static_cast<int64_t>(rb.pos[t * k + s]) * H + h);
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    for (int e = 0; e < E; ++e) {
+      const float d = s_dr[tl * E + e];
+      float w[4];
+      load4(Wr + static_cast<int64_t>(e) * H + h, w);
+      acc.x = fmaf(d, w[0], acc.x);
+      acc.y = fmaf(d, w[1], acc.y);
+      acc.z = fmaf(d, w[2], acc.z);
+      acc.w = fmaf(d, w[3], acc.w);
+    }
+    store4(static_cast<Tin*>(rb.dx) + t * H + h, acc);
+  }
+  // the block's dWr partial: element (e, h) = sum_t dr[t][e] x[t][h] in
+  // token order; a thread holds 4 columns x 8 experts, so each x element is
+  // read once per 8 experts (coalesced: neighbouring threads, neighbouring columns)
+  const int nec = (E + 7) / 8;
+  for (int item = tid; item < nc4 * nec; item += blockDim.x) {
+    const int c4 = item % nc4, e0 = (item / nc4) * 8;
+    float acc[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[j][q] = 0.f;
+#pragma unroll 8
+    for (int tl = 0; tl < ntok; ++tl) {
+      float xv[4];
+      load4(x + (t0 + tl) * H + 4 * c4, xv);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float d = (e0 + j < E) ? s_dr[tl * E + e0 + j] : 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[j][q] = fmaf(d, xv[q], acc[j][q]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (e0 + j < E)
+        *reinterpret_cast<float4*>(rb.dwr_part + (static_cast<int64_t>(blockIdx.x) * E + e0 + j) * H + 4 * c4) =
+            make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
   }
   for (int e = tid; e < E; e += blockDim.x) {
     float acc = 0.f;
@@ -234,23 +277,40 @@ router_bwd_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, int64_t
   }
 }
 
-// dWr[e][h] = sum_b dwr_part[b][e][h] and d_bias[e] = sum_b dbias_part[b][e],
-// blocks in order.
-__global__ void router_bwd_reduce_kernel(const float* __restrict__ dwr_part,
-                                         const float* __restrict__ dbias_part, int nblk, int E,
-                                         int H, float* __restrict__ dWr, float* __restrict__ d_bias) {
+// dWr[e][h] = sum_b dwr_part[b][e][h] and d_bias[e] = sum_b dbias_part[b][e].
+// A block takes 64 outputs; its 4 thread rows split the blocks b into four
+// contiguous quarters, each summed with 4 independent accumulators (loads in
+// flight together), then the quarters are added in order: a fixed order
+// that depends only on nblk.
+constexpr int kRedCols = 64;
+__global__ void __launch_bounds__(256)
+router_bwd_reduce_kernel(const float* __restrict__ dwr_part, const float* __restrict__ dbias_part,
+                         int nblk, int E, int H, float* __restrict__ dWr, float* __restrict__ d_bias) {
+  __shared__ float part[4][kRedCols];
   const int64_t n = static_cast<int64_t>(E) * H;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n + E;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float acc = 0.f;
-    if (i < n) {
-      for (int b = 0; b < nblk; ++b) acc += dwr_part[static_cast<int64_t>(b) * n + i];
-      dWr[i] = acc;
-    } else if (d_bias != nullptr) {
-      const int e = static_cast<int>(i - n);
-      for (int b = 0; b < nblk; ++b) acc += dbias_part[static_cast<int64_t>(b) * E + e];
-      d_bias[e] = acc;
+  const int col = threadIdx.x % kRedCols, q = threadIdx.x / kRedCols;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kRedCols + col;
+  const bool is_w = i < n;
+  const bool is_b = !is_w && i < n + E && d_bias != nullptr;
+  const float* src = is_w ? dwr_part + i : dbias_part + (i - n);
+  const int64_t stride = is_w ? n : E;
+  const int b0 = nblk * q / 4, b1 = nblk * (q + 1) / 4;
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  if (is_w || is_b) {
+    int b = b0;
+    for (; b + 4 <= b1; b += 4) {
+      a0 += src[(b + 0) * stride];
+      a1 += src[(b + 1) * stride];
+      a2 += src[(b + 2) * stride];
+      a3 += src[(b + 3) * stride];
     }
+    for (; b < b1; ++b) a0 += src[b * stride];
+  }
+  part[q][col] = (a0 + a1) + (a2 + a3);
+  __syncthreads();
+  if (q == 0 && (is_w || is_b)) {
+    const float v = ((part[0][col] + part[1][col]) + part[2][col]) + part[3][col];
+    if (is_w) dWr[i] = v; else d_bias[i - n] = v;
   }
 }
 
@@ -285,7 +345,7 @@ cudaError_t launch_router_bwd(const void* x, const void* Wr, int64_t T, int H, i
 cudaError_t launch_router_bwd_reduce(const float* dwr_part, const float* dbias_part, int nblk,
                                      int E, int H, float* dWr, float* d_bias, cudaStream_t st) {
   const int64_t n = static_cast<int64_t>(E) * H + E;
-  const int grid = static_cast<int>(std::min<int64_t>((n + 255) / 256, 1024));
+  const int grid = static_cast<int>((n + kRedCols - 1) / kRedCols);
   router_bwd_reduce_kernel<<<grid, 256, 0, st>>>(dwr_part, dbias_part, nblk, E, H, dWr, d_bias);
   return cudaGetLastError();
 }
