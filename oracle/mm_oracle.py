@@ -347,3 +347,32 @@ def moe_backward(x, Wr, Wg, Wu, Wd, k, coef, dy, d_aux=1.0, logit_bias=None,
     dx += dr @ Wr
     return {"dx": dx, "dWr": dr.T @ x, "dWg": dWg, "dWu": dWu, "dWd": dWd,
             "d_bias": dr.sum(axis=0), "dalpha": dalpha, "dlogits": dr}
+
+
+# --------------------------------------------------------------------------
+# Block fusion: hidden = hidden + mlp(post_attention_layernorm(hidden))
+# --------------------------------------------------------------------------
+def rms_norm(x, w, eps):
+    """RMSNorm of each row: x / sqrt(mean_h x_h^2 + eps) * w.
+
+    The pages name the block's post_attention_layernorm an RMSNorm ([L13]
+    §3 step 2 and the block diagram of §7) without its formula; this is the
+    standard definition, with eps an argument.
+    """
+    x, w = _f64(x), _f64(w)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + F64(eps)) * w[None, :]
+
+
+def swiglu_block(x, norm_w, eps, Wg, Wu, Wd):
+    """x + FFN(RMSNorm(x)): the dense FFN in its MiniMind block ([L13] §3 step 2)."""
+    return _f64(x) + swiglu_ffn(rms_norm(x, norm_w, eps), Wg, Wu, Wd)
+
+
+def moe_block(x, norm_w, eps, Wr, Wg, Wu, Wd, k, coef, logit_bias=None, logit_noise=None,
+              z_coef=0.0):
+    """x + MoE(RMSNorm(x)) ([L13] §3 step 2 with use_moe): the routing outputs
+    are those of the MoE layer on the normalised input."""
+    out = moe_forward(rms_norm(x, norm_w, eps), Wr, Wg, Wu, Wd, k, coef, logit_bias,
+                      logit_noise, z_coef)
+    out["y"] = _f64(x) + out["y"]
+    return out

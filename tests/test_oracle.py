@@ -675,3 +675,50 @@ def test_moe_backward_all_experts_identical_and_k_equal_E():
     np.testing.assert_allclose(g["dx"], dx, rtol=0, atol=1e-12)
     assert np.abs(g["dWr"]).max() < 1e-12
     np.testing.assert_allclose(sum(g["dWg"]), dWg, rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# Block fusion (lesson 13 §3 step 2): RMSNorm and the residual
+# --------------------------------------------------------------------------
+def test_rms_norm_hand_case():
+    """[3, 4]: mean square 12.5, so x / sqrt(12.5) = [0.848528.., 1.131370..];
+    times w = [2, -1]."""
+    y = O.rms_norm(np.array([[3.0, 4.0]]), np.array([2.0, -1.0]), 0.0)
+    np.testing.assert_allclose(y[0], [2 * 3 / math.sqrt(12.5), -4 / math.sqrt(12.5)], rtol=1e-15)
+
+
+def test_rms_norm_properties():
+    r = rng(60)
+    x = r.normal(size=(7, 16)) * 3
+    ones = np.ones(16)
+    y = O.rms_norm(x, ones, 0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(y ** 2, axis=1)), 1.0, rtol=1e-14)   # unit rms
+    np.testing.assert_allclose(O.rms_norm(5.0 * x, ones, 0.0), y, rtol=1e-14)      # scale invariant
+    # eps: a constant row c gives c / sqrt(c^2 + eps)
+    c = 0.01
+    assert abs(O.rms_norm(np.full((1, 4), c), ones[:4], 1e-4)[0, 0] - c / math.sqrt(c * c + 1e-4)) < 1e-16
+    w = r.normal(size=16)
+    np.testing.assert_allclose(O.rms_norm(x, w, 1e-5), O.rms_norm(x, ones, 1e-5) * w, rtol=1e-14)
+
+
+def test_block_residual_and_zero_mlp():
+    """A zero down projection makes the block the identity; otherwise block -
+    x is the FFN of the normalised input (dense and MoE)."""
+    r = rng(61)
+    x = r.normal(size=(9, 8))
+    w = r.normal(size=8)
+    Wg, Wu, Wd = r.normal(size=(6, 8)), r.normal(size=(6, 8)), r.normal(size=(8, 6))
+    np.testing.assert_array_equal(O.swiglu_block(x, w, 1e-5, Wg, Wu, np.zeros_like(Wd)), x)
+    np.testing.assert_allclose(O.swiglu_block(x, w, 1e-5, Wg, Wu, Wd) - x,
+                               O.swiglu_ffn(O.rms_norm(x, w, 1e-5), Wg, Wu, Wd), atol=1e-13)
+    Wr = r.normal(size=(3, 8))
+    G = [r.normal(size=(6, 8)) for _ in range(3)]
+    U = [r.normal(size=(6, 8)) for _ in range(3)]
+    D = [r.normal(size=(8, 6)) for _ in range(3)]
+    b = O.moe_block(x, w, 1e-5, Wr, G, U, D, 2, 0.01)
+    m = O.moe_forward(O.rms_norm(x, w, 1e-5), Wr, G, U, D, 2, 0.01)
+    assert np.array_equal(b["topk_idx"], m["topk_idx"])   # routing on the normalised input
+    np.testing.assert_allclose(b["y"] - x, m["y"], atol=1e-13)
+    assert b["aux_loss"] == m["aux_loss"]
+    zero = O.moe_block(x, w, 1e-5, Wr, G, U, [np.zeros((8, 6))] * 3, 2, 0.01)
+    np.testing.assert_array_equal(zero["y"], x)
