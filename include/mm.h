@@ -112,6 +112,18 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
                      void* y, int64_t T, int H, int I, int dtype,
                      void* workspace, size_t workspace_bytes, void* stream, int path);
 
+/* Dense FFN in its MiniMind block ([L13] §3 step 2):
+ *   y = x + FFN(RMSNorm(x)),  RMSNorm(x) = x / sqrt(mean_h x_h^2 + norm_eps) * w
+ * norm_w [H] in x's dtype.  The normalised rows are written once (x's dtype)
+ * for the GEMMs; the residual is added in the down GEMM's epilogue before y's
+ * one rounding.  bf16: tensor cores; fp32: CUDA cores.  y must not alias x. */
+size_t mm_swiglu_ffn_block_workspace_bytes(int64_t T, int H, int I, int dtype);
+
+int mm_swiglu_ffn_block(const void* x, const void* norm_w, float norm_eps,
+                        const void* Wg, const void* Wu, const void* Wd,
+                        void* y, int64_t T, int H, int I, int dtype,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------------------------------
  * Dense SwiGLU FFN without caller-provided scratch
  *
@@ -218,6 +230,15 @@ typedef struct {
   float* z_loss;              /* device fp32 scalar out, or NULL (not computed)    */
   float* router_probs;        /* device fp32 [T, E] out: softmax p, or NULL        */
   float* router_lse;          /* device fp32 [T] out: logsumexp of the logits, or NULL */
+  /* MiniMind block ([L13] §3 step 2: hidden + mlp(post_attention_layernorm(hidden))):
+   * with norm_weight, the layer's input is x_n = x / sqrt(mean_h x_h^2 + norm_eps) * w
+   * (RMSNorm; the router takes it at full precision, the experts rounded to x's
+   * dtype); with residual != 0, y = x + MoE(...).  Either one runs the call on the
+   * tensor-core (bf16) or CUDA-core GEMMs; the streaming paths return
+   * MM_ERR_UNSUPPORTED.  y must not alias x. */
+  const void* norm_weight;    /* device [H], x's dtype, or NULL                    */
+  float norm_eps;
+  int residual;
 } mm_moe_options;
 
 int mm_moe_forward_opts(const void* x, const void* Wr,

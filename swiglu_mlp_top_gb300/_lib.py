@@ -26,7 +26,8 @@ class MoeOptions(C.Structure):
     """mm_moe_options (include/mm.h), field for field."""
     _fields_ = [("path", C.c_int), ("logit_noise", C.c_void_p), ("z_coef", C.c_float),
                 ("z_loss", C.c_void_p), ("router_probs", C.c_void_p),
-                ("router_lse", C.c_void_p)]
+                ("router_lse", C.c_void_p), ("norm_weight", C.c_void_p),
+                ("norm_eps", C.c_float), ("residual", C.c_int)]
 
 
 _opt = C.POINTER(MoeOptions)
@@ -53,6 +54,9 @@ SIGNATURES = {
                                  _vp, _vp, _sz, _vp, _opt]),
     "mm_moe_route": (_i32, [_vp, _vp, _i64, _i32, _i32, _i32, _f32, _i32, _vp, _vp, _vp, _vp,
                             _vp, _vp, _sz, _vp]),
+    "mm_swiglu_ffn_block_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32]),
+    "mm_swiglu_ffn_block": (_i32, [_vp, _vp, _f32, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32,
+                                   _vp, _sz, _vp]),
     "mm_swiglu_ffn_backward_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32]),
     "mm_swiglu_ffn_backward": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _vp, _vp,
                                       _vp, _vp, _vp, _sz, _vp]),

@@ -73,6 +73,29 @@ def swiglu_ffn(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Te
     return out
 
 
+def swiglu_block(x: torch.Tensor, norm_weight: torch.Tensor, Wg: torch.Tensor,
+                 Wu: torch.Tensor, Wd: torch.Tensor, *, norm_eps: float = 1e-5,
+                 out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    """y = x + FFN(RMSNorm(x)) (mm_swiglu_ffn_block): the dense FFN in its block."""
+    lib = L.load()
+    T, H = x.shape
+    I = Wg.shape[0]
+    dt = _dtype_code(x)
+    if out is None:
+        out = torch.empty_like(x)
+    need = lib.mm_swiglu_ffn_block_workspace_bytes(T, H, I, dt)
+    if workspace is None:
+        workspace = new_workspace(need, x.device)
+    rc = lib.mm_swiglu_ffn_block(
+        _dev(x, "x"), _dev(norm_weight, "norm_weight", x.dtype), float(norm_eps),
+        _dev(Wg, "Wg", x.dtype), _dev(Wu, "Wu", x.dtype), _dev(Wd, "Wd", x.dtype),
+        _dev(out, "out", x.dtype), T, H, I, dt, _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    L.check(rc, "mm_swiglu_ffn_block")
+    return out
+
+
 def swiglu_ffn_noalloc(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Tensor, *,
                        out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """mm_swiglu_ffn_noalloc: the dense FFN using the library's fixed device
@@ -90,11 +113,17 @@ def swiglu_ffn_noalloc(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: 
     return out
 
 
-def _router_options(T: int, E: int, dev, path: str, logit_noise, z_coef, stats):
-    """mm_moe_options for the router variants; fills `stats` (a dict) with the
-    output tensors it asks for: z_loss [], probs [T, E], lse [T] (fp32)."""
+def _router_options(T: int, E: int, dev, path: str, logit_noise, z_coef, stats,
+                    norm_weight=None, norm_eps=1e-5, residual=False, dtype=None):
+    """mm_moe_options for the router variants and the block prologue /
+    epilogue; fills `stats` (a dict) with the output tensors it asks for:
+    z_loss [], probs [T, E], lse [T] (fp32)."""
     o = L.MoeOptions()
     o.path = _PATHS[path]
+    if norm_weight is not None:
+        o.norm_weight = _dev(norm_weight, "norm_weight", dtype)
+        o.norm_eps = float(norm_eps)
+    o.residual = 1 if residual else 0
     if logit_noise is not None:
         if tuple(logit_noise.shape) != (T, E):
             raise ValueError(f"logit_noise must be [{T}, {E}]")
@@ -117,13 +146,17 @@ def moe_forward(x: torch.Tensor, Wr: torch.Tensor, Wg: Sequence[torch.Tensor],
                 topk_idx: Optional[torch.Tensor] = None, topk_w: Optional[torch.Tensor] = None,
                 aux_loss: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                 path: str = "auto", stream=None, logit_noise: Optional[torch.Tensor] = None,
-                z_coef: float = 0.0, stats: Optional[dict] = None):
+                z_coef: float = 0.0, stats: Optional[dict] = None,
+                norm_weight: Optional[torch.Tensor] = None, norm_eps: float = 1e-5,
+                residual: bool = False):
     """Top-k MoE forward (mm_moe_forward; mm_moe_forward_opts when router
-    noise, z-loss or router statistics are asked for).
+    noise, z-loss, router statistics or the block's norm / residual are asked
+    for).
 
     Returns (y [T,H], topk_idx [T,k] int32, topk_w [T,k] fp32, aux_loss [] fp32).
     With a dict `stats`, it also receives z_loss [] (z_coef * mean_t lse_t^2),
-    probs [T, E] and lse [T] (fp32 device tensors).
+    probs [T, E] and lse [T] (fp32 device tensors).  With norm_weight the
+    layer runs on RMSNorm(x); with residual, y = x + MoE(...).
     """
     lib = L.load()
     T, H = x.shape
@@ -147,10 +180,11 @@ def moe_forward(x: torch.Tensor, Wr: torch.Tensor, Wg: Sequence[torch.Tensor],
             _dev(topk_w, "topk_w", torch.float32), _dev(aux_loss, "aux_loss", torch.float32),
             _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
             _stream(stream))
-    if logit_noise is None and not z_coef and stats is None:
+    if logit_noise is None and not z_coef and stats is None and norm_weight is None and not residual:
         rc = lib.mm_moe_forward_ex(*args, _PATHS[path])
     else:
-        o = _router_options(T, E, dev, path, logit_noise, z_coef, stats)
+        o = _router_options(T, E, dev, path, logit_noise, z_coef, stats, norm_weight, norm_eps,
+                            residual, x.dtype)
         rc = lib.mm_moe_forward_opts(*args, C.byref(o))
     del ag, au, ad
     L.check(rc, "mm_moe_forward")

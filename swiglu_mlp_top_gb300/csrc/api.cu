@@ -29,7 +29,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 // ----------------------------------------------------------------- layouts
 struct MoeLayout {
-  size_t offsets, counts, blk_cnt, blk_prob, blk_z, perm, xp, h, acc32, wd16, total;
+  size_t offsets, counts, blk_cnt, blk_prob, blk_z, inv_rms, wr_hl, perm, xp, h, acc32, wd16, total;
 };
 
 // h is stored in fp16 for bf16 inputs (see gemm_tc.cu) and in fp32 for fp32.
@@ -51,6 +51,8 @@ MoeLayout moe_layout(int64_t T, int H, int I, int E, int k, int dtype) {
   L.blk_cnt = off;  off += align_up(4 * nblk * G);
   L.blk_prob = off; off += align_up(4 * nblk * E);
   L.blk_z = off;    off += align_up(4 * nblk);
+  L.inv_rms = off;  off += align_up(4 * static_cast<size_t>(T));            // block norm
+  L.wr_hl = off;    off += align_up(4 * static_cast<size_t>(E) * H);        // block norm, bf16 [2E, H]
   L.perm = off;     off += align_up(4 * rows);
   L.xp = off;       off += align_up(es * rows * H);
   L.h = off;        off += align_up(h_bytes(dtype) * rows * I);
@@ -136,6 +138,13 @@ size_t dense_h_bytes(int64_t T, int I, int dtype) {
 size_t dense_tensor_ws_bytes(int64_t T, int H, int I, int dtype) {
   return sizeof(WsHeader) + dense_h_bytes(T, I, dtype) +
          (dtype == kDtypeBF16 ? align_up(2 * static_cast<size_t>(H) * I) : 0);
+}
+
+// The dense block (x + FFN(RMSNorm(x))): the tensor-core / SIMT workspace,
+// then the normalised rows x_n [T, H] and inv_rms [T].
+size_t dense_block_ws_bytes(int64_t T, int H, int I, int dtype) {
+  return dense_tensor_ws_bytes(T, H, I, dtype) + align_up(elem_bytes(dtype) * static_cast<size_t>(T) * H) +
+         align_up(4 * static_cast<size_t>(T));
 }
 
 bool valid_dtype(int dtype) { return dtype == kDtypeF32 || dtype == kDtypeBF16; }
@@ -226,6 +235,7 @@ size_t dense_workspace_for_path(int64_t T, int H, int I, int dtype, int path) {
 namespace {
 
 inline char* ws_at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
+inline float* f32_at(void* ws, size_t off) { return reinterpret_cast<float*>(ws_at(ws, off)); }
 
 // ----------------------------------------------------------- measurement hooks
 std::atomic<uint64_t> g_launches{0};
@@ -416,9 +426,19 @@ static int moe_forward_impl(const void* x, const void* Wr, const void* const* Wg
                             int E, int k, float coef, int dtype, const float* logit_bias, void* y,
                             int32_t* topk_idx, float* topk_w, float* aux_loss, void* workspace,
                             size_t workspace_bytes, void* stream, const mm_moe_options* opts) {
-  const int path = opts ? opts->path : MM_PATH_AUTO;
+  int path = opts ? opts->path : MM_PATH_AUTO;
+  const void* norm_w = opts ? opts->norm_weight : nullptr;
+  const bool resid = opts && opts->residual;
   int rc = check_route_args(x, Wr, T, H, E, k, dtype, logit_bias, topk_idx, topk_w, aux_loss);
   if (rc != MM_OK) return rc;
+  if (norm_w != nullptr || resid) {
+    // the block prologue / epilogue live in the router, dispatch and down
+    // kernels: the tensor-core or CUDA-core GEMM paths, not the streaming ones
+    if (path == MM_PATH_STREAM || path == MM_PATH_STREAM_TC) return MM_ERR_UNSUPPORTED;
+    if (path == MM_PATH_AUTO) path = dtype == kDtypeBF16 ? MM_PATH_TENSOR : MM_PATH_SIMT;
+    if (norm_w != nullptr && (!aligned16(norm_w) || !(opts->norm_eps >= 0.f))) return MM_ERR_INVALID_ARG;
+    if (resid && y == x) return MM_ERR_INVALID_ARG;   // x is read as the residual while y is written
+  }
   if (I < 1) return MM_ERR_INVALID_ARG;
   if (I % 8 != 0) return MM_ERR_UNSUPPORTED;
   if (path < MM_PATH_AUTO || path > MM_PATH_STREAM_TC) return MM_ERR_INVALID_ARG;
@@ -473,13 +493,22 @@ static int moe_forward_impl(const void* x, const void* Wr, const void* const* Wg
   RouterVariant rv;
   rc = router_variant(opts, ws_at(workspace, L.blk_z), &rv);
   if (rc != MM_OK) return rc;
-  const RouteOut ro{nullptr, nullptr, nullptr, nullptr, coef, 0, rv};
+  BlockNorm nrm{norm_w, norm_w ? opts->norm_eps : 0.f, f32_at(workspace, L.inv_rms),
+                ws_at(workspace, L.wr_hl)};
+  if (norm_w != nullptr && dtype == kDtypeBF16) {
+    // w folded into the router weights (exact bf16 halves) for the tensor-core router
+    cudaError_t e0 = counted_launch(MM_KERNEL_ROUTER, st, [&] {
+      return launch_norm_fold_router(Wr, norm_w, E, H, ws_at(workspace, L.wr_hl), st);
+    });
+    if (e0 != cudaSuccess) return cuda_fail(e0, "norm fold");
+  }
+  const RouteOut ro{nullptr, nullptr, nullptr, nullptr, coef, 0, rv, nrm};
   cudaError_t e = counted_launch(MM_KERNEL_ROUTER, st, [&] {
     return launch_router(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w, blk_cnt, blk_prob,
                          ro, hdr, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "router");
-  const DispatchOut dout{offsets, counts, aux_loss, coef, hdr, rv};
+  const DispatchOut dout{offsets, counts, aux_loss, coef, hdr, rv, nrm};
   e = counted_launch(MM_KERNEL_DISPATCH, st, [&] {
     return launch_dispatch(dtype, x, T, H, E, k, topk_idx, blk_cnt, blk_prob, dout, perm, xp, st);
   });
@@ -504,7 +533,8 @@ static int moe_forward_impl(const void* x, const void* Wr, const void* const* Wg
     GroupRows gd{offsets + static_cast<size_t>(s) * E, E, 0, E};
     DownEpilogue ep{y, acc32, perm, topk_w, k,
                     k == 1 ? kCombineStore
-                           : (s == 0 ? kCombineFirst : (s == k - 1 ? kCombineLast : kCombineAccum))};
+                           : (s == 0 ? kCombineFirst : (s == k - 1 ? kCombineLast : kCombineAccum)),
+                    resid ? x : nullptr};
     if (p == MM_PATH_TENSOR)
       e = counted_launch(MM_KERNEL_DOWN, st, [&] {
         return launch_down_tc(h, rows, H, I, gd, wd16p, ep, hdr, st);
@@ -577,12 +607,68 @@ int mm_moe_route_opts(const void* x, const void* Wr, int64_t T, int H, int E, in
   RouterVariant rv;
   rc = router_variant(opts, ws_at(workspace, L.blk_z), &rv);
   if (rc != MM_OK) return rc;
-  const RouteOut ro{nullptr, nullptr, expert_counts, aux_loss, coef, 1, rv};
+  const RouteOut ro{nullptr, nullptr, expert_counts, aux_loss, coef, 1, rv, BlockNorm{}};
   cudaError_t e = counted_launch(MM_KERNEL_ROUTER, st, [&] {
     return launch_router(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w, blk_cnt, blk_prob,
                          ro, hdr, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "router");
+  return MM_OK;
+}
+
+// ------------------------------------------------------------------ dense block
+size_t mm_swiglu_ffn_block_workspace_bytes(int64_t T, int H, int I, int dtype) {
+  if (T < 0 || H < 1 || I < 1 || !valid_dtype(dtype)) return 0;
+  return dense_block_ws_bytes(T, H, I, dtype);
+}
+
+int mm_swiglu_ffn_block(const void* x, const void* norm_w, float norm_eps, const void* Wg,
+                        const void* Wu, const void* Wd, void* y, int64_t T, int H, int I,
+                        int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!valid_dtype(dtype) || T < 0 || H < 1 || I < 1 || !(norm_eps >= 0.f)) return MM_ERR_INVALID_ARG;
+  if (H % 8 != 0 || I % 8 != 0) return MM_ERR_UNSUPPORTED;
+  if (dtype == kDtypeBF16 && !tensor_shape_ok(H, I)) return MM_ERR_UNSUPPORTED;
+  if (T > (int64_t{1} << 30)) return MM_ERR_UNSUPPORTED;
+  if (T == 0) return MM_OK;
+  if (!x || !norm_w || !Wg || !Wu || !Wd || !y) return MM_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, norm_w, Wg, Wu, Wd, y};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MM_ERR_INVALID_ARG;
+  if (y == x) return MM_ERR_INVALID_ARG;            // the residual is read while y is written
+  if (!workspace || !aligned16(workspace)) return MM_ERR_WORKSPACE;
+  const size_t need = dense_block_ws_bytes(T, H, I, dtype);
+  if (workspace_bytes < need) return MM_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(workspace);
+  const size_t base = dense_tensor_ws_bytes(T, H, I, dtype);
+  void* xn = ws_at(workspace, base);
+  float* inv = f32_at(workspace, base + align_up(elem_bytes(dtype) * static_cast<size_t>(T) * H));
+  // prologue: the normalised rows (the GEMMs read their A operand by TMA)
+  cudaError_t e = counted_launch(MM_KERNEL_DISPATCH, st, [&] {
+    return launch_rms_norm_rows(dtype, x, norm_w, norm_eps, T, H, xn, inv, st);
+  });
+  if (e != cudaSuccess) return cuda_fail(e, "rms norm");
+  void* h = ws_at(workspace, sizeof(WsHeader));
+  GroupRows g{nullptr, 1, static_cast<int>(T), 1};
+  DownEpilogue ep{y, nullptr, nullptr, nullptr, 1, kCombineStore, x};   // + the residual
+  const void* wg[1] = {Wg};
+  const void* wu[1] = {Wu};
+  const void* wd[1] = {Wd};
+  if (dtype == kDtypeBF16) {
+    void* wd16 = ws_at(workspace, sizeof(WsHeader) + dense_h_bytes(T, I, dtype));
+    const void* wd16p[1] = {wd16};
+    e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
+      return launch_gateup_tc(xn, T, H, I, g, wg, wu, h, wd, 1, wd16, hdr, st);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "gateup_tc");
+    e = counted_launch(MM_KERNEL_DOWN, st, [&] { return launch_down_tc(h, T, H, I, g, wd16p, ep, hdr, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "down_tc");
+  } else {
+    e = counted_launch(MM_KERNEL_GATEUP, st, [&] { return launch_gateup_simt(dtype, xn, T, H, I, g, wg, wu, h, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "gateup_simt");
+    e = counted_launch(MM_KERNEL_DOWN, st, [&] { return launch_down_simt(dtype, h, T, H, I, g, wd, ep, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "down_simt");
+  }
   return MM_OK;
 }
 

@@ -336,7 +336,8 @@ __device__ __forceinline__ void down_prefetch(const DownLanes& L, const DownEpil
 template <int HC>
 __device__ __forceinline__ void epilogue_down_dense(uint32_t tb, const TileInfo& ti, int H,
                                                     int half, int lane, int row_base,
-                                                    uint8_t* wstage, const CUtensorMap* ymap) {
+                                                    uint8_t* wstage, const CUtensorMap* ymap,
+                                                    const __nv_bfloat16* resid) {
   const int col0 = ti.n0 + half * HC;
 #pragma unroll 1
   for (int c = 0; c < HC / 32; ++c) {
@@ -345,6 +346,24 @@ __device__ __forceinline__ void epilogue_down_dense(uint32_t tb, const TileInfo&
     tmem_ld_32x32b_x16(tb + half * HC + c * 32, r0);
     tmem_ld_32x32b_x16(tb + half * HC + c * 32 + 16, r1);
     tmem_ld_wait();
+    if (resid != nullptr) {
+      // the block's residual x[row, 32 columns], added before the one rounding
+      const uint4* xr = reinterpret_cast<const uint4*>(
+          resid + static_cast<int64_t>(row_base + lane) * H + col0 + c * 32);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = xr[q];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t* dst = q < 2 ? r0 : r1;
+        const int b = (q & 1) * 8;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          dst[b + 2 * j] = __float_as_uint(__uint_as_float(dst[b + 2 * j]) + __uint_as_float(w[j] << 16));
+          dst[b + 2 * j + 1] =
+              __float_as_uint(__uint_as_float(dst[b + 2 * j + 1]) + __uint_as_float(w[j] & 0xffff0000u));
+        }
+      }
+    }
     uint32_t pk[16];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -412,6 +431,13 @@ __device__ __forceinline__ void epilogue_down(uint32_t tb, const DownRow& d, con
       if (ep.mode == kCombineFirst || ep.mode == kCombineAccum) {
         __stcg(reinterpret_cast<float4*>(ep.acc32 + o), v);
       } else {
+        if (ep.resid != nullptr) {       // the block's residual, before the one rounding
+          const uint2 xr = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(ep.resid) + o);
+          v.x += __uint_as_float(xr.x << 16);
+          v.y += __uint_as_float(xr.x & 0xffff0000u);
+          v.z += __uint_as_float(xr.y << 16);
+          v.w += __uint_as_float(xr.y & 0xffff0000u);
+        }
         *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(ep.y) + o) =
             make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
       }
@@ -713,7 +739,8 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
       else if constexpr (OP == kOpUpBwd)
         epilogue_up_bwd(tb, ti, NCOLS, row, half, ub);
       else if (ep.perm == nullptr && ep.mode == kCombineStore && (row | 31) < ti.rows)
-        epilogue_down_dense<kHC>(tb, ti, NCOLS, half, lane, ti.row0 + (row & ~31), wstage, &P.out);
+        epilogue_down_dense<kHC>(tb, ti, NCOLS, half, lane, ti.row0 + (row & ~31), wstage, &P.out,
+                                 static_cast<const __nv_bfloat16*>(ep.resid));
       else
         epilogue_down<kHC>(tb, dr, dl, ti, NCOLS, ep, half, lane, wstage, pre, pre2);
       tc_fence_before();

@@ -58,6 +58,8 @@ struct DownEpilogue {
   const float* topk_w;      // [T*k] alpha, or nullptr (alpha = 1)
   int k;
   int mode;                 // CombineMode
+  const void* resid;        // [T, H] x's dtype, added to y at the final store
+                            // (the block's residual), or nullptr
 };
 
 // fp16 copy of the down matrices, made by the epilogue warps of the gate/up
@@ -87,6 +89,19 @@ struct RouterVariant {
   float* blk_z;          // [nblk] fp32 (prefill router)
 };
 
+// RMSNorm prologue of the MiniMind block (lesson 13 §3 step 2: hidden +
+// mlp(post_attention_layernorm(hidden))), x_n = x / sqrt(mean x^2 + eps) * w.
+// The router takes it at full precision: logits = inv_rms * x . (w * Wr),
+// with w * Wr as the tensor core's two exact bf16 halves (wr_hl rows [0, E):
+// high part, [E, 2E): remainder), or w folded into x on the CUDA cores; it
+// stores each token's inv_rms for the dispatch, which writes the rows x_n.
+struct BlockNorm {
+  const void* w;          // [H] x's dtype; null: no norm
+  float eps;
+  float* inv_rms;         // [T] fp32 out (router) / in (dispatch)
+  const void* wr_hl;      // bf16 [2E, H] (tensor-core router)
+};
+
 // Router grid (routing.cu): per 64-token block logits, softmax, top-k, alpha
 // and partial counts / probability sums; with do_scan the block that
 // finishes last runs the scan (counts, aux loss; its counter lives in the
@@ -99,6 +114,7 @@ struct RouteOut {
   float coef;
   int do_scan;           // 0: the dispatch kernel derives bases, offsets, counts, aux
   RouterVariant rv;
+  BlockNorm norm;
 };
 struct RouteExtras {
   int32_t* blk_base;
@@ -111,6 +127,8 @@ struct RouteExtras {
   uint32_t x_off;
   int do_scan;
   RouterVariant rv;
+  BlockNorm norm;
+  const void* xrow;      // x in global memory (the norm's sums of squares)
 };
 cudaError_t launch_router(int dtype, const void* x, const void* Wr, const float* bias, int64_t T,
                           int H, int E, int k, int32_t* topk_idx, float* topk_w, int32_t* blk_cnt,
@@ -125,6 +143,7 @@ struct DispatchOut {
   float coef;
   WsHeader* hdr;
   RouterVariant rv;      // block 0 finalises the z-loss from rv.blk_z
+  BlockNorm norm;        // w != null: the rows written are x * inv_rms * w
 };
 cudaError_t launch_dispatch(int dtype, const void* x, int64_t T, int H, int E, int k,
                             const int32_t* topk_idx, const int32_t* blk_cnt, const float* blk_prob,
@@ -183,6 +202,14 @@ cudaError_t launch_decode_sw(const void* x, const void* Wg, const void* Wu, cons
                              int H, int I, void* scratch, void* y, WsHeader* hdr, cudaStream_t st);
 
 cudaError_t launch_watchdog_selftest(WsHeader* hdr, uint32_t limit_us, cudaStream_t st);
+
+// Block prologue helpers (norm.cu): the router weights with the norm weight
+// folded in, as exact bf16 halves (hi = bf16(w * Wr), lo = w * Wr - hi), and
+// the normalised rows x_n = x * inv_rms * w (x's dtype) with inv_rms [T].
+cudaError_t launch_norm_fold_router(const void* Wr, const void* w, int E, int H, void* wr_hl,
+                                    cudaStream_t st);
+cudaError_t launch_rms_norm_rows(int dtype, const void* x, const void* w, float eps, int64_t T,
+                                 int H, void* xn, float* inv_rms, cudaStream_t st);
 
 // ----------------------------------------------------------- backward pass
 // Tensor-core GEMMs of the backward (gemm_bwd.cu).  kSchedRows: row groups

@@ -125,6 +125,7 @@ router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float
   __shared__ __align__(8) uint64_t xbar;
   __shared__ int s_last;
   const RouterVariant& rv = X.rv;
+  const Tin* norm_w = static_cast<const Tin*>(X.norm.w);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = k * E;
@@ -178,6 +179,9 @@ router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float
     u64 acc[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) acc[i] = 0ull;
+    u64 ss2[TPW];                                  // block norm: sums of x^2 per token
+#pragma unroll
+    for (int t = 0; t < TPW; ++t) ss2[t] = 0ull;
     for (int c = lane; c < nch; c += 32) {
       u64 xv[TPW][4];
 #pragma unroll
@@ -188,6 +192,18 @@ router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float
 #pragma unroll
           for (int i = 0; i < 4; ++i) xv[t][i] = 0ull;
         }
+      }
+      if (norm_w != nullptr) {
+        // x_h^2 for the norm, then x_h * w_h (exact in fp32 for bf16)
+        u64 wv[4];
+        load_pairs8(norm_w + c * 8, wv);
+#pragma unroll
+        for (int t = 0; t < TPW; ++t)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            ss2[t] = ffma2(xv[t][q], xv[t][q], ss2[t]);
+            xv[t][q] = ffma2(xv[t][q], wv[q], 0ull);
+          }
       }
 #pragma unroll
       for (int e = 0; e < EP; ++e) {
@@ -224,11 +240,23 @@ router_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, const float
     }
     const int64_t tok = tbase + t_loc;
     const bool valid = tok < T;
+    float inv = 1.0f;
+    if (norm_w != nullptr) {
+      // this lane's token: its sum of squares over all lanes, in a fixed order
+      float ssv = 0.f;
+#pragma unroll
+      for (int t = 0; t < TPW; ++t) {
+        const float w = warp_sum(hsum2(ss2[t]));
+        if (t == t_loc) ssv = w;
+      }
+      inv = 1.0f / sqrtf(ssv / static_cast<float>(H) + X.norm.eps);
+      if (valid && lane == gbase) X.norm.inv_rms[tok] = inv;
+    }
     float r[R];
     float m = -INFINITY;
 #pragma unroll
     for (int j = 0; j < R; ++j) {
-      r[j] = (e_of[j] < E) ? v[j * 32] + bias_v[j] : -INFINITY;
+      r[j] = (e_of[j] < E) ? inv * v[j * 32] + bias_v[j] : -INFINITY;
       if (rv.noise != nullptr && valid && e_of[j] < E) r[j] += rv.noise[tok * E + e_of[j]];
       m = fmaxf(m, r[j]);
     }
@@ -620,9 +648,20 @@ dispatch_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, int k,
   }
 
   const int na = ntok * k;
+  const Tin* norm_w = static_cast<const Tin*>(D.norm.w);
   if (stage_x) {
     // one bulk copy per assignment row, shared -> global
     if (!__syncthreads_and(mbar_wait(&xbar, 0, nullptr, D.hdr, 61))) return;
+    if (norm_w != nullptr) {
+      // block norm: the staged rows become x * inv_rms * w in place
+      for (int i = tid; i < ntok * H; i += kRouteThreads) {
+        const int tl = i / H, h = i - tl * H;
+        const float v = to_f32(xs[i]) * D.norm.inv_rms[tok0 + tl] * to_f32(norm_w[h]);
+        xs[i] = static_cast<Tin>(v);
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+    }
     if (tid < na) {
       for (int a = tid; a < na; a += kRouteThreads)
         bulk_store(Xp + static_cast<int64_t>(s_pos[a]) * H, xs + static_cast<int64_t>(a / k) * H, rowb);
@@ -634,6 +673,14 @@ dispatch_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, int k,
     constexpr int kVec = 16 / sizeof(Tin);
     const int nv = H / kVec;
     for (int a = warp; a < na; a += kWarps) {
+      if (norm_w != nullptr) {
+        const Tin* src = x + (tok0 + a / k) * H;
+        Tin* dst = Xp + static_cast<int64_t>(s_pos[a]) * H;
+        const float inv = D.norm.inv_rms[tok0 + a / k];
+        for (int h = lane; h < H; h += 32)
+          dst[h] = static_cast<Tin>(to_f32(src[h]) * inv * to_f32(norm_w[h]));
+        continue;
+      }
       const uint4* src = reinterpret_cast<const uint4*>(x + (tok0 + a / k) * H);
       uint4* dst = reinterpret_cast<uint4*>(Xp + static_cast<int64_t>(s_pos[a]) * H);
 #pragma unroll 4
@@ -675,6 +722,7 @@ router_tc_kernel(const __grid_constant__ RtMaps M, int64_t T, int H, int E, int 
   __shared__ float s_red[2][EP];
   __shared__ float s_redz[2];
   __shared__ float s_bias[EP];
+  __shared__ float s_inv[kRouteTokensPerBlock];
   __shared__ int s_last;
   const RouterVariant& rv = X.rv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -743,6 +791,36 @@ router_tc_kernel(const __grid_constant__ RtMaps M, int64_t T, int H, int E, int 
     }
     if (ok) umma_commit(&lbar);
   }
+  // block RMSNorm: the other warps take each token's 1 / rms from its row of
+  // x while the MMAs run (warp w' = warp - 2 takes tokens w', w' + 6, ...;
+  // lanes over 16-byte vectors, a fixed tree)
+  const bool norm = X.norm.w != nullptr;
+  if (norm) {
+    if (warp >= 2) {
+      for (int t = warp - 2; t < ntok; t += kRouteThreads / 32 - 2) {
+        const uint4* row = reinterpret_cast<const uint4*>(X.xrow) + (t0 + t) * (H / 8);
+        float ss = 0.f;
+        for (int v = lane; v < H / 8; v += 32) {
+          const uint4 q = row[v];
+          const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float a = __uint_as_float(w4[j] << 16), b = __uint_as_float(w4[j] & 0xffff0000u);
+            ss = fmaf(a, a, ss);
+            ss = fmaf(b, b, ss);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) {
+          const float sv = 1.0f / sqrtf(ss / static_cast<float>(H) + X.norm.eps);
+          s_inv[t] = sv;
+          X.norm.inv_rms[t0 + t] = sv;
+        }
+      }
+    }
+    __syncthreads();
+  }
   if (warp < 2) {
     const int t = warp * 32 + lane;              // TMEM lane = token of the block
     const bool valid = t < ntok;
@@ -757,6 +835,15 @@ router_tc_kernel(const __grid_constant__ RtMaps M, int64_t T, int H, int E, int 
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) p[c0 + j] = __uint_as_float(r[j]);
+      }
+      if (norm) {
+        // logits = inv_rms * (x . hi + x . lo); columns E.. hold the remainders
+        const float sv = valid ? s_inv[t] : 0.f;
+#pragma unroll
+        for (int e = 0; e < EP; ++e) {
+          if (e >= E) break;
+          p[e] = sv * (p[e] + p[E + e]);
+        }
       }
       // loops over the E experts only (E is uniform; the padded columns past
       // E are never read)
@@ -933,9 +1020,11 @@ static cudaError_t launch_router_tc(const void* x, const void* Wr, const float* 
   const uint64_t dx[3] = {64, static_cast<uint64_t>(T), static_cast<uint64_t>(KB)};
   const uint32_t bx[3] = {64, static_cast<uint32_t>(kRouteTokensPerBlock), static_cast<uint32_t>(nkb)};
   if (!make_map_3d(&m.x, x, dx, sx, bx)) return cudaErrorInvalidValue;
-  const uint64_t dw[3] = {64, static_cast<uint64_t>(E), static_cast<uint64_t>(KB)};
+  // with the block norm, the B operand is w * Wr as 2E rows (high parts, remainders)
+  const bool norm = X.norm.w != nullptr;
+  const uint64_t dw[3] = {64, static_cast<uint64_t>(norm ? 2 * E : E), static_cast<uint64_t>(KB)};
   const uint32_t bw[3] = {64, static_cast<uint32_t>(EP), static_cast<uint32_t>(nkb)};
-  if (!make_map_3d(&m.wr, Wr, dw, sx, bw)) return cudaErrorInvalidValue;
+  if (!make_map_3d(&m.wr, norm ? X.norm.wr_hl : Wr, dw, sx, bw)) return cudaErrorInvalidValue;
   auto fn = router_tc_kernel<EP>;
   cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem);
   if (err != cudaSuccess) return err;
@@ -968,12 +1057,16 @@ cudaError_t launch_router(int dtype, const void* x, const void* Wr, const float*
   X.do_scan = out.do_scan;
   X.hdr = hdr;
   X.rv = out.rv;
-  const bool tc_ok = dtype == kDtypeBF16 && H % 64 == 0 && E <= 64 &&
+  X.norm = out.norm;
+  X.xrow = x;
+  // the block norm doubles the router's N (high parts and remainders)
+  const int En = X.norm.w != nullptr ? 2 * E : E;
+  const bool tc_ok = dtype == kDtypeBF16 && H % 64 == 0 && En <= 64 &&
                      (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && (reinterpret_cast<uintptr_t>(Wr) & 15u) == 0;
   if (tc_ok) {
-    if (E <= 16)
+    if (En <= 16)
       return launch_router_tc<16>(x, Wr, bias, T, H, E, k, topk_idx, topk_w, blk_cnt, blk_prob, X, st);
-    if (E <= 32)
+    if (En <= 32)
       return launch_router_tc<32>(x, Wr, bias, T, H, E, k, topk_idx, topk_w, blk_cnt, blk_prob, X, st);
     return launch_router_tc<64>(x, Wr, bias, T, H, E, k, topk_idx, topk_w, blk_cnt, blk_prob, X, st);
   }

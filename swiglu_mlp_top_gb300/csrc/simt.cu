@@ -184,10 +184,12 @@ down_simt_kernel(const Th* __restrict__ Hm, const GroupRows g, const PtrArray wd
           continue;
         }
         if (ep.mode != kCombineStore) v += ep.acc32[o];
-        if (ep.mode == kCombineAccum)
+        if (ep.mode == kCombineAccum) {
           ep.acc32[o] = v;
-        else
+        } else {
+          if (ep.resid != nullptr) v += ld_f32(static_cast<const T*>(ep.resid) + o);
           y[o] = from_f32<T>(v);
+        }
       }
     }
   }
