@@ -507,6 +507,42 @@ def make_step(w, dev):
     return Step(w, dev, n_sets)
 
 
+class VariantStep(Step):
+    """The MoE forward of a workload with extra options: the MiniMind block
+    (RMSNorm prologue + residual), the router variants (noise, z-loss and the
+    saved statistics) or the gathering gate/up path."""
+
+    def __init__(self, w, dev, n_sets, variant):
+        super().__init__(w, dev, n_sets)
+        self.variant = variant
+        self.kw = {}
+        if variant == "block":
+            gen = torch.Generator().manual_seed(7)
+            nw = (1.0 + 0.1 * torch.randn(w.H, generator=gen)).to(torch.bfloat16).to(dev)
+            self.kw = dict(norm_weight=nw, norm_eps=1e-5, residual=True)
+        elif variant == "variants":
+            from swiglu_mlp_top_gb300.inputs import make_router_noise
+            self.kw = dict(logit_noise=make_router_noise(w.T, w.E, 0.5).to(dev), z_coef=1e-3,
+                           stats={})
+        elif variant == "gather":
+            self.kw = dict(path="tensor_gather")
+        if w.kind == "dense":
+            self.ws = self.mm.new_workspace(
+                self.mm.api.L.load().mm_swiglu_ffn_block_workspace_bytes(w.T, w.H, w.I, 1), dev)
+            gen = torch.Generator().manual_seed(7)
+            self.nw = (1.0 + 0.1 * torch.randn(w.H, generator=gen)).to(torch.bfloat16).to(dev)
+
+    def __call__(self, i, x=None, outs=None):
+        s = self.sets[i % len(self.sets)]
+        if self.w.kind == "dense":
+            self.mm.swiglu_block(s["x"], self.nw, s["Wg"], s["Wu"], s["Wd"], out=self.y,
+                                 workspace=self.ws)
+            return
+        self.mm.moe_forward(s["x"], s["Wr"], s["Wg"], s["Wu"], s["Wd"], self.w.k, self.w.coef,
+                            logit_bias=s.get("logit_bias"), out=self.y, topk_idx=self.idx,
+                            topk_w=self.tw, aux_loss=self.aux, workspace=self.ws, **self.kw)
+
+
 class BwdStep(Step):
     """One backward pass of the workload (mm_swiglu_ffn_backward /
     mm_moe_backward) on device inputs: an upstream gradient dy per input
@@ -553,15 +589,20 @@ class BwdStep(Step):
 #: per_workload object (each the configuration a parity test covers).
 PER_WORKLOADS = ["dense_t4096", "dense_t100", "moe_e4k1_t8192"] + \
     [f"decode_{kind}_t{T}" for kind in ("dense", "moe_e8k2") for T in (1, 4, 16, 64)] + \
-    ["backward:dense_t4096", "backward:moe_e4k1_t8192", "backward:moe_e8k2_t16384_skew"]
+    ["backward:dense_t4096", "backward:moe_e4k1_t8192", "backward:moe_e8k2_t16384_skew",
+     "block:dense_t4096", "block:moe_e8k2_t16384_skew", "variants:moe_e8k2_t16384_skew",
+     "gather:moe_e8k2_t16384_skew"]
 
 
 def per_workload_entry(name, lib, ws, local, dev, warmup):
     if name.startswith("backward:"):
         return backward_entry(WORKLOADS[name.split(":", 1)[1]], lib, ws, local, dev, warmup)
+    variant = None
+    if ":" in name:
+        variant, name = name.split(":", 1)
     w = WORKLOADS[name]
-    step = make_step(w, dev)
-    use_graph = streams_weights(w)
+    step = make_step(w, dev) if variant is None else VariantStep(w, dev, l2_rotation(w)[0], variant)
+    use_graph = streams_weights(w) and variant is None
     dominant = 7 if use_graph else 4          # MM_KERNEL_DECODE / MM_KERNEL_GATEUP
     # calibrate: K steps per region so that one region takes about 20 ms
     for i in range(3):

@@ -71,7 +71,10 @@ typedef enum {
   MM_PATH_TENSOR = 1,  /* bf16 only: grouped tcgen05/TMEM GEMMs fed by TMA          */
   MM_PATH_STREAM = 2,  /* bf16 only, T <= 16: weight streaming on the CUDA cores       */
   MM_PATH_SIMT = 3,    /* any dtype: plain fp32-FMA CUDA-core kernels                */
-  MM_PATH_STREAM_TC = 4 /* bf16 only, T <= 128 dense / 64 MoE: weight streaming on the tensor cores */
+  MM_PATH_STREAM_TC = 4, /* bf16 only, T <= 128 dense / 64 MoE: weight streaming on the tensor cores */
+  MM_PATH_TENSOR_GATHER = 5 /* bf16 MoE only: as MM_PATH_TENSOR, but the gate/up GEMM gathers x
+                               rows by token index (TMA gather4) and no permuted copy of x
+                               is made (a dense FFN call takes MM_PATH_TENSOR) */
 } mm_path;
 
 /* Limits of this build. */
@@ -189,6 +192,10 @@ int mm_swiglu_ffn_noalloc(const void* x, const void* Wg, const void* Wu, const v
  * H a multiple of 8 and (E*H + k*E)*4 <= 200 KiB.
  * ---------------------------------------------------------------------- */
 size_t mm_moe_workspace_bytes(int64_t T, int H, int I, int E, int k, int dtype);
+/* The workspace one path needs (0: the path does not take the shape); the
+ * gathering path (MM_PATH_TENSOR_GATHER) needs no T*k*H permuted copy of x. */
+size_t mm_moe_workspace_bytes_for_path(int64_t T, int H, int I, int E, int k, int dtype,
+                                       int path);
 
 int mm_moe_forward(const void* x, const void* Wr,
                    const void* const* Wg, const void* const* Wu, const void* const* Wd,

@@ -13,7 +13,8 @@ LIB_PATH = os.path.join(_PKG, "libmm.so")
 (MM_OK, MM_ERR_INVALID_ARG, MM_ERR_UNSUPPORTED, MM_ERR_WORKSPACE, MM_ERR_CUDA, MM_ERR_TIMEOUT,
  MM_ERR_RANGE) = range(7)
 MM_DTYPE_F32, MM_DTYPE_BF16 = 0, 1
-MM_PATH_AUTO, MM_PATH_TENSOR, MM_PATH_STREAM, MM_PATH_SIMT, MM_PATH_STREAM_TC = 0, 1, 2, 3, 4
+(MM_PATH_AUTO, MM_PATH_TENSOR, MM_PATH_STREAM, MM_PATH_SIMT, MM_PATH_STREAM_TC,
+ MM_PATH_TENSOR_GATHER) = 0, 1, 2, 3, 4, 5
 MM_MAX_EXPERTS = 64
 MM_MAX_TOPK = 8
 MM_NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -43,6 +44,7 @@ SIGNATURES = {
                                 _i32]),
     "mm_swiglu_ffn_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _vp]),
     "mm_moe_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32, _i32, _i32]),
+    "mm_moe_workspace_bytes_for_path": (_sz, [_i64, _i32, _i32, _i32, _i32, _i32, _i32]),
     "mm_moe_forward": (_i32, [_vp, _vp, _pp, _pp, _pp, _i64, _i32, _i32, _i32, _i32, _f32, _i32,
                               _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "mm_moe_forward_ex": (_i32, [_vp, _vp, _pp, _pp, _pp, _i64, _i32, _i32, _i32, _i32, _f32,

@@ -14,7 +14,8 @@ from . import _lib as L
 
 _DTYPES = {torch.bfloat16: L.MM_DTYPE_BF16, torch.float32: L.MM_DTYPE_F32}
 _PATHS = {"auto": L.MM_PATH_AUTO, "tensor": L.MM_PATH_TENSOR, "stream": L.MM_PATH_STREAM,
-          "simt": L.MM_PATH_SIMT, "stream_tc": L.MM_PATH_STREAM_TC}
+          "simt": L.MM_PATH_SIMT, "stream_tc": L.MM_PATH_STREAM_TC,
+          "tensor_gather": L.MM_PATH_TENSOR_GATHER}
 
 
 def _dev(t: torch.Tensor, name: str, dtype=None) -> int:

@@ -39,7 +39,7 @@ inline size_t h_bytes(int dtype) { return dtype == kDtypeBF16 ? 2 : 4; }
 // ([T*k, H], grouped by slot, then expert, then token), h ([T*k, I]) and,
 // for bf16, the fp32 running sum of y ([T, H], k >= 2) and fp16 copies of the
 // E down-projection matrices.
-MoeLayout moe_layout(int64_t T, int H, int I, int E, int k, int dtype) {
+MoeLayout moe_layout(int64_t T, int H, int I, int E, int k, int dtype, bool with_xp = true) {
   MoeLayout L;
   const size_t es = elem_bytes(dtype);
   const size_t nblk = static_cast<size_t>(route_blocks(T));
@@ -54,7 +54,7 @@ MoeLayout moe_layout(int64_t T, int H, int I, int E, int k, int dtype) {
   L.inv_rms = off;  off += align_up(4 * static_cast<size_t>(T));            // block norm
   L.wr_hl = off;    off += align_up(4 * static_cast<size_t>(E) * H);        // block norm, bf16 [2E, H]
   L.perm = off;     off += align_up(4 * rows);
-  L.xp = off;       off += align_up(es * rows * H);
+  L.xp = off;       if (with_xp) off += align_up(es * rows * H);   // not with the gathering gate/up
   L.h = off;        off += align_up(h_bytes(dtype) * rows * I);
   L.acc32 = off;    if (k >= 2 && dtype == kDtypeBF16) off += align_up(4 * static_cast<size_t>(T) * H);
   // bf16: fp16 copy of the E down matrices
@@ -194,6 +194,7 @@ size_t moe_path_bytes(int64_t T, int H, int I, int E, int k, int dtype, int p) {
   switch (p) {
     case MM_PATH_STREAM: b = stream_simt_bytes(T, H, I, E, k, dtype); break;
     case MM_PATH_STREAM_TC: b = stream_tc_bytes(T, H, I, E, k, dtype); break;
+    case MM_PATH_TENSOR_GATHER: return moe_layout(T, H, I, E, k, dtype, false).total;
     default: return moe_layout(T, H, I, E, k, dtype).total;
   }
   return b ? sizeof(WsHeader) + b : 0;
@@ -314,7 +315,8 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
   if (!valid_dtype(dtype) || T < 0 || H < 1 || I < 1) return MM_ERR_INVALID_ARG;
   if (H % 8 != 0 || I % 8 != 0) return MM_ERR_UNSUPPORTED;
   if (T > (int64_t{1} << 30)) return MM_ERR_UNSUPPORTED;
-  if (path < MM_PATH_AUTO || path > MM_PATH_STREAM_TC) return MM_ERR_INVALID_ARG;
+  if (path < MM_PATH_AUTO || path > MM_PATH_TENSOR_GATHER) return MM_ERR_INVALID_ARG;
+  if (path == MM_PATH_TENSOR_GATHER) path = MM_PATH_TENSOR;   // nothing to gather in a dense FFN
   if (T == 0) return MM_OK;
   if (!x || !Wg || !Wu || !Wd || !y) return MM_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) || !aligned16(y))
@@ -379,6 +381,15 @@ int mm_swiglu_ffn(const void* x, const void* Wg, const void* Wu, const void* Wd,
                           MM_PATH_AUTO);
 }
 
+size_t mm_moe_workspace_bytes_for_path(int64_t T, int H, int I, int E, int k, int dtype,
+                                       int path) {
+  if (T < 1 || H < 1 || I < 1 || E < 1 || E > MM_MAX_EXPERTS || k < 1 || k > E ||
+      k > MM_MAX_TOPK || !valid_dtype(dtype) || path < MM_PATH_AUTO || path > MM_PATH_TENSOR_GATHER)
+    return 0;
+  if (path == MM_PATH_AUTO) return moe_ws_bytes(T, H, I, E, k, dtype);
+  return moe_path_bytes(T, H, I, E, k, dtype, path);
+}
+
 size_t mm_moe_workspace_bytes(int64_t T, int H, int I, int E, int k, int dtype) {
   if (T < 1 || H < 1 || I < 1 || E < 1 || E > MM_MAX_EXPERTS || k < 1 || k > E ||
       !valid_dtype(dtype))
@@ -441,7 +452,15 @@ static int moe_forward_impl(const void* x, const void* Wr, const void* const* Wg
   }
   if (I < 1) return MM_ERR_INVALID_ARG;
   if (I % 8 != 0) return MM_ERR_UNSUPPORTED;
-  if (path < MM_PATH_AUTO || path > MM_PATH_STREAM_TC) return MM_ERR_INVALID_ARG;
+  if (path < MM_PATH_AUTO || path > MM_PATH_TENSOR_GATHER) return MM_ERR_INVALID_ARG;
+  // gathering x rows needs them as the layer's input: with the block norm the
+  // dispatch writes normalised rows instead
+  bool gather = path == MM_PATH_TENSOR_GATHER;
+  if (gather) {
+    if (dtype != kDtypeBF16) return MM_ERR_UNSUPPORTED;
+    path = MM_PATH_TENSOR;
+    if (norm_w != nullptr) gather = false;
+  }
   if (!Wg || !Wu || !Wd || !y || !aligned16(y)) return MM_ERR_INVALID_ARG;
   for (int e = 0; e < E; ++e) {
     if (!Wg[e] || !Wu[e] || !Wd[e]) return MM_ERR_INVALID_ARG;
@@ -451,7 +470,7 @@ static int moe_forward_impl(const void* x, const void* Wr, const void* const* Wg
   const int p = resolve_path(path, dtype, T, H, I, E, k, false);
   if (p == MM_PATH_TENSOR && (dtype != kDtypeBF16 || !tensor_shape_ok(H, I)))
     return MM_ERR_UNSUPPORTED;
-  const size_t need = moe_path_bytes(T, H, I, E, k, dtype, p);
+  const size_t need = moe_path_bytes(T, H, I, E, k, dtype, gather ? MM_PATH_TENSOR_GATHER : p);
   if (need == 0) return MM_ERR_UNSUPPORTED;
   if (workspace_bytes < need) return MM_ERR_WORKSPACE;
 
@@ -474,7 +493,7 @@ static int moe_forward_impl(const void* x, const void* Wr, const void* const* Wg
     if (e != cudaSuccess) return cuda_fail(e, "decode ffn");
     return MM_OK;
   }
-  const MoeLayout L = moe_layout(T, H, I, E, k, dtype);
+  const MoeLayout L = moe_layout(T, H, I, E, k, dtype, !gather);
   int32_t* offsets = reinterpret_cast<int32_t*>(ws_at(workspace, L.offsets));
   int32_t* counts = reinterpret_cast<int32_t*>(ws_at(workspace, L.counts));
   int32_t* blk_cnt = reinterpret_cast<int32_t*>(ws_at(workspace, L.blk_cnt));
@@ -510,7 +529,8 @@ static int moe_forward_impl(const void* x, const void* Wr, const void* const* Wg
   if (e != cudaSuccess) return cuda_fail(e, "router");
   const DispatchOut dout{offsets, counts, aux_loss, coef, hdr, rv, nrm};
   e = counted_launch(MM_KERNEL_DISPATCH, st, [&] {
-    return launch_dispatch(dtype, x, T, H, E, k, topk_idx, blk_cnt, blk_prob, dout, perm, xp, st);
+    return launch_dispatch(dtype, x, T, H, E, k, topk_idx, blk_cnt, blk_prob, dout, perm,
+                           gather ? nullptr : xp, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "dispatch");
 
@@ -518,9 +538,11 @@ static int moe_forward_impl(const void* x, const void* Wr, const void* const* Wg
   // the same kernel makes the fp16 copy of Wd that the down GEMM reads, with
   // its epilogue warps while the tensor pipe runs (HBM is mostly idle then)
   GroupRows gu{offsets, k * E, 0, E};
+  const RowGather rg{perm, k, static_cast<int>(rows)};
   if (p == MM_PATH_TENSOR)
     e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
-      return launch_gateup_tc(xp, rows, H, I, gu, Wg, Wu, h, Wd, E, wd16, hdr, st);
+      return launch_gateup_tc(gather ? x : xp, rows, H, I, gu, Wg, Wu, h, Wd, E, wd16, hdr, st,
+                              gather ? &rg : nullptr);
     });
   else
     e = counted_launch(MM_KERNEL_GATEUP, st, [&] {

@@ -79,6 +79,7 @@ struct TcParams {
   CUtensorMap a;            // A [a_rows, K]
   CUtensorMap b0[MAXW];     // gate/up: Wg; down: fp16 Wd  (box rows = N/2)
   CUtensorMap b1[MAXW];     // gate/up: Wu; down: unused
+  CUtensorMap ag;           // gate/up gathering rows: x [T, K], box 64 x 1 row
 };
 
 struct TileInfo {
@@ -523,7 +524,8 @@ template <int OP, int MAXW, int NW = kN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g, const int K,
                     const int NCOLS, __half* __restrict__ hout, const DownEpilogue ep,
-                    const WdConvert cv, WsHeader* hdr, const int dep_mainloop, const UpBwd ub) {
+                    const WdConvert cv, WsHeader* hdr, const int dep_mainloop, const UpBwd ub,
+                    const RowGather gat) {
   static_assert(NW == kN || (OP == kOpDown && NW == kNWide), "tile width");
   constexpr bool kWide = NW == kNWide;
   constexpr bool kUpLike = OP != kOpDown;       // gate/up tiles (forward or backward)
@@ -574,7 +576,7 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
     if (dep_mainloop && g.offsets != nullptr) asm volatile("griddepcontrol.wait;" ::: "memory");
     build_schedule(g, n_tiles, s_off, s_tstart);
   }
-  if (warp == kWarpProducer && lane == 0) tma_prefetch_desc(&P.a);
+  if (warp == kWarpProducer && lane == 0) tma_prefetch_desc(gat.perm != nullptr ? &P.ag : &P.a);
   if (warp == kWarpMma) {
     tmem_alloc_cta2(&s_tmem, kTmemCols);
     tmem_relinquish_cta2();
@@ -592,7 +594,56 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
   // kernel's inputs being complete); otherwise the next kernel may launch at
   // once.  griddepcontrol is a no-op for a launch without the attribute.
   if (!dep_mainloop && threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (warp == kWarpProducer) {
+  if (warp == kWarpProducer && OP == kOpUp && gat.perm != nullptr) {
+    // ------------------------------------------------ TMA producer, A rows gathered
+    // Lane l gathers rows 4l .. 4l + 3 of the CTA's 128 (x rows of their
+    // tokens; rows past the problem read row 0, their results are never
+    // stored); lane 0 waits for the stage and loads B.  Both k-blocks of a
+    // stage are always requested (columns past K read as zero), so every
+    // stage carries the same bytes.
+    if (dep_mainloop) {
+      if (lane == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
+    int it = 0;
+    bool ok = true;
+    for (int tile = cluster; ok && tile < total; tile += n_clusters) {
+      const TileInfo ti = decode_tile(tile, s_off, s_tstart, g.G, g.n_weights, n_tiles, kOutCols,
+                                      static_cast<int>(rank));
+      int tok[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = ti.row0 + 4 * lane + j;
+        tok[j] = r < gat.n_rows ? gat.perm[r] / gat.k : 0;
+      }
+      const CUtensorMap* bmap = rank == 1 ? &P.b1[ti.w] : &P.b0[ti.w];
+      for (int kb = 0; kb < nkb; kb += kKbStage, ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
+        bool w_ok = true;
+        if (lane == 0) w_ok = mbar_wait(&empty[s], ph ^ 1, abort, hdr, 1);
+        if (!__shfl_sync(0xffffffffu, w_ok ? 1 : 0, 0)) { ok = false; break; }
+        const uint32_t fb = mapa_shared(smem_u32(&full[s]), 0);
+        if (lane == 0) {
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * (kAStage + kBStage));
+          tma_load_3d_cta2(sB + s * kBStage, bmap, fb, 0, ti.n0, kb);
+        }
+#pragma unroll
+        for (int kl = 0; kl < kKbStage; ++kl)
+          tma_gather4_cta2(sA + s * kAStage + kl * kATile + lane * 4 * 128, &P.ag, fb,
+                           (kb + kl) * kTcBK, tok[0], tok[1], tok[2], tok[3]);
+      }
+    }
+    if (!ok && rank == 0 && lane == 0) {
+      for (int j = 0; j < kStages; ++j) {
+        const int i2 = it - 1 - j;
+        if (i2 < 0) break;
+        mbar_wait(&full[i2 % kStages], (i2 / kStages) & 1, nullptr, hdr, 2);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kWarpProducer) {
     // ------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       if (dep_mainloop) {
@@ -719,6 +770,16 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
           for (int j = 0; j < kHC / 32; ++j)
             if (ti.n0 + half * kHC + j * 32 < NCOLS)
               asm volatile("prefetch.global.L2 [%0];" ::"l"(a + j * 32) : "memory");
+        }
+        // the block's residual rows: pulled into L2 while the MMAs run
+        if (ep.resid != nullptr && dr.valid && ti.n0 + half * kHC < NCOLS &&
+            (ep.mode == kCombineStore || ep.mode == kCombineLast)) {
+          const __nv_bfloat16* a = static_cast<const __nv_bfloat16*>(ep.resid) + dr.tok * NCOLS +
+                                   ti.n0 + half * kHC;
+#pragma unroll
+          for (int j = 0; j < kHC / 64; ++j)
+            if (ti.n0 + half * kHC + j * 64 < NCOLS)
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(a + j * 64) : "memory");
         }
         dl = down_lanes(dr, ti, NCOLS, half, lane, kHC);
         if (ti.n0 + half * kHC < NCOLS) down_prefetch(dl, ep, 0, pre);
@@ -918,13 +979,20 @@ static int clusters_for(int64_t a_rows, const GroupRows& g, int n_tiles) {
 template <int MAXW>
 static cudaError_t gateup_impl(const void* A, int64_t a_rows, int H, int I, const GroupRows& g,
                                const void* const* Wg, const void* const* Wu, void* h_out,
-                               const WdConvert& cv, WsHeader* hdr, cudaStream_t st) {
+                               const WdConvert& cv, WsHeader* hdr, cudaStream_t st,
+                               const RowGather& gat, int64_t x_rows) {
   TcParams<MAXW> p;
   memset(&p, 0, sizeof(p));
   if (!make_map_16(&p.out, h_out, I, a_rows, 32, true, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   constexpr int kb = OpTraits<kOpUp>::kKb;
-  if (!kblock_map(&p.a, A, H, a_rows, kTcBM, false, kb)) return cudaErrorInvalidValue;
+  if (gat.perm != nullptr) {
+    // A = x [x_rows, H] gathered one row per box row
+    if (!make_map_16(&p.ag, A, H, x_rows, 1, false, kTcBK, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  } else if (!kblock_map(&p.a, A, H, a_rows, kTcBM, false, kb)) {
+    return cudaErrorInvalidValue;
+  }
   for (int e = 0; e < g.n_weights; ++e) {
     if (!kblock_map(&p.b0[e], Wg[e], H, I, kN / 2, false, kb)) return cudaErrorInvalidValue;
     if (!kblock_map(&p.b1[e], Wu[e], H, I, kN / 2, false, kb)) return cudaErrorInvalidValue;
@@ -935,7 +1003,7 @@ static cudaError_t gateup_impl(const void* A, int64_t a_rows, int H, int I, cons
   const int n_tiles = (I + kN / 2 - 1) / (kN / 2);
   DownEpilogue none{};
   return launch_pdl(fn, 2 * clusters_for(a_rows, g, n_tiles), kSmem, st, p, g, H, I,
-                    static_cast<__half*>(h_out), none, cv, hdr, 1, UpBwd{});
+                    static_cast<__half*>(h_out), none, cv, hdr, 1, UpBwd{}, gat);
 }
 
 template <int MAXW>
@@ -957,7 +1025,7 @@ static cudaError_t gateup_bwd_impl(const void* A, int64_t a_rows, int H, int I, 
   DownEpilogue none{};
   WdConvert no_cv{};
   return launch_pdl(fn, 2 * clusters_for(a_rows, g, n_tiles), kSmem, st, p, g, H, I,
-                    static_cast<__half*>(nullptr), none, no_cv, hdr, 1, ub);
+                    static_cast<__half*>(nullptr), none, no_cv, hdr, 1, ub, RowGather{});
 }
 
 cudaError_t launch_gateup_bwd_tc(const void* A, int64_t a_rows, int H, int I, const GroupRows& g,
@@ -1000,13 +1068,16 @@ static cudaError_t down_impl(const void* h, int64_t a_rows, int H, int I, const 
   const int dep = (ep.mode == kCombineAccum || ep.mode == kCombineLast) ? 0 : 1;
   WdConvert no_cv{};
   return launch_pdl(fn, 2 * clusters_for(a_rows, g, n_tiles), smem, st, p, g, I, H,
-                    static_cast<__half*>(nullptr), ep, no_cv, hdr, dep, UpBwd{});
+                    static_cast<__half*>(nullptr), ep, no_cv, hdr, dep, UpBwd{}, RowGather{});
 }
 
 cudaError_t launch_gateup_tc(const void* A, int64_t a_rows, int H, int I, const GroupRows& g,
                              const void* const* Wg, const void* const* Wu, void* h_out,
                              const void* const* wd_src, int n_wd, void* wd16, WsHeader* hdr,
-                             cudaStream_t st) {
+                             cudaStream_t st, const RowGather* gather) {
+  const RowGather gat = gather ? *gather : RowGather{};
+  // gathering: A is x [T, H] with T = a_rows / k rows
+  const int64_t x_rows = gather ? a_rows / gather->k : a_rows;
   WdConvert cv{};
   if (n_wd > 0) {
     if (n_wd > MM_MAX_EXPERTS || (static_cast<int64_t>(H) * I) % 8 != 0 || wd16 == nullptr)
@@ -1016,8 +1087,8 @@ cudaError_t launch_gateup_tc(const void* A, int64_t a_rows, int H, int I, const 
     cv.nvec = static_cast<int64_t>(H) * I / 8;
     cv.n_mat = n_wd;
   }
-  if (g.n_weights <= 8) return gateup_impl<8>(A, a_rows, H, I, g, Wg, Wu, h_out, cv, hdr, st);
-  return gateup_impl<MM_MAX_EXPERTS>(A, a_rows, H, I, g, Wg, Wu, h_out, cv, hdr, st);
+  if (g.n_weights <= 8) return gateup_impl<8>(A, a_rows, H, I, g, Wg, Wu, h_out, cv, hdr, st, gat, x_rows);
+  return gateup_impl<MM_MAX_EXPERTS>(A, a_rows, H, I, g, Wg, Wu, h_out, cv, hdr, st, gat, x_rows);
 }
 
 cudaError_t launch_down_tc(const void* h, int64_t a_rows, int H, int I, const GroupRows& g,

@@ -403,6 +403,20 @@ __device__ __forceinline__ void tma_load_3d_cta2(void* smem_dst, const void* tma
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster_addr), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// Four rows (r0..r3) x 64 columns from column c0 of a 2-D tensor map whose
+// box is one row high, into four consecutive 128-byte rows of this CTA's
+// shared memory (the map's swizzle applies by address, as for a tile);
+// completion on an mbarrier that may live in the peer CTA of the pair.
+__device__ __forceinline__ void tma_gather4_cta2(void* smem_dst, const void* tmap,
+                                                 uint32_t bar_cluster_addr, int32_t c0, int32_t r0,
+                                                 int32_t r1, int32_t r2, int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster_addr), "r"(c0), "r"(r0), "r"(r1),
+      "r"(r2), "r"(r3)
+      : "memory");
+}
 // TMEM allocation shared by the CTA pair: one warp of EACH CTA executes these.
 __device__ __forceinline__ void tmem_alloc_cta2(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(

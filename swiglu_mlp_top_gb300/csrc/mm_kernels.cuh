@@ -149,6 +149,14 @@ cudaError_t launch_dispatch(int dtype, const void* x, int64_t T, int H, int E, i
                             const int32_t* topk_idx, const int32_t* blk_cnt, const float* blk_prob,
                             const DispatchOut& D, int32_t* perm, void* Xp, cudaStream_t st);
 
+// Permute-free gate/up: row r of the grouped problem is x row perm[r] / k
+// (gathered by TMA, four rows per request) instead of a copied row of Xp.
+struct RowGather {
+  const int32_t* perm;      // [n_rows] row -> assignment t*k + s, or null: A rows as stored
+  int k;
+  int n_rows;               // rows of the grouped problem (T*k)
+};
+
 // Tensor-core grouped GEMMs.  A is [rows, K] row-major; each group multiplies
 // its rows by its own weight matrices.  gate/up: bf16 A and weights, fp16 h
 // out.  down: fp16 h and fp16 Wd.
@@ -156,7 +164,7 @@ cudaError_t launch_dispatch(int dtype, const void* x, int64_t T, int H, int E, i
 cudaError_t launch_gateup_tc(const void* A, int64_t a_rows, int H, int I, const GroupRows& g,
                              const void* const* Wg, const void* const* Wu, void* h_out,
                              const void* const* wd_src, int n_wd, void* wd16, WsHeader* hdr,
-                             cudaStream_t st);
+                             cudaStream_t st, const RowGather* gather = nullptr);
 cudaError_t launch_down_tc(const void* h, int64_t a_rows, int H, int I, const GroupRows& g,
                            const void* const* Wd, const DownEpilogue& ep, WsHeader* hdr,
                            cudaStream_t st);

@@ -649,15 +649,25 @@ dispatch_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, int k,
 
   const int na = ntok * k;
   const Tin* norm_w = static_cast<const Tin*>(D.norm.w);
+  if (Xp == nullptr) return;                   // permute-free: the GEMM gathers x rows itself
   if (stage_x) {
     // one bulk copy per assignment row, shared -> global
     if (!__syncthreads_and(mbar_wait(&xbar, 0, nullptr, D.hdr, 61))) return;
     if (norm_w != nullptr) {
-      // block norm: the staged rows become x * inv_rms * w in place
-      for (int i = tid; i < ntok * H; i += kRouteThreads) {
-        const int tl = i / H, h = i - tl * H;
-        const float v = to_f32(xs[i]) * D.norm.inv_rms[tok0 + tl] * to_f32(norm_w[h]);
-        xs[i] = static_cast<Tin>(v);
+      // block norm: the staged rows become x * inv_rms * w in place, by
+      // 8-element chunks (a warp per row at a time)
+      const int nch = H / 8;
+      for (int tl = warp; tl < ntok; tl += kWarps) {
+        const float inv = D.norm.inv_rms[tok0 + tl];
+        Tin* row = xs + static_cast<int64_t>(tl) * H;
+        for (int c = lane; c < nch; c += 32) {
+          float v[8];
+          load_vec8(row + c * 8, v);
+          float g[8];
+          load_vec8(norm_w + c * 8, g);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) row[c * 8 + j] = static_cast<Tin>(v[j] * inv * g[j]);
+        }
       }
       fence_proxy_async_smem();
       __syncthreads();
@@ -1087,7 +1097,7 @@ static cudaError_t launch_dispatch_t(const Tin* x, int64_t T, int H, int E, int 
                                      Tin* Xp, cudaStream_t st) {
   const int nblk = static_cast<int>((T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock);
   const size_t smem = static_cast<size_t>(kRouteTokensPerBlock) * H * sizeof(Tin);
-  const int stage = smem <= 110 * 1024 ? 1 : 0;
+  const int stage = (Xp != nullptr && smem <= 110 * 1024) ? 1 : 0;   // no rows to copy: no staging
   auto fn = dispatch_kernel<Tin>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), stage ? smem : 0);
   if (e != cudaSuccess) return e;

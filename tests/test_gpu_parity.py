@@ -401,3 +401,49 @@ def test_watchdog_reports_timeout_and_recovers():
     g = to_dev(inp)
     mm.swiglu_ffn(g["x"], g["Wg"], g["Wu"], g["Wd"], workspace=None)
     torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ permute-free gate/up
+@pytest.mark.parametrize("T,H,I,E,k,bias", [
+    (1000, 256, 384, 4, 1, None),
+    (777, 256, 320, 8, 2, (1.5, 0.5, 0, 0, 0, 0, 0, 0)),
+    (300, 256, 192, 64, 8, None),
+    (1, 256, 384, 8, 2, None),
+    (2000, 256, 320, 8, 2, (0.0, 0.0, 0.0, 8.0, 0.0, -8.0, -8.0, -8.0)),
+])
+def test_moe_gather_path_matches_copy_path(T, H, I, E, k, bias):
+    """The gate/up GEMM gathering x rows by token index (TMA gather4, no
+    permuted copy) reads the same rows as the copy path: the same MMAs on
+    the same values, so every output is bit-identical."""
+    inp = moe_inputs(T, H, I, E, "bf16", seed=1100 + T, bias=bias)
+    a = run_moe(inp, k, 0.01, "tensor")
+    b = run_moe(inp, k, 0.01, "tensor_gather")
+    assert all(np.array_equal(u, v) for u, v in zip(a[:3], b[:3])) and a[3] == b[3]
+
+
+@pytest.mark.parametrize("name", ["moe_e4k1_t8192", "moe_e8k2_t16384_skew"])
+def test_moe_gather_path_full_size(name):
+    w = WORKLOADS[name]
+    full_moe_check(make_workload_inputs(w), w.k, w.coef, "bf16", path="tensor_gather")
+
+
+def test_moe_gather_path_runs_in_its_smaller_workspace():
+    """Without the permuted copy of x the gathering path needs T*k*H*2 bytes
+    less workspace; the copy path refuses that smaller workspace."""
+    from swiglu_mlp_top_gb300 import _lib as L
+    T, H, I, E, k = 1500, 256, 320, 8, 2
+    lib = L.load()
+    small = lib.mm_moe_workspace_bytes_for_path(T, H, I, E, k, L.MM_DTYPE_BF16, L.MM_PATH_TENSOR_GATHER)
+    full = lib.mm_moe_workspace_bytes_for_path(T, H, I, E, k, L.MM_DTYPE_BF16, L.MM_PATH_TENSOR)
+    assert full - small >= T * k * H * 2
+    inp = moe_inputs(T, H, I, E, "bf16", seed=1200)
+    g = to_dev(inp)
+    ws = mm.new_workspace(small)
+    y, idx, w, aux = mm.moe_forward(g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], k, 0.01,
+                                    workspace=ws, path="tensor_gather")
+    torch.cuda.synchronize()
+    ref = run_moe(inp, k, 0.01, "tensor")
+    assert np.array_equal(y.double().cpu().numpy(), ref[0])
+    with pytest.raises(RuntimeError, match="MM_ERR_WORKSPACE"):
+        mm.moe_forward(g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], k, 0.01, workspace=ws,
+                       path="tensor")
