@@ -128,6 +128,29 @@ int mm_swiglu_ffn_block(const void* x, const void* norm_w, float norm_eps,
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Prepared down weights
+ *
+ * The pages have no counterpart: the bf16 tensor-core prefill path keeps h
+ * in fp16 (precision, see the dense FFN above), so it multiplies h by an fp16
+ * copy of Wd, which both forwards otherwise make inside every call.  A caller
+ * whose weights change less often than it runs the layer converts once:
+ *   Wd16 [H, I] fp16 = Wd [H, I] bf16, exact for |w| >= 2^-14 (smaller
+ *   magnitudes become fp16 subnormals, absolute error <= 2^-25).
+ * A value at or beyond the fp16 range (|w| >= 65520) is recorded as
+ * MM_ERR_RANGE in `status_ws` (a workspace of >= 256 bytes read by
+ * mm_check_status; nullable: no report).  Asynchronous on `stream`.
+ * H * I must be a multiple of 8; pointers 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+int mm_prepare_down_weights(const void* Wd, void* Wd16, int H, int I, void* status_ws,
+                            void* stream);
+
+/* mm_swiglu_ffn_ex with prepared down weights: Wd16 (nullable) is used by the
+ * tensor-core path in place of the in-call fp16 copy of Wd. */
+int mm_swiglu_ffn_prepared(const void* x, const void* Wg, const void* Wu, const void* Wd,
+                           const void* Wd16, void* y, int64_t T, int H, int I, int dtype,
+                           void* workspace, size_t workspace_bytes, void* stream, int path);
+
+/* ------------------------------------------------------------------------
  * Dense SwiGLU FFN without caller-provided scratch
  *
  * The pages describe no counterpart of this entry point; it exists for
@@ -246,6 +269,11 @@ typedef struct {
   const void* norm_weight;    /* device [H], x's dtype, or NULL                    */
   float norm_eps;
   int residual;
+  /* Prepared down weights (mm_prepare_down_weights): a HOST array of E device
+   * pointers to fp16 [H, I] copies of Wd[e], or NULL.  The bf16 tensor-core
+   * path then multiplies by them instead of making the fp16 copy inside the
+   * call; the other paths read Wd. */
+  const void* const* wd_f16;
 } mm_moe_options;
 
 int mm_moe_forward_opts(const void* x, const void* Wr,

@@ -28,7 +28,7 @@ class MoeOptions(C.Structure):
     _fields_ = [("path", C.c_int), ("logit_noise", C.c_void_p), ("z_coef", C.c_float),
                 ("z_loss", C.c_void_p), ("router_probs", C.c_void_p),
                 ("router_lse", C.c_void_p), ("norm_weight", C.c_void_p),
-                ("norm_eps", C.c_float), ("residual", C.c_int)]
+                ("norm_eps", C.c_float), ("residual", C.c_int), ("wd_f16", C.c_void_p)]
 
 
 _opt = C.POINTER(MoeOptions)
@@ -43,6 +43,9 @@ SIGNATURES = {
     "mm_swiglu_ffn_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _vp, _sz, _vp,
                                 _i32]),
     "mm_swiglu_ffn_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _vp]),
+    "mm_prepare_down_weights": (_i32, [_vp, _vp, _i32, _i32, _vp, _vp]),
+    "mm_swiglu_ffn_prepared": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _vp,
+                                      _sz, _vp, _i32]),
     "mm_moe_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32, _i32, _i32]),
     "mm_moe_workspace_bytes_for_path": (_sz, [_i64, _i32, _i32, _i32, _i32, _i32, _i32]),
     "mm_moe_forward": (_i32, [_vp, _vp, _pp, _pp, _pp, _i64, _i32, _i32, _i32, _i32, _f32, _i32,

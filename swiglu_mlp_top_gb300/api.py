@@ -53,10 +53,27 @@ def new_workspace(nbytes: int, device=None) -> torch.Tensor:
     return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
 
 
+def prepare_down_weights(Wd: torch.Tensor, *, status_workspace: Optional[torch.Tensor] = None,
+                         stream=None) -> torch.Tensor:
+    """The fp16 copy of a bf16 down-projection matrix for the tensor-core
+    prefill path (mm_prepare_down_weights); values beyond the fp16 range are
+    reported through check_status(status_workspace)."""
+    H, I = Wd.shape
+    out = torch.empty(H, I, dtype=torch.float16, device=Wd.device)
+    rc = L.load().mm_prepare_down_weights(
+        _dev(Wd, "Wd", torch.bfloat16), out.data_ptr(), H, I,
+        None if status_workspace is None else _dev(status_workspace, "status_workspace"),
+        _stream(stream))
+    L.check(rc, "mm_prepare_down_weights")
+    return out
+
+
 def swiglu_ffn(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Tensor, *,
                out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-               path: str = "auto", stream=None) -> torch.Tensor:
-    """y = Wd (SiLU(Wg x) ⊙ Wu x) for x [T, H] (mm_swiglu_ffn)."""
+               path: str = "auto", stream=None,
+               wd_f16: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """y = Wd (SiLU(Wg x) ⊙ Wu x) for x [T, H] (mm_swiglu_ffn; with wd_f16,
+    the prepared fp16 down weights, mm_swiglu_ffn_prepared)."""
     lib = L.load()
     T, H = x.shape
     I = Wg.shape[0]
@@ -66,10 +83,17 @@ def swiglu_ffn(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Te
     need = lib.mm_swiglu_ffn_workspace_bytes(T, H, I, dt)
     if workspace is None:
         workspace = new_workspace(need, x.device)
-    rc = lib.mm_swiglu_ffn_ex(
-        _dev(x, "x"), _dev(Wg, "Wg", x.dtype), _dev(Wu, "Wu", x.dtype), _dev(Wd, "Wd", x.dtype),
-        _dev(out, "out", x.dtype), T, H, I, dt, _dev(workspace, "workspace"),
-        workspace.numel() * workspace.element_size(), _stream(stream), _PATHS[path])
+    if wd_f16 is None:
+        rc = lib.mm_swiglu_ffn_ex(
+            _dev(x, "x"), _dev(Wg, "Wg", x.dtype), _dev(Wu, "Wu", x.dtype), _dev(Wd, "Wd", x.dtype),
+            _dev(out, "out", x.dtype), T, H, I, dt, _dev(workspace, "workspace"),
+            workspace.numel() * workspace.element_size(), _stream(stream), _PATHS[path])
+    else:
+        rc = lib.mm_swiglu_ffn_prepared(
+            _dev(x, "x"), _dev(Wg, "Wg", x.dtype), _dev(Wu, "Wu", x.dtype), _dev(Wd, "Wd", x.dtype),
+            _dev(wd_f16, "wd_f16", torch.float16), _dev(out, "out", x.dtype), T, H, I, dt,
+            _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+            _stream(stream), _PATHS[path])
     L.check(rc, "mm_swiglu_ffn")
     return out
 
@@ -115,12 +139,17 @@ def swiglu_ffn_noalloc(x: torch.Tensor, Wg: torch.Tensor, Wu: torch.Tensor, Wd: 
 
 
 def _router_options(T: int, E: int, dev, path: str, logit_noise, z_coef, stats,
-                    norm_weight=None, norm_eps=1e-5, residual=False, dtype=None):
-    """mm_moe_options for the router variants and the block prologue /
-    epilogue; fills `stats` (a dict) with the output tensors it asks for:
-    z_loss [], probs [T, E], lse [T] (fp32)."""
+                    norm_weight=None, norm_eps=1e-5, residual=False, dtype=None, wd_f16=None):
+    """mm_moe_options for the router variants, the block prologue / epilogue
+    and prepared down weights; fills `stats` (a dict) with the output tensors
+    it asks for: z_loss [], probs [T, E], lse [T] (fp32).  Returns (options,
+    objects to keep alive during the call)."""
     o = L.MoeOptions()
     o.path = _PATHS[path]
+    keep = None
+    if wd_f16 is not None:
+        pw, keep = L.ptr_array([_dev(w, "wd_f16", torch.float16) for w in wd_f16])
+        o.wd_f16 = C.cast(pw, C.c_void_p)
     if norm_weight is not None:
         o.norm_weight = _dev(norm_weight, "norm_weight", dtype)
         o.norm_eps = float(norm_eps)
@@ -138,7 +167,7 @@ def _router_options(T: int, E: int, dev, path: str, logit_noise, z_coef, stats,
         o.z_loss = _dev(stats["z_loss"], "z_loss", torch.float32)
         o.router_probs = _dev(stats["probs"], "probs", torch.float32)
         o.router_lse = _dev(stats["lse"], "lse", torch.float32)
-    return o
+    return o, keep
 
 
 def moe_forward(x: torch.Tensor, Wr: torch.Tensor, Wg: Sequence[torch.Tensor],
@@ -149,7 +178,7 @@ def moe_forward(x: torch.Tensor, Wr: torch.Tensor, Wg: Sequence[torch.Tensor],
                 path: str = "auto", stream=None, logit_noise: Optional[torch.Tensor] = None,
                 z_coef: float = 0.0, stats: Optional[dict] = None,
                 norm_weight: Optional[torch.Tensor] = None, norm_eps: float = 1e-5,
-                residual: bool = False):
+                residual: bool = False, wd_f16: Optional[Sequence[torch.Tensor]] = None):
     """Top-k MoE forward (mm_moe_forward; mm_moe_forward_opts when router
     noise, z-loss, router statistics or the block's norm / residual are asked
     for).
@@ -157,7 +186,8 @@ def moe_forward(x: torch.Tensor, Wr: torch.Tensor, Wg: Sequence[torch.Tensor],
     Returns (y [T,H], topk_idx [T,k] int32, topk_w [T,k] fp32, aux_loss [] fp32).
     With a dict `stats`, it also receives z_loss [] (z_coef * mean_t lse_t^2),
     probs [T, E] and lse [T] (fp32 device tensors).  With norm_weight the
-    layer runs on RMSNorm(x); with residual, y = x + MoE(...).
+    layer runs on RMSNorm(x); with residual, y = x + MoE(...).  wd_f16: the
+    experts' prepared fp16 down weights (prepare_down_weights).
     """
     lib = L.load()
     T, H = x.shape
@@ -181,12 +211,14 @@ def moe_forward(x: torch.Tensor, Wr: torch.Tensor, Wg: Sequence[torch.Tensor],
             _dev(topk_w, "topk_w", torch.float32), _dev(aux_loss, "aux_loss", torch.float32),
             _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
             _stream(stream))
-    if logit_noise is None and not z_coef and stats is None and norm_weight is None and not residual:
+    if (logit_noise is None and not z_coef and stats is None and norm_weight is None
+            and not residual and wd_f16 is None):
         rc = lib.mm_moe_forward_ex(*args, _PATHS[path])
     else:
-        o = _router_options(T, E, dev, path, logit_noise, z_coef, stats, norm_weight, norm_eps,
-                            residual, x.dtype)
+        o, keep = _router_options(T, E, dev, path, logit_noise, z_coef, stats, norm_weight,
+                                  norm_eps, residual, x.dtype, wd_f16)
         rc = lib.mm_moe_forward_opts(*args, C.byref(o))
+        del keep
     del ag, au, ad
     L.check(rc, "mm_moe_forward")
     return out, topk_idx, topk_w, aux_loss
@@ -218,7 +250,7 @@ def moe_route(x: torch.Tensor, Wr: torch.Tensor, k: int, coef: float, *,
     if logit_noise is None and not z_coef and stats is None:
         rc = lib.mm_moe_route(*args)
     else:
-        o = _router_options(T, E, dev, "auto", logit_noise, z_coef, stats)
+        o, _ = _router_options(T, E, dev, "auto", logit_noise, z_coef, stats)
         rc = lib.mm_moe_route_opts(*args, C.byref(o))
     L.check(rc, "mm_moe_route")
     return idx, w, aux, counts

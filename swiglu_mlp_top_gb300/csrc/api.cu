@@ -309,9 +309,28 @@ size_t mm_swiglu_ffn_workspace_bytes(int64_t T, int H, int I, int dtype) {
   return dense_ws_bytes(T, H, I, dtype);
 }
 
+static int swiglu_ffn_impl(const void* x, const void* Wg, const void* Wu, const void* Wd,
+                           const void* Wd16, void* y, int64_t T, int H, int I, int dtype,
+                           void* workspace, size_t workspace_bytes, void* stream, int path);
+
 int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* Wd, void* y,
                      int64_t T, int H, int I, int dtype, void* workspace, size_t workspace_bytes,
                      void* stream, int path) {
+  return swiglu_ffn_impl(x, Wg, Wu, Wd, nullptr, y, T, H, I, dtype, workspace, workspace_bytes,
+                         stream, path);
+}
+
+int mm_swiglu_ffn_prepared(const void* x, const void* Wg, const void* Wu, const void* Wd,
+                           const void* Wd16, void* y, int64_t T, int H, int I, int dtype,
+                           void* workspace, size_t workspace_bytes, void* stream, int path) {
+  if (Wd16 != nullptr && !aligned16(Wd16)) return MM_ERR_INVALID_ARG;
+  return swiglu_ffn_impl(x, Wg, Wu, Wd, Wd16, y, T, H, I, dtype, workspace, workspace_bytes,
+                         stream, path);
+}
+
+static int swiglu_ffn_impl(const void* x, const void* Wg, const void* Wu, const void* Wd,
+                           const void* Wd16, void* y, int64_t T, int H, int I, int dtype,
+                           void* workspace, size_t workspace_bytes, void* stream, int path) {
   if (!valid_dtype(dtype) || T < 0 || H < 1 || I < 1) return MM_ERR_INVALID_ARG;
   if (H % 8 != 0 || I % 8 != 0) return MM_ERR_UNSUPPORTED;
   if (T > (int64_t{1} << 30)) return MM_ERR_UNSUPPORTED;
@@ -356,11 +375,12 @@ int mm_swiglu_ffn_ex(const void* x, const void* Wg, const void* Wu, const void* 
   const void* wd[1] = {Wd};
   cudaError_t e;
   if (p == MM_PATH_TENSOR) {
-    // the gate/up kernel also makes the fp16 copy of Wd that the down GEMM reads
+    // the gate/up kernel also makes the fp16 copy of Wd that the down GEMM
+    // reads, unless the caller prepared one
     void* wd16 = ws_at(workspace, sizeof(WsHeader) + dense_h_bytes(T, I, dtype));
-    const void* wd16p[1] = {wd16};
+    const void* wd16p[1] = {Wd16 != nullptr ? Wd16 : wd16};
     e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
-      return launch_gateup_tc(x, T, H, I, g, wg, wu, h, wd, 1, wd16, hdr, st);
+      return launch_gateup_tc(x, T, H, I, g, wg, wu, h, wd, Wd16 != nullptr ? 0 : 1, wd16, hdr, st);
     });
     if (e != cudaSuccess) return cuda_fail(e, "gateup_tc");
     e = counted_launch(MM_KERNEL_DOWN, st, [&] { return launch_down_tc(h, T, H, I, g, wd16p, ep, hdr, st); });
@@ -507,8 +527,13 @@ static int moe_forward_impl(const void* x, const void* Wr, const void* const* Wg
   const int64_t rows = T * k;
   const void* wd16p[MM_MAX_EXPERTS];
   char* wd16 = ws_at(workspace, L.wd16);
+  const void* const* prep = opts ? opts->wd_f16 : nullptr;   // prepared fp16 down weights
+  if (prep != nullptr)
+    for (int q = 0; q < E; ++q)
+      if (prep[q] == nullptr || !aligned16(prep[q])) return MM_ERR_INVALID_ARG;
   if (p == MM_PATH_TENSOR)
-    for (int q = 0; q < E; ++q) wd16p[q] = wd16 + static_cast<size_t>(q) * H * I * 2;
+    for (int q = 0; q < E; ++q)
+      wd16p[q] = prep != nullptr ? prep[q] : wd16 + static_cast<size_t>(q) * H * I * 2;
   RouterVariant rv;
   rc = router_variant(opts, ws_at(workspace, L.blk_z), &rv);
   if (rc != MM_OK) return rc;
@@ -541,8 +566,8 @@ static int moe_forward_impl(const void* x, const void* Wr, const void* const* Wg
   const RowGather rg{perm, k, static_cast<int>(rows)};
   if (p == MM_PATH_TENSOR)
     e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
-      return launch_gateup_tc(gather ? x : xp, rows, H, I, gu, Wg, Wu, h, Wd, E, wd16, hdr, st,
-                              gather ? &rg : nullptr);
+      return launch_gateup_tc(gather ? x : xp, rows, H, I, gu, Wg, Wu, h, Wd,
+                              prep != nullptr ? 0 : E, wd16, hdr, st, gather ? &rg : nullptr);
     });
   else
     e = counted_launch(MM_KERNEL_GATEUP, st, [&] {
@@ -635,6 +660,20 @@ int mm_moe_route_opts(const void* x, const void* Wr, int64_t T, int H, int E, in
                          ro, hdr, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "router");
+  return MM_OK;
+}
+
+// ------------------------------------------------------------------ prepared weights
+int mm_prepare_down_weights(const void* Wd, void* Wd16, int H, int I, void* status_ws,
+                            void* stream) {
+  if (!Wd || !Wd16 || H < 1 || I < 1) return MM_ERR_INVALID_ARG;
+  if (!aligned16(Wd) || !aligned16(Wd16) || (status_ws && !aligned16(status_ws)))
+    return MM_ERR_INVALID_ARG;
+  const int64_t n = static_cast<int64_t>(H) * I;
+  if (n % 8 != 0) return MM_ERR_UNSUPPORTED;
+  cudaError_t e = launch_prepare_wd16(Wd, Wd16, n, static_cast<WsHeader*>(status_ws),
+                                      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prepare Wd");
   return MM_OK;
 }
 

@@ -211,6 +211,11 @@ cudaError_t launch_decode_sw(const void* x, const void* Wg, const void* Wu, cons
 
 cudaError_t launch_watchdog_selftest(WsHeader* hdr, uint32_t limit_us, cudaStream_t st);
 
+// fp16 copy of a bf16 down-projection matrix of n elements (n a multiple of
+// 8, 16-byte aligned); out-of-range values set MM_ERR_RANGE in hdr (nullable).
+cudaError_t launch_prepare_wd16(const void* Wd, void* Wd16, int64_t n, WsHeader* hdr,
+                                cudaStream_t st);
+
 // Block prologue helpers (norm.cu): the router weights with the norm weight
 // folded in, as exact bf16 halves (hi = bf16(w * Wr), lo = w * Wr - hi), and
 // the normalised rows x_n = x * inv_rms * w (x's dtype) with inv_rms [T].

@@ -447,3 +447,38 @@ def test_moe_gather_path_runs_in_its_smaller_workspace():
     with pytest.raises(RuntimeError, match="MM_ERR_WORKSPACE"):
         mm.moe_forward(g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], k, 0.01, workspace=ws,
                        path="tensor")
+
+
+# ------------------------------------------------------------------ prepared down weights
+def test_prepared_down_weights_give_the_same_outputs():
+    """The fp16 copy of Wd made once (mm_prepare_down_weights) is the copy the
+    tensor-core path makes inside every call: the outputs agree bit for bit
+    (MoE top-2 and the dense FFN), and the forward no longer converts."""
+    inp = moe_inputs(1500, 256, 320, 8, "bf16", seed=1300, bias=(1.5, 0.5, 0, 0, 0, 0, 0, 0))
+    g = to_dev(inp)
+    wd16 = [mm.prepare_down_weights(w) for w in g["Wd"]]
+    a = mm.moe_forward(g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], 2, 0.01,
+                       logit_bias=g["logit_bias"], path="tensor")
+    b = mm.moe_forward(g["x"], g["Wr"], g["Wg"], g["Wu"], g["Wd"], 2, 0.01,
+                       logit_bias=g["logit_bias"], path="tensor", wd_f16=wd16)
+    torch.cuda.synchronize()
+    assert all(torch.equal(u, v) for u, v in zip(a, b))
+    d = make_inputs(700, 256, 384, "bf16", seed=1301)
+    gd = to_dev(d)
+    y0 = mm.swiglu_ffn(gd["x"], gd["Wg"], gd["Wu"], gd["Wd"], path="tensor")
+    y1 = mm.swiglu_ffn(gd["x"], gd["Wg"], gd["Wu"], gd["Wd"], path="tensor",
+                       wd_f16=mm.prepare_down_weights(gd["Wd"]))
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1)
+    assert torch.equal(wd16[0], g["Wd"][0].to(torch.float16))     # exact conversion
+
+
+def test_prepare_down_weights_reports_the_fp16_range():
+    ws = mm.new_workspace(256)
+    Wd = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    Wd[3, 5] = 70000.0
+    mm.prepare_down_weights(Wd, status_workspace=ws)
+    assert mm.check_status(ws) == 6
+    Wd[3, 5] = 60000.0
+    mm.prepare_down_weights(Wd, status_workspace=ws)
+    assert mm.check_status(ws) == 0
