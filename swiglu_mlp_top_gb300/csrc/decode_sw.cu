@@ -72,6 +72,7 @@ struct SwArgs {
   float* pd;                      // [n_units][H / 4][T][4] fp32 partials
   void* y;                        // [T, H] bf16
   WsHeader* hdr;
+  int pdl;                        // launched as a programmatic dependent (see the kernel)
 };
 
 __device__ __forceinline__ float sw_swiglu(float g, float u) {
@@ -154,19 +155,41 @@ decode_sw_kernel(const __grid_constant__ SwMaps M, const SwArgs A) {
     // the A operand: 128 rows are read, and the tiles behind it fill rows
     // >= Np, whose products land in TMEM lanes that are never read.  A down
     // stage = the three Wd tiles of one TMEM pass (blocks past H read as 0).
+    //
+    // As a programmatic dependent of the previous call, the weights of the
+    // first S stages are requested before griddepcontrol.wait (they need
+    // nothing from the previous kernel); the x tiles of those stages wait for
+    // it, and are requested before any stage is reused.
     const uint64_t pol = l2_evict_first_policy();
+    bool waited = !A.pdl;
+    int n_def = 0, def_s[kSwMaxStages], def_kb[kSwMaxStages];
+    auto flush = [&]() {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      waited = true;
+      for (int i = 0; i < n_def; ++i)
+        tma_load_3d(ring + def_s[i] * SB, &M.x, &full[def_s[i]], 0, 0, def_kb[i]);
+      n_def = 0;
+    };
     for (int u = cta; ok && u < A.n_units; u += G) {
       for (int kb0 = 0; kb0 < KB_H; kb0 += nkb) {
+        if (!waited && p_it >= S) flush();
         int s;
         if (!acquire(s)) { ok = false; break; }
         uint8_t* st = ring + s * SB;
         mbar_arrive_expect_tx(&full[s], xpart + 2 * wpart);
-        tma_load_3d(st, &M.x, &full[s], 0, 0, kb0);
+        if (waited) {
+          tma_load_3d(st, &M.x, &full[s], 0, 0, kb0);
+        } else {
+          def_s[n_def] = s;
+          def_kb[n_def] = kb0;
+          ++n_def;
+        }
         tma_load_3d_hint(st + xpart, &M.wg, &full[s], 0, u * kSwRows, kb0, pol);
         tma_load_3d_hint(st + xpart + wpart, &M.wu, &full[s], 0, u * kSwRows, kb0, pol);
         ++p_it;
       }
       for (int p = 0; ok && p < n_pass; ++p) {
+        if (!waited && p_it >= S) flush();
         int s;
         if (!acquire(s)) { ok = false; break; }
         mbar_arrive_expect_tx(&full[s], kSwPassBlocks * kSwDTile);
@@ -174,6 +197,7 @@ decode_sw_kernel(const __grid_constant__ SwMaps M, const SwArgs A) {
         ++p_it;
       }
     }
+    if (!waited) flush();
   }
   if (tid == 32) {
     const uint32_t idesc_gu = idesc_bf16_f32(128, kSwRows);
@@ -241,6 +265,8 @@ decode_sw_kernel(const __grid_constant__ SwMaps M, const SwArgs A) {
     const int half = (warp - 2) >> 2;
     const int t = quad * 32 + lane;            // TMEM lane = token
     const bool quad_live = quad * 32 < T, live = t < T;
+    // the partials of y go to the workspace the previous call also used
+    if (A.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
     int j = 0, uses[2] = {0, 0};
     for (int u = cta; ok && u < A.n_units; u += G, ++j) {
       if (!warp_wait(&tfull, j & 1, nullptr, hdr, 65)) { ok = false; break; }
@@ -332,7 +358,13 @@ decode_sw_kernel(const __grid_constant__ SwMaps M, const SwArgs A) {
   // range of quads q = g * T + t (columns 4g .. 4g + 3 of token t), up to
   // kSwMaxSlices threads share a quad
   unsigned ticket = 0xffffffffu;
+  // the barrier's counters are the previous call's too: every thread has
+  // waited for that kernel (the producer and epilogue above; the rest here)
+  if (A.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
   if (ok) ok = grid_barrier(hdr, 68, 1, &ticket);
+  // every CTA of this grid is resident once it passes the barrier: only now
+  // may the next kernel start taking the SMs that this one leaves
+  if (A.pdl && threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (ok) {
     const int Gp = A.n_units;
     const int nq_all = T * H / 4;
@@ -497,9 +529,15 @@ cudaError_t launch_decode_sw(const void* x, const void* Wg, const void* Wu, cons
   cfg.blockDim = dim3(kSwThreads);
   cfg.dynamicSmemBytes = L.smem;
   cfg.stream = st;
+  // One wave (grid <= SMs x resident CTAs), launched as a programmatic
+  // dependent of the previous kernel: its CTAs start as that kernel's CTAs
+  // leave the SMs, and every one of them becomes resident once that kernel
+  // ends (no kernel waits for a later one), so the grid barrier needs no
+  // cooperative launch.  Its successor starts only after this grid's barrier.
+  A.pdl = 1;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, fn, m, A);
