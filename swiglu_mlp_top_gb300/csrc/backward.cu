@@ -159,41 +159,44 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, const float4& a) {
   *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
 }
 
-// Router backward, one block per 64 tokens, one warp per token at a time
-// (lane l holds experts l and l + 32).  Writes dr [T, E], dx [T, H] (the k
-// per-assignment rows in slot order plus dr Wr), and the block's partials of
-// dWr = dr^T x and d_bias = sum_t dr_t.
+// Router backward over blocks of 8 tokens (one warp per token: lane l holds
+// experts l and l + 32): dr [T, E] and dx [T, H] (the k per-assignment rows
+// in slot order plus dr Wr, by all the block's threads).  Small blocks keep
+// many tokens in flight: each step is a short chain of dependent loads.
+constexpr int kRbTok = 8;
+
 template <typename Tin>
 __global__ void __launch_bounds__(kBwdThreads)
-router_bwd_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, int64_t T, int H, int E,
-                  int k, const RouterBwd rb) {
-  extern __shared__ float s_dr[];              // [64][E] this block's dr
+router_bwd_kernel(const Tin* __restrict__ Wr, int64_t T, int H, int E, int k, const RouterBwd rb) {
+  __shared__ float s_dr[kRbTok * MM_MAX_EXPERTS];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int kWarps = kBwdThreads / 32;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kBwdTok;
-  const int ntok = static_cast<int>(T - t0 < kBwdTok ? T - t0 : kBwdTok);
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kRbTok;
+  const int ntok = static_cast<int>(T - t0 < kRbTok ? T - t0 : kRbTok);
   const float invT = 1.0f / static_cast<float>(T);
   const bool v0 = lane < E, v1 = lane + 32 < E;
-  const float aux0 = v0 ? rb.d_aux * static_cast<float>(E) * rb.coef * static_cast<float>(rb.counts[lane]) * invT * invT : 0.f;
-  const float aux1 = v1 ? rb.d_aux * static_cast<float>(E) * rb.coef * static_cast<float>(rb.counts[lane + 32]) * invT * invT : 0.f;
-  for (int tl = warp; tl < ntok; tl += kWarps) {
+  if (warp < ntok) {
+    const int tl = warp;
     const int64_t t = t0 + tl;
+    const float aux0 = v0 ? rb.d_aux * static_cast<float>(E) * rb.coef * static_cast<float>(rb.counts[lane]) * invT * invT : 0.f;
+    const float aux1 = v1 ? rb.d_aux * static_cast<float>(E) * rb.coef * static_cast<float>(rb.counts[lane + 32]) * invT * invT : 0.f;
     const float p0 = v0 ? rb.probs[t * E + lane] : 0.f;
     const float p1 = v1 ? rb.probs[t * E + lane + 32] : 0.f;
     float dp0 = aux0, dp1 = aux1;
     // dalpha_s = sum of the row's partials (lane-strided, then a fixed tree)
     float Z = 0.f, c = 0.f;
     float da[MM_MAX_TOPK];
+    int sel[MM_MAX_TOPK];
 #pragma unroll
     for (int s = 0; s < MM_MAX_TOPK; ++s) {
       da[s] = 0.f;
+      sel[s] = 0;
       if (s < k) {
         const float* part = rb.dalpha_part + static_cast<int64_t>(rb.pos[t * k + s]) * rb.n_parts;
         float v = 0.f;
         for (int j = lane; j < rb.n_parts; j += 32) v += part[j];
         da[s] = bw_warp_sum(v);
-        const int e = rb.topk_idx[t * k + s];
-        Z += __shfl_sync(0xffffffffu, e < 32 ? p0 : p1, e & 31);
+        sel[s] = rb.topk_idx[t * k + s];
+        Z += __shfl_sync(0xffffffffu, sel[s] < 32 ? p0 : p1, sel[s] & 31);
         c = fmaf(da[s], rb.topk_w[t * k + s], c);
       }
     }
@@ -201,10 +204,9 @@ router_bwd_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, int64_t
 #pragma unroll
     for (int s = 0; s < MM_MAX_TOPK; ++s) {
       if (s < k) {
-        const int e = rb.topk_idx[t * k + s];
         const float g = (da[s] - c) / Z;
-        if (e == lane) dp0 += g;
-        if (e == lane + 32) dp1 += g;
+        if (sel[s] == lane) dp0 += g;
+        if (sel[s] == lane + 32) dp1 += g;
       }
     }
     const float S = bw_warp_sum(p0 * dp0 + p1 * dp1);
@@ -216,13 +218,10 @@ router_bwd_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, int64_t
     }
     if (v0) { rb.dr[t * E + lane] = dr0; s_dr[tl * E + lane] = dr0; }
     if (v1) { rb.dr[t * E + lane + 32] = dr1; s_dr[tl * E + lane + 32] = dr1; }
-    __syncwarp();
   }
   __syncthreads();
-  // dx_t = sum_s dxp[pos(t, s)] (slot order) + sum_e dr_e Wr_e: one flat
-  // loop over (token, 4-column group) items of the block
+  // dx_t = sum_s dxp[pos(t, s)] (slot order) + sum_e dr_e Wr_e
   const int nc4 = H / 4;
-#pragma unroll 2
   for (int i = tid; i < ntok * nc4; i += blockDim.x) {
     const int tl = i / nc4, h = 4 * (i - tl * nc4);
     const int64_t t = t0 + tl;
@@ -242,10 +241,22 @@ router_bwd_kernel(const Tin* __restrict__ x, const Tin* __restrict__ Wr, int64_t
     }
     store4(static_cast<Tin*>(rb.dx) + t * H + h, acc);
   }
-  // the block's dWr partial: element (e, h) = sum_t dr[t][e] x[t][h] in
-  // token order; a thread holds 4 columns x 8 experts, so each x element is
-  // read once per 8 experts (coalesced: neighbouring threads, neighbouring columns)
-  const int nec = (E + 7) / 8;
+}
+
+// Per block of 64 tokens, the partials of dWr = dr^T x (element (e, h) =
+// sum_t dr[t][e] x[t][h] in token order; a thread holds 4 columns x 8
+// experts, so each x element is read once per 8 experts) and of
+// d_bias = sum_t dr_t.
+template <typename Tin>
+__global__ void __launch_bounds__(kBwdThreads)
+router_dwr_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, const RouterBwd rb) {
+  extern __shared__ float s_dr[];              // [64][E]
+  const int tid = threadIdx.x;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kBwdTok;
+  const int ntok = static_cast<int>(T - t0 < kBwdTok ? T - t0 : kBwdTok);
+  for (int i = tid; i < ntok * E; i += blockDim.x) s_dr[i] = rb.dr[t0 * E + i];
+  __syncthreads();
+  const int nc4 = H / 4, nec = (E + 7) / 8;
   for (int item = tid; item < nc4 * nec; item += blockDim.x) {
     const int c4 = item % nc4, e0 = (item / nc4) * 8;
     float acc[8][4];
@@ -336,9 +347,14 @@ cudaError_t launch_bwd_dispatch(const void* x, const void* dy, const int32_t* to
 cudaError_t launch_router_bwd(const void* x, const void* Wr, int64_t T, int H, int E, int k,
                               const RouterBwd& rb, cudaStream_t st) {
   if (H % 4 != 0) return cudaErrorInvalidValue;
+  const int grid = static_cast<int>((T + kRbTok - 1) / kRbTok);
+  router_bwd_kernel<__nv_bfloat16><<<grid, kBwdThreads, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(Wr), T, H, E, k, rb);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   const size_t smem = static_cast<size_t>(kBwdTok) * E * sizeof(float);
-  router_bwd_kernel<__nv_bfloat16><<<bwd_blocks(T), kBwdThreads, smem, st>>>(
-      static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(Wr), T, H, E, k, rb);
+  router_dwr_kernel<__nv_bfloat16><<<bwd_blocks(T), kBwdThreads, smem, st>>>(
+      static_cast<const __nv_bfloat16*>(x), T, H, E, rb);
   return cudaGetLastError();
 }
 

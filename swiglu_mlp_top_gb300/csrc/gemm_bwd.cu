@@ -15,8 +15,11 @@
 // epilogue of one tile overlaps the MMAs of the next, warp roles: 8 epilogue
 // warps, 1 TMA producer, 1 MMA issuer (even CTA).
 //
-// An MN-major tile of 128 (M or N) x 64 (K) is two TMA boxes of 64 x 64:
-// each box is 64 K-rows of 128 bytes, in 1024-byte swizzle atoms of 8 rows.
+// An MN-major tile of 128 (M or N) x 64 (K) is one 3-D TMA box of the
+// matrix viewed as (64 columns, rows, column blocks of 64): box 64 x 64 x 2,
+// landing as two 8 KiB halves, each 64 K-rows of 128 bytes in 1024-byte
+// swizzle atoms of 8 rows (one 16 KiB request; two 8 KiB requests per tile
+// left the GEMM waiting on the TMA).
 // Its UMMA descriptor: leading byte offset = 8192 (the next 64 elements
 // along M / N, i.e. the second box), stride byte offset = 1024 (the next 8
 // K-rows); one MMA of K = 16 starts 16 K-rows (2048 bytes) further.
@@ -187,17 +190,14 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
             const bool hi = kb >= P.kb_split;
             const CUtensorMap* bm = hi ? &P.b_hi[ti.g] : &P.b_lo[ti.g];
             const int kk = (hi ? kb - P.kb_split : kb) * 64;
-            tma_load_2d_cta2(b_dst, bm, fb, ncol, kk);
-            tma_load_2d_cta2(b_dst + kBwTile / 2, bm, fb, ncol + 64, kk);
+            tma_load_3d_cta2(b_dst, bm, fb, 0, kk, ncol / 64);
           } else {
             // A and B both MN-major: K rows kb0 + kb of the group
             const BwProblem& pr = P.prob[ti.p];
             const int krow = (ti.kb0 + kb) * 64;
             const int mcol = pr.a_col0 + ti.m0;
-            tma_load_2d_cta2(a_dst, &P.a[pr.a_map], fb, mcol, krow);
-            tma_load_2d_cta2(a_dst + kBwTile / 2, &P.a[pr.a_map], fb, mcol + 64, krow);
-            tma_load_2d_cta2(b_dst, &P.b_lo[pr.b_map], fb, ncol, krow);
-            tma_load_2d_cta2(b_dst + kBwTile / 2, &P.b_lo[pr.b_map], fb, ncol + 64, krow);
+            tma_load_3d_cta2(a_dst, &P.a[pr.a_map], fb, 0, krow, mcol / 64);
+            tma_load_3d_cta2(b_dst, &P.b_lo[pr.b_map], fb, 0, krow, ncol / 64);
           }
         }
       }
@@ -324,10 +324,15 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
 }
 
 // =============================================================== host side
-// 64 x 64 box of a bf16 row-major [rows, cols] matrix, 128-byte swizzle.
+// MN-major tiles of a bf16 row-major [rows, cols] matrix (cols a multiple of
+// 64): the matrix as (64 columns, rows, cols / 64 column blocks), box 64 x 64
+// x 2 (two column blocks of 64 K-rows), 128-byte swizzle; zero fill past
+// the matrix.
 static bool box64(CUtensorMap* m, const void* ptr, int64_t cols, int64_t rows) {
-  return make_map_16(m, ptr, static_cast<uint64_t>(cols), static_cast<uint64_t>(rows), 64, false,
-                     64, CU_TENSOR_MAP_SWIZZLE_128B);
+  const uint64_t dims[3] = {64, static_cast<uint64_t>(rows), static_cast<uint64_t>(cols / 64)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(cols) * 2, 128};
+  const uint32_t box[3] = {64, 64, 2};
+  return make_map_3d(m, ptr, dims, strides, box);
 }
 
 static int bw_clusters(int64_t tiles) {
