@@ -396,6 +396,7 @@ __device__ __forceinline__ void epilogue_down(uint32_t tb, const DownRow& d, con
   const int col0 = ti.n0 + half * HC;
   constexpr int kPieces = HC / kDnPiece;
   const uint32_t st0 = smem_u32(wstage);
+  const uint64_t keep = l2_evict_last_policy();
   if (lane == 0) bulk_wait_read();               // a dense tile's tensor stores used the tile
   __syncwarp();
 #pragma unroll 1
@@ -430,7 +431,8 @@ __device__ __forceinline__ void epilogue_down(uint32_t tb, const DownRow& d, con
       }
       const int64_t o = L.off[i] + c * kDnPiece;
       if (ep.mode == kCombineFirst || ep.mode == kCombineAccum) {
-        __stcg(reinterpret_cast<float4*>(ep.acc32 + o), v);
+        // the next slot's launch reads it back: keep it in L2 if it can
+        st_f32x4_hint(ep.acc32 + o, v, keep);
       } else {
         if (ep.resid != nullptr) {       // the block's residual, before the one rounding
           const uint2 xr = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(ep.resid) + o);
