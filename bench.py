@@ -606,6 +606,31 @@ PER_WORKLOADS = ["dense_t4096", "dense_t100", "moe_e4k1_t8192"] + \
      "gather:moe_e8k2_t16384_skew"]
 
 
+def entry_step(name, dev):
+    """The step object of a per-workload entry ("backward:W", "block:W", ...)
+    or of a plain workload name."""
+    if name.startswith("backward:"):
+        w = WORKLOADS[name.split(":", 1)[1]]
+        return BwdStep(w, dev, l2_rotation(w)[0])
+    variant = None
+    if ":" in name:
+        variant, name = name.split(":", 1)
+    w = WORKLOADS[name]
+    return make_step(w, dev) if variant is None else VariantStep(w, dev, l2_rotation(w)[0], variant)
+
+
+def run_profile(args):
+    """W + K untimed steps of one entry, nothing else: the command that
+    profiler launch lists and counter captures are taken on."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    step = entry_step(args.profile, dev)
+    for i in range(args.warmup + args.steps):
+        step(i)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": args.profile, "warmup": args.warmup, "steps": args.steps}))
+
+
 def per_workload_entry(name, lib, ws, local, dev, warmup):
     if name.startswith("backward:"):
         return backward_entry(WORKLOADS[name.split(":", 1)[1]], lib, ws, local, dev, warmup)
@@ -842,9 +867,15 @@ def main():
                     help="comma-separated subset of the per-workload entries")
     ap.add_argument("--graph", choices=["auto", "on", "off"], default="auto",
                     help="time a CUDA-graph replay of the K steps (auto: T <= 64)")
+    ap.add_argument("--profile", default="",
+                    help="run W + K untimed steps of one entry (a workload or a per-workload "
+                         "name such as backward:moe_e8k2_t16384_skew) for a profiler, and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.profile:
+        run_profile(args)
+        return
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference_arm(args, w)

@@ -43,8 +43,12 @@ constexpr int kBwTile = 128 * 64 * 2;                 // 16 KiB: 128 rows x one 
 constexpr int kBwEpiWarps = 8;
 constexpr int kBwThreads = 32 * (kBwEpiWarps + 2);
 constexpr int kBwWarpProducer = kBwEpiWarps, kBwWarpMma = kBwEpiWarps + 1;
-constexpr int kBwSmem = kBwStages * 2 * kBwTile + 1024 + 1024;
-static_assert(kBwSmem <= 232448, "shared memory budget");
+// Epilogue staging: one 32-row x 32-column piece per warp (4 KiB of fp32).
+constexpr int kBwStage = 32 * 128;
+// + 1024 bytes of alignment slack and 256 of barriers
+constexpr int kBwSmem = kBwStages * 2 * kBwTile + kBwEpiWarps * kBwStage + 1024 + 256;
+// with the static arrays (s_off, s_tstart, s_tmem, s_abort) within the 227 KiB of a block
+static_assert(kBwSmem + 8 * (kBwMaxGroups + 1) + 16 <= 232448, "shared memory budget");
 
 // UMMA descriptor of an MN-major 128 x 64 tile stored as two 64 x 64
 // 128-byte-swizzled TMA boxes (see the file comment).
@@ -113,7 +117,8 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
   uint8_t* sB = smem + kBwStages * kBwTile;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kBwStages * kBwTile);
+  uint8_t* sEpi = sB + kBwStages * kBwTile;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + kBwEpiWarps * kBwStage);
   uint64_t* full = bars;                   // [kBwStages] even CTA: both CTAs' bytes
   uint64_t* empty = bars + kBwStages;      // [kBwStages] each CTA: released by the pair's MMAs
   uint64_t* tfull = bars + 2 * kBwStages;  // [2] each CTA: accumulator ready
@@ -251,6 +256,7 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
     // ------------------------------------------------ epilogue (warps 0-7, both CTAs)
     const int quad = warp & 3, half = warp >> 2;
     const int row = quad * 32 + lane;
+    uint8_t* wstage = sEpi + warp * kBwStage;     // this warp's staging piece
     const uint32_t te0 = mapa_shared(smem_u32(&tempty[0]), 0);
     const uint32_t te1 = mapa_shared(smem_u32(&tempty[1]), 0);
     int used = 0;
@@ -271,6 +277,9 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
         out32 = P.prob[ti.p].out;
       }
       const bool valid = row < ti.rows;
+      // rows schedule: all 32 rows of the warp in the group, so its pieces
+      // go out as tensor stores (the rows past a group are the next group's)
+      const bool tma_piece = SCHED == kSchedRows && P.out_tma && (row | 31) < ti.rows;
       const int64_t orow = static_cast<int64_t>(ti.row0 + row);
       if (ti.nkb == 0) {
         // empty K range (an expert no token chose): the gradient is zero
@@ -293,7 +302,34 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
         tmem_ld_32x32b_x32(tb + c * 32, r);     // every lane (warp-collective)
         tmem_ld_wait();
         if (col >= ncols) continue;              // warp-uniform
-        if (!valid) {
+        if (tma_piece) {
+          // through the swizzled staging piece: fp32 in 128-byte rows (chunk q
+          // of row r at q ^ (r & 7)), bf16 in 64-byte rows (q ^ ((r >> 1) & 3))
+          if (lane == 0) bulk_wait_read();       // the previous piece's store has read it
+          __syncwarp();
+          if (out16 != nullptr) {
+            uint8_t* r64 = wstage + lane * 64;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(r64 + ((q ^ ((lane >> 1) & 3)) << 4)) =
+                  make_uint4(pack_bf16x2(__uint_as_float(r[8 * q]), __uint_as_float(r[8 * q + 1])),
+                             pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
+                             pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
+                             pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
+          } else {
+            uint8_t* r128 = wstage + lane * 128;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<uint4*>(r128 + ((q ^ (lane & 7)) << 4)) =
+                  make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&P.o, wstage, col, ti.row0 + (row & ~31));
+            bulk_commit();
+          }
+        } else if (!valid) {
           // rows past the group / matrix: nothing to store
         } else if (out16 != nullptr) {
           uint4* d4 = reinterpret_cast<uint4*>(out16 + orow * ldo + col);
@@ -315,6 +351,7 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc ? te1 : te0);
     }
+    bulk_wait_all();   // this warp's tensor stores have landed
   }
 
   tc_fence_before();
@@ -375,6 +412,13 @@ cudaError_t launch_bw_dgrad(const void* A, int64_t a_rows, int K, const int32_t*
   p.out = out;
   p.ldo = ldo;
   p.out_bf16 = out_bf16;
+  // full 32-row pieces as TMA stores, where the output's address and pitch allow
+  const int esz = out_bf16 ? 2 : 4;
+  p.out_tma = (reinterpret_cast<uintptr_t>(out) % 16 == 0 && (ldo * esz) % 16 == 0 &&
+               make_map_2d(&p.o, out, !out_bf16, static_cast<uint64_t>(N),
+                           static_cast<uint64_t>(a_rows), static_cast<uint64_t>(ldo) * esz, 32, 32,
+                           out_bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
+                  ? 1 : 0;
   const int64_t ntn = (N + 255) / 256;
   const int64_t tiles = offsets ? ((a_rows + 255) / 256 + G) * ntn : ((dense_rows + 255) / 256) * ntn;
   return bw_launch<kSchedRows>(p, tiles, hdr, st);

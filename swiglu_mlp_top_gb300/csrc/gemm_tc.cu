@@ -67,10 +67,23 @@ static_assert(kSmemWide <= 232448 - 8192, "shared memory budget (wide down tile)
 constexpr uint32_t kTmemCols = 512;
 static_assert(kSmem <= 232448, "shared memory budget");
 
+// Per op: output columns per tile, k-blocks per TMA stage, k-blocks in the
+// ring, epilogue staging bytes.  The backward gate/up stages three 2 KiB
+// pieces per warp (dG, dU, alpha h; one tensor store each), paid for with a
+// ring of five k-blocks.
 template <int OP> struct OpTraits;
-template <> struct OpTraits<kOpUp> { static constexpr int kOutCols = kN / 2, kKb = 2; };
-template <> struct OpTraits<kOpUpBwd> { static constexpr int kOutCols = kN / 2, kKb = 2; };
-template <> struct OpTraits<kOpDown> { static constexpr int kOutCols = kN, kKb = 1; };
+template <> struct OpTraits<kOpUp> {
+  static constexpr int kOutCols = kN / 2, kKb = 2, kRing = kRingKb, kStage = kStageEpi;
+};
+template <> struct OpTraits<kOpUpBwd> {
+  static constexpr int kOutCols = kN / 2, kKb = 1, kRing = 5, kStage = 3 * kStageEpi;
+};
+template <> struct OpTraits<kOpDown> {
+  static constexpr int kOutCols = kN, kKb = 1, kRing = kRingKb, kStage = kStageEpi;
+};
+template <int OP>
+constexpr int kSmemOf = OpTraits<OP>::kRing * (kATile + kBTile) + OpTraits<OP>::kStage + 2048;
+static_assert(kSmemOf<kOpUpBwd> <= 232448, "shared memory budget (backward gate/up)");
 
 template <int MAXW>
 struct TcParams {
@@ -80,6 +93,7 @@ struct TcParams {
   CUtensorMap b0[MAXW];     // gate/up: Wg; down: fp16 Wd  (box rows = N/2)
   CUtensorMap b1[MAXW];     // gate/up: Wu; down: unused
   CUtensorMap ag;           // gate/up gathering rows: x [T, K], box 64 x 1 row
+  CUtensorMap out2;         // backward gate/up: alpha h [a_rows, I] bf16 (out: dG|dU [a_rows, 2I])
 };
 
 struct TileInfo {
@@ -131,6 +145,17 @@ __device__ __forceinline__ void build_schedule(const GroupRows& gr, int n_tiles,
 // valid rows directly (the rows past the end belong to the next group).
 // Returns true when some value of the lane's pieces is not representable in
 // fp16 (|h| >= 65520 rounds to infinity; a NaN or an infinite g or u).
+// One lane's row of a 32-row x 32-column 16-bit piece into a staging tile in
+// the 64-byte-swizzled layout of a TMA box: 64-byte rows, 16-byte chunk q of
+// row r at chunk q ^ ((r >> 1) & 3).
+__device__ __forceinline__ void stage_row64(uint8_t* tile, int lane, const uint32_t* pk) {
+  uint8_t* r64 = tile + lane * 64;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4*>(r64 + ((q ^ ((lane >> 1) & 3)) << 4)) =
+        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+}
+
 __device__ __forceinline__ bool epilogue_up(uint32_t tb, const TileInfo& ti, int I, __half* hout,
                                             int row, int half, uint8_t* wstage,
                                             const CUtensorMap* hmap) {
@@ -162,12 +187,7 @@ __device__ __forceinline__ bool epilogue_up(uint32_t tb, const TileInfo& ti, int
     if (full_warp) {
       if (lane == 0) bulk_wait_read();             // previous store has read the tile
       __syncwarp();
-      // 64-byte rows, 16-byte chunk q of row r at chunk q ^ ((r >> 1) & 3)
-      uint8_t* r64 = wstage + lane * 64;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4*>(r64 + ((q ^ ((lane >> 1) & 3)) << 4)) =
-            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      stage_row64(wstage, lane, pk);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -188,13 +208,20 @@ __device__ __forceinline__ bool epilogue_up(uint32_t tb, const TileInfo& ti, int
 //   h = g s u;  dalpha += h * dhu;  dh = alpha dhu;  dU = dh g s;
 //   dG = dh u s (1 + g (1 - s))
 // (the chain rule through lesson 13 §0's h = SiLU(g) ⊙ u).  dG, dU and
-// alpha h go out as bf16, 64 contiguous bytes per row and piece; the row's
-// dalpha partial over these 64 columns goes to dalpha_part[row][2 nb + half].
-// Every lane takes part in the TMEM loads (warp-collective); only the rows
-// of the group (`valid`) read dhu and store.
+// alpha h go out as bf16 in 32-column pieces: a warp whose 32 rows are all
+// in the group stages the three pieces and writes each with one TMA tensor
+// store (dG and dU through the [rows, 2I] map, alpha h through its own); a
+// warp holding a group's ragged end stores its valid rows directly.  The
+// row's dalpha partial over these 64 columns goes to
+// dalpha_part[row][2 nb + half].  Every lane takes part in the TMEM loads
+// (warp-collective); only the rows of the group (`valid`) read dhu and store.
 __device__ __forceinline__ void epilogue_up_bwd(uint32_t tb, const TileInfo& ti, int I, int row,
-                                                int half, const UpBwd& ub) {
+                                                int half, const UpBwd& ub, uint8_t* wstage,
+                                                const CUtensorMap* gumap,
+                                                const CUtensorMap* hmap) {
+  const int lane = row & 31;
   const bool valid = row < ti.rows;              // else: past the group, the next group's row
+  const bool full_warp = (row | 31) < ti.rows;   // warp-uniform
   const int64_t r = ti.row0 + (valid ? row : 0);
   float alpha = 1.0f;
   if (valid && ub.perm != nullptr) {
@@ -232,7 +259,7 @@ __device__ __forceinline__ void epilogue_up_bwd(uint32_t tb, const TileInfo& ti,
         const float g = __uint_as_float(gr[2 * j + e]);
         const float u = __uint_as_float(ur[2 * j + e]);
         const float d = dv[2 * j + e];
-        const float sg = 1.0f / (1.0f + __expf(-g));
+        const float sg = __fdividef(1.0f, 1.0f + __expf(-g));   // 0 once exp(-g) > 2^126
         const float silu = g * sg;
         const float h = silu * u;
         dpart = fmaf(h, d, dpart);
@@ -245,7 +272,22 @@ __device__ __forceinline__ void epilogue_up_bwd(uint32_t tb, const TileInfo& ti,
       pu[j] = pack_bf16x2(o_u[0], o_u[1]);
       ph[j] = pack_bf16x2(o_h[0], o_h[1]);
     }
-    if (valid) {
+    if (full_warp) {
+      if (lane == 0) bulk_wait_read();           // the previous pieces' stores have read them
+      __syncwarp();
+      stage_row64(wstage, lane, pg);
+      stage_row64(wstage + 2048, lane, pu);
+      stage_row64(wstage + 4096, lane, ph);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int rb = ti.row0 + (row & ~31);
+        tma_store_2d(gumap, wstage, col, rb);
+        tma_store_2d(gumap, wstage + 2048, I + col, rb);
+        tma_store_2d(hmap, wstage + 4096, col, rb);
+        bulk_commit();
+      }
+    } else if (valid) {
       uint4* dg = reinterpret_cast<uint4*>(ub.dgu + r * (2 * static_cast<int64_t>(I)) + col);
       uint4* du = reinterpret_cast<uint4*>(ub.dgu + r * (2 * static_cast<int64_t>(I)) + I + col);
       uint4* dh4 = reinterpret_cast<uint4*>(ub.ha + r * I + col);
@@ -537,13 +579,13 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
   constexpr int kKbStage = OpTraits<OP>::kKb;
-  constexpr int kStages = (kWide ? kRingKbWide : kRingKb) / kKbStage;
+  constexpr int kStages = (kWide ? kRingKbWide : OpTraits<OP>::kRing) / kKbStage;
   constexpr int kAStage = kKbStage * kATile;
   constexpr int kBTileK = (kUpLike ? kN / 2 : NW / 2) * kTcBK * 2;   // B rows of this CTA, one k-block
   constexpr int kBStage = kKbStage * kBTileK;
   uint8_t* sB = smem + kStages * kAStage;
   uint8_t* sEpi = sB + kStages * kBStage;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + kStageEpi);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + OpTraits<OP>::kStage);
   uint64_t* full = bars;                  // [kStages] even CTA: both CTAs' bytes
   uint64_t* empty = bars + kStages;       // [kStages] each CTA: released by the pair's MMAs
   uint64_t* tfull = bars + 2 * kStages;   // [2] each CTA: accumulator ready
@@ -732,7 +774,7 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
     // ------------------------------------------------ epilogue (warps 0-7, both CTAs)
     const int quad = warp & 3, half = warp >> 2;
     const int row = quad * 32 + lane;
-    uint8_t* wstage = sEpi + warp * 32 * 64;     // this warp's staging tile
+    uint8_t* wstage = sEpi + warp * (OpTraits<OP>::kStage / kEpiWarps);   // this warp's staging
     const uint32_t te0 = mapa_shared(smem_u32(&tempty[0]), 0);
     const uint32_t te1 = mapa_shared(smem_u32(&tempty[1]), 0);
     // the running fp32 sum is the previous kernel's output
@@ -794,13 +836,22 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
         cb = cv0 + (cv1 - cv0) * (local + 1) / n_local;
         cv_load(cv, ca, cb, threadIdx.x, craw);
       }
+      if constexpr (OP == kOpUpBwd) {
+        // this row's 64 dh columns: pulled into L2 while the MMAs run
+        if (row < ti.rows && ti.n0 + half * 64 < NCOLS) {
+          const float* a = ub.dhu + (ti.row0 + row) * NCOLS + ti.n0 + half * 64;
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(a) : "memory");
+          if (ti.n0 + half * 64 + 32 < NCOLS)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(a + 32) : "memory");
+        }
+      }
       if (!warp_wait(&tfull[acc], aph, abort, hdr, 6)) break;
       tc_fence_after();
       const uint32_t tb = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * kAccStride;
       if constexpr (OP == kOpUp)
         range_bad |= epilogue_up(tb, ti, NCOLS, hout, row, half, wstage, &P.out);
       else if constexpr (OP == kOpUpBwd)
-        epilogue_up_bwd(tb, ti, NCOLS, row, half, ub);
+        epilogue_up_bwd(tb, ti, NCOLS, row, half, ub, wstage, &P.out, &P.out2);
       else if (ep.perm == nullptr && ep.mode == kCombineStore && (row | 31) < ti.rows)
         epilogue_down_dense<kHC>(tb, ti, NCOLS, half, lane, ti.row0 + (row & ~31), wstage, &P.out,
                                  static_cast<const __nv_bfloat16*>(ep.resid));
@@ -867,6 +918,35 @@ bool make_map_16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t out
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(out, is_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         2, const_cast<void*>(ptr), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  if (cache.size() > 4096) cache.clear();
+  cache.emplace(key, *out);
+  return true;
+}
+
+bool make_map_2d(CUtensorMap* out, const void* ptr, bool fp32, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {
+  using Key = std::tuple<uintptr_t, bool, uint64_t, uint64_t, uint64_t, uint32_t, uint32_t, int>;
+  static std::mutex mu;
+  static std::map<Key, CUtensorMap> cache;
+  const Key key{reinterpret_cast<uintptr_t>(ptr), fp32, inner, outer, row_bytes, box_inner,
+                box_rows, static_cast<int>(swz)};
+  std::lock_guard<std::mutex> lock(mu);
+  auto itc = cache.find(key);
+  if (itc != cache.end()) {
+    *out = itc->second;
+    return true;
+  }
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(out, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                          2, const_cast<void*>(ptr), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1016,17 +1096,22 @@ static cudaError_t gateup_bwd_impl(const void* A, int64_t a_rows, int H, int I, 
   memset(&p, 0, sizeof(p));
   constexpr int kb = OpTraits<kOpUpBwd>::kKb;
   if (!kblock_map(&p.a, A, H, a_rows, kTcBM, false, kb)) return cudaErrorInvalidValue;
+  // outputs: dG | dU [a_rows, 2I] and alpha h [a_rows, I], 32 x 32 store boxes
+  if (!make_map_16(&p.out, ub.dgu, 2 * static_cast<uint64_t>(I), a_rows, 32, false, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map_16(&p.out2, ub.ha, I, a_rows, 32, false, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
   for (int e = 0; e < g.n_weights; ++e) {
     if (!kblock_map(&p.b0[e], Wg[e], H, I, kN / 2, false, kb)) return cudaErrorInvalidValue;
     if (!kblock_map(&p.b1[e], Wu[e], H, I, kN / 2, false, kb)) return cudaErrorInvalidValue;
   }
   auto fn = grouped_gemm_kernel<kOpUpBwd, MAXW>;
-  cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), kSmem);
+  cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), kSmemOf<kOpUpBwd>);
   if (err != cudaSuccess) return err;
   const int n_tiles = (I + kN / 2 - 1) / (kN / 2);
   DownEpilogue none{};
   WdConvert no_cv{};
-  return launch_pdl(fn, 2 * clusters_for(a_rows, g, n_tiles), kSmem, st, p, g, H, I,
+  return launch_pdl(fn, 2 * clusters_for(a_rows, g, n_tiles), kSmemOf<kOpUpBwd>, st, p, g, H, I,
                     static_cast<__half*>(nullptr), none, no_cv, hdr, 1, ub, RowGather{});
 }
 

@@ -255,6 +255,8 @@ struct BwParams {
   void* out;                            // rows schedule: [rows, ldo]
   int64_t ldo;
   int out_bf16;
+  int out_tma;                          // rows schedule: full 32-row pieces go out through o
+  CUtensorMap o;                        // rows schedule: out as 32 x 32 store boxes
 };
 
 cudaError_t launch_bw_dgrad(const void* A, int64_t a_rows, int K, const int32_t* offsets, int G,
@@ -334,6 +336,11 @@ bool make_map_16(CUtensorMap* out, const void* ptr, uint64_t inner, uint64_t out
 
 // TMA tensor map of a 16-bit tensor (bf16, or fp16) viewed in three dimensions (element
 // strides 1, strides[0], strides[1] bytes), box box[0] x box[1] x box[2],
+// 2-D map of a row-major matrix of fp32 or bf16 elements with an explicit
+// row pitch (bytes, a multiple of 16), for TMA tensor stores; cached like
+// make_map_16.
+bool make_map_2d(CUtensorMap* out, const void* ptr, bool fp32, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz);
 // 128-byte swizzle unless given, zero fill outside; cached like make_map_16.
 bool make_map_3d(CUtensorMap* out, const void* ptr, const uint64_t dims[3],
                  const uint64_t strides[2], const uint32_t box[3], bool is_f16 = false,
