@@ -55,16 +55,20 @@ def decode_kernel_name(w):
     return "decode_tc_kernel (tcgen05 weight streaming)"
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
-# gate/up GEMM, from an ncu capture of the current kernel on this workload;
-# None where no capture of the current kernel exists.
-GATEUP_TRAFFIC_BYTES = {}
+# gate/up GEMM, from an ncu capture of the current kernel on this workload (the
+# fourth launch; ncu flushes the caches before it).  h writes still held in L2
+# when the kernel ends are not counted, so at T <= 8192 the figure is mostly the
+# reads of x and the weights.
+GATEUP_TRAFFIC_BYTES = {"moe_e8k2_t16384_skew": 162316544 + 128596480,
+                        "moe_e4k1_t8192": 42551808 + 5244160,
+                        "dense_t4096": 13830656 + 0}
 # The same for the decode kernel that streams the weights (one launch per step).
-DECODE_TRAFFIC_BYTES = {"decode_moe_e8k2_t64": 89.885696e6 + 3.497984e6,
-                        "decode_moe_e8k2_t16": 89.806336e6 + 2.620416e6,
-                        "decode_moe_e8k2_t4": 87.923712e6 + 2.422528e6,
-                        "decode_dense_t16": 11.281152e6,
-                        "dense_t100": 11.417856e6,
-                        "decode_dense_t1": 11.295744e6}
+DECODE_TRAFFIC_BYTES = {"decode_moe_e8k2_t64": 89892096 + 2775296,
+                        "decode_moe_e8k2_t16": 89829888 + 2516736,
+                        "decode_moe_e8k2_t4": 87931648 + 1900544,
+                        "decode_dense_t16": 11309056 + 0,
+                        "dense_t100": 11440128 + 0,
+                        "decode_dense_t1": 11309056 + 0}
 
 
 def algorithmic_flops(w, T=None) -> float:
