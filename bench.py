@@ -668,7 +668,7 @@ def per_workload_entry(name, lib, ws, local, dev, warmup):
            "region_ms_min": m["region_ms_min"], "region_ms_max": m["region_ms_max"],
            "timing": m["timing"], "roofline": {k: roof[k] for k in
                                                ("kernel", "bound", "achieved", "peak", "unit",
-                                                "frac", "kernel_ms")},
+                                                "frac", "traffic", "kernel_ms")},
            "clocks": m["clocks"], "l2": workload_config(w, ws)["l2"]}
     del step
     torch.cuda.empty_cache()
