@@ -274,6 +274,15 @@ typedef struct {
    * path then multiplies by them instead of making the fp16 copy inside the
    * call; the other paths read Wd. */
   const void* const* wd_f16;
+  /* Router and permute (prefill tensor-core path): 0 runs them as one kernel
+   * where all of its blocks fit on the GPU at once (bf16, H <= 768, E <= 16
+   * (8 with norm_weight), k <= 4, T <= 128 x the SMs), so that x is read once;
+   * its blocks wait for one another at one grid-wide barrier (bounded: after
+   * 1 s the call fails with MM_ERR_TIMEOUT), so it assumes no kernel of
+   * another stream holds SMs meanwhile.  1 always runs the router and the
+   * permute as two kernels with no grid-wide wait.  The results are the same
+   * bit for bit. */
+  int separate_routing;
 } mm_moe_options;
 
 int mm_moe_forward_opts(const void* x, const void* Wr,

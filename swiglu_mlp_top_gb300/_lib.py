@@ -28,7 +28,8 @@ class MoeOptions(C.Structure):
     _fields_ = [("path", C.c_int), ("logit_noise", C.c_void_p), ("z_coef", C.c_float),
                 ("z_loss", C.c_void_p), ("router_probs", C.c_void_p),
                 ("router_lse", C.c_void_p), ("norm_weight", C.c_void_p),
-                ("norm_eps", C.c_float), ("residual", C.c_int), ("wd_f16", C.c_void_p)]
+                ("norm_eps", C.c_float), ("residual", C.c_int), ("wd_f16", C.c_void_p),
+                ("separate_routing", C.c_int)]
 
 
 _opt = C.POINTER(MoeOptions)

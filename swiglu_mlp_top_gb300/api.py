@@ -178,16 +178,19 @@ def moe_forward(x: torch.Tensor, Wr: torch.Tensor, Wg: Sequence[torch.Tensor],
                 path: str = "auto", stream=None, logit_noise: Optional[torch.Tensor] = None,
                 z_coef: float = 0.0, stats: Optional[dict] = None,
                 norm_weight: Optional[torch.Tensor] = None, norm_eps: float = 1e-5,
-                residual: bool = False, wd_f16: Optional[Sequence[torch.Tensor]] = None):
+                residual: bool = False, wd_f16: Optional[Sequence[torch.Tensor]] = None,
+                separate_routing: bool = False):
     """Top-k MoE forward (mm_moe_forward; mm_moe_forward_opts when router
-    noise, z-loss, router statistics or the block's norm / residual are asked
-    for).
+    noise, z-loss, router statistics, the block's norm / residual, prepared
+    down weights or separate routing kernels are asked for).
 
     Returns (y [T,H], topk_idx [T,k] int32, topk_w [T,k] fp32, aux_loss [] fp32).
     With a dict `stats`, it also receives z_loss [] (z_coef * mean_t lse_t^2),
     probs [T, E] and lse [T] (fp32 device tensors).  With norm_weight the
     layer runs on RMSNorm(x); with residual, y = x + MoE(...).  wd_f16: the
     experts' prepared fp16 down weights (prepare_down_weights).
+    separate_routing: the router and the permute as two kernels instead of
+    one (same results; see mm_moe_options.separate_routing).
     """
     lib = L.load()
     T, H = x.shape
@@ -212,11 +215,12 @@ def moe_forward(x: torch.Tensor, Wr: torch.Tensor, Wg: Sequence[torch.Tensor],
             _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
             _stream(stream))
     if (logit_noise is None and not z_coef and stats is None and norm_weight is None
-            and not residual and wd_f16 is None):
+            and not residual and wd_f16 is None and not separate_routing):
         rc = lib.mm_moe_forward_ex(*args, _PATHS[path])
     else:
         o, keep = _router_options(T, E, dev, path, logit_noise, z_coef, stats, norm_weight,
                                   norm_eps, residual, x.dtype, wd_f16)
+        o.separate_routing = 1 if separate_routing else 0
         rc = lib.mm_moe_forward_opts(*args, C.byref(o))
         del keep
     del ag, au, ad

@@ -547,17 +547,29 @@ static int moe_forward_impl(const void* x, const void* Wr, const void* const* Wg
     if (e0 != cudaSuccess) return cuda_fail(e0, "norm fold");
   }
   const RouteOut ro{nullptr, nullptr, nullptr, nullptr, coef, 0, rv, nrm};
-  cudaError_t e = counted_launch(MM_KERNEL_ROUTER, st, [&] {
-    return launch_router(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w, blk_cnt, blk_prob,
-                         ro, hdr, st);
-  });
-  if (e != cudaSuccess) return cuda_fail(e, "router");
   const DispatchOut dout{offsets, counts, aux_loss, coef, hdr, rv, nrm};
-  e = counted_launch(MM_KERNEL_DISPATCH, st, [&] {
-    return launch_dispatch(dtype, x, T, H, E, k, topk_idx, blk_cnt, blk_prob, dout, perm,
-                           gather ? nullptr : xp, st);
-  });
-  if (e != cudaSuccess) return cuda_fail(e, "dispatch");
+  // router and permute in one kernel where every block fits on the GPU at once
+  // (x read once); otherwise the router grid, then the dispatch grid
+  cudaError_t e;
+  const bool separate = opts != nullptr && opts->separate_routing != 0;
+  if (!separate && route_dispatch_ok(dtype, x, Wr, T, H, E, k, dout)) {
+    e = counted_launch(MM_KERNEL_ROUTER, st, [&] {
+      return launch_route_dispatch(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w,
+                                   blk_cnt, blk_prob, dout, perm, gather ? nullptr : xp, st);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "router + dispatch");
+  } else {
+    e = counted_launch(MM_KERNEL_ROUTER, st, [&] {
+      return launch_router(dtype, x, Wr, logit_bias, T, H, E, k, topk_idx, topk_w, blk_cnt,
+                           blk_prob, ro, hdr, st);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "router");
+    e = counted_launch(MM_KERNEL_DISPATCH, st, [&] {
+      return launch_dispatch(dtype, x, T, H, E, k, topk_idx, blk_cnt, blk_prob, dout, perm,
+                             gather ? nullptr : xp, st);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "dispatch");
+  }
 
   // gate/up over all k*E (slot, expert) groups at once; on the tensor path
   // the same kernel makes the fp16 copy of Wd that the down GEMM reads, with

@@ -149,6 +149,17 @@ cudaError_t launch_dispatch(int dtype, const void* x, int64_t T, int H, int E, i
                             const int32_t* topk_idx, const int32_t* blk_cnt, const float* blk_prob,
                             const DispatchOut& D, int32_t* perm, void* Xp, cudaStream_t st);
 
+// Router and dispatch fused into one kernel (routing.cu): the same outputs
+// as launch_router followed by launch_dispatch, with x read once.  Taken
+// where route_dispatch_ok() holds (shapes, alignment, every block resident);
+// otherwise the two kernels run.
+bool route_dispatch_ok(int dtype, const void* x, const void* Wr, int64_t T, int H, int E, int k,
+                       const DispatchOut& D);
+cudaError_t launch_route_dispatch(int dtype, const void* x, const void* Wr, const float* bias,
+                                  int64_t T, int H, int E, int k, int32_t* topk_idx, float* topk_w,
+                                  int32_t* blk_cnt, float* blk_prob, const DispatchOut& D,
+                                  int32_t* perm, void* Xp, cudaStream_t st);
+
 // Permute-free gate/up: row r of the grouped problem is x row perm[r] / k
 // (gathered by TMA, four rows per request) instead of a copied row of Xp.
 struct RowGather {

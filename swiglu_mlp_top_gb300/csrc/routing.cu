@@ -88,6 +88,7 @@ __device__ void scan_block(int E, int k, int nblk, int64_t T, const RouteExtras&
 __device__ __forceinline__ void finalize_z_loss(const RouterVariant& rv, int nblk, int64_t T,
                                                 int lane) {
   float zs = 0.f;
+#pragma unroll 8
   for (int b = lane; b < nblk; b += 32) zs += __ldcg(rv.blk_z + b);
   zs = warp_sum(zs);
   if (lane == 0) *rv.z_loss = rv.z_coef * zs / static_cast<float>(T);
@@ -478,6 +479,150 @@ __device__ void scan_block(int E, int k, int nblk, int64_t T, const RouteExtras&
 }
 
 
+// Group totals s_tot[g] over the nblk router blocks' counts, the rows of
+// each group in router blocks [0, b) (s_base[g]), and the exclusive scan of
+// the totals (s_off[0..G]).  Warp w sums a run of router blocks, lane g its
+// group (all counts of the run requested at once), then the warps' partial
+// sums are added in warp order.  All kRouteThreads threads take part; the
+// counts are read through L2 (another block of the grid may have written
+// them).
+__device__ void group_offsets(const int32_t* __restrict__ blk_cnt, int nblk, int G, int b,
+                              int* s_tot, int* s_base, int* s_off, int (*s_part)[32][2]) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kWarps = kRouteThreads / 32;
+  {
+    const int per = (nblk + kWarps - 1) / kWarps;
+    const int b0 = warp * per, b1 = min(nblk, b0 + per);
+    for (int g0 = 0; g0 < G; g0 += 32) {
+      const int g = g0 + lane;
+      int all = 0, before = 0;
+      if (g < G) {
+        for (int bb = b0; bb < b1; bb += 32) {
+          int c[32];                         // one round of requests for a run of 32 blocks
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            c[j] = (bb + j < b1) ? __ldcg(blk_cnt + static_cast<int64_t>(bb + j) * G + g) : 0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            all += c[j];
+            before += (bb + j < b) ? c[j] : 0;
+          }
+        }
+      }
+      __syncthreads();                       // s_part of the previous round is read
+      if (g < G) {
+        s_part[warp][lane][0] = all;
+        s_part[warp][lane][1] = before;
+      }
+      __syncthreads();
+      if (tid < 32 && g0 + tid < G) {
+        int a = 0, bf = 0;
+        for (int w = 0; w < kWarps; ++w) {
+          a += s_part[w][tid][0];
+          bf += s_part[w][tid][1];
+        }
+        s_tot[g0 + tid] = a;
+        s_base[g0 + tid] = bf;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive scan of the group totals: a lane owns a run of groups
+    const int gper = (G + 31) / 32;
+    const int g0 = lane * gper, g1 = min(G, g0 + gper);
+    int sum = 0;
+    for (int g = g0; g < g1; ++g) sum += s_tot[g];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    int run = incl - sum;
+    for (int g = g0; g < g1; ++g) {
+      s_off[g] = run;
+      run += s_tot[g];
+    }
+    if (lane == 31) s_off[G] = incl;
+  }
+  __syncthreads();
+}
+
+// What one block of the dispatch writes for the whole call: the group
+// offsets, the expert counts, the aux loss ([L13] §1.6; chapter 4 §4.4:
+// aux = E*coef*sum_e (count_e/T)(P_e/T), P_e = sum_b blk_prob[b][e] by warp
+// e % 8 as lane-strided partial sums over the router blocks and a fixed xor
+// tree, then one thread adds count_e * P_e in expert order) and the z-loss.
+// All kRouteThreads threads of that block take part.
+__device__ void write_route_totals(const DispatchOut& D, const int* s_tot, const int* s_off, int G,
+                                   int E, int k, int nblk, const float* __restrict__ blk_prob,
+                                   int64_t T) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kWarps = kRouteThreads / 32;
+  for (int g = tid; g <= G; g += kRouteThreads) D.offsets[g] = s_off[g];
+  for (int e = tid; e < E; e += kRouteThreads) {
+    int c = 0;
+    for (int s = 0; s < k; ++s) c += s_tot[s * E + e];
+    if (D.counts != nullptr) D.counts[e] = c;
+  }
+  __shared__ float s_P[MM_MAX_EXPERTS];
+  for (int e = warp; e < E; e += kWarps) {
+    float P = 0.f;
+#pragma unroll 8
+    for (int bb = lane; bb < nblk; bb += 32) P += __ldcg(blk_prob + static_cast<int64_t>(bb) * E + e);
+    P = warp_sum(P);
+    if (lane == 0) s_P[e] = P;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float acc = 0.f;
+    for (int e = 0; e < E; ++e) {
+      int c = 0;
+      for (int s = 0; s < k; ++s) c += s_tot[s * E + e];
+      acc = fmaf(static_cast<float>(c), s_P[e], acc);
+    }
+    const float invT = 1.0f / static_cast<float>(T);
+    *D.aux_loss = static_cast<float>(E) * D.coef * acc * invT * invT;
+  }
+  if (warp == kWarps - 1 && D.rv.z_loss != nullptr) finalize_z_loss(D.rv, nblk, T, lane);
+}
+
+// write_route_totals for the last four warps of a block alone (their own
+// named barrier), so that the block's other warps can go on meanwhile; the
+// same arithmetic in the same order.
+__device__ void write_route_totals_w4(const DispatchOut& D, const int* s_tot, const int* s_off,
+                                      int G, int E, int k, int nblk,
+                                      const float* __restrict__ blk_prob, int64_t T) {
+  const int t4 = threadIdx.x - (blockDim.x - 128), lane = threadIdx.x & 31, wi = t4 >> 5;
+  for (int g = t4; g <= G; g += 128) D.offsets[g] = s_off[g];
+  for (int e = t4; e < E; e += 128) {
+    int c = 0;
+    for (int s = 0; s < k; ++s) c += s_tot[s * E + e];
+    if (D.counts != nullptr) D.counts[e] = c;
+  }
+  __shared__ float s_P4[MM_MAX_EXPERTS];
+  for (int e = wi; e < E; e += 4) {
+    float P = 0.f;
+#pragma unroll 8
+    for (int bb = lane; bb < nblk; bb += 32) P += __ldcg(blk_prob + static_cast<int64_t>(bb) * E + e);
+    P = warp_sum(P);
+    if (lane == 0) s_P4[e] = P;
+  }
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+  if (t4 == 0) {
+    float acc = 0.f;
+    for (int e = 0; e < E; ++e) {
+      int c = 0;
+      for (int s = 0; s < k; ++s) c += s_tot[s * E + e];
+      acc = fmaf(static_cast<float>(c), s_P4[e], acc);
+    }
+    const float invT = 1.0f / static_cast<float>(T);
+    *D.aux_loss = static_cast<float>(E) * D.coef * acc * invT * invT;
+  }
+  if (wi == 3 && D.rv.z_loss != nullptr) finalize_z_loss(D.rv, nblk, T, lane);
+}
+
 // ---------------------------------------------------------------------------
 // Dispatch: block b owns the same tokens as router block b.  From the
 // router's per-block counts it derives, for every (slot s, expert e) group
@@ -536,95 +681,8 @@ dispatch_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, int k,
   __shared__ int s_sel[kRouteTokensPerBlock * MM_MAX_TOPK];
   for (int a = tid; a < ntok * k; a += kRouteThreads) s_sel[a] = topk_idx[tok0 * k + a];
 
-  // group totals and this block's bases: warp w sums a run of router blocks,
-  // lane g its group (all counts of the run requested at once), then the
-  // warps' partial sums are added in warp order
-  {
-    const int per = (nblk + kWarps - 1) / kWarps;
-    const int b0 = warp * per, b1 = min(nblk, b0 + per);
-    for (int g0 = 0; g0 < G; g0 += 32) {
-      const int g = g0 + lane;
-      int all = 0, before = 0;
-      if (g < G) {
-        for (int bb = b0; bb < b1; bb += 32) {
-          int c[32];                         // one round of requests for a run of 32 blocks
-#pragma unroll
-          for (int j = 0; j < 32; ++j) c[j] = (bb + j < b1) ? blk_cnt[static_cast<int64_t>(bb + j) * G + g] : 0;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            all += c[j];
-            before += (bb + j < b) ? c[j] : 0;
-          }
-        }
-      }
-      __syncthreads();                       // s_part of the previous round is read
-      if (g < G) {
-        s_part[warp][lane][0] = all;
-        s_part[warp][lane][1] = before;
-      }
-      __syncthreads();
-      if (tid < 32 && g0 + tid < G) {
-        int a = 0, bf = 0;
-        for (int w = 0; w < kWarps; ++w) {
-          a += s_part[w][tid][0];
-          bf += s_part[w][tid][1];
-        }
-        s_tot[g0 + tid] = a;
-        s_base[g0 + tid] = bf;
-      }
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // exclusive scan of the group totals: a lane owns a run of groups
-    const int gper = (G + 31) / 32;
-    const int g0 = lane * gper, g1 = min(G, g0 + gper);
-    int sum = 0;
-    for (int g = g0; g < g1; ++g) sum += s_tot[g];
-    int incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += n;
-    }
-    int run = incl - sum;
-    for (int g = g0; g < g1; ++g) {
-      s_off[g] = run;
-      run += s_tot[g];
-    }
-    if (lane == 31) s_off[G] = incl;
-  }
-  __syncthreads();
-  if (b == 0) {
-    for (int g = tid; g <= G; g += kRouteThreads) D.offsets[g] = s_off[g];
-    for (int e = tid; e < E; e += kRouteThreads) {
-      int c = 0;
-      for (int s = 0; s < k; ++s) c += s_tot[s * E + e];
-      if (D.counts != nullptr) D.counts[e] = c;
-    }
-    // aux: P_e by warp e % 8 (lane-strided partial sums over the router
-    // blocks, a fixed xor tree), then one thread adds count_e * P_e in order
-    __shared__ float s_P[MM_MAX_EXPERTS];
-    for (int e = warp; e < E; e += kWarps) {
-      float P = 0.f;
-      for (int bb = lane; bb < nblk; bb += 32) P += blk_prob[static_cast<int64_t>(bb) * E + e];
-      P = warp_sum(P);
-      if (lane == 0) s_P[e] = P;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float acc = 0.f;
-      for (int e = 0; e < E; ++e) {
-        int c = 0;
-        for (int s = 0; s < k; ++s) c += s_tot[s * E + e];
-        acc = fmaf(static_cast<float>(c), s_P[e], acc);
-      }
-      const float invT = 1.0f / static_cast<float>(T);
-      *D.aux_loss = static_cast<float>(E) * D.coef * acc * invT * invT;
-    }
-    if (warp == kWarps - 1 && D.rv.z_loss != nullptr) finalize_z_loss(D.rv, nblk, T, lane);
-  }
-
+  group_offsets(blk_cnt, nblk, G, b, s_tot, s_base, s_off, s_part);
+  if (b == 0) write_route_totals(D, s_tot, s_off, G, E, k, nblk, blk_prob, T);
   for (int s = 0; s < k; ++s) {
     for (int i = tid; i < E; i += kRouteThreads) s_w0cnt[i] = 0;
     __syncthreads();
@@ -710,6 +768,92 @@ dispatch_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, int k,
 // then take softmax, top-k, alpha, the block's group counts and
 // probability sums (fixed-order reductions) exactly as router_kernel does.
 // ---------------------------------------------------------------------------
+// One token's routing from its logits p[0..E) (fp32, as accumulated):
+// p += bias (+ noise); p = softmax(p) (max subtracted); lse = logsumexp of
+// the biased logits; top-k by k arg-max passes in expert order with a strict
+// comparison (equal p -> the lower index first); sel_sum = sum of the k
+// selected p.  The tensor-core router and the fused router + dispatch share
+// it, so both take the same decisions bit for bit.
+template <int EP>
+__device__ __forceinline__ void route_token(float (&p)[EP], int E, int k, const float* s_bias,
+                                            const float* nz, float& lse,
+                                            int (&sel_e)[MM_MAX_TOPK],
+                                            float (&sel_p)[MM_MAX_TOPK], float& sel_sum) {
+  // loops over the E experts only (E is uniform; the padded columns past
+  // E are never read)
+  float m = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < EP; ++e) {
+    if (e >= E) break;
+    p[e] += s_bias[e];
+    if (nz != nullptr) p[e] += nz[e];
+    m = fmaxf(m, p[e]);
+  }
+  float z = 0.f;
+#pragma unroll
+  for (int e = 0; e < EP; ++e) {
+    if (e >= E) break;
+    p[e] = expf(p[e] - m);
+    z += p[e];
+  }
+#pragma unroll
+  for (int e = 0; e < EP; ++e) {
+    if (e >= E) break;
+    p[e] = p[e] / z;
+  }
+  lse = m + logf(z);
+  uint64_t taken = 0;
+  sel_sum = 0.f;
+#pragma unroll
+  for (int sl = 0; sl < MM_MAX_TOPK; ++sl) {
+    sel_e[sl] = 0;
+    sel_p[sl] = 0.f;
+    if (sl < k) {
+      float bp = -1.f;
+      int be = 0;
+#pragma unroll
+      for (int e = 0; e < EP; ++e) {
+        if (e >= E) break;
+        if (!((taken >> e) & 1ull) && p[e] > bp) {
+          bp = p[e];
+          be = e;
+        }
+      }
+      taken |= 1ull << be;
+      sel_sum += bp;
+      sel_e[sl] = be;
+      sel_p[sl] = bp;
+    }
+  }
+}
+
+// Block norm, tensor-core routers: columns [0, E) of the accumulator row
+// hold x . hi, columns [E, 2E) x . lo; the logits are inv_rms * (hi + lo).
+// The remainders are loaded from TMEM at column E (a runtime column address)
+// so that every register index is a compile-time one.  The loads touch
+// columns below E + 16 * ceil(E / 16), inside the callers' allocations (64
+// columns with E <= 32; 32 columns with E <= 8).  Warp-collective.
+template <int EP>
+__device__ __forceinline__ void norm_logits(float (&p)[EP], uint32_t trow, int E, float inv_rms) {
+  float lo[EP];
+#pragma unroll
+  for (int c0 = 0; c0 < EP; c0 += 16) {
+    if (c0 >= E) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) lo[c0 + j] = 0.f;
+      continue;
+    }
+    uint32_t r[16];
+    tmem_ld_32x32b_x16(trow + static_cast<uint32_t>(E + c0), r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) lo[c0 + j] = __uint_as_float(r[j]);
+  }
+#pragma unroll
+  for (int e = 0; e < EP; ++e)
+    if (e < E) p[e] = inv_rms * (p[e] + lo[e]);
+}
+
 constexpr int kRtStages = 2;
 struct RtMaps {
   CUtensorMap x;                 // x as (64, T, H / 64), box 64 x 64 x nkb
@@ -849,36 +993,13 @@ router_tc_kernel(const __grid_constant__ RtMaps M, int64_t T, int H, int E, int 
       if (norm) {
         // logits = inv_rms * (x . hi + x . lo); columns E.. hold the remainders
         const float sv = valid ? s_inv[t] : 0.f;
-#pragma unroll
-        for (int e = 0; e < EP; ++e) {
-          if (e >= E) break;
-          p[e] = sv * (p[e] + p[E + e]);
-        }
+        norm_logits<EP>(p, tmem + (static_cast<uint32_t>(warp * 32) << 16), E, sv);
       }
-      // loops over the E experts only (E is uniform; the padded columns past
-      // E are never read)
-      float m = -INFINITY;
       const float* nz = (rv.noise != nullptr && valid) ? rv.noise + (t0 + t) * E : nullptr;
-#pragma unroll
-      for (int e = 0; e < EP; ++e) {
-        if (e >= E) break;
-        p[e] += s_bias[e];
-        if (nz != nullptr) p[e] += nz[e];
-        m = fmaxf(m, p[e]);
-      }
-      float z = 0.f;
-#pragma unroll
-      for (int e = 0; e < EP; ++e) {
-        if (e >= E) break;
-        p[e] = expf(p[e] - m);
-        z += p[e];
-      }
-#pragma unroll
-      for (int e = 0; e < EP; ++e) {
-        if (e >= E) break;
-        p[e] = p[e] / z;
-      }
-      const float lse = m + logf(z);
+      float lse, sel_sum;
+      int sel_e[MM_MAX_TOPK];
+      float sel_p[MM_MAX_TOPK];
+      route_token<EP>(p, E, k, s_bias, nz, lse, sel_e, sel_p, sel_sum);
       if (valid) {
         if (rv.probs != nullptr) {
           float* pr = rv.probs + (t0 + t) * E;
@@ -895,32 +1016,6 @@ router_tc_kernel(const __grid_constant__ RtMaps M, int64_t T, int H, int E, int 
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
         if (lane == 0) s_redz[warp] = v;
-      }
-      // top-k: k arg-max passes in expert order, strict comparison (lower index first)
-      uint64_t taken = 0;
-      float sel_sum = 0.f;
-      int sel_e[MM_MAX_TOPK];
-      float sel_p[MM_MAX_TOPK];
-#pragma unroll
-      for (int sl = 0; sl < MM_MAX_TOPK; ++sl) {
-        sel_e[sl] = 0;
-        sel_p[sl] = 0.f;
-        if (sl < k) {
-          float bp = -1.f;
-          int be = 0;
-#pragma unroll
-          for (int e = 0; e < EP; ++e) {
-            if (e >= E) break;
-            if (!((taken >> e) & 1ull) && p[e] > bp) {
-              bp = p[e];
-              be = e;
-            }
-          }
-          taken |= 1ull << be;
-          sel_sum += bp;
-          sel_e[sl] = be;
-          sel_p[sl] = bp;
-        }
       }
       if (valid) {
         const float inv = sel_sum + 1e-20f;
@@ -1052,6 +1147,470 @@ static cudaError_t launch_router_tc(const void* x, const void* Wr, const float* 
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, fn, m, T, H, E, k, bias, topk_idx, topk_w, blk_cnt, blk_prob, X,
                             nkb, static_cast<uint32_t>(stage));
+}
+
+// ---------------------------------------------------------------------------
+// Router and dispatch in one kernel, so that x is read from HBM once per
+// call (bf16; H a multiple of 64 up to 768; E, or 2E with the block norm,
+// up to 16; k up to 4; every block resident at once: T <= 128 x the SMs).
+// Block b routes tokens [128 b, +128): router blocks 2b and 2b+1 of the
+// two-kernel path, whose per-block partials (counts, probability sums,
+// lse^2 sums) it writes unchanged, so that every output is the same bit for
+// bit.  Its x rows stay in shared memory for the whole call: all H / 64
+// k-blocks as 128-byte-swizzled tiles, the A operand of the logits' UMMA
+// (M = 128 tokens, N = 16, fp32 in TMEM) and, after one grid barrier that
+// publishes every block's group counts, the source of its rows of Xp.
+// Past the barrier each block derives the group offsets and its bases as
+// the dispatch kernel does, writes perm and its Xp rows (x * inv_rms * w
+// with the block norm), and block 0 the offsets, counts, aux loss and
+// z-loss.  The next kernel of the stream is released only after the
+// barrier, when every block of this grid already holds its SM.
+// Warp roles: warps 0-3 route (thread = token = TMEM lane); warp 4 lane 0
+// issues the TMA loads, warp 5 lane 0 the UMMAs; all 8 warps take the norm's
+// sums of squares and the row copies.
+// ---------------------------------------------------------------------------
+constexpr int kRdTokens = 128;
+constexpr int kRdThreads = 512;                  // 16 warps: the row copies want many
+constexpr int kRdEP = 16;                        // UMMA N: E (2E with the norm) padded
+constexpr int kRdMaxKb = 12;                     // H <= 768
+constexpr int kRdMaxK = 4;
+constexpr int kRdMaxG = kRdEP * kRdMaxK;
+constexpr uint32_t kRdXTile = kRdTokens * 128;   // 16 KiB: 128 rows x one k-block
+constexpr uint32_t kRdWTile = kRdEP * 128;
+
+struct RdMaps {
+  CUtensorMap x;                 // x as (64, T, H / 64), box 64 x 128 x nkb (rows >= T read as 0)
+  CUtensorMap wr;                // Wr (or the norm's halves) as (64, En, H / 64), box 64 x 16 x nkb
+};
+
+__global__ void __launch_bounds__(kRdThreads, 1)
+route_dispatch_kernel(const __grid_constant__ RdMaps M, int64_t T, int H, int E, int k,
+                      const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
+                      float* __restrict__ topk_w, int32_t* __restrict__ blk_cnt,
+                      float* __restrict__ blk_prob, const DispatchOut D,
+                      int32_t* __restrict__ perm, __nv_bfloat16* __restrict__ Xp, int nkb) {
+  constexpr int EP = kRdEP;
+  extern __shared__ unsigned char rd_raw[];
+  uint8_t* smem = align1024(rd_raw);
+  const int KB = H / 64;
+  const int nst = KB / nkb;
+  uint8_t* sx = smem;                            // [KB][128 rows][128 B]
+  uint8_t* sw = smem + KB * kRdXTile;            // [KB][16 rows][128 B]
+  __shared__ __align__(8) uint64_t full[kRdMaxKb], lbar, drained;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_gcnt[2][kRdMaxG];             // per router block of 64 tokens
+  __shared__ float s_red[4][EP];
+  __shared__ float s_redz[4];
+  __shared__ float s_bias[EP];
+  __shared__ float s_inv[kRdTokens];
+  __shared__ int s_wcnt[4][EP];
+  __shared__ int s_pos[kRdTokens * kRdMaxK];
+  __shared__ int s_tot[kRdMaxG], s_base[kRdMaxG], s_off[kRdMaxG + 1];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kWarps = kRdThreads / 32;
+  const int b = blockIdx.x;
+  const int64_t t0 = static_cast<int64_t>(b) * kRdTokens;
+  const int ntok = static_cast<int>(T - t0 < kRdTokens ? T - t0 : kRdTokens);
+  const int nrb = static_cast<int>((T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock);
+  const int rb0 = 2 * b;                         // this block's first router block
+  const int G = k * E;
+  WsHeader* hdr = D.hdr;
+  const RouterVariant& rv = D.rv;
+  const __nv_bfloat16* norm_w = static_cast<const __nv_bfloat16*>(D.norm.w);
+
+  if (tid == 0) {
+    for (int q = 0; q < nst; ++q) mbar_init(&full[q], 1);
+    mbar_init(&lbar, 1);
+    mbar_init(&drained, 1);
+    fence_mbar_init();
+  }
+  for (int g = tid; g < 2 * kRdMaxG; g += kRdThreads) (&s_gcnt[0][0])[g] = 0;
+  if (warp == 4) {
+    tmem_alloc(&s_tmem, 32);
+    tmem_relinquish();
+  }
+  // launched as a programmatic dependent: x, Wr and the outputs belong to
+  // the previous kernel until it has finished
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid < EP) s_bias[tid] = (bias != nullptr && tid < E) ? bias[tid] : 0.f;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  bool ok = true;
+
+  if (tid == 4 * 32) {
+    // producer: every stage at once (nkb k-blocks of x and of Wr each); no slot is reused
+    for (int q = 0; q < nst; ++q) {
+      mbar_arrive_expect_tx(&full[q], static_cast<uint32_t>(nkb) * (kRdXTile + kRdWTile));
+      tma_load_3d(sx + q * nkb * kRdXTile, &M.x, &full[q], 0, static_cast<int32_t>(t0), q * nkb);
+      tma_load_3d(sw + q * nkb * kRdWTile, &M.wr, &full[q], 0, 0, q * nkb);
+    }
+  }
+  if (tid == 5 * 32) {
+    // MMA issuer: L[t, e] = sum over the k-blocks of x_t . Wr_e
+    const uint32_t idesc = idesc_bf16_f32(kRdTokens, EP);
+    bool mok = true;
+    for (int q = 0; q < nst && mok; ++q) {
+      if (!mbar_wait(&full[q], 0, nullptr, hdr, 66)) {
+        mok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int kl = 0; kl < nkb; ++kl) {
+        const int kb = q * nkb + kl;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(tmem, smem_desc_sw128(smem_u32(sx + kb * kRdXTile + kk * 32)),
+                    smem_desc_sw128(smem_u32(sw + kb * kRdWTile + kk * 32)), idesc,
+                    (kb | kk) ? 1u : 0u);
+      }
+    }
+    if (mok) umma_commit(&lbar);
+  }
+  if (norm_w != nullptr) {
+    // block RMSNorm: each token's 1 / rms from its staged row (warp w takes
+    // tokens w, w + 8, ...; lanes over 16-byte vectors in row order, then a
+    // fixed xor tree: the tensor-core router's order)
+    bool landed = true;
+    for (int q = 0; q < nst; ++q) landed = warp_wait(&full[q], 0, nullptr, hdr, 67) && landed;
+    if (landed) {
+      for (int t = warp; t < ntok; t += kWarps) {
+        float ss = 0.f;
+        for (int v = lane; v < H / 8; v += 32) {
+          const uint4 qv = *reinterpret_cast<const uint4*>(
+              sx + (v >> 3) * kRdXTile + t * 128 + (((v & 7) ^ (t & 7)) << 4));
+          const uint32_t w4[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float a = __uint_as_float(w4[j] << 16), c = __uint_as_float(w4[j] & 0xffff0000u);
+            ss = fmaf(a, a, ss);
+            ss = fmaf(c, c, ss);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) {
+          const float sv = 1.0f / sqrtf(ss / static_cast<float>(H) + D.norm.eps);
+          s_inv[t] = sv;
+          D.norm.inv_rms[t0 + t] = sv;
+        }
+      }
+    }
+    ok = ok && landed;
+    __syncthreads();
+  }
+
+  // ---- routing: warps 0-3, thread = token (TMEM lane)
+  int sel_e[MM_MAX_TOPK];
+  int rk[kRdMaxK];
+  const int t = tid;
+  const bool valid = warp < 4 && t < ntok;
+  if (warp < 4) {
+    ok = warp_wait(&lbar, 0, nullptr, hdr, 68) && ok;
+    tc_fence_after();
+    float p[EP];
+    float lse = 0.f, sel_sum = 0.f;
+    float sel_p[MM_MAX_TOPK];
+    if (ok) {
+      uint32_t r[16];
+      tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(warp * 32) << 16), r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) p[j] = __uint_as_float(r[j]);
+      if (norm_w != nullptr) {
+        // logits = inv_rms * (x . hi + x . lo); columns E.. hold the remainders
+        const float sv = valid ? s_inv[t] : 0.f;
+        norm_logits<EP>(p, tmem + (static_cast<uint32_t>(warp * 32) << 16), E, sv);
+      }
+      const float* nz = (rv.noise != nullptr && valid) ? rv.noise + (t0 + t) * E : nullptr;
+      route_token<EP>(p, E, k, s_bias, nz, lse, sel_e, sel_p, sel_sum);
+    } else {
+#pragma unroll
+      for (int e = 0; e < EP; ++e) p[e] = 0.f;
+#pragma unroll
+      for (int sl = 0; sl < MM_MAX_TOPK; ++sl) sel_e[sl] = 0;
+    }
+    if (valid && ok) {
+      if (rv.probs != nullptr) {
+        float* pr = rv.probs + (t0 + t) * E;
+#pragma unroll
+        for (int e = 0; e < EP; ++e) {
+          if (e >= E) break;
+          pr[e] = p[e];
+        }
+      }
+      if (rv.lse != nullptr) rv.lse[t0 + t] = lse;
+      const float inv = sel_sum + 1e-20f;
+#pragma unroll
+      for (int sl = 0; sl < MM_MAX_TOPK; ++sl) {
+        if (sl < k) {
+          topk_idx[(t0 + t) * k + sl] = sel_e[sl];
+          topk_w[(t0 + t) * k + sl] = sel_p[sl] / inv;
+        }
+      }
+    }
+    {
+      float v = (valid && ok) ? lse * lse : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) s_redz[warp] = v;
+    }
+    // the router block's probability sums per expert: fixed butterfly order
+#pragma unroll
+    for (int e = 0; e < EP; ++e) {
+      if (e >= E) break;
+      float v = (valid && ok) ? p[e] : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) s_red[warp][e] = v;
+    }
+  }
+  // rank of each assignment among the block's tokens that chose the same
+  // expert in the same slot, in token order, and from the same matches the
+  // router blocks' group counts (warps 0-1: router block 2b, warps 2-3: 2b + 1)
+#pragma unroll
+  for (int sl = 0; sl < kRdMaxK; ++sl) {
+    if (sl >= k) break;
+    int e = -1, rank = 0;
+    unsigned peers = 0;
+    if (warp < 4) {
+      e = valid ? sel_e[sl] : -1;
+      peers = __match_any_sync(0xffffffffu, e);
+      rank = __popc(peers & ((1u << lane) - 1u));
+    }
+    for (int i = tid; i < 4 * EP; i += kRdThreads) (&s_wcnt[0][0])[i] = 0;
+    __syncthreads();
+    if (warp < 4 && e >= 0 && lane == __ffs(peers) - 1) s_wcnt[warp][e] = __popc(peers);
+    __syncthreads();
+    if (warp < 4 && e >= 0) {
+      for (int w = 0; w < warp; ++w) rank += s_wcnt[w][e];
+      rk[sl] = rank;
+    }
+    if (tid < 2 * E) {
+      const int i = tid / E, ee = tid - i * E;
+      s_gcnt[i][sl * E + ee] = s_wcnt[2 * i][ee] + s_wcnt[2 * i + 1][ee];
+    }
+    __syncthreads();
+  }
+  ok = __syncthreads_and(ok) != 0;
+  // the router blocks' partials, as the tensor-core router writes them (warp
+  // 0; the grid barrier's __syncthreads and release by thread 0 publish them)
+  if (ok && warp == 0) {
+    for (int i = 0; i < 2; ++i) {
+      const int rb = rb0 + i;
+      if (rb >= nrb) break;
+      if (lane < E) blk_prob[static_cast<int64_t>(rb) * E + lane] = s_red[2 * i][lane] + s_red[2 * i + 1][lane];
+      if (lane == 0 && rv.blk_z != nullptr) rv.blk_z[rb] = s_redz[2 * i] + s_redz[2 * i + 1];
+      for (int g = lane; g < G; g += 32) blk_cnt[static_cast<int64_t>(rb) * G + g] = s_gcnt[i][g];
+    }
+  }
+  unsigned ticket = 0;
+  ok = grid_barrier(hdr, 69, 1, &ticket) && ok;
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  if (ok) {
+    // group totals and this block's bases: thread (slice j, group g) adds the
+    // counts of router blocks j, j + S, ... (all requested at once), then the
+    // slices meet in shared memory (integer sums: exact in any order)
+    for (int g = tid; g < G; g += kRdThreads) {
+      s_tot[g] = 0;
+      s_base[g] = 0;
+    }
+    __syncthreads();
+    {
+      const int S = kRdThreads / G;                // G <= 64: at least 8 slices
+      const int g = tid % G, j = tid / G;
+      if (j < S) {
+        int all = 0, before = 0;
+        for (int rb = j; rb < nrb; rb += 8 * S) {
+          int c[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int r = rb + u * S;
+            c[u] = r < nrb ? __ldcg(blk_cnt + static_cast<int64_t>(r) * G + g) : 0;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            all += c[u];
+            before += (rb + u * S < rb0) ? c[u] : 0;
+          }
+        }
+        atomicAdd(&s_tot[g], all);
+        atomicAdd(&s_base[g], before);
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // exclusive scan of the group totals, two groups a lane (G <= 64)
+      const int g0 = 2 * lane;
+      const int c0 = g0 < G ? s_tot[g0] : 0, c1 = g0 + 1 < G ? s_tot[g0 + 1] : 0;
+      int incl = c0 + c1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      const int ex = incl - c0 - c1;
+      if (g0 < G) s_off[g0] = ex;
+      if (g0 + 1 < G) s_off[g0 + 1] = ex + c0;
+      if (lane == 31) s_off[G] = incl;
+    }
+    __syncthreads();
+    const bool totals = b == 0;
+    if (valid) {
+#pragma unroll
+      for (int sl = 0; sl < kRdMaxK; ++sl) {
+        if (sl >= k) break;
+        const int g = sl * E + sel_e[sl];
+        const int pos = s_off[g] + s_base[g] + rk[sl];
+        s_pos[t * k + sl] = pos;
+        perm[pos] = static_cast<int32_t>((t0 + t) * k + sl);
+      }
+    }
+    __syncthreads();
+    if (totals && warp >= kWarps - 4) {
+      // block 0: warps 12-15 write the call's totals while warps 0-11 copy its rows
+      write_route_totals_w4(D, s_tot, s_off, G, E, k, nrb, blk_prob, T);
+    } else if (Xp != nullptr) {
+      // the staged rows, un-swizzled: a warp per assignment row, lane l on
+      // 16-byte chunks l, l + 32, ... (k-block (l >> 3) + 4 j, chunk l & 7),
+      // two rows in flight per warp (block 0: warps 0-11)
+      const int na = ntok * k;
+      const int nv = H / 8;
+      const uint32_t lane_off = static_cast<uint32_t>(lane >> 3) * kRdXTile;
+      const int lq = lane & 7;
+      const int nw = totals ? kWarps - 4 : kWarps;   // copying warps
+      const int cw = warp;
+      constexpr int kCh = kRdMaxKb * 64 / 8 / 32;     // 16-byte chunks per lane and row, at most
+      for (int a0 = cw; a0 < na; a0 += 2 * nw) {
+        // two rows: every chunk requested before any is stored
+        uint4 q[2][kCh];
+        int64_t drow[2];
+        int trow[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int a = a0 + r * nw;
+          trow[r] = a < na ? a / k : -1;
+          drow[r] = a < na ? static_cast<int64_t>(s_pos[a]) * H : 0;
+          if (a >= na) continue;
+          const int tt = trow[r];
+          const uint8_t* src = sx + lane_off + tt * 128 + ((lq ^ (tt & 7)) << 4);
+#pragma unroll
+          for (int c = 0; c < kCh; ++c)
+            if (lane + 32 * c < nv) q[r][c] = *reinterpret_cast<const uint4*>(src + 4 * c * kRdXTile);
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          if (trow[r] < 0) continue;
+          __nv_bfloat16* dst = Xp + drow[r] + lane * 8;
+          const float inv = norm_w != nullptr ? s_inv[trow[r]] : 1.f;
+#pragma unroll
+          for (int c = 0; c < kCh; ++c) {
+            const int v = lane + 32 * c;                // this lane's chunk
+            if (v >= nv) continue;
+            uint4 qv = q[r][c];
+            if (norm_w != nullptr) {
+              float xv[8], g8[8];
+              const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&qv);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float2 f = __bfloat1622float2(h2[j]);
+                xv[2 * j] = f.x;
+                xv[2 * j + 1] = f.y;
+              }
+              load_vec8(norm_w + v * 8, g8);
+              __nv_bfloat16 o8[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) o8[j] = static_cast<__nv_bfloat16>(xv[j] * inv * g8[j]);
+              qv = *reinterpret_cast<const uint4*>(o8);
+            }
+            *reinterpret_cast<uint4*>(dst + 32 * c * 8) = qv;
+          }
+        }
+      }
+    }
+  }
+  if (tid == 5 * 32) {
+    umma_commit(&drained);                       // every issued UMMA has finished
+    mbar_wait(&drained, 0, nullptr, hdr, 70);
+  }
+  if (tid == 4 * 32)                             // every copy into shared memory has landed
+    for (int q = 0; q < nst; ++q) mbar_wait(&full[q], 0, nullptr, hdr, 71);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 4) tmem_dealloc(tmem, 32);
+  if (tid == 0) grid_barrier_reset(hdr, ticket);
+}
+
+// Whether the fused router + dispatch takes this call: bf16, the shapes it
+// is built for, 16-byte aligned x and router weights, and every block
+// resident at once (one per SM).
+bool route_dispatch_ok(int dtype, const void* x, const void* Wr, int64_t T, int H, int E, int k,
+                       const DispatchOut& D) {
+  const bool norm = D.norm.w != nullptr;
+  const int En = norm ? 2 * E : E;
+  const void* wr = norm ? D.norm.wr_hl : Wr;
+  if (dtype != kDtypeBF16 || H % 64 != 0 || H / 64 > kRdMaxKb || En > kRdEP || k > kRdMaxK ||
+      T < 1 || (reinterpret_cast<uintptr_t>(x) & 15u) != 0 ||
+      (reinterpret_cast<uintptr_t>(wr) & 15u) != 0 || D.hdr == nullptr)
+    return false;
+  const size_t smem = static_cast<size_t>(H / 64) * (kRdXTile + kRdWTile) + 1024;
+  auto fn = route_dispatch_kernel;
+  static int max_blocks[kRdMaxKb + 1];
+  static bool known[kRdMaxKb + 1];
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!known[H / 64]) {
+    int per_sm = 0;
+    if (ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kRdThreads, smem) != cudaSuccess) {
+      (void)cudaGetLastError();
+      per_sm = 0;
+    }
+    max_blocks[H / 64] = per_sm * num_sms();
+    known[H / 64] = true;
+  }
+  return (T + kRdTokens - 1) / kRdTokens <= max_blocks[H / 64];
+}
+
+// Launch of the fused router + dispatch; route_dispatch_ok() must hold.
+cudaError_t launch_route_dispatch(int dtype, const void* x, const void* Wr, const float* bias,
+                                  int64_t T, int H, int E, int k, int32_t* topk_idx, float* topk_w,
+                                  int32_t* blk_cnt, float* blk_prob, const DispatchOut& D,
+                                  int32_t* perm, void* Xp, cudaStream_t st) {
+  (void)dtype;
+  const bool norm = D.norm.w != nullptr;
+  const int En = norm ? 2 * E : E;
+  const void* wr = norm ? D.norm.wr_hl : Wr;
+  const int KB = H / 64;
+  int nkb = 4;
+  while (KB % nkb != 0) --nkb;
+  const size_t smem = static_cast<size_t>(KB) * (kRdXTile + kRdWTile) + 1024;
+  auto fn = route_dispatch_kernel;
+  const int64_t nblk = (T + kRdTokens - 1) / kRdTokens;
+  RdMaps m;
+  const uint64_t sx[2] = {static_cast<uint64_t>(H) * 2, 128};
+  const uint64_t dx[3] = {64, static_cast<uint64_t>(T), static_cast<uint64_t>(KB)};
+  const uint32_t bx[3] = {64, static_cast<uint32_t>(kRdTokens), static_cast<uint32_t>(nkb)};
+  if (!make_map_3d(&m.x, x, dx, sx, bx)) return cudaErrorInvalidValue;
+  const uint64_t dw[3] = {64, static_cast<uint64_t>(En), static_cast<uint64_t>(KB)};
+  const uint32_t bw[3] = {64, static_cast<uint32_t>(kRdEP), static_cast<uint32_t>(nkb)};
+  if (!make_map_3d(&m.wr, wr, dw, sx, bw)) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(nblk));
+  cfg.blockDim = dim3(kRdThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, m, T, H, E, k, bias, topk_idx, topk_w, blk_cnt, blk_prob, D,
+                            perm, static_cast<__nv_bfloat16*>(Xp), nkb);
 }
 
 cudaError_t launch_router(int dtype, const void* x, const void* Wr, const float* bias, int64_t T,
