@@ -33,6 +33,7 @@ __device__ __forceinline__ float bw_warp_sum(float v) {
 __global__ void __launch_bounds__(kBwdThreads)
 bwd_count_kernel(const int32_t* __restrict__ topk_idx, int64_t T, int E, int k,
                  int32_t* __restrict__ blk_cnt) {
+  pdl_enter();
   __shared__ int cnt[MM_MAX_EXPERTS];
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -55,6 +56,7 @@ __global__ void __launch_bounds__(kBwdThreads)
 bwd_dispatch_kernel(const Tin* __restrict__ x, const Tin* __restrict__ dy,
                     const int32_t* __restrict__ topk_idx, int64_t T, int H, int E, int k,
                     const int32_t* __restrict__ blk_cnt, BwdDispatchOut o) {
+  pdl_enter();
   __shared__ int s_tot[MM_MAX_EXPERTS], s_base[MM_MAX_EXPERTS], s_off[MM_MAX_EXPERTS + 1];
   __shared__ int s_run[MM_MAX_EXPERTS];
   __shared__ int s_pos[kBwdTok * MM_MAX_TOPK];
@@ -168,6 +170,7 @@ constexpr int kRbTok = 8;
 template <typename Tin>
 __global__ void __launch_bounds__(kBwdThreads)
 router_bwd_kernel(const Tin* __restrict__ Wr, int64_t T, int H, int E, int k, const RouterBwd rb) {
+  pdl_enter();
   __shared__ float s_dr[kRbTok * MM_MAX_EXPERTS];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kRbTok;
@@ -250,6 +253,7 @@ router_bwd_kernel(const Tin* __restrict__ Wr, int64_t T, int H, int E, int k, co
 template <typename Tin>
 __global__ void __launch_bounds__(kBwdThreads)
 router_dwr_kernel(const Tin* __restrict__ x, int64_t T, int H, int E, const RouterBwd rb) {
+  pdl_enter();
   extern __shared__ float s_dr[];              // [64][E]
   const int tid = threadIdx.x;
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kBwdTok;
@@ -297,6 +301,7 @@ constexpr int kRedCols = 64;
 __global__ void __launch_bounds__(256)
 router_bwd_reduce_kernel(const float* __restrict__ dwr_part, const float* __restrict__ dbias_part,
                          int nblk, int E, int H, float* __restrict__ dWr, float* __restrict__ d_bias) {
+  pdl_enter();
   __shared__ float part[4][kRedCols];
   const int64_t n = static_cast<int64_t>(E) * H;
   const int col = threadIdx.x % kRedCols, q = threadIdx.x / kRedCols;
@@ -330,40 +335,40 @@ static int bwd_blocks(int64_t T) { return static_cast<int>((T + kBwdTok - 1) / k
 
 cudaError_t launch_bwd_count(const int32_t* topk_idx, int64_t T, int E, int k, int32_t* blk_cnt,
                              cudaStream_t st) {
-  bwd_count_kernel<<<bwd_blocks(T), kBwdThreads, 0, st>>>(topk_idx, T, E, k, blk_cnt);
-  return cudaGetLastError();
+  return launch_dependent_kernel(bwd_count_kernel, dim3(bwd_blocks(T)), dim3(kBwdThreads), 0, st,
+                                 topk_idx, T, E, k, blk_cnt);
 }
 
 cudaError_t launch_bwd_dispatch(const void* x, const void* dy, const int32_t* topk_idx, int64_t T,
                                 int H, int E, int k, const int32_t* blk_cnt,
                                 const BwdDispatchOut& o, cudaStream_t st) {
   if (H % 8 != 0) return cudaErrorInvalidValue;
-  bwd_dispatch_kernel<__nv_bfloat16><<<bwd_blocks(T), kBwdThreads, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(dy), topk_idx, T, H,
-      E, k, blk_cnt, o);
-  return cudaGetLastError();
+  return launch_dependent_kernel(bwd_dispatch_kernel<__nv_bfloat16>, dim3(bwd_blocks(T)),
+                                 dim3(kBwdThreads), 0, st, static_cast<const __nv_bfloat16*>(x),
+                                 static_cast<const __nv_bfloat16*>(dy), topk_idx, T, H, E, k,
+                                 blk_cnt, o);
 }
 
 cudaError_t launch_router_bwd(const void* x, const void* Wr, int64_t T, int H, int E, int k,
                               const RouterBwd& rb, cudaStream_t st) {
   if (H % 4 != 0) return cudaErrorInvalidValue;
   const int grid = static_cast<int>((T + kRbTok - 1) / kRbTok);
-  router_bwd_kernel<__nv_bfloat16><<<grid, kBwdThreads, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(Wr), T, H, E, k, rb);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_dependent_kernel(router_bwd_kernel<__nv_bfloat16>, dim3(grid),
+                                          dim3(kBwdThreads), 0, st,
+                                          static_cast<const __nv_bfloat16*>(Wr), T, H, E, k, rb);
   if (e != cudaSuccess) return e;
   const size_t smem = static_cast<size_t>(kBwdTok) * E * sizeof(float);
-  router_dwr_kernel<__nv_bfloat16><<<bwd_blocks(T), kBwdThreads, smem, st>>>(
-      static_cast<const __nv_bfloat16*>(x), T, H, E, rb);
-  return cudaGetLastError();
+  return launch_dependent_kernel(router_dwr_kernel<__nv_bfloat16>, dim3(bwd_blocks(T)),
+                                 dim3(kBwdThreads), smem, st,
+                                 static_cast<const __nv_bfloat16*>(x), T, H, E, rb);
 }
 
 cudaError_t launch_router_bwd_reduce(const float* dwr_part, const float* dbias_part, int nblk,
                                      int E, int H, float* dWr, float* d_bias, cudaStream_t st) {
   const int64_t n = static_cast<int64_t>(E) * H + E;
   const int grid = static_cast<int>((n + kRedCols - 1) / kRedCols);
-  router_bwd_reduce_kernel<<<grid, 256, 0, st>>>(dwr_part, dbias_part, nblk, E, H, dWr, d_bias);
-  return cudaGetLastError();
+  return launch_dependent_kernel(router_bwd_reduce_kernel, dim3(grid), dim3(256), 0, st, dwr_part,
+                                 dbias_part, nblk, E, H, dWr, d_bias);
 }
 
 }  // namespace mm

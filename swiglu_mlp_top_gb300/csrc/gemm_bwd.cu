@@ -145,6 +145,11 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
     mbar_init(drained, 1);
     fence_mbar_init();
     s_abort = 0;
+    // a programmatic dependent: the offsets and operands are the previous
+    // kernel's output (every role reads them only after the cluster barrier
+    // below, which follows this wait)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // group rows (rows schedule) or K ranges (K-grouped), from the device
     // offsets, or one dense range [0, dense_rows)
     const int ngrp = SCHED == kSchedRows ? P.G : P.n_groups;
@@ -382,8 +387,8 @@ static cudaError_t bw_launch(const BwParams& p, int64_t tiles_bound, WsHeader* h
   auto fn = bw_gemm_kernel<SCHED>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), kBwSmem);
   if (e != cudaSuccess) return e;
-  fn<<<2 * bw_clusters(tiles_bound), kBwThreads, kBwSmem, st>>>(p, hdr);
-  return cudaGetLastError();
+  return launch_dependent_kernel(fn, dim3(2 * bw_clusters(tiles_bound)), dim3(kBwThreads), kBwSmem,
+                                 st, p, hdr);
 }
 
 cudaError_t launch_bw_dgrad(const void* A, int64_t a_rows, int K, const int32_t* offsets, int G,

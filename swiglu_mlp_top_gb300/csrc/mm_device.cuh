@@ -138,6 +138,14 @@ __device__ __forceinline__ void grid_barrier_reset(WsHeader* hdr, unsigned ticke
   }
 }
 
+// Entry of a programmatic dependent kernel that touches nothing before its
+// predecessor has finished: wait for it (its writes are then visible), and
+// let the next kernel of the stream launch at once (it waits in turn).
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint8_t* align1024(unsigned char* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }

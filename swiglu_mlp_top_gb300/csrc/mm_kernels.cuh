@@ -1,6 +1,8 @@
 // Internal interface between the C-ABI layer (api.cu) and the kernels.
 #pragma once
 
+#include <cstring>
+
 #include "../../include/mm.h"
 #include "mm_device.cuh"
 
@@ -293,6 +295,26 @@ struct UpBwd {
   float* dalpha_part;         // [rows, n_parts] or null
   int n_parts;                // 2 * ceil(I / 128)
 };
+// Launch as a programmatic dependent of the stream's previous kernel (the
+// kernel's set-up and the launch itself overlap that kernel's tail; the
+// kernel waits for it with griddepcontrol.wait before touching its data).
+template <typename Kern, typename... Args>
+inline cudaError_t launch_dependent_kernel(Kern fn, dim3 grid, dim3 block, size_t smem,
+                                           cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, args...);
+}
+
 cudaError_t launch_gateup_bwd_tc(const void* A, int64_t a_rows, int H, int I, const GroupRows& g,
                                  const void* const* Wg, const void* const* Wu, const UpBwd& ub,
                                  WsHeader* hdr, cudaStream_t st);

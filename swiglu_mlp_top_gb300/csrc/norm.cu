@@ -13,13 +13,9 @@
 
 namespace mm {
 
-// Both kernels are programmatic dependents: they wait for the previous
-// kernel (which may still read their output, or write their input), then
-// let the next one launch at once; it waits for them before reading.
-__device__ __forceinline__ void pdl_enter() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
+// Both kernels are programmatic dependents (pdl_enter): they wait for the
+// previous kernel (which may still read their output, or write their input),
+// then let the next one launch at once; it waits for them before reading.
 
 __global__ void norm_fold_router_kernel(const __nv_bfloat16* __restrict__ Wr,
                                         const __nv_bfloat16* __restrict__ w, int E, int H,
