@@ -871,7 +871,7 @@ int mm_moe_backward(const void* x, const void* Wr, const void* const* Wg, const 
     return launch_bwd_count(topk_idx, T, E, k, i32(L.blk_cnt), st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "bwd count");
-  const BwdDispatchOut dout{offsets, i32(L.counts), i32(L.perm), i32(L.pos), xp, dyp};
+  const BwdDispatchOut dout{offsets, i32(L.counts), i32(L.perm), i32(L.pos), xp, dyp, hdr};
   e = counted_launch(MM_KERNEL_BWD_ROUTER, st, [&] {
     return launch_bwd_dispatch(x, dy, topk_idx, T, H, E, k, i32(L.blk_cnt), dout, st);
   });

@@ -55,15 +55,37 @@ template <typename Tin>
 __global__ void __launch_bounds__(kBwdThreads)
 bwd_dispatch_kernel(const Tin* __restrict__ x, const Tin* __restrict__ dy,
                     const int32_t* __restrict__ topk_idx, int64_t T, int H, int E, int k,
-                    const int32_t* __restrict__ blk_cnt, BwdDispatchOut o) {
+                    const int32_t* __restrict__ blk_cnt, BwdDispatchOut o, int stage) {
   pdl_enter();
   __shared__ int s_tot[MM_MAX_EXPERTS], s_base[MM_MAX_EXPERTS], s_off[MM_MAX_EXPERTS + 1];
   __shared__ int s_run[MM_MAX_EXPERTS];
   __shared__ int s_pos[kBwdTok * MM_MAX_TOPK];
+  __shared__ __align__(8) uint64_t rowbar;
+  extern __shared__ __align__(128) unsigned char bwd_rows[];   // stage: x rows, then dy rows
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x, nblk = gridDim.x;
   const int64_t t0 = static_cast<int64_t>(b) * kBwdTok;
-  const int na = static_cast<int>(T - t0 < kBwdTok ? T - t0 : kBwdTok) * k;
+  const int ntok = static_cast<int>(T - t0 < kBwdTok ? T - t0 : kBwdTok);
+  const int na = ntok * k;
+  const uint32_t rowb = static_cast<uint32_t>(H) * sizeof(Tin);
+  Tin* xs = reinterpret_cast<Tin*>(bwd_rows);
+  Tin* ds = xs + static_cast<int64_t>(kBwdTok) * H;
+  if (stage && tid == 0) {
+    // the block's x and dy rows, one bulk copy each, while the ranks are worked out
+    mbar_init(&rowbar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&rowbar, 2u * static_cast<uint32_t>(ntok) * rowb);
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(xs)), "l"(x + t0 * H), "r"(static_cast<uint32_t>(ntok) * rowb),
+        "r"(smem_u32(&rowbar))
+        : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(ds)), "l"(dy + t0 * H), "r"(static_cast<uint32_t>(ntok) * rowb),
+        "r"(smem_u32(&rowbar))
+        : "memory");
+  }
   // totals and this block's base per expert: warp w takes experts w, w + 8,
   // ...; its lanes split the blocks (all loads in flight together) and a
   // warp reduction adds them (integers: any order gives the same sums)
@@ -117,18 +139,32 @@ bwd_dispatch_kernel(const Tin* __restrict__ x, const Tin* __restrict__ dy,
     o.perm[s_pos[a]] = static_cast<int32_t>(t0 * k + a);
     o.pos[t0 * k + a] = s_pos[a];
   }
-  // rows: one flat loop over (assignment, 16-byte vector) items, four in
-  // flight per thread
   constexpr int kVec = 16 / sizeof(Tin);
   const int nv = H / kVec;
-  const int items = na * nv;
+  if (stage) {
+    // rows: two bulk copies per assignment (x, dy), shared -> global
+    const bool landed = __syncthreads_and(mbar_wait(&rowbar, 0, nullptr, o.hdr, 90));
+    if (landed && tid < na) {
+      for (int a = tid; a < na; a += kBwdThreads) {
+        const int64_t d = static_cast<int64_t>(s_pos[a]) * H;
+        bulk_store(static_cast<Tin*>(o.xp) + d, xs + static_cast<int64_t>(a / k) * H, rowb);
+        bulk_store(static_cast<Tin*>(o.dyp) + d, ds + static_cast<int64_t>(a / k) * H, rowb);
+      }
+      bulk_commit();
+      bulk_wait_all();
+    }
+  } else {
+    // rows: one flat loop over (assignment, 16-byte vector) items, four in
+    // flight per thread
+    const int items = na * nv;
 #pragma unroll 4
-  for (int i = tid; i < items; i += kBwdThreads) {
-    const int a = i / nv, v = i - a * nv;
-    const int64_t t = t0 + a / k;
-    const int64_t d = static_cast<int64_t>(s_pos[a]) * nv + v;
-    reinterpret_cast<uint4*>(o.xp)[d] = reinterpret_cast<const uint4*>(x)[t * nv + v];
-    reinterpret_cast<uint4*>(o.dyp)[d] = reinterpret_cast<const uint4*>(dy)[t * nv + v];
+    for (int i = tid; i < items; i += kBwdThreads) {
+      const int a = i / nv, v = i - a * nv;
+      const int64_t t = t0 + a / k;
+      const int64_t d = static_cast<int64_t>(s_pos[a]) * nv + v;
+      reinterpret_cast<uint4*>(o.xp)[d] = reinterpret_cast<const uint4*>(x)[t * nv + v];
+      reinterpret_cast<uint4*>(o.dyp)[d] = reinterpret_cast<const uint4*>(dy)[t * nv + v];
+    }
   }
   if (b == 0) {
     for (int e = tid; e <= E; e += blockDim.x) o.offsets[e] = s_off[e];
@@ -343,10 +379,20 @@ cudaError_t launch_bwd_dispatch(const void* x, const void* dy, const int32_t* to
                                 int H, int E, int k, const int32_t* blk_cnt,
                                 const BwdDispatchOut& o, cudaStream_t st) {
   if (H % 8 != 0) return cudaErrorInvalidValue;
-  return launch_dependent_kernel(bwd_dispatch_kernel<__nv_bfloat16>, dim3(bwd_blocks(T)),
-                                 dim3(kBwdThreads), 0, st, static_cast<const __nv_bfloat16*>(x),
+  // the block's x and dy rows staged in shared memory when they fit (bulk
+  // copies in and out), else 16-byte loads and stores
+  const size_t rows = 2 * static_cast<size_t>(kBwdTok) * H * sizeof(__nv_bfloat16);
+  const int stage = rows <= 200 * 1024 && o.hdr != nullptr ? 1 : 0;
+  const size_t smem = stage ? rows : 0;
+  auto fn = bwd_dispatch_kernel<__nv_bfloat16>;
+  if (stage) {
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_dependent_kernel(fn, dim3(bwd_blocks(T)), dim3(kBwdThreads), smem, st,
+                                 static_cast<const __nv_bfloat16*>(x),
                                  static_cast<const __nv_bfloat16*>(dy), topk_idx, T, H, E, k,
-                                 blk_cnt, o);
+                                 blk_cnt, o, stage);
 }
 
 cudaError_t launch_router_bwd(const void* x, const void* Wr, int64_t T, int H, int E, int k,

@@ -332,6 +332,7 @@ struct BwdDispatchOut {
   int32_t* pos;               // [T*k] assignment -> row
   void* xp;                   // [rows_pad, H] x rows
   void* dyp;                  // [rows_pad, H] dy rows
+  WsHeader* hdr;              // watchdog (the staged copy's bounded wait)
 };
 cudaError_t launch_bwd_dispatch(const void* x, const void* dy, const int32_t* topk_idx, int64_t T,
                                 int H, int E, int k, const int32_t* blk_cnt,
