@@ -160,7 +160,9 @@ __device__ __forceinline__ bool epilogue_up(uint32_t tb, const TileInfo& ti, int
                                             int row, int half, uint8_t* wstage,
                                             const CUtensorMap* hmap) {
   const int lane = row & 31;
-  bool out_of_range = false;
+  // |h| as packed fp16 pairs, max over the lane's values (NaN wins): a half
+  // with an all-ones exponent (inf or NaN) is a value fp16 cannot hold
+  uint32_t hmax = 0u;
   const bool valid = row < ti.rows;
   const bool full_warp = (row | 31) < ti.rows;   // warp-uniform
   const int col0 = ti.n0 + half * 64;
@@ -180,8 +182,7 @@ __device__ __forceinline__ bool epilogue_up(uint32_t tb, const TileInfo& ti, int
       const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
       const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
       pk[j] = pack_f16x2(h0, h1);
-      // false for NaN as well
-      out_of_range |= !(fabsf(h0) < kF16Overflow) | !(fabsf(h1) < kF16Overflow);
+      hmax = hmax2_nan_abs(hmax, pk[j]);
     }
     if (col0 + c * 32 >= I) continue;            // piece past the last column
     if (full_warp) {
@@ -200,6 +201,7 @@ __device__ __forceinline__ bool epilogue_up(uint32_t tb, const TileInfo& ti, int
       for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
     }
   }
+  const bool out_of_range = (hmax & 0x7c00u) == 0x7c00u || (hmax & 0x7c000000u) == 0x7c000000u;
   return out_of_range && valid;
 }
 
