@@ -1152,13 +1152,16 @@ static cudaError_t launch_router_tc(const void* x, const void* Wr, const float* 
 // ---------------------------------------------------------------------------
 // Router and dispatch in one kernel, so that x is read from HBM once per
 // call (bf16; H a multiple of 64 up to 768; E, or 2E with the block norm,
-// up to 16; k up to 4; every block resident at once: T <= 128 x the SMs).
-// Block b routes tokens [128 b, +128): router blocks 2b and 2b+1 of the
-// two-kernel path, whose per-block partials (counts, probability sums,
-// lse^2 sums) it writes unchanged, so that every output is the same bit for
-// bit.  Its x rows stay in shared memory for the whole call: all H / 64
-// k-blocks as 128-byte-swizzled tiles, the A operand of the logits' UMMA
-// (M = 128 tokens, N = 16, fp32 in TMEM) and, after one grid barrier that
+// up to 16; k up to 4; every block resident at once: T <= TB x the SMs).
+// Block b routes tokens [TB b, +TB), TB = 128 or 64 (64 when that still
+// keeps every block resident: twice the SMs for T <= 64 x the SMs): router
+// blocks TB/64 b .. of the two-kernel path, whose per-block partials
+// (counts, probability sums, lse^2 sums) it writes unchanged, so that every
+// output is the same bit for bit.  Its x rows stay in shared memory for the
+// whole call: all H / 64 k-blocks as 128-byte-swizzled tiles, the A operand
+// of the logits' UMMA (M = 128, N = 16, fp32 in TMEM; with TB = 64 the MMA's
+// rows 64-127 read the next tile's rows, whose results in TMEM lanes 64-127
+// no thread uses) and, after one grid barrier that
 // publishes every block's group counts, the source of its rows of Xp.
 // Past the barrier each block derives the group offsets and its bases as
 // the dispatch kernel does, writes perm and its Xp rows (x * inv_rms * w
@@ -1169,20 +1172,28 @@ static cudaError_t launch_router_tc(const void* x, const void* Wr, const float* 
 // issues the TMA loads, warp 5 lane 0 the UMMAs; all 8 warps take the norm's
 // sums of squares and the row copies.
 // ---------------------------------------------------------------------------
-constexpr int kRdTokens = 128;
+constexpr int kRdTokens = 128;                   // tokens per block, at most
 constexpr int kRdThreads = 512;                  // 16 warps: the row copies want many
 constexpr int kRdEP = 16;                        // UMMA N: E (2E with the norm) padded
 constexpr int kRdMaxKb = 12;                     // H <= 768
 constexpr int kRdMaxK = 4;
 constexpr int kRdMaxG = kRdEP * kRdMaxK;
-constexpr uint32_t kRdXTile = kRdTokens * 128;   // 16 KiB: 128 rows x one k-block
 constexpr uint32_t kRdWTile = kRdEP * 128;
 
+// Dynamic shared memory of a block of TB tokens: the x tiles, the router
+// weight tiles, alignment, and for TB < 128 room for the UMMA's rows past
+// the last x tile (it reads 128 rows from each tile's start).
+constexpr size_t rd_smem_bytes(int TB, int KB) {
+  return static_cast<size_t>(KB) * (static_cast<size_t>(TB) * 128 + kRdWTile) +
+         static_cast<size_t>(kRdTokens - TB) * 128 + 1024;
+}
+
 struct RdMaps {
-  CUtensorMap x;                 // x as (64, T, H / 64), box 64 x 128 x nkb (rows >= T read as 0)
+  CUtensorMap x;                 // x as (64, T, H / 64), box 64 x TB x nkb (rows >= T read as 0)
   CUtensorMap wr;                // Wr (or the norm's halves) as (64, En, H / 64), box 64 x 16 x nkb
 };
 
+template <int TB>
 __global__ void __launch_bounds__(kRdThreads, 1)
 route_dispatch_kernel(const __grid_constant__ RdMaps M, int64_t T, int H, int E, int k,
                       const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
@@ -1190,29 +1201,32 @@ route_dispatch_kernel(const __grid_constant__ RdMaps M, int64_t T, int H, int E,
                       float* __restrict__ blk_prob, const DispatchOut D,
                       int32_t* __restrict__ perm, __nv_bfloat16* __restrict__ Xp, int nkb) {
   constexpr int EP = kRdEP;
+  static_assert(TB == 64 || TB == 128, "tokens per block");
+  constexpr int kRB = TB / kRouteTokensPerBlock;         // router blocks per block
+  constexpr uint32_t kRdXTile = TB * 128;                // TB rows x one k-block
   extern __shared__ unsigned char rd_raw[];
   uint8_t* smem = align1024(rd_raw);
   const int KB = H / 64;
   const int nst = KB / nkb;
-  uint8_t* sx = smem;                            // [KB][128 rows][128 B]
+  uint8_t* sx = smem;                            // [KB][TB rows][128 B]
   uint8_t* sw = smem + KB * kRdXTile;            // [KB][16 rows][128 B]
   __shared__ __align__(8) uint64_t full[kRdMaxKb], lbar, drained;
   __shared__ uint32_t s_tmem;
-  __shared__ int s_gcnt[2][kRdMaxG];             // per router block of 64 tokens
+  __shared__ int s_gcnt[kRB][kRdMaxG];           // per router block of 64 tokens
   __shared__ float s_red[4][EP];
   __shared__ float s_redz[4];
   __shared__ float s_bias[EP];
-  __shared__ float s_inv[kRdTokens];
+  __shared__ float s_inv[TB];
   __shared__ int s_wcnt[4][EP];
-  __shared__ int s_pos[kRdTokens * kRdMaxK];
+  __shared__ int s_pos[TB * kRdMaxK];
   __shared__ int s_tot[kRdMaxG], s_base[kRdMaxG], s_off[kRdMaxG + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int kWarps = kRdThreads / 32;
   const int b = blockIdx.x;
-  const int64_t t0 = static_cast<int64_t>(b) * kRdTokens;
-  const int ntok = static_cast<int>(T - t0 < kRdTokens ? T - t0 : kRdTokens);
+  const int64_t t0 = static_cast<int64_t>(b) * TB;
+  const int ntok = static_cast<int>(T - t0 < TB ? T - t0 : TB);
   const int nrb = static_cast<int>((T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock);
-  const int rb0 = 2 * b;                         // this block's first router block
+  const int rb0 = kRB * b;                       // this block's first router block
   const int G = k * E;
   WsHeader* hdr = D.hdr;
   const RouterVariant& rv = D.rv;
@@ -1224,7 +1238,7 @@ route_dispatch_kernel(const __grid_constant__ RdMaps M, int64_t T, int H, int E,
     mbar_init(&drained, 1);
     fence_mbar_init();
   }
-  for (int g = tid; g < 2 * kRdMaxG; g += kRdThreads) (&s_gcnt[0][0])[g] = 0;
+  for (int g = tid; g < kRB * kRdMaxG; g += kRdThreads) (&s_gcnt[0][0])[g] = 0;
   if (warp == 4) {
     tmem_alloc(&s_tmem, 32);
     tmem_relinquish();
@@ -1249,7 +1263,7 @@ route_dispatch_kernel(const __grid_constant__ RdMaps M, int64_t T, int H, int E,
   }
   if (tid == 5 * 32) {
     // MMA issuer: L[t, e] = sum over the k-blocks of x_t . Wr_e
-    const uint32_t idesc = idesc_bf16_f32(kRdTokens, EP);
+    const uint32_t idesc = idesc_bf16_f32(128, EP);
     bool mok = true;
     for (int q = 0; q < nst && mok; ++q) {
       if (!mbar_wait(&full[q], 0, nullptr, hdr, 66)) {
@@ -1368,7 +1382,8 @@ route_dispatch_kernel(const __grid_constant__ RdMaps M, int64_t T, int H, int E,
   }
   // rank of each assignment among the block's tokens that chose the same
   // expert in the same slot, in token order, and from the same matches the
-  // router blocks' group counts (warps 0-1: router block 2b, warps 2-3: 2b + 1)
+  // router blocks' group counts (warps 0-1: router block rb0, warps 2-3:
+  // rb0 + 1 when TB = 128)
 #pragma unroll
   for (int sl = 0; sl < kRdMaxK; ++sl) {
     if (sl >= k) break;
@@ -1387,7 +1402,7 @@ route_dispatch_kernel(const __grid_constant__ RdMaps M, int64_t T, int H, int E,
       for (int w = 0; w < warp; ++w) rank += s_wcnt[w][e];
       rk[sl] = rank;
     }
-    if (tid < 2 * E) {
+    if (tid < kRB * E) {
       const int i = tid / E, ee = tid - i * E;
       s_gcnt[i][sl * E + ee] = s_wcnt[2 * i][ee] + s_wcnt[2 * i + 1][ee];
     }
@@ -1397,7 +1412,7 @@ route_dispatch_kernel(const __grid_constant__ RdMaps M, int64_t T, int H, int E,
   // the router blocks' partials, as the tensor-core router writes them (warp
   // 0; the grid barrier's __syncthreads and release by thread 0 publish them)
   if (ok && warp == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kRB; ++i) {
       const int rb = rb0 + i;
       if (rb >= nrb) break;
       if (lane < E) blk_prob[static_cast<int64_t>(rb) * E + lane] = s_red[2 * i][lane] + s_red[2 * i + 1][lane];
@@ -1544,6 +1559,37 @@ route_dispatch_kernel(const __grid_constant__ RdMaps M, int64_t T, int H, int E,
   if (tid == 0) grid_barrier_reset(hdr, ticket);
 }
 
+// Blocks of TB tokens that can be resident at once (one per SM), per H.
+template <int TB>
+static int64_t rd_max_blocks(int H) {
+  static int64_t max_blocks[kRdMaxKb + 1];
+  static bool known[kRdMaxKb + 1];
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  const int KB = H / 64;
+  if (!known[KB]) {
+    const size_t smem = rd_smem_bytes(TB, KB);
+    auto fn = route_dispatch_kernel<TB>;
+    int per_sm = 0;
+    if (ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kRdThreads, smem) != cudaSuccess) {
+      (void)cudaGetLastError();
+      per_sm = 0;
+    }
+    max_blocks[KB] = static_cast<int64_t>(per_sm) * num_sms();
+    known[KB] = true;
+  }
+  return max_blocks[KB];
+}
+
+// Tokens per block of the fused router + dispatch for this call: 64 while
+// every block of 64 still fits on the GPU at once, else 128; 0 if neither.
+static int rd_tokens_per_block(int64_t T, int H) {
+  if ((T + 63) / 64 <= rd_max_blocks<64>(H)) return 64;
+  if ((T + 127) / 128 <= rd_max_blocks<128>(H)) return 128;
+  return 0;
+}
+
 // Whether the fused router + dispatch takes this call: bf16, the shapes it
 // is built for, 16-byte aligned x and router weights, and every block
 // resident at once (one per SM).
@@ -1556,23 +1602,7 @@ bool route_dispatch_ok(int dtype, const void* x, const void* Wr, int64_t T, int 
       T < 1 || (reinterpret_cast<uintptr_t>(x) & 15u) != 0 ||
       (reinterpret_cast<uintptr_t>(wr) & 15u) != 0 || D.hdr == nullptr)
     return false;
-  const size_t smem = static_cast<size_t>(H / 64) * (kRdXTile + kRdWTile) + 1024;
-  auto fn = route_dispatch_kernel;
-  static int max_blocks[kRdMaxKb + 1];
-  static bool known[kRdMaxKb + 1];
-  static std::mutex mu;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!known[H / 64]) {
-    int per_sm = 0;
-    if (ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kRdThreads, smem) != cudaSuccess) {
-      (void)cudaGetLastError();
-      per_sm = 0;
-    }
-    max_blocks[H / 64] = per_sm * num_sms();
-    known[H / 64] = true;
-  }
-  return (T + kRdTokens - 1) / kRdTokens <= max_blocks[H / 64];
+  return rd_tokens_per_block(T, H) > 0;
 }
 
 // Launch of the fused router + dispatch; route_dispatch_ok() must hold.
@@ -1585,15 +1615,17 @@ cudaError_t launch_route_dispatch(int dtype, const void* x, const void* Wr, cons
   const int En = norm ? 2 * E : E;
   const void* wr = norm ? D.norm.wr_hl : Wr;
   const int KB = H / 64;
+  const int TB = rd_tokens_per_block(T, H);
+  if (TB == 0) return cudaErrorInvalidValue;
   int nkb = 4;
   while (KB % nkb != 0) --nkb;
-  const size_t smem = static_cast<size_t>(KB) * (kRdXTile + kRdWTile) + 1024;
-  auto fn = route_dispatch_kernel;
-  const int64_t nblk = (T + kRdTokens - 1) / kRdTokens;
+  const size_t smem = rd_smem_bytes(TB, KB);
+  auto fn = TB == 64 ? route_dispatch_kernel<64> : route_dispatch_kernel<128>;
+  const int64_t nblk = (T + TB - 1) / TB;
   RdMaps m;
   const uint64_t sx[2] = {static_cast<uint64_t>(H) * 2, 128};
   const uint64_t dx[3] = {64, static_cast<uint64_t>(T), static_cast<uint64_t>(KB)};
-  const uint32_t bx[3] = {64, static_cast<uint32_t>(kRdTokens), static_cast<uint32_t>(nkb)};
+  const uint32_t bx[3] = {64, static_cast<uint32_t>(TB), static_cast<uint32_t>(nkb)};
   if (!make_map_3d(&m.x, x, dx, sx, bx)) return cudaErrorInvalidValue;
   const uint64_t dw[3] = {64, static_cast<uint64_t>(En), static_cast<uint64_t>(KB)};
   const uint32_t bw[3] = {64, static_cast<uint32_t>(kRdEP), static_cast<uint32_t>(nkb)};
