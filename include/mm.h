@@ -56,10 +56,11 @@ typedef enum {
   MM_ERR_WORKSPACE = 3,     /* workspace null or smaller than required        */
   MM_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed              */
   MM_ERR_TIMEOUT = 5,       /* a device pipeline wait hit its time limit      */
-  MM_ERR_RANGE = 6          /* bf16 tensor-core prefill path: a value of h, or
-                               of Wd, is beyond the fp16 range (|v| >= 65520)
-                               of its intermediate copy; y may hold inf/NaN.
-                               Recorded on the device, reported by
+  MM_ERR_RANGE = 6          /* bf16 tensor-core paths: a value of h, or of Wd
+                               (forward), or of dh = dy Wd (backward), is
+                               beyond the fp16 range (|v| >= 65520) of its
+                               intermediate copy; the results may hold
+                               inf/NaN.  Recorded on the device, reported by
                                mm_check_status()                              */
 } mm_status;
 
@@ -320,6 +321,9 @@ int mm_moe_route_opts(const void* x, const void* Wr, int64_t T, int H, int E, in
  *
  * bf16 only, on the tensor cores; H and I multiples of 64.  Inputs and
  * outputs are device memory; every gradient is OVERWRITTEN (not added to).
+ * The intermediate dh = dy Wd is kept in the workspace in fp16 (11
+ * significant bits); a value beyond the fp16 range is reported by
+ * mm_check_status() as MM_ERR_RANGE.
  *
  * Dense FFN: for dy = dL/dy [T, H] (bf16),
  *   dx [T, H] (bf16) and dWg, dWu [I, H], dWd [H, I] (fp32) with

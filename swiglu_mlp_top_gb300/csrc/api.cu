@@ -88,7 +88,7 @@ DenseBwdLayout dense_bwd_layout(int64_t T, int I) {
   DenseBwdLayout L;
   const size_t ti = static_cast<size_t>(T) * I;
   size_t off = sizeof(WsHeader);
-  L.dh = off;  off += align_up(4 * ti);
+  L.dh = off;  off += align_up(2 * ti);
   L.dgu = off; off += align_up(4 * ti);
   L.h = off;   off += align_up(2 * ti);
   L.total = off;
@@ -118,7 +118,7 @@ MoeBwdLayout moe_bwd_layout(int64_t T, int H, int I, int E, int k) {
   L.perm = off;       off += align_up(4 * R);
   L.xp = off;         off += align_up(2 * R * H);
   L.dyp = off;        off += align_up(2 * R * H);
-  L.dhu = off;        off += align_up(4 * R * I);
+  L.dhu = off;        off += align_up(2 * R * I);
   L.dgu = off;        off += align_up(4 * R * I);
   L.ha = off;         off += align_up(2 * R * I);
   L.dpart = off;      off += align_up(4 * R * L.n_parts);
@@ -785,13 +785,13 @@ int mm_swiglu_ffn_backward(const void* x, const void* Wg, const void* Wu, const 
   // dh = dy Wd
   const void* wd1[1] = {Wd};
   cudaError_t e = counted_launch(MM_KERNEL_BWD_DGRAD, st, [&] {
-    return launch_bw_dgrad(dy, T, H, nullptr, 1, Ti, wd1, wd1, H / 64, I, dh, I, 0, hdr, st);
+    return launch_bw_dgrad(dy, T, H, nullptr, 1, Ti, wd1, wd1, H / 64, I, dh, I, kBwOutF16, hdr, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "bwd dh");
   // g, u again; dG, dU, h
   const void* wg1[1] = {Wg};
   const void* wu1[1] = {Wu};
-  UpBwd ub{static_cast<const float*>(dh), nullptr, nullptr,
+  UpBwd ub{static_cast<const __half*>(dh), nullptr, nullptr,
            static_cast<__nv_bfloat16*>(dgu), static_cast<__nv_bfloat16*>(h), nullptr, 0};
   GroupRows gr{nullptr, 1, Ti, 1};
   e = counted_launch(MM_KERNEL_BWD_SWIGLU, st, [&] {
@@ -800,7 +800,7 @@ int mm_swiglu_ffn_backward(const void* x, const void* Wg, const void* Wu, const 
   if (e != cudaSuccess) return cuda_fail(e, "bwd swiglu");
   // dx = dG Wg + dU Wu
   e = counted_launch(MM_KERNEL_BWD_DGRAD, st, [&] {
-    return launch_bw_dgrad(dgu, T, 2 * I, nullptr, 1, Ti, wg1, wu1, I / 64, H, dx, H, 1, hdr, st);
+    return launch_bw_dgrad(dgu, T, 2 * I, nullptr, 1, Ti, wg1, wu1, I / 64, H, dx, H, kBwOutBF16, hdr, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "bwd dx");
   // dWd = dy^T h, dWg = dG^T x, dWu = dU^T x
@@ -878,11 +878,11 @@ int mm_moe_backward(const void* x, const void* Wr, const void* const* Wg, const 
   if (e != cudaSuccess) return cuda_fail(e, "bwd dispatch");
   // 2. dhu = dy Wd_e (unscaled by alpha), per expert group
   e = counted_launch(MM_KERNEL_BWD_DGRAD, st, [&] {
-    return launch_bw_dgrad(dyp, R, H, offsets, E, 0, Wd, Wd, H / 64, I, dhu, I, 0, hdr, st);
+    return launch_bw_dgrad(dyp, R, H, offsets, E, 0, Wd, Wd, H / 64, I, dhu, I, kBwOutF16, hdr, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "bwd dhu");
   // 3. g, u again: dG, dU, alpha h, dalpha partials
-  const UpBwd ub{static_cast<const float*>(dhu), i32(L.perm), topk_w,
+  const UpBwd ub{static_cast<const __half*>(dhu), i32(L.perm), topk_w,
                  static_cast<__nv_bfloat16*>(dgu), static_cast<__nv_bfloat16*>(ha), f32(L.dpart),
                  L.n_parts};
   const GroupRows gr{offsets, E, 0, E};
@@ -892,7 +892,7 @@ int mm_moe_backward(const void* x, const void* Wr, const void* const* Wg, const 
   if (e != cudaSuccess) return cuda_fail(e, "bwd swiglu");
   // 4. per-assignment dx rows (fp32) = dG Wg_e + dU Wu_e
   e = counted_launch(MM_KERNEL_BWD_DGRAD, st, [&] {
-    return launch_bw_dgrad(dgu, R, 2 * I, offsets, E, 0, Wg, Wu, I / 64, H, f32(L.dxp), H, 0, hdr,
+    return launch_bw_dgrad(dgu, R, 2 * I, offsets, E, 0, Wg, Wu, I / 64, H, f32(L.dxp), H, kBwOutF32, hdr,
                            st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "bwd dxp");

@@ -265,17 +265,18 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
     const uint32_t te0 = mapa_shared(smem_u32(&tempty[0]), 0);
     const uint32_t te1 = mapa_shared(smem_u32(&tempty[1]), 0);
     int used = 0;
+    uint32_t hmax = 0u;     // fp16 output: max |value| of the lane's rows, as packed halves
     for (int tile = cluster; tile < total; tile += n_clusters) {
       const BwTile ti = bw_decode<SCHED>(tile, P, s_off, s_tstart, n_tiles_n, static_cast<int>(rank));
       // output row / columns / leading dimension of this tile
       float* out32 = nullptr;
-      __nv_bfloat16* out16 = nullptr;
+      uint16_t* out16 = nullptr;                 // bf16 or fp16 (P.out_type)
       int64_t ldo;
       int ncols;
       if constexpr (SCHED == kSchedRows) {
         ldo = P.ldo;
         ncols = P.N;
-        if (P.out_bf16) out16 = static_cast<__nv_bfloat16*>(P.out); else out32 = static_cast<float*>(P.out);
+        if (P.out_type != kBwOutF32) out16 = static_cast<uint16_t*>(P.out); else out32 = static_cast<float*>(P.out);
       } else {
         ldo = P.prob[ti.p].N;
         ncols = P.prob[ti.p].N;
@@ -307,9 +308,24 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
         tmem_ld_32x32b_x32(tb + c * 32, r);     // every lane (warp-collective)
         tmem_ld_wait();
         if (col >= ncols) continue;              // warp-uniform
+        // 16-bit output: the row's 32 values as 16 packed pairs
+        uint32_t pk[16];
+        if (out16 != nullptr) {
+          if (P.out_type == kBwOutF16) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              pk[j] = pack_f16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+              if (valid) hmax = hmax2_nan_abs(hmax, pk[j]);   // rows past the group do not count
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+          }
+        }
         if (tma_piece) {
           // through the swizzled staging piece: fp32 in 128-byte rows (chunk q
-          // of row r at q ^ (r & 7)), bf16 in 64-byte rows (q ^ ((r >> 1) & 3))
+          // of row r at q ^ (r & 7)), 16-bit in 64-byte rows (q ^ ((r >> 1) & 3))
           if (lane == 0) bulk_wait_read();       // the previous piece's store has read it
           __syncwarp();
           if (out16 != nullptr) {
@@ -317,10 +333,7 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
               *reinterpret_cast<uint4*>(r64 + ((q ^ ((lane >> 1) & 3)) << 4)) =
-                  make_uint4(pack_bf16x2(__uint_as_float(r[8 * q]), __uint_as_float(r[8 * q + 1])),
-                             pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
-                             pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
-                             pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
+                  make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
           } else {
             uint8_t* r128 = wstage + lane * 128;
 #pragma unroll
@@ -339,11 +352,7 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
         } else if (out16 != nullptr) {
           uint4* d4 = reinterpret_cast<uint4*>(out16 + orow * ldo + col);
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            d4[q] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * q]), __uint_as_float(r[8 * q + 1])),
-                               pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
-                               pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
-                               pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
+          for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         } else {
           float4* d4 = reinterpret_cast<float4*>(out32 + orow * ldo + col);
 #pragma unroll
@@ -356,6 +365,8 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acc ? te1 : te0);
     }
+    if constexpr (SCHED == kSchedRows)
+      if (P.out_type == kBwOutF16) report_range(hdr, f16x2_out_of_range(hmax), 101);
     bulk_wait_all();   // this warp's tensor stores have landed
   }
 
@@ -393,7 +404,7 @@ static cudaError_t bw_launch(const BwParams& p, int64_t tiles_bound, WsHeader* h
 
 cudaError_t launch_bw_dgrad(const void* A, int64_t a_rows, int K, const int32_t* offsets, int G,
                             int dense_rows, const void* const* b_lo, const void* const* b_hi,
-                            int kb_split, int N, void* out, int64_t ldo, int out_bf16,
+                            int kb_split, int N, void* out, int64_t ldo, int out_type,
                             WsHeader* hdr, cudaStream_t st) {
   if (G < 1 || G > kBwMaxGroups || K % 64 != 0 || N % 64 != 0) return cudaErrorInvalidValue;
   BwParams p;
@@ -416,14 +427,20 @@ cudaError_t launch_bw_dgrad(const void* A, int64_t a_rows, int K, const int32_t*
   p.kb_split = khi > 0 ? kb_split : K / 64;
   p.out = out;
   p.ldo = ldo;
-  p.out_bf16 = out_bf16;
+  p.out_type = out_type;
   // full 32-row pieces as TMA stores, where the output's address and pitch allow
-  const int esz = out_bf16 ? 2 : 4;
-  p.out_tma = (reinterpret_cast<uintptr_t>(out) % 16 == 0 && (ldo * esz) % 16 == 0 &&
-               make_map_2d(&p.o, out, !out_bf16, static_cast<uint64_t>(N),
-                           static_cast<uint64_t>(a_rows), static_cast<uint64_t>(ldo) * esz, 32, 32,
-                           out_bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
-                  ? 1 : 0;
+  const int esz = out_type == kBwOutF32 ? 4 : 2;
+  const bool aligned = reinterpret_cast<uintptr_t>(out) % 16 == 0 && (ldo * esz) % 16 == 0;
+  if (out_type == kBwOutF16)
+    p.out_tma = (aligned && ldo == N &&
+                 make_map_16(&p.o, out, static_cast<uint64_t>(N), static_cast<uint64_t>(a_rows), 32,
+                             true, 32, CU_TENSOR_MAP_SWIZZLE_64B)) ? 1 : 0;
+  else
+    p.out_tma = (aligned &&
+                 make_map_2d(&p.o, out, out_type == kBwOutF32, static_cast<uint64_t>(N),
+                             static_cast<uint64_t>(a_rows), static_cast<uint64_t>(ldo) * esz, 32, 32,
+                             out_type == kBwOutF32 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                                   : CU_TENSOR_MAP_SWIZZLE_64B)) ? 1 : 0;
   const int64_t ntn = (N + 255) / 256;
   const int64_t tiles = offsets ? ((a_rows + 255) / 256 + G) * ntn : ((dense_rows + 255) / 256) * ntn;
   return bw_launch<kSchedRows>(p, tiles, hdr, st);

@@ -245,11 +245,17 @@ __device__ __forceinline__ void epilogue_up_bwd(uint32_t tb, const TileInfo& ti,
 #pragma unroll
     for (int q = 0; q < 32; ++q) dv[q] = 0.f;
     if (valid) {
-      const float4* dsrc = reinterpret_cast<const float4*>(ub.dhu + r * I + col);
+      const uint4* dsrc = reinterpret_cast<const uint4*>(ub.dhu + r * I + col);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 v = dsrc[q];
-        dv[4 * q] = v.x; dv[4 * q + 1] = v.y; dv[4 * q + 2] = v.z; dv[4 * q + 3] = v.w;
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = dsrc[q];
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[j]));
+          dv[8 * q + 2 * j] = f.x;
+          dv[8 * q + 2 * j + 1] = f.y;
+        }
       }
     }
     uint32_t pg[16], pu[16], ph[16];
@@ -554,13 +560,6 @@ __device__ __forceinline__ bool cv_rest(const WdConvert& cv, int64_t v, int64_t 
   return out_of_range;
 }
 
-// Records MM_ERR_RANGE in the workspace header (first failure wins) when any
-// lane of the warp saw a value that fp16 cannot hold.
-__device__ __forceinline__ void report_range(WsHeader* hdr, bool bad) {
-  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0 && hdr != nullptr) {
-    if (atomicCAS(&hdr->status, 0u, kStatusRange) == 0u) hdr->where = 100;
-  }
-}
 
 // =============================================================== kernel
 // K = contraction length (H for gate/up, I for down); NCOLS = output width
@@ -839,12 +838,10 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
         cv_load(cv, ca, cb, threadIdx.x, craw);
       }
       if constexpr (OP == kOpUpBwd) {
-        // this row's 64 dh columns: pulled into L2 while the MMAs run
+        // this row's 64 dh columns (fp16): pulled into L2 while the MMAs run
         if (row < ti.rows && ti.n0 + half * 64 < NCOLS) {
-          const float* a = ub.dhu + (ti.row0 + row) * NCOLS + ti.n0 + half * 64;
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(a) : "memory");
-          if (ti.n0 + half * 64 + 32 < NCOLS)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(a + 32) : "memory");
+          const __half* a = ub.dhu + (ti.row0 + row) * NCOLS + ti.n0 + half * 64;
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(a) : "memory");   // 128 bytes: 64 columns
         }
       }
       if (!warp_wait(&tfull[acc], aph, abort, hdr, 6)) break;
@@ -867,7 +864,7 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
         range_bad |= cv_rest(cv, ca + kCvBatch, cb, threadIdx.x);
       }
     }
-    if constexpr (OP == kOpUp) report_range(hdr, range_bad);
+    if constexpr (OP == kOpUp) report_range(hdr, range_bad, 100);
     bulk_wait_all();   // this warp's tensor stores have landed
   }
 

@@ -525,6 +525,18 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+// Whether a max from hmax2_nan_abs holds a half with an all-ones exponent
+// (infinity or NaN): a value that fp16 could not hold.
+__device__ __forceinline__ bool f16x2_out_of_range(uint32_t hmax) {
+  return (hmax & 0x7c00u) == 0x7c00u || (hmax & 0x7c000000u) == 0x7c000000u;
+}
+// Records MM_ERR_RANGE in the workspace header (first failure wins) when any
+// lane of the warp saw a value that fp16 cannot hold; `where` names the site.
+__device__ __forceinline__ void report_range(WsHeader* hdr, bool bad, unsigned where) {
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0 && hdr != nullptr) {
+    if (atomicCAS(&hdr->status, 0u, kStatusRange) == 0u) hdr->where = where;
+  }
+}
 
 // y[0..7] += v (8 bf16 as four bf16x2), one 16-byte vector reduction.
 __device__ __forceinline__ void red_add_bf16x8(void* gptr, uint32_t a, uint32_t b, uint32_t c,

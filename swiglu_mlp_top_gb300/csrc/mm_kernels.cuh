@@ -267,14 +267,18 @@ struct BwParams {
   int K, N, kb_split;                   // rows schedule
   void* out;                            // rows schedule: [rows, ldo]
   int64_t ldo;
-  int out_bf16;
+  int out_type;                         // rows schedule: kBwOutF32 / kBwOutBF16 / kBwOutF16
   int out_tma;                          // rows schedule: full 32-row pieces go out through o
   CUtensorMap o;                        // rows schedule: out as 32 x 32 store boxes
 };
 
+// Output element type of a rows-schedule GEMM.  fp16 output (dh, read only
+// by the SwiGLU-backward epilogue) is checked against the fp16 range: a value
+// that rounds to infinity (or a NaN) records MM_ERR_RANGE in the header.
+constexpr int kBwOutF32 = 0, kBwOutBF16 = 1, kBwOutF16 = 2;
 cudaError_t launch_bw_dgrad(const void* A, int64_t a_rows, int K, const int32_t* offsets, int G,
                             int dense_rows, const void* const* b_lo, const void* const* b_hi,
-                            int kb_split, int N, void* out, int64_t ldo, int out_bf16,
+                            int kb_split, int N, void* out, int64_t ldo, int out_type,
                             WsHeader* hdr, cudaStream_t st);
 cudaError_t launch_bw_wgrad(const void* const* a_mats, const int64_t* a_cols, int n_a,
                             const void* const* b_mats, const int64_t* b_cols, int n_b,
@@ -287,7 +291,7 @@ cudaError_t launch_bw_wgrad(const void* const* a_mats, const int64_t* a_cols, in
 //   h = SiLU(g) u;  dalpha partial = sum over the tile's columns of h * dhu;
 //   dh = alpha dhu;  dU = dh SiLU(g);  dG = dh u SiLU'(g);  out: dG | dU, alpha h.
 struct UpBwd {
-  const float* dhu;           // [rows, I] fp32 (not an MMA operand: kept unrounded)
+  const __half* dhu;          // [rows, I] fp16 (not an MMA operand: 11 significant bits)
   const int32_t* perm;        // row -> assignment t*k + s, -1 for padding; null: alpha = 1
   const float* topk_w;        // [T*k] alpha
   __nv_bfloat16* dgu;         // [rows, 2I]: dG in columns [0, I), dU in [I, 2I)

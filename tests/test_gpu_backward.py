@@ -4,9 +4,10 @@ through alpha, aux and z-loss; per-expert weight gradients; dx).
 
 Bar (no tolerance is stated for gradients; this one is derived from the
 arithmetic): every element within 2e-2 * (rms(g*) + |g*|).  Each gradient
-element is a sum of products whose operands passed through at most two
-bf16 roundings (dh, then dG / dU or alpha h: ~2^-8 relative), so its error
-is bounded by that times the sum of |terms|.  For a gradient over one or a
+element is a sum of products whose operands passed through at most one
+fp16 rounding (dh, 2^-11 relative) and one bf16 rounding (dG / dU or
+alpha h: ~2^-8 relative), so its error is bounded by that times the sum
+of |terms|.  For a gradient over one or a
 few tokens (an outer product such as dG^T x for one token) that sum is
 |g*| itself, and the heavy tail of dG = dh u SiLU'(g) puts max|g*| at over
 10 rms: an RMS-only measure would flag elements that are within 2^-8
@@ -66,6 +67,23 @@ def test_dense_backward(T, H, I):
     ref = oracle.swiglu_ffn_backward(*[to_f64(inp[n]) for n in ("x", "Wg", "Wu", "Wd")], to_f64(dy))
     for name, got, want in zip(("dx", "dWg", "dWu", "dWd"), (dx, dWg, dWu, dWd), ref):
         assert_grad(name, got.double().cpu().numpy(), want, rms_bar=T >= 1000)
+
+
+@pytest.mark.parametrize("scale,expect", [(1.0, 0), (1e6, 6)])
+def test_fp16_dh_overflow_is_reported(scale, expect):
+    """The backward keeps dh = dy Wd in fp16.  With dy scaled by 1e6 (Wd
+    N(0, 0.02), H = 256: |dh| ~ 3e5) dh is beyond fp16's 65504, and the call
+    must report MM_ERR_RANGE through mm_check_status; unscaled, nothing.
+    The status clears once read."""
+    T, H, I = 64, 256, 384
+    inp = make_inputs(T, H, I, "bf16", seed=41)
+    dy = (_dy(T, H, 42).float() * scale).to(torch.bfloat16)
+    g = to_dev(inp)
+    lib = mm._lib.load()
+    ws = mm.new_workspace(lib.mm_swiglu_ffn_backward_workspace_bytes(T, H, I, 1))
+    mm.swiglu_ffn_backward(g["x"], g["Wg"], g["Wu"], g["Wd"], dy.cuda(), workspace=ws)
+    assert mm.check_status(ws) == expect
+    assert mm.check_status(ws) == 0
 
 
 def _moe_step(inp, k, coef, z_coef, noise, dy, path="tensor"):

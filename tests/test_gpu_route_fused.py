@@ -9,7 +9,10 @@ parity tests; one case here checks the fused path against the oracle too.
 Shapes cover several fused blocks and a ragged last one (T = 129: a block of
 one token; T = 65: one block spanning one and a bit router blocks), top-1 to
 top-4, E = 16 (the widest it takes), H = 192 / 256 / 512 / 768 (3, 4, 8 and
-12 k-blocks) and the full top-2 workload.
+12 k-blocks) and the full top-2 workload.  The kernel takes blocks of 64
+tokens while one per SM covers T and 128 beyond: T = 64 x SMs (the largest
+grid of 64-token blocks, every SM holding one) and one token more (the first
+call on 128-token blocks, with a block of one token) are both checked.
 """
 import numpy as np
 import pytest
@@ -59,6 +62,15 @@ def test_fused_routing_equals_two_kernels(T, H, I, E, k, bias):
     inp = moe_inputs(T, H, I, E, "bf16", seed=300 + T, bias=bias)
     g = to_dev(inp)
     _assert_same(_both(g, k, 0.01))
+
+
+@pytest.mark.parametrize("extra", [0, 1])
+def test_fused_routing_at_the_block_size_switch(extra):
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T = 64 * n_sms + extra
+    inp = moe_inputs(T, 768, 256, 8, "bf16", seed=330 + extra, bias=SKEW)
+    g = to_dev(inp)
+    _assert_same(_both(g, 2, 0.01))
 
 
 def test_fused_routing_full_size_top2():
