@@ -122,7 +122,7 @@ MoeBwdLayout moe_bwd_layout(int64_t T, int H, int I, int E, int k) {
   L.dgu = off;        off += align_up(4 * R * I);
   L.ha = off;         off += align_up(2 * R * I);
   L.dpart = off;      off += align_up(4 * R * L.n_parts);
-  L.dxp = off;        off += align_up(4 * R * H);
+  L.dxp = off;        off += align_up(2 * R * H);
   L.dr = off;         off += align_up(4 * static_cast<size_t>(T) * E);
   L.dwr_part = off;   off += align_up(4 * nblk * E * H);
   L.dbias_part = off; off += align_up(4 * nblk * E);
@@ -890,10 +890,10 @@ int mm_moe_backward(const void* x, const void* Wr, const void* const* Wg, const 
     return launch_gateup_bwd_tc(xp, R, H, I, gr, Wg, Wu, ub, hdr, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "bwd swiglu");
-  // 4. per-assignment dx rows (fp32) = dG Wg_e + dU Wu_e
+  // 4. per-assignment dx rows (fp16, range-checked) = dG Wg_e + dU Wu_e
   e = counted_launch(MM_KERNEL_BWD_DGRAD, st, [&] {
-    return launch_bw_dgrad(dgu, R, 2 * I, offsets, E, 0, Wg, Wu, I / 64, H, f32(L.dxp), H, kBwOutF32, hdr,
-                           st);
+    return launch_bw_dgrad(dgu, R, 2 * I, offsets, E, 0, Wg, Wu, I / 64, H, ws_at(workspace, L.dxp), H,
+                           kBwOutF16, hdr, st);
   });
   if (e != cudaSuccess) return cuda_fail(e, "bwd dxp");
   // 5. weight gradients over each expert's rows
@@ -913,7 +913,8 @@ int mm_moe_backward(const void* x, const void* Wr, const void* const* Wg, const 
   if (e != cudaSuccess) return cuda_fail(e, "bwd wgrad");
   // 6. router: dr, dx (slot-ordered sum + dr Wr), dWr / d_bias partials, then their sums
   const RouterBwd rb{topk_idx, topk_w, router_probs, (z_coef != 0.f && d_z != 0.f) ? router_lse : nullptr,
-                     i32(L.counts), i32(L.pos), f32(L.dpart), L.n_parts, f32(L.dxp), coef, d_aux,
+                     i32(L.counts), i32(L.pos), f32(L.dpart), L.n_parts,
+                     reinterpret_cast<const __half*>(ws_at(workspace, L.dxp)), coef, d_aux,
                      z_coef, d_z, f32(L.dr), dx, f32(L.dwr_part), f32(L.dbias_part)};
   e = counted_launch(MM_KERNEL_BWD_ROUTER, st, [&] {
     return launch_router_bwd(x, Wr, T, H, E, k, rb, st);

@@ -350,7 +350,7 @@ struct RouterBwd {
   const int32_t* pos;         // [T*k]
   const float* dalpha_part;   // [rows_pad, n_parts]
   int n_parts;
-  const float* dxp;           // [rows_pad, H] fp32 per-assignment dx
+  const __half* dxp;          // [rows_pad, H] fp16 per-assignment dx (range-checked when written)
   float coef, d_aux, z_coef, d_z;
   float* dr;                  // [T, E] out: dL/dlogits
   void* dx;                   // [T, H] out, x's dtype
