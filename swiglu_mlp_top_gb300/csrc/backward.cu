@@ -267,8 +267,7 @@ router_bwd_kernel(const Tin* __restrict__ Wr, int64_t T, int H, int E, int k, co
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 0; s < k; ++s) {
       const uint2 v = *reinterpret_cast<const uint2*>(rb.dxp + static_cast<int64_t>(rb.pos[t * k + s]) * H + h);
-      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
-      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+      const float2 a = f16x2_to_f32x2(v.x), b = f16x2_to_f32x2(v.y);
       acc.x += a.x; acc.y += a.y; acc.z += b.x; acc.w += b.y;
     }
     for (int e = 0; e < E; ++e) {

@@ -249,13 +249,10 @@ __device__ __forceinline__ void epilogue_up_bwd(uint32_t tb, const TileInfo& ti,
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint4 v = dsrc[q];
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[j]));
-          dv[8 * q + 2 * j] = f.x;
-          dv[8 * q + 2 * j + 1] = f.y;
-        }
+        const float2 f0 = f16x2_to_f32x2(v.x), f1 = f16x2_to_f32x2(v.y);
+        const float2 f2 = f16x2_to_f32x2(v.z), f3 = f16x2_to_f32x2(v.w);
+        dv[8 * q] = f0.x; dv[8 * q + 1] = f0.y; dv[8 * q + 2] = f1.x; dv[8 * q + 3] = f1.y;
+        dv[8 * q + 4] = f2.x; dv[8 * q + 5] = f2.y; dv[8 * q + 6] = f3.x; dv[8 * q + 7] = f3.y;
       }
     }
     uint32_t pg[16], pu[16], ph[16];

@@ -525,6 +525,15 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+// Two fp16 values (one 32-bit word, element 0 in the low half) widened to fp32.
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t w) {
+  float2 f;
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "cvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+      : "=f"(f.x), "=f"(f.y)
+      : "r"(w));
+  return f;
+}
 // Whether a max from hmax2_nan_abs holds a half with an all-ones exponent
 // (infinity or NaN): a value that fp16 could not hold.
 __device__ __forceinline__ bool f16x2_out_of_range(uint32_t hmax) {
