@@ -48,7 +48,7 @@ constexpr int kBwStage = 32 * 128;
 // + 1024 bytes of alignment slack and 256 of barriers
 constexpr int kBwSmem = kBwStages * 2 * kBwTile + kBwEpiWarps * kBwStage + 1024 + 256;
 // with the static arrays (s_off, s_tstart, s_tmem, s_abort) within the 227 KiB of a block
-static_assert(kBwSmem + 8 * (kBwMaxGroups + 1) + 16 <= 232448, "shared memory budget");
+static_assert(kBwSmem + 8 * (kBwMaxGroups + 1) + kBwMaxGroups + 16 <= 232448, "shared memory budget");
 
 // UMMA descriptor of an MN-major 128 x 64 tile stored as two 64 x 64
 // 128-byte-swizzled TMA boxes (see the file comment).
@@ -76,8 +76,12 @@ __device__ __forceinline__ int find_last_le(const int* starts, int n, int t) {
 }
 
 template <int SCHED>
+// Tile t: rows schedule in group order; K-grouped in the order s_pord gives
+// the problems (descending K), s_tstart holding the first tile of each in
+// that order.
 __device__ __forceinline__ BwTile bw_decode(int t, const BwParams& P, const int* s_off,
-                                            const int* s_tstart, int n_tiles_n, int rank) {
+                                            const int* s_tstart, const uint8_t* s_pord,
+                                            int n_tiles_n, int rank) {
   BwTile ti;
   if constexpr (SCHED == kSchedRows) {
     const int g = find_last_le(s_tstart, P.G, t);
@@ -92,10 +96,11 @@ __device__ __forceinline__ BwTile bw_decode(int t, const BwParams& P, const int*
     ti.kb0 = 0;
     ti.nkb = P.K / 64;
   } else {
-    const int p = find_last_le(s_tstart, P.G, t);
+    const int i = find_last_le(s_tstart, P.G, t);
+    const int p = s_pord[i];
     const BwProblem& pr = P.prob[p];
     const int ntn = (pr.N + 255) / 256;
-    const int local = t - s_tstart[p];
+    const int local = t - s_tstart[i];
     const int mb = local / ntn, nb = local - mb * ntn;
     ti.p = p;
     ti.g = pr.grp;
@@ -108,6 +113,20 @@ __device__ __forceinline__ BwTile bw_decode(int t, const BwParams& P, const int*
     ti.nkb = (k1 - k0 + 63) / 64;
   }
   return ti;
+}
+
+// The j-th tile of CTA pair c of nc.  Rows schedule: a plain stride (its
+// tiles cost the same).  K-grouped: a tile costs its problem's K, which
+// follows the experts' loads (a skewed top-2 call has one expert with ~8x
+// the rows of another), so the tiles, problems in descending K, go out in
+// rounds of nc, alternately forwards and backwards: the pairs that took a
+// round's longest tiles take the next round's shortest.  (Modelled on the
+// top-2 skewed call's counts, the busiest pair's k-blocks drop from 785 to
+// 710, against a mean of 611.)
+template <int SCHED>
+__device__ __forceinline__ int bw_tile_index(int j, int c, int nc) {
+  if constexpr (SCHED == kSchedKGrp) return j * nc + ((j & 1) ? nc - 1 - c : c);
+  return j * nc + c;
 }
 
 template <int SCHED>
@@ -127,6 +146,7 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_off[kBwMaxGroups + 1], s_tstart[kBwMaxGroups + 1];
+  __shared__ uint8_t s_pord[kBwMaxGroups];        // K-grouped: problems by descending K
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -173,6 +193,33 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
+  if constexpr (SCHED == kSchedKGrp) {
+    // problems in descending K (ties in index order), each thread placing
+    // one problem by counting those before it; then their first tiles
+    const int q = threadIdx.x;
+    if (q < P.G) {
+      const int gq = P.prob[q].grp;
+      const int kq = (s_off[gq + 1] - s_off[gq] + 63) / 64;
+      int pos = 0;
+      for (int o = 0; o < P.G; ++o) {
+        const int go = P.prob[o].grp;
+        const int ko = (s_off[go + 1] - s_off[go] + 63) / 64;
+        pos += (ko > kq || (ko == kq && o < q)) ? 1 : 0;
+      }
+      s_pord[pos] = static_cast<uint8_t>(q);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int run = 0;
+      for (int i = 0; i < P.G; ++i) {
+        const BwProblem& pr = P.prob[s_pord[i]];
+        s_tstart[i] = run;
+        run += ((pr.M + 255) / 256) * ((pr.N + 255) / 256);
+      }
+      s_tstart[P.G] = run;
+    }
+    __syncthreads();
+  }
   const uint32_t tmem = s_tmem;
   const int total = s_tstart[P.G];
   volatile int* abort = &s_abort;
@@ -182,8 +229,11 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int tile = cluster; ok && tile < total; tile += n_clusters) {
-        const BwTile ti = bw_decode<SCHED>(tile, P, s_off, s_tstart, n_tiles_n, static_cast<int>(rank));
+      for (int j = 0; ok && j * n_clusters < total; ++j) {
+        const int tile = bw_tile_index<SCHED>(j, cluster, n_clusters);
+        if (tile >= total) continue;               // the last round's missing tiles
+        const BwTile ti = bw_decode<SCHED>(tile, P, s_off, s_tstart, s_pord, n_tiles_n,
+                                           static_cast<int>(rank));
         for (int kb = 0; kb < ti.nkb; ++kb, ++it) {
           const int s = it % kBwStages;
           const uint32_t ph = (it / kBwStages) & 1;
@@ -227,8 +277,10 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
       constexpr uint32_t idesc = idesc_bf16_f32(256, 256) | (kAMn << 15) | (1u << 16);
       int it = 0, used = 0;
       bool ok = true;
-      for (int tile = cluster; ok && tile < total; tile += n_clusters) {
-        const BwTile ti = bw_decode<SCHED>(tile, P, s_off, s_tstart, n_tiles_n, 0);
+      for (int j = 0; ok && j * n_clusters < total; ++j) {
+        const int tile = bw_tile_index<SCHED>(j, cluster, n_clusters);
+        if (tile >= total) continue;
+        const BwTile ti = bw_decode<SCHED>(tile, P, s_off, s_tstart, s_pord, n_tiles_n, 0);
         if (ti.nkb == 0) continue;                 // the epilogue writes zeros for it
         const int acc = used & 1;
         const uint32_t aph = (used >> 1) & 1;
@@ -266,8 +318,11 @@ bw_gemm_kernel(const __grid_constant__ BwParams P, WsHeader* hdr) {
     const uint32_t te1 = mapa_shared(smem_u32(&tempty[1]), 0);
     int used = 0;
     uint32_t hmax = 0u;     // fp16 output: max |value| of the lane's rows, as packed halves
-    for (int tile = cluster; tile < total; tile += n_clusters) {
-      const BwTile ti = bw_decode<SCHED>(tile, P, s_off, s_tstart, n_tiles_n, static_cast<int>(rank));
+    for (int j = 0; j * n_clusters < total; ++j) {
+      const int tile = bw_tile_index<SCHED>(j, cluster, n_clusters);
+      if (tile >= total) continue;
+      const BwTile ti = bw_decode<SCHED>(tile, P, s_off, s_tstart, s_pord, n_tiles_n,
+                                         static_cast<int>(rank));
       // output row / columns / leading dimension of this tile
       float* out32 = nullptr;
       uint16_t* out16 = nullptr;                 // bf16 or fp16 (P.out_type)
