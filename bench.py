@@ -62,6 +62,9 @@ def decode_kernel_name(w):
 GATEUP_TRAFFIC_BYTES = {"moe_e8k2_t16384_skew": 162316544 + 128596480,
                         "moe_e4k1_t8192": 42551808 + 5244160,
                         "dense_t4096": 13830656 + 0}
+# The same for the backward's weight-gradient GEMM (K-grouped; one launch per
+# backward step), captured on the E = 4, k = 1 workload.
+WGRAD_TRAFFIC_BYTES = {"moe_e4k1_t8192": 146360320 + 49101312}
 # The same for the decode kernel that streams the weights (one launch per step).
 DECODE_TRAFFIC_BYTES = {"decode_moe_e8k2_t64": 89892096 + 2775296,
                         "decode_moe_e8k2_t16": 89829888 + 2516736,
@@ -707,7 +710,8 @@ def backward_entry(w, lib, ws, local, dev, warmup):
            "timing": m["timing"],
            "roofline": {"kernel": "bw_gemm_kernel<K-grouped> (weight gradients)", "bound": "tensor",
                         "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                        "frac": achieved / peaks["bf16_tflops"], "kernel_ms": m["kernel_ms"]},
+                        "frac": achieved / peaks["bf16_tflops"], "kernel_ms": m["kernel_ms"],
+                        "traffic": WGRAD_TRAFFIC_BYTES.get(w.name)},
            "clocks": m["clocks"], "l2": workload_config(w, ws)["l2"],
            "flops_note": "12*H*I per assignment (2x the forward's GEMMs)"}
     del step
