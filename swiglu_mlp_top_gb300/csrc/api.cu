@@ -78,9 +78,9 @@ RouteLayout route_layout(int64_t T, int E, int k) {
   return L;
 }
 
-// Backward of the dense FFN (bf16): dh = dy Wd [T, I] (fp32: only the
-// SwiGLU-backward epilogue reads it), dG | dU [T, 2I] and h [T, I] (bf16:
-// operands of the tensor-core GEMMs).
+// Backward of the dense FFN (bf16): dh = dy Wd [T, I] (fp16: only the
+// SwiGLU-backward epilogue reads it, no MMA), dG | dU [T, 2I] and h [T, I]
+// (bf16: operands of the tensor-core GEMMs).
 struct DenseBwdLayout {
   size_t dh, dgu, h, total;
 };

@@ -28,10 +28,12 @@
 //   kSchedRows  tiles over (group, 256-row block of the group's rows, N
 //               block): the dgrad GEMMs, A [rows, K] K-major, one weight
 //               matrix per group (two for dx: Wg for the first half of K,
-//               Wu for the second); output rows = A rows.
+//               Wu for the second); output rows = A rows, in fp32, bf16 or
+//               fp16 (dh and the per-assignment dx rows; range-checked).
 //   kSchedKGrp  tiles over (problem, M block, N block); a problem is one
 //               weight gradient, whose K runs over the rows of its group
-//               [koff[g], koff[g+1]) (64-row aligned, padding rows zero).
+//               [koff[g], koff[g+1]) (64-row aligned, padding rows zero);
+//               problems in descending K, tiles dealt in snake rounds.
 #include <cstring>
 
 #include "mm_kernels.cuh"
