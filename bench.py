@@ -860,6 +860,45 @@ def run_our_arm(args, w):
         print(json.dumps(line), flush=True)
 
 
+def run_stream_floor(args):
+    """The floor under a one-launch step that streams a given number of bytes:
+    back-to-back passes of one kernel that reads a buffer once (torch's bf16 sum
+    with an fp32 accumulator: every byte read once, nothing else done), at the
+    sizes of the decode rows' weights (dense: 3 H I bf16; MoE: all 8 experts)
+    and at 1 GiB.  Prints one JSON line."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, src = measured_peaks()
+    H, I = 768, 2432
+    sizes = [("dense FFN weights, 3*H*I bf16", 3 * H * I * 2),
+             ("MoE weights of all 8 experts", 8 * 3 * H * I * 2),
+             ("1 GiB", 1 << 30)]
+    out = []
+    for name, nbytes in sizes:
+        buf = torch.empty(nbytes // 2, dtype=torch.bfloat16, device=dev).normal_()
+        n = 200 if nbytes < (1 << 28) else 20
+        for _ in range(10):
+            buf.sum(dtype=torch.float32)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n):
+                buf.sum(dtype=torch.float32)
+            e1.record()
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) / n * 1e3
+            best = us if best is None else min(best, us)
+        gbs = nbytes / (best * 1e-6) / 1e9
+        out.append({"what": name, "bytes": nbytes, "us_per_pass": best, "GB/s": gbs,
+                    "frac_of_measured_hbm": gbs / peaks["hbm_gbs"]})
+        del buf
+    print(json.dumps({"stream_floor": out, "kernel": "torch bf16 sum (fp32 accumulate), one launch "
+                      "per pass, back to back; best of 5 regions", "peak_hbm_gbs": peaks["hbm_gbs"],
+                      "peak_source": src}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -878,11 +917,16 @@ def main():
     ap.add_argument("--profile", default="",
                     help="run W + K untimed steps of one entry (a workload or a per-workload "
                          "name such as backward:moe_e8k2_t16384_skew) for a profiler, and exit")
+    ap.add_argument("--stream-floor", action="store_true",
+                    help="measure the one-launch streaming floor at the decode rows' weight sizes")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.profile:
         run_profile(args)
+        return
+    if args.stream_floor:
+        run_stream_floor(args)
         return
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
