@@ -59,9 +59,9 @@ def decode_kernel_name(w):
 # fourth launch; ncu flushes the caches before it).  h writes still held in L2
 # when the kernel ends are not counted, so at T <= 8192 the figure is mostly the
 # reads of x and the weights.
-GATEUP_TRAFFIC_BYTES = {"moe_e8k2_t16384_skew": 162316544 + 128596480,
-                        "moe_e4k1_t8192": 42551808 + 5244160,
-                        "dense_t4096": 13830656 + 0}
+GATEUP_TRAFFIC_BYTES = {"moe_e8k2_t16384_skew": 162595072 + 129717248,
+                        "moe_e4k1_t8192": 42550528 + 5054976,
+                        "dense_t4096": 13830400 + 0}
 # The same for the backward's weight-gradient GEMM (K-grouped; one launch per
 # backward step), captured on the E = 4, k = 1 workload.
 WGRAD_TRAFFIC_BYTES = {"moe_e4k1_t8192": 146360320 + 49101312}
