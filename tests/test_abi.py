@@ -93,3 +93,51 @@ def test_bad_arguments_rejected_before_any_launch(lib):
     rc = lib.mm_watchdog_selftest(fake, 256, 0, None)
     assert rc == L.MM_ERR_INVALID_ARG
     del keep
+
+
+def test_backward_workspace_layout(lib):
+    """The backward workspaces hold dh and the per-assignment dx rows in fp16
+    (2 bytes each) beside the bf16 operands: dense T*I*(2 dh + 4 dG|dU + 2 h)
+    bytes plus the 256-byte header; MoE R*(6H + 8I) bytes for the padded rows
+    R = T*k + 63*E (x, dy, dx rows: 2H each; dh, alpha*h: 2I; dG|dU: 4I) plus
+    small per-block partials."""
+    bf16 = L.MM_DTYPE_BF16
+    T, H, I = 4096, 768, 2432
+    assert lib.mm_swiglu_ffn_backward_workspace_bytes(T, H, I, bf16) == 256 + T * I * 8
+    T, E, k = 16384, 8, 2
+    R = T * k + 63 * E
+    ws = lib.mm_moe_backward_workspace_bytes(T, H, I, E, k, bf16)
+    core = R * (6 * H + 8 * I)
+    assert core <= ws <= core + 16 * 2 ** 20
+    assert lib.mm_moe_backward_workspace_bytes(T, H, I, E, k, L.MM_DTYPE_F32) == 0
+    assert lib.mm_moe_backward_workspace_bytes(T, H, I, E, 9, bf16) == 0          # k > E
+
+
+def test_backward_bad_arguments_rejected_before_any_launch(lib):
+    fake = C.c_void_p(1 << 20)      # never dereferenced: validation fails first
+    bf16, f32 = L.MM_DTYPE_BF16, L.MM_DTYPE_F32
+    wsb = 1 << 34
+    rc = lib.mm_swiglu_ffn_backward(fake, fake, fake, fake, fake, 10, 768, 2432, f32, fake, fake,
+                                    fake, fake, fake, wsb, None)
+    assert rc == L.MM_ERR_UNSUPPORTED                       # bf16 only
+    rc = lib.mm_swiglu_ffn_backward(fake, fake, fake, fake, fake, 10, 100, 2432, bf16, fake, fake,
+                                    fake, fake, fake, wsb, None)
+    assert rc == L.MM_ERR_UNSUPPORTED                       # H not a multiple of 64
+    rc = lib.mm_swiglu_ffn_backward(fake, fake, fake, fake, fake, 10, 768, 2432, bf16, None, fake,
+                                    fake, fake, fake, wsb, None)
+    assert rc == L.MM_ERR_INVALID_ARG                       # null dx
+    rc = lib.mm_swiglu_ffn_backward(fake, fake, fake, fake, fake, 10, 768, 2432, bf16, fake, fake,
+                                    fake, fake, fake, 100, None)
+    assert rc == L.MM_ERR_WORKSPACE                         # workspace too small
+    ptrs, keep = L.ptr_array([1 << 20] * 4)
+    common = (fake, fake, ptrs, ptrs, ptrs)
+    rc = lib.mm_moe_backward(*common, 10, 768, 2432, 4, 5, 0.01, bf16, fake, fake, fake, fake,
+                             fake, 1.0, 0.0, 0.0, fake, fake, ptrs, ptrs, ptrs, None, fake, wsb, None)
+    assert rc == L.MM_ERR_INVALID_ARG                       # k > E
+    rc = lib.mm_moe_backward(*common, 10, 768, 2432, 4, 2, 0.01, bf16, fake, fake, fake, None,
+                             fake, 1.0, 1e-3, 1.0, fake, fake, ptrs, ptrs, ptrs, None, fake, wsb, None)
+    assert rc == L.MM_ERR_INVALID_ARG                       # z-loss asked for without lse
+    rc = lib.mm_moe_backward(*common, 10, 768, 2432, 4, 2, 0.01, bf16, fake, fake, fake, fake,
+                             fake, 1.0, 0.0, 0.0, fake, fake, ptrs, ptrs, ptrs, None, fake, 100, None)
+    assert rc == L.MM_ERR_WORKSPACE                         # workspace too small
+    del keep
