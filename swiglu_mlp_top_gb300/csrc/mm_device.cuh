@@ -484,12 +484,6 @@ __device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_
                "r"(smem_u32(ssrc)), "r"(bytes)
                : "memory");
 }
-// Element-wise fp32 add of `bytes` of shared memory into global memory.
-__device__ __forceinline__ void bulk_reduce_add_f32(void* gdst, const void* ssrc, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
-               "r"(smem_u32(ssrc)), "r"(bytes)
-               : "memory");
-}
 // 2-D tiled TMA store of a box from shared memory (bulk-group completion).
 __device__ __forceinline__ void tma_store_2d(const void* tmap, const void* smem_src, int32_t c0,
                                              int32_t c1) {
@@ -545,14 +539,6 @@ __device__ __forceinline__ void report_range(WsHeader* hdr, bool bad, unsigned w
   if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0 && hdr != nullptr) {
     if (atomicCAS(&hdr->status, 0u, kStatusRange) == 0u) hdr->where = where;
   }
-}
-
-// y[0..7] += v (8 bf16 as four bf16x2), one 16-byte vector reduction.
-__device__ __forceinline__ void red_add_bf16x8(void* gptr, uint32_t a, uint32_t b, uint32_t c,
-                                               uint32_t d) {
-  asm volatile("red.global.add.noftz.v4.bf16x2 [%0], {%1, %2, %3, %4};" ::"l"(gptr), "r"(a),
-               "r"(b), "r"(c), "r"(d)
-               : "memory");
 }
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
