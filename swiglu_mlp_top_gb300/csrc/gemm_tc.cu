@@ -500,6 +500,56 @@ __device__ __forceinline__ void epilogue_down(uint32_t tb, const DownRow& d, con
   }
 }
 
+// down, y stored straight from the accumulator (mode Store, no residual:
+// top-1 MoE, or a dense warp holding a ragged end): y = round(alpha v), so
+// each 32-column piece is scaled and packed to bf16 before the transpose
+// (64-byte rows in the staging tile, chunk q of row r at q ^ ((r >> 1) & 3))
+// and lane l writes 8 columns (16 bytes) of row 8i + l/4: every warp store
+// covers 8 rows x 64 contiguous bytes, with half the store instructions of
+// the fp32 transpose above.  Same arithmetic, same bits.
+template <int HC>
+__device__ __forceinline__ void epilogue_down_store16(uint32_t tb, const DownRow& d,
+                                                      const DownLanes& L, const TileInfo& ti,
+                                                      int H, const DownEpilogue& ep, int half,
+                                                      int lane, uint8_t* wstage) {
+  const int col0 = ti.n0 + half * HC;
+  const uint32_t st0 = smem_u32(wstage);
+  if (lane == 0) bulk_wait_read();               // a dense tile's tensor stores used the tile
+  __syncwarp();
+  __nv_bfloat16* y = static_cast<__nv_bfloat16*>(ep.y);
+#pragma unroll 1
+  for (int c = 0; c < HC / 32; ++c) {
+    if (col0 + c * 32 >= H) break;               // warp-uniform: past the last column
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(tb + half * HC + c * 32, r);
+    tmem_ld_wait();
+    uint32_t pk[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      pk[j] = pack_bf16x2(d.alpha * __uint_as_float(r[2 * j]), d.alpha * __uint_as_float(r[2 * j + 1]));
+    __syncwarp();                                // the previous piece has been read back
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t a = st0 + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[4 * q]),
+                   "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
+                   : "memory");
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = 8 * i + (lane >> 2);
+      const uint32_t a = st0 + row * 64 + (((lane & 3) ^ ((row >> 1) & 3)) << 4);
+      uint4 v;
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+      if (!((L.valid >> i) & 1u)) continue;
+      // L.off: the row's first column plus 4 (lane & 3); here 8 (lane & 3)
+      *reinterpret_cast<uint4*>(y + L.off[i] + 4 * (lane & 3) + c * 32) = v;
+    }
+  }
+}
+
 // --------------------------------------------------------- fp16 copy of Wd
 // The copy works in batches of four 16-byte vectors per epilogue thread
 // (16 KiB per CTA): vectors v + t + j * 256 of one index space over the
@@ -851,6 +901,8 @@ grouped_gemm_kernel(const __grid_constant__ TcParams<MAXW> P, const GroupRows g,
       else if (ep.perm == nullptr && ep.mode == kCombineStore && (row | 31) < ti.rows)
         epilogue_down_dense<kHC>(tb, ti, NCOLS, half, lane, ti.row0 + (row & ~31), wstage, &P.out,
                                  static_cast<const __nv_bfloat16*>(ep.resid));
+      else if (ep.mode == kCombineStore && ep.resid == nullptr && (NCOLS & 31) == 0)
+        epilogue_down_store16<kHC>(tb, dr, dl, ti, NCOLS, ep, half, lane, wstage);
       else
         epilogue_down<kHC>(tb, dr, dl, ti, NCOLS, ep, half, lane, wstage, pre, pre2);
       tc_fence_before();
